@@ -1,0 +1,134 @@
+// Device helpers shared by the library's kernels: element conversion,
+// block reductions, and the Newton-Schulz epilogue arithmetic.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace gbo {
+
+__device__ __forceinline__ float ld_elem(const void *base, int32_t dtype, int64_t idx) {
+  if (dtype == GBO_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[idx]);
+  return reinterpret_cast<const float *>(base)[idx];
+}
+
+__device__ __forceinline__ void st_elem(void *base, int32_t dtype, int64_t idx, float v) {
+  if (dtype == GBO_BF16)
+    reinterpret_cast<__nv_bfloat16 *>(base)[idx] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float *>(base)[idx] = v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum / max for blockDim.x a multiple of 32 (<= 1024).  `red`
+// is shared scratch of >= 32 floats.  Every thread gets the result.  The
+// combination order is fixed, so results are reproducible.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = lane < nw ? red[lane] : 0.f;
+  t = warp_sum(t);
+  return t;
+}
+
+__device__ __forceinline__ float block_max(float v, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = lane < nw ? red[lane] : 0.f;
+  t = warp_max(t);
+  return t;
+}
+
+__device__ __forceinline__ void flag_status(int32_t *status, int32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Index of the matrix owning global item `t`, given each matrix's first
+// item in `first` (non-decreasing).  Binary search; `n` >= 1.
+template <typename GetFirst>
+__device__ __forceinline__ int find_owner(int64_t t, int n, GetFirst first) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (first(mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// Newton-Schulz epilogue for one accumulator element C[i][j] of matrix S.
+// `s` is the pre-normalisation factor of the iteration's input (alpha for
+// iteration 0, 1 afterwards), so the true iterate is s * X.
+struct EpiScalars {
+  float s;
+  float s2;
+};
+
+__device__ __forceinline__ EpiScalars epi_scalars(const PhaseArgs &A, int sub) {
+  EpiScalars e;
+  e.s = A.first ? A.alpha[sub] : 1.0f;
+  e.s2 = e.s * e.s;
+  return e;
+}
+
+// Weight write of the last iteration (no NorMuon): O = s * C is the
+// orthogonalised update at position (i, j) of the oriented matrix.
+__device__ __forceinline__ void final_write(const PhaseArgs &A, const DevSub &S, int i, int j,
+                                            float o) {
+  const int wi = S.transposed ? j : i;
+  const int wj = S.transposed ? i : j;
+  const int64_t widx = (S.r0 + wi) * S.cols + wj;
+  const float u = S.scale * o;
+  const float w = ld_elem(S.w, S.w_dtype, widx);
+  const float lr = A.lr * S.lr_mult;
+  st_elem(S.w, S.w_dtype, widx, w - lr * (S.wd * w + u));
+  if (A.dbg) A.dbg[S.dbg_off + widx] = u;
+}
+
+__device__ __forceinline__ void ns_epilogue(const PhaseArgs &A, const DevSub &S, const EpiScalars &e,
+                                            int i, int j, float acc) {
+  switch (A.mode) {
+    case kGram: {
+      float v = A.b * e.s2 * acc + (i == j ? A.a : 0.f);
+      st_elem(A.pbuf, A.x_dtype, S.p_off + (int64_t)i * S.ldp + j, v);
+      break;
+    }
+    case kGramA:
+      st_elem(A.abuf, A.x_dtype, S.p_off + (int64_t)i * S.ldp + j, e.s2 * acc);
+      break;
+    case kSquare: {
+      const float av = ld_elem(A.abuf, A.x_dtype, S.p_off + (int64_t)i * S.ldp + j);
+      float v = A.c * acc + A.b * av + (i == j ? A.a : 0.f);
+      st_elem(A.pbuf, A.x_dtype, S.p_off + (int64_t)i * S.ldp + j, v);
+      break;
+    }
+    case kProduct:
+      st_elem(A.x_out, A.x_dtype, S.x_off + (int64_t)i * S.ld + j, e.s * acc);
+      break;
+    default:
+      final_write(A, S, i, j, e.s * acc);
+      break;
+  }
+}
+
+}  // namespace gbo

@@ -1,0 +1,110 @@
+// Internal declarations shared by the host plan code and the CUDA kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "gbo.h"
+
+namespace gbo {
+
+constexpr int kMomTile = 64;        // momentum tiles: 64 x 64 elements of a matrix
+constexpr int kRowBlock = 32;       // NorMuon: stored rows per block
+constexpr int kMaxClassesPerLaunch = 8;
+
+// One independent matrix (a view block or split range of a stored weight),
+// as the kernels see it.  Orientation: the stored matrix is m x n; the
+// Newton-Schulz side is p x q with p = min(m, n); `transposed` is set when
+// m > n, in which case X holds D^T.
+struct DevSub {
+  void *w;
+  const void *g;
+  float *mom;
+  float *row_v;
+  int64_t r0;       // first stored row of this matrix in its weight
+  int64_t cols;     // row stride of the weight (== n)
+  int64_t x_off;    // element offset of this matrix in each X buffer
+  int64_t p_off;    // element offset of this matrix in the P (and A) buffer
+  int64_t dbg_off;  // element offset of the weight's first element in dbg_update
+  int64_t tile0;    // first momentum tile of this matrix (global tile index)
+  int64_t rb0;      // first NorMuon row block of this matrix
+  int32_t m, n;     // stored rows, cols
+  int32_t p, q;     // oriented rows, cols
+  int32_t ld;       // X row stride (elements)
+  int32_t ldp;      // P row stride (elements)
+  int32_t tiles_c;  // momentum tiles along n
+  int32_t transposed;
+  int32_t w_dtype, g_dtype;
+  int32_t vec_ok;   // rows start on 16-byte boundaries and n % 4 == 0
+  int32_t cls;
+  float scale;      // sqrt(max(1, m / n))
+  float lr_mult;
+  float wd;
+  int32_t pad;
+};
+
+// Matrices of one oriented shape (p, q), stored back to back in the
+// workspace so one 3-D TMA map covers all of them.
+struct ShapeClass {
+  int32_t p, q, ld, ldp;
+  int32_t count;  // matrices in the class
+  int32_t sub0;   // index of the first matrix in the DevSub table
+  int64_t x_base; // element offset of the class in each X buffer
+  int64_t p_base; // element offset of the class in the P / A buffers
+};
+
+// Epilogue selector of the Newton-Schulz GEMMs.
+enum GemmMode : int32_t {
+  kGram = 0,      // C = X X^T;  write P = a I + b s^2 C          (c == 0)
+  kGramA = 1,     // C = X X^T;  write A = s^2 C                   (c != 0)
+  kSquare = 2,    // C = A A;    write P = a I + b A + c C
+  kProduct = 3,   // C = P X;    write X' = s C
+  kFinal = 4,     // C = P X;    O = s C; update the weight (+ dbg)
+};
+
+// Per-launch scalars of one Newton-Schulz phase.
+struct PhaseArgs {
+  int32_t mode;
+  int32_t first;      // iteration 0: fold the pre-normalisation factor in
+  float a, b, c;
+  float lr;
+  int32_t x_dtype;    // GBO_BF16 | GBO_F32 (workspace element type)
+  const DevSub *subs;
+  const float *alpha; // per matrix pre-normalisation factor
+  void *x_in;         // X buffer read by this phase
+  void *x_out;        // X buffer written (kProduct)
+  void *pbuf;         // P buffer (read by products, written by kGram/kSquare)
+  void *abuf;         // A buffer (kGramA writes, kSquare reads)
+  float *dbg;         // dbg_update or nullptr
+  int32_t *status;
+};
+
+// Launchers (implemented in the .cu files).  Each returns a cudaError_t as
+// int and adds its launches to the library's counter.
+int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float mu, int32_t nesterov,
+                    void *x0, int32_t x_dtype, float *partials, int sm_count, void *stream);
+int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials,
+                            float *alpha, int32_t *status, void *stream);
+int launch_ns_gemm_simt(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args,
+                        int sm_count, void *stream);
+int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x,
+                        int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
+                        int32_t *status, int sm_count, void *stream);
+int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
+                                 int32_t w_dtype, float beta2, float eps, float scale, float lr,
+                                 float wd, float *dbg, void *stream);
+int launch_clip_norm(const gbo_tensor *grads, int32_t n, float max_norm, float *total, float *coef,
+                     int32_t *status, float *partials, int sm_count, void *stream);
+int launch_adamw(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *opts,
+                 const float *coef, int32_t *status, int sm_count, void *stream);
+
+// tcgen05 path: host-side state for the tensor maps of one launch.
+struct TcLaunch;
+int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args,
+                      int sm_count, void *stream);
+
+void count_launches(uint64_t n);
+
+constexpr int kClipBlocks = 1024;  // partial sums of the clip norm
+
+}  // namespace gbo

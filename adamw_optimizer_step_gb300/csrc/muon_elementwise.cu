@@ -1,0 +1,391 @@
+// Memory-bound kernels of the Muon path:
+//   - momentum + Nesterov direction + per-tile max|D| / sum-of-squares, with
+//     the direction written (transposed for tall matrices) into the
+//     Newton-Schulz workspace;
+//   - the per-matrix reduction of those partials into the pre-normalisation
+//     factor;
+//   - NorMuon row statistics, row normalisation and the weight write.
+//
+// Momentum and direction: NorMuon paper (zskr.cn) section 2.2 eq. (1); OMN
+// page, Muon path (buffer at 0.95, Nesterov adds the scaled buffer back).
+// Pre-normalisation: OMN page, Muon path (max-abs rescale clamped at 1e-7,
+// then the Frobenius norm with an additive 1e-7).  NorMuon rows: NorMuon
+// paper section 3.1.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace gbo {
+
+namespace {
+
+constexpr int kMomThreads = 256;
+
+struct Load4 {
+  float v[4];
+};
+
+__device__ __forceinline__ Load4 load4(const void *base, int32_t dtype, int64_t idx, int valid,
+                                       bool vec) {
+  Load4 r;
+  if (vec && valid == 4) {
+    if (dtype == GBO_BF16) {
+      const uint2 raw = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + idx);
+      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+      r.v[0] = __low2float(lo);
+      r.v[1] = __high2float(lo);
+      r.v[2] = __low2float(hi);
+      r.v[3] = __high2float(hi);
+    } else {
+      const float4 f = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(base) + idx);
+      r.v[0] = f.x; r.v[1] = f.y; r.v[2] = f.z; r.v[3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) r.v[e] = e < valid ? ld_elem(base, dtype, idx + e) : 0.f;
+  }
+  return r;
+}
+
+// One 64 x 64 tile of one matrix per loop trip.  256 threads: thread t
+// covers columns 4*(t%16) .. +3 of rows t/16, t/16+16, t/16+32, t/16+48.
+template <typename XT>
+__global__ void __launch_bounds__(kMomThreads)
+momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles, float mu,
+                int32_t nesterov, XT *__restrict__ x0, float *__restrict__ partials) {
+  __shared__ float tile[kMomTile][kMomTile + 1];
+  __shared__ float red[32];
+  const int cg = threadIdx.x & 15;
+  const int rs = threadIdx.x >> 4;
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int si = find_owner(t, n_subs, [&](int k) { return subs[k].tile0; });
+    const DevSub &S = subs[si];
+    const int64_t lt = t - S.tile0;
+    const int tr = (int)(lt / S.tiles_c), tc = (int)(lt % S.tiles_c);
+    const int rb = tr * kMomTile, cb = tc * kMomTile;
+    const int j = cb + cg * 4;
+    const int valid = min(4, S.n - j);
+    const bool vec = S.vec_ok != 0;
+    float d[16];
+    float lmax = 0.f;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int i = rb + it * 16 + rs;
+      if (i < S.m && valid > 0) {
+        const int64_t widx = (S.r0 + i) * S.cols + j;
+        const Load4 g = load4(S.g, S.g_dtype, widx, valid, vec);
+        const Load4 b = load4(S.mom, GBO_F32, widx, valid, vec);
+        float nb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          nb[e] = mu * b.v[e] + g.v[e];
+          const float dd = nesterov ? g.v[e] + mu * nb[e] : nb[e];
+          d[it * 4 + e] = e < valid ? dd : 0.f;
+          lmax = fmaxf(lmax, fabsf(d[it * 4 + e]));
+        }
+        if (vec && valid == 4) {
+          *reinterpret_cast<float4 *>(S.mom + widx) = make_float4(nb[0], nb[1], nb[2], nb[3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (e < valid) S.mom[widx + e] = nb[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[it * 4 + e] = 0.f;
+      }
+    }
+    // Partials: the tile's max |D| and its sum of squares of D / max, so that
+    // the per-matrix combination cannot overflow.
+    const float M = block_max(lmax, red);
+    float ss = 0.f;
+    if (M > 0.f) {
+      const float inv = 1.0f / M;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float y = d[k] * inv;
+        ss = fmaf(y, y, ss);
+      }
+    }
+    ss = block_sum(ss, red);
+    if (threadIdx.x == 0) {
+      partials[2 * t] = M;
+      partials[2 * t + 1] = ss;
+    }
+    XT *X = x0 + S.x_off;
+    if (!S.transposed) {
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int i = rb + it * 16 + rs;
+        if (i < S.m) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (e < valid) {
+              if constexpr (sizeof(XT) == 2)
+                X[(int64_t)i * S.ld + j + e] = __float2bfloat16_rn(d[it * 4 + e]);
+              else
+                X[(int64_t)i * S.ld + j + e] = d[it * 4 + e];
+            }
+        }
+      }
+    } else {
+      // X = D^T: stage the tile, then write rows of X (columns of D).
+#pragma unroll
+      for (int it = 0; it < 4; ++it)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tile[it * 16 + rs][cg * 4 + e] = d[it * 4 + e];
+      __syncthreads();
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int xr = cb + it * 16 + rs;  // row of X = column of D
+        if (xr < S.n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int xc = rb + cg * 4 + e;  // column of X = row of D
+            if (xc < S.m) {
+              const float v = tile[cg * 4 + e][it * 16 + rs];
+              if constexpr (sizeof(XT) == 2)
+                X[(int64_t)xr * S.ld + xc] = __float2bfloat16_rn(v);
+              else
+                X[(int64_t)xr * S.ld + xc] = v;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// One block per matrix: combine the tile partials in a fixed order into
+// alpha = 1 / (s * (||D / s||_F + 1e-7)), s = max(max|D|, 1e-7), so that
+// X0 = alpha * D.
+__global__ void __launch_bounds__(256)
+prenorm_finalize_kernel(const DevSub *__restrict__ subs, const float *__restrict__ partials,
+                        float *__restrict__ alpha, int32_t *status) {
+  __shared__ float red[32];
+  const DevSub &S = subs[blockIdx.x];
+  const int64_t nt = (int64_t)((S.m + kMomTile - 1) / kMomTile) * S.tiles_c;
+  const float *P = partials + 2 * S.tile0;
+  float M = 0.f;
+  for (int64_t k = threadIdx.x; k < nt; k += blockDim.x) M = fmaxf(M, P[2 * k]);
+  M = block_max(M, red);
+  float ss = 0.f;
+  if (M > 0.f) {
+    const float inv = 1.0f / M;
+    for (int64_t k = threadIdx.x; k < nt; k += blockDim.x) {
+      const float r = P[2 * k] * inv;
+      ss = fmaf(P[2 * k + 1], r * r, ss);
+    }
+  }
+  ss = block_sum(ss, red);
+  if (threadIdx.x == 0) {
+    const float s = fmaxf(M, 1e-7f);
+    const float normY = (M / s) * sqrtf(ss);
+    float a = 1.0f / (s * (normY + 1e-7f));
+    if (!isfinite(M) || !isfinite(ss) || !isfinite(a)) {
+      flag_status(status, GBO_STATUS_NONFINITE);
+      a = __int_as_float(0x7fc00000);
+    }
+    alpha[blockIdx.x] = a;
+  }
+}
+
+// NorMuon rows of the plan's matrices: one block of 256 threads per
+// kRowBlock stored rows of one matrix.  O (the unscaled orthogonalised
+// update) is read from the workspace; for a transposed matrix stored row i
+// is column i of X.  Row statistics, v update, then the weight write.
+template <typename XT>
+__global__ void __launch_bounds__(256)
+normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_blocks,
+                    const XT *__restrict__ xbuf, float beta2, float eps, float lr,
+                    float *__restrict__ dbg, int32_t *status) {
+  __shared__ float tileT[32][33];
+  __shared__ float part[8][32];
+  __shared__ float rinv[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
+    const int si = find_owner(b, n_subs, [&](int k) { return subs[k].rb0; });
+    const DevSub &S = subs[si];
+    const int i0 = (int)(b - S.rb0) * kRowBlock;
+    const int nrows = min(kRowBlock, S.m - i0);
+    const XT *X = xbuf + S.x_off;
+    auto xval = [&](int i, int j) -> float {  // O[i][j] in stored orientation
+      const int64_t idx = S.transposed ? (int64_t)j * S.ld + i : (int64_t)i * S.ld + j;
+      if constexpr (sizeof(XT) == 2) return __bfloat162float(X[idx]);
+      else return X[idx];
+    };
+    // 1) sum of squares per row
+    if (!S.transposed) {
+      for (int r = warp; r < nrows; r += 8) {
+        float ss = 0.f;
+        for (int j = lane; j < S.n; j += 32) {
+          const float o = xval(i0 + r, j);
+          ss = fmaf(o, o, ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) part[0][r] = ss;
+      }
+      __syncthreads();
+    } else {
+      float ss = 0.f;
+      if (lane < nrows)
+        for (int j = warp; j < S.n; j += 8) {
+          const float o = xval(i0 + lane, j);
+          ss = fmaf(o, o, ss);
+        }
+      part[warp][lane] = ss;
+      __syncthreads();
+      if (warp == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) t += part[w][lane];
+        part[0][lane] = t;
+      }
+      __syncthreads();
+    }
+    // 2) second moment and the row factor
+    if (threadIdx.x < nrows) {
+      const int64_t row = S.r0 + i0 + threadIdx.x;
+      const float ms = part[0][threadIdx.x] / (float)S.n;
+      const float v = beta2 * S.row_v[row] + (1.0f - beta2) * ms;
+      S.row_v[row] = v;
+      const float f = S.scale / (sqrtf(v) + eps);
+      if (!isfinite(f)) flag_status(status, GBO_STATUS_NONFINITE);
+      rinv[threadIdx.x] = f;
+    }
+    __syncthreads();
+    // 3) weight write, coalesced along stored rows
+    const float lrm = lr * S.lr_mult;
+    if (!S.transposed) {
+      for (int r = warp; r < nrows; r += 8) {
+        const int64_t wrow = (S.r0 + i0 + r) * S.cols;
+        for (int j = lane; j < S.n; j += 32) {
+          const float u = rinv[r] * xval(i0 + r, j);
+          const float w = ld_elem(S.w, S.w_dtype, wrow + j);
+          st_elem(S.w, S.w_dtype, wrow + j, w - lrm * (S.wd * w + u));
+          if (dbg) dbg[S.dbg_off + wrow + j] = u;
+        }
+      }
+    } else {
+      for (int j0 = 0; j0 < S.n; j0 += 32) {
+        // tileT[c][r] = O[i0 + r][j0 + c] read along X rows (coalesced)
+        for (int c = warp; c < 32; c += 8) {
+          const int j = j0 + c;
+          tileT[c][lane] = (j < S.n && lane < nrows) ? xval(i0 + lane, j) : 0.f;
+        }
+        __syncthreads();
+        for (int r = warp; r < nrows; r += 8) {
+          const int j = j0 + lane;
+          if (j < S.n) {
+            const int64_t widx = (S.r0 + i0 + r) * S.cols + j;
+            const float u = rinv[r] * tileT[lane][r];
+            const float w = ld_elem(S.w, S.w_dtype, widx);
+            st_elem(S.w, S.w_dtype, widx, w - lrm * (S.wd * w + u));
+            if (dbg) dbg[S.dbg_off + widx] = u;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Stand-alone NorMuon rows on a plain fp32 O (rows x cols): one block per
+// kRowBlock rows.
+__global__ void __launch_bounds__(256)
+rownorm_plain_kernel(const float *__restrict__ O, int64_t rows, int64_t cols, float *__restrict__ row_v,
+                     void *w, int32_t w_dtype, float beta2, float eps, float scale, float lr,
+                     float wd, float *__restrict__ dbg) {
+  __shared__ float rinv[kRowBlock];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t b = blockIdx.x; b * kRowBlock < rows; b += gridDim.x) {
+    const int64_t i0 = b * kRowBlock;
+    const int nrows = (int)min((int64_t)kRowBlock, rows - i0);
+    for (int r = warp; r < nrows; r += 8) {
+      const float *o = O + (i0 + r) * cols;
+      float ss = 0.f;
+      for (int64_t j = lane; j < cols; j += 32) ss = fmaf(o[j], o[j], ss);
+      ss = warp_sum(ss);
+      if (lane == 0) {
+        const float v = beta2 * row_v[i0 + r] + (1.0f - beta2) * (ss / (float)cols);
+        row_v[i0 + r] = v;
+        rinv[r] = scale / (sqrtf(v) + eps);
+      }
+    }
+    __syncthreads();
+    for (int r = warp; r < nrows; r += 8) {
+      const int64_t base = (i0 + r) * cols;
+      for (int64_t j = lane; j < cols; j += 32) {
+        const float u = rinv[r] * O[base + j];
+        const float wv = ld_elem(w, w_dtype, base + j);
+        st_elem(w, w_dtype, base + j, wv - lr * (wd * wv + u));
+        if (dbg) dbg[base + j] = u;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float mu, int32_t nesterov,
+                    void *x0, int32_t x_dtype, float *partials, int sm_count, void *stream) {
+  if (n_tiles == 0) return 0;
+  const int64_t grid = std::min<int64_t>(n_tiles, (int64_t)sm_count * 8);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (x_dtype == GBO_BF16)
+    momentum_kernel<__nv_bfloat16><<<(unsigned)grid, kMomThreads, 0, st>>>(
+        subs, n_subs, n_tiles, mu, nesterov, reinterpret_cast<__nv_bfloat16 *>(x0), partials);
+  else
+    momentum_kernel<float><<<(unsigned)grid, kMomThreads, 0, st>>>(
+        subs, n_subs, n_tiles, mu, nesterov, reinterpret_cast<float *>(x0), partials);
+  count_launches(1);
+  return (int)cudaGetLastError();
+}
+
+int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials, float *alpha,
+                            int32_t *status, void *stream) {
+  if (n_subs == 0) return 0;
+  prenorm_finalize_kernel<<<n_subs, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(subs, partials,
+                                                                                      alpha, status);
+  count_launches(1);
+  return (int)cudaGetLastError();
+}
+
+int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x,
+                        int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
+                        int32_t *status, int sm_count, void *stream) {
+  if (n_row_blocks == 0) return 0;
+  const int64_t grid = std::min<int64_t>(n_row_blocks, (int64_t)sm_count * 8);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (x_dtype == GBO_BF16)
+    normuon_rows_kernel<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(
+        subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x), beta2, eps, lr, dbg,
+        status);
+  else
+    normuon_rows_kernel<float><<<(unsigned)grid, 256, 0, st>>>(
+        subs, n_subs, n_row_blocks, reinterpret_cast<const float *>(x), beta2, eps, lr, dbg, status);
+  count_launches(1);
+  return (int)cudaGetLastError();
+}
+
+int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
+                                 int32_t w_dtype, float beta2, float eps, float scale, float lr,
+                                 float wd, float *dbg, void *stream) {
+  if (rows == 0 || cols == 0) return 0;
+  const int64_t nb = (rows + kRowBlock - 1) / kRowBlock;
+  const unsigned grid = (unsigned)std::min<int64_t>(nb, 65535);
+  rownorm_plain_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      O, rows, cols, row_v, w, w_dtype, beta2, eps, scale, lr, wd, dbg);
+  count_launches(1);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace gbo

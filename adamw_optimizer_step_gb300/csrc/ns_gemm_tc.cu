@@ -1,0 +1,519 @@
+// Newton-Schulz GEMMs on the 5th-generation tensor cores (sm_103a):
+// TMA -> shared memory (128-byte swizzle) -> tcgen05.mma (bf16 operands, fp32
+// accumulators in TMEM) -> tcgen05.ld -> fused epilogue.
+//
+// One iteration of eq. (5) of the NorMuon paper (zskr.cn, section 2.2),
+//   X <- (a I + b A + c A^2) X,  A = X X^T,
+// is two (three when c != 0) launches of this kernel over every matrix of
+// the step: the Gram product, the optional square, and the product back
+// onto X whose last instance writes the weights.  Matrices of one oriented
+// shape are stored back to back, so one 3-D tensor map (columns, rows,
+// matrix) covers a whole shape class; out-of-range rows and columns of a
+// tile are zero-filled by TMA and masked in the epilogue.
+//
+// Persistent, warp-specialised CTA (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one lane), STAGES-deep ring of A/B tiles
+//   warp 1      TMEM owner and MMA issuer (one lane)
+//   warps 2..5  epilogue: TMEM -> registers -> global, 32 rows each
+// The accumulator is double-buffered in TMEM (2 x 256 columns) so the
+// epilogue of one tile overlaps the MMAs of the next.  Every wait is
+// bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT, waits (bounded)
+// for its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace gbo {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_BYTES = BN * BK * 2;             // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;                   // two 128 x 256 fp32 accumulators
+constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+
+struct TcParams {
+  CUtensorMap mapA[kMaxClassesPerLaunch];  // A operand, box 64 x 128
+  CUtensorMap mapB[kMaxClassesPerLaunch];  // B operand, box 64 x 256 (K-major) or 64 x 64 (MN-major)
+  int64_t tile_start[kMaxClassesPerLaunch + 1];
+  int32_t tiles_n[kMaxClassesPerLaunch];
+  int32_t k_iters[kMaxClassesPerLaunch];
+  int32_t sub0[kMaxClassesPerLaunch];
+  int32_t tiles_per_mat[kMaxClassesPerLaunch];
+  int32_t n;
+  int32_t b_mn_major;  // products: B = X with the K index along X's rows
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    if (mbar_try(bar, parity)) return true;
+    if ((spin & 255u) == 255u && global_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x,
+                                            int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05), 128-byte swizzle.
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4
+//   bits 32-45  stride-dimension byte offset >> 4
+//   bits 46-47  descriptor version (1)
+//   bits 61-63  layout: 2 = 128-byte swizzle
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
+// A K-major, B K-major or MN-major, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t make_idesc(int b_mn_major) {
+  return (1u << 4)                      // D format: f32
+         | (1u << 7)                    // A format: bf16
+         | (1u << 10)                   // B format: bf16
+         | ((uint32_t)b_mn_major << 16) // B major-ness
+         | ((uint32_t)(BN >> 3) << 17)  // N / 8
+         | ((uint32_t)(BM >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+}
+
+struct TileCoord {
+  int c, mat, tm, tn;
+};
+
+__device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
+  TileCoord tc;
+  int c = 0;
+  while (c + 1 < P.n && P.tile_start[c + 1] <= t) ++c;
+  const int64_t local = t - P.tile_start[c];
+  tc.c = c;
+  tc.mat = (int)(local / P.tiles_per_mat[c]);
+  const int rem = (int)(local % P.tiles_per_mat[c]);
+  tc.tm = rem / P.tiles_n[c];
+  tc.tn = rem % P.tiles_n[c];
+  return tc;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Epilogue of one 32-column chunk of one accumulator row.
+__device__ __forceinline__ void epilogue_chunk(const PhaseArgs &A, const DevSub &S, const EpiScalars &e,
+                                               int i, int col0, float (&v)[32]) {
+  if (A.mode == kFinal) {
+    if (i >= S.p) return;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (col0 + k < S.q) final_write(A, S, i, col0 + k, e.s * v[k]);
+    return;
+  }
+  const bool sq = (A.mode == kGram || A.mode == kGramA || A.mode == kSquare);
+  const int Ncols = sq ? S.p : S.q;
+  if (i >= S.p) return;
+  __nv_bfloat16 *out;
+  int64_t base;
+  if (A.mode == kProduct) {
+    out = reinterpret_cast<__nv_bfloat16 *>(A.x_out);
+    base = S.x_off + (int64_t)i * S.ld;
+  } else if (A.mode == kGramA) {
+    out = reinterpret_cast<__nv_bfloat16 *>(A.abuf);
+    base = S.p_off + (int64_t)i * S.ldp;
+  } else {
+    out = reinterpret_cast<__nv_bfloat16 *>(A.pbuf);
+    base = S.p_off + (int64_t)i * S.ldp;
+  }
+  float o[32];
+  if (A.mode == kSquare) {
+    const __nv_bfloat16 *am = reinterpret_cast<const __nv_bfloat16 *>(A.abuf) + S.p_off + (int64_t)i * S.ldp;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int j = col0 + k;
+      const float av = j < Ncols ? __bfloat162float(am[j]) : 0.f;
+      o[k] = A.c * v[k] + A.b * av + (i == j ? A.a : 0.f);
+    }
+  } else if (A.mode == kGram) {
+    const float bs2 = A.b * e.s2;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = bs2 * v[k] + (i == col0 + k ? A.a : 0.f);
+  } else if (A.mode == kGramA) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = e.s2 * v[k];
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = e.s * v[k];
+  }
+  if (col0 + 32 <= Ncols) {
+    uint4 *dst = reinterpret_cast<uint4 *>(out + base + col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16(o[8 * q + 0], o[8 * q + 1]);
+      w.y = pack_bf16(o[8 * q + 2], o[8 * q + 3]);
+      w.z = pack_bf16(o[8 * q + 4], o[8 * q + 5]);
+      w.w = pack_bf16(o[8 * q + 6], o[8 * q + 7]);
+      dst[q] = w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (col0 + k < Ncols) out[base + col0 + k] = __float2bfloat16_rn(o[k]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ PhaseArgs A) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], accf[2], acce[2], drain
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf0 + 8 * a, 1);
+      mbar_init(acce0 + 8 * a, 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int64_t total = P.tile_start[P.n];
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    flag_status(A.status, GBO_STATUS_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed_parity[STAGES];
+      bool armed[STAGES];
+      for (int s = 0; s < STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
+      for (int64_t t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const TileCoord tc = decode(P, t);
+        const int kit = P.k_iters[tc.c];
+        for (int kb = 0; kb < kit; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) { give_up(); break; }
+          if (*abort_flag) break;
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_expect_tx(fb, STAGE_BYTES);
+          armed[stage] = true;
+          armed_parity[stage] = phase;
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          tma_load_3d(sa, &P.mapA[tc.c], fb, kb * BK, tc.tm * BM, tc.mat);
+          if (!P.b_mn_major) {
+            tma_load_3d(sb, &P.mapB[tc.c], fb, kb * BK, tc.tn * BN, tc.mat);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(sb + j * 8192, &P.mapB[tc.c], fb, tc.tn * BN + j * 64, kb * BK, tc.mat);
+          }
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (*abort_flag) {
+        // let every copy this thread started land before shared memory goes away
+        for (int s = 0; s < STAGES; ++s)
+          if (armed[s]) (void)mbar_wait(full0 + 8 * s, armed_parity[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc(P.b_mn_major);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool issued = false;
+      for (int64_t t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const TileCoord tc = decode(P, t);
+        const int kit = P.k_iters[tc.c];
+        if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1)) { give_up(); break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        bool bad = false;
+        for (int kb = 0; kb < kit; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase)) { give_up(); bad = true; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
+            const uint64_t bd = P.b_mn_major ? smem_desc(sb + k * 2048, 8192, 1024)
+                                             : smem_desc(sb + k * 32, 16, 1024);
+            mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          }
+          issued = true;
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+        if (bad) break;
+        mma_commit(accf0 + 8 * acc);
+        if (++acc == 2) acc = 0, acc_phase ^= 1;
+      }
+      if (*abort_flag && issued) {
+        // wait for this thread's outstanding MMAs before TMEM is released
+        mma_commit(drain);
+        (void)mbar_wait(drain, 0);
+      }
+    }
+  } else {
+    // epilogue warps 2..5: TMEM lane quarter = warp % 4
+    const int quarter = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      const TileCoord tc = decode(P, t);
+      if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
+      tc_fence_after();
+      const int sub = P.sub0[tc.c] + tc.mat;
+      const DevSub &S = A.subs[sub];
+      const EpiScalars e = epi_scalars(A, sub);
+      const int i = tc.tm * BM + quarter * 32 + lane;
+      const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        float v[32];
+        tmem_ld32(trow + ch * 32, v);
+        epilogue_chunk(A, S, e, i, tc.tn * BN + ch * 32, v);
+      }
+      tc_fence_before();
+      mbar_arrive(acce0 + 8 * acc);
+      if (++acc == 2) acc = 0, acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host: tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 map over `count` row-major rows x cols matrices with row stride
+// `ld` elements, stored back to back; box = box_cols x box_rows x 1.
+bool encode_map(CUtensorMap *map, void *base, int64_t cols, int64_t rows, int64_t count, int64_t ld,
+                uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)count};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)(ld * rows * 2)};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args, int sm_count,
+                      void *stream) {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(ns_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return (int)attr_err;
+  const bool gram = (args.mode == kGram || args.mode == kGramA);
+  const bool square = (args.mode == kSquare);
+  for (int32_t c0 = 0; c0 < n_classes; c0 += kMaxClassesPerLaunch) {
+    TcParams T;
+    memset(&T, 0, sizeof T);
+    T.n = std::min(kMaxClassesPerLaunch, n_classes - c0);
+    T.b_mn_major = (gram || square) ? 0 : 1;
+    T.tile_start[0] = 0;
+    for (int k = 0; k < T.n; ++k) {
+      const ShapeClass &C = classes[c0 + k];
+      char *xin = static_cast<char *>(args.x_in) + C.x_base * 2;
+      char *pb = static_cast<char *>(args.pbuf) + C.p_base * 2;
+      char *ab = static_cast<char *>(args.abuf) + C.p_base * 2;
+      bool ok;
+      int Ndim, Kdim;
+      if (gram) {  // A = X rows, B = X rows, K = q
+        ok = encode_map(&T.mapA[k], xin, C.q, C.p, C.count, C.ld, BK, BM) &&
+             encode_map(&T.mapB[k], xin, C.q, C.p, C.count, C.ld, BK, BN);
+        Ndim = C.p;
+        Kdim = C.q;
+      } else if (square) {  // A = Gram rows, B = Gram rows (symmetric), K = p
+        ok = encode_map(&T.mapA[k], ab, C.p, C.p, C.count, C.ldp, BK, BM) &&
+             encode_map(&T.mapB[k], ab, C.p, C.p, C.count, C.ldp, BK, BN);
+        Ndim = C.p;
+        Kdim = C.p;
+      } else {  // A = P rows (K = p), B = X with rows as K, columns as N
+        ok = encode_map(&T.mapA[k], pb, C.p, C.p, C.count, C.ldp, BK, BM) &&
+             encode_map(&T.mapB[k], xin, C.q, C.p, C.count, C.ld, 64, BK);
+        Ndim = C.q;
+        Kdim = C.p;
+      }
+      if (!ok) return (int)cudaErrorInvalidValue;
+      T.tiles_n[k] = (Ndim + BN - 1) / BN;
+      T.k_iters[k] = (Kdim + BK - 1) / BK;
+      T.sub0[k] = C.sub0;
+      T.tiles_per_mat[k] = ((C.p + BM - 1) / BM) * T.tiles_n[k];
+      T.tile_start[k + 1] = T.tile_start[k] + (int64_t)C.count * T.tiles_per_mat[k];
+    }
+    const int64_t total = T.tile_start[T.n];
+    if (total == 0) continue;
+    const unsigned grid = (unsigned)std::min<int64_t>(total, sm_count);
+    ns_gemm_tc_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
+    count_launches(1);
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return (int)err;
+  }
+  return 0;
+}
+
+}  // namespace gbo

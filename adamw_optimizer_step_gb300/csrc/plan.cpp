@@ -1,0 +1,656 @@
+// Host side of the library: descriptor validation, expansion of views into
+// independent matrices, batching by oriented shape, workspace layout, the
+// device tables, and the extern "C" entry points declared in gbo.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+#include <vector>
+#include <atomic>
+
+#include "gbo.h"
+#include "internal.h"
+
+namespace gbo {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+int ok() {
+  t_last_error.clear();
+  return GBO_OK;
+}
+
+int cuda_fail(int err, const char *what) {
+  return fail(GBO_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)err));
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t dtype_size(int32_t dt) { return dt == GBO_BF16 ? 2 : 4; }
+
+bool valid_dtype(int32_t dt) { return dt == GBO_F32 || dt == GBO_BF16; }
+
+// FNV-1a, 64 bit.
+struct Fnv {
+  uint64_t h = 1469598103934665603ull;
+  void bytes(const void *p, size_t n) {
+    const unsigned char *c = static_cast<const unsigned char *>(p);
+    for (size_t i = 0; i < n; ++i) {
+      h ^= c[i];
+      h *= 1099511628211ull;
+    }
+  }
+  template <typename T>
+  void put(T v) { bytes(&v, sizeof v); }
+};
+
+// Per-device facts, looked up once.
+struct DeviceInfo {
+  int sm_count = 0;
+  int major = 0, minor = 0;
+  bool known = false;
+};
+std::mutex g_dev_mu;
+std::map<int, DeviceInfo> g_devs;
+
+int current_device(int *dev, DeviceInfo *info) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo &d = g_devs[*dev];
+  if (!d.known) {
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.known = true;
+  }
+  *info = d;
+  if (!(d.major == 10 && d.minor == 3))
+    return fail(GBO_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only",
+                *dev, d.major, d.minor);
+  return GBO_OK;
+}
+
+constexpr int kPhaseMomentum = 0, kPhaseGram = 1, kPhaseProduct = 2, kPhaseSquare = 3,
+              kPhaseRows = 4;
+
+}  // namespace
+}  // namespace gbo
+
+using namespace gbo;
+
+struct gbo_plan {
+  std::vector<gbo_muon_desc> descs;
+  std::vector<int64_t> pool;
+  gbo_muon_opts opts{};
+  std::vector<float> abc;  // 3 * ns_steps
+  bool any_c = false;
+  std::vector<DevSub> subs;  // sorted by shape class
+  std::vector<ShapeClass> classes;
+  int64_t n_tiles = 0, n_row_blocks = 0;
+  int32_t x_dtype = GBO_BF16;
+  size_t off_x[2] = {0, 0}, off_p = 0, off_a = 0, off_alpha = 0, off_part = 0, ws_bytes = 0;
+  uint64_t hash = 0;
+  gbo_plan_info info{};
+  // device state, set by the first step
+  int device = -1;
+  int sm_count = 0;
+  DevSub *d_subs = nullptr;
+  // phase timing
+  bool timing = false;
+  struct Interval {
+    cudaEvent_t a, b;
+    int phase;
+    int64_t launches;
+  };
+  std::vector<Interval> pending;
+  std::vector<cudaEvent_t> event_pool;
+};
+
+namespace {
+
+int validate_and_expand(gbo_plan *P) {
+  const gbo_muon_opts &o = P->opts;
+  const int32_t n = (int32_t)P->descs.size();
+  std::map<const void *, int32_t> seen;
+  struct Pending {
+    DevSub s;
+    int32_t order;
+  };
+  std::vector<DevSub> subs;
+  std::map<std::pair<int32_t, int32_t>, int32_t> class_of;
+  std::vector<std::pair<int32_t, int32_t>> class_shapes;
+  int64_t dbg_off = 0;
+  for (int32_t t = 0; t < n; ++t) {
+    const gbo_muon_desc &d = P->descs[t];
+    if (!d.w) return fail(GBO_ERR_INVALID_ARG, "desc %d: w is NULL", t);
+    if (!valid_dtype(d.w_dtype) || !valid_dtype(d.g_dtype))
+      return fail(GBO_ERR_DTYPE, "desc %d: dtype must be GBO_F32 or GBO_BF16", t);
+    if (d.rows <= 0 || d.cols <= 0)
+      return fail(GBO_ERR_SHAPE, "desc %d: stored shape %lld x %lld must be positive", t,
+                  (long long)d.rows, (long long)d.cols);
+    if (d.rows > INT32_MAX || d.cols > INT32_MAX)
+      return fail(GBO_ERR_SHAPE, "desc %d: a side above 2^31-1", t);
+    if (!aligned(d.w, dtype_size(d.w_dtype)) || (d.g && !aligned(d.g, dtype_size(d.g_dtype))) ||
+        (d.mom && !aligned(d.mom, 4)) || (d.row_v && !aligned(d.row_v, 4)))
+      return fail(GBO_ERR_INVALID_ARG, "desc %d: pointer not aligned to its element size", t);
+    if (seen.count(d.w))
+      return fail(GBO_ERR_CONFLICT, "desc %d: weight %p already listed as desc %d", t, d.w, seen[d.w]);
+    seen[d.w] = t;
+    // view rules
+    int64_t view[GBO_MAX_VIEW_DIMS];
+    int nd = d.view_ndim;
+    if (nd == 0) {
+      nd = 2;
+      view[0] = d.rows;
+      view[1] = d.cols;
+    } else {
+      if (nd < 2 || nd > GBO_MAX_VIEW_DIMS)
+        return fail(GBO_ERR_SHAPE, "desc %d: view_ndim %d outside 2..%d", t, nd, GBO_MAX_VIEW_DIMS);
+      int64_t lead = 1;
+      for (int k = 0; k < nd; ++k) {
+        view[k] = d.view[k];
+        if (view[k] <= 0) return fail(GBO_ERR_SHAPE, "desc %d: view entry %d is not positive", t, k);
+        if (k < nd - 1) {
+          if (lead > d.rows / view[k] + 1) return fail(GBO_ERR_SHAPE, "desc %d: view product overflows", t);
+          lead *= view[k];
+        }
+      }
+      if (lead != d.rows || view[nd - 1] != d.cols)
+        return fail(GBO_ERR_SHAPE,
+                    "desc %d: flattened view leading axes give %lld x %lld, stored %lld x %lld", t,
+                    (long long)lead, (long long)view[nd - 1], (long long)d.rows, (long long)d.cols);
+    }
+    const int64_t r = view[nd - 2];
+    std::vector<int64_t> split;
+    if (d.n_split < 0) return fail(GBO_ERR_SHAPE, "desc %d: negative n_split", t);
+    if (d.n_split > 0) {
+      if (!P->pool.size() || d.split_off < 0 || (int64_t)d.split_off + d.n_split > (int64_t)P->pool.size())
+        return fail(GBO_ERR_INVALID_ARG, "desc %d: split sizes outside the split pool", t);
+      int64_t sum = 0;
+      for (int k = 0; k < d.n_split; ++k) {
+        const int64_t s = P->pool[d.split_off + k];
+        if (s <= 0) return fail(GBO_ERR_SHAPE, "desc %d: split size %d is not positive", t, k);
+        sum += s;
+        split.push_back(s);
+      }
+      if (sum != r)
+        return fail(GBO_ERR_SHAPE, "desc %d: split sizes sum to %lld, view row axis is %lld", t,
+                    (long long)sum, (long long)r);
+    } else {
+      split.push_back(r);
+    }
+    const int64_t this_dbg = dbg_off;
+    dbg_off += d.rows * d.cols;
+    if (!d.g) continue;  // skipped this step: inactive
+    if (!d.mom) return fail(GBO_ERR_INVALID_ARG, "desc %d: mom is NULL", t);
+    if (o.normuon && !d.row_v) return fail(GBO_ERR_INVALID_ARG, "desc %d: NorMuon needs row_v", t);
+    const bool vec_rows = (d.cols % 4 == 0) && aligned(d.g, 16) && aligned(d.mom, 16) &&
+                          (d.g_dtype == GBO_BF16 ? aligned(d.g, 8) : true);
+    const int64_t blocks = d.rows / r;
+    for (int64_t b = 0; b < blocks; ++b) {
+      int64_t start = b * r;
+      for (int64_t s : split) {
+        DevSub S{};
+        S.w = d.w;
+        S.g = d.g;
+        S.mom = d.mom;
+        S.row_v = d.row_v;
+        S.r0 = start;
+        S.cols = d.cols;
+        S.m = (int32_t)s;
+        S.n = (int32_t)d.cols;
+        S.transposed = S.m > S.n;
+        S.p = std::min(S.m, S.n);
+        S.q = std::max(S.m, S.n);
+        S.w_dtype = d.w_dtype;
+        S.g_dtype = d.g_dtype;
+        S.vec_ok = vec_rows;
+        S.scale = (float)std::sqrt(std::max(1.0, (double)S.m / (double)S.n));
+        S.lr_mult = d.lr_mult;
+        S.wd = d.wd;
+        S.dbg_off = this_dbg;
+        const auto key = std::make_pair(S.p, S.q);
+        auto it = class_of.find(key);
+        if (it == class_of.end()) {
+          it = class_of.emplace(key, (int32_t)class_shapes.size()).first;
+          class_shapes.push_back(key);
+        }
+        S.cls = it->second;
+        subs.push_back(S);
+        start += s;
+      }
+    }
+  }
+  // order by class (stable: table order within a class)
+  std::stable_sort(subs.begin(), subs.end(), [](const DevSub &a, const DevSub &b) { return a.cls < b.cls; });
+  const size_t es = P->x_dtype == GBO_BF16 ? 2 : 4;
+  P->classes.clear();
+  int64_t xoff = 0, poff = 0;
+  for (size_t c = 0; c < class_shapes.size(); ++c) {
+    ShapeClass C{};
+    C.p = class_shapes[c].first;
+    C.q = class_shapes[c].second;
+    C.ld = (int32_t)round_up(C.q, 16);
+    C.ldp = (int32_t)round_up(C.p, 16);
+    C.count = 0;
+    C.sub0 = -1;
+    C.x_base = xoff;
+    C.p_base = poff;
+    for (size_t k = 0; k < subs.size(); ++k)
+      if (subs[k].cls == (int32_t)c) {
+        if (C.sub0 < 0) C.sub0 = (int32_t)k;
+        DevSub &S = subs[k];
+        S.ld = C.ld;
+        S.ldp = C.ldp;
+        S.x_off = xoff + (int64_t)C.count * C.p * C.ld;
+        S.p_off = poff + (int64_t)C.count * C.p * C.ldp;
+        C.count++;
+      }
+    xoff = round_up(xoff + (int64_t)C.count * C.p * C.ld, 128);
+    poff = round_up(poff + (int64_t)C.count * C.p * C.ldp, 128);
+    P->classes.push_back(C);
+  }
+  // momentum tiles and NorMuon row blocks, in table order of subs
+  int64_t tiles = 0, rbs = 0;
+  for (DevSub &S : subs) {
+    S.tiles_c = (S.n + kMomTile - 1) / kMomTile;
+    S.tile0 = tiles;
+    tiles += (int64_t)((S.m + kMomTile - 1) / kMomTile) * S.tiles_c;
+    S.rb0 = rbs;
+    rbs += (S.m + kRowBlock - 1) / kRowBlock;
+  }
+  P->n_tiles = tiles;
+  P->n_row_blocks = rbs;
+  P->subs = std::move(subs);
+  // workspace layout
+  size_t off = 0;
+  auto region = [&](size_t bytes) {
+    const size_t at = off;
+    off = (size_t)round_up((int64_t)(off + bytes), 256);
+    return at;
+  };
+  P->off_x[0] = region((size_t)xoff * es);
+  P->off_x[1] = region((size_t)xoff * es);
+  P->off_p = region((size_t)poff * es);
+  P->off_a = region(P->any_c ? (size_t)poff * es : 0);
+  P->off_alpha = region(P->subs.size() * sizeof(float));
+  P->off_part = region((size_t)tiles * 2 * sizeof(float));
+  P->ws_bytes = off;
+  // info
+  gbo_plan_info &I = P->info;
+  I.n_weights = n;
+  I.n_active = 0;
+  for (const auto &d : P->descs)
+    if (d.g) I.n_active++, I.muon_params += d.rows * d.cols;
+  I.n_matrices = (int64_t)P->subs.size();
+  I.n_shape_classes = (int64_t)P->classes.size();
+  double fl = 0;
+  for (const DevSub &S : P->subs) {
+    const double p = S.p, q = S.q;
+    for (int it = 0; it < o.ns_steps; ++it)
+      fl += 4.0 * p * p * q + (P->abc[3 * it + 2] != 0.f ? 2.0 * p * p * p : 0.0);
+  }
+  I.ns_flops = fl;
+  I.ns_flops_executed = fl;
+  return GBO_OK;
+}
+
+uint64_t layout_hash(const gbo_plan *P) {
+  Fnv f;
+  f.put<int32_t>((int32_t)P->descs.size());
+  for (const auto &d : P->descs) {
+    f.put(d.rows);
+    f.put(d.cols);
+    f.put(d.w_dtype);
+    f.put(d.view_ndim);
+    for (int k = 0; k < d.view_ndim; ++k) f.put(d.view[k]);
+    f.put(d.n_split);
+    for (int k = 0; k < d.n_split; ++k) f.put(P->pool[d.split_off + k]);
+  }
+  f.put(P->opts.normuon);
+  return f.h;
+}
+
+int launch_gemm(const gbo_plan *P, const PhaseArgs &args, void *stream) {
+  if (P->x_dtype == GBO_F32)
+    return launch_ns_gemm_simt(P->classes.data(), (int32_t)P->classes.size(), args, P->sm_count, stream);
+  return launch_ns_gemm_tc(P->classes.data(), (int32_t)P->classes.size(), args, P->sm_count, stream);
+}
+
+int64_t gemm_launches(const gbo_plan *P) {
+  return (int64_t)((P->classes.size() + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch);
+}
+
+cudaEvent_t take_event(gbo_plan *P) {
+  if (!P->event_pool.empty()) {
+    cudaEvent_t e = P->event_pool.back();
+    P->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gbo_last_error(void) { return t_last_error.c_str(); }
+
+int32_t gbo_abi_version(void) { return GBO_ABI_VERSION; }
+
+size_t gbo_struct_size(int32_t which) {
+  switch (which) {
+    case 0: return sizeof(gbo_muon_desc);
+    case 1: return sizeof(gbo_muon_opts);
+    case 2: return sizeof(gbo_tensor);
+    case 3: return sizeof(gbo_adamw_desc);
+    case 4: return sizeof(gbo_adamw_opts);
+    case 5: return sizeof(gbo_plan_info);
+    default: return 0;
+  }
+}
+
+uint64_t gbo_launch_count(void) { return g_launches.load(); }
+
+int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *split_pool,
+                         int32_t pool_len, const gbo_muon_opts *opts, gbo_plan **out) {
+  if (!out) return fail(GBO_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!opts) return fail(GBO_ERR_INVALID_ARG, "opts is NULL");
+  if (n < 0) return fail(GBO_ERR_INVALID_ARG, "negative descriptor count");
+  if (n == 0) return fail(GBO_ERR_EMPTY, "empty descriptor table: nothing to optimise");
+  if (!descs) return fail(GBO_ERR_INVALID_ARG, "descs is NULL");
+  if (pool_len < 0 || (pool_len > 0 && !split_pool)) return fail(GBO_ERR_INVALID_ARG, "bad split pool");
+  if (opts->ns_steps < 1 || opts->ns_steps > GBO_MAX_NS_STEPS)
+    return fail(GBO_ERR_INVALID_ARG, "ns_steps %d outside 1..%d", opts->ns_steps, GBO_MAX_NS_STEPS);
+  if (!opts->abc) return fail(GBO_ERR_INVALID_ARG, "abc is NULL");
+  if (opts->precision != GBO_NS_BF16 && opts->precision != GBO_NS_F32)
+    return fail(GBO_ERR_INVALID_ARG, "precision must be GBO_NS_BF16 or GBO_NS_F32");
+  if (!std::isfinite(opts->mu)) return fail(GBO_ERR_INVALID_ARG, "mu is not finite");
+  if (opts->normuon && (!(opts->beta2 >= 0.f && opts->beta2 <= 1.f) || !(opts->eps >= 0.f)))
+    return fail(GBO_ERR_INVALID_ARG, "NorMuon needs 0 <= beta2 <= 1 and eps >= 0");
+  gbo_plan *P = new gbo_plan();
+  P->descs.assign(descs, descs + n);
+  if (pool_len > 0) P->pool.assign(split_pool, split_pool + pool_len);
+  P->opts = *opts;
+  P->opts.abc = nullptr;
+  const int k = opts->ns_steps;
+  P->abc.resize(3 * k);
+  for (int it = 0; it < k; ++it)
+    for (int j = 0; j < 3; ++j) {
+      const float v = opts->abc_per_step ? opts->abc[3 * it + j] : opts->abc[j];
+      if (!std::isfinite(v)) {
+        delete P;
+        return fail(GBO_ERR_INVALID_ARG, "coefficient %d of iteration %d is not finite", j, it);
+      }
+      P->abc[3 * it + j] = v;
+    }
+  for (int it = 0; it < k; ++it) P->any_c |= P->abc[3 * it + 2] != 0.f;
+  P->x_dtype = opts->precision == GBO_NS_F32 ? GBO_F32 : GBO_BF16;
+  const int rc = validate_and_expand(P);
+  if (rc != GBO_OK) {
+    delete P;
+    return rc;
+  }
+  P->hash = layout_hash(P);
+  int64_t per_iter = 0;
+  for (int it = 0; it < k; ++it) per_iter += (P->abc[3 * it + 2] != 0.f ? 3 : 2) * gemm_launches(P);
+  P->info.launches_per_step = P->subs.empty() ? 0 : 2 + per_iter + (opts->normuon ? 1 : 0);
+  *out = P;
+  return ok();
+}
+
+void gbo_muon_plan_destroy(gbo_plan *P) {
+  if (!P) return;
+  if (P->d_subs) cudaFree(P->d_subs);
+  for (auto &iv : P->pending) {
+    cudaEventDestroy(iv.a);
+    cudaEventDestroy(iv.b);
+  }
+  for (cudaEvent_t e : P->event_pool) cudaEventDestroy(e);
+  delete P;
+}
+
+size_t gbo_muon_workspace_bytes(const gbo_plan *P) { return P ? P->ws_bytes : 0; }
+
+uint64_t gbo_desc_hash(const gbo_plan *P) { return P ? P->hash : 0; }
+
+int gbo_muon_plan_info(const gbo_plan *P, gbo_plan_info *out) {
+  if (!P || !out) return fail(GBO_ERR_INVALID_ARG, "NULL argument");
+  *out = P->info;
+  return ok();
+}
+
+int gbo_muon_plan_set_timing(gbo_plan *P, int32_t enable) {
+  if (!P) return fail(GBO_ERR_INVALID_ARG, "plan is NULL");
+  P->timing = enable != 0;
+  return ok();
+}
+
+int gbo_muon_plan_phase_times(gbo_plan *P, float *ms, int64_t *launches, int32_t n_phases) {
+  if (!P || n_phases < 0 || (n_phases > 0 && (!ms || !launches)))
+    return fail(GBO_ERR_INVALID_ARG, "bad argument");
+  for (int i = 0; i < n_phases; ++i) {
+    ms[i] = 0.f;
+    launches[i] = 0;
+  }
+  if (!P->pending.empty()) {
+    cudaError_t e = cudaEventSynchronize(P->pending.back().b);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+  }
+  for (auto &iv : P->pending) {
+    float t = 0.f;
+    cudaError_t e = cudaEventElapsedTime(&t, iv.a, iv.b);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    if (iv.phase < n_phases) {
+      ms[iv.phase] += t;
+      launches[iv.phase] += iv.launches;
+    }
+    P->event_pool.push_back(iv.a);
+    P->event_pool.push_back(iv.b);
+  }
+  P->pending.clear();
+  return ok();
+}
+
+int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float *dbg_update,
+                  int32_t *dev_status, gbo_stream_t stream) {
+  if (!P) return fail(GBO_ERR_INVALID_ARG, "plan is NULL");
+  if (!std::isfinite(lr)) return fail(GBO_ERR_INVALID_ARG, "lr is not finite");
+  if (P->subs.empty()) return ok();
+  if (!workspace || ws_bytes < P->ws_bytes)
+    return fail(GBO_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P->ws_bytes, ws_bytes);
+  if (!aligned(workspace, 256)) return fail(GBO_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (!aligned(dbg_update, 4) || !aligned(dev_status, 4))
+    return fail(GBO_ERR_INVALID_ARG, "dbg_update / dev_status misaligned");
+  int dev = -1;
+  DeviceInfo di;
+  int rc = current_device(&dev, &di);
+  if (rc != GBO_OK) return rc;
+  if (P->device < 0) {
+    // first call on a device: upload the matrix table
+    cudaError_t e = cudaMalloc(&P->d_subs, P->subs.size() * sizeof(DevSub));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(matrix table)");
+    e = cudaMemcpy(P->d_subs, P->subs.data(), P->subs.size() * sizeof(DevSub), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(matrix table)");
+    P->device = dev;
+    P->sm_count = di.sm_count;
+  } else if (P->device != dev) {
+    return fail(GBO_ERR_INVALID_ARG, "plan was set up on device %d, current device is %d", P->device, dev);
+  }
+  char *ws = static_cast<char *>(workspace);
+  void *x[2] = {ws + P->off_x[0], ws + P->off_x[1]};
+  void *pbuf = ws + P->off_p;
+  void *abuf = ws + P->off_a;
+  float *alpha = reinterpret_cast<float *>(ws + P->off_alpha);
+  float *partials = reinterpret_cast<float *>(ws + P->off_part);
+  void *st = stream;
+  cudaEvent_t last = nullptr;
+  auto mark = [&](int phase, int64_t n_launch) {
+    if (!P->timing) return;
+    cudaEvent_t b = take_event(P);
+    cudaEventRecord(b, reinterpret_cast<cudaStream_t>(stream));
+    P->pending.push_back({last, b, phase, n_launch});
+    last = take_event(P);
+    cudaEventRecord(last, reinterpret_cast<cudaStream_t>(stream));
+  };
+  if (P->timing) {
+    last = take_event(P);
+    cudaEventRecord(last, reinterpret_cast<cudaStream_t>(stream));
+  }
+  const int32_t nsub = (int32_t)P->subs.size();
+  int err = launch_momentum(P->d_subs, nsub, P->n_tiles, P->opts.mu, P->opts.nesterov, x[0], P->x_dtype,
+                            partials, P->sm_count, st);
+  if (err) return cuda_fail(err, "momentum kernel");
+  err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, st);
+  if (err) return cuda_fail(err, "pre-normalisation kernel");
+  mark(kPhaseMomentum, 2);
+  PhaseArgs A{};
+  A.x_dtype = P->x_dtype;
+  A.subs = P->d_subs;
+  A.alpha = alpha;
+  A.pbuf = pbuf;
+  A.abuf = abuf;
+  A.dbg = dbg_update;
+  A.status = dev_status;
+  A.lr = lr;
+  const int k = P->opts.ns_steps;
+  const int64_t gl = gemm_launches(P);
+  int cur = 0;
+  for (int it = 0; it < k; ++it) {
+    A.a = P->abc[3 * it];
+    A.b = P->abc[3 * it + 1];
+    A.c = P->abc[3 * it + 2];
+    A.first = it == 0;
+    A.x_in = x[cur];
+    A.x_out = x[cur ^ 1];
+    if (A.c != 0.f) {
+      A.mode = kGramA;
+      if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "Gram kernel");
+      mark(kPhaseGram, gl);
+      A.mode = kSquare;
+      if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "square kernel");
+      mark(kPhaseSquare, gl);
+    } else {
+      A.mode = kGram;
+      if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "Gram kernel");
+      mark(kPhaseGram, gl);
+    }
+    const bool last_it = it == k - 1;
+    A.mode = (last_it && !P->opts.normuon) ? kFinal : kProduct;
+    if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "product kernel");
+    mark(kPhaseProduct, gl);
+    cur ^= 1;
+  }
+  if (P->opts.normuon) {
+    err = launch_normuon_rows(P->d_subs, nsub, P->n_row_blocks, x[cur], P->x_dtype, P->opts.beta2,
+                              P->opts.eps, lr, dbg_update, dev_status, P->sm_count, st);
+    if (err) return cuda_fail(err, "NorMuon rows kernel");
+    mark(kPhaseRows, 1);
+  }
+  if (P->timing && last) P->event_pool.push_back(last);
+  return ok();
+}
+
+int gbo_normuon_rownorm(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
+                        int32_t w_dtype, float beta2, float eps, float scale, float lr, float wd,
+                        float *dbg_update, gbo_stream_t stream) {
+  if (rows < 0 || cols < 0) return fail(GBO_ERR_INVALID_ARG, "negative size");
+  if (rows == 0 || cols == 0) return ok();
+  if (!O || !row_v || !w) return fail(GBO_ERR_INVALID_ARG, "NULL pointer");
+  if (!valid_dtype(w_dtype)) return fail(GBO_ERR_DTYPE, "w_dtype must be GBO_F32 or GBO_BF16");
+  if (!aligned(O, 4) || !aligned(row_v, 4) || !aligned(w, dtype_size(w_dtype)) || !aligned(dbg_update, 4))
+    return fail(GBO_ERR_INVALID_ARG, "misaligned pointer");
+  int dev;
+  DeviceInfo di;
+  int rc = current_device(&dev, &di);
+  if (rc != GBO_OK) return rc;
+  const int err = launch_normuon_rownorm_plain(O, rows, cols, row_v, w, w_dtype, beta2, eps, scale, lr,
+                                               wd, dbg_update, stream);
+  if (err) return cuda_fail(err, "NorMuon rownorm kernel");
+  return ok();
+}
+
+size_t gbo_clip_norm_workspace_bytes(void) { return (size_t)kClipBlocks * sizeof(float); }
+
+int gbo_clip_norm(const gbo_tensor *grads, int32_t n, float max_norm, float *dev_total_norm,
+                  float *dev_coef, int32_t *dev_status, void *workspace, size_t ws_bytes,
+                  gbo_stream_t stream) {
+  if (n < 0 || (n > 0 && !grads)) return fail(GBO_ERR_INVALID_ARG, "bad gradient table");
+  if (n > 64 * kClipBlocks) return fail(GBO_ERR_INVALID_ARG, "more than %d tensors", 64 * kClipBlocks);
+  if (!(max_norm > 0.f) || !std::isfinite(max_norm)) return fail(GBO_ERR_INVALID_ARG, "max_norm must be > 0");
+  if (!workspace || ws_bytes < gbo_clip_norm_workspace_bytes())
+    return fail(GBO_ERR_WORKSPACE, "clip workspace of %zu bytes needed", gbo_clip_norm_workspace_bytes());
+  if (!aligned(workspace, 16)) return fail(GBO_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  for (int32_t i = 0; i < n; ++i) {
+    if (!valid_dtype(grads[i].dtype)) return fail(GBO_ERR_DTYPE, "tensor %d: bad dtype", i);
+    if (grads[i].numel < 0) return fail(GBO_ERR_INVALID_ARG, "tensor %d: negative numel", i);
+    if (grads[i].numel > 0 && (!grads[i].ptr || !aligned(grads[i].ptr, dtype_size(grads[i].dtype))))
+      return fail(GBO_ERR_INVALID_ARG, "tensor %d: NULL or misaligned pointer", i);
+  }
+  int dev;
+  DeviceInfo di;
+  int rc = current_device(&dev, &di);
+  if (rc != GBO_OK) return rc;
+  const int err = launch_clip_norm(grads, n, max_norm, dev_total_norm, dev_coef, dev_status,
+                                   static_cast<float *>(workspace), di.sm_count, stream);
+  if (err) return cuda_fail(err, "clip-norm kernels");
+  return ok();
+}
+
+int gbo_adamw_step(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *opts,
+                   const float *dev_coef, int32_t *dev_status, gbo_stream_t stream) {
+  if (n < 0 || (n > 0 && !descs) || !opts) return fail(GBO_ERR_INVALID_ARG, "bad argument");
+  if (opts->step < 1) return fail(GBO_ERR_INVALID_ARG, "step must be >= 1");
+  if (!(opts->beta1 >= 0.f && opts->beta1 < 1.f) || !(opts->beta2 >= 0.f && opts->beta2 < 1.f))
+    return fail(GBO_ERR_INVALID_ARG, "betas must be in [0, 1)");
+  if (!std::isfinite(opts->lr) || !std::isfinite(opts->eps) || !std::isfinite(opts->weight_decay))
+    return fail(GBO_ERR_INVALID_ARG, "non-finite hyper-parameter");
+  for (int32_t i = 0; i < n; ++i) {
+    const gbo_adamw_desc &d = descs[i];
+    if (!valid_dtype(d.g_dtype)) return fail(GBO_ERR_DTYPE, "tensor %d: bad g dtype", i);
+    if (d.numel < 0) return fail(GBO_ERR_INVALID_ARG, "tensor %d: negative numel", i);
+    if (d.numel > 0 && (!d.p || !d.g || !d.m || !d.v))
+      return fail(GBO_ERR_INVALID_ARG, "tensor %d: NULL pointer", i);
+    if (!aligned(d.p, 4) || !aligned(d.m, 4) || !aligned(d.v, 4) || !aligned(d.g, dtype_size(d.g_dtype)))
+      return fail(GBO_ERR_INVALID_ARG, "tensor %d: misaligned pointer", i);
+  }
+  if (!aligned(dev_coef, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_coef misaligned");
+  int dev;
+  DeviceInfo di;
+  int rc = current_device(&dev, &di);
+  if (rc != GBO_OK) return rc;
+  const int err = launch_adamw(descs, n, opts, dev_coef, dev_status, di.sm_count, stream);
+  if (err) return cuda_fail(err, "AdamW kernel");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,397 @@
+"""Benchmark: one hybrid optimizer step (Muon on every view-split matrix of
+the 1.23B-parameter OMN-shaped set + global-norm clip + AdamW on the
+262M-parameter embedding and gains), timed on the GPU.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  ``value`` is optimizer steps per second over all
+ranks (each rank runs a full replica: the step has no cross-device exchange
+on one node here), inputs resident in HBM.  ``e2e`` is the same metric
+with each step's gradients copied in from pinned host memory and the step's
+gradient norm read back.  ``--impl reference`` times the fp64 CPU oracle on
+a bounded sample of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "optimizer steps/sec (1.24B-param Muon set); NS TFLOP/s and % BF16 peak"
+WORKLOAD = 3
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, world):
+    """Largest value over all ranks (identity on one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(steps, seconds_max, world):
+    """Whole-job steps/s: every rank ran ``steps`` steps of a full replica."""
+    return world * steps / seconds_max
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the fp64 oracle on a bounded sample (CPU baseline and the reference arm)
+
+def oracle_sample_time(wl, budget_elems=4_000_000):
+    """Time the oracle on one matrix of every distinct oriented shape plus an
+    AdamW slice, and extrapolate to the whole step.  Returns (seconds per
+    full step, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from adamw_optimizer_step_gb300 import workloads as wk
+    from oracle.views import sub_matrices
+
+    counts = {}
+    first = {}
+    for i, t in enumerate(wl.muon):
+        for r0, m, n in sub_matrices(t.rows, t.cols, t.view, t.split):
+            counts[(m, n)] = counts.get((m, n), 0) + 1
+            first.setdefault((m, n), (i, r0))
+    total = 0.0
+    parts = []
+    for (m, n), c in counts.items():
+        i, r0 = first[(m, n)]
+        t = wl.muon[i]
+        W, G, Bm, _ = wk.muon_tensor_inputs(wl, i)
+        W, G, Bm = (x[r0:r0 + m].double().numpy() for x in (W, G, Bm))
+        t0 = time.perf_counter()
+        oracle.muon_step_tensor(W, G, Bm, lr=wl.lr)
+        dt = time.perf_counter() - t0
+        total += c * dt
+        parts.append("%dx%d x%d" % (m, n, c))
+    n_adam = wl.adamw_params
+    if n_adam:
+        k = min(budget_elems, n_adam)
+        g = torch.Generator().manual_seed(7)
+        p, gr, mm, vv = (torch.randn(k, generator=g).double().numpy() for _ in range(4))
+        vv = np.abs(vv)
+        t0 = time.perf_counter()
+        N = oracle.global_grad_norm([gr])
+        oracle.adamw_update(p, gr, mm, vv, coef=oracle.clip_coefficient(N, 1.0), lr=3e-4, t=1)
+        dt = time.perf_counter() - t0
+        total += dt * n_adam / k
+        parts.append("AdamW %d of %d elements" % (k, n_adam))
+    return total, "one matrix per shape (%s), scaled by count; %s" % (", ".join(parts[:-1]), parts[-1])
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from adamw_optimizer_step_gb300 import workloads as wk
+    wl = wk.workload(WORKLOAD)
+    for _ in range(args.warmup):
+        oracle_sample_time(wl, budget_elems=1_000_000)
+    times = []
+    desc = ""
+    for _ in range(args.steps):
+        t, desc = oracle_sample_time(wl)
+        times.append(t)
+    times.sort()
+    per_step = times[len(times) // 2]
+    value = 1.0 / per_step
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "muon_params": wl.muon_params,
+                   "adamw_params": wl.adamw_params},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# ours
+
+def traffic_record(kernel_file):
+    """DRAM bytes per unit from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    src = open(os.path.join(ROOT, "adamw_optimizer_step_gb300", "csrc", kernel_file), "rb").read()
+    if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    return rec
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import adamw_optimizer_step_gb300 as gbo
+    from adamw_optimizer_step_gb300 import workloads as wk
+
+    gbo.lib()
+    wl = wk.workload(WORKLOAD)
+    dev = "cuda"
+    # Muon gradients live in one flat buffer so the end-to-end run can copy
+    # a step's gradients in with one transfer; likewise the AdamW gradients.
+    n_muon = wl.muon_params
+    g_flat = torch.empty(n_muon, dtype=wl.g_dtype, device=dev)
+    entries = []
+    off = 0
+    for i, t in enumerate(wl.muon):
+        W, G, Bm, v = wk.muon_tensor_inputs(wl, i, device=dev)
+        g = g_flat[off:off + t.numel].view(t.rows, t.cols)
+        g.copy_(G)
+        del G
+        off += t.numel
+        entries.append(dict(w=W, g=g, mom=Bm, row_v=v, view=t.view, split=t.split))
+    n_adam = wl.adamw_params
+    ag_flat = torch.empty(n_adam, dtype=torch.float32, device=dev)
+    params = []
+    off = 0
+    for i, t in enumerate(wl.adamw):
+        p, g, m, v = wk.adamw_tensor_inputs(wl, i, device=dev)
+        gv = ag_flat[off:off + t.numel].view(t.shape)
+        gv.copy_(g)
+        del g
+        off += t.numel
+        params.append((p, gv, m, v))
+    plan = gbo.gbo_muon_plan_create(entries, precision=gbo.GBO_NS_BF16, normuon=wl.normuon)
+    info = gbo.gbo_muon_plan_info(plan)
+    ws = torch.empty(gbo.gbo_muon_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+    cws = torch.empty(gbo.gbo_clip_norm_workspace_bytes(), dtype=torch.uint8, device=dev)
+    total = torch.zeros(1, device=dev)
+    coef = torch.zeros(1, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    adam_grads = [p[1] for p in params]
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    step_no = [0]
+
+    def step(record=None):
+        step_no[0] += 1
+        gbo.gbo_muon_step(plan, wl.lr, ws, dev_status=status)
+        if record is not None:
+            record[0].record(stream)
+        gbo.gbo_clip_norm(adam_grads, 1.0, total, coef, cws, dev_status=status)
+        gbo.gbo_adamw_step(params, lr=wl.adamw_lr, step=step_no[0], coef=coef, dev_status=status)
+        if record is not None:
+            record[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: inputs resident in HBM (the working set is ~20 GB, far
+    # above the 129 MB L2, so every step streams from HBM)
+    gbo.gbo_muon_plan_set_timing(plan, True)
+    gbo.gbo_muon_plan_phase_times(plan)  # reset
+    adam_ev = [(ev(), ev()) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    l0 = gbo.gbo_launch_count()
+    start, end = ev(), ev()
+    start.record(stream)
+    for k in range(args.steps):
+        step(adam_ev[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = gbo.gbo_launch_count() - l0
+    clk = clocks.stop()
+    phases = gbo.gbo_muon_plan_phase_times(plan)
+    gbo.gbo_muon_plan_set_timing(plan, False)
+    elapsed = start.elapsed_time(end) / 1e3
+    elapsed_max = max_over_ranks(elapsed, world)
+    adam_ms = sum(a.elapsed_time(b) for a, b in adam_ev) / args.steps
+    value = aggregate(args.steps, elapsed_max, world)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d during the timed steps" % int(status.item()))
+
+    # end to end: gradients from pinned host memory, norm read back
+    h_g = torch.empty(n_muon, dtype=wl.g_dtype, pin_memory=True)
+    h_ag = torch.empty(n_adam, dtype=torch.float32, pin_memory=True)
+    h_g.copy_(g_flat)
+    h_ag.copy_(ag_flat)
+    e2e_steps = max(1, args.e2e_steps)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        g_flat.copy_(h_g, non_blocking=True)
+        ag_flat.copy_(h_ag, non_blocking=True)
+        step()
+        _ = float(total.item())  # the step's gradient norm, read on the host
+    torch.cuda.synchronize()
+    e2e_t = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = aggregate(e2e_steps, e2e_t, world)
+
+    if rank != 0:
+        return
+    ms_step = elapsed_max * 1e3 / args.steps
+    gram_ms, gram_n = phases["gram"]
+    prod_ms, prod_n = phases["product"]
+    sq_ms, sq_n = phases["square"]
+    gemm_ms = (gram_ms + prod_ms + sq_ms) / args.steps
+    gemm_launches = (gram_n + prod_n + sq_n) / args.steps
+    flops = info["ns_flops_executed"]
+    achieved_tf = flops / (gemm_ms / 1e3) / 1e12
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    peak_tf = peaks.get("bf16_tflops_sustained")
+    peak_src = "measured (sustained, MEASURED_PEAKS.json)"
+    if peak_tf is None:
+        peak_tf, peak_src = 1700.0, "fallback sustained"
+    tr = traffic_record("ns_gemm_tc.cu")
+    traffic = None
+    if tr is not None:
+        traffic = tr["bytes_per_unit"] * (flops / gemm_launches) / tr["unit_flops"]
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        t_cpu, desc = oracle_sample_time(wl)
+        cpu = {"value": 1.0 / t_cpu, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": desc}
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    adam_bytes = 32.0 * n_adam
+    out = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "muon_params": wl.muon_params,
+                   "adamw_params": n_adam, "matrices": info["n_matrices"], "ns_steps": wl.ns_steps,
+                   "ns_precision": "bf16 operands, fp32 accumulate", "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "working set ~20 GB per GPU, far above the 129 MB L2: no flush needed"},
+        "roofline": {"bound": "tensor", "kernel": "ns_gemm_tc_kernel (Gram + product launches)",
+                     "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
+                     "peak_source": peak_src, "traffic": traffic,
+                     "flops_per_launch": flops / gemm_launches, "ms_per_launch": gemm_ms / gemm_launches},
+        "phases_ms_per_step": {k: v[0] / args.steps for k, v in phases.items()},
+        "adamw_clip": {"ms": adam_ms, "GB/s": adam_bytes / (adam_ms / 1e3) / 1e9,
+                       "frac_of_hbm": adam_bytes / (adam_ms / 1e3) / 1e9 / hbm},
+        "ns_tflops": achieved_tf,
+        "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": int(h_g.numel() * h_g.element_size()
+                                                                               + h_ag.numel() * 4),
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,306 @@
+/*
+ * gbo.h -- C ABI of the GB300 hybrid-optimizer library (libgbo.so).
+ *
+ * One optimizer step of the hybrid Muon + AdamW recipe on one GPU:
+ *   - the Muon path on 2-D projection weights, each stored weight split into
+ *     independent matrices by a view ("build_parameter_groups", kimi-k3 docs,
+ *     section "Recording independent matrix geometry");
+ *   - the elementwise AdamW path with a global-norm clip on the AdamW
+ *     gradients only ("Dual-Manifold Optimization in OMN", AdamW paragraph).
+ *
+ * Conventions for every entry point
+ *   - Device pointers point to memory the caller allocated (PyTorch, or
+ *     cudaMalloc); the library never frees them.  Host pointers are read
+ *     during the call only unless stated otherwise.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and is asynchronous: no entry point synchronises the
+ *     host with the device, except gbo_muon_plan_phase_times.
+ *   - Return value: GBO_OK (0) or a negative GBO_ERR_* code.  On error
+ *     nothing is enqueued and gbo_last_error() returns a message (per host
+ *     thread).
+ *   - Conditions found on the device (a non-finite norm, a wait that ran out
+ *     of time) are OR-ed into an int32 status word in device memory
+ *     (`dev_status`, may be NULL).  The library never clears it; the caller
+ *     zeroes it when it wants a fresh reading.  Kernels never trap.
+ *   - All matrices are row-major.  A stored weight is rows x cols in
+ *     PyTorch's out-by-in orientation.
+ *   - Every reduction runs in a fixed order: results are bitwise
+ *     reproducible run to run on the same device and inputs.
+ */
+#ifndef GBO_H
+#define GBO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GBO_ABI_VERSION 1
+
+/* ---- status codes (return values) ------------------------------------ */
+#define GBO_OK 0
+#define GBO_ERR_INVALID_ARG (-1) /* NULL or out-of-range argument, misaligned pointer */
+#define GBO_ERR_SHAPE (-2)       /* view product / split-sum / size rules broken       */
+#define GBO_ERR_CONFLICT (-3)    /* one weight listed twice in a descriptor table      */
+#define GBO_ERR_EMPTY (-4)       /* empty descriptor table                             */
+#define GBO_ERR_DTYPE (-5)       /* unsupported dtype                                  */
+#define GBO_ERR_WORKSPACE (-6)   /* workspace missing, too small or misaligned         */
+#define GBO_ERR_CUDA (-7)        /* a CUDA runtime or driver call failed               */
+#define GBO_ERR_UNSUPPORTED (-8) /* device or option this build does not handle        */
+
+/* ---- device status bits (OR-ed into *dev_status) ---------------------- */
+#define GBO_STATUS_NONFINITE 1 /* a norm or a scale came out NaN or Inf             */
+#define GBO_STATUS_TIMEOUT 2   /* a bounded device-side wait gave up; outputs invalid */
+
+/* ---- element types ------------------------------------------------------ */
+#define GBO_F32 0
+#define GBO_BF16 1
+
+/* ---- Newton-Schulz arithmetic ------------------------------------------ */
+#define GBO_NS_BF16 0 /* bf16 operands, fp32 accumulation (tcgen05 tensor cores) */
+#define GBO_NS_F32 1  /* fp32 operands and accumulation (FFMA)                    */
+
+#define GBO_MAX_VIEW_DIMS 6
+#define GBO_MAX_NS_STEPS 64
+
+/* cudaStream_t-compatible handle, so this header needs no CUDA header. */
+typedef struct CUstream_st *gbo_stream_t;
+
+/* Opaque plan: validated descriptor table, the expansion of every view into
+ * independent matrices, their batching by shape, and the device tables. */
+typedef struct gbo_plan gbo_plan;
+
+/*
+ * One Muon weight.  The view and split rules follow "build_parameter_groups"
+ * (kimi-k3 docs), section "Recording independent matrix geometry": every
+ * view entry is a positive integer; the product of all view entries but the
+ * last equals `rows` and the last equals `cols`.  The view's second-to-last
+ * axis `r` is the row count of one block; split sizes (optional) cut each
+ * block's rows into consecutive ranges and must sum to `r`.  Each range is
+ * one independent matrix (worked shapes on that page: (32,8) viewed
+ * (2,16,8) is two 16x8 matrices; (20,8) viewed (2,10,8) split (4,6) is
+ * 4x8, 6x8, 4x8, 6x8).
+ */
+typedef struct {
+  void *w;        /* device: weight, rows x cols, w_dtype; updated in place            */
+  const void *g;  /* device: gradient, rows x cols, g_dtype; read only.  NULL skips the
+                     weight (inactive expert): w, mom, row_v are left untouched       */
+  float *mom;     /* device: fp32 momentum buffer rows x cols, updated in place; start it
+                     at zero                                                           */
+  float *row_v;   /* device: NorMuon row second moment, `rows` fp32 (start at zero), or
+                     NULL when NorMuon is off                                          */
+  int64_t rows;   /* stored rows (out features), >= 1                                 */
+  int64_t cols;   /* stored cols (in features), >= 1                                  */
+  int64_t view[GBO_MAX_VIEW_DIMS]; /* first view_ndim entries used                    */
+  int32_t w_dtype;   /* GBO_F32 | GBO_BF16                                             */
+  int32_t g_dtype;   /* GBO_F32 | GBO_BF16                                             */
+  int32_t view_ndim; /* 0: plain rows x cols matrix; else 2..GBO_MAX_VIEW_DIMS         */
+  int32_t n_split;   /* 0: no split; else the count of split sizes in the shared pool  */
+  int32_t split_off; /* index of this weight's first split size in split_pool          */
+  float lr_mult;     /* per-weight learning-rate multiplier (1.0 for the plain recipe) */
+  float wd;          /* decoupled weight decay (0.0 in the OMN recipe)                 */
+  int32_t reserved;  /* set to 0                                                       */
+} gbo_muon_desc;
+
+/*
+ * Muon options.  Momentum and Nesterov direction: NorMuon paper (zskr.cn),
+ * section 2.2, eq. (1); OMN page, Muon path (coefficient 0.95).  Iterations:
+ * eq. (5) of the same section,
+ *   X <- a X + b (X X^T) X + c (X X^T)^2 X,
+ * whose (a, b, c) = (1.5, -0.5, 0) case is the cubic of the "MuonClip
+ * Optimizer" page.  NorMuon rows: NorMuon paper, section 3.1.
+ */
+typedef struct {
+  const float *abc;      /* host: (a,b,c) triples, 1 triple or ns_steps triples; copied */
+  float mu;              /* momentum coefficient, e.g. 0.95                            */
+  float beta2;           /* NorMuon second-moment decay (e.g. 0.95)                     */
+  float eps;             /* NorMuon epsilon, added outside the square root (1e-8)      */
+  int32_t nesterov;      /* 1: D = G + mu*B (after B = mu*B + G); 0: D = B              */
+  int32_t ns_steps;      /* number of iterations k, 1..GBO_MAX_NS_STEPS (5)             */
+  int32_t abc_per_step;  /* 0: one shared triple; 1: one triple per iteration           */
+  int32_t precision;     /* GBO_NS_BF16 | GBO_NS_F32                                    */
+  int32_t normuon;       /* 1: NorMuon row normalisation; every desc needs row_v        */
+  int32_t reserved;      /* set to 0                                                    */
+} gbo_muon_opts;
+
+/*
+ * Validate a Muon descriptor table and build a plan (host memory only; the
+ * device tables are uploaded by the first gbo_muon_step on a device, which
+ * should therefore come before any stream capture).
+ *   descs[n]            host array; pointers inside are remembered by the plan
+ *   split_pool[pool_len] host array of split sizes, indexed by split_off
+ *   opts                host; abc is copied
+ *   out                 receives the plan; destroy it with gbo_muon_plan_destroy
+ * Errors: INVALID_ARG (NULL table/out, missing mom, row_v missing with
+ * normuon, bad ns_steps/precision/mu, misaligned pointers), SHAPE (a view
+ * or split rule broken, or a matrix side above 2^31-1), CONFLICT (the same w
+ * twice), EMPTY (n == 0), DTYPE.
+ */
+int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *split_pool,
+                         int32_t pool_len, const gbo_muon_opts *opts, gbo_plan **out);
+
+/* Release a plan and its device tables.  NULL is accepted. */
+void gbo_muon_plan_destroy(gbo_plan *plan);
+
+/* Bytes of device workspace gbo_muon_step needs for this plan (>= 0). */
+size_t gbo_muon_workspace_bytes(const gbo_plan *plan);
+
+/*
+ * 64-bit FNV-1a hash of what the plan computes: shapes, views, splits,
+ * dtypes and options, not pointers.  A checkpoint stores it and a resume
+ * with a different layout is refused by comparing it ("build_parameter_groups":
+ * names and shapes take part in checkpoint compatibility).  0 for NULL.
+ */
+uint64_t gbo_desc_hash(const gbo_plan *plan);
+
+/*
+ * One Muon step for every weight of the plan whose g is not NULL
+ * (OMN page, Muon path order):
+ *   B <- mu B + G;  D = G + mu B;
+ *   per matrix: X0 = Y / (||Y||_F + 1e-7), Y = D / max(max|D|, 1e-7);
+ *               transpose if rows > cols; k iterations of eq. (5); restore;
+ *               O scaled by sqrt(max(1, rows/cols)) of that matrix;
+ *               (NorMuon) v_i <- beta2 v_i + (1-beta2) mean_j O_ij^2,
+ *                         O_ij <- O_ij / (sqrt(v_i) + eps), before the scale;
+ *   W <- W - lr*lr_mult*(wd*W + scale*O), rounded once to w_dtype.
+ *   lr          the step's learning rate (host scalar)
+ *   workspace   device, >= gbo_muon_workspace_bytes(plan) bytes, 256-byte
+ *               aligned; contents need no initialisation and are scratch
+ *               after the call
+ *   dbg_update  device fp32, NULL or sum(rows*cols) over the plan's weights in
+ *               table order: receives scale*O (the update before lr) for
+ *               every updated weight; untouched for skipped ones
+ *   dev_status  device int32 or NULL (GBO_STATUS_* bits OR-ed in)
+ * Errors: INVALID_ARG, WORKSPACE, UNSUPPORTED (device is not sm_103),
+ * CUDA.
+ */
+int gbo_muon_step(gbo_plan *plan, float lr, void *workspace, size_t ws_bytes, float *dbg_update,
+                  int32_t *dev_status, gbo_stream_t stream);
+
+/*
+ * NorMuon row normalisation and weight write for one matrix (NorMuon paper,
+ * section 3.1), callable on its own.  O is the unscaled orthogonalised
+ * update, fp32 rows x cols row-major (device, read only).  For every row i:
+ *   v_i <- beta2 v_i + (1-beta2) * mean_j O_ij^2
+ *   U_ij = scale * O_ij / (sqrt(v_i) + eps)
+ *   W_ij <- W_ij - lr * (wd * W_ij + U_ij)      (rounded once to w_dtype)
+ * row_v: device fp32[rows], updated in place.  dbg_update: NULL or device
+ * fp32 rows x cols receiving U.  Errors: INVALID_ARG, DTYPE, CUDA.
+ */
+int gbo_normuon_rownorm(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
+                        int32_t w_dtype, float beta2, float eps, float scale, float lr, float wd,
+                        float *dbg_update, gbo_stream_t stream);
+
+/* ---- AdamW path ---------------------------------------------------------- */
+
+/* One gradient tensor for the clip norm. */
+typedef struct {
+  const void *ptr; /* device, numel elements of dtype, contiguous */
+  int64_t numel;   /* >= 0                                        */
+  int32_t dtype;   /* GBO_F32 | GBO_BF16                          */
+  int32_t reserved;
+} gbo_tensor;
+
+/* Bytes of device scratch gbo_clip_norm needs (a constant of this build). */
+size_t gbo_clip_norm_workspace_bytes(void);
+
+/*
+ * Global gradient norm over the given (AdamW) gradients and the clip
+ * coefficient (OMN page: clipping at 1.0 on AdamW parameters only; the
+ * Muon path is never clipped).
+ *   N = sqrt(sum of g^2 over all tensors);  coef = N > max_norm ? max_norm/N : 1
+ *   dev_total_norm, dev_coef   device fp32 scalars, written (either may be NULL)
+ *   workspace                  device scratch, >= gbo_clip_norm_workspace_bytes()
+ *                              bytes, 16-byte aligned
+ * A non-finite N gives coef = NaN and sets GBO_STATUS_NONFINITE.
+ * The gradients are not modified: gbo_adamw_step applies coef.
+ * Errors: INVALID_ARG, DTYPE, WORKSPACE, CUDA.  n == 0 writes N = 0, coef = 1.
+ */
+int gbo_clip_norm(const gbo_tensor *grads, int32_t n, float max_norm, float *dev_total_norm,
+                  float *dev_coef, int32_t *dev_status, void *workspace, size_t ws_bytes,
+                  gbo_stream_t stream);
+
+/* One AdamW parameter with its state; all fp32 except g (fp32 or bf16). */
+typedef struct {
+  float *p;       /* device, numel, updated in place */
+  const void *g;  /* device, numel, read only        */
+  float *m;       /* device, numel, first moment     */
+  float *v;       /* device, numel, second moment    */
+  int64_t numel;  /* >= 0                            */
+  int32_t g_dtype; /* GBO_F32 | GBO_BF16             */
+  int32_t reserved;
+} gbo_adamw_desc;
+
+/* AdamW hyper-parameters (OMN page: betas (0.9, 0.95), eps 1e-8, zero decay). */
+typedef struct {
+  float lr;
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+  int32_t step; /* t >= 1: the step being taken, for bias correction */
+} gbo_adamw_opts;
+
+/*
+ * Bias-corrected AdamW with decoupled decay (Qwen3.8 optimizer notes: Adam
+ * moments with bias correction, AdamW's decay on the weight), elementwise:
+ *   g' = coef * g;  m <- b1 m + (1-b1) g';  v <- b2 v + (1-b2) g'^2
+ *   p <- p - lr*wd*p - lr * (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps)
+ *   dev_coef  device fp32 scalar (e.g. gbo_clip_norm's output) or NULL for 1
+ * descs is a host array read during the call.  Errors: INVALID_ARG, DTYPE,
+ * CUDA.
+ */
+int gbo_adamw_step(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *opts,
+                   const float *dev_coef, int32_t *dev_status, gbo_stream_t stream);
+
+/* ---- diagnostics ---------------------------------------------------------- */
+
+/* Message for the last non-zero return on this host thread ("" if none). */
+const char *gbo_last_error(void);
+
+/* GBO_ABI_VERSION of the built library. */
+int32_t gbo_abi_version(void);
+
+/* sizeof of an ABI struct, for binding checks: 0 gbo_muon_desc,
+ * 1 gbo_muon_opts, 2 gbo_tensor, 3 gbo_adamw_desc, 4 gbo_adamw_opts,
+ * 5 gbo_plan_info; 0 for other values. */
+size_t gbo_struct_size(int32_t which);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t gbo_launch_count(void);
+
+/* What a plan holds, for reporting. */
+typedef struct {
+  int64_t n_weights;       /* descriptors in the table                          */
+  int64_t n_active;        /* descriptors with a gradient                       */
+  int64_t n_matrices;      /* independent matrices of the active weights        */
+  int64_t n_shape_classes; /* distinct oriented (p, q) shapes                   */
+  int64_t muon_params;     /* elements of the active weights                    */
+  double ns_flops;         /* dense-count Newton-Schulz FLOPs per step          */
+  double ns_flops_executed;/* FLOPs the kernels execute (same unless symmetric) */
+  int64_t launches_per_step; /* kernels one gbo_muon_step launches              */
+} gbo_plan_info;
+
+int gbo_muon_plan_info(const gbo_plan *plan, gbo_plan_info *out);
+
+/*
+ * Phase timing.  When enabled, gbo_muon_step records CUDA events around its
+ * phases on its stream.  gbo_muon_plan_phase_times synchronises on the last
+ * recorded event, adds the elapsed milliseconds of every step since the last
+ * reset into ms[phase] and the number of kernel launches into
+ * launches[phase], then resets.  Phases: 0 momentum (+ the norm reduction),
+ * 1 Newton-Schulz Gram products, 2 Newton-Schulz products back onto X (the
+ * last one writes the weights unless NorMuon is on), 3 Gram squares (c != 0),
+ * 4 NorMuon rows and weight write.  n_phases is the array length (<= 8).
+ */
+#define GBO_N_PHASES 5
+int gbo_muon_plan_set_timing(gbo_plan *plan, int32_t enable);
+int gbo_muon_plan_phase_times(gbo_plan *plan, float *ms, int64_t *launches, int32_t n_phases);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBO_H */

@@ -1,0 +1,192 @@
+"""The C-ABI library builds, loads, exports every declared symbol, and its
+host-side plan logic (validation, view expansion, workspace sizing, layout
+hash) behaves as documented.  No GPU needed: plan creation touches no
+device, and the fake addresses below are never dereferenced."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from adamw_optimizer_step_gb300 import _binding as B
+from adamw_optimizer_step_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return B.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(gbo_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert "gbo_muon_step" in names and "gbo_adamw_step" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert B.gbo_abi_version() == 1
+    for i, S in enumerate(B._STRUCTS):
+        assert B.gbo_struct_size(i) == ctypes.sizeof(S)
+
+
+FAKE = 1 << 20  # aligned fake device addresses; plan creation never dereferences them
+
+
+def desc(i, rows, cols, view=None, split_off=0, n_split=0, w_dtype=B.GBO_BF16, g=True, row_v=False):
+    d = B.MuonDesc()
+    base = FAKE * (4 * i + 1)
+    d.w = base
+    d.g = base + FAKE if g else None
+    d.mom = base + 2 * FAKE
+    d.row_v = base + 3 * FAKE if row_v else None
+    d.rows, d.cols = rows, cols
+    d.w_dtype = w_dtype
+    d.g_dtype = w_dtype
+    if view:
+        d.view_ndim = len(view)
+        for k, s in enumerate(view):
+            d.view[k] = s
+    d.n_split = n_split
+    d.split_off = split_off
+    d.lr_mult = 1.0
+    return d
+
+
+def create(L, descs, pool=(), ns_steps=5, abc=(1.5, -0.5, 0.0), precision=B.GBO_NS_BF16, normuon=0):
+    arr = (B.MuonDesc * max(1, len(descs)))(*descs)
+    cabc = (ctypes.c_float * len(abc))(*abc)
+    opts = B.MuonOpts(ctypes.cast(cabc, ctypes.POINTER(ctypes.c_float)), 0.95, 0.95, 1e-8, 1, ns_steps,
+                      int(len(abc) > 3), precision, normuon, 0)
+    cpool = (ctypes.c_int64 * max(1, len(pool)))(*pool)
+    out = ctypes.c_void_p()
+    rc = L.gbo_muon_plan_create(arr, len(descs), cpool, len(pool), ctypes.byref(opts), ctypes.byref(out))
+    return rc, out.value
+
+
+def info(L, plan):
+    i = B.PlanInfo()
+    assert L.gbo_muon_plan_info(plan, ctypes.byref(i)) == 0
+    return i
+
+
+def test_page_views_expand(L):
+    """The worked view shapes of the build_parameter_groups page."""
+    descs = [desc(0, 32, 8, (2, 16, 8)), desc(1, 24, 8, (3, 2, 4, 8)), desc(2, 20, 8, (2, 10, 8), 0, 2)]
+    rc, plan = create(L, descs, pool=(4, 6))
+    assert rc == 0, L.gbo_last_error()
+    i = info(L, plan)
+    assert (i.n_weights, i.n_active, i.n_matrices) == (3, 3, 2 + 6 + 4)
+    # oriented shapes: (16,8)->(8,16); (4,8); (6,8)
+    assert i.n_shape_classes == 3
+    assert i.muon_params == 32 * 8 + 24 * 8 + 20 * 8
+    assert L.gbo_muon_workspace_bytes(plan) > 0
+    L.gbo_muon_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("case,code", [
+    (dict(rows=32, cols=8, view=(2, 15, 8)), -2),
+    (dict(rows=32, cols=8, view=(2, 16, 4)), -2),
+    (dict(rows=32, cols=8, view=(0, 16, 8)), -2),
+    (dict(rows=20, cols=8, view=(2, 10, 8), split=(4, 5)), -2),
+    (dict(rows=20, cols=8, view=(2, 10, 8), split=(10, 0)), -2),
+    (dict(rows=0, cols=8), -2),
+    (dict(rows=20, cols=8, view=(160,)), -2),
+])
+def test_view_rules_refused(L, case, code):
+    split = case.get("split")
+    d = desc(0, case["rows"], case["cols"], case.get("view"), 0, len(split) if split else 0)
+    rc, plan = create(L, [d], pool=split or ())
+    assert rc == code, L.gbo_last_error()
+    assert plan is None
+    assert L.gbo_last_error()
+
+
+def test_other_refusals(L):
+    # empty table
+    rc, _ = create(L, [])
+    assert rc == -4
+    # the same weight twice
+    d0 = desc(0, 8, 8)
+    d1 = desc(1, 8, 8)
+    d1.w = d0.w
+    rc, _ = create(L, [d0, d1])
+    assert rc == -3
+    # bad dtype
+    d = desc(0, 8, 8)
+    d.w_dtype = 7
+    assert create(L, [d])[0] == -5
+    # NorMuon without row_v
+    assert create(L, [desc(0, 8, 8)], normuon=1)[0] == -1
+    # ns_steps out of range, NaN coefficient
+    assert create(L, [desc(0, 8, 8)], ns_steps=0)[0] == -1
+    assert create(L, [desc(0, 8, 8)], abc=(float("nan"), 0.0, 0.0))[0] == -1
+    # misaligned weight pointer for bf16
+    d = desc(0, 8, 8)
+    d.w += 1
+    assert create(L, [d])[0] == -1
+    # split sizes outside the pool
+    assert create(L, [desc(0, 20, 8, (2, 10, 8), 1, 2)], pool=(4, 6))[0] == -1
+
+
+def test_missing_gradient_skips(L):
+    rc, plan = create(L, [desc(0, 16, 16), desc(1, 32, 16, g=False)])
+    assert rc == 0
+    i = info(L, plan)
+    assert (i.n_weights, i.n_active, i.n_matrices, i.muon_params) == (2, 1, 1, 256)
+    L.gbo_muon_plan_destroy(plan)
+
+
+def test_flop_count_and_launches(L):
+    rc, plan = create(L, [desc(0, 5632 * 2, 2048, (2, 5632, 2048)), desc(1, 2048, 5632)])
+    assert rc == 0
+    i = info(L, plan)
+    assert i.n_matrices == 3 and i.n_shape_classes == 1
+    assert i.ns_flops == 3 * 5 * 4 * 2048 ** 2 * 5632
+    # momentum + finalize + 5 x (Gram + product)
+    assert i.launches_per_step == 12
+    L.gbo_muon_plan_destroy(plan)
+    rc, plan = create(L, [desc(0, 64, 64)], abc=(15 / 8, -5 / 4, 3 / 8))
+    assert info(L, plan).launches_per_step == 2 + 5 * 3
+    L.gbo_muon_plan_destroy(plan)
+
+
+def test_layout_hash(L):
+    """Equal layouts hash equal whatever the pointers; a different view or
+    split changes the hash (the checkpoint compatibility check)."""
+    _, p1 = create(L, [desc(0, 20, 8, (2, 10, 8), 0, 2)], pool=(4, 6))
+    d = desc(5, 20, 8, (2, 10, 8), 0, 2)
+    _, p2 = create(L, [d], pool=(4, 6))
+    _, p3 = create(L, [desc(0, 20, 8, (2, 10, 8), 0, 2)], pool=(6, 4))
+    _, p4 = create(L, [desc(0, 20, 8)])
+    h = [L.gbo_desc_hash(p) for p in (p1, p2, p3, p4)]
+    assert h[0] == h[1] and h[0] != h[2] and h[0] != h[3] and h[0] != 0
+    for p in (p1, p2, p3, p4):
+        L.gbo_muon_plan_destroy(p)
+    assert L.gbo_desc_hash(None) == 0
+
+
+def test_step_without_device_reports_error(L):
+    """On a host without a GPU a step fails with a status, never silently."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host has a GPU")
+    _, plan = create(L, [desc(0, 8, 8)])
+    rc = L.gbo_muon_step(plan, 0.02, FAKE, L.gbo_muon_workspace_bytes(plan), None, None, None)
+    assert rc in (-7, -8)
+    L.gbo_muon_plan_destroy(plan)
+    # workspace too small is reported before any device call
+    _, plan = create(L, [desc(0, 8, 8)])
+    assert L.gbo_muon_step(plan, 0.02, FAKE, 16, None, None, None) == -6
+    L.gbo_muon_plan_destroy(plan)

@@ -1,0 +1,253 @@
+"""GPU parity of the Muon path against the fp64 oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from adamw_optimizer_step_gb300 import _binding as B
+from adamw_optimizer_step_gb300 import workloads as wk
+from tests.parity import (TOL, check_muon, f64, random_entries, rel_fro, run_muon_gpu,
+                          run_muon_oracle)
+from oracle.views import sub_matrices
+
+pytestmark = pytest.mark.gpu
+
+CUBIC = (1.5, -0.5, 0.0)
+QUINTIC = (15.0 / 8.0, -5.0 / 4.0, 3.0 / 8.0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from adamw_optimizer_step_gb300 import build
+    build.build()
+    B.lib()
+
+
+def tiny_entries():
+    wl = wk.workload(1)
+    out = []
+    for i, t in enumerate(wl.muon):
+        W, G, Bm, v = wk.muon_tensor_inputs(wl, i)
+        out.append(dict(w=W, g=G, mom=Bm, row_v=v, view=t.view, split=t.split))
+    return out, wl
+
+
+@pytest.mark.parametrize("precision", ["f32", "bf16"])
+def test_tiny_views(precision):
+    """The tiny fp32 set of the pages' worked views, four 64x64 and two
+    64x128 matrices: one step, every matrix checked."""
+    entries, wl = tiny_entries()
+    gpu, status, _ = run_muon_gpu(entries, lr=wl.lr, precision=precision)
+    ora = run_muon_oracle(entries, lr=wl.lr)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=wl.lr, precision=precision)
+
+
+RAGGED = [
+    (300, 700, None, None),
+    (700, 300, None, None),
+    (129, 257, None, None),
+    (257, 129, None, None),
+    (1, 300, None, None),
+    (300, 1, None, None),
+    (1000, 64, (4, 250, 64), None),
+    (640, 192, (2, 5, 64, 192), (20, 44)),
+    (520, 136, (2, 260, 136), (100, 160), 0.5, 0.1),
+]
+
+
+@pytest.mark.parametrize("precision", ["f32", "bf16"])
+@pytest.mark.parametrize("wdt", [torch.bfloat16, torch.float32])
+def test_ragged_multi_tile(precision, wdt):
+    """Shapes spanning several GEMM and momentum tiles with ragged tails,
+    both orientations, degenerate 1 x n / m x 1, views with splits."""
+    entries = random_entries(RAGGED, seed=11, w_dtype=wdt, g_dtype=wdt, b_std=1e-3)
+    gpu, status, _ = run_muon_gpu(entries, lr=0.02, precision=precision)
+    ora = run_muon_oracle(entries, lr=0.02)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=0.02, precision=precision)
+
+
+@pytest.mark.parametrize("precision", ["f32", "bf16"])
+@pytest.mark.parametrize("opts", [
+    dict(abc=QUINTIC),
+    dict(abc=CUBIC + QUINTIC + (2.0, -1.5, 0.5) + CUBIC + (1.2, -0.3, 0.1)),
+    dict(abc=CUBIC, ns_steps=1),
+    dict(abc=CUBIC, ns_steps=8),
+    dict(abc=CUBIC, nesterov=False),
+    dict(abc=CUBIC, mu=0.8),
+])
+def test_coefficients_and_options(precision, opts):
+    shapes = [(200, 72, None, None), (72, 200, None, None), (96, 96, None, None, 2.0, 0.05)]
+    entries = random_entries(shapes, seed=12, b_std=1e-3)
+    kw = dict(opts)
+    gpu, status, _ = run_muon_gpu(entries, lr=0.05, precision=precision, **kw)
+    ora = run_muon_oracle(entries, lr=0.05, **kw)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=0.05, precision=precision, mu=kw.get("mu", 0.95))
+
+
+@pytest.mark.parametrize("precision", ["f32", "bf16"])
+def test_normuon_rows(precision):
+    shapes = [(300, 130, None, None), (130, 300, None, None), (64, 64, None, None),
+              (200, 40, (2, 100, 40), (30, 70))]
+    entries = random_entries(shapes, seed=13, normuon=True, b_std=1e-3)
+    gpu, status, _ = run_muon_gpu(entries, lr=0.02, precision=precision, normuon=True, beta2=0.95, eps=1e-8)
+    ora = run_muon_oracle(entries, lr=0.02, normuon=True, beta2=0.95, eps=1e-8)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=0.02, precision=precision)
+
+
+def test_skip_zero_and_nonfinite():
+    shapes = [(64, 96, None, None), (48, 48, None, None, 1.0, 0.1), (32, 32, None, None)]
+    entries = random_entries(shapes, seed=14, b_std=0.0)
+    entries[0]["g"] = None                        # inactive: untouched
+    entries[1]["g"] = torch.zeros_like(entries[1]["g"])  # zero direction: pure decay
+    gpu, status, _ = run_muon_gpu(entries, lr=0.1, precision="bf16")
+    assert status == 0
+    assert torch.equal(gpu[0]["W"], entries[0]["w"]) and torch.equal(gpu[0]["B"], entries[0]["mom"])
+    assert torch.count_nonzero(gpu[1]["U"]) == 0
+    want = (entries[1]["w"].double() * (1 - 0.1 * 0.1)).to(torch.bfloat16)
+    assert torch.equal(gpu[1]["W"], want)
+    # a NaN gradient is reported in the status word
+    bad = random_entries([(32, 32, None, None)], seed=15)
+    bad[0]["g"][3, 4] = float("nan")
+    _, status, _ = run_muon_gpu(bad, lr=0.1, precision="bf16")
+    assert status & B.GBO_STATUS_NONFINITE
+
+
+@pytest.mark.parametrize("precision", ["f32", "bf16"])
+def test_deterministic(precision):
+    entries = random_entries([(384, 260, None, None), (260, 384, None, None)], seed=16, b_std=1e-3)
+    a, _, _ = run_muon_gpu(entries, lr=0.02, precision=precision)
+    b, _, _ = run_muon_gpu(entries, lr=0.02, precision=precision)
+    for x, y in zip(a, b):
+        assert torch.equal(x["W"], y["W"]) and torch.equal(x["B"], y["B"]) and torch.equal(x["U"], y["U"])
+
+
+def test_checkpoint_resume_bitwise():
+    """Five steps straight equal three steps, a save/reload of weights and
+    state into fresh buffers and a new plan, then two more steps."""
+    entries = random_entries([(256, 160, None, None), (160, 256, (2, 80, 256), (30, 50))], seed=17,
+                             normuon=True)
+    straight, _, p1 = run_muon_gpu(entries, lr=0.02, precision="bf16", steps=5, normuon=True)
+    mid, _, p2 = run_muon_gpu(entries, lr=0.02, precision="bf16", steps=3, normuon=True)
+    resumed = []
+    for e, m in zip(entries, mid):
+        d = dict(e)
+        d.update(w=m["W"].clone(), mom=m["B"].clone(), row_v=m["v"].clone())
+        resumed.append(d)
+    end, _, p3 = run_muon_gpu(resumed, lr=0.02, precision="bf16", steps=2, normuon=True)
+    assert B.gbo_desc_hash(p1) == B.gbo_desc_hash(p3)
+    for s, r in zip(straight, end):
+        assert torch.equal(s["W"], r["W"]) and torch.equal(s["B"], r["B"]) and torch.equal(s["v"], r["v"])
+
+
+def test_layer_d2048_full_size():
+    """One d=2048 layer (Q, K, V, O 2048^2, gate_up (2, 5632, 2048), down
+    2048 x 5632): step 1 checked on every matrix; ten consecutive steps run
+    with the same gradients, the tenth checked on the gate matrix."""
+    wl = wk.workload(2)
+    entries = []
+    for i, t in enumerate(wl.muon):
+        W, G, Bm, v = wk.muon_tensor_inputs(wl, i)
+        entries.append(dict(w=W, g=G, mom=Bm, view=t.view, split=t.split))
+    gpu, status, _ = run_muon_gpu(entries, lr=wl.lr, precision="bf16")
+    assert status == 0
+    ora = run_muon_oracle(entries, lr=wl.lr)
+    worst = check_muon(entries, gpu, ora, lr=wl.lr, precision="bf16")
+    print("layer d2048 worst rel Frobenius error", worst)
+    ten, status, _ = run_muon_gpu(entries, lr=wl.lr, precision="bf16", steps=10)
+    assert status == 0
+    e = entries[4]
+    G = f64(e["g"])
+    Bm = np.zeros_like(G)
+    for _ in range(10):
+        Bm = oracle.momentum_update(Bm, G, 0.95)
+    D = oracle.nesterov_direction(G, Bm, 0.95)
+    O = oracle.orthogonalize(D[:5632], [CUBIC] * 5) * oracle.rect_scale(5632, 2048)
+    assert rel_fro(f64(ten[4]["U"])[:5632], O) <= TOL["bf16"]
+    assert np.max(np.abs(f64(ten[4]["B"]) - Bm)) <= 1e-6 * np.max(np.abs(Bm))
+
+
+def _sampled_large(idx, n_random=2, normuon=False):
+    """Full-size workload generated on the device; every distinct matrix
+    shape plus a few seeded random matrices are compared to the oracle."""
+    wl = wk.workload(idx)
+    dev = []
+    for i, t in enumerate(wl.muon):
+        W, G, Bm, v = wk.muon_tensor_inputs(wl, i, device="cuda")
+        dev.append(dict(w=W, g=G, mom=Bm, row_v=v, view=t.view, split=t.split))
+    originals = {}
+    shapes = {}
+    for i, t in enumerate(wl.muon):
+        for r0, m, n in sub_matrices(t.rows, t.cols, t.view, t.split):
+            shapes.setdefault((m, n), (i, r0))
+    rng = np.random.default_rng(1000 + idx)
+    picks = list(shapes.values())
+    for _ in range(n_random):
+        i = int(rng.integers(len(wl.muon)))
+        t = wl.muon[i]
+        subs = sub_matrices(t.rows, t.cols, t.view, t.split)
+        picks.append((i, subs[int(rng.integers(len(subs)))][0]))
+    for i, _ in picks:
+        if i not in originals:
+            e = dev[i]
+            originals[i] = dict(w=e["w"].cpu(), g=e["g"].cpu(), mom=e["mom"].cpu(),
+                                row_v=None if e["row_v"] is None else e["row_v"].cpu())
+    plan = B.gbo_muon_plan_create(dev, normuon=normuon)
+    ws = torch.empty(B.gbo_muon_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+    offs = np.cumsum([0] + [t.numel for t in wl.muon])
+    U = torch.empty(int(offs[-1]), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.gbo_muon_step(plan, wl.lr, ws, dbg_update=U, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i, r0 in picks:
+        t = wl.muon[i]
+        m = [s for s in sub_matrices(t.rows, t.cols, t.view, t.split) if s[0] == r0][0][1]
+        o = originals[i]
+        G = f64(o["g"])[r0:r0 + m]
+        Bn = oracle.momentum_update(f64(o["mom"])[r0:r0 + m], G, 0.95)
+        D = oracle.nesterov_direction(G, Bn, 0.95)
+        O = oracle.orthogonalize(D, [CUBIC] * 5)
+        if normuon:
+            O, _ = oracle.normuon_rows(O, f64(o["row_v"])[r0:r0 + m], 0.95, 1e-8)
+        O = O * oracle.rect_scale(m, t.cols)
+        Ug = U[int(offs[i]) + r0 * t.cols: int(offs[i]) + (r0 + m) * t.cols].view(m, t.cols).cpu().double().numpy()
+        err = rel_fro(Ug, O)
+        print("workload %d matrix %s rows %d+%d: rel err %.3e" % (idx, t.name, r0, m, err))
+        assert err <= TOL["bf16"]
+        Bg = dev[i]["mom"][r0:r0 + m].cpu().double().numpy()
+        assert np.all(np.abs(Bg - Bn) <= 1e-6 * (np.abs(G) + 1e-30))
+    del dev, ws, U
+    torch.cuda.empty_cache()
+
+
+def test_omn_shaped_sampled():
+    _sampled_large(3)
+
+
+def test_many_small_sampled():
+    _sampled_large(4, n_random=4)
+
+
+def test_normuon_7b_sampled():
+    _sampled_large(5, n_random=1, normuon=True)
+
+
+def test_standalone_rownorm():
+    gen = torch.Generator().manual_seed(21)
+    O = torch.randn(77, 300, generator=gen)
+    v = torch.rand(77, generator=gen) * 1e-2
+    W = (torch.randn(77, 300, generator=gen) * 0.02).to(torch.bfloat16)
+    Od, vd, Wd = O.cuda(), v.cuda(), W.cuda()
+    U = torch.empty(77, 300, device="cuda")
+    B.gbo_normuon_rownorm(Od, vd, Wd, beta2=0.95, eps=1e-8, scale=1.5, lr=0.02, wd=0.1, dbg_update=U)
+    torch.cuda.synchronize()
+    N, v_new = oracle.normuon_rows(f64(O), f64(v), 0.95, 1e-8)
+    assert np.max(np.abs(f64(vd) - v_new) / v_new) < 1e-5
+    assert rel_fro(f64(U), 1.5 * N) < 1e-5
+    want = f64(W) - 0.02 * (0.1 * f64(W) + f64(U))
+    assert np.max(np.abs(f64(Wd) - want)) <= 2 ** -7 * np.max(np.abs(want))
