@@ -31,11 +31,14 @@ WORKLOAD = 3
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=WORKLOAD,
+                    help="synthetic set: 3 = the 1.23B OMN-shaped set (the benchmark); 2 = one "
+                         "d=2048 layer, 4 = many small MLA/KDA matrices, 5 = 7B NorMuon (profiling)")
     return ap.parse_args()
 
 
@@ -73,7 +76,9 @@ def aggregate(steps, seconds_max, world):
 # clocks during the timed region
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (100 ms) kept only inside [t0, t1] of the host clock."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -88,11 +93,11 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0, t1):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -100,20 +105,28 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        import datetime
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if t0 <= ts <= t1:
                 rows.append(parts)
         os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
-        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed region"]}
+        num = lambda x: float(x) if x.replace(".", "", 1).isdigit() else None  # noqa: E731
+        sm = sorted(v for v in (num(r[1]) for r in rows) if v is not None)
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
-                "samples": len(rows)}
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
 
 
 # ---------------------------------------------------------------------------
@@ -215,6 +228,30 @@ def traffic_record(kernel_file):
     return rec
 
 
+def run_e2e(n_steps, world, g_flat, ag_flat, step, total):
+    """Steps/s with each step's gradients copied in from pinned host memory
+    (one transfer per flat gradient buffer) and the step's gradient norm read
+    back on the host.  Returns (steps/s over all ranks, bytes copied in per
+    step)."""
+    import torch
+    h_g = torch.empty(g_flat.numel(), dtype=g_flat.dtype, pin_memory=True)
+    h_ag = torch.empty(ag_flat.numel(), dtype=ag_flat.dtype, pin_memory=True)
+    h_g.copy_(g_flat)
+    h_ag.copy_(ag_flat)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(n_steps):
+        g_flat.copy_(h_g, non_blocking=True)
+        ag_flat.copy_(h_ag, non_blocking=True)
+        step()
+        _ = float(total.item())  # the step's result on the host
+    torch.cuda.synchronize()
+    e2e_t = max_over_ranks(time.perf_counter() - t0, world)
+    h2d = h_g.numel() * h_g.element_size() + h_ag.numel() * h_ag.element_size()
+    return aggregate(n_steps, e2e_t, world), h2d
+
+
 def run_ours(args):
     import torch
 
@@ -227,7 +264,7 @@ def run_ours(args):
     from adamw_optimizer_step_gb300 import workloads as wk
 
     gbo.lib()
-    wl = wk.workload(WORKLOAD)
+    wl = wk.workload(args.workload)
     dev = "cuda"
     # Muon gradients live in one flat buffer so the end-to-end run can copy
     # a step's gradients in with one transfer; likewise the AdamW gradients.
@@ -285,9 +322,11 @@ def run_ours(args):
     gbo.gbo_muon_plan_phase_times(plan)  # reset
     adam_ev = [(ev(), ev()) for _ in range(args.steps)]
     clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)  # let the sampler start
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
+    t_wall0 = time.time()
     l0 = gbo.gbo_launch_count()
     start, end = ev(), ev()
     start.record(stream)
@@ -297,7 +336,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     launches = gbo.gbo_launch_count() - l0
-    clk = clocks.stop()
+    clk = clocks.stop(t_wall0, time.time())
     phases = gbo.gbo_muon_plan_phase_times(plan)
     gbo.gbo_muon_plan_set_timing(plan, False)
     elapsed = start.elapsed_time(end) / 1e3
@@ -308,22 +347,9 @@ def run_ours(args):
         raise RuntimeError("device status %d during the timed steps" % int(status.item()))
 
     # end to end: gradients from pinned host memory, norm read back
-    h_g = torch.empty(n_muon, dtype=wl.g_dtype, pin_memory=True)
-    h_ag = torch.empty(n_adam, dtype=torch.float32, pin_memory=True)
-    h_g.copy_(g_flat)
-    h_ag.copy_(ag_flat)
-    e2e_steps = max(1, args.e2e_steps)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        g_flat.copy_(h_g, non_blocking=True)
-        ag_flat.copy_(h_ag, non_blocking=True)
-        step()
-        _ = float(total.item())  # the step's gradient norm, read on the host
-    torch.cuda.synchronize()
-    e2e_t = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = aggregate(e2e_steps, e2e_t, world)
+    e2e_value, h2d = None, 0
+    if args.e2e_steps > 0:
+        e2e_value, h2d = run_e2e(args.e2e_steps, world, g_flat, ag_flat, step, total)
 
     if rank != 0:
         return
@@ -370,9 +396,8 @@ def run_ours(args):
         "adamw_clip": {"ms": adam_ms, "GB/s": adam_bytes / (adam_ms / 1e3) / 1e9,
                        "frac_of_hbm": adam_bytes / (adam_ms / 1e3) / 1e9 / hbm},
         "ns_tflops": achieved_tf,
-        "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": int(h_g.numel() * h_g.element_size()
-                                                                               + h_ag.numel() * 4),
-                "d2h_bytes_per_step": 4},
+        "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "steps/s",
+                                               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4},
         "gpu_launches": int(launches),
         "clocks": clk,
         "cpu_baseline": cpu,
