@@ -98,6 +98,8 @@ def lib():
         "gbo_clip_norm_workspace_bytes": (c_size_t, []),
         "gbo_clip_norm": (c_int32, [ctypes.POINTER(Tensor), c_int32, c_float, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_size_t, c_void_p]),
+        "gbo_clip_norm_noalloc": (c_int32, [ctypes.POINTER(Tensor), c_int32, c_float, c_void_p, c_void_p,
+                                            c_void_p, c_void_p]),
         "gbo_adamw_step": (c_int32, [ctypes.POINTER(AdamWDesc), c_int32, ctypes.POINTER(AdamWOpts), c_void_p,
                                      c_void_p, c_void_p]),
         "gbo_last_error": (ctypes.c_char_p, []),
@@ -291,6 +293,19 @@ def gbo_clip_norm(grads, max_norm, total_norm, coef, workspace, dev_status=None,
     _check(lib().gbo_clip_norm(arr, len(grads), float(max_norm), _dev_ptr(total_norm, "total_norm"),
                                _dev_ptr(coef, "coef"), _dev_ptr(dev_status, "dev_status"),
                                _dev_ptr(workspace, "workspace"), nbytes, _stream(stream)))
+
+
+def gbo_clip_norm_noalloc(grads, max_norm, total_norm, coef, dev_status=None, stream=None):
+    """gbo_clip_norm without a workspace: the library's fixed device scratch
+    is used, so nothing is allocated (for callers that cannot allocate)."""
+    arr = (Tensor * max(1, len(grads)))()
+    for d, g in zip(arr, grads):
+        d.ptr = _dev_ptr(g, "grad")
+        d.numel = g.numel()
+        d.dtype = _dtype(g)
+    _check(lib().gbo_clip_norm_noalloc(arr, len(grads), float(max_norm), _dev_ptr(total_norm, "total_norm"),
+                                       _dev_ptr(coef, "coef"), _dev_ptr(dev_status, "dev_status"),
+                                       _stream(stream)))
 
 
 def gbo_adamw_step(params, *, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0, step=1,

@@ -105,6 +105,13 @@ int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseA
 
 void count_launches(uint64_t n);
 
+// Error and device helpers of the host code, for entry points that live in
+// other files: record a message for gbo_last_error, clear it, and check
+// that the current device is an sm_103 part (returns its SM count).
+int report_error(int code, const char *msg);
+int report_ok();
+int require_device(int *dev, int *sm_count);
+
 constexpr int kClipBlocks = 1024;  // partial sums of the clip norm
 
 }  // namespace gbo

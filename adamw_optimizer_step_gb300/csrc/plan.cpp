@@ -100,6 +100,18 @@ constexpr int kPhaseMomentum = 0, kPhaseGram = 1, kPhaseProduct = 2, kPhaseSquar
               kPhaseRows = 4;
 
 }  // namespace
+
+int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
+int report_ok() { return ok(); }
+
+int require_device(int *dev, int *sm_count) {
+  DeviceInfo di;
+  const int rc = current_device(dev, &di);
+  if (rc == GBO_OK) *sm_count = di.sm_count;
+  return rc;
+}
+
 }  // namespace gbo
 
 using namespace gbo;

@@ -222,6 +222,32 @@ int gbo_clip_norm(const gbo_tensor *grads, int32_t n, float max_norm, float *dev
                   float *dev_coef, int32_t *dev_status, void *workspace, size_t ws_bytes,
                   gbo_stream_t stream);
 
+/*
+ * gbo_clip_norm_noalloc -- the same norm and coefficient as gbo_clip_norm,
+ * for callers that cannot allocate device memory.  The source pages have no
+ * counterpart: this is an interface for callers, not part of the method.
+ *
+ * Some callers cannot provide scratch memory: all of the device's memory
+ * already belongs to another allocator (a training framework's caching pool
+ * that reserved HBM at start-up), or they run where a cudaMalloc, which can
+ * synchronise the device, is not allowed.  This entry point allocates
+ * nothing: its scratch (1024 fp32 partial sums, 4 KB) is a fixed array in
+ * the library's device memory, held by every GPU that loads the library
+ * until the process exits.
+ *   grads, n, max_norm, dev_total_norm, dev_coef, dev_status: as gbo_clip_norm
+ *   n           at most GBO_CLIP_NOALLOC_MAX_TENSORS tensors (any sizes);
+ *               more is refused with GBO_ERR_INVALID_ARG
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the one array, so calls whose work overlaps on the GPU race
+ * (use one stream, or order them); it keeps the last call's contents, and no
+ * slot needs clearing because each call writes every slot it reads.
+ * Errors: INVALID_ARG, DTYPE, UNSUPPORTED, CUDA.
+ */
+#define GBO_CLIP_NOALLOC_MAX_TENSORS 65536
+int gbo_clip_norm_noalloc(const gbo_tensor *grads, int32_t n, float max_norm, float *dev_total_norm,
+                          float *dev_coef, int32_t *dev_status, gbo_stream_t stream);
+
 /* One AdamW parameter with its state; all fp32 except g (fp32 or bf16). */
 typedef struct {
   float *p;       /* device, numel, updated in place */
