@@ -21,8 +21,8 @@ GBO_NS_F32 = 1
 GBO_STATUS_NONFINITE = 1
 GBO_STATUS_TIMEOUT = 2
 GBO_MAX_VIEW_DIMS = 6
-GBO_N_PHASES = 5
-PHASE_NAMES = ("momentum", "gram", "product", "square", "rows")
+GBO_N_PHASES = 6
+PHASE_NAMES = ("momentum", "gram", "product", "square", "rows", "final")
 
 c_void_p, c_int32, c_int64, c_float, c_size_t = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                                  ctypes.c_float, ctypes.c_size_t)

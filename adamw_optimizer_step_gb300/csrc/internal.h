@@ -35,12 +35,12 @@ struct DevSub {
   int32_t tiles_c;  // momentum tiles along n
   int32_t transposed;
   int32_t w_dtype, g_dtype;
-  int32_t vec_ok;   // rows start on 16-byte boundaries and n % 4 == 0
+  int32_t vec_ok;   // g and mom rows start on 16-byte boundaries (n % 8 == 0)
   int32_t cls;
   float scale;      // sqrt(max(1, m / n))
   float lr_mult;
   float wd;
-  int32_t pad;
+  int32_t w_vec;    // weight rows start on 16-byte boundaries (vector read-modify-write)
 };
 
 // Matrices of one oriented shape (p, q), stored back to back in the
@@ -102,6 +102,10 @@ int launch_adamw(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *o
 struct TcLaunch;
 int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args,
                       int sm_count, void *stream);
+// FLOPs the tensor-core kernel executes for one p x q matrix and one
+// iteration (Gram over the upper block-triangle of tiles, square when c != 0,
+// product), counting the zero padding of partial tiles.
+double tc_executed_flops(int p, int q, bool square);
 
 void count_launches(uint64_t n);
 

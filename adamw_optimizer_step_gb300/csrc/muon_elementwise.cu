@@ -25,80 +25,109 @@ namespace {
 
 constexpr int kMomThreads = 256;
 
-struct Load4 {
-  float v[4];
-};
-
-__device__ __forceinline__ Load4 load4(const void *base, int32_t dtype, int64_t idx, int valid,
-                                       bool vec) {
-  Load4 r;
-  if (vec && valid == 4) {
+// Eight consecutive elements of a row as fp32: one 16-byte load (bf16) or
+// two (fp32) when `vec`, else element by element under `valid`.
+__device__ __forceinline__ void load8(const void *base, int32_t dtype, int64_t idx, int valid, bool vec,
+                                      float *out) {
+  if (vec && valid == 8) {
     if (dtype == GBO_BF16) {
-      const uint2 raw = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + idx);
-      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
-      r.v[0] = __low2float(lo);
-      r.v[1] = __high2float(lo);
-      r.v[2] = __low2float(hi);
-      r.v[3] = __high2float(hi);
+      const uint4 raw = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + idx);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
+        out[2 * h] = __low2float(b);
+        out[2 * h + 1] = __high2float(b);
+      }
     } else {
-      const float4 f = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(base) + idx);
-      r.v[0] = f.x; r.v[1] = f.y; r.v[2] = f.z; r.v[3] = f.w;
+      const float4 *f = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(base) + idx);
+      const float4 a = f[0], b = f[1];
+      out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+      out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) r.v[e] = e < valid ? ld_elem(base, dtype, idx + e) : 0.f;
+    for (int e = 0; e < 8; ++e) out[e] = e < valid ? ld_elem(base, dtype, idx + e) : 0.f;
   }
-  return r;
+}
+
+// Eight consecutive elements: 16-byte store(s) when `vec` (the caller
+// guarantees alignment) and the segment is whole, else element by element.
+template <typename XT>
+__device__ __forceinline__ void store8(XT *dst, const float *v, int valid, bool vec) {
+  if (vec && valid == 8) {
+    if constexpr (sizeof(XT) == 2) {
+      uint4 u;
+      __nv_bfloat162 h[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+      u.x = *reinterpret_cast<uint32_t *>(&h[0]);
+      u.y = *reinterpret_cast<uint32_t *>(&h[1]);
+      u.z = *reinterpret_cast<uint32_t *>(&h[2]);
+      u.w = *reinterpret_cast<uint32_t *>(&h[3]);
+      *reinterpret_cast<uint4 *>(dst) = u;
+    } else {
+      float4 *f = reinterpret_cast<float4 *>(dst);
+      f[0] = make_float4(v[0], v[1], v[2], v[3]);
+      f[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < valid) {
+        if constexpr (sizeof(XT) == 2) dst[e] = __float2bfloat16_rn(v[e]);
+        else dst[e] = v[e];
+      }
+  }
 }
 
 // One 64 x 64 tile of one matrix per loop trip.  256 threads: thread t
-// covers columns 4*(t%16) .. +3 of rows t/16, t/16+16, t/16+32, t/16+48.
+// covers columns 8*(t%8) .. +7 of tile rows t/8 and t/8 + 32.  Every load
+// of the tile is issued before any arithmetic, so each thread keeps four
+// 16-byte requests in flight.
 template <typename XT>
 __global__ void __launch_bounds__(kMomThreads)
 momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles, float mu,
                 int32_t nesterov, XT *__restrict__ x0, float *__restrict__ partials) {
   __shared__ float tile[kMomTile][kMomTile + 1];
   __shared__ float red[32];
-  const int cg = threadIdx.x & 15;
-  const int rs = threadIdx.x >> 4;
+  const int cg = threadIdx.x & 7;
+  const int rr = threadIdx.x >> 3;
   for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const int si = find_owner(t, n_subs, [&](int k) { return subs[k].tile0; });
     const DevSub &S = subs[si];
     const int64_t lt = t - S.tile0;
     const int tr = (int)(lt / S.tiles_c), tc = (int)(lt % S.tiles_c);
     const int rb = tr * kMomTile, cb = tc * kMomTile;
-    const int j = cb + cg * 4;
-    const int valid = min(4, S.n - j);
+    const int j = cb + cg * 8;
+    const int valid = max(0, min(8, S.n - j));
     const bool vec = S.vec_ok != 0;
-    float d[16];
-    float lmax = 0.f;
+    float g[2][8], b[2][8];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int i = rb + it * 16 + rs;
+    for (int ps = 0; ps < 2; ++ps) {
+      const int i = rb + ps * 32 + rr;
       if (i < S.m && valid > 0) {
         const int64_t widx = (S.r0 + i) * S.cols + j;
-        const Load4 g = load4(S.g, S.g_dtype, widx, valid, vec);
-        const Load4 b = load4(S.mom, GBO_F32, widx, valid, vec);
-        float nb[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          nb[e] = mu * b.v[e] + g.v[e];
-          const float dd = nesterov ? g.v[e] + mu * nb[e] : nb[e];
-          d[it * 4 + e] = e < valid ? dd : 0.f;
-          lmax = fmaxf(lmax, fabsf(d[it * 4 + e]));
-        }
-        if (vec && valid == 4) {
-          *reinterpret_cast<float4 *>(S.mom + widx) = make_float4(nb[0], nb[1], nb[2], nb[3]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (e < valid) S.mom[widx + e] = nb[e];
-        }
+        load8(S.g, S.g_dtype, widx, valid, vec, g[ps]);
+        load8(S.mom, GBO_F32, widx, valid, vec, b[ps]);
       } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) d[it * 4 + e] = 0.f;
+        for (int e = 0; e < 8; ++e) g[ps][e] = b[ps][e] = 0.f;
       }
+    }
+    float d[2][8];
+    float lmax = 0.f;
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps) {
+      const int i = rb + ps * 32 + rr;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float nb = mu * b[ps][e] + g[ps][e];
+        b[ps][e] = nb;
+        d[ps][e] = nesterov ? g[ps][e] + mu * nb : nb;
+        lmax = fmaxf(lmax, fabsf(d[ps][e]));
+      }
+      if (i < S.m && valid > 0) store8(S.mom + (S.r0 + i) * S.cols + j, b[ps], valid, vec);
     }
     // Partials: the tile's max |D| and its sum of squares of D / max, so that
     // the per-matrix combination cannot overflow.
@@ -107,10 +136,12 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
     if (M > 0.f) {
       const float inv = 1.0f / M;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float y = d[k] * inv;
-        ss = fmaf(y, y, ss);
-      }
+      for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float y = d[ps][e] * inv;
+          ss = fmaf(y, y, ss);
+        }
     }
     ss = block_sum(ss, red);
     if (threadIdx.x == 0) {
@@ -120,41 +151,27 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
     XT *X = x0 + S.x_off;
     if (!S.transposed) {
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int i = rb + it * 16 + rs;
-        if (i < S.m) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (e < valid) {
-              if constexpr (sizeof(XT) == 2)
-                X[(int64_t)i * S.ld + j + e] = __float2bfloat16_rn(d[it * 4 + e]);
-              else
-                X[(int64_t)i * S.ld + j + e] = d[it * 4 + e];
-            }
-        }
+      for (int ps = 0; ps < 2; ++ps) {
+        const int i = rb + ps * 32 + rr;
+        if (i < S.m && valid > 0) store8(X + (int64_t)i * S.ld + j, d[ps], valid, true);
       }
     } else {
       // X = D^T: stage the tile, then write rows of X (columns of D).
 #pragma unroll
-      for (int it = 0; it < 4; ++it)
+      for (int ps = 0; ps < 2; ++ps)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) tile[it * 16 + rs][cg * 4 + e] = d[it * 4 + e];
+        for (int e = 0; e < 8; ++e) tile[ps * 32 + rr][cg * 8 + e] = d[ps][e];
       __syncthreads();
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int xr = cb + it * 16 + rs;  // row of X = column of D
-        if (xr < S.n) {
+      for (int ps = 0; ps < 2; ++ps) {
+        const int xr = cb + ps * 32 + rr;  // row of X = column of D
+        const int xc = rb + cg * 8;        // first column of X = row of D
+        const int xvalid = max(0, min(8, S.m - xc));
+        if (xr < S.n && xvalid > 0) {
+          float v[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int xc = rb + cg * 4 + e;  // column of X = row of D
-            if (xc < S.m) {
-              const float v = tile[cg * 4 + e][it * 16 + rs];
-              if constexpr (sizeof(XT) == 2)
-                X[(int64_t)xr * S.ld + xc] = __float2bfloat16_rn(v);
-              else
-                X[(int64_t)xr * S.ld + xc] = v;
-            }
-          }
+          for (int e = 0; e < 8; ++e) v[e] = tile[cg * 8 + e][ps * 32 + rr];
+          store8(X + (int64_t)xr * S.ld + xc, v, xvalid, true);
         }
       }
     }

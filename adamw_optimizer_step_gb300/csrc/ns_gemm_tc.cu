@@ -43,7 +43,8 @@ constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;                   // two 128 x 256 fp32 accumulators
-constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kStageFloats = 32 * 33;             // per epilogue warp: one 32 x 32 transpose
+constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + 4 * kStageFloats * 4;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
 struct TcParams {
@@ -56,6 +57,7 @@ struct TcParams {
   int32_t tiles_per_mat[kMaxClassesPerLaunch];
   int32_t n;
   int32_t b_mn_major;  // products: B = X with the K index along X's rows
+  int32_t tri;         // symmetric output: only tiles touching the upper triangle
 };
 
 // ---------------------------------------------------------------------------
@@ -184,6 +186,10 @@ struct TileCoord {
   int c, mat, tm, tn;
 };
 
+// First computed column tile of tile row tm in a symmetric launch: the
+// tile holds an element on or above the diagonal iff BN*tn + BN - 1 >= BM*tm.
+__host__ __device__ __forceinline__ int tri_tn_min(int tm) { return (tm * BM) / BN; }
+
 __device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
   TileCoord tc;
   int c = 0;
@@ -191,9 +197,21 @@ __device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
   const int64_t local = t - P.tile_start[c];
   tc.c = c;
   tc.mat = (int)(local / P.tiles_per_mat[c]);
-  const int rem = (int)(local % P.tiles_per_mat[c]);
-  tc.tm = rem / P.tiles_n[c];
-  tc.tn = rem % P.tiles_n[c];
+  int rem = (int)(local % P.tiles_per_mat[c]);
+  const int tn_all = P.tiles_n[c];
+  if (!P.tri) {
+    tc.tm = rem / tn_all;
+    tc.tn = rem % tn_all;
+  } else {
+    int tm = 0;
+    for (;; ++tm) {
+      const int cnt = max(0, tn_all - tri_tn_min(tm));
+      if (rem < cnt) break;
+      rem -= cnt;
+    }
+    tc.tm = tm;
+    tc.tn = tri_tn_min(tm) + rem;
+  }
   return tc;
 }
 
@@ -202,66 +220,181 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Epilogue of one 32-column chunk of one accumulator row.
-__device__ __forceinline__ void epilogue_chunk(const PhaseArgs &A, const DevSub &S, const EpiScalars &e,
-                                               int i, int col0, float (&v)[32]) {
-  if (A.mode == kFinal) {
-    if (i >= S.p) return;
+// 32 consecutive values of one row: vector store when the row segment is
+// whole and aligned, else element by element under the mask.
+template <typename T>
+__device__ __forceinline__ void store_row32(T *dst, const float (&o)[32], bool vec, uint32_t mask) {
+  if constexpr (sizeof(T) == 2) {
+    if (vec) {
+      uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        d[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                          pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+      return;
+    }
 #pragma unroll
     for (int k = 0; k < 32; ++k)
-      if (col0 + k < S.q) final_write(A, S, i, col0 + k, e.s * v[k]);
+      if (mask >> k & 1u) dst[k] = __float2bfloat16_rn(o[k]);
+  } else {
+    if (vec) {
+      float4 *d = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) d[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      return;
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (mask >> k & 1u) dst[k] = o[k];
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void load_row32(const T *src, float (&o)[32], bool vec, uint32_t mask) {
+  if constexpr (sizeof(T) == 2) {
+    if (vec) {
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = s4[q];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
+          o[8 * q + 2 * h] = __low2float(b);
+          o[8 * q + 2 * h + 1] = __high2float(b);
+        }
+      }
+      return;
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = (mask >> k & 1u) ? __bfloat162float(src[k]) : 0.f;
+  } else {
+    if (vec) {
+      const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 f = s4[q];
+        o[4 * q] = f.x; o[4 * q + 1] = f.y; o[4 * q + 2] = f.z; o[4 * q + 3] = f.w;
+      }
+      return;
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = (mask >> k & 1u) ? src[k] : 0.f;
+  }
+}
+
+__device__ __forceinline__ uint32_t prefix_mask(int n) {  // the low n bits, n in [0, 32]
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
+// Transpose a warp's 32 x 32 block through shared memory: on entry lane r
+// holds row r (o[k] = B[r][k]); on exit lane l holds column l
+// (o[r] = B[r][l]).  `st` is this warp's [32][33] staging area.
+__device__ __forceinline__ void warp_transpose32(float (&o)[32], float *st, int lane) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k) st[lane * 33 + k] = o[k];
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < 32; ++r) o[r] = st[r * 33 + lane];
+  __syncwarp();
+}
+
+// Weight write of 32 consecutive elements of one stored row: W[row][c0..c0+31]
+// with the update directions u[0..31] (valid under `mask`).
+template <typename WT>
+__device__ __forceinline__ void weight_rmw32(const PhaseArgs &A, const DevSub &S, int64_t row, int c0,
+                                             const float (&u)[32], uint32_t mask) {
+  const int64_t widx = row * S.cols + c0;
+  WT *w = reinterpret_cast<WT *>(S.w) + widx;
+  const bool vec = S.w_vec && mask == 0xffffffffu;
+  float wv[32];
+  load_row32(w, wv, vec, mask);
+  const float lr = A.lr * S.lr_mult;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) wv[k] = wv[k] - lr * (S.wd * wv[k] + u[k]);
+  store_row32(w, wv, vec, mask);
+  if (A.dbg) {
+    float *d = A.dbg + S.dbg_off + widx;
+    const bool dvec = mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0;
+    store_row32(d, u, dvec, mask);
+  }
+}
+
+// Epilogue of one warp's 32 rows x 32 columns of the accumulator.  Lane r
+// holds row i0 + r in v[0..31] (columns col0 .. col0 + 31).
+__device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const DevSub &S, const EpiScalars &e, int i0,
+                                               int col0, float (&v)[32], float *st, int lane) {
+  const int i = i0 + lane;
+  if (A.mode == kProduct) {
+    if (i >= S.p) return;
+    float o[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = e.s * v[k];
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(A.x_out) + S.x_off + (int64_t)i * S.ld + col0;
+    store_row32(dst, o, col0 + 32 <= S.q, prefix_mask(S.q - col0));
     return;
   }
-  const bool sq = (A.mode == kGram || A.mode == kGramA || A.mode == kSquare);
-  const int Ncols = sq ? S.p : S.q;
-  if (i >= S.p) return;
-  __nv_bfloat16 *out;
-  int64_t base;
-  if (A.mode == kProduct) {
-    out = reinterpret_cast<__nv_bfloat16 *>(A.x_out);
-    base = S.x_off + (int64_t)i * S.ld;
-  } else if (A.mode == kGramA) {
-    out = reinterpret_cast<__nv_bfloat16 *>(A.abuf);
-    base = S.p_off + (int64_t)i * S.ldp;
-  } else {
-    out = reinterpret_cast<__nv_bfloat16 *>(A.pbuf);
-    base = S.p_off + (int64_t)i * S.ldp;
+  if (A.mode == kFinal) {
+    // O = s * C; the update direction is scale * O
+    float u[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) u[k] = S.scale * e.s * v[k];
+    if (!S.transposed) {
+      if (i >= S.p) return;
+      const uint32_t mask = prefix_mask(S.q - col0);
+      if (S.w_dtype == GBO_BF16) weight_rmw32<__nv_bfloat16>(A, S, S.r0 + i, col0, u, mask);
+      else weight_rmw32<float>(A, S, S.r0 + i, col0, u, mask);
+    } else {
+      // stored row = column of X: after the transpose lane l holds stored
+      // row col0 + l, stored columns i0 .. i0 + 31
+      warp_transpose32(u, st, lane);
+      if (col0 + lane >= S.q) return;
+      const uint32_t mask = prefix_mask(S.p - i0);
+      if (S.w_dtype == GBO_BF16) weight_rmw32<__nv_bfloat16>(A, S, S.r0 + col0 + lane, i0, u, mask);
+      else weight_rmw32<float>(A, S, S.r0 + col0 + lane, i0, u, mask);
+    }
+    return;
   }
+  // Gram-type (symmetric) outputs: P = a I + b s^2 C, A = s^2 C, or
+  // P = a I + b A + c C.  Only tiles touching the upper triangle run; each
+  // element (r, c) with r <= c is written here and its mirror (c, r) with
+  // r < c is written from the transposed block, so every element of the
+  // symmetric output is written exactly once.
+  __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(A.mode == kGramA ? A.abuf : A.pbuf) + S.p_off;
+  const int p = S.p;
   float o[32];
   if (A.mode == kSquare) {
-    const __nv_bfloat16 *am = reinterpret_cast<const __nv_bfloat16 *>(A.abuf) + S.p_off + (int64_t)i * S.ldp;
+    float am[32];
+    const bool full = i < p && col0 + 32 <= p;
+    if (i < p)
+      load_row32(reinterpret_cast<const __nv_bfloat16 *>(A.abuf) + S.p_off + (int64_t)i * S.ldp + col0, am, full,
+                 prefix_mask(p - col0));
+    else
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int j = col0 + k;
-      const float av = j < Ncols ? __bfloat162float(am[j]) : 0.f;
-      o[k] = A.c * v[k] + A.b * av + (i == j ? A.a : 0.f);
-    }
+      for (int k = 0; k < 32; ++k) am[k] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = A.c * v[k] + A.b * am[k] + (i == col0 + k ? A.a : 0.f);
   } else if (A.mode == kGram) {
     const float bs2 = A.b * e.s2;
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = bs2 * v[k] + (i == col0 + k ? A.a : 0.f);
-  } else if (A.mode == kGramA) {
+  } else {
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = e.s2 * v[k];
-  } else {
-#pragma unroll
-    for (int k = 0; k < 32; ++k) o[k] = e.s * v[k];
   }
-  if (col0 + 32 <= Ncols) {
-    uint4 *dst = reinterpret_cast<uint4 *>(out + base + col0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w;
-      w.x = pack_bf16(o[8 * q + 0], o[8 * q + 1]);
-      w.y = pack_bf16(o[8 * q + 2], o[8 * q + 3]);
-      w.z = pack_bf16(o[8 * q + 4], o[8 * q + 5]);
-      w.w = pack_bf16(o[8 * q + 6], o[8 * q + 7]);
-      dst[q] = w;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      if (col0 + k < Ncols) out[base + col0 + k] = __float2bfloat16_rn(o[k]);
+  // direct: (i, j) with i <= j
+  if (i < p) {
+    const int jlo = max(i, col0);                 // first column to write
+    const uint32_t mask = prefix_mask(p - col0) & ~prefix_mask(jlo - col0);
+    store_row32(out + (int64_t)i * S.ldp + col0, o, mask == 0xffffffffu, mask);
+  }
+  // mirror: lane l writes row col0 + l, columns i0 + r for i0 + r < col0 + l
+  warp_transpose32(o, st, lane);
+  const int jm = col0 + lane;
+  if (jm < p) {
+    const uint32_t mask = prefix_mask(p - i0) & prefix_mask(jm - i0);
+    store_row32(out + (int64_t)jm * S.ldp + i0, o, mask == 0xffffffffu, mask);
   }
 }
 
@@ -273,6 +406,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   // bars: full[STAGES], empty[STAGES], accf[2], acce[2], drain
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
+  float *stage_base = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + 256);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
@@ -397,13 +531,18 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const int sub = P.sub0[tc.c] + tc.mat;
       const DevSub &S = A.subs[sub];
       const EpiScalars e = epi_scalars(A, sub);
-      const int i = tc.tm * BM + quarter * 32 + lane;
+      const int i0 = tc.tm * BM + quarter * 32;
+      float *st = stage_base + (warp - 2) * kStageFloats;
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      // skip column chunks that hold nothing this warp writes
+      const int ncols = (A.mode == kProduct || A.mode == kFinal) ? S.q : S.p;
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
+        const int col0 = tc.tn * BN + ch * 32;
+        if (col0 >= ncols) break;
         float v[32];
         tmem_ld32(trow + ch * 32, v);
-        epilogue_chunk(A, S, e, i, tc.tn * BN + ch * 32, v);
+        if (i0 < S.p) epilogue_block(A, S, e, i0, col0, v, st, lane);
       }
       tc_fence_before();
       mbar_arrive(acce0 + 8 * acc);
@@ -459,6 +598,20 @@ bool encode_map(CUtensorMap *map, void *base, int64_t cols, int64_t rows, int64_
 
 }  // namespace
 
+double tc_executed_flops(int p, int q, bool square) {
+  const int tiles_m = (p + BM - 1) / BM;
+  const int tiles_n_sym = (p + BN - 1) / BN;
+  int64_t sym_tiles = 0;
+  for (int tm = 0; tm < tiles_m; ++tm) sym_tiles += std::max(0, tiles_n_sym - tri_tn_min(tm));
+  const double kq = (double)((q + BK - 1) / BK) * BK;   // Gram: K = q
+  const double kp = (double)((p + BK - 1) / BK) * BK;   // square and product: K = p
+  const double tile = 2.0 * BM * BN;
+  double f = sym_tiles * tile * kq;                       // Gram
+  if (square) f += sym_tiles * tile * kp;                 // A A
+  f += (double)tiles_m * ((q + BN - 1) / BN) * tile * kp; // product
+  return f;
+}
+
 int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args, int sm_count,
                       void *stream) {
   static std::once_flag attr_once;
@@ -474,6 +627,7 @@ int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseA
     memset(&T, 0, sizeof T);
     T.n = std::min(kMaxClassesPerLaunch, n_classes - c0);
     T.b_mn_major = (gram || square) ? 0 : 1;
+    T.tri = (gram || square) ? 1 : 0;
     T.tile_start[0] = 0;
     for (int k = 0; k < T.n; ++k) {
       const ShapeClass &C = classes[c0 + k];
@@ -502,7 +656,14 @@ int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseA
       T.tiles_n[k] = (Ndim + BN - 1) / BN;
       T.k_iters[k] = (Kdim + BK - 1) / BK;
       T.sub0[k] = C.sub0;
-      T.tiles_per_mat[k] = ((C.p + BM - 1) / BM) * T.tiles_n[k];
+      const int tiles_m = (C.p + BM - 1) / BM;
+      if (T.tri) {
+        int cnt = 0;
+        for (int tm = 0; tm < tiles_m; ++tm) cnt += std::max(0, T.tiles_n[k] - tri_tn_min(tm));
+        T.tiles_per_mat[k] = cnt;
+      } else {
+        T.tiles_per_mat[k] = tiles_m * T.tiles_n[k];
+      }
       T.tile_start[k + 1] = T.tile_start[k] + (int64_t)C.count * T.tiles_per_mat[k];
     }
     const int64_t total = T.tile_start[T.n];

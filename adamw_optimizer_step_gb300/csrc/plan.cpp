@@ -97,7 +97,7 @@ int current_device(int *dev, DeviceInfo *info) {
 }
 
 constexpr int kPhaseMomentum = 0, kPhaseGram = 1, kPhaseProduct = 2, kPhaseSquare = 3,
-              kPhaseRows = 4;
+              kPhaseRows = 4, kPhaseFinal = 5;
 
 }  // namespace
 
@@ -222,8 +222,8 @@ int validate_and_expand(gbo_plan *P) {
     if (!d.g) continue;  // skipped this step: inactive
     if (!d.mom) return fail(GBO_ERR_INVALID_ARG, "desc %d: mom is NULL", t);
     if (o.normuon && !d.row_v) return fail(GBO_ERR_INVALID_ARG, "desc %d: NorMuon needs row_v", t);
-    const bool vec_rows = (d.cols % 4 == 0) && aligned(d.g, 16) && aligned(d.mom, 16) &&
-                          (d.g_dtype == GBO_BF16 ? aligned(d.g, 8) : true);
+    // momentum kernel: eight elements per 16-byte (bf16) or 2 x 16-byte (fp32) access
+    const bool vec_rows = (d.cols % 8 == 0) && aligned(d.g, 16) && aligned(d.mom, 16);
     const int64_t blocks = d.rows / r;
     for (int64_t b = 0; b < blocks; ++b) {
       int64_t start = b * r;
@@ -243,6 +243,7 @@ int validate_and_expand(gbo_plan *P) {
         S.w_dtype = d.w_dtype;
         S.g_dtype = d.g_dtype;
         S.vec_ok = vec_rows;
+        S.w_vec = ((d.cols * (int64_t)dtype_size(d.w_dtype)) % 16 == 0) && aligned(d.w, 16);
         S.scale = (float)std::sqrt(std::max(1.0, (double)S.m / (double)S.n));
         S.lr_mult = d.lr_mult;
         S.wd = d.wd;
@@ -329,7 +330,14 @@ int validate_and_expand(gbo_plan *P) {
       fl += 4.0 * p * p * q + (P->abc[3 * it + 2] != 0.f ? 2.0 * p * p * p : 0.0);
   }
   I.ns_flops = fl;
-  I.ns_flops_executed = fl;
+  if (P->x_dtype == GBO_BF16) {
+    double ex = 0;
+    for (const DevSub &S : P->subs)
+      for (int it = 0; it < o.ns_steps; ++it) ex += tc_executed_flops(S.p, S.q, P->abc[3 * it + 2] != 0.f);
+    I.ns_flops_executed = ex;
+  } else {
+    I.ns_flops_executed = fl;
+  }
   return GBO_OK;
 }
 
@@ -579,7 +587,7 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
     const bool last_it = it == k - 1;
     A.mode = (last_it && !P->opts.normuon) ? kFinal : kProduct;
     if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "product kernel");
-    mark(kPhaseProduct, gl);
+    mark(A.mode == kFinal ? kPhaseFinal : kPhaseProduct, gl);
     cur ^= 1;
   }
   if (P->opts.normuon) {

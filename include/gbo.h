@@ -317,11 +317,12 @@ int gbo_muon_plan_info(const gbo_plan *plan, gbo_plan_info *out);
  * recorded event, adds the elapsed milliseconds of every step since the last
  * reset into ms[phase] and the number of kernel launches into
  * launches[phase], then resets.  Phases: 0 momentum (+ the norm reduction),
- * 1 Newton-Schulz Gram products, 2 Newton-Schulz products back onto X (the
- * last one writes the weights unless NorMuon is on), 3 Gram squares (c != 0),
- * 4 NorMuon rows and weight write.  n_phases is the array length (<= 8).
+ * 1 Newton-Schulz Gram products, 2 Newton-Schulz products back onto X
+ * except the one that writes the weights, 3 Gram squares (c != 0), 4 NorMuon
+ * rows and weight write, 5 the last product with the weight write (no
+ * NorMuon).  n_phases is the array length (<= GBO_N_PHASES).
  */
-#define GBO_N_PHASES 5
+#define GBO_N_PHASES 6
 int gbo_muon_plan_set_timing(gbo_plan *plan, int32_t enable);
 int gbo_muon_plan_phase_times(gbo_plan *plan, float *ms, int64_t *launches, int32_t n_phases);
 
