@@ -108,6 +108,7 @@ def lib():
         "gbo_launch_count": (ctypes.c_uint64, []),
         "gbo_muon_plan_info": (c_int32, [c_void_p, ctypes.POINTER(PlanInfo)]),
         "gbo_muon_plan_set_timing": (c_int32, [c_void_p, c_int32]),
+        "gbo_muon_plan_set_event": (c_int32, [c_void_p, c_int32, c_void_p]),
         "gbo_muon_plan_phase_times": (c_int32, [c_void_p, ctypes.POINTER(c_float), ctypes.POINTER(c_int64),
                                                 c_int32]),
     }
@@ -257,6 +258,18 @@ def gbo_muon_step(plan, lr, workspace, dbg_update=None, dev_status=None, stream=
 
 def gbo_muon_plan_set_timing(plan, enable=True):
     _check(lib().gbo_muon_plan_set_timing(plan.handle, int(bool(enable))))
+
+
+def gbo_muon_plan_set_event(plan, phase, event):
+    """Record ``event`` (a torch.cuda.Event, or None to stop) after ``phase``
+    (0 = momentum) of every later step, on the step's stream."""
+    handle = None
+    if event is not None:
+        if not event.cuda_event:  # torch creates the CUDA event on first use
+            event.record()
+        handle = event.cuda_event
+    _check(lib().gbo_muon_plan_set_event(plan.handle, int(phase), handle))
+    plan._event = event  # keep it alive while the plan records it
 
 
 def gbo_muon_plan_phase_times(plan):

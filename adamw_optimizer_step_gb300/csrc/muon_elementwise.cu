@@ -24,6 +24,7 @@ namespace gbo {
 namespace {
 
 constexpr int kMomThreads = 256;
+constexpr int kMomWarps = kMomThreads / 32;  // one partial pair per warp and tile
 
 // Eight consecutive elements of a row as fp32: one 16-byte load (bf16) or
 // two (fp32) when `vec`, else element by element under `valid`.
@@ -90,7 +91,6 @@ __global__ void __launch_bounds__(kMomThreads)
 momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles, float mu,
                 int32_t nesterov, XT *__restrict__ x0, float *__restrict__ partials) {
   __shared__ float tile[kMomTile][kMomTile + 1];
-  __shared__ float red[32];
   const int cg = threadIdx.x & 7;
   const int rr = threadIdx.x >> 3;
   for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
@@ -129,9 +129,10 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
       }
       if (i < S.m && valid > 0) store8(S.mom + (S.r0 + i) * S.cols + j, b[ps], valid, vec);
     }
-    // Partials: the tile's max |D| and its sum of squares of D / max, so that
-    // the per-matrix combination cannot overflow.
-    const float M = block_max(lmax, red);
+    // Partials, one pair per warp: the max |D| of the warp's part of the tile
+    // and the sum of squares of D / max, so that the per-matrix combination
+    // cannot overflow.  Warp shuffles only: no block-wide barrier.
+    const float M = warp_max(lmax);
     float ss = 0.f;
     if (M > 0.f) {
       const float inv = 1.0f / M;
@@ -143,10 +144,11 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
           ss = fmaf(y, y, ss);
         }
     }
-    ss = block_sum(ss, red);
-    if (threadIdx.x == 0) {
-      partials[2 * t] = M;
-      partials[2 * t + 1] = ss;
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) {
+      float *pp = partials + 2 * (t * kMomWarps + (threadIdx.x >> 5));
+      pp[0] = M;
+      pp[1] = ss;
     }
     XT *X = x0 + S.x_off;
     if (!S.transposed) {
@@ -157,6 +159,7 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
       }
     } else {
       // X = D^T: stage the tile, then write rows of X (columns of D).
+      __syncthreads();  // the previous transposed tile's reads are done
 #pragma unroll
       for (int ps = 0; ps < 2; ++ps)
 #pragma unroll
@@ -175,7 +178,6 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
         }
       }
     }
-    __syncthreads();
   }
 }
 
@@ -187,8 +189,8 @@ prenorm_finalize_kernel(const DevSub *__restrict__ subs, const float *__restrict
                         float *__restrict__ alpha, int32_t *status) {
   __shared__ float red[32];
   const DevSub &S = subs[blockIdx.x];
-  const int64_t nt = (int64_t)((S.m + kMomTile - 1) / kMomTile) * S.tiles_c;
-  const float *P = partials + 2 * S.tile0;
+  const int64_t nt = (int64_t)((S.m + kMomTile - 1) / kMomTile) * S.tiles_c * kMomWarps;
+  const float *P = partials + 2 * S.tile0 * kMomWarps;
   float M = 0.f;
   for (int64_t k = threadIdx.x; k < nt; k += blockDim.x) M = fmaxf(M, P[2 * k]);
   M = block_max(M, red);

@@ -69,7 +69,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
 
@@ -116,6 +116,29 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Same copy, multicast to the CTAs of `mask` in the cluster: the data lands
+// at the same shared-memory offset in each, and each one's mbarrier at
+// offset `bar` gets the complete_tx.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                               int z, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs of the pair.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -160,6 +183,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Arrive on the mbarrier at offset `bar` in every CTA of `mask` once this
+// thread's earlier MMAs have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -183,13 +215,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 struct TileCoord {
-  int c, mat, tm, tn;
+  int c, mat, tm, tn;  // tm: tile-pair row
 };
 
 // First computed column tile of tile row tm in a symmetric launch: the
 // tile holds an element on or above the diagonal iff BN*tn + BN - 1 >= BM*tm.
 __host__ __device__ __forceinline__ int tri_tn_min(int tm) { return (tm * BM) / BN; }
 
+// Work items are tile pairs: the two CTAs of a cluster take tile rows
+// 2 * tm and 2 * tm + 1 of the same column tile tn (and so share the B tile).
 __device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
   TileCoord tc;
   int c = 0;
@@ -203,14 +237,14 @@ __device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
     tc.tm = rem / tn_all;
     tc.tn = rem % tn_all;
   } else {
-    int tm = 0;
-    for (;; ++tm) {
-      const int cnt = max(0, tn_all - tri_tn_min(tm));
+    int pr = 0;
+    for (;; ++pr) {
+      const int cnt = max(0, tn_all - tri_tn_min(2 * pr));
       if (rem < cnt) break;
       rem -= cnt;
     }
-    tc.tm = tm;
-    tc.tn = tri_tn_min(tm) + rem;
+    tc.tm = pr;
+    tc.tn = tri_tn_min(2 * pr) + rem;
   }
   return tc;
 }
@@ -415,7 +449,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 2);  // released by the MMAs of both CTAs of the pair
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf0 + 8 * a, 1);
@@ -434,8 +468,11 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();  // both CTAs' barriers are initialised before any multicast
   const uint32_t tmem_base = *tmem_slot;
   const int64_t total = P.tile_start[P.n];
+  const uint32_t crank = cluster_rank();
+  const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -449,8 +486,9 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       uint32_t armed_parity[STAGES];
       bool armed[STAGES];
       for (int s = 0; s < STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
-      for (int64_t t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
         const TileCoord tc = decode(P, t);
+        const int tm = 2 * tc.tm + (int)crank;
         const int kit = P.k_iters[tc.c];
         for (int kb = 0; kb < kit; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) { give_up(); break; }
@@ -461,13 +499,17 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
           armed_parity[stage] = phase;
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          tma_load_3d(sa, &P.mapA[tc.c], fb, kb * BK, tc.tm * BM, tc.mat);
+          tma_load_3d(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
+          // this CTA's half of the shared B tile, multicast to both CTAs
           if (!P.b_mn_major) {
-            tma_load_3d(sb, &P.mapB[tc.c], fb, kb * BK, tc.tn * BN, tc.mat);
+            tma_load_3d_mc(sb + crank * (B_BYTES / 2), &P.mapB[tc.c], fb, kb * BK, tc.tn * BN + (int)crank * (BN / 2),
+                           tc.mat, 0x3);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(sb + j * 8192, &P.mapB[tc.c], fb, tc.tn * BN + j * 64, kb * BK, tc.mat);
+            for (int h = 0; h < BN / 128; ++h) {
+              const int j = (int)crank * (BN / 128) + h;
+              tma_load_3d_mc(sb + j * 8192, &P.mapB[tc.c], fb, tc.tn * BN + j * 64, kb * BK, tc.mat, 0x3);
+            }
           }
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
@@ -486,7 +528,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       int acc = 0;
       uint32_t acc_phase = 0;
       bool issued = false;
-      for (int64_t t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
         const TileCoord tc = decode(P, t);
         const int kit = P.k_iters[tc.c];
         if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1)) { give_up(); break; }
@@ -506,7 +548,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
             mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           issued = true;
-          mma_commit(empty0 + 8 * stage);
+          mma_commit_mc(empty0 + 8 * stage, 0x3);  // frees this slot in both CTAs' rings
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (bad) break;
@@ -524,14 +566,14 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     const int quarter = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+    for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
       const TileCoord tc = decode(P, t);
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
       tc_fence_after();
       const int sub = P.sub0[tc.c] + tc.mat;
       const DevSub &S = A.subs[sub];
       const EpiScalars e = epi_scalars(A, sub);
-      const int i0 = tc.tm * BM + quarter * 32;
+      const int i0 = (2 * tc.tm + (int)crank) * BM + quarter * 32;
       float *st = stage_base + (warp - 2) * kStageFloats;
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       // skip column chunks that hold nothing this warp writes
@@ -553,6 +595,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();  // no multicast copy or remote arrive may target an exited CTA
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                  : "memory");
@@ -599,16 +642,18 @@ bool encode_map(CUtensorMap *map, void *base, int64_t cols, int64_t rows, int64_
 }  // namespace
 
 double tc_executed_flops(int p, int q, bool square) {
-  const int tiles_m = (p + BM - 1) / BM;
+  // work items are pairs of 128-row tiles: an odd tile-row count runs one
+  // all-padding tile in the last pair
+  const int pair_rows = ((p + BM - 1) / BM + 1) / 2;
   const int tiles_n_sym = (p + BN - 1) / BN;
-  int64_t sym_tiles = 0;
-  for (int tm = 0; tm < tiles_m; ++tm) sym_tiles += std::max(0, tiles_n_sym - tri_tn_min(tm));
+  int64_t sym_pairs = 0;
+  for (int pr = 0; pr < pair_rows; ++pr) sym_pairs += std::max(0, tiles_n_sym - tri_tn_min(2 * pr));
   const double kq = (double)((q + BK - 1) / BK) * BK;   // Gram: K = q
   const double kp = (double)((p + BK - 1) / BK) * BK;   // square and product: K = p
-  const double tile = 2.0 * BM * BN;
-  double f = sym_tiles * tile * kq;                       // Gram
-  if (square) f += sym_tiles * tile * kp;                 // A A
-  f += (double)tiles_m * ((q + BN - 1) / BN) * tile * kp; // product
+  const double pair = 2.0 * 2.0 * BM * BN;              // two 128 x 256 tiles, 2 FLOPs per MAC
+  double f = sym_pairs * pair * kq;                       // Gram
+  if (square) f += sym_pairs * pair * kp;                 // A A
+  f += (double)pair_rows * ((q + BN - 1) / BN) * pair * kp; // product
   return f;
 }
 
@@ -638,12 +683,12 @@ int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseA
       int Ndim, Kdim;
       if (gram) {  // A = X rows, B = X rows, K = q
         ok = encode_map(&T.mapA[k], xin, C.q, C.p, C.count, C.ld, BK, BM) &&
-             encode_map(&T.mapB[k], xin, C.q, C.p, C.count, C.ld, BK, BN);
+             encode_map(&T.mapB[k], xin, C.q, C.p, C.count, C.ld, BK, BN / 2);
         Ndim = C.p;
         Kdim = C.q;
       } else if (square) {  // A = Gram rows, B = Gram rows (symmetric), K = p
         ok = encode_map(&T.mapA[k], ab, C.p, C.p, C.count, C.ldp, BK, BM) &&
-             encode_map(&T.mapB[k], ab, C.p, C.p, C.count, C.ldp, BK, BN);
+             encode_map(&T.mapB[k], ab, C.p, C.p, C.count, C.ldp, BK, BN / 2);
         Ndim = C.p;
         Kdim = C.p;
       } else {  // A = P rows (K = p), B = X with rows as K, columns as N
@@ -656,20 +701,41 @@ int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseA
       T.tiles_n[k] = (Ndim + BN - 1) / BN;
       T.k_iters[k] = (Kdim + BK - 1) / BK;
       T.sub0[k] = C.sub0;
-      const int tiles_m = (C.p + BM - 1) / BM;
+      const int pair_rows = ((C.p + BM - 1) / BM + 1) / 2;
       if (T.tri) {
         int cnt = 0;
-        for (int tm = 0; tm < tiles_m; ++tm) cnt += std::max(0, T.tiles_n[k] - tri_tn_min(tm));
+        for (int pr = 0; pr < pair_rows; ++pr) cnt += std::max(0, T.tiles_n[k] - tri_tn_min(2 * pr));
         T.tiles_per_mat[k] = cnt;
       } else {
-        T.tiles_per_mat[k] = tiles_m * T.tiles_n[k];
+        T.tiles_per_mat[k] = pair_rows * T.tiles_n[k];
       }
       T.tile_start[k + 1] = T.tile_start[k] + (int64_t)C.count * T.tiles_per_mat[k];
     }
     const int64_t total = T.tile_start[T.n];
     if (total == 0) continue;
-    const unsigned grid = (unsigned)std::min<int64_t>(total, sm_count);
-    ns_gemm_tc_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
+    // persistent grid: as many CTA pairs as can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static std::once_flag occ_once;
+    static int max_clusters = 0;
+    std::call_once(occ_once, [&] {
+      cfg.gridDim = dim3(2 * std::max(1, sm_count / 2));
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, ns_gemm_tc_kernel, &cfg) != cudaSuccess)
+        max_clusters = 0;
+    });
+    const int clusters = (int)std::min<int64_t>(total, max_clusters > 0 ? max_clusters : std::max(1, sm_count / 2));
+    cfg.gridDim = dim3(2 * clusters);
+    const cudaError_t lerr = cudaLaunchKernelEx(&cfg, ns_gemm_tc_kernel, T, args);
+    if (lerr != cudaSuccess) return (int)lerr;
     count_launches(1);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return (int)err;

@@ -142,6 +142,7 @@ struct gbo_plan {
   };
   std::vector<Interval> pending;
   std::vector<cudaEvent_t> event_pool;
+  cudaEvent_t after_phase[8] = {};  // caller events recorded after a phase
 };
 
 namespace {
@@ -313,7 +314,7 @@ int validate_and_expand(gbo_plan *P) {
   P->off_p = region((size_t)poff * es);
   P->off_a = region(P->any_c ? (size_t)poff * es : 0);
   P->off_alpha = region(P->subs.size() * sizeof(float));
-  P->off_part = region((size_t)tiles * 2 * sizeof(float));
+  P->off_part = region((size_t)tiles * 8 * 2 * sizeof(float));  // (max, sum of squares) per warp of a tile
   P->ws_bytes = off;
   // info
   gbo_plan_info &I = P->info;
@@ -475,6 +476,12 @@ int gbo_muon_plan_set_timing(gbo_plan *P, int32_t enable) {
   return ok();
 }
 
+int gbo_muon_plan_set_event(gbo_plan *P, int32_t phase, void *event) {
+  if (!P || phase < 0 || phase >= GBO_N_PHASES) return fail(GBO_ERR_INVALID_ARG, "bad plan or phase");
+  P->after_phase[phase] = static_cast<cudaEvent_t>(event);
+  return ok();
+}
+
 int gbo_muon_plan_phase_times(gbo_plan *P, float *ms, int64_t *launches, int32_t n_phases) {
   if (!P || n_phases < 0 || (n_phases > 0 && (!ms || !launches)))
     return fail(GBO_ERR_INVALID_ARG, "bad argument");
@@ -535,6 +542,7 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   void *st = stream;
   cudaEvent_t last = nullptr;
   auto mark = [&](int phase, int64_t n_launch) {
+    if (P->after_phase[phase]) cudaEventRecord(P->after_phase[phase], reinterpret_cast<cudaStream_t>(stream));
     if (!P->timing) return;
     cudaEvent_t b = take_event(P);
     cudaEventRecord(b, reinterpret_cast<cudaStream_t>(stream));

@@ -323,6 +323,16 @@ int gbo_muon_plan_info(const gbo_plan *plan, gbo_plan_info *out);
  * NorMuon).  n_phases is the array length (<= GBO_N_PHASES).
  */
 #define GBO_N_PHASES 6
+
+/*
+ * Record `event` (a cudaEvent_t, created by the caller) on the step's stream
+ * right after phase `phase` of every later gbo_muon_step, or stop doing so
+ * when `event` is NULL.  Phase numbers as above; after phase 0 the momentum
+ * buffers are updated and the gradients are no longer read, so work on
+ * another stream that waits on the event (the AdamW path, the next
+ * gradients) overlaps the Newton-Schulz GEMMs.  Errors: INVALID_ARG.
+ */
+int gbo_muon_plan_set_event(gbo_plan *plan, int32_t phase, void *event);
 int gbo_muon_plan_set_timing(gbo_plan *plan, int32_t enable);
 int gbo_muon_plan_phase_times(gbo_plan *plan, float *ms, int64_t *launches, int32_t n_phases);
 

@@ -251,3 +251,30 @@ def test_standalone_rownorm():
     assert rel_fro(f64(U), 1.5 * N) < 1e-5
     want = f64(W) - 0.02 * (0.1 * f64(W) + f64(U))
     assert np.max(np.abs(f64(Wd) - want)) <= 2 ** -7 * np.max(np.abs(want))
+
+
+def test_after_momentum_event_and_side_stream():
+    """An event recorded after the momentum phase lets another stream start
+    (here: a copy of the updated momentum); results match a plain step."""
+    entries = random_entries([(256, 160, None, None), (160, 256, None, None)], seed=31, b_std=1e-3)
+    plain, _, _ = run_muon_gpu(entries, lr=0.02, precision="bf16")
+    dev = []
+    for e in entries:
+        d = dict(e)
+        for k in ("w", "g", "mom"):
+            d[k] = d[k].cuda()
+        dev.append(d)
+    plan = B.gbo_muon_plan_create(dev)
+    ev = torch.cuda.Event()
+    B.gbo_muon_plan_set_event(plan, 0, ev)
+    ws = torch.empty(B.gbo_muon_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    B.gbo_muon_step(plan, 0.02, ws)
+    side.wait_event(ev)
+    with torch.cuda.stream(side):
+        mom_copy = dev[0]["mom"].clone()
+    torch.cuda.synchronize()
+    assert torch.equal(mom_copy, plain[0]["B"].cuda())
+    for d, p in zip(dev, plain):
+        assert torch.equal(d["w"].cpu(), p["W"]) and torch.equal(d["mom"].cpu(), p["B"])
+    B.gbo_muon_plan_set_event(plan, 0, None)
