@@ -34,13 +34,13 @@ namespace gbo {
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;             // 16 KB
-constexpr int B_BYTES = BN * BK * 2;             // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int BM = 128;  // accumulator rows per CTA; a CTA pair computes a 256 x BN tile
+constexpr int BN = 256;  // columns of the pair tile; each CTA holds BN / 2 rows of B
+constexpr int BK = 64;   // 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's rows of A
+constexpr int B_BYTES = (BN / 2) * BK * 2;       // 16 KB: this CTA's half of B
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;                   // two 128 x 256 fp32 accumulators
 constexpr int kStageFloats = 32 * 33;             // per epilogue warp: one 32 x 32 transpose
@@ -128,6 +128,50 @@ __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *
       : "memory");
 }
 
+// Copy into this CTA's shared memory and signal the mbarrier at the
+// shared::cluster address `bar`, which may be in either CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                                 int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// shared::cluster address of the same shared::cta offset in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on a local barrier that CTAs of the cluster arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  if (mbar_try_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    if ((spin & 255u) == 255u && global_ns() - t0 > kWaitNs) return false;
+  }
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -163,37 +207,40 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
-// A K-major, B K-major or MN-major, M = 128, N = 256.
+// A K-major, B K-major or MN-major, M = 256 (two CTAs), N = 256.
 __host__ __device__ constexpr uint32_t make_idesc(int b_mn_major) {
   return (1u << 4)                      // D format: f32
          | (1u << 7)                    // A format: bf16
          | (1u << 10)                   // B format: bf16
          | ((uint32_t)b_mn_major << 16) // B major-ness
          | ((uint32_t)(BN >> 3) << 17)  // N / 8
-         | ((uint32_t)(BM >> 4) << 24); // M / 16
+         | ((uint32_t)((2 * BM) >> 4) << 24); // M / 16 (the CTA pair)
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// One 256 x 256 x 16 MMA over the CTA pair (issued by the even CTA): A
+// rows 0-127 and B rows 0-127 come from this CTA's shared memory, the rest
+// from the peer's at the same offsets; each CTA's TMEM receives its 128 rows.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive on the mbarrier at offset `bar` in every CTA of `mask` once this
-// thread's earlier MMAs have completed.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+// Arrive on the mbarrier at offset `bar` in every CTA of `mask` once the
+// pair MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
 
@@ -445,34 +492,44 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank();
+  const bool leader = crank == 0;
 
+  // Barrier protocol of the CTA pair (the even CTA leads):
+  //   full[s]   leader only: both CTAs' copies of stage s complete_tx on it;
+  //             the leader's producer arms it with both CTAs' bytes
+  //   empty[s]  each CTA: the leader's MMA commit (multicast) frees slot s
+  //   accf[a]   each CTA: the leader's MMA commit (multicast) says
+  //             accumulator a is complete in both TMEMs
+  //   acce[a]   leader only: one arrival per epilogue warp of both CTAs
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 2);  // released by the MMAs of both CTAs of the pair
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf0 + 8 * a, 1);
-      mbar_init(acce0 + 8 * a, 128);
+      mbar_init(acce0 + 8 * a, 8);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+  if (warp == 1) {  // one warp of each CTA allocates the pair's TMEM together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // both CTAs' barriers are initialised before any multicast
+  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
   const uint32_t tmem_base = *tmem_slot;
   const int64_t total = P.tile_start[P.n];
-  const uint32_t crank = cluster_rank();
   const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const uint32_t full_lead0 = map_to_rank(full0, 0);
+  const uint32_t acce_lead0 = map_to_rank(acce0, 0);
 
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -493,35 +550,35 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
         for (int kb = 0; kb < kit; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) { give_up(); break; }
           if (*abort_flag) break;
-          const uint32_t fb = full0 + 8 * stage;
-          mbar_expect_tx(fb, STAGE_BYTES);
-          armed[stage] = true;
-          armed_parity[stage] = phase;
+          if (leader) {
+            mbar_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
+            armed[stage] = true;
+            armed_parity[stage] = phase;
+          }
+          const uint32_t fb = full_lead0 + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          tma_load_3d(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
-          // this CTA's half of the shared B tile, multicast to both CTAs
+          tma_load_3d_pair(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
+          // this CTA's half of B: columns tn * BN + crank * BN / 2 ...
+          const int n0 = tc.tn * BN + (int)crank * (BN / 2);
           if (!P.b_mn_major) {
-            tma_load_3d_mc(sb + crank * (B_BYTES / 2), &P.mapB[tc.c], fb, kb * BK, tc.tn * BN + (int)crank * (BN / 2),
-                           tc.mat, 0x3);
+            tma_load_3d_pair(sb, &P.mapB[tc.c], fb, kb * BK, n0, tc.mat);
           } else {
 #pragma unroll
-            for (int h = 0; h < BN / 128; ++h) {
-              const int j = (int)crank * (BN / 128) + h;
-              tma_load_3d_mc(sb + j * 8192, &P.mapB[tc.c], fb, tc.tn * BN + j * 64, kb * BK, tc.mat, 0x3);
-            }
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_3d_pair(sb + h * 8192, &P.mapB[tc.c], fb, n0 + h * 64, kb * BK, tc.mat);
           }
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
       }
-      if (*abort_flag) {
-        // let every copy this thread started land before shared memory goes away
+      if (*abort_flag && leader) {
+        // let every copy of the pair armed here land before shared memory goes away
         for (int s = 0; s < STAGES; ++s)
           if (armed[s]) (void)mbar_wait(full0 + 8 * s, armed_parity[s]);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       const uint32_t idesc = make_idesc(P.b_mn_major);
       int stage = 0;
       uint32_t phase = 0;
@@ -531,7 +588,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
         const TileCoord tc = decode(P, t);
         const int kit = P.k_iters[tc.c];
-        if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1)) { give_up(); break; }
+        if (!mbar_wait_cluster(acce0 + 8 * acc, acc_phase ^ 1)) { give_up(); break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         bool bad = false;
@@ -545,19 +602,19 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
             const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
             const uint64_t bd = P.b_mn_major ? smem_desc(sb + k * 2048, 8192, 1024)
                                              : smem_desc(sb + k * 32, 16, 1024);
-            mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           issued = true;
-          mma_commit_mc(empty0 + 8 * stage, 0x3);  // frees this slot in both CTAs' rings
+          mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees slot `stage` in both CTAs
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (bad) break;
-        mma_commit(accf0 + 8 * acc);
+        mma_commit_pair_mc(accf0 + 8 * acc, 0x3);  // accumulator `acc` ready in both TMEMs
         if (++acc == 2) acc = 0, acc_phase ^= 1;
       }
       if (*abort_flag && issued) {
-        // wait for this thread's outstanding MMAs before TMEM is released
-        mma_commit(drain);
+        // wait for the outstanding MMAs before TMEM is released
+        mma_commit_pair(drain);
         (void)mbar_wait(drain, 0);
       }
     }
@@ -587,7 +644,8 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
         if (i0 < S.p) epilogue_block(A, S, e, i0, col0, v, st, lane);
       }
       tc_fence_before();
-      mbar_arrive(acce0 + 8 * acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce_lead0 + 8 * acc);  // this warp is done with `acc`
       if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
   }
@@ -595,9 +653,9 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // no multicast copy or remote arrive may target an exited CTA
+  cluster_sync();  // no copy or remote arrive may target an exited CTA
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                  : "memory");
   }
 }
