@@ -93,8 +93,15 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
   __shared__ float tile[kMomTile][kMomTile + 1];
   const int cg = threadIdx.x & 7;
   const int rr = threadIdx.x >> 3;
-  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-    const int si = find_owner(t, n_subs, [&](int k) { return subs[k].tile0; });
+  // Each block takes a contiguous range of tiles, so the owning matrix is
+  // found once and then only advanced.
+  const int64_t per = (n_tiles + gridDim.x - 1) / gridDim.x;
+  const int64_t t_begin = (int64_t)blockIdx.x * per;
+  const int64_t t_end = min(n_tiles, t_begin + per);
+  if (t_begin >= t_end) return;
+  int si = find_owner(t_begin, n_subs, [&](int k) { return subs[k].tile0; });
+  for (int64_t t = t_begin; t < t_end; ++t) {
+    while (si + 1 < n_subs && subs[si + 1].tile0 <= t) ++si;
     const DevSub &S = subs[si];
     const int64_t lt = t - S.tile0;
     const int tr = (int)(lt / S.tiles_c), tc = (int)(lt % S.tiles_c);
@@ -357,7 +364,17 @@ rownorm_plain_kernel(const float *__restrict__ O, int64_t rows, int64_t cols, fl
 int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float mu, int32_t nesterov,
                     void *x0, int32_t x_dtype, float *partials, int sm_count, void *stream) {
   if (n_tiles == 0) return 0;
-  const int64_t grid = std::min<int64_t>(n_tiles, (int64_t)sm_count * 8);
+  // one wave: as many blocks as can be resident, each a contiguous tile range
+  static int resident[2] = {0, 0};
+  const int which = x_dtype == GBO_BF16 ? 0 : 1;
+  if (!resident[which]) {
+    int r = 0;
+    const cudaError_t e = x_dtype == GBO_BF16
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, momentum_kernel<__nv_bfloat16>, kMomThreads, 0)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, momentum_kernel<float>, kMomThreads, 0);
+    resident[which] = (e == cudaSuccess && r > 0) ? r : 4;
+  }
+  const int64_t grid = std::min<int64_t>(n_tiles, (int64_t)sm_count * resident[which]);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (x_dtype == GBO_BF16)
     momentum_kernel<__nv_bfloat16><<<(unsigned)grid, kMomThreads, 0, st>>>(

@@ -11,10 +11,10 @@
 // matrix) covers a whole shape class; out-of-range rows and columns of a
 // tile are zero-filled by TMA and masked in the epilogue.
 //
-// Persistent, warp-specialised CTA (192 threads, one CTA per SM):
+// Persistent, warp-specialised CTA (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane), STAGES-deep ring of A/B tiles
 //   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2..5  epilogue: TMEM -> registers -> global, 32 rows each
+//   warps 2..9  epilogue: TMEM -> registers -> global, 32 rows x 128 columns each
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the
 // epilogue of one tile overlaps the MMAs of the next.  Every wait is
 // bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT, waits (bounded)
@@ -41,10 +41,18 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's rows of A
 constexpr int B_BYTES = (BN / 2) * BK * 2;       // 16 KB: this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB
-constexpr int kThreads = 192;
+#ifndef GBO_EPI_WARPS
+#define GBO_EPI_WARPS 4
+#endif
+// Epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter, each
+// taking half of the tile's columns).
+constexpr int kEpiWarps = GBO_EPI_WARPS;
+static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;                   // two 128 x 256 fp32 accumulators
 constexpr int kStageFloats = 32 * 33;             // per epilogue warp: one 32 x 32 transpose
-constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + 4 * kStageFloats * 4;
+constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + kEpiWarps * kStageFloats * 4;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
 struct TcParams {
@@ -502,6 +510,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   //   accf[a]   each CTA: the leader's MMA commit (multicast) says
   //             accumulator a is complete in both TMEMs
   //   acce[a]   leader only: one arrival per epilogue warp of both CTAs
+  //             (2 x kEpiWarps)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -509,7 +518,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf0 + 8 * a, 1);
-      mbar_init(acce0 + 8 * a, 8);
+      mbar_init(acce0 + 8 * a, 2 * kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -619,8 +628,11 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       }
     }
   } else {
-    // epilogue warps 2..5: TMEM lane quarter = warp % 4
+    // epilogue warps 2..9: TMEM lane quarter = warp % 4; warps 2-5 take
+    // columns 0-127 of the tile, warps 6-9 columns 128-255
     const int quarter = warp & 3;
+    const int half = kEpiWarps == 8 ? (warp - 2) >> 2 : 0;
+    const int nch = kEpiWarps == 8 ? BN / 64 : BN / 32;  // column chunks per warp
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
@@ -636,7 +648,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       // skip column chunks that hold nothing this warp writes
       const int ncols = (A.mode == kProduct || A.mode == kFinal) ? S.q : S.p;
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
+      for (int ch = half * nch; ch < (half + 1) * nch; ++ch) {
         const int col0 = tc.tn * BN + ch * 32;
         if (col0 >= ncols) break;
         float v[32];

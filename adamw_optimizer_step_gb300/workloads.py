@@ -187,6 +187,19 @@ def normuon_7b():
 WORKLOADS = {1: tiny_fp32, 2: one_layer, 3: omn_shaped, 4: many_small, 5: normuon_7b}
 
 
+def first_layers(wl, n):
+    """The same workload restricted to its first ``n`` layers (tensors named
+    ``l<k>.*`` with k < n), for small profiling cases; other tensors stay."""
+    keep = []
+    for t in wl.muon:
+        head = t.name.split(".")[0]
+        if not (head.startswith("l") and head[1:].isdigit()) or int(head[1:]) < n:
+            keep.append(t)
+    wl.muon = keep
+    wl.name = "%s_first_%d_layers" % (wl.name, n)
+    return wl
+
+
 def workload(index):
     return WORKLOADS[index]()
 

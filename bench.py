@@ -36,6 +36,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="keep only the first N layers of the workload (small cases for ncu captures)")
     ap.add_argument("--overlap", action="store_true",
                     help="run clip + AdamW on a side stream that starts after the momentum phase")
     ap.add_argument("--workload", type=int, default=WORKLOAD,
@@ -267,6 +269,8 @@ def run_ours(args):
 
     gbo.lib()
     wl = wk.workload(args.workload)
+    if args.layers:
+        wl = wk.first_layers(wl, args.layers)
     dev = "cuda"
     # Muon gradients live in one flat buffer so the end-to-end run can copy
     # a step's gradients in with one transfer; likewise the AdamW gradients.
