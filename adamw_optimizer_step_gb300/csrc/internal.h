@@ -8,7 +8,8 @@
 
 namespace gbo {
 
-constexpr int kMomTile = 64;        // momentum tiles: 64 x 64 elements of a matrix
+constexpr int kMomTile = 64;        // momentum tiles: 64 x 64 elements of a matrix, or
+constexpr int kMomFlat = kMomTile * kMomTile;  // 4096 consecutive elements of a matrix
 constexpr int kRowBlock = 32;       // NorMuon: stored rows per block
 constexpr int kMaxClassesPerLaunch = 8;
 
@@ -32,7 +33,8 @@ struct DevSub {
   int32_t p, q;     // oriented rows, cols
   int32_t ld;       // X row stride (elements)
   int32_t ldp;      // P row stride (elements)
-  int32_t tiles_c;  // momentum tiles along n
+  int32_t tiles_c;  // momentum tiles along n (2-D tiles), or 0 for flat tiles
+  int32_t ntiles;   // momentum tiles of this matrix
   int32_t transposed;
   int32_t w_dtype, g_dtype;
   int32_t vec_ok;   // g and mom rows start on 16-byte boundaries (n % 8 == 0)
@@ -41,6 +43,7 @@ struct DevSub {
   float lr_mult;
   float wd;
   int32_t w_vec;    // weight rows start on 16-byte boundaries (vector read-modify-write)
+  int32_t pad0;
 };
 
 // Matrices of one oriented shape (p, q), stored back to back in the
@@ -106,6 +109,9 @@ int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseA
 // iteration (Gram over the upper block-triangle of tiles, square when c != 0,
 // product), counting the zero padding of partial tiles.
 double tc_executed_flops(int p, int q, bool square);
+// Whether the tensor-core kernel runs a shape class of p oriented rows on
+// single CTAs (p <= 128) rather than on CTA pairs.
+bool single_mode(int p);
 
 void count_launches(uint64_t n);
 

@@ -104,37 +104,101 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
     while (si + 1 < n_subs && subs[si + 1].tile0 <= t) ++si;
     const DevSub &S = subs[si];
     const int64_t lt = t - S.tile0;
-    const int tr = (int)(lt / S.tiles_c), tc = (int)(lt % S.tiles_c);
-    const int rb = tr * kMomTile, cb = tc * kMomTile;
-    const int j = cb + cg * 8;
-    const int valid = max(0, min(8, S.n - j));
     const bool vec = S.vec_ok != 0;
-    float g[2][8], b[2][8];
-#pragma unroll
-    for (int ps = 0; ps < 2; ++ps) {
-      const int i = rb + ps * 32 + rr;
-      if (i < S.m && valid > 0) {
-        const int64_t widx = (S.r0 + i) * S.cols + j;
-        load8(S.g, S.g_dtype, widx, valid, vec, g[ps]);
-        load8(S.mom, GBO_F32, widx, valid, vec, b[ps]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) g[ps][e] = b[ps][e] = 0.f;
-      }
-    }
-    float d[2][8];
+    float g[2][8], b[2][8], d[2][8];
     float lmax = 0.f;
+    if (S.tiles_c == 0) {
+      // flat tile: elements [lt * 4096, +4096) of the contiguous matrix;
+      // thread t covers 8 consecutive elements in each half
+      const int64_t nel = (int64_t)S.m * S.n;
+      const int64_t e0 = lt * kMomFlat;
+      const int64_t wbase = S.r0 * S.cols;
 #pragma unroll
-    for (int ps = 0; ps < 2; ++ps) {
-      const int i = rb + ps * 32 + rr;
+      for (int ps = 0; ps < 2; ++ps) {
+        const int64_t e = e0 + ps * (kMomFlat / 2) + threadIdx.x * 8;
+        const int valid = (int)max((int64_t)0, min((int64_t)8, nel - e));
+        if (valid > 0) {
+          load8(S.g, S.g_dtype, wbase + e, valid, vec, g[ps]);
+          load8(S.mom, GBO_F32, wbase + e, valid, vec, b[ps]);
+        } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float nb = mu * b[ps][e] + g[ps][e];
-        b[ps][e] = nb;
-        d[ps][e] = nesterov ? g[ps][e] + mu * nb : nb;
-        lmax = fmaxf(lmax, fabsf(d[ps][e]));
+          for (int k = 0; k < 8; ++k) g[ps][k] = b[ps][k] = 0.f;
+        }
       }
-      if (i < S.m && valid > 0) store8(S.mom + (S.r0 + i) * S.cols + j, b[ps], valid, vec);
+#pragma unroll
+      for (int ps = 0; ps < 2; ++ps) {
+        const int64_t e = e0 + ps * (kMomFlat / 2) + threadIdx.x * 8;
+        const int valid = (int)max((int64_t)0, min((int64_t)8, nel - e));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float nb = mu * b[ps][k] + g[ps][k];
+          b[ps][k] = nb;
+          d[ps][k] = k < valid ? (nesterov ? g[ps][k] + mu * nb : nb) : 0.f;
+          lmax = fmaxf(lmax, fabsf(d[ps][k]));
+        }
+        if (valid > 0) {
+          store8(S.mom + wbase + e, b[ps], valid, vec);
+          store8(x0 + S.x_off + e, d[ps], valid, true);
+        }
+      }
+    } else {
+      // 2-D tile (tall matrices, or rows that do not allow 16-byte access)
+      const int tr = (int)(lt / S.tiles_c), tc = (int)(lt % S.tiles_c);
+      const int rb = tr * kMomTile, cb = tc * kMomTile;
+      const int j = cb + cg * 8;
+      const int valid = max(0, min(8, S.n - j));
+#pragma unroll
+      for (int ps = 0; ps < 2; ++ps) {
+        const int i = rb + ps * 32 + rr;
+        if (i < S.m && valid > 0) {
+          const int64_t widx = (S.r0 + i) * S.cols + j;
+          load8(S.g, S.g_dtype, widx, valid, vec, g[ps]);
+          load8(S.mom, GBO_F32, widx, valid, vec, b[ps]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) g[ps][e] = b[ps][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int ps = 0; ps < 2; ++ps) {
+        const int i = rb + ps * 32 + rr;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float nb = mu * b[ps][e] + g[ps][e];
+          b[ps][e] = nb;
+          d[ps][e] = nesterov ? g[ps][e] + mu * nb : nb;
+          lmax = fmaxf(lmax, fabsf(d[ps][e]));
+        }
+        if (i < S.m && valid > 0) store8(S.mom + (S.r0 + i) * S.cols + j, b[ps], valid, vec);
+      }
+      XT *X = x0 + S.x_off;
+      if (!S.transposed) {
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps) {
+          const int i = rb + ps * 32 + rr;
+          if (i < S.m && valid > 0) store8(X + (int64_t)i * S.ld + j, d[ps], valid, true);
+        }
+      } else {
+        // X = D^T: stage the tile, then write rows of X (columns of D).
+        __syncthreads();  // the previous transposed tile's reads are done
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) tile[ps * 32 + rr][cg * 8 + e] = d[ps][e];
+        __syncthreads();
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps) {
+          const int xr = cb + ps * 32 + rr;  // row of X = column of D
+          const int xc = rb + cg * 8;        // first column of X = row of D
+          const int xvalid = max(0, min(8, S.m - xc));
+          if (xr < S.n && xvalid > 0) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = tile[cg * 8 + e][ps * 32 + rr];
+            store8(X + (int64_t)xr * S.ld + xc, v, xvalid, true);
+          }
+        }
+      }
     }
     // Partials, one pair per warp: the max |D| of the warp's part of the tile
     // and the sum of squares of D / max, so that the per-matrix combination
@@ -157,34 +221,6 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
       pp[0] = M;
       pp[1] = ss;
     }
-    XT *X = x0 + S.x_off;
-    if (!S.transposed) {
-#pragma unroll
-      for (int ps = 0; ps < 2; ++ps) {
-        const int i = rb + ps * 32 + rr;
-        if (i < S.m && valid > 0) store8(X + (int64_t)i * S.ld + j, d[ps], valid, true);
-      }
-    } else {
-      // X = D^T: stage the tile, then write rows of X (columns of D).
-      __syncthreads();  // the previous transposed tile's reads are done
-#pragma unroll
-      for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) tile[ps * 32 + rr][cg * 8 + e] = d[ps][e];
-      __syncthreads();
-#pragma unroll
-      for (int ps = 0; ps < 2; ++ps) {
-        const int xr = cb + ps * 32 + rr;  // row of X = column of D
-        const int xc = rb + cg * 8;        // first column of X = row of D
-        const int xvalid = max(0, min(8, S.m - xc));
-        if (xr < S.n && xvalid > 0) {
-          float v[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = tile[cg * 8 + e][ps * 32 + rr];
-          store8(X + (int64_t)xr * S.ld + xc, v, xvalid, true);
-        }
-      }
-    }
   }
 }
 
@@ -196,7 +232,7 @@ prenorm_finalize_kernel(const DevSub *__restrict__ subs, const float *__restrict
                         float *__restrict__ alpha, int32_t *status) {
   __shared__ float red[32];
   const DevSub &S = subs[blockIdx.x];
-  const int64_t nt = (int64_t)((S.m + kMomTile - 1) / kMomTile) * S.tiles_c * kMomWarps;
+  const int64_t nt = (int64_t)S.ntiles * kMomWarps;
   const float *P = partials + 2 * S.tile0 * kMomWarps;
   float M = 0.f;
   for (int64_t k = threadIdx.x; k < nt; k += blockDim.x) M = fmaxf(M, P[2 * k]);

@@ -34,13 +34,27 @@ namespace gbo {
 
 namespace {
 
-constexpr int BM = 128;  // accumulator rows per CTA; a CTA pair computes a 256 x BN tile
-constexpr int BN = 256;  // columns of the pair tile; each CTA holds BN / 2 rows of B
+constexpr int BM = 128;  // accumulator rows per CTA
+constexpr int BN = 256;  // tile columns (a pair tile is 256 x BN, split by rows)
 constexpr int BK = 64;   // 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's rows of A
-constexpr int B_BYTES = (BN / 2) * BK * 2;       // 16 KB: this CTA's half of B
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB
+constexpr int B_HALF = (BN / 2) * BK * 2;        // 16 KB: 128 rows of B
+// Two modes share the kernel source:
+//   pair   (kPair = true)  2-CTA cluster, tcgen05 cta_group::2, 256 x 256 tile;
+//                          each CTA stages A 16 KB + half of B 16 KB (6 stages)
+//   single (kPair = false) one CTA, cta_group::1, 128 x 256 tile; the CTA
+//                          stages A 16 KB + all of B 32 KB (4 stages); used for
+//                          matrices of at most 128 rows, where a pair would
+//                          spend its second CTA on padding
+template <bool kPair>
+struct Mode {
+  static constexpr int kStageBytes = A_BYTES + (kPair ? B_HALF : 2 * B_HALF);
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kRows = kPair ? 2 : 1;  // 128-row tiles per work item
+};
+constexpr int kRingBytes = 6 * (A_BYTES + B_HALF);
+static_assert(Mode<true>::kStages * Mode<true>::kStageBytes == kRingBytes, "ring size");
+static_assert(Mode<false>::kStages * Mode<false>::kStageBytes == kRingBytes, "ring size");
 #ifndef GBO_EPI_WARPS
 #define GBO_EPI_WARPS 4
 #endif
@@ -51,7 +65,7 @@ static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;                   // two 128 x 256 fp32 accumulators
 constexpr int kStageFloats = 32 * 33;             // per epilogue warp: one 32 x 32 transpose
-constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + kEpiWarps * kStageFloats * 4;
+constexpr int kSmemBytes = kRingBytes + 1024 /*align*/ + 256 /*barriers*/ + kEpiWarps * kStageFloats * 4;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
@@ -121,18 +135,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-// Same copy, multicast to the CTAs of `mask` in the cluster: the data lands
-// at the same shared-memory offset in each, and each one's mbarrier at
-// offset `bar` gets the complete_tx.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
-                                               int z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
       : "memory");
 }
 
@@ -215,14 +217,30 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
-// A K-major, B K-major or MN-major, M = 256 (two CTAs), N = 256.
-__host__ __device__ constexpr uint32_t make_idesc(int b_mn_major) {
+// A K-major, B K-major or MN-major, N = 256, M = 128 (one CTA) or 256 (pair).
+__host__ __device__ constexpr uint32_t make_idesc(int b_mn_major, int m) {
   return (1u << 4)                      // D format: f32
          | (1u << 7)                    // A format: bf16
          | (1u << 10)                   // B format: bf16
          | ((uint32_t)b_mn_major << 16) // B major-ness
          | ((uint32_t)(BN >> 3) << 17)  // N / 8
-         | ((uint32_t)((2 * BM) >> 4) << 24); // M / 16 (the CTA pair)
+         | ((uint32_t)(m >> 4) << 24);  // M / 16
+}
+
+// One 128 x 256 x 16 MMA of this CTA (cta_group::1).
+__device__ __forceinline__ void mma_bf16_one(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_one(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
 }
 
 // One 256 x 256 x 16 MMA over the CTA pair (issued by the even CTA): A
@@ -270,15 +288,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 struct TileCoord {
-  int c, mat, tm, tn;  // tm: tile-pair row
+  int c, mat, tm, tn;  // tm: work-item row (a pair of tile rows in pair mode)
 };
 
 // First computed column tile of tile row tm in a symmetric launch: the
 // tile holds an element on or above the diagonal iff BN*tn + BN - 1 >= BM*tm.
 __host__ __device__ __forceinline__ int tri_tn_min(int tm) { return (tm * BM) / BN; }
 
-// Work items are tile pairs: the two CTAs of a cluster take tile rows
-// 2 * tm and 2 * tm + 1 of the same column tile tn (and so share the B tile).
+// Work items: kRows consecutive 128-row tiles of one column tile tn (the two
+// CTAs of a pair take rows kRows * r and kRows * r + 1).  In a symmetric
+// launch only items touching the upper triangle exist.
+template <int kRows>
 __device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
   TileCoord tc;
   int c = 0;
@@ -292,14 +312,14 @@ __device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
     tc.tm = rem / tn_all;
     tc.tn = rem % tn_all;
   } else {
-    int pr = 0;
-    for (;; ++pr) {
-      const int cnt = max(0, tn_all - tri_tn_min(2 * pr));
+    int r = 0;
+    for (;; ++r) {
+      const int cnt = max(0, tn_all - tri_tn_min(kRows * r));
       if (rem < cnt) break;
       rem -= cnt;
     }
-    tc.tm = pr;
-    tc.tn = tri_tn_min(2 * pr) + rem;
+    tc.tm = r;
+    tc.tn = tri_tn_min(kRows * r) + rem;
   }
   return tc;
 }
@@ -487,30 +507,34 @@ __device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const DevSub 
   }
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ PhaseArgs A) {
+  constexpr int STAGES = Mode<kPair>::kStages;
+  constexpr int STAGE_BYTES = Mode<kPair>::kStageBytes;
+  constexpr int kRows = Mode<kPair>::kRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
   // bars: full[STAGES], empty[STAGES], accf[2], acce[2], drain
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
-  float *stage_base = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + 256);
+  float *stage_base = reinterpret_cast<float *>(smem + kRingBytes + 256);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_rank();
+  const uint32_t crank = kPair ? cluster_rank() : 0u;
   const bool leader = crank == 0;
 
-  // Barrier protocol of the CTA pair (the even CTA leads):
+  // Barrier protocol.  Single mode: everything is local to the CTA.  Pair
+  // mode (the even CTA leads):
   //   full[s]   leader only: both CTAs' copies of stage s complete_tx on it;
   //             the leader's producer arms it with both CTAs' bytes
   //   empty[s]  each CTA: the leader's MMA commit (multicast) frees slot s
   //   accf[a]   each CTA: the leader's MMA commit (multicast) says
   //             accumulator a is complete in both TMEMs
   //   acce[a]   leader only: one arrival per epilogue warp of both CTAs
-  //             (2 x kEpiWarps)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -518,27 +542,35 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf0 + 8 * a, 1);
-      mbar_init(acce0 + 8 * a, 2 * kEpiWarps);
+      mbar_init(acce0 + 8 * a, (kPair ? 2 : 1) * kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {  // one warp of each CTA allocates the pair's TMEM together
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  if (warp == 1) {  // pair mode: one warp of each CTA allocates the pair's TMEM together
+    if constexpr (kPair) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
+  if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before any remote arrive
   const uint32_t tmem_base = *tmem_slot;
   const int64_t total = P.tile_start[P.n];
-  const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
-  const uint32_t full_lead0 = map_to_rank(full0, 0);
-  const uint32_t acce_lead0 = map_to_rank(acce0, 0);
+  const int64_t cid = kPair ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t ncl = kPair ? (gridDim.x >> 1) : gridDim.x;
+  const uint32_t full_lead0 = kPair ? map_to_rank(full0, 0) : full0;
+  const uint32_t acce_lead0 = kPair ? map_to_rank(acce0, 0) : acce0;
 
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -553,51 +585,68 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       bool armed[STAGES];
       for (int s = 0; s < STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
       for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
-        const TileCoord tc = decode(P, t);
-        const int tm = 2 * tc.tm + (int)crank;
+        const TileCoord tc = decode<kRows>(P, t);
+        const int tm = kRows * tc.tm + (int)crank;
         const int kit = P.k_iters[tc.c];
         for (int kb = 0; kb < kit; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) { give_up(); break; }
           if (*abort_flag) break;
           if (leader) {
-            mbar_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
+            mbar_expect_tx(full0 + 8 * stage, (kPair ? 2 : 1) * STAGE_BYTES);
             armed[stage] = true;
             armed_parity[stage] = phase;
           }
-          const uint32_t fb = full_lead0 + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          tma_load_3d_pair(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
-          // this CTA's half of B: columns tn * BN + crank * BN / 2 ...
-          const int n0 = tc.tn * BN + (int)crank * (BN / 2);
-          if (!P.b_mn_major) {
-            tma_load_3d_pair(sb, &P.mapB[tc.c], fb, kb * BK, n0, tc.mat);
-          } else {
+          if constexpr (kPair) {
+            const uint32_t fb = full_lead0 + 8 * stage;
+            tma_load_3d_pair(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
+            // this CTA's half of B: columns tn * BN + crank * BN / 2 ...
+            const int n0 = tc.tn * BN + (int)crank * (BN / 2);
+            if (!P.b_mn_major) {
+              tma_load_3d_pair(sb, &P.mapB[tc.c], fb, kb * BK, n0, tc.mat);
+            } else {
 #pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-              tma_load_3d_pair(sb + h * 8192, &P.mapB[tc.c], fb, n0 + h * 64, kb * BK, tc.mat);
+              for (int h = 0; h < BN / 128; ++h)
+                tma_load_3d_pair(sb + h * 8192, &P.mapB[tc.c], fb, n0 + h * 64, kb * BK, tc.mat);
+            }
+          } else {
+            const uint32_t fb = full0 + 8 * stage;
+            tma_load_3d(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
+            const int n0 = tc.tn * BN;
+            if (!P.b_mn_major) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d(sb + h * B_HALF, &P.mapB[tc.c], fb, kb * BK, n0 + h * (BN / 2), tc.mat);
+            } else {
+#pragma unroll
+              for (int h = 0; h < BN / 64; ++h)
+                tma_load_3d(sb + h * 8192, &P.mapB[tc.c], fb, n0 + h * 64, kb * BK, tc.mat);
+            }
           }
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
       }
       if (*abort_flag && leader) {
-        // let every copy of the pair armed here land before shared memory goes away
+        // let every copy armed here land before shared memory goes away
         for (int s = 0; s < STAGES; ++s)
           if (armed[s]) (void)mbar_wait(full0 + 8 * s, armed_parity[s]);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
-      const uint32_t idesc = make_idesc(P.b_mn_major);
+      const uint32_t idesc = make_idesc(P.b_mn_major, kRows * BM);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool issued = false;
       for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
-        const TileCoord tc = decode(P, t);
+        const TileCoord tc = decode<kRows>(P, t);
         const int kit = P.k_iters[tc.c];
-        if (!mbar_wait_cluster(acce0 + 8 * acc, acc_phase ^ 1)) { give_up(); break; }
+        const bool freed = kPair ? mbar_wait_cluster(acce0 + 8 * acc, acc_phase ^ 1)
+                                 : mbar_wait(acce0 + 8 * acc, acc_phase ^ 1);
+        if (!freed) { give_up(); break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         bool bad = false;
@@ -611,38 +660,42 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
             const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
             const uint64_t bd = P.b_mn_major ? smem_desc(sb + k * 2048, 8192, 1024)
                                              : smem_desc(sb + k * 32, 16, 1024);
-            mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            if constexpr (kPair) mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            else mma_bf16_one(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           issued = true;
-          mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees slot `stage` in both CTAs
+          if constexpr (kPair) mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs
+          else mma_commit_one(empty0 + 8 * stage);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (bad) break;
-        mma_commit_pair_mc(accf0 + 8 * acc, 0x3);  // accumulator `acc` ready in both TMEMs
+        if constexpr (kPair) mma_commit_pair_mc(accf0 + 8 * acc, 0x3);  // accumulator ready in both TMEMs
+        else mma_commit_one(accf0 + 8 * acc);
         if (++acc == 2) acc = 0, acc_phase ^= 1;
       }
       if (*abort_flag && issued) {
         // wait for the outstanding MMAs before TMEM is released
-        mma_commit_pair(drain);
+        if constexpr (kPair) mma_commit_pair(drain);
+        else mma_commit_one(drain);
         (void)mbar_wait(drain, 0);
       }
     }
   } else {
-    // epilogue warps 2..9: TMEM lane quarter = warp % 4; warps 2-5 take
-    // columns 0-127 of the tile, warps 6-9 columns 128-255
+    // epilogue warps: TMEM lane quarter = warp % 4; with 8 warps, warps 6-9
+    // take columns 128-255 of the tile
     const int quarter = warp & 3;
     const int half = kEpiWarps == 8 ? (warp - 2) >> 2 : 0;
     const int nch = kEpiWarps == 8 ? BN / 64 : BN / 32;  // column chunks per warp
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
-      const TileCoord tc = decode(P, t);
+      const TileCoord tc = decode<kRows>(P, t);
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
       tc_fence_after();
       const int sub = P.sub0[tc.c] + tc.mat;
       const DevSub &S = A.subs[sub];
       const EpiScalars e = epi_scalars(A, sub);
-      const int i0 = (2 * tc.tm + (int)crank) * BM + quarter * 32;
+      const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
       float *st = stage_base + (warp - 2) * kStageFloats;
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       // skip column chunks that hold nothing this warp writes
@@ -657,7 +710,10 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acce_lead0 + 8 * acc);  // this warp is done with `acc`
+      if (lane == 0) {  // this warp is done with accumulator `acc`
+        if constexpr (kPair) mbar_arrive_cluster(acce_lead0 + 8 * acc);
+        else mbar_arrive(acce0 + 8 * acc);
+      }
       if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
   }
@@ -665,10 +721,14 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // no copy or remote arrive may target an exited CTA
+  if constexpr (kPair) cluster_sync();  // no copy or remote arrive may target an exited CTA
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
-                 : "memory");
+    if constexpr (kPair)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                   : "memory");
   }
 }
 
@@ -711,30 +771,40 @@ bool encode_map(CUtensorMap *map, void *base, int64_t cols, int64_t rows, int64_
 
 }  // namespace
 
+// Matrices of at most 128 oriented rows run in single mode; larger ones in
+// pairs.
+bool single_mode(int p) { return p <= BM; }
+
 double tc_executed_flops(int p, int q, bool square) {
-  // work items are pairs of 128-row tiles: an odd tile-row count runs one
-  // all-padding tile in the last pair
-  const int pair_rows = ((p + BM - 1) / BM + 1) / 2;
+  // work items are kRows consecutive 128-row tiles; in pair mode an odd
+  // tile-row count runs one all-padding tile in the last pair
+  const int rows = single_mode(p) ? 1 : 2;
+  const int items_m = ((p + BM - 1) / BM + rows - 1) / rows;
   const int tiles_n_sym = (p + BN - 1) / BN;
-  int64_t sym_pairs = 0;
-  for (int pr = 0; pr < pair_rows; ++pr) sym_pairs += std::max(0, tiles_n_sym - tri_tn_min(2 * pr));
+  int64_t sym_items = 0;
+  for (int r = 0; r < items_m; ++r) sym_items += std::max(0, tiles_n_sym - tri_tn_min(rows * r));
   const double kq = (double)((q + BK - 1) / BK) * BK;   // Gram: K = q
   const double kp = (double)((p + BK - 1) / BK) * BK;   // square and product: K = p
-  const double pair = 2.0 * 2.0 * BM * BN;              // two 128 x 256 tiles, 2 FLOPs per MAC
-  double f = sym_pairs * pair * kq;                       // Gram
-  if (square) f += sym_pairs * pair * kp;                 // A A
-  f += (double)pair_rows * ((q + BN - 1) / BN) * pair * kp; // product
+  const double item = 2.0 * rows * BM * BN;             // MACs x 2 per item and unit K
+  double f = sym_items * item * kq;                       // Gram
+  if (square) f += sym_items * item * kp;                 // A A
+  f += (double)items_m * ((q + BN - 1) / BN) * item * kp; // product
   return f;
 }
 
-int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args, int sm_count,
-                      void *stream) {
+namespace {
+
+template <bool kPair>
+int launch_mode(const ShapeClass *const *classes, int32_t n_classes, const PhaseArgs &args, int sm_count,
+                void *stream) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(ns_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err = cudaFuncSetAttribute(ns_gemm_tc_kernel<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemBytes);
   });
   if (attr_err != cudaSuccess) return (int)attr_err;
+  constexpr int kRows = Mode<kPair>::kRows;
   const bool gram = (args.mode == kGram || args.mode == kGramA);
   const bool square = (args.mode == kSquare);
   for (int32_t c0 = 0; c0 < n_classes; c0 += kMaxClassesPerLaunch) {
@@ -745,7 +815,7 @@ int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseA
     T.tri = (gram || square) ? 1 : 0;
     T.tile_start[0] = 0;
     for (int k = 0; k < T.n; ++k) {
-      const ShapeClass &C = classes[c0 + k];
+      const ShapeClass &C = *classes[c0 + k];
       char *xin = static_cast<char *>(args.x_in) + C.x_base * 2;
       char *pb = static_cast<char *>(args.pbuf) + C.p_base * 2;
       char *ab = static_cast<char *>(args.abuf) + C.p_base * 2;
@@ -771,46 +841,71 @@ int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseA
       T.tiles_n[k] = (Ndim + BN - 1) / BN;
       T.k_iters[k] = (Kdim + BK - 1) / BK;
       T.sub0[k] = C.sub0;
-      const int pair_rows = ((C.p + BM - 1) / BM + 1) / 2;
+      const int items_m = ((C.p + BM - 1) / BM + kRows - 1) / kRows;
       if (T.tri) {
         int cnt = 0;
-        for (int pr = 0; pr < pair_rows; ++pr) cnt += std::max(0, T.tiles_n[k] - tri_tn_min(2 * pr));
+        for (int r = 0; r < items_m; ++r) cnt += std::max(0, T.tiles_n[k] - tri_tn_min(kRows * r));
         T.tiles_per_mat[k] = cnt;
       } else {
-        T.tiles_per_mat[k] = pair_rows * T.tiles_n[k];
+        T.tiles_per_mat[k] = items_m * T.tiles_n[k];
       }
       T.tile_start[k + 1] = T.tile_start[k] + (int64_t)C.count * T.tiles_per_mat[k];
     }
     const int64_t total = T.tile_start[T.n];
     if (total == 0) continue;
-    // persistent grid: as many CTA pairs as can be resident at once
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static std::once_flag occ_once;
-    static int max_clusters = 0;
-    std::call_once(occ_once, [&] {
-      cfg.gridDim = dim3(2 * std::max(1, sm_count / 2));
-      if (cudaOccupancyMaxActiveClusters(&max_clusters, ns_gemm_tc_kernel, &cfg) != cudaSuccess)
-        max_clusters = 0;
-    });
-    const int clusters = (int)std::min<int64_t>(total, max_clusters > 0 ? max_clusters : std::max(1, sm_count / 2));
-    cfg.gridDim = dim3(2 * clusters);
-    const cudaError_t lerr = cudaLaunchKernelEx(&cfg, ns_gemm_tc_kernel, T, args);
+    if constexpr (kPair) {
+      // persistent grid: as many CTA pairs as can be resident at once
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      static std::once_flag occ_once;
+      static int max_clusters = 0;
+      std::call_once(occ_once, [&] {
+        cfg.gridDim = dim3(2 * std::max(1, sm_count / 2));
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, ns_gemm_tc_kernel<true>, &cfg) != cudaSuccess)
+          max_clusters = 0;
+      });
+      const int clusters =
+          (int)std::min<int64_t>(total, max_clusters > 0 ? max_clusters : std::max(1, sm_count / 2));
+      cfg.gridDim = dim3(2 * clusters);
+    } else {
+      cfg.gridDim = dim3((unsigned)std::min<int64_t>(total, sm_count));  // one CTA per SM
+    }
+    const cudaError_t lerr = cudaLaunchKernelEx(&cfg, ns_gemm_tc_kernel<kPair>, T, args);
     if (lerr != cudaSuccess) return (int)lerr;
     count_launches(1);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return (int)err;
   }
   return 0;
+}
+
+}  // namespace
+
+int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args, int sm_count,
+                      void *stream) {
+  const ShapeClass *single[4096], *pair[4096];
+  int ns = 0, np = 0;
+  for (int32_t c = 0; c < n_classes; ++c) {
+    if (single_mode(classes[c].p)) {
+      if (ns == 4096) return (int)cudaErrorInvalidValue;
+      single[ns++] = &classes[c];
+    } else {
+      if (np == 4096) return (int)cudaErrorInvalidValue;
+      pair[np++] = &classes[c];
+    }
+  }
+  int err = launch_mode<true>(pair, np, args, sm_count, stream);
+  if (err) return err;
+  return launch_mode<false>(single, ns, args, sm_count, stream);
 }
 
 }  // namespace gbo

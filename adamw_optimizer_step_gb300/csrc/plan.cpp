@@ -293,9 +293,16 @@ int validate_and_expand(gbo_plan *P) {
   // momentum tiles and NorMuon row blocks, in table order of subs
   int64_t tiles = 0, rbs = 0;
   for (DevSub &S : subs) {
-    S.tiles_c = (S.n + kMomTile - 1) / kMomTile;
+    // A matrix that is not transposed is one contiguous block of its weight
+    // (views split rows only), and so is its X when ld == n: its momentum
+    // tiles are flat runs of 4096 elements.  Tall matrices use 64 x 64 tiles
+    // transposed through shared memory.
+    const bool flat = !S.transposed && S.vec_ok && S.ld == S.n;
+    S.tiles_c = flat ? 0 : (S.n + kMomTile - 1) / kMomTile;
+    S.ntiles = flat ? (int32_t)(((int64_t)S.m * S.n + kMomFlat - 1) / kMomFlat)
+                    : ((S.m + kMomTile - 1) / kMomTile) * S.tiles_c;
     S.tile0 = tiles;
-    tiles += (int64_t)((S.m + kMomTile - 1) / kMomTile) * S.tiles_c;
+    tiles += S.ntiles;
     S.rb0 = rbs;
     rbs += (S.m + kRowBlock - 1) / kRowBlock;
   }
@@ -365,7 +372,11 @@ int launch_gemm(const gbo_plan *P, const PhaseArgs &args, void *stream) {
 }
 
 int64_t gemm_launches(const gbo_plan *P) {
-  return (int64_t)((P->classes.size() + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch);
+  auto groups = [](int64_t n) { return (n + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch; };
+  if (P->x_dtype != GBO_BF16) return groups((int64_t)P->classes.size());
+  int64_t single = 0;
+  for (const ShapeClass &C : P->classes) single += single_mode(C.p) ? 1 : 0;
+  return groups(single) + groups((int64_t)P->classes.size() - single);
 }
 
 cudaEvent_t take_event(gbo_plan *P) {
