@@ -10,7 +10,7 @@ namespace gbo {
 
 constexpr int kMomTile = 64;        // momentum tiles: 64 x 64 elements of a matrix, or
 constexpr int kMomFlat = kMomTile * kMomTile;  // 4096 consecutive elements of a matrix
-constexpr int kRowBlock = 32;       // NorMuon: stored rows per block
+constexpr int kRowBlock = 64;       // NorMuon: stored rows per block
 constexpr int kMaxClassesPerLaunch = 8;
 
 // One independent matrix (a view block or split range of a stored weight),

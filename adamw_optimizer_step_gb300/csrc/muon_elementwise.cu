@@ -258,18 +258,71 @@ prenorm_finalize_kernel(const DevSub *__restrict__ subs, const float *__restrict
   }
 }
 
+// Eight consecutive fp32 values from X (bf16 or fp32 workspace): 16-byte
+// loads when the segment is whole (the workspace rows are 16-element
+// aligned), else element by element.
+template <typename XT>
+__device__ __forceinline__ void load8x(const XT *src, int valid, float *out) {
+  if (valid == 8) {
+    if constexpr (sizeof(XT) == 2) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
+        out[2 * h] = __low2float(b);
+        out[2 * h + 1] = __high2float(b);
+      }
+    } else {
+      const float4 a = reinterpret_cast<const float4 *>(src)[0], b = reinterpret_cast<const float4 *>(src)[1];
+      out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+      out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if constexpr (sizeof(XT) == 2) out[e] = e < valid ? __bfloat162float(src[e]) : 0.f;
+      else out[e] = e < valid ? src[e] : 0.f;
+    }
+  }
+}
+
+// W[widx .. widx + valid) <- W - lrm * (wd * W + f * o), and the update f * o
+// to dbg; 16-byte accesses when `vec` and the segment is whole.
+__device__ __forceinline__ void weight_rmw8(const DevSub &S, int64_t widx, int valid, bool vec, float lrm, float f,
+                                            const float *o, float *dbg) {
+  float w[8], u[8];
+  load8(S.w, S.w_dtype, widx, valid, vec, w);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    u[e] = f * o[e];
+    w[e] = w[e] - lrm * (S.wd * w[e] + u[e]);
+  }
+  if (S.w_dtype == GBO_BF16) store8(reinterpret_cast<__nv_bfloat16 *>(S.w) + widx, w, valid, vec);
+  else store8(reinterpret_cast<float *>(S.w) + widx, w, valid, vec);
+  if (dbg) {
+    float *d = dbg + S.dbg_off + widx;
+    store8(d, u, valid, (reinterpret_cast<uintptr_t>(d) & 15) == 0);
+  }
+}
+
 // NorMuon rows of the plan's matrices: one block of 256 threads per
 // kRowBlock stored rows of one matrix.  O (the unscaled orthogonalised
-// update) is read from the workspace; for a transposed matrix stored row i
-// is column i of X.  Row statistics, v update, then the weight write.
+// update) is read from the workspace.  Row statistics, v update, then the
+// weight write, with 16-byte accesses throughout.
+//   untransposed: warp w takes stored rows w, w + 8, ... of the block; a
+//     row is X's row, read twice (statistics, then the write)
+//   transposed: stored row i is column i of X; the block reads 32 x 64
+//     tiles of X (8 threads per 64-column row segment), keeps per-column
+//     sums, then transposes tiles through shared memory for the write
 template <typename XT>
 __global__ void __launch_bounds__(256)
 normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_blocks,
                     const XT *__restrict__ xbuf, float beta2, float eps, float lr,
                     float *__restrict__ dbg, int32_t *status) {
-  __shared__ float tileT[32][33];
-  __shared__ float part[8][32];
-  __shared__ float rinv[32];
+  __shared__ float tileT[32][kRowBlock + 1];
+  __shared__ float colsum[32][kRowBlock + 1];
+  __shared__ float rfac[kRowBlock];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
     const int si = find_owner(b, n_subs, [&](int k) { return subs[k].rb0; });
@@ -277,80 +330,83 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
     const int i0 = (int)(b - S.rb0) * kRowBlock;
     const int nrows = min(kRowBlock, S.m - i0);
     const XT *X = xbuf + S.x_off;
-    auto xval = [&](int i, int j) -> float {  // O[i][j] in stored orientation
-      const int64_t idx = S.transposed ? (int64_t)j * S.ld + i : (int64_t)i * S.ld + j;
-      if constexpr (sizeof(XT) == 2) return __bfloat162float(X[idx]);
-      else return X[idx];
-    };
-    // 1) sum of squares per row
+    const float lrm = lr * S.lr_mult;
+    const bool wvec = S.w_vec != 0;
     if (!S.transposed) {
       for (int r = warp; r < nrows; r += 8) {
+        const int row = i0 + r;
+        const XT *xr = X + (int64_t)row * S.ld;
         float ss = 0.f;
-        for (int j = lane; j < S.n; j += 32) {
-          const float o = xval(i0 + r, j);
-          ss = fmaf(o, o, ss);
+        for (int j = lane * 8; j < S.n; j += 256) {
+          float o[8];
+          load8x(xr + j, min(8, S.n - j), o);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss = fmaf(o[e], o[e], ss);
         }
         ss = warp_sum(ss);
-        if (lane == 0) part[0][r] = ss;
-      }
-      __syncthreads();
-    } else {
-      float ss = 0.f;
-      if (lane < nrows)
-        for (int j = warp; j < S.n; j += 8) {
-          const float o = xval(i0 + lane, j);
-          ss = fmaf(o, o, ss);
+        const int64_t vrow = S.r0 + row;
+        const float v = beta2 * S.row_v[vrow] + (1.0f - beta2) * (ss / (float)S.n);
+        const float f = S.scale / (sqrtf(v) + eps);
+        if (!isfinite(f)) flag_status(status, GBO_STATUS_NONFINITE);
+        __syncwarp();
+        if (lane == 0) S.row_v[vrow] = v;
+        for (int j = lane * 8; j < S.n; j += 256) {
+          const int valid = min(8, S.n - j);
+          float o[8];
+          load8x(xr + j, valid, o);
+          weight_rmw8(S, vrow * S.cols + j, valid, wvec, lrm, f, o, dbg);
         }
-      part[warp][lane] = ss;
-      __syncthreads();
-      if (warp == 0) {
-        float t = 0.f;
+      }
+    } else {
+      const int cg = threadIdx.x & 7, rr = threadIdx.x >> 3;  // 8 columns x 32 rows of X per pass
+      const int c = i0 + cg * 8;                                // first X column (stored row)
+      const int cvalid = max(0, min(8, i0 + nrows - c));
+      float acc[8];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) t += part[w][lane];
-        part[0][lane] = t;
-      }
-      __syncthreads();
-    }
-    // 2) second moment and the row factor
-    if (threadIdx.x < nrows) {
-      const int64_t row = S.r0 + i0 + threadIdx.x;
-      const float ms = part[0][threadIdx.x] / (float)S.n;
-      const float v = beta2 * S.row_v[row] + (1.0f - beta2) * ms;
-      S.row_v[row] = v;
-      const float f = S.scale / (sqrtf(v) + eps);
-      if (!isfinite(f)) flag_status(status, GBO_STATUS_NONFINITE);
-      rinv[threadIdx.x] = f;
-    }
-    __syncthreads();
-    // 3) weight write, coalesced along stored rows
-    const float lrm = lr * S.lr_mult;
-    if (!S.transposed) {
-      for (int r = warp; r < nrows; r += 8) {
-        const int64_t wrow = (S.r0 + i0 + r) * S.cols;
-        for (int j = lane; j < S.n; j += 32) {
-          const float u = rinv[r] * xval(i0 + r, j);
-          const float w = ld_elem(S.w, S.w_dtype, wrow + j);
-          st_elem(S.w, S.w_dtype, wrow + j, w - lrm * (S.wd * w + u));
-          if (dbg) dbg[S.dbg_off + wrow + j] = u;
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int j = rr; j < S.n; j += 32) {
+        if (cvalid > 0) {
+          float o[8];
+          load8x(X + (int64_t)j * S.ld + c, cvalid, o);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = fmaf(o[e], o[e], acc[e]);
         }
       }
-    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) colsum[rr][cg * 8 + e] = acc[e];
+      __syncthreads();
+      if (threadIdx.x < nrows) {
+        float ss = 0.f;
+        for (int k = 0; k < 32; ++k) ss += colsum[k][threadIdx.x];  // fixed order
+        const int64_t vrow = S.r0 + i0 + threadIdx.x;
+        const float v = beta2 * S.row_v[vrow] + (1.0f - beta2) * (ss / (float)S.n);
+        S.row_v[vrow] = v;
+        const float f = S.scale / (sqrtf(v) + eps);
+        if (!isfinite(f)) flag_status(status, GBO_STATUS_NONFINITE);
+        rfac[threadIdx.x] = f;
+      }
+      __syncthreads();
+      // write: stored rows i0 + k (k < nrows), stored columns j0 .. j0 + 31
+      const int k = threadIdx.x >> 2, seg = threadIdx.x & 3;  // 64 rows x 4 segments of 8
       for (int j0 = 0; j0 < S.n; j0 += 32) {
-        // tileT[c][r] = O[i0 + r][j0 + c] read along X rows (coalesced)
-        for (int c = warp; c < 32; c += 8) {
-          const int j = j0 + c;
-          tileT[c][lane] = (j < S.n && lane < nrows) ? xval(i0 + lane, j) : 0.f;
+        {
+          const int j = j0 + rr;
+          float o[8];
+          if (j < S.n && cvalid > 0) load8x(X + (int64_t)j * S.ld + c, cvalid, o);
+          else
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) tileT[rr][cg * 8 + e] = o[e];
         }
         __syncthreads();
-        for (int r = warp; r < nrows; r += 8) {
-          const int j = j0 + lane;
-          if (j < S.n) {
-            const int64_t widx = (S.r0 + i0 + r) * S.cols + j;
-            const float u = rinv[r] * tileT[lane][r];
-            const float w = ld_elem(S.w, S.w_dtype, widx);
-            st_elem(S.w, S.w_dtype, widx, w - lrm * (S.wd * w + u));
-            if (dbg) dbg[S.dbg_off + widx] = u;
-          }
+        const int jc = j0 + seg * 8;
+        const int valid = max(0, min(8, S.n - jc));
+        if (k < nrows && valid > 0) {
+          float o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = tileT[seg * 8 + e][k];
+          weight_rmw8(S, (S.r0 + i0 + k) * S.cols + jc, valid, wvec, lrm, rfac[k], o, dbg);
         }
         __syncthreads();
       }

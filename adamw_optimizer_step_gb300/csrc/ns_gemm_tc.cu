@@ -430,6 +430,32 @@ __device__ __forceinline__ void weight_rmw32(const PhaseArgs &A, const DevSub &S
   }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Bring into L2 the weight elements the last product's epilogue of this
+// warp will read-modify-write for the tile at (i0.., col0 .. col0 + BN): the
+// warp issues them while it waits for the tile's accumulator.
+__device__ __forceinline__ void prefetch_weight_tile(const DevSub &S, int i0, int col0, int lane) {
+  const int64_t es = S.w_dtype == GBO_BF16 ? 2 : 4;
+  const char *w = static_cast<const char *>(S.w);
+  if (!S.transposed) {
+    const int i = i0 + lane;  // stored row r0 + i, stored columns col0 ..
+    if (i >= S.p) return;
+    const int c1 = min(S.q, col0 + BN);
+    for (int c = col0; c < c1; c += (int)(128 / es))
+      prefetch_l2(w + ((S.r0 + i) * S.cols + c) * es);
+  } else {
+    if (i0 >= S.p) return;   // stored rows r0 + col0 + k, stored columns i0 .. i0 + 31
+#pragma unroll
+    for (int j = 0; j < BN / 32; ++j) {
+      const int c = col0 + lane + 32 * j;
+      if (c < S.q) prefetch_l2(w + ((S.r0 + c) * S.cols + i0) * es);
+    }
+  }
+}
+
 // Epilogue of one warp's 32 rows x 32 columns of the accumulator.  Lane r
 // holds row i0 + r in v[0..31] (columns col0 .. col0 + 31).
 __device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const DevSub &S, const EpiScalars &e, int i0,
@@ -690,10 +716,12 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     uint32_t acc_phase = 0;
     for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
       const TileCoord tc = decode<kRows>(P, t);
-      if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
-      tc_fence_after();
       const int sub = P.sub0[tc.c] + tc.mat;
       const DevSub &S = A.subs[sub];
+      if (A.mode == kFinal)
+        prefetch_weight_tile(S, (kRows * tc.tm + (int)crank) * BM + quarter * 32, tc.tn * BN, lane);
+      if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
+      tc_fence_after();
       const EpiScalars e = epi_scalars(A, sub);
       const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
       float *st = stage_base + (warp - 2) * kStageFloats;
