@@ -102,6 +102,7 @@ def lib():
                                             c_void_p, c_void_p]),
         "gbo_adamw_step": (c_int32, [ctypes.POINTER(AdamWDesc), c_int32, ctypes.POINTER(AdamWOpts), c_void_p,
                                      c_void_p, c_void_p]),
+        "gbo_testing_wait_timeout": (c_int32, [c_void_p, ctypes.c_uint32, c_void_p]),
         "gbo_last_error": (ctypes.c_char_p, []),
         "gbo_abi_version": (c_int32, []),
         "gbo_struct_size": (c_size_t, [c_int32]),
@@ -350,6 +351,11 @@ def gbo_abi_version():
 
 def gbo_struct_size(which):
     return int(lib().gbo_struct_size(which))
+
+
+def gbo_testing_wait_timeout(dev_status, limit_us, stream=None):
+    """Test hook: the GEMM's bounded wait on a barrier nothing arrives on."""
+    _check(lib().gbo_testing_wait_timeout(_dev_ptr(dev_status, "dev_status"), int(limit_us), _stream(stream)))
 
 
 def gbo_launch_count():

@@ -112,6 +112,8 @@ double tc_executed_flops(int p, int q, bool square);
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);
+// Testing: the GEMM's bounded mbarrier wait on a barrier nothing arrives on.
+int launch_wait_timeout(int32_t *status, uint64_t limit_ns, void *stream);
 
 void count_launches(uint64_t n);
 

@@ -119,15 +119,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity to complete: gives up
+// (returns false) after `limit_ns` of the global timer.
+__device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t spin = 0;; ++spin) {
     if (mbar_try(bar, parity)) return true;
-    if ((spin & 255u) == 255u && global_ns() - t0 > kWaitNs) return false;
+    if ((spin & 255u) == 255u && global_ns() - t0 > limit_ns) return false;
   }
 }
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_ns(bar, parity, kWaitNs); }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x,
                                             int y, int z) {
@@ -917,6 +920,28 @@ int launch_mode(const ShapeClass *const *classes, int32_t n_classes, const Phase
 }
 
 }  // namespace
+
+namespace {
+
+// The bounded wait of the Newton-Schulz kernel, on an mbarrier that nothing
+// arrives on: it must give up after `limit_ns`, flag the time-out and
+// return, leaving the context usable.
+__global__ void wait_timeout_kernel(int32_t *status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (!mbar_wait_ns(b, 0, limit_ns)) flag_status(status, GBO_STATUS_TIMEOUT);
+}
+
+}  // namespace
+
+int launch_wait_timeout(int32_t *status, uint64_t limit_ns, void *stream) {
+  wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+  count_launches(1);
+  return (int)cudaGetLastError();
+}
 
 int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args, int sm_count,
                       void *stream) {

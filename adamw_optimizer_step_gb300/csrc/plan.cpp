@@ -16,6 +16,7 @@
 #include <atomic>
 
 #include "gbo.h"
+#include "gbo_testing.h"
 #include "internal.h"
 
 namespace gbo {
@@ -635,6 +636,18 @@ int gbo_normuon_rownorm(const float *O, int64_t rows, int64_t cols, float *row_v
   const int err = launch_normuon_rownorm_plain(O, rows, cols, row_v, w, w_dtype, beta2, eps, scale, lr,
                                                wd, dbg_update, stream);
   if (err) return cuda_fail(err, "NorMuon rownorm kernel");
+  return ok();
+}
+
+int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream) {
+  if (!dev_status || !aligned(dev_status, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_status is NULL or misaligned");
+  if (limit_us == 0 || limit_us > 10000000u) return fail(GBO_ERR_INVALID_ARG, "limit_us must be in 1..10^7");
+  int dev;
+  DeviceInfo di;
+  int rc = current_device(&dev, &di);
+  if (rc != GBO_OK) return rc;
+  const int err = launch_wait_timeout(dev_status, (uint64_t)limit_us * 1000u, stream);
+  if (err) return cuda_fail(err, "wait time-out kernel");
   return ok();
 }
 

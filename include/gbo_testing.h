@@ -1,0 +1,30 @@
+/*
+ * gbo_testing.h -- test hooks of libgbo.so.  These are not part of the
+ * optimizer (the source pages have no counterpart); they let tests exercise
+ * the library's failure handling without faulting or hanging a GPU.
+ */
+#ifndef GBO_TESTING_H
+#define GBO_TESTING_H
+
+#include "gbo.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Launch one thread that runs the Newton-Schulz kernel's bounded mbarrier
+ * wait on a barrier nothing ever arrives on, with a limit of `limit_us`
+ * microseconds instead of the kernel's 2 s.  The wait gives up, ORs
+ * GBO_STATUS_TIMEOUT into *dev_status (device int32) and the kernel returns;
+ * the CUDA context stays usable.  Asynchronous on `stream`.
+ * Errors: INVALID_ARG (NULL/misaligned status, limit outside 1..10^7 us),
+ * UNSUPPORTED, CUDA.
+ */
+int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBO_TESTING_H */
