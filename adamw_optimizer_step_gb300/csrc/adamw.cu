@@ -134,7 +134,10 @@ __device__ __forceinline__ void adam_elem(float &p, float g, float &m, float &v,
   p = p - s.lr * s.wd * p - s.step_size * (m / denom);
 }
 
-__global__ void __launch_bounds__(kThreads)
+#ifndef GBO_ADAM_MIN_BLOCKS
+#define GBO_ADAM_MIN_BLOCKS 1  // compiler choice (58 regs, 4 blocks/SM): measured faster than forcing 5 or 6
+#endif
+__global__ void __launch_bounds__(kThreads, GBO_ADAM_MIN_BLOCKS)
 adamw_kernel(const __grid_constant__ AdamTable T, const __grid_constant__ AdamScalars s,
              const float *__restrict__ coef_ptr) {
   const float coef = coef_ptr ? __ldg(coef_ptr) : 1.0f;
