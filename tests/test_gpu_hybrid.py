@@ -1,0 +1,91 @@
+"""The HybridOptimizer front end on a toy model: one step through the
+library matches the oracle route by route, and its state round-trips."""
+
+import copy
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.views import sub_matrices
+from tests.parity import TOL, f64, ulp
+from tests.test_routing import Toy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from adamw_optimizer_step_gb300 import build, _binding as B
+    build.build()
+    B.lib()
+
+
+def make_model(seed):
+    torch.manual_seed(seed)
+    m = Toy().cuda()
+    for p in m.parameters():
+        if p.requires_grad:
+            p.grad = torch.randn_like(p) * 1e-2
+    return m
+
+
+def test_hybrid_step_matches_oracle():
+    from adamw_optimizer_step_gb300.routing import HybridOptimizer
+    model = make_model(1)
+    before = {n: (p.detach().clone(), p.grad.clone()) for n, p in model.named_parameters() if p.requires_grad}
+    opt = HybridOptimizer(model, muon_lr=0.02, adamw_lr=1e-3, weight_decay=0.1, precision="bf16")
+    norm = opt.step()
+    torch.cuda.synchronize()
+    assert int(opt.status.item()) == 0
+    adam_grads = [f64(before[r.name][1]) for r in opt.adamw]
+    N = oracle.global_grad_norm(adam_grads)
+    assert abs(float(norm.item()) - N) <= 1e-6 * N
+    c = oracle.clip_coefficient(N, 1.0)
+    for r in opt.routes:
+        W0, G = (f64(t) for t in before[r.name])
+        got = f64(r.param.detach())
+        if r.algorithm == "muon":
+            Wn, _, _, U = oracle.muon_step_tensor(W0, G, np.zeros_like(G), view=r.view, split=r.split,
+                                                  lr=0.02, wd=r.weight_decay)
+            for r0, m, n in sub_matrices(W0.shape[0], W0.shape[1], r.view, r.split):
+                sl = slice(r0, r0 + m)
+                bound = (np.linalg.norm(ulp(Wn[sl], torch.float32)) + 0.02 * TOL["bf16"] * np.linalg.norm(U[sl])
+                         + 1e-6 * np.linalg.norm(W0[sl]))
+                assert np.linalg.norm(got[sl] - Wn[sl]) <= bound, r.name
+        else:
+            pn, _, _ = oracle.adamw_update(W0, G, np.zeros_like(G), np.zeros_like(G), coef=c, lr=1e-3,
+                                           wd=r.weight_decay, t=1)
+            assert np.max(np.abs(got - pn) - (1e-6 * 1e-3 + 2 ** -23 * np.abs(pn))) <= 0, r.name
+
+
+def test_hybrid_state_round_trip():
+    """Step, save, restore into a fresh optimizer on a copy of the model,
+    step both: bitwise equal parameters."""
+    from adamw_optimizer_step_gb300.routing import HybridOptimizer
+    a = make_model(2)
+    opt_a = HybridOptimizer(a, muon_lr=0.02, adamw_lr=1e-3)
+    opt_a.step()
+    sd = opt_a.state_dict()
+    b = copy.deepcopy(a)
+    for pa, pb in zip(a.parameters(), b.parameters()):
+        if pa.requires_grad:
+            pb.grad = pa.grad.clone()
+    opt_b = HybridOptimizer(b, muon_lr=0.02, adamw_lr=1e-3)
+    opt_b.load_state_dict(sd)
+    opt_a.step()
+    opt_b.step()
+    torch.cuda.synchronize()
+    for (na, pa), (nb, pb) in zip(a.named_parameters(), b.named_parameters()):
+        assert torch.equal(pa, pb), na
+    # a different Muon layout is refused
+    c = Toy().cuda()
+    c.ffn.intermediate_size = 8  # gate_up viewed (2, 8, 8) would not flatten -> use another layout
+    c.ffn.gate_up_proj = torch.nn.Linear(8, 16, bias=False).cuda()
+    for p in c.parameters():
+        if p.requires_grad:
+            p.grad = torch.zeros_like(p)
+    opt_c = HybridOptimizer(c)
+    with pytest.raises(ValueError):
+        opt_c.load_state_dict(sd)
