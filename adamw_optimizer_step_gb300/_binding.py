@@ -18,6 +18,9 @@ GBO_F32 = 0
 GBO_BF16 = 1
 GBO_NS_BF16 = 0
 GBO_NS_F32 = 1
+GBO_ROUTE_AUTO = 0
+GBO_ROUTE_X = 1
+GBO_ROUTE_GRAM = 2
 GBO_STATUS_NONFINITE = 1
 GBO_STATUS_TIMEOUT = 2
 GBO_MAX_VIEW_DIMS = 6
@@ -46,7 +49,7 @@ class MuonOpts(ctypes.Structure):
     _fields_ = [("abc", ctypes.POINTER(c_float)), ("mu", c_float), ("beta2", c_float),
                 ("eps", c_float), ("nesterov", c_int32), ("ns_steps", c_int32),
                 ("abc_per_step", c_int32), ("precision", c_int32), ("normuon", c_int32),
-                ("reserved", c_int32)]
+                ("route", c_int32)]
 
 
 class Tensor(ctypes.Structure):
@@ -66,7 +69,8 @@ class AdamWOpts(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("n_weights", c_int64), ("n_active", c_int64), ("n_matrices", c_int64),
                 ("n_shape_classes", c_int64), ("muon_params", c_int64), ("ns_flops", ctypes.c_double),
-                ("ns_flops_executed", ctypes.c_double), ("launches_per_step", c_int64)]
+                ("ns_flops_executed", ctypes.c_double), ("launches_per_step", c_int64),
+                ("n_gram_route", c_int64)]
 
 
 _STRUCTS = (MuonDesc, MuonOpts, Tensor, AdamWDesc, AdamWOpts, PlanInfo)
@@ -212,8 +216,9 @@ def muon_desc_table(entries):
 
 
 def gbo_muon_plan_create(entries, *, abc=(1.5, -0.5, 0.0), ns_steps=5, mu=0.95, nesterov=True,
-                         precision=GBO_NS_BF16, normuon=False, beta2=0.95, eps=1e-8):
-    """Validate a Muon table and build a plan (``abc``: one triple or one per step)."""
+                         precision=GBO_NS_BF16, normuon=False, beta2=0.95, eps=1e-8, route=GBO_ROUTE_AUTO):
+    """Validate a Muon table and build a plan (``abc``: one triple or one per step;
+    ``route``: GBO_ROUTE_AUTO, GBO_ROUTE_X or GBO_ROUTE_GRAM)."""
     L = lib()
     arr, pool, keep = muon_desc_table(entries)
     flat = []
@@ -222,7 +227,7 @@ def gbo_muon_plan_create(entries, *, abc=(1.5, -0.5, 0.0), ns_steps=5, mu=0.95, 
     per_step = len(flat) > 3
     cabc = (c_float * len(flat))(*flat)
     opts = MuonOpts(ctypes.cast(cabc, ctypes.POINTER(c_float)), mu, beta2, eps, int(bool(nesterov)),
-                    int(ns_steps), int(per_step), int(precision), int(bool(normuon)), 0)
+                    int(ns_steps), int(per_step), int(precision), int(bool(normuon)), int(route))
     cpool = (c_int64 * max(1, len(pool)))(*pool)
     out = c_void_p()
     _check(L.gbo_muon_plan_create(arr, len(entries), cpool, len(pool), ctypes.byref(opts), ctypes.byref(out)))

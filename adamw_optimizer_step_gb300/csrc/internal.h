@@ -43,18 +43,32 @@ struct DevSub {
   float lr_mult;
   float wd;
   int32_t w_vec;    // weight rows start on 16-byte boundaries (vector read-modify-write)
-  int32_t pad0;
+  int32_t x_sel;    // X buffer (0 or 1) that holds the last iterate (NorMuon rows read it)
 };
 
 // Matrices of one oriented shape (p, q), stored back to back in the
 // workspace so one 3-D TMA map covers all of them.
+//
+// Two routes to the same k-step result (bf16 mode):
+//   kRouteX     every iteration forms A = X X^T and X <- P X on the p x q
+//               iterate;
+//   kRouteGram  the iteration runs on p x p matrices only.  Every iterate is
+//               X_j = Q_j X_0 with Q_j a polynomial in A_0 = X_0 X_0^T, so
+//               A_{j+1} = P_j A_j P_j and Q_{j+1} = P_j Q_j are products of
+//               commuting symmetric matrices (upper triangle only), and the
+//               p x q product runs once, X_k = Q_k X_0.  Cheaper whenever
+//               q > p; used when every iteration has c == 0.
 struct ShapeClass {
   int32_t p, q, ld, ldp;
   int32_t count;  // matrices in the class
   int32_t sub0;   // index of the first matrix in the DevSub table
+  int32_t route;  // kRouteX | kRouteGram
+  int32_t pad0;
   int64_t x_base; // element offset of the class in each X buffer
-  int64_t p_base; // element offset of the class in the P / A buffers
+  int64_t p_base; // element offset of the class in its p x p buffers (its route's space)
 };
+
+enum NsRoute : int32_t { kRouteX = 0, kRouteGram = 1 };
 
 // Epilogue selector of the Newton-Schulz GEMMs.
 enum GemmMode : int32_t {
@@ -63,6 +77,29 @@ enum GemmMode : int32_t {
   kSquare = 2,    // C = A A;    write P = a I + b A + c C
   kProduct = 3,   // C = P X;    write X' = s C
   kFinal = 4,     // C = P X;    O = s C; update the weight (+ dbg)
+  kGramAP = 5,    // C symmetric; write A = s^2 C and P = a I + b A
+};
+
+// Operand shapes of one tensor-core GEMM job.
+enum GemmKind : int32_t {
+  kKindGram = 0,  // C = X X^T: A and B operands are rows of X (K = q), symmetric output
+  kKindSym = 1,   // C = L R, L and R symmetric p x p and commuting: symmetric output
+  kKindProd = 2,  // C = L X: L p x p, B = X with K along its rows (MN-major), p x q output
+};
+
+// One shape class of a tensor-core launch and what it computes.  Operand
+// and output pointers are region bases; the launcher adds the class base
+// (x-space for X operands, the class's p x p space otherwise) and the
+// epilogue adds each matrix's offset.
+struct GemmJob {
+  const ShapeClass *cls;
+  int32_t mode;   // GemmMode of the epilogue
+  int32_t kind;   // GemmKind
+  int32_t first;  // fold the pre-normalisation factor (s = alpha)
+  float a, b, c;
+  const void *opA, *opB;
+  void *out, *out2;  // out: P, A, T, Q or X'; out2: A of kGramAP
+  const void *aux;   // kSquare: the A matrix read by the epilogue
 };
 
 // Per-launch scalars of one Newton-Schulz phase.
@@ -90,8 +127,8 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
                             float *alpha, int32_t *status, void *stream);
 int launch_ns_gemm_simt(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args,
                         int sm_count, void *stream);
-int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x,
-                        int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
+int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
+                        const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
                         int32_t *status, int sm_count, void *stream);
 int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
                                  int32_t w_dtype, float beta2, float eps, float scale, float lr,
@@ -101,14 +138,18 @@ int launch_clip_norm(const gbo_tensor *grads, int32_t n, float max_norm, float *
 int launch_adamw(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *opts,
                  const float *coef, int32_t *status, int sm_count, void *stream);
 
-// tcgen05 path: host-side state for the tensor maps of one launch.
-struct TcLaunch;
-int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args,
-                      int sm_count, void *stream);
+// tcgen05 path: one Newton-Schulz step over a set of jobs (any mix of
+// classes and kinds).  `globals` supplies subs, alpha, lr, dbg and status.
+// Adds the number of kernel launches made to *n_launch.
+int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
+                      void *stream, int64_t *n_launch);
 // FLOPs the tensor-core kernel executes for one p x q matrix and one
 // iteration (Gram over the upper block-triangle of tiles, square when c != 0,
 // product), counting the zero padding of partial tiles.
 double tc_executed_flops(int p, int q, bool square);
+// FLOPs executed for one p x q matrix over k iterations on the Gram route:
+// the Gram, 3k - 3 symmetric p x p products, the product with X_0.
+double tc_gram_route_flops(int p, int q, int k);
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);

@@ -321,7 +321,7 @@ __device__ __forceinline__ void weight_rmw8(const DevSub &S, int64_t widx, int v
 template <typename XT>
 __global__ void __launch_bounds__(256)
 normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_blocks,
-                    const XT *__restrict__ xbuf, float beta2, float eps, float lr,
+                    const XT *__restrict__ xbuf0, const XT *__restrict__ xbuf1, float beta2, float eps, float lr,
                     float *__restrict__ dbg, int32_t *status) {
   __shared__ float tileT[32][kRowBlock + 1];
   __shared__ float colsum[32][kRowBlock + 1];
@@ -332,7 +332,7 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
     const DevSub &S = subs[si];
     const int i0 = (int)(b - S.rb0) * kRowBlock;
     const int nrows = min(kRowBlock, S.m - i0);
-    const XT *X = xbuf + S.x_off;
+    const XT *X = (S.x_sel ? xbuf1 : xbuf0) + S.x_off;  // the buffer holding the last iterate
     const float lrm = lr * S.lr_mult;
     const bool wvec = S.w_vec != 0;
     if (!S.transposed) {
@@ -490,19 +490,20 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
   return (int)cudaGetLastError();
 }
 
-int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x,
-                        int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
+int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
+                        const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
                         int32_t *status, int sm_count, void *stream) {
   if (n_row_blocks == 0) return 0;
   const int64_t grid = std::min<int64_t>(n_row_blocks, (int64_t)sm_count * 8);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (x_dtype == GBO_BF16)
     normuon_rows_kernel<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(
-        subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x), beta2, eps, lr, dbg,
-        status);
+        subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x0),
+        reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status);
   else
     normuon_rows_kernel<float><<<(unsigned)grid, 256, 0, st>>>(
-        subs, n_subs, n_row_blocks, reinterpret_cast<const float *>(x), beta2, eps, lr, dbg, status);
+        subs, n_subs, n_row_blocks, reinterpret_cast<const float *>(x0), reinterpret_cast<const float *>(x1),
+        beta2, eps, lr, dbg, status);
   count_launches(1);
   return (int)cudaGetLastError();
 }

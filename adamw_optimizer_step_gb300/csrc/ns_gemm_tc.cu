@@ -9,7 +9,9 @@
 // onto X whose last instance writes the weights.  Matrices of one oriented
 // shape are stored back to back, so one 3-D tensor map (columns, rows,
 // matrix) covers a whole shape class; out-of-range rows and columns of a
-// tile are zero-filled by TMA and masked in the epilogue.
+// tile are zero-filled by TMA and masked in the epilogue.  Each shape class
+// of a launch is a job with its own operands, output and epilogue, so one
+// launch may run X-route and Gram-route steps (see internal.h) side by side.
 //
 // Persistent, warp-specialised CTA (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane), STAGES-deep ring of A/B tiles
@@ -26,6 +28,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -69,6 +72,17 @@ constexpr int kSmemBytes = kRingBytes + 1024 /*align*/ + 256 /*barriers*/ + kEpi
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
+// What one class of a launch computes, as the kernel sees it.
+struct TcJob {
+  int32_t mode;   // GemmMode
+  int32_t kind;   // GemmKind: kKindProd has B = X MN-major and a full p x q output;
+                  // the others a symmetric p x p output (upper-triangle tiles only)
+  int32_t first;  // s = alpha of the matrix (pre-normalisation folded in), else 1
+  float a, b, c;
+  void *out, *out2;
+  const void *aux;
+};
+
 struct TcParams {
   CUtensorMap mapA[kMaxClassesPerLaunch];  // A operand, box 64 x 128
   CUtensorMap mapB[kMaxClassesPerLaunch];  // B operand, box 64 x 256 (K-major) or 64 x 64 (MN-major)
@@ -77,9 +91,8 @@ struct TcParams {
   int32_t k_iters[kMaxClassesPerLaunch];
   int32_t sub0[kMaxClassesPerLaunch];
   int32_t tiles_per_mat[kMaxClassesPerLaunch];
+  TcJob job[kMaxClassesPerLaunch];
   int32_t n;
-  int32_t b_mn_major;  // products: B = X with the K index along X's rows
-  int32_t tri;         // symmetric output: only tiles touching the upper triangle
 };
 
 // ---------------------------------------------------------------------------
@@ -311,7 +324,7 @@ __device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
   tc.mat = (int)(local / P.tiles_per_mat[c]);
   int rem = (int)(local % P.tiles_per_mat[c]);
   const int tn_all = P.tiles_n[c];
-  if (!P.tri) {
+  if (P.job[c].kind == kKindProd) {
     tc.tm = rem / tn_all;
     tc.tn = rem % tn_all;
   } else {
@@ -459,25 +472,47 @@ __device__ __forceinline__ void prefetch_weight_tile(const DevSub &S, int i0, in
   }
 }
 
+// Symmetric output: element (r, c) with r <= c is written directly and its
+// mirror (c, r) with r < c from the transposed block, so every element of
+// the p x p output is written exactly once by the tiles touching the upper
+// triangle.  `o` is destroyed (transposed in place).
+__device__ __forceinline__ void sym_store32(__nv_bfloat16 *out, const DevSub &S, int i0, int col0, float (&o)[32],
+                                            float *st, int lane) {
+  const int i = i0 + lane, p = S.p;
+  if (i < p) {  // direct: (i, j) with i <= j
+    const int jlo = max(i, col0);
+    const uint32_t mask = prefix_mask(p - col0) & ~prefix_mask(jlo - col0);
+    store_row32(out + (int64_t)i * S.ldp + col0, o, mask == 0xffffffffu, mask);
+  }
+  // mirror: lane l writes row col0 + l, columns i0 + r for i0 + r < col0 + l
+  warp_transpose32(o, st, lane);
+  const int jm = col0 + lane;
+  if (jm < p) {
+    const uint32_t mask = prefix_mask(p - i0) & prefix_mask(jm - i0);
+    store_row32(out + (int64_t)jm * S.ldp + i0, o, mask == 0xffffffffu, mask);
+  }
+}
+
 // Epilogue of one warp's 32 rows x 32 columns of the accumulator.  Lane r
-// holds row i0 + r in v[0..31] (columns col0 .. col0 + 31).
-__device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const DevSub &S, const EpiScalars &e, int i0,
+// holds row i0 + r in v[0..31] (columns col0 .. col0 + 31); s is the
+// matrix's folded pre-normalisation factor (1 unless the job folds it).
+__device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const TcJob &J, const DevSub &S, float s, int i0,
                                                int col0, float (&v)[32], float *st, int lane) {
   const int i = i0 + lane;
-  if (A.mode == kProduct) {
+  if (J.mode == kProduct) {
     if (i >= S.p) return;
     float o[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) o[k] = e.s * v[k];
-    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(A.x_out) + S.x_off + (int64_t)i * S.ld + col0;
+    for (int k = 0; k < 32; ++k) o[k] = s * v[k];
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(J.out) + S.x_off + (int64_t)i * S.ld + col0;
     store_row32(dst, o, col0 + 32 <= S.q, prefix_mask(S.q - col0));
     return;
   }
-  if (A.mode == kFinal) {
+  if (J.mode == kFinal) {
     // O = s * C; the update direction is scale * O
     float u[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) u[k] = S.scale * e.s * v[k];
+    for (int k = 0; k < 32; ++k) u[k] = S.scale * s * v[k];
     if (!S.transposed) {
       if (i >= S.p) return;
       const uint32_t mask = prefix_mask(S.q - col0);
@@ -494,45 +529,36 @@ __device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const DevSub 
     }
     return;
   }
-  // Gram-type (symmetric) outputs: P = a I + b s^2 C, A = s^2 C, or
-  // P = a I + b A + c C.  Only tiles touching the upper triangle run; each
-  // element (r, c) with r <= c is written here and its mirror (c, r) with
-  // r < c is written from the transposed block, so every element of the
-  // symmetric output is written exactly once.
-  __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(A.mode == kGramA ? A.abuf : A.pbuf) + S.p_off;
+  // symmetric outputs: P = a I + b s^2 C, A = s^2 C, both (kGramAP), or
+  // P = a I + b A + c C (kSquare)
+  __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(J.out) + S.p_off;
   const int p = S.p;
+  const float s2 = s * s;
   float o[32];
-  if (A.mode == kSquare) {
+  if (J.mode == kSquare) {
     float am[32];
     const bool full = i < p && col0 + 32 <= p;
     if (i < p)
-      load_row32(reinterpret_cast<const __nv_bfloat16 *>(A.abuf) + S.p_off + (int64_t)i * S.ldp + col0, am, full,
+      load_row32(reinterpret_cast<const __nv_bfloat16 *>(J.aux) + S.p_off + (int64_t)i * S.ldp + col0, am, full,
                  prefix_mask(p - col0));
     else
 #pragma unroll
       for (int k = 0; k < 32; ++k) am[k] = 0.f;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) o[k] = A.c * v[k] + A.b * am[k] + (i == col0 + k ? A.a : 0.f);
-  } else if (A.mode == kGram) {
-    const float bs2 = A.b * e.s2;
+    for (int k = 0; k < 32; ++k) o[k] = J.c * v[k] + J.b * am[k] + (i == col0 + k ? J.a : 0.f);
+  } else if (J.mode == kGram || J.mode == kGramAP) {
+    const float bs2 = J.b * s2;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) o[k] = bs2 * v[k] + (i == col0 + k ? A.a : 0.f);
+    for (int k = 0; k < 32; ++k) o[k] = bs2 * v[k] + (i == col0 + k ? J.a : 0.f);
   } else {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) o[k] = e.s2 * v[k];
+    for (int k = 0; k < 32; ++k) o[k] = s2 * v[k];
   }
-  // direct: (i, j) with i <= j
-  if (i < p) {
-    const int jlo = max(i, col0);                 // first column to write
-    const uint32_t mask = prefix_mask(p - col0) & ~prefix_mask(jlo - col0);
-    store_row32(out + (int64_t)i * S.ldp + col0, o, mask == 0xffffffffu, mask);
-  }
-  // mirror: lane l writes row col0 + l, columns i0 + r for i0 + r < col0 + l
-  warp_transpose32(o, st, lane);
-  const int jm = col0 + lane;
-  if (jm < p) {
-    const uint32_t mask = prefix_mask(p - i0) & prefix_mask(jm - i0);
-    store_row32(out + (int64_t)jm * S.ldp + i0, o, mask == 0xffffffffu, mask);
+  sym_store32(out, S, i0, col0, o, st, lane);
+  if (J.mode == kGramAP) {  // and A = s^2 C
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = s2 * v[k];
+    sym_store32(reinterpret_cast<__nv_bfloat16 *>(J.out2) + S.p_off, S, i0, col0, o, st, lane);
   }
 }
 
@@ -632,7 +658,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
             tma_load_3d_pair(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
             // this CTA's half of B: columns tn * BN + crank * BN / 2 ...
             const int n0 = tc.tn * BN + (int)crank * (BN / 2);
-            if (!P.b_mn_major) {
+            if (P.job[tc.c].kind != kKindProd) {
               tma_load_3d_pair(sb, &P.mapB[tc.c], fb, kb * BK, n0, tc.mat);
             } else {
 #pragma unroll
@@ -643,7 +669,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
             const uint32_t fb = full0 + 8 * stage;
             tma_load_3d(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
             const int n0 = tc.tn * BN;
-            if (!P.b_mn_major) {
+            if (P.job[tc.c].kind != kKindProd) {
 #pragma unroll
               for (int h = 0; h < 2; ++h)
                 tma_load_3d(sb + h * B_HALF, &P.mapB[tc.c], fb, kb * BK, n0 + h * (BN / 2), tc.mat);
@@ -664,7 +690,6 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
-      const uint32_t idesc = make_idesc(P.b_mn_major, kRows * BM);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -673,6 +698,8 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
         const TileCoord tc = decode<kRows>(P, t);
         const int kit = P.k_iters[tc.c];
+        const int bmn = P.job[tc.c].kind == kKindProd ? 1 : 0;
+        const uint32_t idesc = make_idesc(bmn, kRows * BM);
         const bool freed = kPair ? mbar_wait_cluster(acce0 + 8 * acc, acc_phase ^ 1)
                                  : mbar_wait(acce0 + 8 * acc, acc_phase ^ 1);
         if (!freed) { give_up(); break; }
@@ -687,8 +714,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
-            const uint64_t bd = P.b_mn_major ? smem_desc(sb + k * 2048, 8192, 1024)
-                                             : smem_desc(sb + k * 32, 16, 1024);
+            const uint64_t bd = bmn ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
             if constexpr (kPair) mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
             else mma_bf16_one(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
@@ -721,23 +747,24 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const TileCoord tc = decode<kRows>(P, t);
       const int sub = P.sub0[tc.c] + tc.mat;
       const DevSub &S = A.subs[sub];
-      if (A.mode == kFinal)
+      const TcJob &J = P.job[tc.c];
+      if (J.mode == kFinal)
         prefetch_weight_tile(S, (kRows * tc.tm + (int)crank) * BM + quarter * 32, tc.tn * BN, lane);
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
       tc_fence_after();
-      const EpiScalars e = epi_scalars(A, sub);
+      const float s = J.first ? A.alpha[sub] : 1.0f;
       const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
       float *st = stage_base + (warp - 2) * kStageFloats;
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       // skip column chunks that hold nothing this warp writes
-      const int ncols = (A.mode == kProduct || A.mode == kFinal) ? S.q : S.p;
+      const int ncols = J.kind == kKindProd ? S.q : S.p;
 #pragma unroll 1
       for (int ch = half * nch; ch < (half + 1) * nch; ++ch) {
         const int col0 = tc.tn * BN + ch * 32;
         if (col0 >= ncols) break;
         float v[32];
         tmem_ld32(trow + ch * 32, v);
-        if (i0 < S.p) epilogue_block(A, S, e, i0, col0, v, st, lane);
+        if (i0 < S.p) epilogue_block(A, J, S, s, i0, col0, v, st, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -806,28 +833,57 @@ bool encode_map(CUtensorMap *map, void *base, int64_t cols, int64_t rows, int64_
 // pairs.
 bool single_mode(int p) { return p <= BM; }
 
-double tc_executed_flops(int p, int q, bool square) {
-  // work items are kRows consecutive 128-row tiles; in pair mode an odd
-  // tile-row count runs one all-padding tile in the last pair
+namespace {
+
+// Work items of one matrix: kRows consecutive 128-row tiles x one column
+// tile; in pair mode an odd tile-row count runs one all-padding tile in the
+// last pair.
+int items_m_of(int p) {
   const int rows = single_mode(p) ? 1 : 2;
-  const int items_m = ((p + BM - 1) / BM + rows - 1) / rows;
-  const int tiles_n_sym = (p + BN - 1) / BN;
-  int64_t sym_items = 0;
-  for (int r = 0; r < items_m; ++r) sym_items += std::max(0, tiles_n_sym - tri_tn_min(rows * r));
-  const double kq = (double)((q + BK - 1) / BK) * BK;   // Gram: K = q
-  const double kp = (double)((p + BK - 1) / BK) * BK;   // square and product: K = p
-  const double item = 2.0 * rows * BM * BN;             // MACs x 2 per item and unit K
-  double f = sym_items * item * kq;                       // Gram
-  if (square) f += sym_items * item * kp;                 // A A
-  f += (double)items_m * ((q + BN - 1) / BN) * item * kp; // product
+  return ((p + BM - 1) / BM + rows - 1) / rows;
+}
+
+int64_t sym_items_of(int p) {
+  const int rows = single_mode(p) ? 1 : 2;
+  const int tiles_n = (p + BN - 1) / BN;
+  int64_t n = 0;
+  for (int r = 0; r < items_m_of(p); ++r) n += std::max(0, tiles_n - tri_tn_min(rows * r));
+  return n;
+}
+
+double item_flops(int p, int kdim) {  // one work item: rows x 128 x 256 outputs, K padded to BK
+  const int rows = single_mode(p) ? 1 : 2;
+  return 2.0 * rows * BM * BN * (double)((kdim + BK - 1) / BK) * BK;
+}
+
+}  // namespace
+
+double tc_executed_flops(int p, int q, bool square) {
+  double f = sym_items_of(p) * item_flops(p, q);                        // Gram, K = q
+  if (square) f += sym_items_of(p) * item_flops(p, p);                  // A A
+  f += (double)items_m_of(p) * ((q + BN - 1) / BN) * item_flops(p, p);  // product, K = p
   return f;
+}
+
+double tc_gram_route_flops(int p, int q, int k) {
+  return sym_items_of(p) * item_flops(p, q) + (3.0 * k - 3.0) * sym_items_of(p) * item_flops(p, p) +
+         (double)items_m_of(p) * ((q + BN - 1) / BN) * item_flops(p, p);
 }
 
 namespace {
 
+// Class base of an operand or output region: X operands live in x-space,
+// everything p x p in the class's own p-space.
+inline const char *xbase(const void *region, const ShapeClass &C) {
+  return static_cast<const char *>(region) + C.x_base * 2;
+}
+inline const char *pbase(const void *region, const ShapeClass &C) {
+  return static_cast<const char *>(region) + C.p_base * 2;
+}
+
 template <bool kPair>
-int launch_mode(const ShapeClass *const *classes, int32_t n_classes, const PhaseArgs &args, int sm_count,
-                void *stream) {
+int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count, void *stream,
+                int64_t *n_launch) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -836,44 +892,49 @@ int launch_mode(const ShapeClass *const *classes, int32_t n_classes, const Phase
   });
   if (attr_err != cudaSuccess) return (int)attr_err;
   constexpr int kRows = Mode<kPair>::kRows;
-  const bool gram = (args.mode == kGram || args.mode == kGramA);
-  const bool square = (args.mode == kSquare);
-  for (int32_t c0 = 0; c0 < n_classes; c0 += kMaxClassesPerLaunch) {
+  for (int32_t j0 = 0; j0 < n_jobs; j0 += kMaxClassesPerLaunch) {
     TcParams T;
     memset(&T, 0, sizeof T);
-    T.n = std::min(kMaxClassesPerLaunch, n_classes - c0);
-    T.b_mn_major = (gram || square) ? 0 : 1;
-    T.tri = (gram || square) ? 1 : 0;
+    T.n = std::min(kMaxClassesPerLaunch, n_jobs - j0);
     T.tile_start[0] = 0;
     for (int k = 0; k < T.n; ++k) {
-      const ShapeClass &C = *classes[c0 + k];
-      char *xin = static_cast<char *>(args.x_in) + C.x_base * 2;
-      char *pb = static_cast<char *>(args.pbuf) + C.p_base * 2;
-      char *ab = static_cast<char *>(args.abuf) + C.p_base * 2;
+      const GemmJob &J = *jobs[j0 + k];
+      const ShapeClass &C = *J.cls;
       bool ok;
       int Ndim, Kdim;
-      if (gram) {  // A = X rows, B = X rows, K = q
-        ok = encode_map(&T.mapA[k], xin, C.q, C.p, C.count, C.ld, BK, BM) &&
-             encode_map(&T.mapB[k], xin, C.q, C.p, C.count, C.ld, BK, BN / 2);
+      if (J.kind == kKindGram) {  // A = X rows, B = X rows, K = q
+        void *x = const_cast<char *>(xbase(J.opA, C));
+        ok = encode_map(&T.mapA[k], x, C.q, C.p, C.count, C.ld, BK, BM) &&
+             encode_map(&T.mapB[k], x, C.q, C.p, C.count, C.ld, BK, BN / 2);
         Ndim = C.p;
         Kdim = C.q;
-      } else if (square) {  // A = Gram rows, B = Gram rows (symmetric), K = p
-        ok = encode_map(&T.mapA[k], ab, C.p, C.p, C.count, C.ldp, BK, BM) &&
-             encode_map(&T.mapB[k], ab, C.p, C.p, C.count, C.ldp, BK, BN / 2);
+      } else if (J.kind == kKindSym) {  // A = L rows, B = R rows (R symmetric), K = p
+        ok = encode_map(&T.mapA[k], const_cast<char *>(pbase(J.opA, C)), C.p, C.p, C.count, C.ldp, BK, BM) &&
+             encode_map(&T.mapB[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 2);
         Ndim = C.p;
         Kdim = C.p;
-      } else {  // A = P rows (K = p), B = X with rows as K, columns as N
-        ok = encode_map(&T.mapA[k], pb, C.p, C.p, C.count, C.ldp, BK, BM) &&
-             encode_map(&T.mapB[k], xin, C.q, C.p, C.count, C.ld, 64, BK);
+      } else {  // A = L rows (K = p), B = X with rows as K, columns as N
+        ok = encode_map(&T.mapA[k], const_cast<char *>(pbase(J.opA, C)), C.p, C.p, C.count, C.ldp, BK, BM) &&
+             encode_map(&T.mapB[k], const_cast<char *>(xbase(J.opB, C)), C.q, C.p, C.count, C.ld, 64, BK);
         Ndim = C.q;
         Kdim = C.p;
       }
       if (!ok) return (int)cudaErrorInvalidValue;
+      TcJob &tj = T.job[k];
+      tj.mode = J.mode;
+      tj.kind = J.kind;
+      tj.first = J.first;
+      tj.a = J.a;
+      tj.b = J.b;
+      tj.c = J.c;
+      tj.out = J.out;
+      tj.out2 = J.out2;
+      tj.aux = J.aux;
       T.tiles_n[k] = (Ndim + BN - 1) / BN;
       T.k_iters[k] = (Kdim + BK - 1) / BK;
       T.sub0[k] = C.sub0;
       const int items_m = ((C.p + BM - 1) / BM + kRows - 1) / kRows;
-      if (T.tri) {
+      if (J.kind != kKindProd) {
         int cnt = 0;
         for (int r = 0; r < items_m; ++r) cnt += std::max(0, T.tiles_n[k] - tri_tn_min(kRows * r));
         T.tiles_per_mat[k] = cnt;
@@ -913,6 +974,7 @@ int launch_mode(const ShapeClass *const *classes, int32_t n_classes, const Phase
     const cudaError_t lerr = cudaLaunchKernelEx(&cfg, ns_gemm_tc_kernel<kPair>, T, args);
     if (lerr != cudaSuccess) return (int)lerr;
     count_launches(1);
+    if (n_launch) ++*n_launch;
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return (int)err;
   }
@@ -943,22 +1005,16 @@ int launch_wait_timeout(int32_t *status, uint64_t limit_ns, void *stream) {
   return (int)cudaGetLastError();
 }
 
-int launch_ns_gemm_tc(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args, int sm_count,
-                      void *stream) {
-  const ShapeClass *single[4096], *pair[4096];
-  int ns = 0, np = 0;
-  for (int32_t c = 0; c < n_classes; ++c) {
-    if (single_mode(classes[c].p)) {
-      if (ns == 4096) return (int)cudaErrorInvalidValue;
-      single[ns++] = &classes[c];
-    } else {
-      if (np == 4096) return (int)cudaErrorInvalidValue;
-      pair[np++] = &classes[c];
-    }
+int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count, void *stream,
+                      int64_t *n_launch) {
+  std::vector<const GemmJob *> single, pair;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    if (jobs[j].cls->count == 0) continue;
+    (single_mode(jobs[j].cls->p) ? single : pair).push_back(&jobs[j]);
   }
-  int err = launch_mode<true>(pair, np, args, sm_count, stream);
+  int err = launch_mode<true>(pair.data(), (int32_t)pair.size(), globals, sm_count, stream, n_launch);
   if (err) return err;
-  return launch_mode<false>(single, ns, args, sm_count, stream);
+  return launch_mode<false>(single.data(), (int32_t)single.size(), globals, sm_count, stream, n_launch);
 }
 
 }  // namespace gbo

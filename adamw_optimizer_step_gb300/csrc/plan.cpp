@@ -123,11 +123,14 @@ struct gbo_plan {
   gbo_muon_opts opts{};
   std::vector<float> abc;  // 3 * ns_steps
   bool any_c = false;
+  bool any_gram = false;     // some class takes the Gram route
   std::vector<DevSub> subs;  // sorted by shape class
   std::vector<ShapeClass> classes;
   int64_t n_tiles = 0, n_row_blocks = 0;
   int32_t x_dtype = GBO_BF16;
   size_t off_x[2] = {0, 0}, off_p = 0, off_a = 0, off_alpha = 0, off_part = 0, ws_bytes = 0;
+  // Gram-route p x p buffers: A, T, P (two), Q (two)
+  size_t off_g[6] = {0, 0, 0, 0, 0, 0};
   uint64_t hash = 0;
   gbo_plan_info info{};
   // device state, set by the first step
@@ -147,6 +150,17 @@ struct gbo_plan {
 };
 
 namespace {
+
+// Route of a p x q class: the Gram route needs bf16 mode, k >= 2 and c == 0
+// in every iteration; AUTO takes it when it executes at least 10% fewer
+// FLOPs (in practice: whenever q is clearly above p).
+int32_t choose_route(const gbo_plan *P, int p, int q) {
+  const int k = P->opts.ns_steps;
+  if (P->x_dtype != GBO_BF16 || P->any_c || k < 2 || P->opts.route == GBO_ROUTE_X) return kRouteX;
+  if (P->opts.route == GBO_ROUTE_GRAM) return kRouteGram;
+  const double fx = k * tc_executed_flops(p, q, false);
+  return tc_gram_route_flops(p, q, k) < 0.9 * fx ? kRouteGram : kRouteX;
+}
 
 int validate_and_expand(gbo_plan *P) {
   const gbo_muon_opts &o = P->opts;
@@ -262,21 +276,36 @@ int validate_and_expand(gbo_plan *P) {
       }
     }
   }
+  // Route of each class; X-route classes first, so the second X buffer only
+  // spans them when nothing else needs it.
+  std::vector<int32_t> route(class_shapes.size());
+  for (size_t c = 0; c < class_shapes.size(); ++c) route[c] = choose_route(P, class_shapes[c].first, class_shapes[c].second);
+  std::vector<int32_t> order;
+  for (int r : {(int)kRouteX, (int)kRouteGram})
+    for (size_t c = 0; c < class_shapes.size(); ++c)
+      if (route[c] == r) order.push_back((int32_t)c);
+  std::vector<int32_t> new_index(class_shapes.size());
+  for (size_t k = 0; k < order.size(); ++k) new_index[order[k]] = (int32_t)k;
+  for (DevSub &S : subs) S.cls = new_index[S.cls];
   // order by class (stable: table order within a class)
   std::stable_sort(subs.begin(), subs.end(), [](const DevSub &a, const DevSub &b) { return a.cls < b.cls; });
   const size_t es = P->x_dtype == GBO_BF16 ? 2 : 4;
   P->classes.clear();
-  int64_t xoff = 0, poff = 0;
-  for (size_t c = 0; c < class_shapes.size(); ++c) {
+  P->any_gram = false;
+  int64_t xoff = 0, poff = 0, goff = 0, x_route_end = 0;
+  for (size_t c = 0; c < order.size(); ++c) {
     ShapeClass C{};
-    C.p = class_shapes[c].first;
-    C.q = class_shapes[c].second;
+    C.p = class_shapes[order[c]].first;
+    C.q = class_shapes[order[c]].second;
+    C.route = route[order[c]];
     C.ld = (int32_t)round_up(C.q, 16);
     C.ldp = (int32_t)round_up(C.p, 16);
     C.count = 0;
     C.sub0 = -1;
     C.x_base = xoff;
-    C.p_base = poff;
+    // p x p buffers: the X route's P (and A) space, or the Gram route's own space
+    int64_t &pspace = C.route == kRouteGram ? goff : poff;
+    C.p_base = pspace;
     for (size_t k = 0; k < subs.size(); ++k)
       if (subs[k].cls == (int32_t)c) {
         if (C.sub0 < 0) C.sub0 = (int32_t)k;
@@ -284,11 +313,16 @@ int validate_and_expand(gbo_plan *P) {
         S.ld = C.ld;
         S.ldp = C.ldp;
         S.x_off = xoff + (int64_t)C.count * C.p * C.ld;
-        S.p_off = poff + (int64_t)C.count * C.p * C.ldp;
+        S.p_off = pspace + (int64_t)C.count * C.p * C.ldp;
+        // the last iterate: X_k of the X route alternates buffers from X0;
+        // the Gram route writes X_k = Q_k X_0 into the second buffer
+        S.x_sel = C.route == kRouteGram ? 1 : (o.ns_steps & 1);
         C.count++;
       }
     xoff = round_up(xoff + (int64_t)C.count * C.p * C.ld, 128);
-    poff = round_up(poff + (int64_t)C.count * C.p * C.ldp, 128);
+    pspace = round_up(pspace + (int64_t)C.count * C.p * C.ldp, 128);
+    if (C.route == kRouteX) x_route_end = xoff;
+    else P->any_gram = true;
     P->classes.push_back(C);
   }
   // momentum tiles and NorMuon row blocks, in table order of subs
@@ -318,9 +352,11 @@ int validate_and_expand(gbo_plan *P) {
     return at;
   };
   P->off_x[0] = region((size_t)xoff * es);
-  P->off_x[1] = region((size_t)xoff * es);
+  // the Gram route writes its last iterate into the second buffer only for NorMuon
+  P->off_x[1] = region((size_t)(o.normuon ? xoff : x_route_end) * es);
   P->off_p = region((size_t)poff * es);
   P->off_a = region(P->any_c ? (size_t)poff * es : 0);
+  for (int b = 0; b < 6; ++b) P->off_g[b] = region((size_t)goff * es);
   P->off_alpha = region(P->subs.size() * sizeof(float));
   P->off_part = region((size_t)tiles * 8 * 2 * sizeof(float));  // (max, sum of squares) per warp of a tile
   P->ws_bytes = off;
@@ -339,10 +375,18 @@ int validate_and_expand(gbo_plan *P) {
       fl += 4.0 * p * p * q + (P->abc[3 * it + 2] != 0.f ? 2.0 * p * p * p : 0.0);
   }
   I.ns_flops = fl;
+  I.n_gram_route = 0;
   if (P->x_dtype == GBO_BF16) {
     double ex = 0;
-    for (const DevSub &S : P->subs)
-      for (int it = 0; it < o.ns_steps; ++it) ex += tc_executed_flops(S.p, S.q, P->abc[3 * it + 2] != 0.f);
+    for (const ShapeClass &C : P->classes) {
+      if (C.route == kRouteGram) {
+        ex += C.count * tc_gram_route_flops(C.p, C.q, o.ns_steps);
+        I.n_gram_route += C.count;
+      } else {
+        for (int it = 0; it < o.ns_steps; ++it)
+          ex += C.count * tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f);
+      }
+    }
     I.ns_flops_executed = ex;
   } else {
     I.ns_flops_executed = fl;
@@ -366,18 +410,124 @@ uint64_t layout_hash(const gbo_plan *P) {
   return f.h;
 }
 
-int launch_gemm(const gbo_plan *P, const PhaseArgs &args, void *stream) {
-  if (P->x_dtype == GBO_F32)
-    return launch_ns_gemm_simt(P->classes.data(), (int32_t)P->classes.size(), args, P->sm_count, stream);
-  return launch_ns_gemm_tc(P->classes.data(), (int32_t)P->classes.size(), args, P->sm_count, stream);
+int launch_gemm_simt(const gbo_plan *P, const PhaseArgs &args, void *stream) {
+  return launch_ns_gemm_simt(P->classes.data(), (int32_t)P->classes.size(), args, P->sm_count, stream);
 }
 
-int64_t gemm_launches(const gbo_plan *P) {
+int64_t simt_launches(const gbo_plan *P) {
+  return ((int64_t)P->classes.size() + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch;
+}
+
+// One tensor-core step of the schedule: the jobs of every class that has
+// work at this point, and the phase it is timed under.
+struct TcStep {
+  std::vector<GemmJob> jobs;
+  int phase = kPhaseGram;
+};
+
+// The tensor-core schedule of one Muon step (bf16 mode).  The X route takes
+// 2k steps (3 per iteration when c != 0), the Gram route 2k + 1; step i of
+// the step runs step i of both routes, whose classes and buffers are
+// disjoint.  With ws == nullptr the pointers are offsets (for counting).
+std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
+  const int k = P->opts.ns_steps;
+  const bool normuon = P->opts.normuon != 0;
+  auto R = [ws](size_t off) { return reinterpret_cast<void *>(reinterpret_cast<uintptr_t>(ws) + off); };
+  void *x[2] = {R(P->off_x[0]), R(P->off_x[1])};
+  void *pb = R(P->off_p), *ab = R(P->off_a);
+  void *gA = R(P->off_g[0]), *gT = R(P->off_g[1]);
+  void *gP[2] = {R(P->off_g[2]), R(P->off_g[3])};
+  void *gQ[2] = {R(P->off_g[4]), R(P->off_g[5])};
+  auto job = [](const ShapeClass *C, int mode, int kind, int first, const float *abc, const void *opA,
+                const void *opB, void *out, void *out2 = nullptr, const void *aux = nullptr) {
+    GemmJob J{};
+    J.cls = C;
+    J.mode = mode;
+    J.kind = kind;
+    J.first = first;
+    J.a = abc ? abc[0] : 0.f;
+    J.b = abc ? abc[1] : 0.f;
+    J.c = abc ? abc[2] : 0.f;
+    J.opA = opA;
+    J.opB = opB;
+    J.out = out;
+    J.out2 = out2;
+    J.aux = aux;
+    return J;
+  };
+  std::vector<TcStep> xs, gs;
+  auto at = [](std::vector<TcStep> &v, size_t i, int phase) -> TcStep & {
+    if (v.size() <= i) v.resize(i + 1);
+    v[i].phase = phase;
+    return v[i];
+  };
+  for (const ShapeClass &C : P->classes) {
+    if (C.count == 0) continue;
+    if (C.route == kRouteX) {
+      size_t i = 0;
+      int cur = 0;
+      for (int it = 0; it < k; ++it) {
+        const float *abc = &P->abc[3 * it];
+        const int first = it == 0;
+        if (abc[2] != 0.f) {
+          at(xs, i++, kPhaseGram).jobs.push_back(job(&C, kGramA, kKindGram, first, abc, x[cur], x[cur], ab));
+          at(xs, i++, kPhaseSquare).jobs.push_back(job(&C, kSquare, kKindSym, 0, abc, ab, ab, pb, nullptr, ab));
+        } else {
+          at(xs, i++, kPhaseGram).jobs.push_back(job(&C, kGram, kKindGram, first, abc, x[cur], x[cur], pb));
+        }
+        const bool last = it == k - 1;
+        const int mode = (last && !normuon) ? kFinal : kProduct;
+        at(xs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
+            .jobs.push_back(job(&C, mode, kKindProd, first, abc, pb, x[cur], x[cur ^ 1]));
+        cur ^= 1;
+      }
+    } else {
+      // A_0 = alpha^2 X_0 X_0^T and P_0;  Q_1 = P_0
+      size_t i = 0;
+      at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kKindGram, 1, &P->abc[0], x[0], x[0], gP[0], gA));
+      for (int j = 0; j + 1 < k; ++j) {
+        void *Pj = gP[j & 1];
+        // T = P_j A_j and, from j = 1, Q_{j+1} = P_j Q_j
+        TcStep &la = at(gs, i++, kPhaseProduct);
+        la.jobs.push_back(job(&C, kGramA, kKindSym, 0, nullptr, Pj, gA, gT));
+        if (j >= 1) la.jobs.push_back(job(&C, kGramA, kKindSym, 0, nullptr, Pj, j == 1 ? gP[0] : gQ[j & 1], gQ[(j + 1) & 1]));
+        // A_{j+1} = P_j T and P_{j+1} (A_{k-1} itself is not needed)
+        const float *abc = &P->abc[3 * (j + 1)];
+        if (j + 2 < k)
+          at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kKindSym, 0, abc, Pj, gT, gP[(j + 1) & 1], gA));
+        else
+          at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGram, kKindSym, 0, abc, Pj, gT, gP[(j + 1) & 1]));
+      }
+      // Q_k = P_{k-1} Q_{k-1}, then X_k = Q_k X_0 (alpha folded in)
+      at(gs, i++, kPhaseProduct)
+          .jobs.push_back(job(&C, kGramA, kKindSym, 0, nullptr, gP[(k - 1) & 1], k == 2 ? gP[0] : gQ[(k - 1) & 1],
+                              gQ[k & 1]));
+      const int mode = normuon ? kProduct : kFinal;
+      at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
+          .jobs.push_back(job(&C, mode, kKindProd, 1, nullptr, gQ[k & 1], x[0], x[1]));
+    }
+  }
+  std::vector<TcStep> steps(std::max(xs.size(), gs.size()));
+  for (size_t i = 0; i < steps.size(); ++i) {
+    if (i < gs.size()) {
+      steps[i].phase = gs[i].phase;
+      steps[i].jobs = gs[i].jobs;
+    }
+    if (i < xs.size()) {  // label by the X route where it has a step
+      steps[i].phase = xs[i].phase;
+      steps[i].jobs.insert(steps[i].jobs.end(), xs[i].jobs.begin(), xs[i].jobs.end());
+    }
+  }
+  return steps;
+}
+
+// Kernel launches of one step of the schedule (classes go 8 to a launch,
+// pairs and single CTAs separately).
+int64_t tc_step_launches(const TcStep &st) {
+  int64_t single = 0, pair = 0;
+  for (const GemmJob &J : st.jobs) (single_mode(J.cls->p) ? single : pair)++;
   auto groups = [](int64_t n) { return (n + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch; };
-  if (P->x_dtype != GBO_BF16) return groups((int64_t)P->classes.size());
-  int64_t single = 0;
-  for (const ShapeClass &C : P->classes) single += single_mode(C.p) ? 1 : 0;
-  return groups(single) + groups((int64_t)P->classes.size() - single);
+  return groups(single) + groups(pair);
 }
 
 cudaEvent_t take_event(gbo_plan *P) {
@@ -427,6 +577,8 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   if (!opts->abc) return fail(GBO_ERR_INVALID_ARG, "abc is NULL");
   if (opts->precision != GBO_NS_BF16 && opts->precision != GBO_NS_F32)
     return fail(GBO_ERR_INVALID_ARG, "precision must be GBO_NS_BF16 or GBO_NS_F32");
+  if (opts->route != GBO_ROUTE_AUTO && opts->route != GBO_ROUTE_X && opts->route != GBO_ROUTE_GRAM)
+    return fail(GBO_ERR_INVALID_ARG, "route must be GBO_ROUTE_AUTO, GBO_ROUTE_X or GBO_ROUTE_GRAM");
   if (!std::isfinite(opts->mu)) return fail(GBO_ERR_INVALID_ARG, "mu is not finite");
   if (opts->normuon && (!(opts->beta2 >= 0.f && opts->beta2 <= 1.f) || !(opts->eps >= 0.f)))
     return fail(GBO_ERR_INVALID_ARG, "NorMuon needs 0 <= beta2 <= 1 and eps >= 0");
@@ -454,9 +606,13 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
     return rc;
   }
   P->hash = layout_hash(P);
-  int64_t per_iter = 0;
-  for (int it = 0; it < k; ++it) per_iter += (P->abc[3 * it + 2] != 0.f ? 3 : 2) * gemm_launches(P);
-  P->info.launches_per_step = P->subs.empty() ? 0 : 2 + per_iter + (opts->normuon ? 1 : 0);
+  int64_t gemm = 0;
+  if (P->x_dtype == GBO_BF16) {
+    for (const TcStep &st : build_schedule(P, nullptr)) gemm += tc_step_launches(st);
+  } else {
+    for (int it = 0; it < k; ++it) gemm += (P->abc[3 * it + 2] != 0.f ? 3 : 2) * simt_launches(P);
+  }
+  P->info.launches_per_step = P->subs.empty() ? 0 : 2 + gemm + (opts->normuon ? 1 : 0);
   *out = P;
   return ok();
 }
@@ -583,35 +739,44 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   A.status = dev_status;
   A.lr = lr;
   const int k = P->opts.ns_steps;
-  const int64_t gl = gemm_launches(P);
-  int cur = 0;
-  for (int it = 0; it < k; ++it) {
-    A.a = P->abc[3 * it];
-    A.b = P->abc[3 * it + 1];
-    A.c = P->abc[3 * it + 2];
-    A.first = it == 0;
-    A.x_in = x[cur];
-    A.x_out = x[cur ^ 1];
-    if (A.c != 0.f) {
-      A.mode = kGramA;
-      if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "Gram kernel");
-      mark(kPhaseGram, gl);
-      A.mode = kSquare;
-      if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "square kernel");
-      mark(kPhaseSquare, gl);
-    } else {
-      A.mode = kGram;
-      if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "Gram kernel");
-      mark(kPhaseGram, gl);
+  if (P->x_dtype == GBO_BF16) {
+    for (const TcStep &step : build_schedule(P, ws)) {
+      int64_t nl = 0;
+      if ((err = launch_ns_gemm_tc(step.jobs.data(), (int32_t)step.jobs.size(), A, P->sm_count, st, &nl)))
+        return cuda_fail(err, "Newton-Schulz kernel");
+      mark(step.phase, nl);
     }
-    const bool last_it = it == k - 1;
-    A.mode = (last_it && !P->opts.normuon) ? kFinal : kProduct;
-    if ((err = launch_gemm(P, A, st))) return cuda_fail(err, "product kernel");
-    mark(A.mode == kFinal ? kPhaseFinal : kPhaseProduct, gl);
-    cur ^= 1;
+  } else {
+    const int64_t gl = simt_launches(P);
+    int cur = 0;
+    for (int it = 0; it < k; ++it) {
+      A.a = P->abc[3 * it];
+      A.b = P->abc[3 * it + 1];
+      A.c = P->abc[3 * it + 2];
+      A.first = it == 0;
+      A.x_in = x[cur];
+      A.x_out = x[cur ^ 1];
+      if (A.c != 0.f) {
+        A.mode = kGramA;
+        if ((err = launch_gemm_simt(P, A, st))) return cuda_fail(err, "Gram kernel");
+        mark(kPhaseGram, gl);
+        A.mode = kSquare;
+        if ((err = launch_gemm_simt(P, A, st))) return cuda_fail(err, "square kernel");
+        mark(kPhaseSquare, gl);
+      } else {
+        A.mode = kGram;
+        if ((err = launch_gemm_simt(P, A, st))) return cuda_fail(err, "Gram kernel");
+        mark(kPhaseGram, gl);
+      }
+      const bool last_it = it == k - 1;
+      A.mode = (last_it && !P->opts.normuon) ? kFinal : kProduct;
+      if ((err = launch_gemm_simt(P, A, st))) return cuda_fail(err, "product kernel");
+      mark(A.mode == kFinal ? kPhaseFinal : kPhaseProduct, gl);
+      cur ^= 1;
+    }
   }
   if (P->opts.normuon) {
-    err = launch_normuon_rows(P->d_subs, nsub, P->n_row_blocks, x[cur], P->x_dtype, P->opts.beta2,
+    err = launch_normuon_rows(P->d_subs, nsub, P->n_row_blocks, x[0], x[1], P->x_dtype, P->opts.beta2,
                               P->opts.eps, lr, dbg_update, dev_status, P->sm_count, st);
     if (err) return cuda_fail(err, "NorMuon rows kernel");
     mark(kPhaseRows, 1);

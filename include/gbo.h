@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define GBO_ABI_VERSION 1
+#define GBO_ABI_VERSION 2
 
 /* ---- status codes (return values) ------------------------------------ */
 #define GBO_OK 0
@@ -122,8 +122,25 @@ typedef struct {
   int32_t abc_per_step;  /* 0: one shared triple; 1: one triple per iteration           */
   int32_t precision;     /* GBO_NS_BF16 | GBO_NS_F32                                    */
   int32_t normuon;       /* 1: NorMuon row normalisation; every desc needs row_v        */
-  int32_t reserved;      /* set to 0                                                    */
+  int32_t route;         /* GBO_ROUTE_AUTO (0) | GBO_ROUTE_X | GBO_ROUTE_GRAM          */
 } gbo_muon_opts;
+
+/*
+ * Route of the k iterations of one shape class (bf16 mode).  Both give the
+ * k-step result of eq. (5); they differ in rounding order and cost.
+ *   X     every iteration forms A = X X^T (p x p) and X <- P X (p x q).
+ *   GRAM  every iterate is X_j = Q_j X_0 with Q_j a polynomial in
+ *         A_0 = X_0 X_0^T, so the iteration runs on p x p matrices only
+ *         (A_{j+1} = P_j A_j P_j, Q_{j+1} = P_j Q_j) and the p x q product
+ *         runs once: X_k = Q_k X_0.  Executes p^2 q + (3k - 3) p^3 + 2 p^2 q
+ *         instead of about k (p^2 q + 2 p^2 q) FLOPs; allowed when every
+ *         iteration has c == 0 and k >= 2.
+ *   AUTO  GRAM where it is allowed and executes fewer FLOPs (q > p), else X.
+ * The fp32 mode always takes the X route.
+ */
+#define GBO_ROUTE_AUTO 0
+#define GBO_ROUTE_X 1
+#define GBO_ROUTE_GRAM 2
 
 /*
  * Validate a Muon descriptor table and build a plan (host memory only; the
@@ -307,6 +324,7 @@ typedef struct {
   double ns_flops;         /* dense-count Newton-Schulz FLOPs per step          */
   double ns_flops_executed;/* FLOPs the kernels execute (same unless symmetric) */
   int64_t launches_per_step; /* kernels one gbo_muon_step launches              */
+  int64_t n_gram_route;    /* matrices whose iterations take the Gram route     */
 } gbo_plan_info;
 
 int gbo_muon_plan_info(const gbo_plan *plan, gbo_plan_info *out);

@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(L):
     assert "gbo_muon_step" in names and "gbo_adamw_step" in names
     for n in names:
         assert hasattr(L, n), n
-    assert B.gbo_abi_version() == 1
+    assert B.gbo_abi_version() == 2
     for i, S in enumerate(B._STRUCTS):
         assert B.gbo_struct_size(i) == ctypes.sizeof(S)
 
@@ -64,11 +64,12 @@ def desc(i, rows, cols, view=None, split_off=0, n_split=0, w_dtype=B.GBO_BF16, g
     return d
 
 
-def create(L, descs, pool=(), ns_steps=5, abc=(1.5, -0.5, 0.0), precision=B.GBO_NS_BF16, normuon=0):
+def create(L, descs, pool=(), ns_steps=5, abc=(1.5, -0.5, 0.0), precision=B.GBO_NS_BF16, normuon=0,
+           route=B.GBO_ROUTE_AUTO):
     arr = (B.MuonDesc * max(1, len(descs)))(*descs)
     cabc = (ctypes.c_float * len(abc))(*abc)
     opts = B.MuonOpts(ctypes.cast(cabc, ctypes.POINTER(ctypes.c_float)), 0.95, 0.95, 1e-8, 1, ns_steps,
-                      int(len(abc) > 3), precision, normuon, 0)
+                      int(len(abc) > 3), precision, normuon, route)
     cpool = (ctypes.c_int64 * max(1, len(pool)))(*pool)
     out = ctypes.c_void_p()
     rc = L.gbo_muon_plan_create(arr, len(descs), cpool, len(pool), ctypes.byref(opts), ctypes.byref(out))
@@ -149,14 +150,43 @@ def test_missing_gradient_skips(L):
 
 
 def test_flop_count_and_launches(L):
-    rc, plan = create(L, [desc(0, 5632 * 2, 2048, (2, 5632, 2048)), desc(1, 2048, 5632)])
+    descs = lambda: [desc(0, 5632 * 2, 2048, (2, 5632, 2048)), desc(1, 2048, 5632)]
+    # p = 2048, q = 5632 on CTA pairs: 256 x 256 output tiles, K padded to 64.
+    # A symmetric 2048 x 2048 output runs the 8 * 9 / 2 = 36 tiles on or above
+    # the diagonal; a 2048 x 5632 output runs 8 x 22 tiles.
+    tile = 2 * 256 * 256
+    gram, sym, prod = 36 * tile * 5632, 36 * tile * 2048, 8 * 22 * tile * 2048
+    rc, plan = create(L, descs(), route=B.GBO_ROUTE_X)
     assert rc == 0
     i = info(L, plan)
-    assert i.n_matrices == 3 and i.n_shape_classes == 1
+    assert i.n_matrices == 3 and i.n_shape_classes == 1 and i.n_gram_route == 0
     assert i.ns_flops == 3 * 5 * 4 * 2048 ** 2 * 5632
+    assert i.ns_flops_executed == 3 * 5 * (gram + prod)
     # momentum + finalize + 5 x (Gram + product)
     assert i.launches_per_step == 12
     L.gbo_muon_plan_destroy(plan)
+    # the automatic route takes the Gram route for q > p: the Gram, 12
+    # symmetric 2048^3 products, one product with X_0, in 2k + 1 launches
+    for route in (B.GBO_ROUTE_AUTO, B.GBO_ROUTE_GRAM):
+        rc, plan = create(L, descs(), route=route)
+        i = info(L, plan)
+        assert i.n_gram_route == 3 and i.ns_flops == 3 * 5 * 4 * 2048 ** 2 * 5632
+        assert i.ns_flops_executed == 3 * (gram + 12 * sym + prod)
+        assert i.launches_per_step == 2 + 11
+        L.gbo_muon_plan_destroy(plan)
+    # square matrices stay on the X route unless forced; c != 0, k = 1 and
+    # fp32 mode never take the Gram route
+    rc, plan = create(L, [desc(0, 256, 256)])
+    assert info(L, plan).n_gram_route == 0
+    L.gbo_muon_plan_destroy(plan)
+    rc, plan = create(L, [desc(0, 256, 256)], route=B.GBO_ROUTE_GRAM)
+    assert info(L, plan).n_gram_route == 1
+    L.gbo_muon_plan_destroy(plan)
+    for kw in (dict(abc=(15 / 8, -5 / 4, 3 / 8)), dict(ns_steps=1), dict(precision=B.GBO_NS_F32)):
+        rc, plan = create(L, descs(), route=B.GBO_ROUTE_GRAM, **kw)
+        assert rc == 0 and info(L, plan).n_gram_route == 0
+        L.gbo_muon_plan_destroy(plan)
+    assert create(L, descs(), route=3)[0] == -1
     rc, plan = create(L, [desc(0, 64, 64)], abc=(15 / 8, -5 / 4, 3 / 8))
     assert info(L, plan).launches_per_step == 2 + 5 * 3
     L.gbo_muon_plan_destroy(plan)

@@ -88,6 +88,37 @@ def test_coefficients_and_options(precision, opts):
     check_muon(entries, gpu, ora, lr=0.05, precision=precision, mu=kw.get("mu", 0.95))
 
 
+@pytest.mark.parametrize("route", ["x", "gram"])
+@pytest.mark.parametrize("ns_steps", [2, 3, 5, 8])
+def test_routes(route, ns_steps):
+    """Both routes of the bf16 iterations reach the oracle's k-step result:
+    the X route, and the Gram route forced on every shape (square, tall,
+    1 x n and split views included), for short and long k (the Gram route
+    rotates its P and Q buffers by iteration)."""
+    entries = random_entries(RAGGED, seed=21, b_std=1e-3)
+    r = B.GBO_ROUTE_X if route == "x" else B.GBO_ROUTE_GRAM
+    gpu, status, plan = run_muon_gpu(entries, lr=0.02, precision="bf16", ns_steps=ns_steps, route=r)
+    info = B.gbo_muon_plan_info(plan)
+    assert info["n_gram_route"] == (0 if route == "x" else info["n_matrices"])
+    ora = run_muon_oracle(entries, lr=0.02, ns_steps=ns_steps)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
+
+
+@pytest.mark.parametrize("ns_steps", [3, 5])
+def test_normuon_gram_route(ns_steps):
+    """NorMuon rows read the last iterate from the buffer each route leaves
+    it in: mixed X-route (square) and Gram-route (rectangular) classes."""
+    shapes = [(300, 130, None, None), (130, 300, None, None), (96, 96, None, None)]
+    entries = random_entries(shapes, seed=22, normuon=True, b_std=1e-3)
+    gpu, status, plan = run_muon_gpu(entries, lr=0.02, precision="bf16", normuon=True, beta2=0.95, eps=1e-8,
+                                     ns_steps=ns_steps)
+    assert B.gbo_muon_plan_info(plan)["n_gram_route"] == 2
+    ora = run_muon_oracle(entries, lr=0.02, normuon=True, beta2=0.95, eps=1e-8, ns_steps=ns_steps)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
+
+
 @pytest.mark.parametrize("precision", ["f32", "bf16"])
 def test_normuon_rows(precision):
     shapes = [(300, 130, None, None), (130, 300, None, None), (64, 64, None, None),
