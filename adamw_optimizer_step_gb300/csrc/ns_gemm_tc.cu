@@ -13,10 +13,12 @@
 // of a launch is a job with its own operands, output and epilogue, so one
 // launch may run X-route and Gram-route steps (see internal.h) side by side.
 //
-// Persistent, warp-specialised CTA (320 threads, one CTA per SM):
+// Persistent, warp-specialised CTA (192 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane), STAGES-deep ring of A/B tiles
 //   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2..9  epilogue: TMEM -> registers -> global, 32 rows x 128 columns each
+//   warps 2..5  epilogue, one per TMEM lane quarter: TMEM -> registers ->
+//               a 64-byte-swizzled staging slot -> TMA store (the weight
+//               write of the last product goes registers -> global)
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the
 // epilogue of one tile overlaps the MMAs of the next.  Every wait is
 // bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT, waits (bounded)
@@ -58,17 +60,18 @@ struct Mode {
 constexpr int kRingBytes = 6 * (A_BYTES + B_HALF);
 static_assert(Mode<true>::kStages * Mode<true>::kStageBytes == kRingBytes, "ring size");
 static_assert(Mode<false>::kStages * Mode<false>::kStageBytes == kRingBytes, "ring size");
-#ifndef GBO_EPI_WARPS
-#define GBO_EPI_WARPS 4
-#endif
-// Epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter, each
-// taking half of the tile's columns).
-constexpr int kEpiWarps = GBO_EPI_WARPS;
-static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
+// Epilogue warps: one per TMEM lane quarter.
+constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;                   // two 128 x 256 fp32 accumulators
-constexpr int kStageFloats = 32 * 33;             // per epilogue warp: one 32 x 32 transpose
-constexpr int kSmemBytes = kRingBytes + 1024 /*align*/ + 256 /*barriers*/ + kEpiWarps * kStageFloats * 4;
+// Per epilogue warp: two 4 KB store slots, each a 32 x 32 bf16 block and its
+// transpose in the 64-byte-swizzled layout TMA stores read; the weight
+// write of the last product reuses the area as one 32 x 33 fp32 transpose.
+constexpr int kSlotBytes = 4096;
+constexpr int kWarpStageBytes = 2 * kSlotBytes;
+static_assert(32 * 33 * 4 <= kWarpStageBytes, "transpose staging");
+constexpr int kStageBytes = kEpiWarps * kWarpStageBytes;
+constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + kStageBytes + 256 /*barriers*/;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
@@ -86,6 +89,8 @@ struct TcJob {
 struct TcParams {
   CUtensorMap mapA[kMaxClassesPerLaunch];  // A operand, box 64 x 128
   CUtensorMap mapB[kMaxClassesPerLaunch];  // B operand, box 64 x 256 (K-major) or 64 x 64 (MN-major)
+  CUtensorMap mapO[kMaxClassesPerLaunch];  // output (TMA store), box 32 x 32, 64-byte swizzle
+  CUtensorMap mapO2[kMaxClassesPerLaunch]; // second output of kGramAP
   int64_t tile_start[kMaxClassesPerLaunch + 1];
   int32_t tiles_n[kMaxClassesPerLaunch];
   int32_t k_iters[kMaxClassesPerLaunch];
@@ -164,6 +169,29 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+
+// Bulk tensor store of one box from this CTA's shared memory; completion is
+// tracked by the issuing thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until all of this thread's bulk groups have completed their writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Make this thread's shared-memory writes visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // shared::cluster address of the same shared::cta offset in CTA `rank`.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
@@ -425,6 +453,51 @@ __device__ __forceinline__ void warp_transpose32(float (&o)[32], float *st, int 
   __syncwarp();
 }
 
+// Byte offset of 16-byte chunk q of row r in a 32-row x 64-byte bf16 block in
+// the 64-byte swizzle layout of TMA (chunk index XOR bits 7-8 of the offset).
+__device__ __forceinline__ uint32_t sw64(int r, int q) { return (uint32_t)(r * 64 + ((q ^ ((r >> 1) & 3)) << 4)); }
+
+// Lane r holds row r of a 32 x 32 block: write it as bf16 row r.
+__device__ __forceinline__ void stage_rows(uint32_t dst, const float (&o)[32], int lane) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + sw64(lane, q)),
+                 "r"(pack_bf16(o[8 * q], o[8 * q + 1])), "r"(pack_bf16(o[8 * q + 2], o[8 * q + 3])),
+                 "r"(pack_bf16(o[8 * q + 4], o[8 * q + 5])), "r"(pack_bf16(o[8 * q + 6], o[8 * q + 7]))
+                 : "memory");
+}
+
+// The transpose: element (lane, k) goes to row k, column lane.  For each k
+// the warp writes one 64-byte row, two lanes per 32-bit word.
+__device__ __forceinline__ void stage_cols(uint32_t dst, const float (&o)[32], int lane) {
+  const uint32_t col = (uint32_t)((lane & 7) * 2);
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(dst + sw64(k, lane >> 3) + col),
+                 "h"(__bfloat16_as_ushort(__float2bfloat16_rn(o[k])))
+                 : "memory");
+}
+
+// Store a warp's 32 x 32 block at (x0, y0) of matrix z, and with `mirror`
+// its transpose at (y0, x0), through the next of the warp's two staging
+// slots; TMA drops whatever falls outside the tensor.
+__device__ __forceinline__ void tma_store_block(const CUtensorMap *map, uint32_t stage, int &slot,
+                                                const float (&o)[32], bool mirror, int x0, int y0, int z, int lane) {
+  const uint32_t dst = stage + (uint32_t)(slot * kSlotBytes);
+  slot ^= 1;
+  if (lane == 0) bulk_wait_read<1>();  // the stores that last used this slot have read it
+  __syncwarp();
+  stage_rows(dst, o, lane);
+  if (mirror) stage_cols(dst + 2048, o, lane);
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(map, dst, x0, y0, z);
+    if (mirror) tma_store_3d(map, dst + 2048, y0, x0, z);
+    bulk_commit();
+  }
+}
+
 // Weight write of 32 consecutive elements of one stored row: W[row][c0..c0+31]
 // with the update directions u[0..31] (valid under `mask`).
 template <typename WT>
@@ -472,40 +545,22 @@ __device__ __forceinline__ void prefetch_weight_tile(const DevSub &S, int i0, in
   }
 }
 
-// Symmetric output: element (r, c) with r <= c is written directly and its
-// mirror (c, r) with r < c from the transposed block, so every element of
-// the p x p output is written exactly once by the tiles touching the upper
-// triangle.  `o` is destroyed (transposed in place).
-__device__ __forceinline__ void sym_store32(__nv_bfloat16 *out, const DevSub &S, int i0, int col0, float (&o)[32],
-                                            float *st, int lane) {
-  const int i = i0 + lane, p = S.p;
-  if (i < p) {  // direct: (i, j) with i <= j
-    const int jlo = max(i, col0);
-    const uint32_t mask = prefix_mask(p - col0) & ~prefix_mask(jlo - col0);
-    store_row32(out + (int64_t)i * S.ldp + col0, o, mask == 0xffffffffu, mask);
-  }
-  // mirror: lane l writes row col0 + l, columns i0 + r for i0 + r < col0 + l
-  warp_transpose32(o, st, lane);
-  const int jm = col0 + lane;
-  if (jm < p) {
-    const uint32_t mask = prefix_mask(p - i0) & prefix_mask(jm - i0);
-    store_row32(out + (int64_t)jm * S.ldp + i0, o, mask == 0xffffffffu, mask);
-  }
-}
-
 // Epilogue of one warp's 32 rows x 32 columns of the accumulator.  Lane r
 // holds row i0 + r in v[0..31] (columns col0 .. col0 + 31); s is the
 // matrix's folded pre-normalisation factor (1 unless the job folds it).
-__device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const TcJob &J, const DevSub &S, float s, int i0,
-                                               int col0, float (&v)[32], float *st, int lane) {
+// Outputs other than the weights leave through TMA stores from the warp's
+// staging slots (`stage`, `slot`); `st` is the same area as fp32, for the
+// weight write's transpose.
+__device__ __forceinline__ void epilogue_block(const TcParams &P, const PhaseArgs &A, int c, int mat,
+                                               const DevSub &S, float s, int i0, int col0, float (&v)[32],
+                                               uint32_t stage, int &slot, float *st, int lane) {
+  const TcJob &J = P.job[c];
   const int i = i0 + lane;
   if (J.mode == kProduct) {
-    if (i >= S.p) return;
     float o[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = s * v[k];
-    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(J.out) + S.x_off + (int64_t)i * S.ld + col0;
-    store_row32(dst, o, col0 + 32 <= S.q, prefix_mask(S.q - col0));
+    tma_store_block(&P.mapO[c], stage, slot, o, false, col0, i0, mat, lane);
     return;
   }
   if (J.mode == kFinal) {
@@ -520,7 +575,10 @@ __device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const TcJob &
       else weight_rmw32<float>(A, S, S.r0 + i, col0, u, mask);
     } else {
       // stored row = column of X: after the transpose lane l holds stored
-      // row col0 + l, stored columns i0 .. i0 + 31
+      // row col0 + l, stored columns i0 .. i0 + 31.  The staging area must
+      // be free of TMA stores still reading it.
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
       warp_transpose32(u, st, lane);
       if (col0 + lane >= S.q) return;
       const uint32_t mask = prefix_mask(S.p - i0);
@@ -529,9 +587,13 @@ __device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const TcJob &
     }
     return;
   }
-  // symmetric outputs: P = a I + b s^2 C, A = s^2 C, both (kGramAP), or
-  // P = a I + b A + c C (kSquare)
-  __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(J.out) + S.p_off;
+  // Symmetric outputs: P = a I + b s^2 C, A = s^2 C, both (kGramAP), or
+  // P = a I + b A + c C (kSquare).  Blocks are 32-aligned, so each lies on,
+  // above or below the diagonal.  A block above it is stored with its
+  // mirror; a block on it is stored whole; a block below it is the mirror
+  // of a block above and is skipped.  Every element is written once.
+  if (col0 + 32 <= i0) return;
+  const bool mirror = col0 >= i0 + 32;
   const int p = S.p;
   const float s2 = s * s;
   float o[32];
@@ -554,11 +616,11 @@ __device__ __forceinline__ void epilogue_block(const PhaseArgs &A, const TcJob &
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = s2 * v[k];
   }
-  sym_store32(out, S, i0, col0, o, st, lane);
+  tma_store_block(&P.mapO[c], stage, slot, o, mirror, col0, i0, mat, lane);
   if (J.mode == kGramAP) {  // and A = s^2 C
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = s2 * v[k];
-    sym_store32(reinterpret_cast<__nv_bfloat16 *>(J.out2) + S.p_off, S, i0, col0, o, st, lane);
+    tma_store_block(&P.mapO2[c], stage, slot, o, mirror, col0, i0, mat, lane);
   }
 }
 
@@ -570,11 +632,11 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   constexpr int kRows = Mode<kPair>::kRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes + kStageBytes);
   // bars: full[STAGES], empty[STAGES], accf[2], acce[2], drain
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
-  float *stage_base = reinterpret_cast<float *>(smem + kRingBytes + 256);
+  uint8_t *stage_base = smem + kRingBytes;  // epilogue staging, 1024-byte aligned
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
@@ -736,11 +798,11 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       }
     }
   } else {
-    // epilogue warps: TMEM lane quarter = warp % 4; with 8 warps, warps 6-9
-    // take columns 128-255 of the tile
+    // epilogue warps: TMEM lane quarter = warp % 4
     const int quarter = warp & 3;
-    const int half = kEpiWarps == 8 ? (warp - 2) >> 2 : 0;
-    const int nch = kEpiWarps == 8 ? BN / 64 : BN / 32;  // column chunks per warp
+    const uint32_t stage = smem_u32(stage_base + (warp - 2) * kWarpStageBytes);
+    float *st = reinterpret_cast<float *>(stage_base + (warp - 2) * kWarpStageBytes);
+    int slot = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
@@ -754,17 +816,16 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       tc_fence_after();
       const float s = J.first ? A.alpha[sub] : 1.0f;
       const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
-      float *st = stage_base + (warp - 2) * kStageFloats;
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       // skip column chunks that hold nothing this warp writes
       const int ncols = J.kind == kKindProd ? S.q : S.p;
 #pragma unroll 1
-      for (int ch = half * nch; ch < (half + 1) * nch; ++ch) {
+      for (int ch = 0; ch < BN / 32; ++ch) {
         const int col0 = tc.tn * BN + ch * 32;
         if (col0 >= ncols) break;
         float v[32];
         tmem_ld32(trow + ch * 32, v);
-        if (i0 < S.p) epilogue_block(A, J, S, s, i0, col0, v, st, lane);
+        if (i0 < S.p) epilogue_block(P, A, tc.c, tc.mat, S, s, i0, col0, v, stage, slot, st, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -774,6 +835,9 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       }
       if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
+    // this warp's TMA stores have landed before the kernel ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -813,9 +877,12 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D bf16 map over `count` row-major rows x cols matrices with row stride
-// `ld` elements, stored back to back; box = box_cols x box_rows x 1.
+// `ld` elements, stored back to back; box = box_cols x box_rows x 1.  Loads
+// use the 128-byte swizzle the MMA descriptors expect; stores (32 x 32
+// boxes) the 64-byte swizzle of the epilogue's staging slots.
 bool encode_map(CUtensorMap *map, void *base, int64_t cols, int64_t rows, int64_t count, int64_t ld,
-                uint32_t box_cols, uint32_t box_rows) {
+                uint32_t box_cols, uint32_t box_rows,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)count};
@@ -823,7 +890,7 @@ bool encode_map(CUtensorMap *map, void *base, int64_t cols, int64_t rows, int64_
   const cuuint32_t box[3] = {box_cols, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -918,6 +985,17 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
              encode_map(&T.mapB[k], const_cast<char *>(xbase(J.opB, C)), C.q, C.p, C.count, C.ld, 64, BK);
         Ndim = C.q;
         Kdim = C.p;
+      }
+      // outputs stored by TMA: a p x p matrix in the class's p-space, or X'
+      if (J.mode == kProduct) {
+        ok = ok && encode_map(&T.mapO[k], static_cast<char *>(J.out) + C.x_base * 2, C.q, C.p, C.count, C.ld, 32,
+                              32, CU_TENSOR_MAP_SWIZZLE_64B);
+      } else if (J.mode != kFinal) {
+        ok = ok && encode_map(&T.mapO[k], static_cast<char *>(J.out) + C.p_base * 2, C.p, C.p, C.count, C.ldp, 32,
+                              32, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (J.mode == kGramAP)
+          ok = ok && encode_map(&T.mapO2[k], static_cast<char *>(J.out2) + C.p_base * 2, C.p, C.p, C.count, C.ldp,
+                                32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
       }
       if (!ok) return (int)cudaErrorInvalidValue;
       TcJob &tj = T.job[k];
