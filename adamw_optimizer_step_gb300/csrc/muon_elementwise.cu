@@ -26,62 +26,6 @@ namespace {
 constexpr int kMomThreads = 256;
 constexpr int kMomWarps = kMomThreads / 32;  // one partial pair per warp and tile
 
-// Eight consecutive elements of a row as fp32: one 16-byte load (bf16) or
-// two (fp32) when `vec`, else element by element under `valid`.
-__device__ __forceinline__ void load8(const void *base, int32_t dtype, int64_t idx, int valid, bool vec,
-                                      float *out) {
-  if (vec && valid == 8) {
-    if (dtype == GBO_BF16) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + idx);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
-        out[2 * h] = __low2float(b);
-        out[2 * h + 1] = __high2float(b);
-      }
-    } else {
-      const float4 *f = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(base) + idx);
-      const float4 a = f[0], b = f[1];
-      out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-      out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) out[e] = e < valid ? ld_elem(base, dtype, idx + e) : 0.f;
-  }
-}
-
-// Eight consecutive elements: 16-byte store(s) when `vec` (the caller
-// guarantees alignment) and the segment is whole, else element by element.
-template <typename XT>
-__device__ __forceinline__ void store8(XT *dst, const float *v, int valid, bool vec) {
-  if (vec && valid == 8) {
-    if constexpr (sizeof(XT) == 2) {
-      uint4 u;
-      __nv_bfloat162 h[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
-      u.x = *reinterpret_cast<uint32_t *>(&h[0]);
-      u.y = *reinterpret_cast<uint32_t *>(&h[1]);
-      u.z = *reinterpret_cast<uint32_t *>(&h[2]);
-      u.w = *reinterpret_cast<uint32_t *>(&h[3]);
-      *reinterpret_cast<uint4 *>(dst) = u;
-    } else {
-      float4 *f = reinterpret_cast<float4 *>(dst);
-      f[0] = make_float4(v[0], v[1], v[2], v[3]);
-      f[1] = make_float4(v[4], v[5], v[6], v[7]);
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (e < valid) {
-        if constexpr (sizeof(XT) == 2) dst[e] = __float2bfloat16_rn(v[e]);
-        else dst[e] = v[e];
-      }
-  }
-}
-
 // One 64 x 64 tile of one matrix per loop trip.  256 threads: thread t
 // covers columns 8*(t%8) .. +7 of tile rows t/8 and t/8 + 32.  Every load
 // of the tile is issued before any arithmetic, so each thread keeps four

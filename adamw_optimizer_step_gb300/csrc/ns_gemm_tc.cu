@@ -519,6 +519,101 @@ __device__ __forceinline__ void weight_rmw32(const PhaseArgs &A, const DevSub &S
   }
 }
 
+// 32 consecutive bf16 weights of one row, as raw bits.
+struct WSeg {
+  uint4 q[4];
+};
+
+__device__ __forceinline__ void wseg_load(WSeg &r, const __nv_bfloat16 *w, bool vec, uint32_t mask) {
+  if (vec) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(w);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) r.q[q] = p[q];
+    return;
+  }
+  uint32_t h[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t lo = (mask >> (2 * k) & 1u) ? __bfloat16_as_ushort(w[2 * k]) : 0u;
+    const uint32_t hi = (mask >> (2 * k + 1) & 1u) ? __bfloat16_as_ushort(w[2 * k + 1]) : 0u;
+    h[k] = lo | (hi << 16);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) r.q[q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+}
+
+__device__ __forceinline__ void wseg_unpack(const WSeg &r, float (&o)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w[4] = {r.q[q].x, r.q[q].y, r.q[q].z, r.q[q].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
+      o[8 * q + 2 * h] = __low2float(b);
+      o[8 * q + 2 * h + 1] = __high2float(b);
+    }
+  }
+}
+
+// The last product's epilogue of one warp for one tile when W is bf16.  The
+// weights of chunk ch + 1 are loaded before chunk ch is computed, so a load
+// of each lane's row segment is always in flight instead of the warp
+// waiting on every chunk's loads in turn.  Lane r owns X row i0 + r; with a
+// transposed matrix it owns stored row col0 + r of each chunk after the
+// transpose.
+__device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub &S, float s, int i0, int tile_col0,
+                                                uint32_t trow, float *st, int lane) {
+  const int nch = min(BN / 32, (S.q - tile_col0 + 31) / 32);  // chunks holding columns < q
+  const float lr = A.lr * S.lr_mult, su = S.scale * s;
+  __nv_bfloat16 *W = reinterpret_cast<__nv_bfloat16 *>(S.w);
+  auto seg = [&](int ch, int64_t &widx, uint32_t &mask) -> bool {
+    const int col0 = tile_col0 + ch * 32;
+    if (!S.transposed) {
+      if (i0 + lane >= S.p) return false;
+      widx = (S.r0 + i0 + lane) * S.cols + col0;
+      mask = prefix_mask(S.q - col0);
+    } else {
+      if (col0 + lane >= S.q) return false;
+      widx = (S.r0 + col0 + lane) * S.cols + i0;
+      mask = prefix_mask(S.p - i0);
+    }
+    return true;
+  };
+  WSeg nxt;
+  int64_t widx_n = 0;
+  uint32_t mask_n = 0;
+  bool ok_n = seg(0, widx_n, mask_n);
+  if (ok_n) wseg_load(nxt, W + widx_n, S.w_vec && mask_n == 0xffffffffu, mask_n);
+#pragma unroll 1
+  for (int ch = 0; ch < nch; ++ch) {
+    const WSeg cur = nxt;
+    const int64_t widx = widx_n;
+    const uint32_t mask = mask_n;
+    const bool ok = ok_n;
+    if (ch + 1 < nch) {
+      ok_n = seg(ch + 1, widx_n, mask_n);
+      if (ok_n) wseg_load(nxt, W + widx_n, S.w_vec && mask_n == 0xffffffffu, mask_n);
+    }
+    float u[32];
+    tmem_ld32(trow + ch * 32, u);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) u[k] *= su;
+    if (S.transposed) warp_transpose32(u, st, lane);
+    if (ok) {
+      float w[32];
+      wseg_unpack(cur, w);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) w[k] = w[k] - lr * (S.wd * w[k] + u[k]);
+      const bool vec = S.w_vec && mask == 0xffffffffu;
+      store_row32(W + widx, w, vec, mask);
+      if (A.dbg) {
+        float *d = A.dbg + S.dbg_off + widx;
+        store_row32(d, u, mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0, mask);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -819,6 +914,15 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       // skip column chunks that hold nothing this warp writes
       const int ncols = J.kind == kKindProd ? S.q : S.p;
+      if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
+        if (i0 < S.p) {
+          if (S.transposed) {  // the transposes use the staging area: no TMA store may still read it
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+          }
+          final_tile_bf16(A, S, s, i0, tc.tn * BN, trow, st, lane);
+        }
+      } else
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         const int col0 = tc.tn * BN + ch * 32;
