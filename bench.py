@@ -34,7 +34,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
@@ -232,23 +232,43 @@ def traffic_record(kernel_file):
     return rec
 
 
-def run_e2e(n_steps, world, g_flat, ag_flat, step, total):
+def run_e2e(n_steps, world, bufs, step, total):
     """Steps/s with each step's gradients copied in from pinned host memory
-    (one transfer per flat gradient buffer) and the step's gradient norm read
-    back on the host.  Returns (steps/s over all ranks, bytes copied in per
-    step)."""
+    and the step's gradient norm read back on the host.  ``bufs`` holds two
+    (Muon, AdamW) flat gradient buffer pairs, each bound to its own plan:
+    the upload of step n + 1's gradients runs on a copy stream into one pair
+    while step n computes on the other, as a trainer overlaps its input
+    transfers.  Every step's copy and read stay inside the timed region.
+    Returns (steps/s over all ranks, bytes copied in per step)."""
     import torch
+    g_flat, ag_flat = bufs[0]
     h_g = torch.empty(g_flat.numel(), dtype=g_flat.dtype, pin_memory=True)
     h_ag = torch.empty(ag_flat.numel(), dtype=ag_flat.dtype, pin_memory=True)
     h_g.copy_(g_flat)
     h_ag.copy_(ag_flat)
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def upload(b):
+        copy.wait_event(done[b])  # the step that last read buffer pair b has finished
+        with torch.cuda.stream(copy):
+            bufs[b][0].copy_(h_g, non_blocking=True)
+            bufs[b][1].copy_(h_ag, non_blocking=True)
+        copied[b].record(copy)
+
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    for _ in range(n_steps):
-        g_flat.copy_(h_g, non_blocking=True)
-        ag_flat.copy_(h_ag, non_blocking=True)
-        step()
+    upload(0)
+    for n in range(n_steps):
+        b = n % 2
+        compute.wait_event(copied[b])
+        step(buf=b)
+        done[b].record(compute)
+        if n + 1 < n_steps:
+            upload(1 - b)
         _ = float(total.item())  # the step's result on the host
     torch.cuda.synchronize()
     e2e_t = max_over_ranks(time.perf_counter() - t0, world)
@@ -303,7 +323,9 @@ def run_ours(args):
     total = torch.zeros(1, device=dev)
     coef = torch.zeros(1, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    adam_grads = [p[1] for p in params]
+    # plans and AdamW tables bound to gradient buffer pairs (the end-to-end
+    # run adds a second pair)
+    bound = [(plan, params, [p[1] for p in params])]
     stream = torch.cuda.current_stream()
     side = torch.cuda.Stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -314,7 +336,7 @@ def run_ours(args):
     if overlap:
         gbo.gbo_muon_plan_set_event(plan, 0, after_momentum)
 
-    def step(record=None):
+    def step(record=None, buf=0):
         """One optimizer step: Muon, then clip + AdamW, on one stream.  With
         --overlap the AdamW path (independent of the Muon path) runs on a side
         stream that starts once the momentum kernel is done, overlapping the
@@ -322,16 +344,17 @@ def run_ours(args):
         Measured on GB300 the overlap saves nothing: the memory-bound AdamW
         slows the concurrent Gram products by about as much as it hides."""
         step_no[0] += 1
+        plan_b, params_b, adam_grads = bound[buf]
         if overlap:
             side.wait_stream(stream)
-        gbo.gbo_muon_step(plan, wl.lr, ws, dev_status=status, stream=stream)
+        gbo.gbo_muon_step(plan_b, wl.lr, ws, dev_status=status, stream=stream)
         adam_stream = side if overlap else stream
         if overlap:
             side.wait_event(after_momentum)
         if record is not None:
             record[0].record(adam_stream)
         gbo.gbo_clip_norm(adam_grads, 1.0, total, coef, cws, dev_status=status, stream=adam_stream)
-        gbo.gbo_adamw_step(params, lr=wl.adamw_lr, step=step_no[0], coef=coef, dev_status=status,
+        gbo.gbo_adamw_step(params_b, lr=wl.adamw_lr, step=step_no[0], coef=coef, dev_status=status,
                            stream=adam_stream)
         if record is not None:
             record[1].record(adam_stream)
@@ -375,7 +398,19 @@ def run_ours(args):
     # end to end: gradients from pinned host memory, norm read back
     e2e_value, h2d = None, 0
     if args.e2e_steps > 0:
-        e2e_value, h2d = run_e2e(args.e2e_steps, world, g_flat, ag_flat, step, total)
+        g_flat2, ag_flat2 = torch.empty_like(g_flat), torch.empty_like(ag_flat)
+        entries2, off = [], 0
+        for e in entries:
+            n = e["w"].numel()
+            entries2.append(dict(e, g=g_flat2[off:off + n].view(e["w"].shape)))
+            off += n
+        params2, off = [], 0
+        for p, g, m, v in params:
+            params2.append((p, ag_flat2[off:off + g.numel()].view(g.shape), m, v))
+            off += g.numel()
+        plan2 = gbo.gbo_muon_plan_create(entries2, precision=gbo.GBO_NS_BF16, normuon=wl.normuon)
+        bound.append((plan2, params2, [p[1] for p in params2]))
+        e2e_value, h2d = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total)
 
     if rank != 0:
         return
@@ -427,7 +462,9 @@ def run_ours(args):
         "ns_tflops": {"executed": achieved_tf, "counted_dense": counted_tf,
                       "executed_tflop_per_step": flops / 1e12, "counted_tflop_per_step": info["ns_flops"] / 1e12},
         "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "steps/s",
-                                               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4},
+                                               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4,
+                                               "overlap": "step n+1's gradient upload runs during step n "
+                                                          "(two gradient buffers)"},
         "gpu_launches": int(launches),
         "clocks": clk,
         "cpu_baseline": cpu,
