@@ -35,7 +35,7 @@ struct DevSub {
   int32_t ldp;      // P row stride (elements)
   int32_t tiles_c;  // momentum tiles along n (2-D tiles), or 0 for flat tiles
   int32_t ntiles;   // momentum tiles of this matrix
-  int32_t transposed;
+  int32_t transposed;  // X holds D^T (fp32 mode: tall matrices)
   int32_t w_dtype, g_dtype;
   int32_t vec_ok;   // g and mom rows start on 16-byte boundaries (n % 8 == 0)
   int32_t cls;
@@ -63,7 +63,7 @@ struct ShapeClass {
   int32_t count;  // matrices in the class
   int32_t sub0;   // index of the first matrix in the DevSub table
   int32_t route;  // kRouteX | kRouteGram
-  int32_t pad0;
+  int32_t tall;   // X holds the matrix in stored orientation, q x p (tensor-core path)
   int64_t x_base; // element offset of the class in each X buffer
   int64_t p_base; // element offset of the class in its p x p buffers (its route's space)
 };
@@ -80,12 +80,21 @@ enum GemmMode : int32_t {
   kGramAP = 5,    // C symmetric; write A = s^2 C and P = a I + b A
 };
 
-// Operand shapes of one tensor-core GEMM job.
+// Operand shapes of one tensor-core GEMM job.  X is p x q ("wide") or, for
+// a matrix stored with more rows than columns, q x p in stored orientation
+// ("tall"); the tall kinds are the transposes of the wide ones, so no
+// matrix is ever transposed in memory on the tensor-core path.
 enum GemmKind : int32_t {
-  kKindGram = 0,  // C = X X^T: A and B operands are rows of X (K = q), symmetric output
-  kKindSym = 1,   // C = L R, L and R symmetric p x p and commuting: symmetric output
-  kKindProd = 2,  // C = L X: L p x p, B = X with K along its rows (MN-major), p x q output
+  kKindGram = 0,   // C = X X^T, X wide: A and B operands are rows of X (K = q); symmetric output
+  kKindSym = 1,    // C = L R, L and R symmetric p x p and commuting: symmetric output
+  kKindProd = 2,   // C = L X, X wide: B = X with K along its rows (MN-major); p x q output
+  kKindGramT = 3,  // C = X^T X, X tall: A and B are columns of X (both MN-major, K = q); symmetric output
+  kKindProdT = 4,  // C = X L, X tall: A = rows of X (K = p), B = rows of L; q x p output
 };
+
+// Rows and columns of a job's output for matrix S.
+__host__ __device__ inline int kind_rows(int kind, int p, int q) { return kind == kKindProdT ? q : p; }
+__host__ __device__ inline int kind_cols(int kind, int p, int q) { return kind == kKindProd ? q : p; }
 
 // One shape class of a tensor-core launch and what it computes.  Operand
 // and output pointers are region bases; the launcher adds the class base
@@ -145,11 +154,12 @@ int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &glob
                       void *stream, int64_t *n_launch);
 // FLOPs the tensor-core kernel executes for one p x q matrix and one
 // iteration (Gram over the upper block-triangle of tiles, square when c != 0,
-// product), counting the zero padding of partial tiles.
-double tc_executed_flops(int p, int q, bool square);
+// product), counting the zero padding of partial tiles; `tall`: X is held
+// q x p and the product runs transposed.
+double tc_executed_flops(int p, int q, bool square, bool tall);
 // FLOPs executed for one p x q matrix over k iterations on the Gram route:
 // the Gram, 3k - 3 symmetric p x p products, the product with X_0.
-double tc_gram_route_flops(int p, int q, int k);
+double tc_gram_route_flops(int p, int q, int k, bool tall);
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);

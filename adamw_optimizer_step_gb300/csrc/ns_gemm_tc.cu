@@ -65,11 +65,9 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;                   // two 128 x 256 fp32 accumulators
 // Per epilogue warp: two 4 KB store slots, each a 32 x 32 bf16 block and its
-// transpose in the 64-byte-swizzled layout TMA stores read; the weight
-// write of the last product reuses the area as one 32 x 33 fp32 transpose.
+// transpose in the 64-byte-swizzled layout TMA stores read.
 constexpr int kSlotBytes = 4096;
 constexpr int kWarpStageBytes = 2 * kSlotBytes;
-static_assert(32 * 33 * 4 <= kWarpStageBytes, "transpose staging");
 constexpr int kStageBytes = kEpiWarps * kWarpStageBytes;
 constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + kStageBytes + 256 /*barriers*/;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -78,8 +76,8 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 // What one class of a launch computes, as the kernel sees it.
 struct TcJob {
   int32_t mode;   // GemmMode
-  int32_t kind;   // GemmKind: kKindProd has B = X MN-major and a full p x q output;
-                  // the others a symmetric p x p output (upper-triangle tiles only)
+  int32_t kind;   // GemmKind: the products have full outputs, the others a
+                  // symmetric p x p output (upper-triangle tiles only)
   int32_t first;  // s = alpha of the matrix (pre-normalisation folded in), else 1
   float a, b, c;
   void *out, *out2;
@@ -261,11 +259,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
-// A K-major, B K-major or MN-major, N = 256, M = 128 (one CTA) or 256 (pair).
-__host__ __device__ constexpr uint32_t make_idesc(int b_mn_major, int m) {
+// each K-major or MN-major, N = 256, M = 128 (one CTA) or 256 (pair).
+__host__ __device__ constexpr uint32_t make_idesc(int a_mn_major, int b_mn_major, int m) {
   return (1u << 4)                      // D format: f32
          | (1u << 7)                    // A format: bf16
          | (1u << 10)                   // B format: bf16
+         | ((uint32_t)a_mn_major << 15) // A major-ness
          | ((uint32_t)b_mn_major << 16) // B major-ness
          | ((uint32_t)(BN >> 3) << 17)  // N / 8
          | ((uint32_t)(m >> 4) << 24);  // M / 16
@@ -352,7 +351,7 @@ __device__ __forceinline__ TileCoord decode(const TcParams &P, int64_t t) {
   tc.mat = (int)(local / P.tiles_per_mat[c]);
   int rem = (int)(local % P.tiles_per_mat[c]);
   const int tn_all = P.tiles_n[c];
-  if (P.job[c].kind == kKindProd) {
+  if (P.job[c].kind == kKindProd || P.job[c].kind == kKindProdT) {
     tc.tm = rem / tn_all;
     tc.tn = rem % tn_all;
   } else {
@@ -439,18 +438,6 @@ __device__ __forceinline__ void load_row32(const T *src, float (&o)[32], bool ve
 
 __device__ __forceinline__ uint32_t prefix_mask(int n) {  // the low n bits, n in [0, 32]
   return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
-}
-
-// Transpose a warp's 32 x 32 block through shared memory: on entry lane r
-// holds row r (o[k] = B[r][k]); on exit lane l holds column l
-// (o[r] = B[r][l]).  `st` is this warp's [32][33] staging area.
-__device__ __forceinline__ void warp_transpose32(float (&o)[32], float *st, int lane) {
-#pragma unroll
-  for (int k = 0; k < 32; ++k) st[lane * 33 + k] = o[k];
-  __syncwarp();
-#pragma unroll
-  for (int r = 0; r < 32; ++r) o[r] = st[r * 33 + lane];
-  __syncwarp();
 }
 
 // Byte offset of 16-byte chunk q of row r in a 32-row x 64-byte bf16 block in
@@ -556,58 +543,44 @@ __device__ __forceinline__ void wseg_unpack(const WSeg &r, float (&o)[32]) {
 }
 
 // The last product's epilogue of one warp for one tile when W is bf16.  The
-// weights of chunk ch + 1 are loaded before chunk ch is computed, so a load
-// of each lane's row segment is always in flight instead of the warp
-// waiting on every chunk's loads in turn.  Lane r owns X row i0 + r; with a
-// transposed matrix it owns stored row col0 + r of each chunk after the
-// transpose.
+// output is in stored orientation (rows x cols of the matrix); lane r owns
+// stored row r0 + i0 + r.  The weights of chunk ch + 1 are loaded before
+// chunk ch is computed, so a load of each lane's row segment is always in
+// flight instead of the warp waiting on every chunk's loads in turn.
 __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub &S, float s, int i0, int tile_col0,
-                                                uint32_t trow, float *st, int lane) {
-  const int nch = min(BN / 32, (S.q - tile_col0 + 31) / 32);  // chunks holding columns < q
+                                                int rows, int cols, uint32_t trow, int lane) {
+  const int nch = min(BN / 32, (cols - tile_col0 + 31) / 32);  // chunks holding columns < cols
   const float lr = A.lr * S.lr_mult, su = S.scale * s;
   __nv_bfloat16 *W = reinterpret_cast<__nv_bfloat16 *>(S.w);
-  auto seg = [&](int ch, int64_t &widx, uint32_t &mask) -> bool {
-    const int col0 = tile_col0 + ch * 32;
-    if (!S.transposed) {
-      if (i0 + lane >= S.p) return false;
-      widx = (S.r0 + i0 + lane) * S.cols + col0;
-      mask = prefix_mask(S.q - col0);
-    } else {
-      if (col0 + lane >= S.q) return false;
-      widx = (S.r0 + col0 + lane) * S.cols + i0;
-      mask = prefix_mask(S.p - i0);
-    }
-    return true;
-  };
+  const bool ok = i0 + lane < rows;
+  const int64_t wrow = (S.r0 + i0 + lane) * S.cols;
   WSeg nxt;
-  int64_t widx_n = 0;
-  uint32_t mask_n = 0;
-  bool ok_n = seg(0, widx_n, mask_n);
-  if (ok_n) wseg_load(nxt, W + widx_n, S.w_vec && mask_n == 0xffffffffu, mask_n);
+  if (ok) {
+    const uint32_t m0 = prefix_mask(cols - tile_col0);
+    wseg_load(nxt, W + wrow + tile_col0, S.w_vec && m0 == 0xffffffffu, m0);
+  }
 #pragma unroll 1
   for (int ch = 0; ch < nch; ++ch) {
     const WSeg cur = nxt;
-    const int64_t widx = widx_n;
-    const uint32_t mask = mask_n;
-    const bool ok = ok_n;
-    if (ch + 1 < nch) {
-      ok_n = seg(ch + 1, widx_n, mask_n);
-      if (ok_n) wseg_load(nxt, W + widx_n, S.w_vec && mask_n == 0xffffffffu, mask_n);
+    const int col0 = tile_col0 + ch * 32;
+    const uint32_t mask = prefix_mask(cols - col0);
+    if (ok && ch + 1 < nch) {
+      const uint32_t mn = prefix_mask(cols - col0 - 32);
+      wseg_load(nxt, W + wrow + col0 + 32, S.w_vec && mn == 0xffffffffu, mn);
     }
     float u[32];
     tmem_ld32(trow + ch * 32, u);
-#pragma unroll
-    for (int k = 0; k < 32; ++k) u[k] *= su;
-    if (S.transposed) warp_transpose32(u, st, lane);
     if (ok) {
       float w[32];
       wseg_unpack(cur, w);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) w[k] = w[k] - lr * (S.wd * w[k] + u[k]);
-      const bool vec = S.w_vec && mask == 0xffffffffu;
-      store_row32(W + widx, w, vec, mask);
+      for (int k = 0; k < 32; ++k) {
+        u[k] *= su;
+        w[k] = w[k] - lr * (S.wd * w[k] + u[k]);
+      }
+      store_row32(W + wrow + col0, w, S.w_vec && mask == 0xffffffffu, mask);
       if (A.dbg) {
-        float *d = A.dbg + S.dbg_off + widx;
+        float *d = A.dbg + S.dbg_off + wrow + col0;
         store_row32(d, u, mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0, mask);
       }
     }
@@ -619,36 +592,26 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
 }
 
 // Bring into L2 the weight elements the last product's epilogue of this
-// warp will read-modify-write for the tile at (i0.., col0 .. col0 + BN): the
-// warp issues them while it waits for the tile's accumulator.
-__device__ __forceinline__ void prefetch_weight_tile(const DevSub &S, int i0, int col0, int lane) {
+// warp will read-modify-write for the tile at (i0.., col0 .. col0 + BN) of
+// the stored-orientation output (rows x cols).
+__device__ __forceinline__ void prefetch_weight_tile(const DevSub &S, int i0, int col0, int rows, int cols,
+                                                     int lane) {
   const int64_t es = S.w_dtype == GBO_BF16 ? 2 : 4;
   const char *w = static_cast<const char *>(S.w);
-  if (!S.transposed) {
-    const int i = i0 + lane;  // stored row r0 + i, stored columns col0 ..
-    if (i >= S.p) return;
-    const int c1 = min(S.q, col0 + BN);
-    for (int c = col0; c < c1; c += (int)(128 / es))
-      prefetch_l2(w + ((S.r0 + i) * S.cols + c) * es);
-  } else {
-    if (i0 >= S.p) return;   // stored rows r0 + col0 + k, stored columns i0 .. i0 + 31
-#pragma unroll
-    for (int j = 0; j < BN / 32; ++j) {
-      const int c = col0 + lane + 32 * j;
-      if (c < S.q) prefetch_l2(w + ((S.r0 + c) * S.cols + i0) * es);
-    }
-  }
+  const int i = i0 + lane;
+  if (i >= rows) return;
+  const int c1 = min(cols, col0 + BN);
+  for (int c = col0; c < c1; c += (int)(128 / es)) prefetch_l2(w + ((S.r0 + i) * S.cols + c) * es);
 }
 
 // Epilogue of one warp's 32 rows x 32 columns of the accumulator.  Lane r
 // holds row i0 + r in v[0..31] (columns col0 .. col0 + 31); s is the
 // matrix's folded pre-normalisation factor (1 unless the job folds it).
 // Outputs other than the weights leave through TMA stores from the warp's
-// staging slots (`stage`, `slot`); `st` is the same area as fp32, for the
-// weight write's transpose.
+// staging slots (`stage`, `slot`).
 __device__ __forceinline__ void epilogue_block(const TcParams &P, const PhaseArgs &A, int c, int mat,
                                                const DevSub &S, float s, int i0, int col0, float (&v)[32],
-                                               uint32_t stage, int &slot, float *st, int lane) {
+                                               uint32_t stage, int &slot, int lane) {
   const TcJob &J = P.job[c];
   const int i = i0 + lane;
   if (J.mode == kProduct) {
@@ -658,28 +621,13 @@ __device__ __forceinline__ void epilogue_block(const TcParams &P, const PhaseArg
     tma_store_block(&P.mapO[c], stage, slot, o, false, col0, i0, mat, lane);
     return;
   }
-  if (J.mode == kFinal) {
-    // O = s * C; the update direction is scale * O
+  if (J.mode == kFinal) {  // fp32 weights: O = s * C, the update direction is scale * O
+    const int rows = kind_rows(J.kind, S.p, S.q), cols = kind_cols(J.kind, S.p, S.q);
+    if (i >= rows) return;
     float u[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) u[k] = S.scale * s * v[k];
-    if (!S.transposed) {
-      if (i >= S.p) return;
-      const uint32_t mask = prefix_mask(S.q - col0);
-      if (S.w_dtype == GBO_BF16) weight_rmw32<__nv_bfloat16>(A, S, S.r0 + i, col0, u, mask);
-      else weight_rmw32<float>(A, S, S.r0 + i, col0, u, mask);
-    } else {
-      // stored row = column of X: after the transpose lane l holds stored
-      // row col0 + l, stored columns i0 .. i0 + 31.  The staging area must
-      // be free of TMA stores still reading it.
-      if (lane == 0) bulk_wait_read<0>();
-      __syncwarp();
-      warp_transpose32(u, st, lane);
-      if (col0 + lane >= S.q) return;
-      const uint32_t mask = prefix_mask(S.p - i0);
-      if (S.w_dtype == GBO_BF16) weight_rmw32<__nv_bfloat16>(A, S, S.r0 + col0 + lane, i0, u, mask);
-      else weight_rmw32<float>(A, S, S.r0 + col0 + lane, i0, u, mask);
-    }
+    weight_rmw32<float>(A, S, S.r0 + i, col0, u, prefix_mask(cols - col0));
     return;
   }
   // Symmetric outputs: P = a I + b s^2 C, A = s^2 C, both (kGramAP), or
@@ -717,6 +665,94 @@ __device__ __forceinline__ void epilogue_block(const TcParams &P, const PhaseArg
     for (int k = 0; k < 32; ++k) o[k] = s2 * v[k];
     tma_store_block(&P.mapO2[c], stage, slot, o, mirror, col0, i0, mat, lane);
   }
+}
+
+// The producer's and the MMA issuer's work for one tile, specialised on the
+// operand layouts (A, B K-major or MN-major), so that the single-thread
+// issue loops carry no per-k-block choices.  Return false on a time-out.
+template <bool kPair, bool kAmn, bool kBmn>
+__device__ __forceinline__ bool produce_tile(const TcParams &P, const TileCoord &tc, int tm, uint8_t *smem,
+                                             uint32_t full0, uint32_t empty0, uint32_t full_lead0, bool leader,
+                                             uint32_t crank, int &stage, uint32_t &phase, uint32_t *armed_parity,
+                                             bool *armed, volatile int32_t *abort_flag) {
+  constexpr int STAGES = Mode<kPair>::kStages;
+  constexpr int STAGE_BYTES = Mode<kPair>::kStageBytes;
+  const CUtensorMap *ma = &P.mapA[tc.c], *mb = &P.mapB[tc.c];
+  const int kit = P.k_iters[tc.c];
+  const int m0 = tm * BM;
+  const int n0 = tc.tn * BN + (kPair ? (int)crank * (BN / 2) : 0);  // this CTA's first B row (column of C)
+  for (int kb = 0; kb < kit; ++kb) {
+    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) return false;
+    if (*abort_flag) return true;
+    if (leader) {
+      mbar_expect_tx(full0 + 8 * stage, (kPair ? 2 : 1) * STAGE_BYTES);
+      armed[stage] = true;
+      armed_parity[stage] = phase;
+    }
+    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+    const uint32_t sb = sa + A_BYTES;
+    const int k0 = kb * BK;
+    if constexpr (kPair) {
+      const uint32_t fb = full_lead0 + 8 * stage;
+      if constexpr (!kAmn) {
+        tma_load_3d_pair(sa, ma, fb, k0, m0, tc.mat);
+      } else {  // this CTA's 128 rows of A = columns of X, as two 64-column boxes
+#pragma unroll
+        for (int h = 0; h < BM / 64; ++h) tma_load_3d_pair(sa + h * 8192, ma, fb, m0 + h * 64, k0, tc.mat);
+      }
+      if constexpr (!kBmn) {
+        tma_load_3d_pair(sb, mb, fb, k0, n0, tc.mat);
+      } else {
+#pragma unroll
+        for (int h = 0; h < BN / 128; ++h) tma_load_3d_pair(sb + h * 8192, mb, fb, n0 + h * 64, k0, tc.mat);
+      }
+    } else {
+      const uint32_t fb = full0 + 8 * stage;
+      if constexpr (!kAmn) {
+        tma_load_3d(sa, ma, fb, k0, m0, tc.mat);
+      } else {
+#pragma unroll
+        for (int h = 0; h < BM / 64; ++h) tma_load_3d(sa + h * 8192, ma, fb, m0 + h * 64, k0, tc.mat);
+      }
+      if constexpr (!kBmn) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tma_load_3d(sb + h * B_HALF, mb, fb, k0, n0 + h * (BN / 2), tc.mat);
+      } else {
+#pragma unroll
+        for (int h = 0; h < BN / 64; ++h) tma_load_3d(sb + h * 8192, mb, fb, n0 + h * 64, k0, tc.mat);
+      }
+    }
+    if (++stage == STAGES) stage = 0, phase ^= 1;
+  }
+  return true;
+}
+
+template <bool kPair, bool kAmn, bool kBmn>
+__device__ __forceinline__ bool mma_tile(uint8_t *smem, uint32_t full0, uint32_t empty0, uint32_t d_tmem, int kit,
+                                         int &stage, uint32_t &phase, bool &issued) {
+  constexpr int STAGES = Mode<kPair>::kStages;
+  constexpr int STAGE_BYTES = Mode<kPair>::kStageBytes;
+  constexpr uint32_t idesc = make_idesc(kAmn, kBmn, Mode<kPair>::kRows * BM);
+  // descriptors of stage 0, K step 0: a stage is STAGE_BYTES further, a K
+  // step of 16 is 32 bytes (K-major) or two 8-row groups, 2048 bytes (MN-major)
+  const uint64_t a0 = smem_desc(smem_u32(smem), kAmn ? 8192 : 16, 1024);
+  const uint64_t b0 = smem_desc(smem_u32(smem) + A_BYTES, kBmn ? 8192 : 16, 1024);
+  constexpr uint32_t astep = (kAmn ? 2048 : 32) >> 4, bstep = (kBmn ? 2048 : 32) >> 4;
+  for (int kb = 0; kb < kit; ++kb) {
+    if (!mbar_wait(full0 + 8 * stage, phase)) return false;
+    tc_fence_after();
+    const uint32_t soff = (uint32_t)(stage * STAGE_BYTES) >> 4;
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k) {
+      if constexpr (kPair) mma_bf16_pair(d_tmem, a0 + soff + k * astep, b0 + soff + k * bstep, idesc, (kb | k) != 0);
+      else mma_bf16_one(d_tmem, a0 + soff + k * astep, b0 + soff + k * bstep, idesc, (kb | k) != 0);
+    }
+    issued = true;
+    if constexpr (kPair) mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs
+    else mma_commit_one(empty0 + 8 * stage);
+    if (++stage == STAGES) stage = 0, phase ^= 1;
+  }
+  return true;
 }
 
 template <bool kPair>
@@ -799,45 +835,18 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
         const TileCoord tc = decode<kRows>(P, t);
         const int tm = kRows * tc.tm + (int)crank;
-        const int kit = P.k_iters[tc.c];
-        for (int kb = 0; kb < kit; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) { give_up(); break; }
-          if (*abort_flag) break;
-          if (leader) {
-            mbar_expect_tx(full0 + 8 * stage, (kPair ? 2 : 1) * STAGE_BYTES);
-            armed[stage] = true;
-            armed_parity[stage] = phase;
-          }
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
-          if constexpr (kPair) {
-            const uint32_t fb = full_lead0 + 8 * stage;
-            tma_load_3d_pair(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
-            // this CTA's half of B: columns tn * BN + crank * BN / 2 ...
-            const int n0 = tc.tn * BN + (int)crank * (BN / 2);
-            if (P.job[tc.c].kind != kKindProd) {
-              tma_load_3d_pair(sb, &P.mapB[tc.c], fb, kb * BK, n0, tc.mat);
-            } else {
-#pragma unroll
-              for (int h = 0; h < BN / 128; ++h)
-                tma_load_3d_pair(sb + h * 8192, &P.mapB[tc.c], fb, n0 + h * 64, kb * BK, tc.mat);
-            }
-          } else {
-            const uint32_t fb = full0 + 8 * stage;
-            tma_load_3d(sa, &P.mapA[tc.c], fb, kb * BK, tm * BM, tc.mat);
-            const int n0 = tc.tn * BN;
-            if (P.job[tc.c].kind != kKindProd) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                tma_load_3d(sb + h * B_HALF, &P.mapB[tc.c], fb, kb * BK, n0 + h * (BN / 2), tc.mat);
-            } else {
-#pragma unroll
-              for (int h = 0; h < BN / 64; ++h)
-                tma_load_3d(sb + h * 8192, &P.mapB[tc.c], fb, n0 + h * 64, kb * BK, tc.mat);
-            }
-          }
-          if (++stage == STAGES) stage = 0, phase ^= 1;
-        }
+        const int kind = P.job[tc.c].kind;
+        bool ok;
+        if (kind == kKindGramT)
+          ok = produce_tile<kPair, true, true>(P, tc, tm, smem, full0, empty0, full_lead0, leader, crank, stage, phase,
+                                               armed_parity, armed, abort_flag);
+        else if (kind == kKindProd)
+          ok = produce_tile<kPair, false, true>(P, tc, tm, smem, full0, empty0, full_lead0, leader, crank, stage,
+                                                phase, armed_parity, armed, abort_flag);
+        else
+          ok = produce_tile<kPair, false, false>(P, tc, tm, smem, full0, empty0, full_lead0, leader, crank, stage,
+                                                 phase, armed_parity, armed, abort_flag);
+        if (!ok) { give_up(); break; }
       }
       if (*abort_flag && leader) {
         // let every copy armed here land before shared memory goes away
@@ -855,32 +864,17 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
         const TileCoord tc = decode<kRows>(P, t);
         const int kit = P.k_iters[tc.c];
-        const int bmn = P.job[tc.c].kind == kKindProd ? 1 : 0;
-        const uint32_t idesc = make_idesc(bmn, kRows * BM);
+        const int kind = P.job[tc.c].kind;
         const bool freed = kPair ? mbar_wait_cluster(acce0 + 8 * acc, acc_phase ^ 1)
                                  : mbar_wait(acce0 + 8 * acc, acc_phase ^ 1);
         if (!freed) { give_up(); break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        bool bad = false;
-        for (int kb = 0; kb < kit; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase)) { give_up(); bad = true; break; }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
-            const uint64_t bd = bmn ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
-            if constexpr (kPair) mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
-            else mma_bf16_one(d_tmem, ad, bd, idesc, (kb | k) != 0);
-          }
-          issued = true;
-          if constexpr (kPair) mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs
-          else mma_commit_one(empty0 + 8 * stage);
-          if (++stage == STAGES) stage = 0, phase ^= 1;
-        }
-        if (bad) break;
+        bool ok;
+        if (kind == kKindGramT) ok = mma_tile<kPair, true, true>(smem, full0, empty0, d_tmem, kit, stage, phase, issued);
+        else if (kind == kKindProd) ok = mma_tile<kPair, false, true>(smem, full0, empty0, d_tmem, kit, stage, phase, issued);
+        else ok = mma_tile<kPair, false, false>(smem, full0, empty0, d_tmem, kit, stage, phase, issued);
+        if (!ok) { give_up(); break; }
         if constexpr (kPair) mma_commit_pair_mc(accf0 + 8 * acc, 0x3);  // accumulator ready in both TMEMs
         else mma_commit_one(accf0 + 8 * acc);
         if (++acc == 2) acc = 0, acc_phase ^= 1;
@@ -896,7 +890,6 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     // epilogue warps: TMEM lane quarter = warp % 4
     const int quarter = warp & 3;
     const uint32_t stage = smem_u32(stage_base + (warp - 2) * kWarpStageBytes);
-    float *st = reinterpret_cast<float *>(stage_base + (warp - 2) * kWarpStageBytes);
     int slot = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -905,31 +898,27 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const int sub = P.sub0[tc.c] + tc.mat;
       const DevSub &S = A.subs[sub];
       const TcJob &J = P.job[tc.c];
-      if (J.mode == kFinal)
-        prefetch_weight_tile(S, (kRows * tc.tm + (int)crank) * BM + quarter * 32, tc.tn * BN, lane);
+      const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
+      // the job's output is rows x cols (stored orientation for the weights)
+      const int rows = kind_rows(J.kind, S.p, S.q), cols = kind_cols(J.kind, S.p, S.q);
+      if (J.mode == kFinal) prefetch_weight_tile(S, i0, tc.tn * BN, rows, cols, lane);
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
       tc_fence_after();
       const float s = J.first ? A.alpha[sub] : 1.0f;
-      const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      // skip column chunks that hold nothing this warp writes
-      const int ncols = J.kind == kKindProd ? S.q : S.p;
-      if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
-        if (i0 < S.p) {
-          if (S.transposed) {  // the transposes use the staging area: no TMA store may still read it
-            if (lane == 0) bulk_wait_read<0>();
-            __syncwarp();
-          }
-          final_tile_bf16(A, S, s, i0, tc.tn * BN, trow, st, lane);
-        }
-      } else
+      if (i0 < rows) {  // warps whose rows are all padding have nothing to write
+        if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
+          final_tile_bf16(A, S, s, i0, tc.tn * BN, rows, cols, trow, lane);
+        } else {
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        const int col0 = tc.tn * BN + ch * 32;
-        if (col0 >= ncols) break;
-        float v[32];
-        tmem_ld32(trow + ch * 32, v);
-        if (i0 < S.p) epilogue_block(P, A, tc.c, tc.mat, S, s, i0, col0, v, stage, slot, st, lane);
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            const int col0 = tc.tn * BN + ch * 32;
+            if (col0 >= cols) break;  // column chunks past the output hold nothing to write
+            float v[32];
+            tmem_ld32(trow + ch * 32, v);
+            epilogue_block(P, A, tc.c, tc.mat, S, s, i0, col0, v, stage, slot, lane);
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -1006,19 +995,20 @@ bool single_mode(int p) { return p <= BM; }
 
 namespace {
 
-// Work items of one matrix: kRows consecutive 128-row tiles x one column
-// tile; in pair mode an odd tile-row count runs one all-padding tile in the
+// Work items of one matrix of a class with p oriented rows: kRows
+// consecutive 128-row tiles x one column tile, over an output of `rows`
+// rows; in pair mode an odd tile-row count runs one all-padding tile in the
 // last pair.
-int items_m_of(int p) {
-  const int rows = single_mode(p) ? 1 : 2;
-  return ((p + BM - 1) / BM + rows - 1) / rows;
+int items_m_of(int p, int rows) {
+  const int k = single_mode(p) ? 1 : 2;
+  return ((rows + BM - 1) / BM + k - 1) / k;
 }
 
 int64_t sym_items_of(int p) {
   const int rows = single_mode(p) ? 1 : 2;
   const int tiles_n = (p + BN - 1) / BN;
   int64_t n = 0;
-  for (int r = 0; r < items_m_of(p); ++r) n += std::max(0, tiles_n - tri_tn_min(rows * r));
+  for (int r = 0; r < items_m_of(p, p); ++r) n += std::max(0, tiles_n - tri_tn_min(rows * r));
   return n;
 }
 
@@ -1027,18 +1017,23 @@ double item_flops(int p, int kdim) {  // one work item: rows x 128 x 256 outputs
   return 2.0 * rows * BM * BN * (double)((kdim + BK - 1) / BK) * BK;
 }
 
-}  // namespace
-
-double tc_executed_flops(int p, int q, bool square) {
-  double f = sym_items_of(p) * item_flops(p, q);                        // Gram, K = q
-  if (square) f += sym_items_of(p) * item_flops(p, p);                  // A A
-  f += (double)items_m_of(p) * ((q + BN - 1) / BN) * item_flops(p, p);  // product, K = p
-  return f;
+// The p x q product (wide: p x q output) or its transpose (tall: q x p).
+double product_flops(int p, int q, bool tall) {
+  return tall ? (double)items_m_of(p, q) * ((p + BN - 1) / BN) * item_flops(p, p)
+              : (double)items_m_of(p, p) * ((q + BN - 1) / BN) * item_flops(p, p);
 }
 
-double tc_gram_route_flops(int p, int q, int k) {
+}  // namespace
+
+double tc_executed_flops(int p, int q, bool square, bool tall) {
+  double f = sym_items_of(p) * item_flops(p, q);                  // Gram, K = q
+  if (square) f += sym_items_of(p) * item_flops(p, p);            // A A
+  return f + product_flops(p, q, tall);                           // product, K = p
+}
+
+double tc_gram_route_flops(int p, int q, int k, bool tall) {
   return sym_items_of(p) * item_flops(p, q) + (3.0 * k - 3.0) * sym_items_of(p) * item_flops(p, p) +
-         (double)items_m_of(p) * ((q + BN - 1) / BN) * item_flops(p, p);
+         product_flops(p, q, tall);
 }
 
 namespace {
@@ -1072,28 +1067,35 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
       const GemmJob &J = *jobs[j0 + k];
       const ShapeClass &C = *J.cls;
       bool ok;
-      int Ndim, Kdim;
-      if (J.kind == kKindGram) {  // A = X rows, B = X rows, K = q
-        void *x = const_cast<char *>(xbase(J.opA, C));
+      int Mdim, Ndim, Kdim;
+      void *x = const_cast<char *>(xbase(J.kind == kKindProd ? J.opB : J.opA, C));
+      if (J.kind == kKindGram) {  // X wide: A = X rows, B = X rows, K = q
         ok = encode_map(&T.mapA[k], x, C.q, C.p, C.count, C.ld, BK, BM) &&
              encode_map(&T.mapB[k], x, C.q, C.p, C.count, C.ld, BK, BN / 2);
-        Ndim = C.p;
-        Kdim = C.q;
+        Mdim = C.p, Ndim = C.p, Kdim = C.q;
+      } else if (J.kind == kKindGramT) {  // X tall: A and B = columns of X (MN-major boxes), K = q
+        ok = encode_map(&T.mapA[k], x, C.p, C.q, C.count, C.ld, 64, BK) &&
+             encode_map(&T.mapB[k], x, C.p, C.q, C.count, C.ld, 64, BK);
+        Mdim = C.p, Ndim = C.p, Kdim = C.q;
       } else if (J.kind == kKindSym) {  // A = L rows, B = R rows (R symmetric), K = p
         ok = encode_map(&T.mapA[k], const_cast<char *>(pbase(J.opA, C)), C.p, C.p, C.count, C.ldp, BK, BM) &&
              encode_map(&T.mapB[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 2);
-        Ndim = C.p;
-        Kdim = C.p;
-      } else {  // A = L rows (K = p), B = X with rows as K, columns as N
+        Mdim = C.p, Ndim = C.p, Kdim = C.p;
+      } else if (J.kind == kKindProd) {  // X wide: A = L rows (K = p), B = X with rows as K, columns as N
         ok = encode_map(&T.mapA[k], const_cast<char *>(pbase(J.opA, C)), C.p, C.p, C.count, C.ldp, BK, BM) &&
-             encode_map(&T.mapB[k], const_cast<char *>(xbase(J.opB, C)), C.q, C.p, C.count, C.ld, 64, BK);
-        Ndim = C.q;
-        Kdim = C.p;
+             encode_map(&T.mapB[k], x, C.q, C.p, C.count, C.ld, 64, BK);
+        Mdim = C.p, Ndim = C.q, Kdim = C.p;
+      } else {  // kKindProdT, X tall: A = X rows (K = p), B = L rows (L symmetric)
+        ok = encode_map(&T.mapA[k], x, C.p, C.q, C.count, C.ld, BK, BM) &&
+             encode_map(&T.mapB[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 2);
+        Mdim = C.q, Ndim = C.p, Kdim = C.p;
       }
       // outputs stored by TMA: a p x p matrix in the class's p-space, or X'
       if (J.mode == kProduct) {
-        ok = ok && encode_map(&T.mapO[k], static_cast<char *>(J.out) + C.x_base * 2, C.q, C.p, C.count, C.ld, 32,
-                              32, CU_TENSOR_MAP_SWIZZLE_64B);
+        char *xo = static_cast<char *>(J.out) + C.x_base * 2;
+        ok = ok && (J.kind == kKindProdT
+                        ? encode_map(&T.mapO[k], xo, C.p, C.q, C.count, C.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
+                        : encode_map(&T.mapO[k], xo, C.q, C.p, C.count, C.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       } else if (J.mode != kFinal) {
         ok = ok && encode_map(&T.mapO[k], static_cast<char *>(J.out) + C.p_base * 2, C.p, C.p, C.count, C.ldp, 32,
                               32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -1115,8 +1117,8 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
       T.tiles_n[k] = (Ndim + BN - 1) / BN;
       T.k_iters[k] = (Kdim + BK - 1) / BK;
       T.sub0[k] = C.sub0;
-      const int items_m = ((C.p + BM - 1) / BM + kRows - 1) / kRows;
-      if (J.kind != kKindProd) {
+      const int items_m = ((Mdim + BM - 1) / BM + kRows - 1) / kRows;
+      if (J.kind != kKindProd && J.kind != kKindProdT) {
         int cnt = 0;
         for (int r = 0; r < items_m; ++r) cnt += std::max(0, T.tiles_n[k] - tri_tn_min(kRows * r));
         T.tiles_per_mat[k] = cnt;

@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <string>
 #include <utility>
@@ -154,12 +155,12 @@ namespace {
 // Route of a p x q class: the Gram route needs bf16 mode, k >= 2 and c == 0
 // in every iteration; AUTO takes it when it executes at least 10% fewer
 // FLOPs (in practice: whenever q is clearly above p).
-int32_t choose_route(const gbo_plan *P, int p, int q) {
+int32_t choose_route(const gbo_plan *P, int p, int q, bool tall) {
   const int k = P->opts.ns_steps;
   if (P->x_dtype != GBO_BF16 || P->any_c || k < 2 || P->opts.route == GBO_ROUTE_X) return kRouteX;
   if (P->opts.route == GBO_ROUTE_GRAM) return kRouteGram;
-  const double fx = k * tc_executed_flops(p, q, false);
-  return tc_gram_route_flops(p, q, k) < 0.9 * fx ? kRouteGram : kRouteX;
+  const double fx = k * tc_executed_flops(p, q, false, tall);
+  return tc_gram_route_flops(p, q, k, tall) < 0.9 * fx ? kRouteGram : kRouteX;
 }
 
 int validate_and_expand(gbo_plan *P) {
@@ -171,8 +172,13 @@ int validate_and_expand(gbo_plan *P) {
     int32_t order;
   };
   std::vector<DevSub> subs;
-  std::map<std::pair<int32_t, int32_t>, int32_t> class_of;
-  std::vector<std::pair<int32_t, int32_t>> class_shapes;
+  // classes: (p, q, tall); the tensor-core path keeps a matrix with more
+  // rows than columns in stored orientation ("tall"), the fp32 path holds
+  // its transpose
+  using ClassKey = std::tuple<int32_t, int32_t, int32_t>;
+  std::map<ClassKey, int32_t> class_of;
+  std::vector<ClassKey> class_shapes;
+  const bool tc_path = P->x_dtype == GBO_BF16;
   int64_t dbg_off = 0;
   for (int32_t t = 0; t < n; ++t) {
     const gbo_muon_desc &d = P->descs[t];
@@ -253,7 +259,7 @@ int validate_and_expand(gbo_plan *P) {
         S.cols = d.cols;
         S.m = (int32_t)s;
         S.n = (int32_t)d.cols;
-        S.transposed = S.m > S.n;
+        S.transposed = !tc_path && S.m > S.n;
         S.p = std::min(S.m, S.n);
         S.q = std::max(S.m, S.n);
         S.w_dtype = d.w_dtype;
@@ -264,7 +270,7 @@ int validate_and_expand(gbo_plan *P) {
         S.lr_mult = d.lr_mult;
         S.wd = d.wd;
         S.dbg_off = this_dbg;
-        const auto key = std::make_pair(S.p, S.q);
+        const ClassKey key(S.p, S.q, tc_path && S.m > S.n ? 1 : 0);
         auto it = class_of.find(key);
         if (it == class_of.end()) {
           it = class_of.emplace(key, (int32_t)class_shapes.size()).first;
@@ -279,7 +285,9 @@ int validate_and_expand(gbo_plan *P) {
   // Route of each class; X-route classes first, so the second X buffer only
   // spans them when nothing else needs it.
   std::vector<int32_t> route(class_shapes.size());
-  for (size_t c = 0; c < class_shapes.size(); ++c) route[c] = choose_route(P, class_shapes[c].first, class_shapes[c].second);
+  for (size_t c = 0; c < class_shapes.size(); ++c)
+    route[c] = choose_route(P, std::get<0>(class_shapes[c]), std::get<1>(class_shapes[c]),
+                            std::get<2>(class_shapes[c]) != 0);
   std::vector<int32_t> order;
   for (int r : {(int)kRouteX, (int)kRouteGram})
     for (size_t c = 0; c < class_shapes.size(); ++c)
@@ -295,10 +303,12 @@ int validate_and_expand(gbo_plan *P) {
   int64_t xoff = 0, poff = 0, goff = 0, x_route_end = 0;
   for (size_t c = 0; c < order.size(); ++c) {
     ShapeClass C{};
-    C.p = class_shapes[order[c]].first;
-    C.q = class_shapes[order[c]].second;
+    C.p = std::get<0>(class_shapes[order[c]]);
+    C.q = std::get<1>(class_shapes[order[c]]);
+    C.tall = std::get<2>(class_shapes[order[c]]);
     C.route = route[order[c]];
-    C.ld = (int32_t)round_up(C.q, 16);
+    const int32_t xrows = C.tall ? C.q : C.p;  // X is p x q, or q x p when tall
+    C.ld = (int32_t)round_up(C.tall ? C.p : C.q, 16);
     C.ldp = (int32_t)round_up(C.p, 16);
     C.count = 0;
     C.sub0 = -1;
@@ -312,14 +322,14 @@ int validate_and_expand(gbo_plan *P) {
         DevSub &S = subs[k];
         S.ld = C.ld;
         S.ldp = C.ldp;
-        S.x_off = xoff + (int64_t)C.count * C.p * C.ld;
+        S.x_off = xoff + (int64_t)C.count * xrows * C.ld;
         S.p_off = pspace + (int64_t)C.count * C.p * C.ldp;
         // the last iterate: X_k of the X route alternates buffers from X0;
         // the Gram route writes X_k = Q_k X_0 into the second buffer
         S.x_sel = C.route == kRouteGram ? 1 : (o.ns_steps & 1);
         C.count++;
       }
-    xoff = round_up(xoff + (int64_t)C.count * C.p * C.ld, 128);
+    xoff = round_up(xoff + (int64_t)C.count * xrows * C.ld, 128);
     pspace = round_up(pspace + (int64_t)C.count * C.p * C.ldp, 128);
     if (C.route == kRouteX) x_route_end = xoff;
     else P->any_gram = true;
@@ -380,11 +390,11 @@ int validate_and_expand(gbo_plan *P) {
     double ex = 0;
     for (const ShapeClass &C : P->classes) {
       if (C.route == kRouteGram) {
-        ex += C.count * tc_gram_route_flops(C.p, C.q, o.ns_steps);
+        ex += C.count * tc_gram_route_flops(C.p, C.q, o.ns_steps, C.tall != 0);
         I.n_gram_route += C.count;
       } else {
         for (int it = 0; it < o.ns_steps; ++it)
-          ex += C.count * tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f);
+          ex += C.count * tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f, C.tall != 0);
       }
     }
     I.ns_flops_executed = ex;
@@ -463,6 +473,8 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
   };
   for (const ShapeClass &C : P->classes) {
     if (C.count == 0) continue;
+    const int kGramK = C.tall ? kKindGramT : kKindGram;  // X X^T, or X^T X of a tall X
+    const int kProdK = C.tall ? kKindProdT : kKindProd;  // P X, or X P of a tall X
     if (C.route == kRouteX) {
       size_t i = 0;
       int cur = 0;
@@ -470,21 +482,22 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
         const float *abc = &P->abc[3 * it];
         const int first = it == 0;
         if (abc[2] != 0.f) {
-          at(xs, i++, kPhaseGram).jobs.push_back(job(&C, kGramA, kKindGram, first, abc, x[cur], x[cur], ab));
+          at(xs, i++, kPhaseGram).jobs.push_back(job(&C, kGramA, kGramK, first, abc, x[cur], x[cur], ab));
           at(xs, i++, kPhaseSquare).jobs.push_back(job(&C, kSquare, kKindSym, 0, abc, ab, ab, pb, nullptr, ab));
         } else {
-          at(xs, i++, kPhaseGram).jobs.push_back(job(&C, kGram, kKindGram, first, abc, x[cur], x[cur], pb));
+          at(xs, i++, kPhaseGram).jobs.push_back(job(&C, kGram, kGramK, first, abc, x[cur], x[cur], pb));
         }
         const bool last = it == k - 1;
         const int mode = (last && !normuon) ? kFinal : kProduct;
         at(xs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
-            .jobs.push_back(job(&C, mode, kKindProd, first, abc, pb, x[cur], x[cur ^ 1]));
+            .jobs.push_back(C.tall ? job(&C, mode, kProdK, first, abc, x[cur], pb, x[cur ^ 1])
+                                   : job(&C, mode, kProdK, first, abc, pb, x[cur], x[cur ^ 1]));
         cur ^= 1;
       }
     } else {
       // A_0 = alpha^2 X_0 X_0^T and P_0;  Q_1 = P_0
       size_t i = 0;
-      at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kKindGram, 1, &P->abc[0], x[0], x[0], gP[0], gA));
+      at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kGramK, 1, &P->abc[0], x[0], x[0], gP[0], gA));
       for (int j = 0; j + 1 < k; ++j) {
         void *Pj = gP[j & 1];
         // T = P_j A_j and, from j = 1, Q_{j+1} = P_j Q_j
@@ -504,7 +517,8 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
                               gQ[k & 1]));
       const int mode = normuon ? kProduct : kFinal;
       at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
-          .jobs.push_back(job(&C, mode, kKindProd, 1, nullptr, gQ[k & 1], x[0], x[1]));
+          .jobs.push_back(C.tall ? job(&C, mode, kProdK, 1, nullptr, x[0], gQ[k & 1], x[1])
+                                 : job(&C, mode, kProdK, 1, nullptr, gQ[k & 1], x[0], x[1]));
     }
   }
   std::vector<TcStep> steps(std::max(xs.size(), gs.size()));

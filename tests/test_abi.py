@@ -159,7 +159,8 @@ def test_flop_count_and_launches(L):
     rc, plan = create(L, descs(), route=B.GBO_ROUTE_X)
     assert rc == 0
     i = info(L, plan)
-    assert i.n_matrices == 3 and i.n_shape_classes == 1 and i.n_gram_route == 0
+    # the tall gate/up halves and the wide down projection: two classes (X kept in stored orientation)
+    assert i.n_matrices == 3 and i.n_shape_classes == 2 and i.n_gram_route == 0
     assert i.ns_flops == 3 * 5 * 4 * 2048 ** 2 * 5632
     assert i.ns_flops_executed == 3 * 5 * (gram + prod)
     # momentum + finalize + 5 x (Gram + product)
