@@ -25,10 +25,12 @@ docstrings of the functions that take them.
 
 Parity unpinned: the NorMuon ordering choices (statistics on the unscaled
 Newton-Schulz output, epsilon outside the square root, no bias correction on
-the row second moment).  The NorMuon algorithm listing is not printed on the
-page; the oracle fixes these choices by reading and the tests pin only the
-properties the page states (row normalisation, unit rows for an exactly
-orthogonal update).
+the row second moment) and the form of its RMS-keeping learning-rate scale
+(per matrix, to a caller-supplied target RMS, in place of the rectangular
+scale).  The NorMuon algorithm listing is not printed on the page; the
+oracle fixes these choices by reading and the tests pin only the properties
+the page states (row normalisation, unit rows for an exactly orthogonal
+update, an update RMS held at a target).
 """
 
 from .views import sub_matrices, validate_view
@@ -40,6 +42,7 @@ from .muon import (
     orthogonalize,
     rect_scale,
     normuon_rows,
+    rms_match,
     weight_update,
     muon_step_tensor,
     ns_flops,
@@ -56,6 +59,7 @@ __all__ = [
     "orthogonalize",
     "rect_scale",
     "normuon_rows",
+    "rms_match",
     "weight_update",
     "muon_step_tensor",
     "ns_flops",

@@ -132,6 +132,22 @@ def normuon_rows(O, v, beta2, eps):
     return O / (np.sqrt(v_new)[:, None] + eps), v_new
 
 
+def rms_match(U, rms_target):
+    """Scale a row-normalised update so that its root-mean-square is rms_target.
+
+    NorMuon paper, section 3.1: the row normalisation leaves a direction of
+    larger norm, so the update gets a learning-rate scale that keeps its RMS
+    near Adam's.  Reading (the listing line is not printed): per matrix,
+    U = rms_target * sqrt(m n) / ||U||_F * U, with the target supplied by
+    the caller; an all-zero update stays zero.
+    """
+    U = np.asarray(U, dtype=np.float64)
+    f = float(np.sqrt(np.sum(U * U)))
+    if f == 0.0:
+        return U.copy()
+    return U * (rms_target * np.sqrt(U.size) / f)
+
+
 def weight_update(W, U, lr, wd):
     """W_t = W_{t-1} - lr * wd * W_{t-1} - lr * U_t.
 
@@ -145,7 +161,7 @@ def weight_update(W, U, lr, wd):
 
 def muon_step_tensor(W, G, B, *, view=None, split=None, mu=0.95, nesterov=True,
                      coeffs=None, ns_steps=5, lr=0.02, lr_mult=1.0, wd=0.0,
-                     v_row=None, normuon=False, beta2=0.95, eps=1e-8):
+                     v_row=None, normuon=False, beta2=0.95, eps=1e-8, rms_target=0.0):
     """One Muon step for one stored weight with its matrix view.
 
     Order (OMN page, Muon path): gradient -> momentum -> Nesterov direction
@@ -159,6 +175,10 @@ def muon_step_tensor(W, G, B, *, view=None, split=None, mu=0.95, nesterov=True,
 
     The per-tensor learning-rate multiplier scales both the decay and the
     update: W <- W - (lr * lr_mult) * (wd * W + U).
+
+    With NorMuon and ``rms_target > 0`` each matrix's normalised update is
+    rescaled to that RMS (:func:`rms_match`) in place of the rectangular
+    scale, which the rescaling would cancel.
 
     Returns ``(W_new, B_new, v_new, U)`` in float64, where ``U`` is the update
     direction (scale times the normalised NS output), or ``None`` for ``U``
@@ -182,7 +202,10 @@ def muon_step_tensor(W, G, B, *, view=None, split=None, mu=0.95, nesterov=True,
         O = orthogonalize(D[r0:r0 + m], coeffs)
         if normuon:
             O, v_new[r0:r0 + m] = normuon_rows(O, v_new[r0:r0 + m], beta2, eps)
-        U[r0:r0 + m] = rect_scale(m, n) * O
+        if normuon and rms_target > 0:
+            U[r0:r0 + m] = rms_match(O, rms_target)
+        else:
+            U[r0:r0 + m] = rect_scale(m, n) * O
     W_new = weight_update(W, U, lr * lr_mult, wd)
     return W_new, B_new, v_new, U
 

@@ -81,6 +81,21 @@ def test_planted_ns_mistake_is_caught(monkeypatch, name, patch, coeffs, shape):
     assert spectral_error(om.orthogonalize, shape, coeffs) > 1e-6, name
 
 
+def test_planted_rms_mistake_is_caught(monkeypatch):
+    """An RMS factor over the rows only (sqrt(m) instead of sqrt(mn)) fails
+    the RMS pin of the NorMuon step."""
+    import tests.test_oracle_views_adamw as t
+
+    def bad(U, rho):
+        U = np.asarray(U, dtype=np.float64)
+        f = float(np.sqrt(np.sum(U * U)))
+        return U * (rho * np.sqrt(U.shape[0]) / f) if f > 0 else U.copy()
+
+    monkeypatch.setattr(om, "rms_match", bad)
+    with pytest.raises(AssertionError):
+        t.test_normuon_rms_step()
+
+
 def test_planted_scale_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(om, "rect_scale", lambda m, n: float(np.sqrt(max(1.0, n / m))))
     W = np.random.default_rng(0).standard_normal((32, 8))

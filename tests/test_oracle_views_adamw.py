@@ -137,6 +137,43 @@ def test_normuon_row_properties():
     assert np.max(np.abs(v2 - (1 - 0.95 ** 2) * np.mean(O * O, axis=1))) < 1e-15
 
 
+def test_rms_match_pins():
+    """NorMuon section 3.1, the learning-rate scale that keeps the update's
+    RMS at a target (reading: per matrix, U * rho sqrt(mn) / ||U||_F).
+    Worked value: [[3, 4]] at rho = 0.5 is [[3, 4]] * 0.5 sqrt(2) / 5, whose
+    RMS is 0.5; the result keeps the direction; a positive multiple of U
+    gives the same result; zero stays zero."""
+    U = om.rms_match(np.array([[3.0, 4.0]]), 0.5)
+    assert np.max(np.abs(U - np.array([[3.0, 4.0]]) * (0.5 * math.sqrt(2.0) / 5.0))) < 1e-15
+    assert abs(math.sqrt(np.mean(U * U)) - 0.5) < 1e-15
+    for shape in [(7, 3), (3, 7), (16, 16)]:
+        X = rng(15).standard_normal(shape)
+        Y = om.rms_match(X, 0.2)
+        assert abs(math.sqrt(np.mean(Y * Y)) - 0.2) < 1e-14
+        cos = np.sum(X * Y) / (np.linalg.norm(X) * np.linalg.norm(Y))
+        assert abs(cos - 1.0) < 1e-14
+        assert np.max(np.abs(om.rms_match(3.7 * X, 0.2) - Y)) < 1e-14
+    assert np.all(om.rms_match(np.zeros((4, 5)), 0.2) == 0.0)
+
+
+def test_normuon_rms_step():
+    """In the step, each matrix of a view gets its own RMS (per-matrix
+    granularity of the build_parameter_groups views), the rectangular scale
+    is not applied on top, and rms_target = 0 is the plain NorMuon step."""
+    m, n = 20, 8
+    W = rng(16).standard_normal((m, n))
+    G = rng(17).standard_normal((m, n))
+    kw = dict(v_row=np.zeros(m), normuon=True, view=(2, 10, 8), split=(4, 6))
+    _, _, _, U = _step(W, G, np.zeros((m, n)), rms_target=0.3, **kw)
+    for r0, rows in [(0, 4), (4, 6), (10, 4), (14, 6)]:
+        blk = U[r0:r0 + rows]
+        assert abs(math.sqrt(np.mean(blk * blk)) - 0.3) < 1e-13
+    _, _, _, U0 = _step(W, G, np.zeros((m, n)), **kw)
+    for r0, rows in [(0, 4), (4, 6), (10, 4), (14, 6)]:
+        a, b = U[r0:r0 + rows], U0[r0:r0 + rows]
+        assert abs(np.sum(a * b) / (np.linalg.norm(a) * np.linalg.norm(b)) - 1.0) < 1e-13
+
+
 def test_state_memory_formulas():
     """NorMuon section 3.3: Muon keeps m n state numbers, NorMuon m (n + 1)."""
     m, n = 20, 8
