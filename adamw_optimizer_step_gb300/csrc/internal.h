@@ -136,9 +136,13 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
                             float *alpha, int32_t *status, void *stream);
 int launch_ns_gemm_simt(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args,
                         int sm_count, void *stream);
+// NorMuon rows; with rms_target > 0 a statistics pass, the per-matrix
+// RMS-keeping scale and a write pass (rowf: n_row_blocks * kRowBlock floats,
+// rowpart: n_row_blocks, mscale: n_subs), else one fused pass.
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
-                        int32_t *status, int sm_count, void *stream);
+                        int32_t *status, float rms_target, float *rowf, float *rowpart, float *mscale,
+                        int sm_count, void *stream);
 int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
                                  int32_t w_dtype, float beta2, float eps, float scale, float lr,
                                  float wd, float *dbg, void *stream);

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -259,17 +260,26 @@ __device__ __forceinline__ void weight_rmw8(const DevSub &S, int64_t widx, int v
 // weight write, with 16-byte accesses throughout.
 //   untransposed: warp w takes stored rows w, w + 8, ... of the block; a
 //     row is X's row, read twice (statistics, then the write)
-//   transposed: stored row i is column i of X; the block reads 32 x 64
-//     tiles of X (8 threads per 64-column row segment), keeps per-column
-//     sums, then transposes tiles through shared memory for the write
-template <typename XT>
+//   transposed (fp32 mode): stored row i is column i of X; the block reads
+//     32 x 64 tiles of X (8 threads per 64-column row segment), keeps
+//     per-column sums, then transposes tiles through shared memory for the
+//     write
+// kMode selects the pass (NorMuon paper, section 3.1):
+//   0  statistics and write, f_i = scale / (sqrt(v_i) + eps)
+//   1  statistics only, for the RMS-keeping scale: f_i = 1 / (sqrt(v_i) + eps)
+//      to rowf, and the block's sum of f_i^2 * sum_j X_ij^2 (its share of
+//      ||O_hat||_F^2) to rowpart
+//   2  write only, f_i = mscale[matrix] * rowf[i]
+template <typename XT, int kMode>
 __global__ void __launch_bounds__(256)
 normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_blocks,
                     const XT *__restrict__ xbuf0, const XT *__restrict__ xbuf1, float beta2, float eps, float lr,
-                    float *__restrict__ dbg, int32_t *status) {
+                    float *__restrict__ dbg, int32_t *status, float *__restrict__ rowf,
+                    float *__restrict__ rowpart, const float *__restrict__ mscale) {
   __shared__ float tileT[32][kRowBlock + 1];
   __shared__ float colsum[32][kRowBlock + 1];
   __shared__ float rfac[kRowBlock];
+  __shared__ float red[kRowBlock];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
     const int si = find_owner(b, n_subs, [&](int k) { return subs[k].rb0; });
@@ -279,86 +289,150 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
     const XT *X = (S.x_sel ? xbuf1 : xbuf0) + S.x_off;  // the buffer holding the last iterate
     const float lrm = lr * S.lr_mult;
     const bool wvec = S.w_vec != 0;
+    float *rf = rowf + b * kRowBlock;  // per-row factors of this block (modes 1, 2)
     if (!S.transposed) {
+      float part = 0.f;  // mode 1: this warp's share of the block partial
       for (int r = warp; r < nrows; r += 8) {
         const int row = i0 + r;
         const XT *xr = X + (int64_t)row * S.ld;
-        float ss = 0.f;
-        for (int j = lane * 8; j < S.n; j += 256) {
-          float o[8];
-          load8x(xr + j, min(8, S.n - j), o);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ss = fmaf(o[e], o[e], ss);
-        }
-        ss = warp_sum(ss);
         const int64_t vrow = S.r0 + row;
-        const float v = beta2 * S.row_v[vrow] + (1.0f - beta2) * (ss / (float)S.n);
-        const float f = S.scale / (sqrtf(v) + eps);
-        if (!isfinite(f)) flag_status(status, GBO_STATUS_NONFINITE);
-        __syncwarp();
-        if (lane == 0) S.row_v[vrow] = v;
-        for (int j = lane * 8; j < S.n; j += 256) {
-          const int valid = min(8, S.n - j);
-          float o[8];
-          load8x(xr + j, valid, o);
-          weight_rmw8(S, vrow * S.cols + j, valid, wvec, lrm, f, o, dbg);
+        float f;
+        if constexpr (kMode != 2) {
+          float ss = 0.f;
+          for (int j = lane * 8; j < S.n; j += 256) {
+            float o[8];
+            load8x(xr + j, min(8, S.n - j), o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(o[e], o[e], ss);
+          }
+          ss = warp_sum(ss);
+          const float v = beta2 * S.row_v[vrow] + (1.0f - beta2) * (ss / (float)S.n);
+          f = (kMode == 0 ? S.scale : 1.0f) / (sqrtf(v) + eps);
+          if (!isfinite(f)) flag_status(status, GBO_STATUS_NONFINITE);
+          __syncwarp();
+          if (lane == 0) S.row_v[vrow] = v;
+          if constexpr (kMode == 1) {
+            if (lane == 0) rf[r] = f;
+            part = fmaf(f * f, ss, part);
+          }
+        } else {
+          f = mscale[si] * rf[r];
+        }
+        if constexpr (kMode != 1) {
+          for (int j = lane * 8; j < S.n; j += 256) {
+            const int valid = min(8, S.n - j);
+            float o[8];
+            load8x(xr + j, valid, o);
+            weight_rmw8(S, vrow * S.cols + j, valid, wvec, lrm, f, o, dbg);
+          }
+        }
+      }
+      if constexpr (kMode == 1) {  // fixed-order block sum of the warps' shares
+        if (lane == 0) red[warp] = part;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          float t = 0.f;
+          for (int w = 0; w < 8; ++w) t += red[w];
+          rowpart[b] = t;
         }
       }
     } else {
       const int cg = threadIdx.x & 7, rr = threadIdx.x >> 3;  // 8 columns x 32 rows of X per pass
       const int c = i0 + cg * 8;                                // first X column (stored row)
       const int cvalid = max(0, min(8, i0 + nrows - c));
-      float acc[8];
+      if constexpr (kMode != 2) {
+        float acc[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-      for (int j = rr; j < S.n; j += 32) {
-        if (cvalid > 0) {
-          float o[8];
-          load8x(X + (int64_t)j * S.ld + c, cvalid, o);
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int j = rr; j < S.n; j += 32) {
+          if (cvalid > 0) {
+            float o[8];
+            load8x(X + (int64_t)j * S.ld + c, cvalid, o);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] = fmaf(o[e], o[e], acc[e]);
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(o[e], o[e], acc[e]);
+          }
         }
-      }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) colsum[rr][cg * 8 + e] = acc[e];
-      __syncthreads();
-      if (threadIdx.x < nrows) {
-        float ss = 0.f;
-        for (int k = 0; k < 32; ++k) ss += colsum[k][threadIdx.x];  // fixed order
-        const int64_t vrow = S.r0 + i0 + threadIdx.x;
-        const float v = beta2 * S.row_v[vrow] + (1.0f - beta2) * (ss / (float)S.n);
-        S.row_v[vrow] = v;
-        const float f = S.scale / (sqrtf(v) + eps);
-        if (!isfinite(f)) flag_status(status, GBO_STATUS_NONFINITE);
-        rfac[threadIdx.x] = f;
-      }
-      __syncthreads();
-      // write: stored rows i0 + k (k < nrows), stored columns j0 .. j0 + 31
-      const int k = threadIdx.x >> 2, seg = threadIdx.x & 3;  // 64 rows x 4 segments of 8
-      for (int j0 = 0; j0 < S.n; j0 += 32) {
-        {
-          const int j = j0 + rr;
-          float o[8];
-          if (j < S.n && cvalid > 0) load8x(X + (int64_t)j * S.ld + c, cvalid, o);
-          else
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) tileT[rr][cg * 8 + e] = o[e];
-        }
+        for (int e = 0; e < 8; ++e) colsum[rr][cg * 8 + e] = acc[e];
         __syncthreads();
-        const int jc = j0 + seg * 8;
-        const int valid = max(0, min(8, S.n - jc));
-        if (k < nrows && valid > 0) {
-          float o[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = tileT[seg * 8 + e][k];
-          weight_rmw8(S, (S.r0 + i0 + k) * S.cols + jc, valid, wvec, lrm, rfac[k], o, dbg);
+        float part = 0.f;
+        if (threadIdx.x < nrows) {
+          float ss = 0.f;
+          for (int k = 0; k < 32; ++k) ss += colsum[k][threadIdx.x];  // fixed order
+          const int64_t vrow = S.r0 + i0 + threadIdx.x;
+          const float v = beta2 * S.row_v[vrow] + (1.0f - beta2) * (ss / (float)S.n);
+          S.row_v[vrow] = v;
+          const float f = (kMode == 0 ? S.scale : 1.0f) / (sqrtf(v) + eps);
+          if (!isfinite(f)) flag_status(status, GBO_STATUS_NONFINITE);
+          rfac[threadIdx.x] = f;
+          if constexpr (kMode == 1) {
+            rf[threadIdx.x] = f;
+            part = f * f * ss;
+          }
         }
-        __syncthreads();
+        if constexpr (kMode == 1) {
+          if (threadIdx.x < kRowBlock) red[threadIdx.x] = part;
+          __syncthreads();
+          if (threadIdx.x == 0) {
+            float t = 0.f;
+            for (int k = 0; k < kRowBlock; ++k) t += red[k];  // fixed order
+            rowpart[b] = t;
+          }
+        }
+      } else {
+        if (threadIdx.x < nrows) rfac[threadIdx.x] = mscale[si] * rf[threadIdx.x];
+      }
+      __syncthreads();
+      if constexpr (kMode != 1) {
+        // write: stored rows i0 + k (k < nrows), stored columns j0 .. j0 + 31
+        const int k = threadIdx.x >> 2, seg = threadIdx.x & 3;  // 64 rows x 4 segments of 8
+        for (int j0 = 0; j0 < S.n; j0 += 32) {
+          {
+            const int j = j0 + rr;
+            float o[8];
+            if (j < S.n && cvalid > 0) load8x(X + (int64_t)j * S.ld + c, cvalid, o);
+            else
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tileT[rr][cg * 8 + e] = o[e];
+          }
+          __syncthreads();
+          const int jc = j0 + seg * 8;
+          const int valid = max(0, min(8, S.n - jc));
+          if (k < nrows && valid > 0) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = tileT[seg * 8 + e][k];
+            weight_rmw8(S, (S.r0 + i0 + k) * S.cols + jc, valid, wvec, lrm, rfac[k], o, dbg);
+          }
+          __syncthreads();
+        }
       }
     }
     __syncthreads();
+  }
+}
+
+// The RMS-keeping scale of each matrix (one block per matrix): the row-block
+// partials of ||O_hat||_F^2 summed in a fixed order, then
+// rho * sqrt(m n) / ||O_hat||_F; an all-zero update keeps a zero scale.
+__global__ void __launch_bounds__(256)
+normuon_scale_kernel(const DevSub *__restrict__ subs, const float *__restrict__ rowpart, float rho,
+                     float *__restrict__ mscale, int32_t *status) {
+  __shared__ float red[32];
+  const DevSub &S = subs[blockIdx.x];
+  const int nb = (S.m + kRowBlock - 1) / kRowBlock;
+  float t = 0.f;
+  for (int k = threadIdx.x; k < nb; k += blockDim.x) t += rowpart[S.rb0 + k];
+  t = block_sum(t, red);
+  if (threadIdx.x == 0) {
+    float g = t > 0.f ? rho * sqrtf((float)S.m * (float)S.n) / sqrtf(t) : 0.f;
+    if (!isfinite(t) || !isfinite(g)) {
+      flag_status(status, GBO_STATUS_NONFINITE);
+      g = __int_as_float(0x7fc00000);
+    }
+    mscale[blockIdx.x] = g;
   }
 }
 
@@ -436,19 +510,31 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
 
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
-                        int32_t *status, int sm_count, void *stream) {
+                        int32_t *status, float rms_target, float *rowf, float *rowpart, float *mscale,
+                        int sm_count, void *stream) {
   if (n_row_blocks == 0) return 0;
   const int64_t grid = std::min<int64_t>(n_row_blocks, (int64_t)sm_count * 8);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (x_dtype == GBO_BF16)
-    normuon_rows_kernel<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(
-        subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x0),
-        reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status);
-  else
-    normuon_rows_kernel<float><<<(unsigned)grid, 256, 0, st>>>(
-        subs, n_subs, n_row_blocks, reinterpret_cast<const float *>(x0), reinterpret_cast<const float *>(x1),
-        beta2, eps, lr, dbg, status);
-  count_launches(1);
+  auto rows = [&](auto mode) {
+    constexpr int kMode = decltype(mode)::value;
+    if (x_dtype == GBO_BF16)
+      normuon_rows_kernel<__nv_bfloat16, kMode><<<(unsigned)grid, 256, 0, st>>>(
+          subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x0),
+          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf, rowpart, mscale);
+    else
+      normuon_rows_kernel<float, kMode><<<(unsigned)grid, 256, 0, st>>>(
+          subs, n_subs, n_row_blocks, reinterpret_cast<const float *>(x0), reinterpret_cast<const float *>(x1),
+          beta2, eps, lr, dbg, status, rowf, rowpart, mscale);
+    count_launches(1);
+  };
+  if (rms_target > 0.f) {
+    rows(std::integral_constant<int, 1>());
+    normuon_scale_kernel<<<(unsigned)n_subs, 256, 0, st>>>(subs, rowpart, rms_target, mscale, status);
+    count_launches(1);
+    rows(std::integral_constant<int, 2>());
+  } else {
+    rows(std::integral_constant<int, 0>());
+  }
   return (int)cudaGetLastError();
 }
 

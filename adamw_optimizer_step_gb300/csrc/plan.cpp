@@ -132,6 +132,8 @@ struct gbo_plan {
   size_t off_x[2] = {0, 0}, off_p = 0, off_a = 0, off_alpha = 0, off_part = 0, ws_bytes = 0;
   // Gram-route p x p buffers: A, T, P (two), Q (two)
   size_t off_g[6] = {0, 0, 0, 0, 0, 0};
+  // NorMuon RMS-keeping scale: per-row factors, row-block partials, per-matrix scales
+  size_t off_rowf = 0, off_rowpart = 0, off_mscale = 0;
   uint64_t hash = 0;
   gbo_plan_info info{};
   // device state, set by the first step
@@ -369,6 +371,10 @@ int validate_and_expand(gbo_plan *P) {
   for (int b = 0; b < 6; ++b) P->off_g[b] = region((size_t)goff * es);
   P->off_alpha = region(P->subs.size() * sizeof(float));
   P->off_part = region((size_t)tiles * 8 * 2 * sizeof(float));  // (max, sum of squares) per warp of a tile
+  const bool rms = o.normuon && o.rms_target > 0.f;
+  P->off_rowf = region(rms ? (size_t)rbs * kRowBlock * sizeof(float) : 0);
+  P->off_rowpart = region(rms ? (size_t)rbs * sizeof(float) : 0);
+  P->off_mscale = region(rms ? P->subs.size() * sizeof(float) : 0);
   P->ws_bytes = off;
   // info
   gbo_plan_info &I = P->info;
@@ -596,6 +602,10 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   if (!std::isfinite(opts->mu)) return fail(GBO_ERR_INVALID_ARG, "mu is not finite");
   if (opts->normuon && (!(opts->beta2 >= 0.f && opts->beta2 <= 1.f) || !(opts->eps >= 0.f)))
     return fail(GBO_ERR_INVALID_ARG, "NorMuon needs 0 <= beta2 <= 1 and eps >= 0");
+  if (!(opts->rms_target >= 0.f) || !std::isfinite(opts->rms_target))
+    return fail(GBO_ERR_INVALID_ARG, "rms_target must be finite and >= 0");
+  if (opts->rms_target > 0.f && !opts->normuon)
+    return fail(GBO_ERR_INVALID_ARG, "rms_target needs NorMuon");
   gbo_plan *P = new gbo_plan();
   P->descs.assign(descs, descs + n);
   if (pool_len > 0) P->pool.assign(split_pool, split_pool + pool_len);
@@ -626,7 +636,8 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   } else {
     for (int it = 0; it < k; ++it) gemm += (P->abc[3 * it + 2] != 0.f ? 3 : 2) * simt_launches(P);
   }
-  P->info.launches_per_step = P->subs.empty() ? 0 : 2 + gemm + (opts->normuon ? 1 : 0);
+  P->info.launches_per_step =
+      P->subs.empty() ? 0 : 2 + gemm + (opts->normuon ? (opts->rms_target > 0.f ? 3 : 1) : 0);
   *out = P;
   return ok();
 }
@@ -791,9 +802,12 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   }
   if (P->opts.normuon) {
     err = launch_normuon_rows(P->d_subs, nsub, P->n_row_blocks, x[0], x[1], P->x_dtype, P->opts.beta2,
-                              P->opts.eps, lr, dbg_update, dev_status, P->sm_count, st);
+                              P->opts.eps, lr, dbg_update, dev_status, P->opts.rms_target,
+                              reinterpret_cast<float *>(ws + P->off_rowf),
+                              reinterpret_cast<float *>(ws + P->off_rowpart),
+                              reinterpret_cast<float *>(ws + P->off_mscale), P->sm_count, st);
     if (err) return cuda_fail(err, "NorMuon rows kernel");
-    mark(kPhaseRows, 1);
+    mark(kPhaseRows, P->opts.rms_target > 0.f ? 3 : 1);
   }
   if (P->timing && last) P->event_pool.push_back(last);
   return ok();

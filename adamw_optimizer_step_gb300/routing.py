@@ -157,7 +157,7 @@ class HybridOptimizer:
 
     def __init__(self, model, *, muon_lr=0.01, adamw_lr=3e-4, weight_decay=0.0, auxiliary_decay=True, mu=0.95,
                  ns_steps=5, abc=(1.5, -0.5, 0.0), normuon=False, beta2_rows=0.95, eps_rows=1e-8,
-                 betas=(0.9, 0.95), eps=1e-8, max_norm=1.0, precision="bf16"):
+                 rms_target=0.0, betas=(0.9, 0.95), eps=1e-8, max_norm=1.0, precision="bf16"):
         from . import _binding as B
         self.B = B
         self.routes = build_parameter_groups(model, weight_decay, auxiliary_decay)
@@ -169,6 +169,7 @@ class HybridOptimizer:
         self.muon_lr, self.adamw_lr = muon_lr, adamw_lr
         self.betas, self.eps, self.max_norm = betas, eps, max_norm
         self.opts = dict(abc=abc, ns_steps=ns_steps, mu=mu, normuon=normuon, beta2=beta2_rows, eps=eps_rows,
+                         rms_target=rms_target,
                          precision=B.GBO_NS_F32 if precision == "f32" else B.GBO_NS_BF16)
         self.state = {}
         for r in self.muon:

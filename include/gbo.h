@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define GBO_ABI_VERSION 2
+#define GBO_ABI_VERSION 3
 
 /* ---- status codes (return values) ------------------------------------ */
 #define GBO_OK 0
@@ -110,7 +110,10 @@ typedef struct {
  * eq. (5) of the same section,
  *   X <- a X + b (X X^T) X + c (X X^T)^2 X,
  * whose (a, b, c) = (1.5, -0.5, 0) case is the cubic of the "MuonClip
- * Optimizer" page.  NorMuon rows: NorMuon paper, section 3.1.
+ * Optimizer" page.  NorMuon rows: NorMuon paper, section 3.1; its
+ * RMS-keeping learning-rate scale is read as: with rms_target > 0, each
+ * matrix's row-normalised update U becomes rms_target sqrt(m n) U / ||U||_F
+ * (no rectangular scale on top; an all-zero U stays zero).
  */
 typedef struct {
   const float *abc;      /* host: (a,b,c) triples, 1 triple or ns_steps triples; copied */
@@ -123,6 +126,7 @@ typedef struct {
   int32_t precision;     /* GBO_NS_BF16 | GBO_NS_F32                                    */
   int32_t normuon;       /* 1: NorMuon row normalisation; every desc needs row_v        */
   int32_t route;         /* GBO_ROUTE_AUTO (0) | GBO_ROUTE_X | GBO_ROUTE_GRAM          */
+  float rms_target;      /* NorMuon only: > 0 scales each matrix's update to this RMS  */
 } gbo_muon_opts;
 
 /*

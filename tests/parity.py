@@ -70,7 +70,7 @@ def run_muon_gpu(entries, *, lr, precision, steps=1, dbg=True, **opts):
 
 
 def run_muon_oracle(entries, *, lr, steps=1, abc=(1.5, -0.5, 0.0), ns_steps=5, mu=0.95, nesterov=True,
-                    normuon=False, beta2=0.95, eps=1e-8):
+                    normuon=False, beta2=0.95, eps=1e-8, rms_target=0.0):
     coeffs = [tuple(abc[3 * i:3 * i + 3]) for i in range(len(abc) // 3)] if len(abc) > 3 else [tuple(abc)]
     res = []
     for e in entries:
@@ -81,7 +81,7 @@ def run_muon_oracle(entries, *, lr, steps=1, abc=(1.5, -0.5, 0.0), ns_steps=5, m
             W, Bm, v, U = oracle.muon_step_tensor(
                 W, G, Bm, view=e.get("view"), split=e.get("split"), mu=mu, nesterov=nesterov,
                 coeffs=coeffs, ns_steps=ns_steps, lr=lr, lr_mult=e.get("lr_mult", 1.0), wd=e.get("wd", 0.0),
-                v_row=v, normuon=normuon, beta2=beta2, eps=eps)
+                v_row=v, normuon=normuon, beta2=beta2, eps=eps, rms_target=rms_target)
         res.append(dict(W=W, B=Bm, v=v, U=U))
     return res
 

@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(L):
     assert "gbo_muon_step" in names and "gbo_adamw_step" in names
     for n in names:
         assert hasattr(L, n), n
-    assert B.gbo_abi_version() == 2
+    assert B.gbo_abi_version() == 3
     for i, S in enumerate(B._STRUCTS):
         assert B.gbo_struct_size(i) == ctypes.sizeof(S)
 
@@ -65,11 +65,11 @@ def desc(i, rows, cols, view=None, split_off=0, n_split=0, w_dtype=B.GBO_BF16, g
 
 
 def create(L, descs, pool=(), ns_steps=5, abc=(1.5, -0.5, 0.0), precision=B.GBO_NS_BF16, normuon=0,
-           route=B.GBO_ROUTE_AUTO):
+           route=B.GBO_ROUTE_AUTO, rms_target=0.0):
     arr = (B.MuonDesc * max(1, len(descs)))(*descs)
     cabc = (ctypes.c_float * len(abc))(*abc)
     opts = B.MuonOpts(ctypes.cast(cabc, ctypes.POINTER(ctypes.c_float)), 0.95, 0.95, 1e-8, 1, ns_steps,
-                      int(len(abc) > 3), precision, normuon, route)
+                      int(len(abc) > 3), precision, normuon, route, rms_target)
     cpool = (ctypes.c_int64 * max(1, len(pool)))(*pool)
     out = ctypes.c_void_p()
     rc = L.gbo_muon_plan_create(arr, len(descs), cpool, len(pool), ctypes.byref(opts), ctypes.byref(out))
@@ -139,6 +139,10 @@ def test_other_refusals(L):
     assert create(L, [d])[0] == -1
     # split sizes outside the pool
     assert create(L, [desc(0, 20, 8, (2, 10, 8), 1, 2)], pool=(4, 6))[0] == -1
+    # the RMS-keeping scale: finite and >= 0, and only with NorMuon
+    assert create(L, [desc(0, 8, 8)], rms_target=0.2)[0] == -1
+    assert create(L, [desc(0, 8, 8)], rms_target=-1.0)[0] == -1
+    assert create(L, [desc(0, 8, 8)], rms_target=float("inf"))[0] == -1
 
 
 def test_missing_gradient_skips(L):

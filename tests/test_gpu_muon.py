@@ -105,6 +105,27 @@ def test_routes(route, ns_steps):
     check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
 
 
+@pytest.mark.parametrize("precision", ["f32", "bf16"])
+def test_normuon_rms_target(precision):
+    """NorMuon with the RMS-keeping scale: statistics pass, per-matrix
+    scale, write pass.  Parity with the oracle, and each matrix of the
+    exported update (a split view included) has RMS rho."""
+    shapes = [(300, 130, None, None), (130, 300, None, None), (64, 64, None, None, 1.5, 0.1),
+              (200, 40, (2, 100, 40), (30, 70))]
+    entries = random_entries(shapes, seed=23, normuon=True, b_std=1e-3)
+    kw = dict(normuon=True, beta2=0.95, eps=1e-8, rms_target=0.2)
+    gpu, status, plan = run_muon_gpu(entries, lr=0.02, precision=precision, **kw)
+    ora = run_muon_oracle(entries, lr=0.02, **kw)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=0.02, precision=precision)
+    for e, g in zip(entries, gpu):
+        U = g["U"].double().numpy()
+        rows, cols = U.shape
+        for r0, m, n in sub_matrices(rows, cols, e.get("view"), e.get("split")):
+            blk = U[r0:r0 + m]
+            assert abs(np.sqrt(np.mean(blk * blk)) / 0.2 - 1.0) < 1e-3
+
+
 @pytest.mark.parametrize("ns_steps", [3, 5])
 def test_normuon_gram_route(ns_steps):
     """NorMuon rows read the last iterate from the buffer each route leaves
