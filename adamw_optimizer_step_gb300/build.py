@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libgbo.so")
 
-SOURCES = ["plan.cpp", "muon_elementwise.cu", "ns_gemm_simt.cu", "ns_gemm_tc.cu", "adamw.cu",
+SOURCES = ["plan.cpp", "muon_elementwise.cu", "ns_gemm_tc.cu", "ns_gemm_tf32.cu", "adamw.cu",
            "clip_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,

@@ -131,60 +131,4 @@ __device__ __forceinline__ void store8(XT *dst, const float *v, int valid, bool 
   }
 }
 
-// ---------------------------------------------------------------------------
-// Newton-Schulz epilogue for one accumulator element C[i][j] of matrix S.
-// `s` is the pre-normalisation factor of the iteration's input (alpha for
-// iteration 0, 1 afterwards), so the true iterate is s * X.
-struct EpiScalars {
-  float s;
-  float s2;
-};
-
-__device__ __forceinline__ EpiScalars epi_scalars(const PhaseArgs &A, int sub) {
-  EpiScalars e;
-  e.s = A.first ? A.alpha[sub] : 1.0f;
-  e.s2 = e.s * e.s;
-  return e;
-}
-
-// Weight write of the last iteration (no NorMuon): O = s * C is the
-// orthogonalised update at position (i, j) of the oriented matrix.
-__device__ __forceinline__ void final_write(const PhaseArgs &A, const DevSub &S, int i, int j,
-                                            float o) {
-  const int wi = S.transposed ? j : i;
-  const int wj = S.transposed ? i : j;
-  const int64_t widx = (S.r0 + wi) * S.cols + wj;
-  const float u = S.scale * o;
-  const float w = ld_elem(S.w, S.w_dtype, widx);
-  const float lr = A.lr * S.lr_mult;
-  st_elem(S.w, S.w_dtype, widx, w - lr * (S.wd * w + u));
-  if (A.dbg) A.dbg[S.dbg_off + widx] = u;
-}
-
-__device__ __forceinline__ void ns_epilogue(const PhaseArgs &A, const DevSub &S, const EpiScalars &e,
-                                            int i, int j, float acc) {
-  switch (A.mode) {
-    case kGram: {
-      float v = A.b * e.s2 * acc + (i == j ? A.a : 0.f);
-      st_elem(A.pbuf, A.x_dtype, S.p_off + (int64_t)i * S.ldp + j, v);
-      break;
-    }
-    case kGramA:
-      st_elem(A.abuf, A.x_dtype, S.p_off + (int64_t)i * S.ldp + j, e.s2 * acc);
-      break;
-    case kSquare: {
-      const float av = ld_elem(A.abuf, A.x_dtype, S.p_off + (int64_t)i * S.ldp + j);
-      float v = A.c * acc + A.b * av + (i == j ? A.a : 0.f);
-      st_elem(A.pbuf, A.x_dtype, S.p_off + (int64_t)i * S.ldp + j, v);
-      break;
-    }
-    case kProduct:
-      st_elem(A.x_out, A.x_dtype, S.x_off + (int64_t)i * S.ld + j, e.s * acc);
-      break;
-    default:
-      final_write(A, S, i, j, e.s * acc);
-      break;
-  }
-}
-
 }  // namespace gbo

@@ -25,6 +25,7 @@ struct DevSub {
   int64_t r0;       // first stored row of this matrix in its weight
   int64_t cols;     // row stride of the weight (== n)
   int64_t x_off;    // element offset of this matrix in each X buffer
+  int64_t xt_off;   // element offset of this matrix in each XT buffer (fp32 mode: X transposed)
   int64_t p_off;    // element offset of this matrix in the P (and A) buffer
   int64_t dbg_off;  // element offset of the weight's first element in dbg_update
   int64_t tile0;    // first momentum tile of this matrix (global tile index)
@@ -32,6 +33,8 @@ struct DevSub {
   int32_t m, n;     // stored rows, cols
   int32_t p, q;     // oriented rows, cols
   int32_t ld;       // X row stride (elements)
+  int32_t ldt;      // XT row stride (elements), fp32 mode
+  int32_t has_xt;   // the momentum pass also writes X0 transposed (fp32 mode)
   int32_t ldp;      // P row stride (elements)
   int32_t tiles_c;  // momentum tiles along n (2-D tiles), or 0 for flat tiles
   int32_t ntiles;   // momentum tiles of this matrix
@@ -63,7 +66,11 @@ struct ShapeClass {
   int32_t count;  // matrices in the class
   int32_t sub0;   // index of the first matrix in the DevSub table
   int32_t route;  // kRouteX | kRouteGram
-  int32_t tall;   // X holds the matrix in stored orientation, q x p (tensor-core path)
+  int32_t tall;   // the stored matrix has more rows than columns (m > n)
+  int32_t x_tall; // bf16 mode: X holds a tall matrix in stored orientation, q x p
+  int32_t ldt;    // fp32 mode: row stride of XT, X's transposed twin (q x p)
+  int32_t pad1;
+  int64_t xt_base; // element offset of the class in each XT buffer
   int64_t x_base; // element offset of the class in each X buffer
   int64_t p_base; // element offset of the class in its p x p buffers (its route's space)
 };
@@ -90,11 +97,19 @@ enum GemmKind : int32_t {
   kKindProd = 2,   // C = L X, X wide: B = X with K along its rows (MN-major); p x q output
   kKindGramT = 3,  // C = X^T X, X tall: A and B are columns of X (both MN-major, K = q); symmetric output
   kKindProdT = 4,  // C = X L, X tall: A = rows of X (K = p), B = rows of L; q x p output
+  kKindProdK = 5,  // C = L X, X wide, from its transposed twin XT (q x p): B = rows of XT; p x q output
 };
+
+// Products have full outputs; the other kinds a symmetric p x p output.
+__host__ __device__ inline bool is_product_kind(int kind) {
+  return kind == kKindProd || kind == kKindProdT || kind == kKindProdK;
+}
 
 // Rows and columns of a job's output for matrix S.
 __host__ __device__ inline int kind_rows(int kind, int p, int q) { return kind == kKindProdT ? q : p; }
-__host__ __device__ inline int kind_cols(int kind, int p, int q) { return kind == kKindProd ? q : p; }
+__host__ __device__ inline int kind_cols(int kind, int p, int q) {
+  return (kind == kKindProd || kind == kKindProdK) ? q : p;
+}
 
 // One shape class of a tensor-core launch and what it computes.  Operand
 // and output pointers are region bases; the launcher adds the class base
@@ -111,31 +126,23 @@ struct GemmJob {
   const void *aux;   // kSquare: the A matrix read by the epilogue
 };
 
-// Per-launch scalars of one Newton-Schulz phase.
+// Per-step arguments every Newton-Schulz launch shares (the per-class work
+// is in its GemmJob).
 struct PhaseArgs {
-  int32_t mode;
-  int32_t first;      // iteration 0: fold the pre-normalisation factor in
-  float a, b, c;
   float lr;
-  int32_t x_dtype;    // GBO_BF16 | GBO_F32 (workspace element type)
   const DevSub *subs;
   const float *alpha; // per matrix pre-normalisation factor
-  void *x_in;         // X buffer read by this phase
-  void *x_out;        // X buffer written (kProduct)
-  void *pbuf;         // P buffer (read by products, written by kGram/kSquare)
-  void *abuf;         // A buffer (kGramA writes, kSquare reads)
   float *dbg;         // dbg_update or nullptr
   int32_t *status;
 };
 
 // Launchers (implemented in the .cu files).  Each returns a cudaError_t as
 // int and adds its launches to the library's counter.
+// x0t: X0's transposed twin (fp32 mode), or nullptr.
 int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float mu, int32_t nesterov,
-                    void *x0, int32_t x_dtype, float *partials, int sm_count, void *stream);
+                    void *x0, void *x0t, int32_t x_dtype, float *partials, int sm_count, void *stream);
 int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials,
                             float *alpha, int32_t *status, void *stream);
-int launch_ns_gemm_simt(const ShapeClass *classes, int32_t n_classes, const PhaseArgs &args,
-                        int sm_count, void *stream);
 // NorMuon rows; with rms_target > 0 a statistics pass, the per-matrix
 // RMS-keeping scale and a write pass (rowf: n_row_blocks * kRowBlock floats,
 // rowpart: n_row_blocks, mscale: n_subs), else one fused pass.
@@ -153,9 +160,13 @@ int launch_adamw(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *o
 
 // tcgen05 path: one Newton-Schulz step over a set of jobs (any mix of
 // classes and kinds).  `globals` supplies subs, alpha, lr, dbg and status.
-// Adds the number of kernel launches made to *n_launch.
+// Adds the number of kernel launches made to *n_launch.  The bf16 kernel,
+// and the fp32 one (three TF32 products, K-major operands only: the Gram,
+// symmetric and ProdK / ProdT kinds).
 int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
                       void *stream, int64_t *n_launch);
+int launch_ns_gemm_tf32(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
+                        void *stream, int64_t *n_launch);
 // FLOPs the tensor-core kernel executes for one p x q matrix and one
 // iteration (Gram over the upper block-triangle of tiles, square when c != 0,
 // product), counting the zero padding of partial tiles; `tall`: X is held

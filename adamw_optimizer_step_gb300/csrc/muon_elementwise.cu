@@ -37,7 +37,7 @@ constexpr int kMomWarps = kMomThreads / 32;  // one partial pair per warp and ti
 template <typename XT>
 __global__ void __launch_bounds__(kMomThreads, GBO_MOM_MIN_BLOCKS)
 momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles, float mu,
-                int32_t nesterov, XT *__restrict__ x0, float *__restrict__ partials) {
+                int32_t nesterov, XT *__restrict__ x0, XT *__restrict__ x0t, float *__restrict__ partials) {
   __shared__ float tile[kMomTile][kMomTile + 1];
   const int cg = threadIdx.x & 7;
   const int rr = threadIdx.x >> 3;
@@ -119,15 +119,21 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
         }
         if (i < S.m && valid > 0) store8(S.mom + (S.r0 + i) * S.cols + j, b[ps], valid, vec);
       }
-      XT *X = x0 + S.x_off;
-      if (!S.transposed) {
+      // D itself goes to X, or with a transposed twin (fp32 mode) to XT when X
+      // holds D^T; D^T goes to X when transposed, else to XT when it exists
+      XT *direct = S.transposed ? (S.has_xt ? x0t + S.xt_off : nullptr) : x0 + S.x_off;
+      const int ld_direct = S.transposed ? S.ldt : S.ld;
+      XT *trans = S.transposed ? x0 + S.x_off : (S.has_xt ? x0t + S.xt_off : nullptr);
+      const int ld_trans = S.transposed ? S.ld : S.ldt;
+      if (direct) {
 #pragma unroll
         for (int ps = 0; ps < 2; ++ps) {
           const int i = rb + ps * 32 + rr;
-          if (i < S.m && valid > 0) store8(X + (int64_t)i * S.ld + j, d[ps], valid, true);
+          if (i < S.m && valid > 0) store8(direct + (int64_t)i * ld_direct + j, d[ps], valid, true);
         }
-      } else {
-        // X = D^T: stage the tile, then write rows of X (columns of D).
+      }
+      if (trans) {
+        // D^T: stage the tile, then write rows of D^T (columns of D).
         __syncthreads();  // the previous transposed tile's reads are done
 #pragma unroll
         for (int ps = 0; ps < 2; ++ps)
@@ -143,7 +149,7 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
             float v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = tile[cg * 8 + e][ps * 32 + rr];
-            store8(X + (int64_t)xr * S.ld + xc, v, xvalid, true);
+            store8(trans + (int64_t)xr * ld_trans + xc, v, xvalid, true);
           }
         }
       }
@@ -475,7 +481,7 @@ rownorm_plain_kernel(const float *__restrict__ O, int64_t rows, int64_t cols, fl
 }  // namespace
 
 int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float mu, int32_t nesterov,
-                    void *x0, int32_t x_dtype, float *partials, int sm_count, void *stream) {
+                    void *x0, void *x0t, int32_t x_dtype, float *partials, int sm_count, void *stream) {
   if (n_tiles == 0) return 0;
   // one wave: as many blocks as can be resident, each a contiguous tile range
   static int resident[2] = {0, 0};
@@ -491,10 +497,12 @@ int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float m
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (x_dtype == GBO_BF16)
     momentum_kernel<__nv_bfloat16><<<(unsigned)grid, kMomThreads, 0, st>>>(
-        subs, n_subs, n_tiles, mu, nesterov, reinterpret_cast<__nv_bfloat16 *>(x0), partials);
+        subs, n_subs, n_tiles, mu, nesterov, reinterpret_cast<__nv_bfloat16 *>(x0),
+        reinterpret_cast<__nv_bfloat16 *>(x0t), partials);
   else
     momentum_kernel<float><<<(unsigned)grid, kMomThreads, 0, st>>>(
-        subs, n_subs, n_tiles, mu, nesterov, reinterpret_cast<float *>(x0), partials);
+        subs, n_subs, n_tiles, mu, nesterov, reinterpret_cast<float *>(x0), reinterpret_cast<float *>(x0t),
+        partials);
   count_launches(1);
   return (int)cudaGetLastError();
 }

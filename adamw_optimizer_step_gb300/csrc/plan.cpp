@@ -130,6 +130,7 @@ struct gbo_plan {
   int64_t n_tiles = 0, n_row_blocks = 0;
   int32_t x_dtype = GBO_BF16;
   size_t off_x[2] = {0, 0}, off_p = 0, off_a = 0, off_alpha = 0, off_part = 0, ws_bytes = 0;
+  size_t off_xt[2] = {0, 0};  // fp32 mode: the X buffers' transposed twins
   // Gram-route p x p buffers: A, T, P (two), Q (two)
   size_t off_g[6] = {0, 0, 0, 0, 0, 0};
   // NorMuon RMS-keeping scale: per-row factors, row-block partials, per-matrix scales
@@ -154,15 +155,16 @@ struct gbo_plan {
 
 namespace {
 
-// Route of a p x q class: the Gram route needs bf16 mode, k >= 2 and c == 0
-// in every iteration; AUTO takes it when it executes at least 10% fewer
-// FLOPs (in practice: whenever q is clearly above p).
+// Route of a p x q class: the Gram route needs k >= 2 and c == 0 in every
+// iteration; AUTO takes it when it executes at least 10% fewer FLOPs (in
+// practice: whenever q is clearly above p).
 int32_t choose_route(const gbo_plan *P, int p, int q, bool tall) {
   const int k = P->opts.ns_steps;
-  if (P->x_dtype != GBO_BF16 || P->any_c || k < 2 || P->opts.route == GBO_ROUTE_X) return kRouteX;
+  if (P->any_c || k < 2 || P->opts.route == GBO_ROUTE_X) return kRouteX;
   if (P->opts.route == GBO_ROUTE_GRAM) return kRouteGram;
-  const double fx = k * tc_executed_flops(p, q, false, tall);
-  return tc_gram_route_flops(p, q, k, tall) < 0.9 * fx ? kRouteGram : kRouteX;
+  const bool x_tall = P->x_dtype == GBO_BF16 && tall;
+  const double fx = k * tc_executed_flops(p, q, false, x_tall);
+  return tc_gram_route_flops(p, q, k, x_tall) < 0.9 * fx ? kRouteGram : kRouteX;
 }
 
 int validate_and_expand(gbo_plan *P) {
@@ -174,9 +176,9 @@ int validate_and_expand(gbo_plan *P) {
     int32_t order;
   };
   std::vector<DevSub> subs;
-  // classes: (p, q, tall); the tensor-core path keeps a matrix with more
-  // rows than columns in stored orientation ("tall"), the fp32 path holds
-  // its transpose
+  // classes: (p, q, tall), tall = more rows than columns.  The bf16 path keeps
+  // a tall matrix's X in stored orientation (q x p); the fp32 path holds X =
+  // D^T (p x q) and a transposed twin XT (q x p) of every X
   using ClassKey = std::tuple<int32_t, int32_t, int32_t>;
   std::map<ClassKey, int32_t> class_of;
   std::vector<ClassKey> class_shapes;
@@ -262,6 +264,7 @@ int validate_and_expand(gbo_plan *P) {
         S.m = (int32_t)s;
         S.n = (int32_t)d.cols;
         S.transposed = !tc_path && S.m > S.n;
+        S.has_xt = !tc_path;
         S.p = std::min(S.m, S.n);
         S.q = std::max(S.m, S.n);
         S.w_dtype = d.w_dtype;
@@ -272,7 +275,7 @@ int validate_and_expand(gbo_plan *P) {
         S.lr_mult = d.lr_mult;
         S.wd = d.wd;
         S.dbg_off = this_dbg;
-        const ClassKey key(S.p, S.q, tc_path && S.m > S.n ? 1 : 0);
+        const ClassKey key(S.p, S.q, S.m > S.n ? 1 : 0);
         auto it = class_of.find(key);
         if (it == class_of.end()) {
           it = class_of.emplace(key, (int32_t)class_shapes.size()).first;
@@ -302,19 +305,22 @@ int validate_and_expand(gbo_plan *P) {
   const size_t es = P->x_dtype == GBO_BF16 ? 2 : 4;
   P->classes.clear();
   P->any_gram = false;
-  int64_t xoff = 0, poff = 0, goff = 0, x_route_end = 0;
+  int64_t xoff = 0, xtoff = 0, poff = 0, goff = 0, x_route_end = 0;
   for (size_t c = 0; c < order.size(); ++c) {
     ShapeClass C{};
     C.p = std::get<0>(class_shapes[order[c]]);
     C.q = std::get<1>(class_shapes[order[c]]);
     C.tall = std::get<2>(class_shapes[order[c]]);
+    C.x_tall = tc_path && C.tall;
     C.route = route[order[c]];
-    const int32_t xrows = C.tall ? C.q : C.p;  // X is p x q, or q x p when tall
-    C.ld = (int32_t)round_up(C.tall ? C.p : C.q, 16);
+    const int32_t xrows = C.x_tall ? C.q : C.p;  // X is p x q, or q x p when held tall
+    C.ld = (int32_t)round_up(C.x_tall ? C.p : C.q, 16);
+    C.ldt = tc_path ? 0 : (int32_t)round_up(C.p, 16);  // XT: q x p
     C.ldp = (int32_t)round_up(C.p, 16);
     C.count = 0;
     C.sub0 = -1;
     C.x_base = xoff;
+    C.xt_base = xtoff;
     // p x p buffers: the X route's P (and A) space, or the Gram route's own space
     int64_t &pspace = C.route == kRouteGram ? goff : poff;
     C.p_base = pspace;
@@ -323,8 +329,10 @@ int validate_and_expand(gbo_plan *P) {
         if (C.sub0 < 0) C.sub0 = (int32_t)k;
         DevSub &S = subs[k];
         S.ld = C.ld;
+        S.ldt = C.ldt;
         S.ldp = C.ldp;
         S.x_off = xoff + (int64_t)C.count * xrows * C.ld;
+        S.xt_off = xtoff + (int64_t)C.count * C.q * C.ldt;
         S.p_off = pspace + (int64_t)C.count * C.p * C.ldp;
         // the last iterate: X_k of the X route alternates buffers from X0;
         // the Gram route writes X_k = Q_k X_0 into the second buffer
@@ -332,6 +340,7 @@ int validate_and_expand(gbo_plan *P) {
         C.count++;
       }
     xoff = round_up(xoff + (int64_t)C.count * xrows * C.ld, 128);
+    xtoff = round_up(xtoff + (int64_t)C.count * C.q * C.ldt, 128);
     pspace = round_up(pspace + (int64_t)C.count * C.p * C.ldp, 128);
     if (C.route == kRouteX) x_route_end = xoff;
     else P->any_gram = true;
@@ -344,7 +353,7 @@ int validate_and_expand(gbo_plan *P) {
     // (views split rows only), and so is its X when ld == n: its momentum
     // tiles are flat runs of 4096 elements.  Tall matrices use 64 x 64 tiles
     // transposed through shared memory.
-    const bool flat = !S.transposed && S.vec_ok && S.ld == S.n;
+    const bool flat = !S.transposed && !S.has_xt && S.vec_ok && S.ld == S.n;
     S.tiles_c = flat ? 0 : (S.n + kMomTile - 1) / kMomTile;
     S.ntiles = flat ? (int32_t)(((int64_t)S.m * S.n + kMomFlat - 1) / kMomFlat)
                     : ((S.m + kMomTile - 1) / kMomTile) * S.tiles_c;
@@ -366,6 +375,10 @@ int validate_and_expand(gbo_plan *P) {
   P->off_x[0] = region((size_t)xoff * es);
   // the Gram route writes its last iterate into the second buffer only for NorMuon
   P->off_x[1] = region((size_t)(o.normuon ? xoff : x_route_end) * es);
+  // fp32 mode: XT twins of both X buffers (the second one for the X route's
+  // products and the NorMuon last iterate)
+  P->off_xt[0] = region((size_t)xtoff * es);
+  P->off_xt[1] = region((size_t)xtoff * es);
   P->off_p = region((size_t)poff * es);
   P->off_a = region(P->any_c ? (size_t)poff * es : 0);
   for (int b = 0; b < 6; ++b) P->off_g[b] = region((size_t)goff * es);
@@ -392,7 +405,8 @@ int validate_and_expand(gbo_plan *P) {
   }
   I.ns_flops = fl;
   I.n_gram_route = 0;
-  if (P->x_dtype == GBO_BF16) {
+  {
+    // the tile FLOPs of one pass (the fp32 kernel runs each as three TF32 products)
     double ex = 0;
     for (const ShapeClass &C : P->classes) {
       if (C.route == kRouteGram) {
@@ -404,8 +418,6 @@ int validate_and_expand(gbo_plan *P) {
       }
     }
     I.ns_flops_executed = ex;
-  } else {
-    I.ns_flops_executed = fl;
   }
   return GBO_OK;
 }
@@ -424,14 +436,6 @@ uint64_t layout_hash(const gbo_plan *P) {
   }
   f.put(P->opts.normuon);
   return f.h;
-}
-
-int launch_gemm_simt(const gbo_plan *P, const PhaseArgs &args, void *stream) {
-  return launch_ns_gemm_simt(P->classes.data(), (int32_t)P->classes.size(), args, P->sm_count, stream);
-}
-
-int64_t simt_launches(const gbo_plan *P) {
-  return ((int64_t)P->classes.size() + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch;
 }
 
 // One tensor-core step of the schedule: the jobs of every class that has
@@ -454,6 +458,8 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
   void *gA = R(P->off_g[0]), *gT = R(P->off_g[1]);
   void *gP[2] = {R(P->off_g[2]), R(P->off_g[3])};
   void *gQ[2] = {R(P->off_g[4]), R(P->off_g[5])};
+  void *xt[2] = {R(P->off_xt[0]), R(P->off_xt[1])};
+  const bool f32 = P->x_dtype == GBO_F32;
   auto job = [](const ShapeClass *C, int mode, int kind, int first, const float *abc, const void *opA,
                 const void *opB, void *out, void *out2 = nullptr, const void *aux = nullptr) {
     GemmJob J{};
@@ -479,8 +485,18 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
   };
   for (const ShapeClass &C : P->classes) {
     if (C.count == 0) continue;
-    const int kGramK = C.tall ? kKindGramT : kKindGram;  // X X^T, or X^T X of a tall X
-    const int kProdK = C.tall ? kKindProdT : kKindProd;  // P X, or X P of a tall X
+    const int kGramK = C.x_tall ? kKindGramT : kKindGram;  // X X^T, or X^T X of an X held tall
+    // the product with X = x[cur] into x[cur ^ 1]:
+    //   bf16   L X, or X L of an X held tall (then weights in stored orientation)
+    //   fp32   L X with B from X's twin XT, writing X' and X'T; the weight write
+    //          of a tall matrix takes XT L, which is in stored orientation
+    auto product = [&](int mode, int first, const float *abc, const void *L, int cur) {
+      if (!f32)
+        return C.x_tall ? job(&C, mode, kKindProdT, first, abc, x[cur], L, x[cur ^ 1])
+                        : job(&C, mode, kKindProd, first, abc, L, x[cur], x[cur ^ 1]);
+      if (mode == kFinal && C.tall) return job(&C, mode, kKindProdT, first, abc, xt[cur], L, nullptr);
+      return job(&C, mode, kKindProdK, first, abc, L, xt[cur], x[cur ^ 1], xt[cur ^ 1]);
+    };
     if (C.route == kRouteX) {
       size_t i = 0;
       int cur = 0;
@@ -495,9 +511,7 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
         }
         const bool last = it == k - 1;
         const int mode = (last && !normuon) ? kFinal : kProduct;
-        at(xs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
-            .jobs.push_back(C.tall ? job(&C, mode, kProdK, first, abc, x[cur], pb, x[cur ^ 1])
-                                   : job(&C, mode, kProdK, first, abc, pb, x[cur], x[cur ^ 1]));
+        at(xs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct).jobs.push_back(product(mode, first, abc, pb, cur));
         cur ^= 1;
       }
     } else {
@@ -522,9 +536,7 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
           .jobs.push_back(job(&C, kGramA, kKindSym, 0, nullptr, gP[(k - 1) & 1], k == 2 ? gP[0] : gQ[(k - 1) & 1],
                               gQ[k & 1]));
       const int mode = normuon ? kProduct : kFinal;
-      at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
-          .jobs.push_back(C.tall ? job(&C, mode, kProdK, 1, nullptr, x[0], gQ[k & 1], x[1])
-                                 : job(&C, mode, kProdK, 1, nullptr, gQ[k & 1], x[0], x[1]));
+      at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct).jobs.push_back(product(mode, 1, nullptr, gQ[k & 1], 0));
     }
   }
   std::vector<TcStep> steps(std::max(xs.size(), gs.size()));
@@ -631,11 +643,7 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   }
   P->hash = layout_hash(P);
   int64_t gemm = 0;
-  if (P->x_dtype == GBO_BF16) {
-    for (const TcStep &st : build_schedule(P, nullptr)) gemm += tc_step_launches(st);
-  } else {
-    for (int it = 0; it < k; ++it) gemm += (P->abc[3 * it + 2] != 0.f ? 3 : 2) * simt_launches(P);
-  }
+  for (const TcStep &st : build_schedule(P, nullptr)) gemm += tc_step_launches(st);
   P->info.launches_per_step =
       P->subs.empty() ? 0 : 2 + gemm + (opts->normuon ? (opts->rms_target > 0.f ? 3 : 1) : 0);
   *out = P;
@@ -728,8 +736,6 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   }
   char *ws = static_cast<char *>(workspace);
   void *x[2] = {ws + P->off_x[0], ws + P->off_x[1]};
-  void *pbuf = ws + P->off_p;
-  void *abuf = ws + P->off_a;
   float *alpha = reinterpret_cast<float *>(ws + P->off_alpha);
   float *partials = reinterpret_cast<float *>(ws + P->off_part);
   void *st = stream;
@@ -748,57 +754,26 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
     cudaEventRecord(last, reinterpret_cast<cudaStream_t>(stream));
   }
   const int32_t nsub = (int32_t)P->subs.size();
-  int err = launch_momentum(P->d_subs, nsub, P->n_tiles, P->opts.mu, P->opts.nesterov, x[0], P->x_dtype,
+  void *x0t = P->x_dtype == GBO_F32 ? ws + P->off_xt[0] : nullptr;
+  int err = launch_momentum(P->d_subs, nsub, P->n_tiles, P->opts.mu, P->opts.nesterov, x[0], x0t, P->x_dtype,
                             partials, P->sm_count, st);
   if (err) return cuda_fail(err, "momentum kernel");
   err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, st);
   if (err) return cuda_fail(err, "pre-normalisation kernel");
   mark(kPhaseMomentum, 2);
   PhaseArgs A{};
-  A.x_dtype = P->x_dtype;
   A.subs = P->d_subs;
   A.alpha = alpha;
-  A.pbuf = pbuf;
-  A.abuf = abuf;
   A.dbg = dbg_update;
   A.status = dev_status;
   A.lr = lr;
-  const int k = P->opts.ns_steps;
-  if (P->x_dtype == GBO_BF16) {
-    for (const TcStep &step : build_schedule(P, ws)) {
-      int64_t nl = 0;
-      if ((err = launch_ns_gemm_tc(step.jobs.data(), (int32_t)step.jobs.size(), A, P->sm_count, st, &nl)))
-        return cuda_fail(err, "Newton-Schulz kernel");
-      mark(step.phase, nl);
-    }
-  } else {
-    const int64_t gl = simt_launches(P);
-    int cur = 0;
-    for (int it = 0; it < k; ++it) {
-      A.a = P->abc[3 * it];
-      A.b = P->abc[3 * it + 1];
-      A.c = P->abc[3 * it + 2];
-      A.first = it == 0;
-      A.x_in = x[cur];
-      A.x_out = x[cur ^ 1];
-      if (A.c != 0.f) {
-        A.mode = kGramA;
-        if ((err = launch_gemm_simt(P, A, st))) return cuda_fail(err, "Gram kernel");
-        mark(kPhaseGram, gl);
-        A.mode = kSquare;
-        if ((err = launch_gemm_simt(P, A, st))) return cuda_fail(err, "square kernel");
-        mark(kPhaseSquare, gl);
-      } else {
-        A.mode = kGram;
-        if ((err = launch_gemm_simt(P, A, st))) return cuda_fail(err, "Gram kernel");
-        mark(kPhaseGram, gl);
-      }
-      const bool last_it = it == k - 1;
-      A.mode = (last_it && !P->opts.normuon) ? kFinal : kProduct;
-      if ((err = launch_gemm_simt(P, A, st))) return cuda_fail(err, "product kernel");
-      mark(A.mode == kFinal ? kPhaseFinal : kPhaseProduct, gl);
-      cur ^= 1;
-    }
+  for (const TcStep &step : build_schedule(P, ws)) {
+    int64_t nl = 0;
+    err = P->x_dtype == GBO_BF16
+              ? launch_ns_gemm_tc(step.jobs.data(), (int32_t)step.jobs.size(), A, P->sm_count, st, &nl)
+              : launch_ns_gemm_tf32(step.jobs.data(), (int32_t)step.jobs.size(), A, P->sm_count, st, &nl);
+    if (err) return cuda_fail(err, "Newton-Schulz kernel");
+    mark(step.phase, nl);
   }
   if (P->opts.normuon) {
     err = launch_normuon_rows(P->d_subs, nsub, P->n_row_blocks, x[0], x[1], P->x_dtype, P->opts.beta2,

@@ -60,7 +60,7 @@ extern "C" {
 
 /* ---- Newton-Schulz arithmetic ------------------------------------------ */
 #define GBO_NS_BF16 0 /* bf16 operands, fp32 accumulation (tcgen05 tensor cores) */
-#define GBO_NS_F32 1  /* fp32 operands and accumulation (FFMA)                    */
+#define GBO_NS_F32 1  /* fp32 operands (three TF32 products), fp32 accumulation    */
 
 #define GBO_MAX_VIEW_DIMS 6
 #define GBO_MAX_NS_STEPS 64
@@ -140,7 +140,8 @@ typedef struct {
  *         instead of about k (p^2 q + 2 p^2 q) FLOPs; allowed when every
  *         iteration has c == 0 and k >= 2.
  *   AUTO  GRAM where it is allowed and executes fewer FLOPs (q > p), else X.
- * The fp32 mode always takes the X route.
+ * Both precisions run on the tensor cores: bf16 operands, or in the fp32
+ * mode fp32 operands as three TF32 products (hi hi + hi lo + lo hi).
  */
 #define GBO_ROUTE_AUTO 0
 #define GBO_ROUTE_X 1
