@@ -45,15 +45,21 @@ constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's rows of A
 constexpr int B_HALF = (BN / 2) * BK * 2;        // 16 KB: 128 rows of B
 // Two modes share the kernel source:
 //   pair   (kPair = true)  2-CTA cluster, tcgen05 cta_group::2, 256 x 256 tile;
-//                          each CTA stages A 16 KB + half of B 16 KB (6 stages)
-//   single (kPair = false) one CTA, cta_group::1, 128 x 256 tile; the CTA
-//                          stages A 16 KB + all of B 32 KB (4 stages); used for
-//                          matrices of at most 128 rows, where a pair would
-//                          spend its second CTA on padding
+//                          a stage holds two 64-wide K blocks, each A 16 KB +
+//                          half of B 16 KB per CTA (3 stages of 64 KB: one
+//                          barrier handshake per 8 MMAs; about 1% faster on
+//                          the 1.23B set than 6 stages of one block, over
+//                          eight interleaved runs)
+//   single (kPair = false) one CTA, cta_group::1, 128 x 256 tile; a stage
+//                          holds one K block, A 16 KB + all of B 32 KB (4
+//                          stages); used for matrices of at most 128 rows,
+//                          where a pair would spend its second CTA on padding
 template <bool kPair>
 struct Mode {
-  static constexpr int kStageBytes = A_BYTES + (kPair ? B_HALF : 2 * B_HALF);
-  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kSub = kPair ? 2 : 1;  // BK-wide K blocks per stage
+  static constexpr int kSubBytes = A_BYTES + (kPair ? B_HALF : 2 * B_HALF);
+  static constexpr int kStageBytes = kSub * kSubBytes;
+  static constexpr int kStages = kPair ? 3 : 4;
   static constexpr int kRows = kPair ? 2 : 1;  // 128-row tiles per work item
 };
 constexpr int kRingBytes = 6 * (A_BYTES + B_HALF);
@@ -235,9 +241,11 @@ __device__ __forceinline__ bool produce_tile(const TcParams &P, const TileCoord 
       armed[stage] = true;
       armed_parity[stage] = phase;
     }
-    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+#pragma unroll
+    for (int sub = 0; sub < Mode<kPair>::kSub; ++sub) {
+    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES + sub * Mode<kPair>::kSubBytes);
     const uint32_t sb = sa + A_BYTES;
-    const int k0 = kb * BK;
+    const int k0 = (kb * Mode<kPair>::kSub + sub) * BK;
     if constexpr (kPair) {
       const uint32_t fb = full_lead0 + 8 * stage;
       if constexpr (!kAmn) {
@@ -268,6 +276,7 @@ __device__ __forceinline__ bool produce_tile(const TcParams &P, const TileCoord 
         for (int h = 0; h < BN / 64; ++h) tma_load_3d(sb + h * 8192, mb, fb, n0 + h * 64, k0, tc.mat);
       }
     }
+    }
     if (++stage == STAGES) stage = 0, phase ^= 1;
   }
   return true;
@@ -287,11 +296,15 @@ __device__ __forceinline__ bool mma_tile(uint8_t *smem, uint32_t full0, uint32_t
   for (int kb = 0; kb < kit; ++kb) {
     if (!mbar_wait(full0 + 8 * stage, phase)) return false;
     tc_fence_after();
-    const uint32_t soff = (uint32_t)(stage * STAGE_BYTES) >> 4;
 #pragma unroll
-    for (int k = 0; k < BK / 16; ++k) {
-      if constexpr (kPair) mma_bf16_pair(d_tmem, a0 + soff + k * astep, b0 + soff + k * bstep, idesc, (kb | k) != 0);
-      else mma_bf16_one(d_tmem, a0 + soff + k * astep, b0 + soff + k * bstep, idesc, (kb | k) != 0);
+    for (int sub = 0; sub < Mode<kPair>::kSub; ++sub) {
+      const uint32_t soff = (uint32_t)(stage * STAGE_BYTES + sub * Mode<kPair>::kSubBytes) >> 4;
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k) {
+        const uint32_t acc = (kb | sub | k) != 0;
+        if constexpr (kPair) mma_bf16_pair(d_tmem, a0 + soff + k * astep, b0 + soff + k * bstep, idesc, acc);
+        else mma_bf16_one(d_tmem, a0 + soff + k * astep, b0 + soff + k * bstep, idesc, acc);
+      }
     }
     issued = true;
     if constexpr (kPair) mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs
@@ -518,9 +531,10 @@ int64_t sym_items_of(int p) {
   return n;
 }
 
-double item_flops(int p, int kdim) {  // one work item: rows x 128 x 256 outputs, K padded to BK
+double item_flops(int p, int kdim) {  // one work item: rows x 128 x 256 outputs, K padded to a stage
   const int rows = single_mode(p) ? 1 : 2;
-  return 2.0 * rows * BM * BN * (double)((kdim + BK - 1) / BK) * BK;
+  const int kstage = rows * BK;  // pairs stage two BK-wide blocks, single CTAs one
+  return 2.0 * rows * BM * BN * (double)((kdim + kstage - 1) / kstage) * kstage;
 }
 
 // The p x q product (wide: p x q output) or its transpose (tall: q x p).
@@ -621,7 +635,8 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
       tj.out2 = J.out2;
       tj.aux = J.aux;
       T.tiles_n[k] = (Ndim + BN - 1) / BN;
-      T.k_iters[k] = (Kdim + BK - 1) / BK;
+      constexpr int kStageK = Mode<kPair>::kSub * BK;
+      T.k_iters[k] = (Kdim + kStageK - 1) / kStageK;
       T.sub0[k] = C.sub0;
       const int items_m = ((Mdim + BM - 1) / BM + kRows - 1) / kRows;
       if (!is_product_kind(J.kind)) {
