@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "f32"],
+                    help="Newton-Schulz operands: bf16 (the benchmark) or the fp32 mode (three TF32 products)")
     ap.add_argument("--overlap", action="store_true",
                     help="run clip + AdamW on a side stream that starts after the momentum phase")
     ap.add_argument("--workload", type=int, default=WORKLOAD,
@@ -316,7 +318,9 @@ def run_ours(args):
         del g
         off += t.numel
         params.append((p, gv, m, v))
-    plan = gbo.gbo_muon_plan_create(entries, precision=gbo.GBO_NS_BF16, normuon=wl.normuon)
+    f32 = args.precision == "f32"
+    prec = gbo.GBO_NS_F32 if f32 else gbo.GBO_NS_BF16
+    plan = gbo.gbo_muon_plan_create(entries, precision=prec, normuon=wl.normuon)
     info = gbo.gbo_muon_plan_info(plan)
     ws = torch.empty(gbo.gbo_muon_workspace_bytes(plan), dtype=torch.uint8, device=dev)
     cws = torch.empty(gbo.gbo_clip_norm_workspace_bytes(), dtype=torch.uint8, device=dev)
@@ -408,7 +412,7 @@ def run_ours(args):
         for p, g, m, v in params:
             params2.append((p, ag_flat2[off:off + g.numel()].view(g.shape), m, v))
             off += g.numel()
-        plan2 = gbo.gbo_muon_plan_create(entries2, precision=gbo.GBO_NS_BF16, normuon=wl.normuon)
+        plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon)
         bound.append((plan2, params2, [p[1] for p in params2]))
         e2e_value, h2d = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total)
 
@@ -421,7 +425,8 @@ def run_ours(args):
     fin_ms, fin_n = phases["final"]
     gemm_ms = (gram_ms + prod_ms + sq_ms + fin_ms) / args.steps
     gemm_launches = (gram_n + prod_n + sq_n + fin_n) / args.steps
-    flops = info["ns_flops_executed"]
+    # executed tensor FLOPs: the tile products, three TF32 passes each in the fp32 mode
+    flops = info["ns_flops_executed"] * (3 if f32 else 1)
     achieved_tf = flops / (gemm_ms / 1e3) / 1e12
     counted_tf = info["ns_flops"] / (gemm_ms / 1e3) / 1e12
     peaks = {}
@@ -432,7 +437,10 @@ def run_ours(args):
     peak_src = "measured (sustained, MEASURED_PEAKS.json)"
     if peak_tf is None:
         peak_tf, peak_src = 1700.0, "fallback sustained"
-    tr = traffic_record("ns_gemm_tc.cu")
+    if f32:  # TF32 runs at the nominal 1.1 / 2.25 of the bf16 dense rate
+        peak_tf *= 1.1 / 2.25
+        peak_src += " x nominal TF32/bf16 ratio 1.1/2.25"
+    tr = traffic_record("ns_gemm_tc.cu") if not f32 else None
     traffic = None
     if tr is not None:
         traffic = tr["bytes_per_unit"] * (flops / gemm_launches) / tr["unit_flops"]
@@ -446,12 +454,16 @@ def run_ours(args):
     out = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32" if f32 else "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "muon_params": wl.muon_params,
                    "adamw_params": n_adam, "matrices": info["n_matrices"], "ns_steps": wl.ns_steps,
-                   "ns_precision": "bf16 operands, fp32 accumulate", "parallelism": "replicas" if world > 1 else "single",
+                   "ns_precision": ("fp32 operands as three TF32 products, fp32 accumulate" if f32
+                                    else "bf16 operands, fp32 accumulate"),
+                   "parallelism": "replicas" if world > 1 else "single",
                    "l2": "working set ~20 GB per GPU, far above the 129 MB L2: no flush needed"},
-        "roofline": {"bound": "tensor", "kernel": "ns_gemm_tc_kernel (all Newton-Schulz launches), executed FLOPs",
+        "roofline": {"bound": "tensor",
+                     "kernel": ("ns_gemm_tf32_kernel" if f32 else "ns_gemm_tc_kernel")
+                               + " (all Newton-Schulz launches), executed FLOPs",
                      "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
                      "peak_source": peak_src, "traffic": traffic,
                      "flops_per_launch": flops / gemm_launches, "ms_per_launch": gemm_ms / gemm_launches},
