@@ -11,15 +11,15 @@
 // iterate is held both as X (p x q) and as its transpose XT (q x p), and
 // the products take XT where they need X with K along its rows.
 //
-// Persistent, warp-specialised CTA (256 threads, one CTA per SM):
+// Persistent, warp-specialised CTA (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane): each CTA loads its own A rows and
 //               its half of B into the raw part of a stage
 //   warp 1      TMEM owner and MMA issuer (one lane, the pair's even CTA)
 //   warps 2..5  epilogue, one per TMEM lane quarter: TMEM -> registers ->
 //               a 128-byte-swizzled staging slot -> TMA store
-//   warps 6, 7  split: once a stage has landed, each of its fp32 values x
+//   warps 6..9  split: once a stage has landed, each of its fp32 values x
 //               becomes hi(x) in place and lo(x) in the stage's lo part;
-//               both warps of both CTAs then arrive on the leader's
+//               the split warps of both CTAs then arrive on the leader's
 //               split barrier, which the MMA issuer waits on
 // Every wait is bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT,
 // waits (bounded) for its own copies and MMAs, frees TMEM and returns.
@@ -54,7 +54,7 @@ constexpr int kFRing = 3 * (FA_BYTES + FB_HALF);  // raw parts; the lo parts fol
 static_assert(FMode<true>::kStages * FMode<true>::kRawBytes == kFRing, "ring size");
 static_assert(FMode<false>::kStages * FMode<false>::kRawBytes == kFRing, "ring size");
 constexpr int kFEpiWarps = 4;
-constexpr int kFSplitWarps = 2;
+constexpr int kFSplitWarps = 4;  // A/B on the 1.23B set: 140 ms per step with 2, 115 with 4, 114.5 with 6
 constexpr int kFThreads = 32 * (2 + kFEpiWarps + kFSplitWarps);
 // Per epilogue warp: one 8 KB slot, a 32 x 32 fp32 block and its transpose.
 constexpr int kFSlotBytes = 8192;
@@ -363,7 +363,7 @@ ns_gemm_tf32_kernel(const __grid_constant__ TcParams P, const __grid_constant__ 
       }
     }
   } else if (warp >= 2 + kFEpiWarps) {
-    // split warps: each takes every other 16-byte chunk of the stage's raw part
+    // split warps: each takes every kFSplitWarps-th run of 32 16-byte chunks of the stage's raw part
     const int sw = warp - (2 + kFEpiWarps);
     int stage = 0;
     uint32_t phase = 0;
