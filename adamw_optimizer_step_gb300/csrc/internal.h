@@ -47,6 +47,8 @@ struct DevSub {
   float wd;
   int32_t w_vec;    // weight rows start on 16-byte boundaries (vector read-modify-write)
   int32_t x_sel;    // X buffer (0 or 1) that holds the last iterate (NorMuon rows read it)
+  int32_t wmap;     // index of the weight's TMA map (bf16 weights with 16-byte rows), or -1
+  int32_t pad2;
 };
 
 // Matrices of one oriented shape (p, q), stored back to back in the
@@ -130,6 +132,7 @@ struct GemmJob {
 // is in its GemmJob).
 struct PhaseArgs {
   float lr;
+  const void *wmaps;  // device array of the weights' TMA maps (CUtensorMap), see build_weight_maps
   const DevSub *subs;
   const float *alpha; // per matrix pre-normalisation factor
   float *dbg;         // dbg_update or nullptr
@@ -178,6 +181,11 @@ double tc_gram_route_flops(int p, int q, int k, bool tall);
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);
+// One 3-D TMA map (columns, rows, 1) per descriptor for the last product's
+// weight stores: 32 x 32 boxes, 64-byte swizzle, for bf16 weights whose rows
+// start on 16-byte boundaries (others zero, and their matrices carry wmap =
+// -1).  *out receives a device array the caller frees with cudaFree.
+int build_weight_maps(const gbo_muon_desc *descs, int32_t n, void **out);
 // Testing: the GEMM's bounded mbarrier wait on a barrier nothing arrives on.
 int launch_wait_timeout(int32_t *status, uint64_t limit_ns, void *stream);
 

@@ -68,9 +68,7 @@ static_assert(Mode<false>::kStages * Mode<false>::kStageBytes == kRingBytes, "ri
 // Epilogue warps: one per TMEM lane quarter.
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-// Per epilogue warp: two 4 KB store slots, each a 32 x 32 bf16 block and its
-// transpose in the 64-byte-swizzled layout TMA stores read.
-constexpr int kSlotBytes = 4096;
+// Per epilogue warp: two store slots (kSlotBytes each, tc_common.cuh).
 constexpr int kWarpStageBytes = 2 * kSlotBytes;
 constexpr int kStageBytes = kEpiWarps * kWarpStageBytes;
 constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + kStageBytes + 256 /*barriers*/;
@@ -109,51 +107,6 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-
-// Byte offset of 16-byte chunk q of row r in a 32-row x 64-byte bf16 block in
-// the 64-byte swizzle layout of TMA (chunk index XOR bits 7-8 of the offset).
-__device__ __forceinline__ uint32_t sw64(int r, int q) { return (uint32_t)(r * 64 + ((q ^ ((r >> 1) & 3)) << 4)); }
-
-// Lane r holds row r of a 32 x 32 block: write it as bf16 row r.
-__device__ __forceinline__ void stage_rows(uint32_t dst, const float (&o)[32], int lane) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + sw64(lane, q)),
-                 "r"(pack_bf16(o[8 * q], o[8 * q + 1])), "r"(pack_bf16(o[8 * q + 2], o[8 * q + 3])),
-                 "r"(pack_bf16(o[8 * q + 4], o[8 * q + 5])), "r"(pack_bf16(o[8 * q + 6], o[8 * q + 7]))
-                 : "memory");
-}
-
-// The transpose: element (lane, k) goes to row k, column lane.  For each k
-// the warp writes one 64-byte row, two lanes per 32-bit word.
-__device__ __forceinline__ void stage_cols(uint32_t dst, const float (&o)[32], int lane) {
-  const uint32_t col = (uint32_t)((lane & 7) * 2);
-#pragma unroll
-  for (int k = 0; k < 32; ++k)
-    asm volatile("st.shared.b16 [%0], %1;" ::"r"(dst + sw64(k, lane >> 3) + col),
-                 "h"(__bfloat16_as_ushort(__float2bfloat16_rn(o[k])))
-                 : "memory");
-}
-
-// Store a warp's 32 x 32 block at (x0, y0) of matrix z, and with `mirror`
-// its transpose at (y0, x0), through the next of the warp's two staging
-// slots; TMA drops whatever falls outside the tensor.
-__device__ __forceinline__ void tma_store_block(const CUtensorMap *map, uint32_t stage, int &slot,
-                                                const float (&o)[32], bool mirror, int x0, int y0, int z, int lane) {
-  const uint32_t dst = stage + (uint32_t)(slot * kSlotBytes);
-  slot ^= 1;
-  if (lane == 0) bulk_wait_read<1>();  // the stores that last used this slot have read it
-  __syncwarp();
-  stage_rows(dst, o, lane);
-  if (mirror) stage_cols(dst + 2048, o, lane);
-  fence_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    tma_store_3d(map, dst, x0, y0, z);
-    if (mirror) tma_store_3d(map, dst + 2048, y0, x0, z);
-    bulk_commit();
-  }
 }
 
 // Epilogue of one warp's 32 rows x 32 columns of the accumulator.  Lane r
@@ -467,7 +420,8 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (i0 < rows) {  // warps whose rows are all padding have nothing to write
         if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
-          final_tile_bf16(A, S, s, i0, tc.tn * BN, rows, cols, trow, lane);
+          const CUtensorMap *wmap = S.wmap >= 0 ? static_cast<const CUtensorMap *>(A.wmaps) + S.wmap : nullptr;
+          final_tile_bf16(A, S, s, i0, tc.tn * BN, rows, cols, trow, lane, wmap, stage, &slot);
         } else {
 #pragma unroll 1
           for (int ch = 0; ch < BN / 32; ++ch) {
@@ -708,6 +662,29 @@ int launch_wait_timeout(int32_t *status, uint64_t limit_ns, void *stream) {
   wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, limit_ns);
   count_launches(1);
   return (int)cudaGetLastError();
+}
+
+int build_weight_maps(const gbo_muon_desc *descs, int32_t n, void **out) {
+  *out = nullptr;
+  if (n <= 0) return 0;
+  std::vector<CUtensorMap> maps((size_t)n);
+  memset(maps.data(), 0, maps.size() * sizeof(CUtensorMap));
+  for (int32_t t = 0; t < n; ++t) {
+    const gbo_muon_desc &d = descs[t];
+    if (d.w_dtype != GBO_BF16 || (d.cols * 2) % 16 != 0 || (reinterpret_cast<uintptr_t>(d.w) & 15) != 0) continue;
+    if (!encode_map(&maps[t], d.w, d.cols, d.rows, 1, d.cols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return (int)cudaErrorInvalidValue;
+  }
+  void *dev = nullptr;
+  cudaError_t e = cudaMalloc(&dev, maps.size() * sizeof(CUtensorMap));
+  if (e != cudaSuccess) return (int)e;
+  e = cudaMemcpy(dev, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(dev);
+    return (int)e;
+  }
+  *out = dev;
+  return 0;
 }
 
 int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count, void *stream,

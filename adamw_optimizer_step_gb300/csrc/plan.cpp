@@ -141,6 +141,7 @@ struct gbo_plan {
   int device = -1;
   int sm_count = 0;
   DevSub *d_subs = nullptr;
+  void *d_wmaps = nullptr;  // the weights' TMA maps (bf16 mode)
   // phase timing
   bool timing = false;
   struct Interval {
@@ -271,6 +272,8 @@ int validate_and_expand(gbo_plan *P) {
         S.g_dtype = d.g_dtype;
         S.vec_ok = vec_rows;
         S.w_vec = ((d.cols * (int64_t)dtype_size(d.w_dtype)) % 16 == 0) && aligned(d.w, 16);
+        // the last product stores bf16 weights through a TMA map of the weight
+        S.wmap = (P->x_dtype == GBO_BF16 && d.w_dtype == GBO_BF16 && S.w_vec) ? t : -1;
         S.scale = (float)std::sqrt(std::max(1.0, (double)S.m / (double)S.n));
         S.lr_mult = d.lr_mult;
         S.wd = d.wd;
@@ -653,6 +656,7 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
 void gbo_muon_plan_destroy(gbo_plan *P) {
   if (!P) return;
   if (P->d_subs) cudaFree(P->d_subs);
+  if (P->d_wmaps) cudaFree(P->d_wmaps);
   for (auto &iv : P->pending) {
     cudaEventDestroy(iv.a);
     cudaEventDestroy(iv.b);
@@ -729,6 +733,10 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(matrix table)");
     e = cudaMemcpy(P->d_subs, P->subs.data(), P->subs.size() * sizeof(DevSub), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(matrix table)");
+    if (P->x_dtype == GBO_BF16) {
+      const int me = build_weight_maps(P->descs.data(), (int32_t)P->descs.size(), &P->d_wmaps);
+      if (me) return cuda_fail(me, "weight tensor maps");
+    }
     P->device = dev;
     P->sm_count = di.sm_count;
   } else if (P->device != dev) {
@@ -763,6 +771,7 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   mark(kPhaseMomentum, 2);
   PhaseArgs A{};
   A.subs = P->d_subs;
+  A.wmaps = P->d_wmaps;
   A.alpha = alpha;
   A.dbg = dbg_update;
   A.status = dev_status;

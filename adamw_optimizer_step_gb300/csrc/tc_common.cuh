@@ -356,6 +356,55 @@ __device__ __forceinline__ uint32_t prefix_mask(int n) {  // the low n bits, n i
   return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
+// bf16 staging of the bf16 kernel's epilogue: per warp two slots of
+// kSlotBytes, each a 32 x 32 bf16 block and its transpose.
+constexpr int kSlotBytes = 4096;
+
+// Byte offset of 16-byte chunk q of row r in a 32-row x 64-byte bf16 block in
+// the 64-byte swizzle layout of TMA (chunk index XOR bits 7-8 of the offset).
+__device__ __forceinline__ uint32_t sw64(int r, int q) { return (uint32_t)(r * 64 + ((q ^ ((r >> 1) & 3)) << 4)); }
+
+// Lane r holds row r of a 32 x 32 block: write it as bf16 row r.
+__device__ __forceinline__ void stage_rows(uint32_t dst, const float (&o)[32], int lane) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + sw64(lane, q)),
+                 "r"(pack_bf16(o[8 * q], o[8 * q + 1])), "r"(pack_bf16(o[8 * q + 2], o[8 * q + 3])),
+                 "r"(pack_bf16(o[8 * q + 4], o[8 * q + 5])), "r"(pack_bf16(o[8 * q + 6], o[8 * q + 7]))
+                 : "memory");
+}
+
+// The transpose: element (lane, k) goes to row k, column lane.  For each k
+// the warp writes one 64-byte row, two lanes per 32-bit word.
+__device__ __forceinline__ void stage_cols(uint32_t dst, const float (&o)[32], int lane) {
+  const uint32_t col = (uint32_t)((lane & 7) * 2);
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(dst + sw64(k, lane >> 3) + col),
+                 "h"(__bfloat16_as_ushort(__float2bfloat16_rn(o[k])))
+                 : "memory");
+}
+
+// Store a warp's 32 x 32 block at (x0, y0) of matrix z, and with `mirror`
+// its transpose at (y0, x0), through the next of the warp's two staging
+// slots; TMA drops whatever falls outside the tensor.
+__device__ __forceinline__ void tma_store_block(const CUtensorMap *map, uint32_t stage, int &slot,
+                                                const float (&o)[32], bool mirror, int x0, int y0, int z, int lane) {
+  const uint32_t dst = stage + (uint32_t)(slot * kSlotBytes);
+  slot ^= 1;
+  if (lane == 0) bulk_wait_read<1>();  // the stores that last used this slot have read it
+  __syncwarp();
+  stage_rows(dst, o, lane);
+  if (mirror) stage_cols(dst + 2048, o, lane);
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(map, dst, x0, y0, z);
+    if (mirror) tma_store_3d(map, dst + 2048, y0, x0, z);
+    bulk_commit();
+  }
+}
+
 // Weight write of 32 consecutive elements of one stored row: W[row][c0..c0+31]
 // with the update directions u[0..31] (valid under `mask`).
 template <typename WT>
@@ -418,8 +467,17 @@ __device__ __forceinline__ void wseg_unpack(const WSeg &r, float (&o)[32]) {
 // stored row r0 + i0 + r.  The weights of chunk ch + 1 are loaded before
 // chunk ch is computed, so a load of each lane's row segment is always in
 // flight instead of the warp waiting on every chunk's loads in turn.
+//
+// With `wmap` (a TMA map over the whole weight, 32 x 32 boxes, 64-byte
+// swizzle) and a block of 32 whole rows, the new weights leave through the
+// warp's staging slots and TMA stores; a block that would reach past the
+// matrix's rows (into another matrix of the same weight) keeps the masked
+// stores.
 __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub &S, float s, int i0, int tile_col0,
-                                                int rows, int cols, uint32_t trow, int lane) {
+                                                int rows, int cols, uint32_t trow, int lane,
+                                                const CUtensorMap *wmap = nullptr, uint32_t stage = 0,
+                                                int *slot = nullptr) {
+  const bool tma = wmap != nullptr && i0 + 32 <= rows;  // the same for every lane
   const int nch = min(BN / 32, (cols - tile_col0 + 31) / 32);  // chunks holding columns < cols
   const float lr = A.lr * S.lr_mult, su = S.scale * s;
   __nv_bfloat16 *W = reinterpret_cast<__nv_bfloat16 *>(S.w);
@@ -449,7 +507,8 @@ __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub
         u[k] *= su;
         w[k] = w[k] - lr * (S.wd * w[k] + u[k]);
       }
-      store_row32(W + wrow + col0, w, S.w_vec && mask == 0xffffffffu, mask);
+      if (tma) tma_store_block(wmap, stage, *slot, w, false, col0, (int)(S.r0 + i0), 0, lane);
+      else store_row32(W + wrow + col0, w, S.w_vec && mask == 0xffffffffu, mask);
       if (A.dbg) {
         float *d = A.dbg + S.dbg_off + wrow + col0;
         store_row32(d, u, mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0, mask);
