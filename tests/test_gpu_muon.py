@@ -88,21 +88,22 @@ def test_coefficients_and_options(precision, opts):
     check_muon(entries, gpu, ora, lr=0.05, precision=precision, mu=kw.get("mu", 0.95))
 
 
+@pytest.mark.parametrize("precision", ["bf16", "f32"])
 @pytest.mark.parametrize("route", ["x", "gram"])
 @pytest.mark.parametrize("ns_steps", [2, 3, 5, 8])
-def test_routes(route, ns_steps):
-    """Both routes of the bf16 iterations reach the oracle's k-step result:
-    the X route, and the Gram route forced on every shape (square, tall,
-    1 x n and split views included), for short and long k (the Gram route
-    rotates its P and Q buffers by iteration)."""
+def test_routes(route, ns_steps, precision):
+    """Both routes reach the oracle's k-step result in both precisions: the
+    X route, and the Gram route forced on every shape (square, tall, 1 x n
+    and split views included), for short and long k (the Gram route rotates
+    its P and Q buffers by iteration)."""
     entries = random_entries(RAGGED, seed=21, b_std=1e-3)
     r = B.GBO_ROUTE_X if route == "x" else B.GBO_ROUTE_GRAM
-    gpu, status, plan = run_muon_gpu(entries, lr=0.02, precision="bf16", ns_steps=ns_steps, route=r)
+    gpu, status, plan = run_muon_gpu(entries, lr=0.02, precision=precision, ns_steps=ns_steps, route=r)
     info = B.gbo_muon_plan_info(plan)
     assert info["n_gram_route"] == (0 if route == "x" else info["n_matrices"])
     ora = run_muon_oracle(entries, lr=0.02, ns_steps=ns_steps)
     assert status == 0
-    check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
+    check_muon(entries, gpu, ora, lr=0.02, precision=precision)
 
 
 @pytest.mark.parametrize("precision", ["f32", "bf16"])
