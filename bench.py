@@ -241,7 +241,8 @@ def run_e2e(n_steps, world, bufs, step, total):
     the upload of step n + 1's gradients runs on a copy stream into one pair
     while step n computes on the other, as a trainer overlaps its input
     transfers.  Every step's copy and read stay inside the timed region.
-    Returns (steps/s over all ranks, bytes copied in per step)."""
+    Returns (steps/s over all ranks, bytes copied in per step, the upload's
+    GB/s when it runs alone)."""
     import torch
     g_flat, ag_flat = bufs[0]
     h_g = torch.empty(g_flat.numel(), dtype=g_flat.dtype, pin_memory=True)
@@ -260,7 +261,15 @@ def run_e2e(n_steps, world, bufs, step, total):
             bufs[b][1].copy_(h_ag, non_blocking=True)
         copied[b].record(copy)
 
+    # the upload alone (after one untimed copy), to tell a copy-bound host
+    # from a compute-bound one: the host side of this path varies between hosts
+    h2d = h_g.numel() * h_g.element_size() + h_ag.numel() * h_ag.element_size()
+    upload(0)
     torch.cuda.synchronize()
+    t_up = time.perf_counter()
+    upload(0)
+    torch.cuda.synchronize()
+    up_gbs = h2d / (time.perf_counter() - t_up) / 1e9
     barrier(world)
     t0 = time.perf_counter()
     upload(0)
@@ -274,8 +283,7 @@ def run_e2e(n_steps, world, bufs, step, total):
         _ = float(total.item())  # the step's result on the host
     torch.cuda.synchronize()
     e2e_t = max_over_ranks(time.perf_counter() - t0, world)
-    h2d = h_g.numel() * h_g.element_size() + h_ag.numel() * h_ag.element_size()
-    return aggregate(n_steps, e2e_t, world), h2d
+    return aggregate(n_steps, e2e_t, world), h2d, up_gbs
 
 
 def run_ours(args):
@@ -400,7 +408,7 @@ def run_ours(args):
         raise RuntimeError("device status %d during the timed steps" % int(status.item()))
 
     # end to end: gradients from pinned host memory, norm read back
-    e2e_value, h2d = None, 0
+    e2e_value, h2d, up_gbs = None, 0, None
     if args.e2e_steps > 0:
         g_flat2, ag_flat2 = torch.empty_like(g_flat), torch.empty_like(ag_flat)
         entries2, off = [], 0
@@ -414,7 +422,7 @@ def run_ours(args):
             off += g.numel()
         plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon)
         bound.append((plan2, params2, [p[1] for p in params2]))
-        e2e_value, h2d = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total)
+        e2e_value, h2d, up_gbs = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total)
 
     if rank != 0:
         return
@@ -476,7 +484,9 @@ def run_ours(args):
         "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "steps/s",
                                                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4,
                                                "overlap": "step n+1's gradient upload runs during step n "
-                                                          "(two gradient buffers)"},
+                                                          "(two gradient buffers)",
+                                               "upload_GBps_alone": up_gbs,
+                                               "upload_ms_alone": None if not up_gbs else h2d / up_gbs / 1e6},
         "gpu_launches": int(launches),
         "clocks": clk,
         "cpu_baseline": cpu,
