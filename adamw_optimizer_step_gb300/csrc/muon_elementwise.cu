@@ -120,11 +120,16 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
         if (i < S.m && valid > 0) store8(S.mom + (S.r0 + i) * S.cols + j, b[ps], valid, vec);
       }
       // D itself goes to X, or with a transposed twin (fp32 mode) to XT when X
-      // holds D^T; D^T goes to X when transposed, else to XT when it exists
-      XT *direct = S.transposed ? (S.has_xt ? x0t + S.xt_off : nullptr) : x0 + S.x_off;
-      const int ld_direct = S.transposed ? S.ldt : S.ld;
-      XT *trans = S.transposed ? x0 + S.x_off : (S.has_xt ? x0t + S.xt_off : nullptr);
-      const int ld_trans = S.transposed ? S.ld : S.ldt;
+      // holds D^T; D^T goes to X when transposed, else to XT when it exists.
+      // The bf16 mode holds every X in stored orientation: D to X only.
+      XT *direct = x0 + S.x_off, *trans = nullptr;
+      int ld_direct = S.ld, ld_trans = 0;
+      if constexpr (sizeof(XT) == 4) {
+        direct = S.transposed ? (S.has_xt ? x0t + S.xt_off : nullptr) : x0 + S.x_off;
+        ld_direct = S.transposed ? S.ldt : S.ld;
+        trans = S.transposed ? x0 + S.x_off : (S.has_xt ? x0t + S.xt_off : nullptr);
+        ld_trans = S.transposed ? S.ld : S.ldt;
+      }
       if (direct) {
 #pragma unroll
         for (int ps = 0; ps < 2; ++ps) {
