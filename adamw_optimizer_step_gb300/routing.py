@@ -153,11 +153,15 @@ class HybridOptimizer:
     Muon weights may be bf16 or fp32; AdamW parameters must be fp32.  The
     Muon plan binds the gradient tensors; it is rebuilt when the set of
     gradient tensors changes (e.g. after ``zero_grad(set_to_none=True)``).
+
+    ``precision`` "bf16" or "f32" (three TF32 products); ``route`` "auto",
+    "x" or "gram" (see gbo_muon_opts); ``rms_target`` > 0 with NorMuon
+    scales each matrix's update to that RMS.
     """
 
     def __init__(self, model, *, muon_lr=0.01, adamw_lr=3e-4, weight_decay=0.0, auxiliary_decay=True, mu=0.95,
                  ns_steps=5, abc=(1.5, -0.5, 0.0), normuon=False, beta2_rows=0.95, eps_rows=1e-8,
-                 rms_target=0.0, betas=(0.9, 0.95), eps=1e-8, max_norm=1.0, precision="bf16"):
+                 rms_target=0.0, betas=(0.9, 0.95), eps=1e-8, max_norm=1.0, precision="bf16", route="auto"):
         from . import _binding as B
         self.B = B
         self.routes = build_parameter_groups(model, weight_decay, auxiliary_decay)
@@ -170,6 +174,7 @@ class HybridOptimizer:
         self.betas, self.eps, self.max_norm = betas, eps, max_norm
         self.opts = dict(abc=abc, ns_steps=ns_steps, mu=mu, normuon=normuon, beta2=beta2_rows, eps=eps_rows,
                          rms_target=rms_target,
+                         route={"auto": B.GBO_ROUTE_AUTO, "x": B.GBO_ROUTE_X, "gram": B.GBO_ROUTE_GRAM}[route],
                          precision=B.GBO_NS_F32 if precision == "f32" else B.GBO_NS_BF16)
         self.state = {}
         for r in self.muon:

@@ -152,21 +152,27 @@ def test_normuon_rows(precision):
     check_muon(entries, gpu, ora, lr=0.02, precision=precision)
 
 
-def test_skip_zero_and_nonfinite():
+@pytest.mark.parametrize("precision", ["bf16", "f32"])
+@pytest.mark.parametrize("route", ["x", "gram"])
+def test_skip_zero_and_nonfinite(route, precision):
+    """Inactive weights stay untouched, a zero gradient gives a pure decay
+    step (A_0 = 0 on the Gram route: Q_k = a^k I times a zero X_0), and a NaN
+    gradient is reported in the status word, on both routes."""
+    r = B.GBO_ROUTE_X if route == "x" else B.GBO_ROUTE_GRAM
     shapes = [(64, 96, None, None), (48, 48, None, None, 1.0, 0.1), (32, 32, None, None)]
     entries = random_entries(shapes, seed=14, b_std=0.0)
     entries[0]["g"] = None                        # inactive: untouched
     entries[1]["g"] = torch.zeros_like(entries[1]["g"])  # zero direction: pure decay
-    gpu, status, _ = run_muon_gpu(entries, lr=0.1, precision="bf16")
+    gpu, status, _ = run_muon_gpu(entries, lr=0.1, precision=precision, route=r)
     assert status == 0
     assert torch.equal(gpu[0]["W"], entries[0]["w"]) and torch.equal(gpu[0]["B"], entries[0]["mom"])
     assert torch.count_nonzero(gpu[1]["U"]) == 0
-    want = (entries[1]["w"].double() * (1 - 0.1 * 0.1)).to(torch.bfloat16)
+    want = (entries[1]["w"].double() * (1 - 0.1 * 0.1)).to(entries[1]["w"].dtype)
     assert torch.equal(gpu[1]["W"], want)
     # a NaN gradient is reported in the status word
     bad = random_entries([(32, 32, None, None)], seed=15)
     bad[0]["g"][3, 4] = float("nan")
-    _, status, _ = run_muon_gpu(bad, lr=0.1, precision="bf16")
+    _, status, _ = run_muon_gpu(bad, lr=0.1, precision=precision, route=r)
     assert status & B.GBO_STATUS_NONFINITE
 
 
