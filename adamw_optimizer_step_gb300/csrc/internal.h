@@ -62,7 +62,8 @@ struct DevSub {
 //               A_{j+1} = P_j A_j P_j and Q_{j+1} = P_j Q_j are products of
 //               commuting symmetric matrices (upper triangle only), and the
 //               p x q product runs once, X_k = Q_k X_0.  Cheaper whenever
-//               q > p; used when every iteration has c == 0.
+//               q > p.  With c != 0, P_j = a I + b A_j + c A_j^2 takes one
+//               more symmetric product, the square of A_j.
 struct ShapeClass {
   int32_t p, q, ld, ldp;
   int32_t count;  // matrices in the class
@@ -176,8 +177,9 @@ int launch_ns_gemm_tf32(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &gl
 // q x p and the product runs transposed.
 double tc_executed_flops(int p, int q, bool square, bool tall);
 // FLOPs executed for one p x q matrix over k iterations on the Gram route:
-// the Gram, 3k - 3 symmetric p x p products, the product with X_0.
-double tc_gram_route_flops(int p, int q, int k, bool tall);
+// the Gram, 3k - 3 symmetric p x p products plus one square of A for each
+// of `squares` iterations with c != 0, the product with X_0.
+double tc_gram_route_flops(int p, int q, int k, int squares, bool tall);
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);

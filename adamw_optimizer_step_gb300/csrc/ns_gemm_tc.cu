@@ -505,8 +505,8 @@ double tc_executed_flops(int p, int q, bool square, bool tall) {
   return f + product_flops(p, q, tall);                           // product, K = p
 }
 
-double tc_gram_route_flops(int p, int q, int k, bool tall) {
-  return sym_items_of(p) * item_flops(p, q) + (3.0 * k - 3.0) * sym_items_of(p) * item_flops(p, p) +
+double tc_gram_route_flops(int p, int q, int k, int squares, bool tall) {
+  return sym_items_of(p) * item_flops(p, q) + (3.0 * k - 3.0 + squares) * sym_items_of(p) * item_flops(p, p) +
          product_flops(p, q, tall);
 }
 

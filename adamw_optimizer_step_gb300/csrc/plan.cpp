@@ -156,16 +156,24 @@ struct gbo_plan {
 
 namespace {
 
-// Route of a p x q class: the Gram route needs k >= 2 and c == 0 in every
-// iteration; AUTO takes it when it executes at least 10% fewer FLOPs (in
-// practice: whenever q is clearly above p).
+// Iterations whose polynomial has c != 0 (each costs a square of A).
+int squares(const gbo_plan *P) {
+  int n = 0;
+  for (int it = 0; it < P->opts.ns_steps; ++it) n += P->abc[3 * it + 2] != 0.f;
+  return n;
+}
+
+// Route of a p x q class: the Gram route needs k >= 2; AUTO takes it when it
+// executes at least 10% fewer FLOPs (in practice: whenever q is clearly
+// above p).
 int32_t choose_route(const gbo_plan *P, int p, int q, bool tall) {
   const int k = P->opts.ns_steps;
-  if (P->any_c || k < 2 || P->opts.route == GBO_ROUTE_X) return kRouteX;
+  if (k < 2 || P->opts.route == GBO_ROUTE_X) return kRouteX;
   if (P->opts.route == GBO_ROUTE_GRAM) return kRouteGram;
   const bool x_tall = P->x_dtype == GBO_BF16 && tall;
-  const double fx = k * tc_executed_flops(p, q, false, x_tall);
-  return tc_gram_route_flops(p, q, k, x_tall) < 0.9 * fx ? kRouteGram : kRouteX;
+  double fx = 0;
+  for (int it = 0; it < k; ++it) fx += tc_executed_flops(p, q, P->abc[3 * it + 2] != 0.f, x_tall);
+  return tc_gram_route_flops(p, q, k, squares(P), x_tall) < 0.9 * fx ? kRouteGram : kRouteX;
 }
 
 int validate_and_expand(gbo_plan *P) {
@@ -413,11 +421,11 @@ int validate_and_expand(gbo_plan *P) {
     double ex = 0;
     for (const ShapeClass &C : P->classes) {
       if (C.route == kRouteGram) {
-        ex += C.count * tc_gram_route_flops(C.p, C.q, o.ns_steps, C.tall != 0);
+        ex += C.count * tc_gram_route_flops(C.p, C.q, o.ns_steps, squares(P), C.x_tall != 0);
         I.n_gram_route += C.count;
       } else {
         for (int it = 0; it < o.ns_steps; ++it)
-          ex += C.count * tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f, C.tall != 0);
+          ex += C.count * tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f, C.x_tall != 0);
       }
     }
     I.ns_flops_executed = ex;
@@ -518,21 +526,32 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
         cur ^= 1;
       }
     } else {
-      // A_0 = alpha^2 X_0 X_0^T and P_0;  Q_1 = P_0
+      // A_0 = alpha^2 X_0 X_0^T and P_0;  Q_1 = P_0.  An iteration with c != 0
+      // writes A only and takes P = a I + b A + c A^2 from a square of A.
       size_t i = 0;
-      at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kGramK, 1, &P->abc[0], x[0], x[0], gP[0], gA));
+      if (P->abc[2] == 0.f) {
+        at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kGramK, 1, &P->abc[0], x[0], x[0], gP[0], gA));
+      } else {
+        at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramA, kGramK, 1, &P->abc[0], x[0], x[0], gA));
+        at(gs, i++, kPhaseSquare).jobs.push_back(job(&C, kSquare, kKindSym, 0, &P->abc[0], gA, gA, gP[0], nullptr, gA));
+      }
       for (int j = 0; j + 1 < k; ++j) {
         void *Pj = gP[j & 1];
         // T = P_j A_j and, from j = 1, Q_{j+1} = P_j Q_j
         TcStep &la = at(gs, i++, kPhaseProduct);
         la.jobs.push_back(job(&C, kGramA, kKindSym, 0, nullptr, Pj, gA, gT));
         if (j >= 1) la.jobs.push_back(job(&C, kGramA, kKindSym, 0, nullptr, Pj, j == 1 ? gP[0] : gQ[j & 1], gQ[(j + 1) & 1]));
-        // A_{j+1} = P_j T and P_{j+1} (A_{k-1} itself is not needed)
+        // A_{j+1} = P_j T and P_{j+1} (with c == 0, A_{k-1} itself is not needed)
         const float *abc = &P->abc[3 * (j + 1)];
-        if (j + 2 < k)
-          at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kKindSym, 0, abc, Pj, gT, gP[(j + 1) & 1], gA));
-        else
-          at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGram, kKindSym, 0, abc, Pj, gT, gP[(j + 1) & 1]));
+        void *Pn = gP[(j + 1) & 1];
+        if (abc[2] != 0.f) {
+          at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramA, kKindSym, 0, abc, Pj, gT, gA));
+          at(gs, i++, kPhaseSquare).jobs.push_back(job(&C, kSquare, kKindSym, 0, abc, gA, gA, Pn, nullptr, gA));
+        } else if (j + 2 < k) {
+          at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kKindSym, 0, abc, Pj, gT, Pn, gA));
+        } else {
+          at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGram, kKindSym, 0, abc, Pj, gT, Pn));
+        }
       }
       // Q_k = P_{k-1} Q_{k-1}, then X_k = Q_k X_0 (alpha folded in)
       at(gs, i++, kPhaseProduct)

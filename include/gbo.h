@@ -137,8 +137,8 @@ typedef struct {
  *         A_0 = X_0 X_0^T, so the iteration runs on p x p matrices only
  *         (A_{j+1} = P_j A_j P_j, Q_{j+1} = P_j Q_j) and the p x q product
  *         runs once: X_k = Q_k X_0.  Executes p^2 q + (3k - 3) p^3 + 2 p^2 q
- *         instead of about k (p^2 q + 2 p^2 q) FLOPs; allowed when every
- *         iteration has c == 0 and k >= 2.
+ *         instead of about k (p^2 q + 2 p^2 q) FLOPs (plus one p x p square
+ *         of A per iteration with c != 0, on both routes); needs k >= 2.
  *   AUTO  GRAM where it is allowed and executes fewer FLOPs (q > p), else X.
  * Both precisions run on the tensor cores: bf16 operands, or in the fp32
  * mode fp32 operands as three TF32 products (hi hi + hi lo + lo hi).

@@ -179,18 +179,24 @@ def test_flop_count_and_launches(L):
         assert i.ns_flops_executed == 3 * (gram + 12 * sym + prod)
         assert i.launches_per_step == 2 + 11
         L.gbo_muon_plan_destroy(plan)
-    # square matrices stay on the X route unless forced; c != 0 and k = 1
-    # never take the Gram route; the fp32 mode takes it as bf16 does
+    # square matrices stay on the X route unless forced; k = 1 never takes
+    # the Gram route; c != 0 (one square of A per iteration) and the fp32
+    # mode take it as the cubic in bf16 does
     rc, plan = create(L, [desc(0, 256, 256)])
     assert info(L, plan).n_gram_route == 0
     L.gbo_muon_plan_destroy(plan)
     rc, plan = create(L, [desc(0, 256, 256)], route=B.GBO_ROUTE_GRAM)
     assert info(L, plan).n_gram_route == 1
     L.gbo_muon_plan_destroy(plan)
-    for kw in (dict(abc=(15 / 8, -5 / 4, 3 / 8)), dict(ns_steps=1)):
-        rc, plan = create(L, descs(), route=B.GBO_ROUTE_GRAM, **kw)
-        assert rc == 0 and info(L, plan).n_gram_route == 0
-        L.gbo_muon_plan_destroy(plan)
+    rc, plan = create(L, descs(), route=B.GBO_ROUTE_GRAM, ns_steps=1)
+    assert rc == 0 and info(L, plan).n_gram_route == 0
+    L.gbo_muon_plan_destroy(plan)
+    rc, plan = create(L, descs(), abc=(15 / 8, -5 / 4, 3 / 8))
+    i = info(L, plan)
+    # Gram (+ square), then per iteration T / Q, A and a square: 1 + 1 + 4 x 3 + Q_5 + X_5
+    assert i.n_gram_route == 3 and i.launches_per_step == 2 + 16
+    assert i.ns_flops_executed == 3 * (gram + (12 + 5) * sym + prod)
+    L.gbo_muon_plan_destroy(plan)
     rc, plan = create(L, descs(), precision=B.GBO_NS_F32)
     assert rc == 0 and info(L, plan).n_gram_route == 3 and info(L, plan).launches_per_step == 2 + 11
     L.gbo_muon_plan_destroy(plan)

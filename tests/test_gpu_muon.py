@@ -127,6 +127,24 @@ def test_normuon_rms_target(precision):
             assert abs(np.sqrt(np.mean(blk * blk)) / 0.2 - 1.0) < 1e-3
 
 
+@pytest.mark.parametrize("precision", ["bf16", "f32"])
+@pytest.mark.parametrize("route", ["x", "gram"])
+@pytest.mark.parametrize("abc", ["quintic", "schedule"])
+def test_routes_with_square(route, precision, abc):
+    """Iterations with c != 0 (P = a I + b A + c A^2, one square of A) on
+    both routes: the textbook quintic triple, and a per-step schedule that
+    mixes c == 0 and c != 0 iterations."""
+    coeffs = QUINTIC if abc == "quintic" else CUBIC + QUINTIC + (2.0, -1.5, 0.5) + CUBIC + (1.2, -0.3, 0.1)
+    entries = random_entries(RAGGED, seed=24, b_std=1e-3)
+    r = B.GBO_ROUTE_X if route == "x" else B.GBO_ROUTE_GRAM
+    gpu, status, plan = run_muon_gpu(entries, lr=0.02, precision=precision, abc=coeffs, route=r)
+    info = B.gbo_muon_plan_info(plan)
+    assert info["n_gram_route"] == (0 if route == "x" else info["n_matrices"])
+    ora = run_muon_oracle(entries, lr=0.02, abc=coeffs)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=0.02, precision=precision)
+
+
 @pytest.mark.parametrize("ns_steps", [3, 5])
 def test_normuon_gram_route(ns_steps):
     """NorMuon rows read the last iterate from the buffer each route leaves
