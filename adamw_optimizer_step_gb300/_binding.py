@@ -63,7 +63,7 @@ class AdamWDesc(ctypes.Structure):
 
 class AdamWOpts(ctypes.Structure):
     _fields_ = [("lr", c_float), ("beta1", c_float), ("beta2", c_float), ("eps", c_float),
-                ("weight_decay", c_float), ("step", c_int32)]
+                ("weight_decay", c_float), ("step", c_int32), ("dev_step", c_void_p)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -331,8 +331,10 @@ def gbo_clip_norm_noalloc(grads, max_norm, total_norm, coef, dev_status=None, st
 
 
 def gbo_adamw_step(params, *, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0, step=1,
-                   coef=None, dev_status=None, stream=None):
-    """AdamW on ``params``: a list of (p, g, m, v) tensors (p, m, v float32)."""
+                   coef=None, dev_status=None, stream=None, dev_step=None):
+    """AdamW on ``params``: a list of (p, g, m, v) tensors (p, m, v float32).
+    ``dev_step``: an int32 CUDA tensor holding t, read when the kernel runs
+    (for CUDA graph replay), instead of the host ``step``."""
     arr = (AdamWDesc * max(1, len(params)))()
     for d, (p, g, m, v) in zip(arr, params):
         for t, nm in ((p, "p"), (m, "m"), (v, "v")):
@@ -341,7 +343,9 @@ def gbo_adamw_step(params, *, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=
         d.p, d.g, d.m, d.v = (_dev_ptr(p, "p"), _dev_ptr(g, "g"), _dev_ptr(m, "m"), _dev_ptr(v, "v"))
         d.numel = p.numel()
         d.g_dtype = _dtype(g)
-    opts = AdamWOpts(lr, beta1, beta2, eps, weight_decay, int(step))
+    if dev_step is not None and dev_step.dtype != torch.int32:
+        raise TypeError("dev_step must be int32")
+    opts = AdamWOpts(lr, beta1, beta2, eps, weight_decay, int(step), _dev_ptr(dev_step, "dev_step"))
     _check(lib().gbo_adamw_step(arr, len(params), ctypes.byref(opts), _dev_ptr(coef, "coef"),
                                 _dev_ptr(dev_status, "dev_status"), _stream(stream)))
 

@@ -138,9 +138,23 @@ __device__ __forceinline__ void adam_elem(float &p, float g, float &m, float &v,
 #define GBO_ADAM_MIN_BLOCKS 1  // compiler choice (58 regs, 4 blocks/SM): measured faster than forcing 5 or 6
 #endif
 __global__ void __launch_bounds__(kThreads, GBO_ADAM_MIN_BLOCKS)
-adamw_kernel(const __grid_constant__ AdamTable T, const __grid_constant__ AdamScalars s,
-             const float *__restrict__ coef_ptr) {
+adamw_kernel(const __grid_constant__ AdamTable T, const __grid_constant__ AdamScalars s0,
+             const float *__restrict__ coef_ptr, const int32_t *__restrict__ dev_step) {
   const float coef = coef_ptr ? __ldg(coef_ptr) : 1.0f;
+  // the bias corrections, from a device step count when one is given
+  // (computed as on the host, in double, once per block)
+  __shared__ float bc[2];
+  AdamScalars s = s0;
+  if (dev_step) {
+    if (threadIdx.x == 0) {
+      const double t = (double)*dev_step;
+      bc[0] = (float)((double)s.lr / (1.0 - pow((double)s.beta1, t)));
+      bc[1] = (float)(1.0 / sqrt(1.0 - pow((double)s.beta2, t)));
+    }
+    __syncthreads();
+    s.step_size = bc[0];
+    s.inv_sqrt_bc2 = bc[1];
+  }
   const int64_t n_chunks = T.chunk0[T.n];
   for (int64_t ch = blockIdx.x; ch < n_chunks; ch += gridDim.x) {
     const int ti = find_owner(ch, T.n, [&](int k) { return T.chunk0[k]; });
@@ -237,10 +251,12 @@ int launch_adamw(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *o
   s.beta2 = opts->beta2;
   s.eps = opts->eps;
   s.wd = opts->weight_decay;
-  const double bc1 = 1.0 - std::pow((double)opts->beta1, (double)opts->step);
-  const double bc2 = 1.0 - std::pow((double)opts->beta2, (double)opts->step);
-  s.step_size = (float)((double)opts->lr / bc1);
-  s.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  if (!opts->dev_step) {
+    const double bc1 = 1.0 - std::pow((double)opts->beta1, (double)opts->step);
+    const double bc2 = 1.0 - std::pow((double)opts->beta2, (double)opts->step);
+    s.step_size = (float)((double)opts->lr / bc1);
+    s.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  }
   for (int l = 0; l * kMaxTensors < n; ++l) {
     AdamTable T{};
     T.n = min(kMaxTensors, n - l * kMaxTensors);
@@ -260,7 +276,7 @@ int launch_adamw(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *o
     const int64_t chunks = T.chunk0[T.n];
     if (chunks == 0) continue;
     const unsigned grid = (unsigned)std::min<int64_t>(chunks, (int64_t)sm_count * 8);
-    adamw_kernel<<<grid, kThreads, 0, st>>>(T, s, coef);
+    adamw_kernel<<<grid, kThreads, 0, st>>>(T, s, coef, opts->dev_step);
     count_launches(1);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return (int)err;

@@ -877,7 +877,8 @@ int gbo_clip_norm(const gbo_tensor *grads, int32_t n, float max_norm, float *dev
 int gbo_adamw_step(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *opts,
                    const float *dev_coef, int32_t *dev_status, gbo_stream_t stream) {
   if (n < 0 || (n > 0 && !descs) || !opts) return fail(GBO_ERR_INVALID_ARG, "bad argument");
-  if (opts->step < 1) return fail(GBO_ERR_INVALID_ARG, "step must be >= 1");
+  if (!opts->dev_step && opts->step < 1) return fail(GBO_ERR_INVALID_ARG, "step must be >= 1");
+  if (!aligned(opts->dev_step, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_step misaligned");
   if (!(opts->beta1 >= 0.f && opts->beta1 < 1.f) || !(opts->beta2 >= 0.f && opts->beta2 < 1.f))
     return fail(GBO_ERR_INVALID_ARG, "betas must be in [0, 1)");
   if (!std::isfinite(opts->lr) || !std::isfinite(opts->eps) || !std::isfinite(opts->weight_decay))

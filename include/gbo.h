@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define GBO_ABI_VERSION 3
+#define GBO_ABI_VERSION 4
 
 /* ---- status codes (return values) ------------------------------------ */
 #define GBO_OK 0
@@ -289,6 +289,10 @@ typedef struct {
   float eps;
   float weight_decay;
   int32_t step; /* t >= 1: the step being taken, for bias correction */
+  /* NULL, or a device int32 holding t >= 1, read when the kernel runs (then
+   * `step` is ignored): a launch captured in a CUDA graph then replays with
+   * the current count, which the caller advances on the device. */
+  const int32_t *dev_step;
 } gbo_adamw_opts;
 
 /*

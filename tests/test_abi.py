@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(L):
     assert "gbo_muon_step" in names and "gbo_adamw_step" in names
     for n in names:
         assert hasattr(L, n), n
-    assert B.gbo_abi_version() == 3
+    assert B.gbo_abi_version() == 4
     for i, S in enumerate(B._STRUCTS):
         assert B.gbo_struct_size(i) == ctypes.sizeof(S)
 

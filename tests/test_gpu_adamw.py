@@ -148,3 +148,36 @@ def test_omn_adamw_full_size():
         sub = [x.reshape(-1)[idx] for x in (p, g, m, v)]
         got = [x.reshape(-1)[idx.cuda()].cpu() for x in (pd, md, vd)]
         check([tuple(sub)], [(got[0], None, got[1], got[2])], lr=3e-4, t=5, coef=c)
+
+
+def test_device_step_in_cuda_graph():
+    """With the step count on the device, clip + AdamW captured once in a
+    CUDA graph (with the count's increment) replays steps t = 2, 3, 4 as
+    direct launches with the host count give them."""
+    params = tiny_params("random")
+    devs = [[tuple(x.cuda().clone() for x in p) for p in params] for _ in range(2)]
+    ws = [torch.empty(B.gbo_clip_norm_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    tot = [torch.zeros(1, device="cuda") for _ in range(2)]
+    coef = [torch.zeros(1, device="cuda") for _ in range(2)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step(k, **kw):
+        B.gbo_clip_norm([d[1] for d in devs[k]], 1.0, tot[k], coef[k], ws[k], dev_status=status)
+        B.gbo_adamw_step(devs[k], lr=3e-4, coef=coef[k], dev_status=status, **kw)
+
+    for t in (1, 2, 3, 4):  # direct, host step count
+        step(0, step=t)
+    t_dev = torch.ones(1, dtype=torch.int32, device="cuda")
+    step(1, dev_step=t_dev)  # t = 1, direct
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        t_dev.add_(1)
+        step(1, dev_step=t_dev)
+    for _ in range(3):  # t = 2, 3, 4
+        graph.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and int(t_dev.item()) == 4
+    for a, b in zip(devs[0], devs[1]):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
