@@ -157,11 +157,17 @@ class HybridOptimizer:
     ``precision`` "bf16" or "f32" (three TF32 products); ``route`` "auto",
     "x" or "gram" (see gbo_muon_opts); ``rms_target`` > 0 with NorMuon
     scales each matrix's update to that RMS.
+
+    ``graph=True``: the first step (and the first after the parameter or
+    gradient tensors change) runs directly, then one step is captured in a
+    CUDA graph, with the AdamW step count kept on the device, and later
+    steps replay it.  The learning rates are fixed at capture.
     """
 
     def __init__(self, model, *, muon_lr=0.01, adamw_lr=3e-4, weight_decay=0.0, auxiliary_decay=True, mu=0.95,
                  ns_steps=5, abc=(1.5, -0.5, 0.0), normuon=False, beta2_rows=0.95, eps_rows=1e-8,
-                 rms_target=0.0, betas=(0.9, 0.95), eps=1e-8, max_norm=1.0, precision="bf16", route="auto"):
+                 rms_target=0.0, betas=(0.9, 0.95), eps=1e-8, max_norm=1.0, precision="bf16", route="auto",
+                 graph=False):
         from . import _binding as B
         self.B = B
         self.routes = build_parameter_groups(model, weight_decay, auxiliary_decay)
@@ -195,6 +201,10 @@ class HybridOptimizer:
         self.coef = torch.zeros(1, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self._cws = torch.empty(B.gbo_clip_norm_workspace_bytes(), dtype=torch.uint8, device=dev)
+        self.graph = graph
+        self._graph = None      # torch.cuda.CUDAGraph of one step, or None
+        self._graph_key = None  # the tensors it was captured with
+        self._step_t = torch.zeros(1, dtype=torch.int32, device=dev)  # AdamW t on the device
 
     def _muon_entries(self):
         out = []
@@ -220,13 +230,10 @@ class HybridOptimizer:
         self._ensure_plan()
         return self.B.gbo_desc_hash(self._plan)
 
-    @torch.no_grad()
-    def step(self):
-        """One hybrid step; returns the pre-clip AdamW gradient norm (a device
-        tensor) and leaves the device status word in ``self.status``."""
-        self.step_count += 1
+    def _launch(self, dev_step=None):
+        """Enqueue one step on the current stream: the host step count, or
+        with ``dev_step`` the device one."""
         if self.muon:
-            self._ensure_plan()
             self.B.gbo_muon_step(self._plan, self.muon_lr, self._ws, dev_status=self.status)
         active = [r for r in self.adamw if r.param.grad is not None]
         if active:
@@ -237,7 +244,35 @@ class HybridOptimizer:
                           for r in active if r.weight_decay == wd]
                 self.B.gbo_adamw_step(params, lr=self.adamw_lr, beta1=self.betas[0], beta2=self.betas[1],
                                       eps=self.eps, weight_decay=wd, step=self.step_count, coef=self.coef,
-                                      dev_status=self.status)
+                                      dev_status=self.status, dev_step=dev_step)
+
+    def _tensor_key(self):
+        return tuple((r.param.data_ptr(), None if r.param.grad is None else r.param.grad.data_ptr())
+                     for r in self.routes)
+
+    @torch.no_grad()
+    def step(self):
+        """One hybrid step; returns the pre-clip AdamW gradient norm (a device
+        tensor) and leaves the device status word in ``self.status``."""
+        self.step_count += 1
+        if self.muon:
+            self._ensure_plan()
+        if not self.graph:
+            self._launch()
+            return self.total_norm
+        key = self._tensor_key()
+        if self._graph is not None and key == self._graph_key:
+            self._graph.replay()  # advances the device count, then the step
+            return self.total_norm
+        # direct step (sets the plan up on the device), then capture the next
+        self._step_t.fill_(self.step_count)
+        self._launch(dev_step=self._step_t)
+        torch.cuda.synchronize()
+        self._graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self._graph):
+            self._step_t.add_(1)
+            self._launch(dev_step=self._step_t)
+        self._graph_key = key
         return self.total_norm
 
     def state_dict(self):
@@ -248,6 +283,7 @@ class HybridOptimizer:
         if self.muon and sd["layout_hash"] != self.layout_hash():
             raise ValueError("checkpoint was written for a different Muon layout (views, splits or shapes)")
         self.step_count = int(sd["step"])
+        self._graph = None  # a captured step holds the old count
         for k, v in sd["state"].items():
             for n, t in v.items():
                 self.state[k][n].copy_(t)

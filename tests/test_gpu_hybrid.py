@@ -89,3 +89,30 @@ def test_hybrid_state_round_trip():
     opt_c = HybridOptimizer(c)
     with pytest.raises(ValueError):
         opt_c.load_state_dict(sd)
+
+
+def test_graph_mode_matches_direct_steps():
+    """graph=True (a direct first step, then replays of one captured step with
+    the AdamW count on the device) gives bitwise the parameters and states
+    of direct steps, in both precisions."""
+    from adamw_optimizer_step_gb300.routing import HybridOptimizer
+    for precision in ("bf16", "f32"):
+        a = make_model(3)
+        b = copy.deepcopy(a)
+        for pa, pb in zip(a.parameters(), b.parameters()):
+            if pa.grad is not None:
+                pb.grad = pa.grad.clone()
+        kw = dict(muon_lr=0.02, adamw_lr=1e-3, weight_decay=0.1, precision=precision)
+        oa = HybridOptimizer(a, **kw)
+        ob = HybridOptimizer(b, graph=True, **kw)
+        for _ in range(4):
+            oa.step()
+            ob.step()
+        torch.cuda.synchronize()
+        assert ob._graph is not None and int(ob._step_t.item()) == 4
+        assert int(oa.status.item()) == 0 and int(ob.status.item()) == 0
+        for (na, pa), (nb, pb) in zip(a.named_parameters(), b.named_parameters()):
+            assert torch.equal(pa, pb), na
+        for k in oa.state:
+            for n in oa.state[k]:
+                assert torch.equal(oa.state[k][n], ob.state[k][n]), (k, n)
