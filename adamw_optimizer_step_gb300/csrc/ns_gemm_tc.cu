@@ -9,7 +9,7 @@
 // onto X whose last instance writes the weights.  Matrices of one oriented
 // shape are stored back to back, so one 3-D tensor map (columns, rows,
 // matrix) covers a whole shape class; out-of-range rows and columns of a
-// tile are zero-filled by TMA and masked in the epilogue.  Each shape class
+// tile are zero-filled by TMA loads and dropped by TMA stores.  Each shape class
 // of a launch is a job with its own operands, output and epilogue, so one
 // launch may run X-route and Gram-route steps (see internal.h) side by side.
 //
@@ -17,8 +17,10 @@
 //   warp 0      TMA producer (one lane), STAGES-deep ring of A/B tiles
 //   warp 1      TMEM owner and MMA issuer (one lane)
 //   warps 2..5  epilogue, one per TMEM lane quarter: TMEM -> registers ->
-//               a 64-byte-swizzled staging slot -> TMA store (the weight
-//               write of the last product goes registers -> global)
+//               a 64-byte-swizzled staging slot -> TMA store; the last
+//               product reads the weights into registers and stores full
+//               32-row blocks of bf16 weights the same way, through a map
+//               of the weight
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the
 // epilogue of one tile overlaps the MMAs of the next.  Every wait is
 // bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT, waits (bounded)
