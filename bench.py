@@ -221,15 +221,24 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # ours
 
-def traffic_record(kernel_file):
+# the sources of ns_gemm_tc_kernel, whose DRAM traffic profiles/traffic.json records
+TC_KERNEL_SOURCES = ["ns_gemm_tc.cu", "tc_common.cuh"]
+
+
+def traffic_record(kernel_files):
     """DRAM bytes per unit from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    kernel's sources changed since the counters were taken (sha256 over the
+    listed files, concatenated in order)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
-    src = open(os.path.join(ROOT, "adamw_optimizer_step_gb300", "csrc", kernel_file), "rb").read()
-    if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+    if rec.get("source_files") != list(kernel_files):
+        return None
+    h = hashlib.sha256()
+    for f in kernel_files:
+        h.update(open(os.path.join(ROOT, "adamw_optimizer_step_gb300", "csrc", f), "rb").read())
+    if rec.get("source_sha256") != h.hexdigest():
         return None
     return rec
 
@@ -448,7 +457,7 @@ def run_ours(args):
     if f32:  # TF32 runs at the nominal 1.1 / 2.25 of the bf16 dense rate
         peak_tf *= 1.1 / 2.25
         peak_src += " x nominal TF32/bf16 ratio 1.1/2.25"
-    tr = traffic_record("ns_gemm_tc.cu") if not f32 else None
+    tr = traffic_record(TC_KERNEL_SOURCES) if not f32 else None
     traffic = None
     if tr is not None:
         traffic = tr["bytes_per_unit"] * (flops / gemm_launches) / tr["unit_flops"]
