@@ -17,10 +17,11 @@
 //   warp 0      TMA producer (one lane), STAGES-deep ring of A/B tiles
 //   warp 1      TMEM owner and MMA issuer (one lane)
 //   warps 2..5  epilogue, one per TMEM lane quarter: TMEM -> registers ->
-//               a 64-byte-swizzled staging slot -> TMA store; the last
-//               product reads the weights into registers and stores full
-//               32-row blocks of bf16 weights the same way, through a map
-//               of the weight
+//               a 64-byte-swizzled staging slot -> TMA store; in the last
+//               product, full 32-row blocks of bf16 weights are loaded by
+//               TMA into the staging area three 32 x 32 blocks ahead,
+//               updated in place and stored by TMA, through a map of the
+//               weight
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the
 // epilogue of one tile overlaps the MMAs of the next.  Every wait is
 // bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT, waits (bounded)
@@ -73,8 +74,9 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 // Per epilogue warp: two store slots (kSlotBytes each, tc_common.cuh).
 constexpr int kWarpStageBytes = 2 * kSlotBytes;
 constexpr int kStageBytes = kEpiWarps * kWarpStageBytes;
-constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + kStageBytes + 256 /*barriers*/;
+constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + kStageBytes + 512 /*barriers*/;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kWBufs * kWBufBytes <= kWarpStageBytes, "weight buffers fit a warp's staging area");
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
 // each K-major or MN-major, N = 256, M = 128 (one CTA) or 256 (pair).
 __host__ __device__ constexpr uint32_t make_idesc(int a_mn_major, int b_mn_major, int m) {
@@ -273,14 +275,15 @@ template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ PhaseArgs A) {
   constexpr int STAGES = Mode<kPair>::kStages;
-  constexpr int STAGE_BYTES = Mode<kPair>::kStageBytes;
   constexpr int kRows = Mode<kPair>::kRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes + kStageBytes);
-  // bars: full[STAGES], empty[STAGES], accf[2], acce[2], drain
+  // bars: full[STAGES], empty[STAGES], accf[2], acce[2], drain, (TMEM
+  // address, abort flag), then kWBufs weight-load barriers per epilogue warp
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
+  uint64_t *wbars = bars + 2 * STAGES + 6;
   uint8_t *stage_base = smem + kRingBytes;  // epilogue staging, 1024-byte aligned
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
@@ -307,6 +310,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       mbar_init(acce0 + 8 * a, (kPair ? 2 : 1) * kEpiWarps);
     }
     mbar_init(drain, 1);
+    for (int b = 0; b < kEpiWarps * kWBufs; ++b) mbar_init(smem_u32(wbars + b), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -404,6 +408,8 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     // epilogue warps: TMEM lane quarter = warp % 4
     const int quarter = warp & 3;
     const uint32_t stage = smem_u32(stage_base + (warp - 2) * kWarpStageBytes);
+    const uint32_t wbar0 = smem_u32(wbars + (warp - 2) * kWBufs);
+    uint32_t wpar = 0, winfl = 0;  // weight-load barriers: next parities, loads in flight
     int slot = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -415,15 +421,27 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
       // the job's output is rows x cols (stored orientation for the weights)
       const int rows = kind_rows(J.kind, S.p, S.q), cols = kind_cols(J.kind, S.p, S.q);
-      if (J.mode == kFinal) prefetch_weight_tile(S, i0, tc.tn * BN, rows, cols, lane);
+      // bf16 weights in blocks of 32 whole rows with a TMA map move by TMA
+      // (their first loads overlap this tile's MMAs); the rest are
+      // prefetched into L2 and read by the epilogue threads
+      const CUtensorMap *wmap = (J.mode == kFinal && S.w_dtype == GBO_BF16 && S.wmap >= 0)
+                                    ? static_cast<const CUtensorMap *>(A.wmaps) + S.wmap
+                                    : nullptr;
+      const bool wtma = wmap != nullptr && i0 + 32 <= rows;
+      if (wtma) weight_loads_begin(wmap, stage, wbar0, tc.tn * BN, cols, (int)(S.r0 + i0), lane, winfl);
+      else if (J.mode == kFinal) prefetch_weight_tile(S, i0, tc.tn * BN, rows, cols, lane);
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
       tc_fence_after();
       const float s = J.first ? A.alpha[sub] : 1.0f;
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (i0 < rows) {  // warps whose rows are all padding have nothing to write
-        if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
-          const CUtensorMap *wmap = S.wmap >= 0 ? static_cast<const CUtensorMap *>(A.wmaps) + S.wmap : nullptr;
-          final_tile_bf16(A, S, s, i0, tc.tn * BN, rows, cols, trow, lane, wmap, stage, &slot);
+        if (wtma) {
+          if (!final_tile_bf16_tma(A, S, s, i0, tc.tn * BN, cols, trow, lane, wmap, stage, wbar0, wpar, winfl)) {
+            give_up();
+            break;
+          }
+        } else if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
+          final_tile_bf16(A, S, s, i0, tc.tn * BN, rows, cols, trow, lane);
         } else {
 #pragma unroll 1
           for (int ch = 0; ch < BN / 32; ++ch) {
@@ -443,7 +461,10 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       }
       if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
-    // this warp's TMA stores have landed before the kernel ends
+    // weight loads of an abandoned tile land, and this warp's TMA stores
+    // complete, before the kernel ends
+    for (int b = 0; b < kWBufs; ++b)
+      if (winfl >> b & 1u) (void)mbar_wait(wbar0 + 8 * b, (wpar >> b) & 1u);
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }

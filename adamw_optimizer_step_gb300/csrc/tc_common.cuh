@@ -462,22 +462,14 @@ __device__ __forceinline__ void wseg_unpack(const WSeg &r, float (&o)[32]) {
   }
 }
 
-// The last product's epilogue of one warp for one tile when W is bf16.  The
-// output is in stored orientation (rows x cols of the matrix); lane r owns
-// stored row r0 + i0 + r.  The weights of chunk ch + 1 are loaded before
-// chunk ch is computed, so a load of each lane's row segment is always in
-// flight instead of the warp waiting on every chunk's loads in turn.
-//
-// With `wmap` (a TMA map over the whole weight, 32 x 32 boxes, 64-byte
-// swizzle) and a block of 32 whole rows, the new weights leave through the
-// warp's staging slots and TMA stores; a block that would reach past the
-// matrix's rows (into another matrix of the same weight) keeps the masked
-// stores.
+// The last product's epilogue of one warp for one tile when W is bf16 and
+// no TMA map covers the block (rows past the end of the matrix, or weight
+// rows that do not start on 16-byte boundaries).  The output is in stored
+// orientation (rows x cols of the matrix); lane r owns stored row
+// r0 + i0 + r.  The weights of chunk ch + 1 are loaded before chunk ch is
+// computed, so a load of each lane's row segment is always in flight.
 __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub &S, float s, int i0, int tile_col0,
-                                                int rows, int cols, uint32_t trow, int lane,
-                                                const CUtensorMap *wmap = nullptr, uint32_t stage = 0,
-                                                int *slot = nullptr) {
-  const bool tma = wmap != nullptr && i0 + 32 <= rows;  // the same for every lane
+                                                int rows, int cols, uint32_t trow, int lane) {
   const int nch = min(BN / 32, (cols - tile_col0 + 31) / 32);  // chunks holding columns < cols
   const float lr = A.lr * S.lr_mult, su = S.scale * s;
   __nv_bfloat16 *W = reinterpret_cast<__nv_bfloat16 *>(S.w);
@@ -507,14 +499,116 @@ __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub
         u[k] *= su;
         w[k] = w[k] - lr * (S.wd * w[k] + u[k]);
       }
-      if (tma) tma_store_block(wmap, stage, *slot, w, false, col0, (int)(S.r0 + i0), 0, lane);
-      else store_row32(W + wrow + col0, w, S.w_vec && mask == 0xffffffffu, mask);
+      store_row32(W + wrow + col0, w, S.w_vec && mask == 0xffffffffu, mask);
       if (A.dbg) {
         float *d = A.dbg + S.dbg_off + wrow + col0;
         store_row32(d, u, mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0, mask);
       }
     }
   }
+}
+
+// The same epilogue for a block of 32 whole rows of a bf16 weight with a TMA
+// map (`wmap`: the whole weight, 32 x 32 boxes, 64-byte swizzle): the weights
+// travel by TMA both ways.  Column chunk c (a 32 x 32 block) is loaded into
+// buffer c % kWBufs of the warp's staging area, updated in place and stored
+// from there.  Loads run kWAhead chunks ahead of the chunk being updated;
+// the first kWAhead are issued before the accumulator is ready
+// (weight_loads_begin).  Each buffer has an mbarrier (wbar0 + 8 b); wpar
+// holds the parity each waits for next (bit b) and winfl the buffers with a
+// load in flight (bit b).  The warp's state is uniform across its lanes.
+constexpr int kWBufs = 4, kWAhead = 3, kWBufBytes = 2048;
+
+__device__ __forceinline__ void weight_load_chunk(const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0, int c,
+                                                  int col0, int row0) {
+  const uint32_t b = (uint32_t)(c & (kWBufs - 1));
+  mbar_expect_tx(wbar0 + 8 * b, kWBufBytes);
+  tma_load_3d(stage + b * kWBufBytes, wmap, wbar0 + 8 * b, col0, row0, 0);
+}
+
+__device__ __forceinline__ int weight_chunks(int tile_col0, int cols) {
+  return min(BN / 32, (cols - tile_col0 + 31) / 32);
+}
+
+__device__ __forceinline__ void weight_loads_begin(const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
+                                                   int tile_col0, int cols, int row0, int lane, uint32_t &winfl) {
+  const int n0 = min(kWAhead, weight_chunks(tile_col0, cols));
+  if (lane == 0) {
+    bulk_wait_read<0>();  // earlier stores from the staging area have read it
+    for (int c = 0; c < n0; ++c) weight_load_chunk(wmap, stage, wbar0, c, tile_col0 + 32 * c, row0);
+  }
+  __syncwarp();
+  winfl |= (1u << n0) - 1u;
+}
+
+// Lane r reads bf16 row r of a 32 x 32 block in the 64-byte swizzle layout.
+__device__ __forceinline__ void stage_read_row(uint32_t src, float (&o)[32], int lane) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(src + sw64(lane, q))
+                 : "memory");
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
+      o[8 * q + 2 * h] = __low2float(b);
+      o[8 * q + 2 * h + 1] = __high2float(b);
+    }
+  }
+}
+
+// Returns false on a time-out of a load wait.
+__device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const DevSub &S, float s, int i0,
+                                                    int tile_col0, int cols, uint32_t trow, int lane,
+                                                    const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
+                                                    uint32_t &wpar, uint32_t &winfl) {
+  const int nch = weight_chunks(tile_col0, cols);
+  const float lr = A.lr * S.lr_mult, su = S.scale * s;
+  const int row0 = (int)(S.r0 + i0);
+  const int64_t wrow = (S.r0 + i0 + lane) * S.cols;
+#pragma unroll 1
+  for (int ch = 0; ch < nch; ++ch) {
+    const uint32_t b = (uint32_t)(ch & (kWBufs - 1));
+    const uint32_t buf = stage + b * kWBufBytes;
+    const int col0 = tile_col0 + ch * 32;
+    float u[32];
+    tmem_ld32(trow + ch * 32, u);
+    if (!mbar_wait(wbar0 + 8 * b, (wpar >> b) & 1u)) return false;
+    wpar ^= 1u << b;
+    winfl &= ~(1u << b);
+    float w[32];
+    stage_read_row(buf, w, lane);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      u[k] *= su;
+      w[k] = w[k] - lr * (S.wd * w[k] + u[k]);
+    }
+    stage_rows(buf, w, lane);
+    fence_async_smem();
+    __syncwarp();
+    const bool more = ch + kWAhead < nch;
+    if (lane == 0) {
+      tma_store_3d(wmap, buf, col0, row0, 0);
+      bulk_commit();
+      if (more) {
+        // the buffer of chunk ch + kWAhead was last stored from by chunk
+        // ch - 1: at most this chunk's store may still read the staging area
+        bulk_wait_read<1>();
+        weight_load_chunk(wmap, stage, wbar0, ch + kWAhead, col0 + 32 * kWAhead, row0);
+      }
+    }
+    if (more) winfl |= 1u << ((ch + kWAhead) & (kWBufs - 1));
+    if (A.dbg) {
+      const uint32_t mask = prefix_mask(cols - col0);
+      float *d = A.dbg + S.dbg_off + wrow + col0;
+      store_row32(d, u, mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0, mask);
+    }
+  }
+  if (lane == 0) bulk_wait_read<0>();  // the staging area is free for the other epilogues
+  __syncwarp();
+  return true;
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *p) {
