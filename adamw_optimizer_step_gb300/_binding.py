@@ -107,6 +107,7 @@ def lib():
         "gbo_adamw_step": (c_int32, [ctypes.POINTER(AdamWDesc), c_int32, ctypes.POINTER(AdamWOpts), c_void_p,
                                      c_void_p, c_void_p]),
         "gbo_testing_wait_timeout": (c_int32, [c_void_p, ctypes.c_uint32, c_void_p]),
+        "gbo_testing_set_small_chain": (c_int32, [c_int32]),
         "gbo_last_error": (ctypes.c_char_p, []),
         "gbo_abi_version": (c_int32, []),
         "gbo_struct_size": (c_size_t, [c_int32]),
@@ -363,6 +364,13 @@ def gbo_abi_version():
 
 def gbo_struct_size(which):
     return int(lib().gbo_struct_size(which))
+
+
+def gbo_testing_set_small_chain(enable):
+    """Whether plans created from now on run the Gram route's p x p
+    iterations of matrices with p <= 128 (bf16) in one on-chip chain launch.
+    Returns the previous setting."""
+    return bool(lib().gbo_testing_set_small_chain(1 if enable else 0))
 
 
 def gbo_testing_wait_timeout(dev_status, limit_us, stream=None):

@@ -88,6 +88,7 @@ enum GemmMode : int32_t {
   kProduct = 3,   // C = P X;    write X' = s C
   kFinal = 4,     // C = P X;    O = s C; update the weight (+ dbg)
   kGramAP = 5,    // C symmetric; write A = s^2 C and P = a I + b A
+  kChain = 6,     // the Gram route's p x p chain on chip (p <= 128): A_0, P_0 -> Q_k
 };
 
 // Operand shapes of one tensor-core GEMM job.  X is p x q ("wide") or, for
@@ -127,6 +128,8 @@ struct GemmJob {
   const void *opA, *opB;
   void *out, *out2;  // out: P, A, T, Q or X'; out2: A of kGramAP
   const void *aux;   // kSquare: the A matrix read by the epilogue
+  int32_t steps;     // kChain: iterations k and their coefficients (3 per iteration)
+  const float *abc;
 };
 
 // Per-step arguments every Newton-Schulz launch shares (the per-class work
@@ -171,6 +174,13 @@ int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &glob
                       void *stream, int64_t *n_launch);
 int launch_ns_gemm_tf32(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
                         void *stream, int64_t *n_launch);
+// kChain jobs (bf16, p <= 128): opA = P_0, opB = A_0, out = Q_k regions;
+// every job of one call has the same steps and abc.
+int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
+                       void *stream, int64_t *n_launch);
+// FLOPs the chain kernel executes for one p x p matrix (p <= 128) over k
+// iterations with coefficients abc: 128 x 128 (or x 256) tiles, K padded to 64.
+double tc_chain_flops(int p, int k, const float *abc);
 // FLOPs the tensor-core kernel executes for one p x q matrix and one
 // iteration (Gram over the upper block-triangle of tiles, square when c != 0,
 // product), counting the zero padding of partial tiles; `tall`: X is held
@@ -180,6 +190,9 @@ double tc_executed_flops(int p, int q, bool square, bool tall);
 // the Gram, 3k - 3 symmetric p x p products plus one square of A for each
 // of `squares` iterations with c != 0, the product with X_0.
 double tc_gram_route_flops(int p, int q, int k, int squares, bool tall);
+// The same when the p x p chain runs on chip: the Gram (and the square of
+// A_0 when c_0 != 0), the chain, the product with X_0.
+double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall);
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);

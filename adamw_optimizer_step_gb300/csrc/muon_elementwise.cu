@@ -270,7 +270,9 @@ __device__ __forceinline__ void weight_rmw8(const DevSub &S, int64_t widx, int v
 // update) is read from the workspace.  Row statistics, v update, then the
 // weight write, with 16-byte accesses throughout.
 //   untransposed: warp w takes stored rows w, w + 8, ... of the block; a
-//     row is X's row, read twice (statistics, then the write)
+//     row is X's row, read twice (statistics, then the write), two 256-element
+//     segments per step with every load issued before the stores (two
+//     segments kept 64 registers; four took 119 and were slower)
 //   transposed (fp32 mode): stored row i is column i of X; the block reads
 //     32 x 64 tiles of X (8 threads per 64-column row segment), keeps
 //     per-column sums, then transposes tiles through shared memory for the
@@ -310,7 +312,17 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
         float f;
         if constexpr (kMode != 2) {
           float ss = 0.f;
-          for (int j = lane * 8; j < S.n; j += 256) {
+          int j = lane * 8;
+          for (; j + 1 * 256 + 8 <= S.n; j += 2 * 256) {  // two whole segments: loads first
+            float o[2][8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) load8x(xr + j + u * 256, 8, o[u]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) ss = fmaf(o[u][e], o[u][e], ss);
+          }
+          for (; j < S.n; j += 256) {
             float o[8];
             load8x(xr + j, min(8, S.n - j), o);
 #pragma unroll
@@ -330,7 +342,32 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
           f = mscale[si] * rf[r];
         }
         if constexpr (kMode != 1) {
-          for (int j = lane * 8; j < S.n; j += 256) {
+          int j = lane * 8;
+          for (; j + 1 * 256 + 8 <= S.n; j += 2 * 256) {  // two whole segments: all loads, then the stores
+            float o[2][8], w[2][8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              load8x(xr + j + u * 256, 8, o[u]);
+              load8(S.w, S.w_dtype, vrow * S.cols + j + u * 256, 8, wvec, w[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              float uu[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                uu[e] = f * o[u][e];
+                w[u][e] = w[u][e] - lrm * (S.wd * w[u][e] + uu[e]);
+              }
+              const int64_t widx = vrow * S.cols + j + u * 256;
+              if (S.w_dtype == GBO_BF16) store8(reinterpret_cast<__nv_bfloat16 *>(S.w) + widx, w[u], 8, wvec);
+              else store8(reinterpret_cast<float *>(S.w) + widx, w[u], 8, wvec);
+              if (dbg) {
+                float *d = dbg + S.dbg_off + widx;
+                store8(d, uu, 8, (reinterpret_cast<uintptr_t>(d) & 15) == 0);
+              }
+            }
+          }
+          for (; j < S.n; j += 256) {
             const int valid = min(8, S.n - j);
             float o[8];
             load8x(xr + j, valid, o);

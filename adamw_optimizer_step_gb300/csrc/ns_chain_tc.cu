@@ -1,0 +1,451 @@
+// The Gram route's p x p iterations for matrices of at most 128 rows, on
+// chip (bf16 mode).  With A_0 = X_0 X_0^T and P_0 from the Gram launch, the
+// iterations of eq. (5) of the NorMuon paper (zskr.cn, section 2.2) become
+// products of commuting symmetric p x p matrices,
+//   T = P_j A_j,  Q_{j+1} = P_j Q_j (Q_1 = P_0),  A_{j+1} = P_j T,
+//   P_{j+1} = a I + b A_{j+1} (+ c A_{j+1}^2),
+// and only Q_k is needed for X_k = Q_k X_0.  For a small matrix every one of
+// these products is a single 128 x 128 tile, so instead of one launch per
+// product, with each p x p result making a round trip through HBM, one CTA
+// keeps the matrix's P, A (or T) and Q in shared memory as bf16 MMA operands
+// and runs the whole chain: loads A_0 and P_0 by TMA, runs each product on
+// the tensor cores (tcgen05.mma, fp32 accumulators in TMEM), turns the
+// accumulator back into the next bf16 operand in shared memory, and stores
+// Q_k by TMA.  Every result is rounded to bf16 and mirrored from its upper
+// triangle exactly as the tile kernel's epilogue stores it, so the chain
+// computes the same values as the per-product launches.
+//
+// Persistent CTA (192 threads, one per SM), two matrices in flight:
+//   warp 0      TMA loads (one lane): A_0, P_0 (into P and Q) of the next
+//               matrix of each slot
+//   warp 1      TMEM owner and MMA issuer (one lane), alternating slots
+//   warps 2..5  epilogue, one per TMEM lane quarter; the epilogue of one
+//               slot's product overlaps the other slot's MMAs
+// Every wait is bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT,
+// lets its own copies and MMAs land (bounded), frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace gbo {
+
+namespace {
+
+constexpr int CM = 128;                       // rows (and columns) of a slot matrix
+constexpr int CK = 64;                        // 64 bf16: one 128-byte swizzle row
+constexpr int kBlk = CM * CK * 2;             // 16 KB: one 64-column block of a slot matrix
+constexpr int kMat = 2 * kBlk;                // 32 KB: a 128 x 128 bf16 matrix, K-major
+constexpr int kSlotMats = 3;                  // P, A (or T), Q
+constexpr int kSlotSize = kSlotMats * kMat;
+constexpr int kCSlots = 2;
+constexpr int kCThreads = 192;
+constexpr int kCSmem = 1024 /*align*/ + kCSlots * kSlotSize + 256 /*barriers*/;
+static_assert(kCSmem <= 232448, "shared memory per CTA");
+constexpr int kMaxOps = 3 * GBO_MAX_NS_STEPS + 1;
+constexpr int kCTmemCols = 512;               // per slot: two 128-column accumulators (+ spare)
+
+// Products (operands are slot matrices, all K-major: R symmetric, so its
+// rows serve as the B operand) and epilogues of one op of the chain.
+enum ChainMma : int32_t {
+  kMmaPA = 0,   // acc0 = P A
+  kMmaPAQ = 1,  // acc0 = P A, acc1 = P Q
+  kMmaAA = 2,   // acc0 = A A
+  kMmaPQ = 3,   // acc0 = P Q
+};
+enum ChainEpi : int32_t {
+  kEpiT = 0,    // A <- acc0 (T)
+  kEpiTQ = 1,   // A <- acc0 (T), Q <- acc1
+  kEpiAP = 2,   // A <- acc0, P <- a I + b acc0
+  kEpiA = 3,    // A <- acc0
+  kEpiP = 4,    // P <- a I + b acc0
+  kEpiSq = 5,   // P <- a I + b A + c acc0 (acc0 = A A)
+  kEpiOut = 6,  // Q <- acc0, then Q is stored to HBM
+};
+
+struct ChainOp {
+  int32_t mma, epi;
+  float a, b, c;
+};
+
+struct ChainParams {
+  CUtensorMap mapP[kMaxClassesPerLaunch];  // P_0 (loads: 64 x 128 boxes, 128-byte swizzle)
+  CUtensorMap mapA[kMaxClassesPerLaunch];  // A_0
+  CUtensorMap mapQ[kMaxClassesPerLaunch];  // Q_k (stores, same boxes)
+  int64_t mat_start[kMaxClassesPerLaunch + 1];
+  int32_t p[kMaxClassesPerLaunch];
+  int32_t n;
+  int32_t n_ops;
+  ChainOp ops[kMaxOps];
+};
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
+                            ((uint32_t)(128 >> 4) << 24);
+
+__device__ __forceinline__ void chain_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// D = L R over kit 64-wide K blocks, in 16-wide K steps (the tile kernel's
+// order); L and R are slot matrices at shared-memory addresses l and r.
+__device__ __forceinline__ void chain_product(uint32_t d_tmem, uint32_t l, uint32_t r, int kit) {
+  const uint64_t ld = smem_desc(l, 16, 1024), rd = smem_desc(r, 16, 1024);
+  for (int kb = 0; kb < kit; ++kb)
+#pragma unroll
+    for (int k = 0; k < CK / 16; ++k) {
+      const uint32_t off = (uint32_t)(kb * kBlk + k * 32) >> 4;
+      chain_mma(d_tmem, ld + off, rd + off, (kb | k) != 0);
+    }
+}
+
+// Byte offset of 16-byte chunk q (columns 8q .. 8q + 7) of row r of a slot
+// matrix: two 64-column blocks, rows of 128 bytes, 128-byte swizzle (the
+// chunk index within a row XOR the row index mod 8), as TMA writes it.
+__device__ __forceinline__ uint32_t sw128(int r, int q) {
+  return (uint32_t)((q >> 3) * kBlk + r * 128 + (((q & 7) ^ (r & 7)) << 4));
+}
+
+// Lane r writes row i = i0 + r, columns col0 .. col0 + 31 (col0 a multiple
+// of 32), as bf16.
+__device__ __forceinline__ void put_row(uint32_t m, int i, int col0, const float (&o)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(m + sw128(i, col0 / 8 + q)),
+                 "r"(pack_bf16(o[8 * q], o[8 * q + 1])), "r"(pack_bf16(o[8 * q + 2], o[8 * q + 3])),
+                 "r"(pack_bf16(o[8 * q + 4], o[8 * q + 5])), "r"(pack_bf16(o[8 * q + 6], o[8 * q + 7]))
+                 : "memory");
+}
+
+// The transpose: element (i, col0 + k) goes to (col0 + k, i).
+__device__ __forceinline__ void put_col(uint32_t m, int i, int col0, const float (&o)[32]) {
+  const uint32_t byte = (uint32_t)((i & 7) * 2);
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(m + sw128(col0 + k, i >> 3) + byte),
+                 "h"(__bfloat16_as_ushort(__float2bfloat16_rn(o[k])))
+                 : "memory");
+}
+
+__device__ __forceinline__ void get_row(uint32_t m, int i, int col0, float (&o)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(m + sw128(i, col0 / 8 + q))
+                 : "memory");
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
+      o[8 * q + 2 * h] = __low2float(b);
+      o[8 * q + 2 * h + 1] = __high2float(b);
+    }
+  }
+}
+
+// A symmetric result leaves the accumulator as the tile kernel stores it:
+// of the 32 x 32 blocks, one on the diagonal is written whole, one above it
+// is written with its mirror, one below it is skipped.  Rows and columns at
+// or past p hold zeros (the padding the next products multiply by).
+__device__ __forceinline__ void put_sym(uint32_t m, int i, int i0, int col0, int p, float (&o)[32]) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    if (i >= p || col0 + k >= p) o[k] = 0.f;
+  put_row(m, i, col0, o);
+  if (col0 >= i0 + 32) put_col(m, i, col0, o);
+}
+
+__device__ __forceinline__ int chain_class(const ChainParams &P, int64_t t) {
+  int c = 0;
+  while (c + 1 < P.n && P.mat_start[c + 1] <= t) ++c;
+  return c;
+}
+
+__global__ void __launch_bounds__(kCThreads, 1)
+ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ PhaseArgs A) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kCSlots * kSlotSize);
+  // bars: loaded[2], mmad[2], epid[2], qdone[2], freed[2], drain, then the
+  // TMEM address and the abort flag
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
+  const uint32_t loaded0 = smem_u32(bars), mmad0 = smem_u32(bars + 2), epid0 = smem_u32(bars + 4);
+  const uint32_t qdone0 = smem_u32(bars + 6), freed0 = smem_u32(bars + 8), drain = smem_u32(bars + 10);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kCSlots; ++s) {
+      mbar_init(loaded0 + 8 * s, 1);
+      mbar_init(mmad0 + 8 * s, 1);
+      mbar_init(epid0 + 8 * s, 4);
+      mbar_init(qdone0 + 8 * s, 4);
+      mbar_init(freed0 + 8 * s, 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kCTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int64_t total = P.mat_start[P.n];
+  const uint32_t slots = smem_u32(smem);
+  // matrix g of this CTA is blockIdx.x + g * gridDim.x, in slot g % 2; a
+  // slot's matrices run P.n_ops ops each, counted by u (barrier phases)
+  auto mat_of = [&](int64_t g) { return (int64_t)blockIdx.x + g * (int64_t)gridDim.x; };
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    flag_status(A.status, GBO_STATUS_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int64_t armed[kCSlots] = {-1, -1};
+      for (int64_t g = 0; mat_of(g) < total && !*abort_flag; ++g) {
+        const int s = (int)(g & 1);
+        if (g >= 2 && !mbar_wait(freed0 + 8 * s, (uint32_t)(((g >> 1) - 1) & 1))) {
+          give_up();
+          break;
+        }
+        const int64_t t = mat_of(g);
+        const int c = chain_class(P, t);
+        const int mat = (int)(t - P.mat_start[c]);
+        const uint32_t base = slots + s * kSlotSize, bar = loaded0 + 8 * s;
+        mbar_expect_tx(bar, 3 * kMat);
+        armed[s] = g;
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_3d(base + kb * kBlk, &P.mapP[c], bar, kb * CK, 0, mat);             // P <- P_0
+          tma_load_3d(base + kMat + kb * kBlk, &P.mapA[c], bar, kb * CK, 0, mat);      // A <- A_0
+          tma_load_3d(base + 2 * kMat + kb * kBlk, &P.mapP[c], bar, kb * CK, 0, mat);  // Q <- Q_1 = P_0
+        }
+      }
+      if (*abort_flag)  // let the copies armed here land before shared memory goes away
+        for (int s = 0; s < kCSlots; ++s)
+          if (armed[s] >= 0) (void)mbar_wait(loaded0 + 8 * s, (uint32_t)((armed[s] >> 1) & 1));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int64_t g[kCSlots] = {0, 1};
+      int op[kCSlots] = {0, 0};
+      uint32_t u[kCSlots] = {0, 0};
+      bool issued = false;
+      for (bool any = true; any && !*abort_flag;) {
+        any = false;
+        for (int s = 0; s < kCSlots && !*abort_flag; ++s) {
+          const int64_t t = mat_of(g[s]);
+          if (t >= total) continue;
+          any = true;
+          // the slot's previous epilogue has read its accumulators and
+          // written the operands; a new matrix's loads have landed
+          if (u[s] > 0 && !mbar_wait(epid0 + 8 * s, (u[s] - 1) & 1)) { give_up(); break; }
+          if (op[s] == 0 && !mbar_wait(loaded0 + 8 * s, (uint32_t)((g[s] >> 1) & 1))) { give_up(); break; }
+          tc_fence_after();
+          const int kit = (P.p[chain_class(P, t)] + CK - 1) / CK;
+          const uint32_t base = slots + s * kSlotSize;
+          const uint32_t mP = base, mA = base + kMat, mQ = base + 2 * kMat;
+          const uint32_t acc0 = tmem_base + (uint32_t)(s * 256), acc1 = acc0 + 128;
+          switch (P.ops[op[s]].mma) {
+            case kMmaPA: chain_product(acc0, mP, mA, kit); break;
+            case kMmaPAQ:
+              chain_product(acc0, mP, mA, kit);
+              chain_product(acc1, mP, mQ, kit);
+              break;
+            case kMmaAA: chain_product(acc0, mA, mA, kit); break;
+            default: chain_product(acc0, mP, mQ, kit); break;
+          }
+          issued = true;
+          mma_commit_one(mmad0 + 8 * s);
+          ++u[s];
+          if (++op[s] == P.n_ops) op[s] = 0, g[s] += kCSlots;
+        }
+      }
+      if (*abort_flag && issued) {  // the outstanding MMAs complete before TMEM is released
+        mma_commit_one(drain);
+        (void)mbar_wait(drain, 0);
+      }
+    }
+  } else {
+    const int quarter = warp & 3;  // TMEM lane quarter of this warp
+    const int i0 = quarter * 32, i = i0 + lane;
+    int64_t g[kCSlots] = {0, 1};
+    int op[kCSlots] = {0, 0};
+    uint32_t u[kCSlots] = {0, 0};
+    for (bool any = true; any && !*abort_flag;) {
+      any = false;
+      for (int s = 0; s < kCSlots && !*abort_flag; ++s) {
+        const int64_t t = mat_of(g[s]);
+        if (t >= total) continue;
+        any = true;
+        if (!mbar_wait(mmad0 + 8 * s, u[s] & 1)) { give_up(); break; }
+        tc_fence_after();
+        const int c = chain_class(P, t);
+        const int p = P.p[c];
+        const ChainOp o = P.ops[op[s]];
+        const uint32_t base = slots + s * kSlotSize;
+        const uint32_t mP = base, mA = base + kMat, mQ = base + 2 * kMat;
+        const uint32_t acc0 = tmem_base + ((uint32_t)i0 << 16) + (uint32_t)(s * 256), acc1 = acc0 + 128;
+        for (int cb = quarter; cb < CM / 32; ++cb) {  // blocks on or above the diagonal
+          const int col0 = cb * 32;
+          float v[32];
+          tmem_ld32(acc0 + col0, v);
+          float w[32];
+          switch (o.epi) {
+            case kEpiT:
+            case kEpiA:
+            case kEpiOut:
+              put_sym(o.epi == kEpiOut ? mQ : mA, i, i0, col0, p, v);
+              break;
+            case kEpiTQ:
+              put_sym(mA, i, i0, col0, p, v);
+              tmem_ld32(acc1 + col0, w);
+              put_sym(mQ, i, i0, col0, p, w);
+              break;
+            case kEpiAP:
+            case kEpiP:
+#pragma unroll
+              for (int k = 0; k < 32; ++k) w[k] = o.b * v[k] + (i == col0 + k ? o.a : 0.f);
+              if (o.epi == kEpiAP) put_sym(mA, i, i0, col0, p, v);
+              put_sym(mP, i, i0, col0, p, w);
+              break;
+            default: {  // kEpiSq
+              float am[32];
+              get_row(mA, i, col0, am);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) w[k] = o.c * v[k] + o.b * am[k] + (i == col0 + k ? o.a : 0.f);
+              put_sym(mP, i, i0, col0, p, w);
+              break;
+            }
+          }
+        }
+        // the writes reach the tensor cores' and TMA's proxy; the
+        // accumulators have been read
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (o.epi == kEpiOut) {
+          // Q_k to HBM once all four warps have written it; the slot is free
+          // for its next matrix when the store has read it
+          if (lane == 0) mbar_arrive(qdone0 + 8 * s);
+          if (warp == 2) {
+            const uint32_t qpar = (uint32_t)((g[s] >> 1) & 1);
+            if (!mbar_wait(qdone0 + 8 * s, qpar)) { give_up(); break; }
+            if (lane == 0) {
+              const int mat = (int)(t - P.mat_start[c]);
+              for (int kb = 0; kb * CK < p; ++kb) tma_store_3d(&P.mapQ[c], mQ + kb * kBlk, kb * CK, 0, mat);
+              bulk_commit();
+              bulk_wait_read<0>();
+              mbar_arrive(freed0 + 8 * s);
+            }
+            __syncwarp();
+          }
+        }
+        if (lane == 0) mbar_arrive(epid0 + 8 * s);
+        ++u[s];
+        if (++op[s] == P.n_ops) op[s] = 0, g[s] += kCSlots;
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // this warp's stores complete before the kernel ends
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kCTmemCols)
+                 : "memory");
+}
+
+// The ops of one matrix's chain for k iterations with coefficients abc
+// (3 per iteration): iteration j < k - 1 forms T = P_j A_j (with
+// Q_{j+1} = P_j Q_j from j = 1), then A_{j+1} = P_j T and P_{j+1} (through a
+// square of A_{j+1} when its c != 0); Q_k = P_{k-1} Q_{k-1} closes the chain.
+int chain_ops(int k, const float *abc, ChainOp *ops) {
+  int n = 0;
+  for (int j = 0; j + 1 < k; ++j) {
+    ops[n++] = ChainOp{j == 0 ? kMmaPA : kMmaPAQ, j == 0 ? kEpiT : kEpiTQ, 0.f, 0.f, 0.f};
+    const float *t = abc + 3 * (j + 1);
+    if (t[2] != 0.f) {
+      ops[n++] = ChainOp{kMmaPA, kEpiA, 0.f, 0.f, 0.f};
+      ops[n++] = ChainOp{kMmaAA, kEpiSq, t[0], t[1], t[2]};
+    } else {
+      ops[n++] = ChainOp{kMmaPA, j + 2 < k ? kEpiAP : kEpiP, t[0], t[1], 0.f};
+    }
+  }
+  ops[n++] = ChainOp{kMmaPQ, kEpiOut, 0.f, 0.f, 0.f};
+  return n;
+}
+
+}  // namespace
+
+double tc_chain_flops(int p, int k, const float *abc) {
+  std::vector<ChainOp> ops(kMaxOps);
+  const int n = chain_ops(k, abc, ops.data());
+  const double kdim = (double)((p + CK - 1) / CK) * CK;
+  double f = 0;
+  for (int j = 0; j < n; ++j) f += 2.0 * CM * (ops[j].mma == kMmaPAQ ? 2 * CM : CM) * kdim;
+  return f;
+}
+
+int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count,
+                       void *stream, int64_t *n_launch) {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(ns_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCSmem);
+  });
+  if (attr_err != cudaSuccess) return (int)attr_err;
+  for (int32_t j0 = 0; j0 < n_jobs; j0 += kMaxClassesPerLaunch) {
+    ChainParams T;
+    memset(&T, 0, sizeof T);
+    T.n = std::min(kMaxClassesPerLaunch, n_jobs - j0);
+    const GemmJob &J0 = *jobs[j0];
+    if (J0.steps < 2 || J0.steps > GBO_MAX_NS_STEPS || !J0.abc) return (int)cudaErrorInvalidValue;
+    T.n_ops = chain_ops(J0.steps, J0.abc, T.ops);
+    for (int k = 0; k < T.n; ++k) {
+      const GemmJob &J = *jobs[j0 + k];
+      const ShapeClass &C = *J.cls;
+      if (C.p > CM || J.steps != J0.steps || J.abc != J0.abc) return (int)cudaErrorInvalidValue;
+      auto at = [&](const void *region) { return static_cast<char *>(const_cast<void *>(region)) + C.p_base * 2; };
+      const bool ok = encode_map(&T.mapP[k], at(J.opA), C.p, C.p, C.count, C.ldp, CK, CM) &&
+                      encode_map(&T.mapA[k], at(J.opB), C.p, C.p, C.count, C.ldp, CK, CM) &&
+                      encode_map(&T.mapQ[k], at(J.out), C.p, C.p, C.count, C.ldp, CK, CM);
+      if (!ok) return (int)cudaErrorInvalidValue;
+      T.p[k] = C.p;
+      T.mat_start[k + 1] = T.mat_start[k] + C.count;
+    }
+    const int64_t total = T.mat_start[T.n];
+    if (total == 0) continue;
+    const unsigned grid = (unsigned)std::min<int64_t>(total, sm_count);  // one CTA per SM
+    ns_chain_kernel<<<grid, kCThreads, kCSmem, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
+    count_launches(1);
+    if (n_launch) ++*n_launch;
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return (int)err;
+  }
+  return 0;
+}
+
+}  // namespace gbo

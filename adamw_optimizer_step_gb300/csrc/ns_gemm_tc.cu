@@ -533,6 +533,11 @@ double tc_gram_route_flops(int p, int q, int k, int squares, bool tall) {
          product_flops(p, q, tall);
 }
 
+double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall) {
+  return sym_items_of(p) * item_flops(p, q) + (abc[2] != 0.f ? sym_items_of(p) * item_flops(p, p) : 0.0) +
+         tc_chain_flops(p, k, abc) + product_flops(p, q, tall);
+}
+
 namespace {
 
 // Class base of an operand or output region: X operands live in x-space,
@@ -712,14 +717,17 @@ int build_weight_maps(const gbo_muon_desc *descs, int32_t n, void **out) {
 
 int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count, void *stream,
                       int64_t *n_launch) {
-  std::vector<const GemmJob *> single, pair;
+  std::vector<const GemmJob *> single, pair, chain;
   for (int32_t j = 0; j < n_jobs; ++j) {
     if (jobs[j].cls->count == 0) continue;
-    (single_mode(jobs[j].cls->p) ? single : pair).push_back(&jobs[j]);
+    if (jobs[j].mode == kChain) chain.push_back(&jobs[j]);
+    else (single_mode(jobs[j].cls->p) ? single : pair).push_back(&jobs[j]);
   }
   int err = launch_mode<true>(pair.data(), (int32_t)pair.size(), globals, sm_count, stream, n_launch);
   if (err) return err;
-  return launch_mode<false>(single.data(), (int32_t)single.size(), globals, sm_count, stream, n_launch);
+  err = launch_mode<false>(single.data(), (int32_t)single.size(), globals, sm_count, stream, n_launch);
+  if (err) return err;
+  return launch_ns_chain_tc(chain.data(), (int32_t)chain.size(), globals, sm_count, stream, n_launch);
 }
 
 }  // namespace gbo

@@ -23,6 +23,7 @@
 namespace gbo {
 
 static std::atomic<uint64_t> g_launches{0};
+static std::atomic<int32_t> g_small_chain{1};  // see gbo_testing_set_small_chain
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 namespace {
@@ -125,6 +126,7 @@ struct gbo_plan {
   std::vector<float> abc;  // 3 * ns_steps
   bool any_c = false;
   bool any_gram = false;     // some class takes the Gram route
+  bool small_chain = true;   // Gram-route classes with p <= 128 run the on-chip chain (bf16)
   std::vector<DevSub> subs;  // sorted by shape class
   std::vector<ShapeClass> classes;
   int64_t n_tiles = 0, n_row_blocks = 0;
@@ -161,6 +163,13 @@ int squares(const gbo_plan *P) {
   int n = 0;
   for (int it = 0; it < P->opts.ns_steps; ++it) n += P->abc[3 * it + 2] != 0.f;
   return n;
+}
+
+// Gram-route classes of at most 128 rows run their p x p iterations in the
+// on-chip chain kernel (bf16 mode).
+bool uses_chain(const gbo_plan *P, const ShapeClass &C) {
+  return P->small_chain && P->x_dtype == GBO_BF16 && C.route == kRouteGram && single_mode(C.p) &&
+         P->opts.ns_steps >= 2;
 }
 
 // Route of a p x q class: the Gram route needs k >= 2; AUTO takes it when it
@@ -421,7 +430,8 @@ int validate_and_expand(gbo_plan *P) {
     double ex = 0;
     for (const ShapeClass &C : P->classes) {
       if (C.route == kRouteGram) {
-        ex += C.count * tc_gram_route_flops(C.p, C.q, o.ns_steps, squares(P), C.x_tall != 0);
+        ex += C.count * (uses_chain(P, C) ? tc_gram_chain_flops(C.p, C.q, o.ns_steps, P->abc.data(), C.x_tall != 0)
+                                          : tc_gram_route_flops(C.p, C.q, o.ns_steps, squares(P), C.x_tall != 0));
         I.n_gram_route += C.count;
       } else {
         for (int it = 0; it < o.ns_steps; ++it)
@@ -534,6 +544,15 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
       } else {
         at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramA, kGramK, 1, &P->abc[0], x[0], x[0], gA));
         at(gs, i++, kPhaseSquare).jobs.push_back(job(&C, kSquare, kKindSym, 0, &P->abc[0], gA, gA, gP[0], nullptr, gA));
+      }
+      if (uses_chain(P, C)) {  // every p x p product of the iterations in one on-chip launch
+        GemmJob J = job(&C, kChain, kKindSym, 0, nullptr, gP[0], gA, gQ[k & 1]);
+        J.steps = k;
+        J.abc = P->abc.data();
+        at(gs, i++, kPhaseProduct).jobs.push_back(J);
+        const int mode = normuon ? kProduct : kFinal;
+        at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct).jobs.push_back(product(mode, 1, nullptr, gQ[k & 1], 0));
+        continue;
       }
       for (int j = 0; j + 1 < k; ++j) {
         void *Pj = gP[j & 1];
@@ -658,6 +677,7 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
     }
   for (int it = 0; it < k; ++it) P->any_c |= P->abc[3 * it + 2] != 0.f;
   P->x_dtype = opts->precision == GBO_NS_F32 ? GBO_F32 : GBO_BF16;
+  P->small_chain = g_small_chain.load() != 0;
   const int rc = validate_and_expand(P);
   if (rc != GBO_OK) {
     delete P;
@@ -834,6 +854,8 @@ int gbo_normuon_rownorm(const float *O, int64_t rows, int64_t cols, float *row_v
   if (err) return cuda_fail(err, "NorMuon rownorm kernel");
   return ok();
 }
+
+int32_t gbo_testing_set_small_chain(int32_t enable) { return g_small_chain.exchange(enable != 0 ? 1 : 0); }
 
 int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream) {
   if (!dev_status || !aligned(dev_status, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_status is NULL or misaligned");

@@ -23,6 +23,16 @@ extern "C" {
  */
 int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream);
 
+/*
+ * Whether Muon plans created from now on (any thread) run the Gram route's
+ * p x p iterations of matrices with p <= 128 in bf16 mode as one on-chip
+ * chain launch (enable != 0, the default) or as one tensor-core launch per
+ * product with every p x p result stored in the workspace (enable == 0).
+ * Both round and mirror every p x p result the same way; tests compare them.
+ * Returns the previous setting.  Plans already created keep theirs.
+ */
+int32_t gbo_testing_set_small_chain(int32_t enable);
+
 #ifdef __cplusplus
 }
 #endif

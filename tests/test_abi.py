@@ -206,6 +206,44 @@ def test_flop_count_and_launches(L):
     L.gbo_muon_plan_destroy(plan)
 
 
+def test_small_chain_counts(L):
+    """Gram-route matrices of at most 128 rows (bf16) run their p x p
+    iterations in one on-chip launch: the Gram, the chain, the product with
+    X_0.  Each op of the chain is one 128 x 128 tile (128 x 256 when T and Q
+    are formed together) with K padded to 64; with the chain switched off
+    every p x p product is a tile-kernel launch of its own."""
+    d = lambda: [desc(0, 4 * 96, 1000, (4, 96, 1000))]  # four 96 x 1000 matrices: p = 96, q = 1000
+    tile = 2 * 128 * 256            # one single-CTA tile of the tile kernel, per unit of K
+    gram, prod, sym = tile * 1024, 4 * tile * 128, tile * 128
+    op128, op256 = 2 * 128 * 128 * 128, 2 * 128 * 256 * 128
+    # cubic, k = 5: T, A_1/P_1, then 3 x (T with Q, A/P), Q_5
+    cubic_chain = 6 * op128 + 3 * op256
+    # quintic, k = 5: T, A_1, square; 3 x (T with Q, A, square); Q_5 -- plus the square of A_0
+    quintic_chain = 10 * op128 + 3 * op256
+    rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM)
+    i = info(L, plan)
+    assert i.n_gram_route == 4 and i.launches_per_step == 2 + 3
+    assert i.ns_flops_executed == 4 * (gram + cubic_chain + prod)
+    L.gbo_muon_plan_destroy(plan)
+    rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM, abc=(15 / 8, -5 / 4, 3 / 8))
+    i = info(L, plan)
+    assert i.launches_per_step == 2 + 4
+    assert i.ns_flops_executed == 4 * (gram + sym + quintic_chain + prod)
+    L.gbo_muon_plan_destroy(plan)
+    # the fp32 mode and classes on CTA pairs keep one launch per product
+    rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM, precision=B.GBO_NS_F32)
+    assert info(L, plan).launches_per_step == 2 + 11
+    L.gbo_muon_plan_destroy(plan)
+    prev = L.gbo_testing_set_small_chain(0)
+    try:
+        rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM)
+        i = info(L, plan)
+        assert i.launches_per_step == 2 + 11 and i.ns_flops_executed == 4 * (gram + 12 * sym + prod)
+        L.gbo_muon_plan_destroy(plan)
+    finally:
+        assert L.gbo_testing_set_small_chain(prev) == 0
+
+
 def test_layout_hash(L):
     """Equal layouts hash equal whatever the pointers; a different view or
     split changes the hash (the checkpoint compatibility check)."""

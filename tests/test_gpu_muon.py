@@ -145,6 +145,38 @@ def test_routes_with_square(route, precision, abc):
     check_muon(entries, gpu, ora, lr=0.02, precision=precision)
 
 
+SMALL = [(4 * 96, 1000, (4, 96, 1000), None), (300, 100, None, None), (40, 300, None, None),
+         (128, 512, None, None), (640, 192, (2, 5, 64, 192), (20, 44))]
+
+
+@pytest.mark.parametrize("abc,ns_steps", [
+    (CUBIC, 5), (CUBIC, 2), (QUINTIC, 3),
+    (CUBIC + QUINTIC + (2.0, -1.5, 0.5) + CUBIC + (1.2, -0.3, 0.1), 5),
+])
+def test_small_chain_matches_launches(abc, ns_steps):
+    """Matrices of at most 128 rows on the Gram route: the on-chip chain
+    (one launch for all p x p products) writes bit for bit what one launch
+    per product writes (the same bf16 rounding and mirroring of every p x p
+    result), for p = 20 .. 128, wide and tall, c == 0 and c != 0, k = 2 .. 5;
+    and both match the oracle."""
+    entries = random_entries(SMALL, seed=31, b_std=1e-3)
+    kw = dict(lr=0.02, precision="bf16", abc=abc, ns_steps=ns_steps, route=B.GBO_ROUTE_GRAM)
+    prev = B.gbo_testing_set_small_chain(False)
+    try:
+        ref, st0, plan0 = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_small_chain(prev)
+    B.gbo_testing_set_small_chain(True)
+    gpu, st1, plan1 = run_muon_gpu(entries, **kw)
+    B.gbo_testing_set_small_chain(prev)
+    assert st0 == 0 and st1 == 0
+    assert B.gbo_muon_plan_info(plan1)["launches_per_step"] < B.gbo_muon_plan_info(plan0)["launches_per_step"]
+    for a, b in zip(ref, gpu):
+        assert torch.equal(a["U"], b["U"]) and torch.equal(a["W"], b["W"])
+    ora = run_muon_oracle(entries, lr=0.02, abc=abc, ns_steps=ns_steps)
+    check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
+
+
 @pytest.mark.parametrize("ns_steps", [3, 5])
 def test_normuon_gram_route(ns_steps):
     """NorMuon rows read the last iterate from the buffer each route leaves
