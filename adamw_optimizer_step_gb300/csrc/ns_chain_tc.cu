@@ -11,15 +11,19 @@
 // and runs the whole chain: loads A_0 and P_0 by TMA, runs each product on
 // the tensor cores (tcgen05.mma, fp32 accumulators in TMEM), turns the
 // accumulator back into the next bf16 operand in shared memory, and stores
-// Q_k by TMA.  Every result is rounded to bf16 and mirrored from its upper
-// triangle exactly as the tile kernel's epilogue stores it, so the chain
-// computes the same values as the per-product launches.
+// Q_k by TMA.  The left operand is read K-major (rows of L) and the right
+// one MN-major (rows of R as K), so no product relies on its operands being
+// exactly symmetric: intermediate results are written whole, row by row,
+// each element rounded to bf16 once.  Q_k leaves mirrored from its upper
+// triangle, as the tile kernel's epilogue stores symmetric results, because
+// the product of a tall X_0 with Q_k takes Q_k's rows as its columns.
 //
-// Persistent CTA (192 threads, one per SM), two matrices in flight:
+// Persistent CTA (320 threads, one per SM), two matrices in flight:
 //   warp 0      TMA loads (one lane): A_0, P_0 (into P and Q) of the next
 //               matrix of each slot
 //   warp 1      TMEM owner and MMA issuer (one lane), alternating slots
-//   warps 2..5  epilogue, one per TMEM lane quarter; the epilogue of one
+//   warps 2..9  epilogue, two per TMEM lane quarter (columns 0-63 and
+//               64-127 of the quarter's rows); the epilogue of one
 //               slot's product overlaps the other slot's MMAs
 // Every wait is bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT,
 // lets its own copies and MMAs land (bounded), frees TMEM and returns.
@@ -47,14 +51,15 @@ constexpr int kMat = 2 * kBlk;                // 32 KB: a 128 x 128 bf16 matrix,
 constexpr int kSlotMats = 3;                  // P, A (or T), Q
 constexpr int kSlotSize = kSlotMats * kMat;
 constexpr int kCSlots = 2;
-constexpr int kCThreads = 192;
+constexpr int kCEpiWarps = 8;
+constexpr int kCThreads = 64 + 32 * kCEpiWarps;
 constexpr int kCSmem = 1024 /*align*/ + kCSlots * kSlotSize + 256 /*barriers*/;
 static_assert(kCSmem <= 232448, "shared memory per CTA");
 constexpr int kMaxOps = 3 * GBO_MAX_NS_STEPS + 1;
 constexpr int kCTmemCols = 512;               // per slot: two 128-column accumulators (+ spare)
 
-// Products (operands are slot matrices, all K-major: R symmetric, so its
-// rows serve as the B operand) and epilogues of one op of the chain.
+// Products of slot matrices (L R: L read K-major, R MN-major) and
+// epilogues of one op of the chain.
 enum ChainMma : int32_t {
   kMmaPA = 0,   // acc0 = P A
   kMmaPAQ = 1,  // acc0 = P A, acc1 = P Q
@@ -87,9 +92,9 @@ struct ChainParams {
   ChainOp ops[kMaxOps];
 };
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, M = 128, N = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A
+// K-major, B MN-major, M = 128, N = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(128 >> 3) << 17) |
                             ((uint32_t)(128 >> 4) << 24);
 
 __device__ __forceinline__ void chain_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
@@ -101,16 +106,19 @@ __device__ __forceinline__ void chain_mma(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
-// D = L R over kit 64-wide K blocks, in 16-wide K steps (the tile kernel's
-// order); L and R are slot matrices at shared-memory addresses l and r.
+// D = L R over kit 64-wide K blocks, in 16-wide K steps; L and R are slot
+// matrices at shared-memory addresses l and r.  L is K-major: a K step of 16
+// is 32 bytes along its rows, a K block the next 64-column block.  R is
+// MN-major: its rows are K, a K step is two 8-row groups (2048 bytes), a K
+// block 64 rows (8192 bytes), and its N columns continue in the next
+// 64-column block (leading byte offset kBlk).
 __device__ __forceinline__ void chain_product(uint32_t d_tmem, uint32_t l, uint32_t r, int kit) {
-  const uint64_t ld = smem_desc(l, 16, 1024), rd = smem_desc(r, 16, 1024);
+  const uint64_t ld = smem_desc(l, 16, 1024), rd = smem_desc(r, kBlk, 1024);
   for (int kb = 0; kb < kit; ++kb)
 #pragma unroll
-    for (int k = 0; k < CK / 16; ++k) {
-      const uint32_t off = (uint32_t)(kb * kBlk + k * 32) >> 4;
-      chain_mma(d_tmem, ld + off, rd + off, (kb | k) != 0);
-    }
+    for (int k = 0; k < CK / 16; ++k)
+      chain_mma(d_tmem, ld + ((uint32_t)(kb * kBlk + k * 32) >> 4), rd + ((uint32_t)(kb * 8192 + k * 2048) >> 4),
+                (kb | k) != 0);
 }
 
 // Byte offset of 16-byte chunk q (columns 8q .. 8q + 7) of row r of a slot
@@ -158,16 +166,31 @@ __device__ __forceinline__ void get_row(uint32_t m, int i, int col0, float (&o)[
   }
 }
 
-// A symmetric result leaves the accumulator as the tile kernel stores it:
-// of the 32 x 32 blocks, one on the diagonal is written whole, one above it
-// is written with its mirror, one below it is skipped.  Rows and columns at
-// or past p hold zeros (the padding the next products multiply by).
-__device__ __forceinline__ void put_sym(uint32_t m, int i, int i0, int col0, int p, float (&o)[32]) {
+// Rows and columns at or past p hold zeros (the padding the next products
+// multiply by).
+__device__ __forceinline__ void mask_pad(int i, int col0, int p, float (&o)[32]) {
+  if (i >= p) {
 #pragma unroll
-  for (int k = 0; k < 32; ++k)
-    if (i >= p || col0 + k >= p) o[k] = 0.f;
+    for (int k = 0; k < 32; ++k) o[k] = 0.f;
+  } else if (col0 + 32 > p) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (col0 + k >= p) o[k] = 0.f;
+  }
+}
+
+// Q_k leaves the accumulator as the tile kernel stores a symmetric result:
+// of the 32 x 32 blocks, one on the diagonal is written whole, one above it
+// is written with its mirror, one below it is skipped.
+__device__ __forceinline__ void put_sym(uint32_t m, int i, int i0, int col0, int p, float (&o)[32]) {
+  mask_pad(i, col0, p, o);
   put_row(m, i, col0, o);
   if (col0 >= i0 + 32) put_col(m, i, col0, o);
+}
+
+__device__ __forceinline__ void put_full(uint32_t m, int i, int col0, int p, float (&o)[32]) {
+  mask_pad(i, col0, p, o);
+  put_row(m, i, col0, o);
 }
 
 __device__ __forceinline__ int chain_class(const ChainParams &P, int64_t t) {
@@ -192,8 +215,8 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
     for (int s = 0; s < kCSlots; ++s) {
       mbar_init(loaded0 + 8 * s, 1);
       mbar_init(mmad0 + 8 * s, 1);
-      mbar_init(epid0 + 8 * s, 4);
-      mbar_init(qdone0 + 8 * s, 4);
+      mbar_init(epid0 + 8 * s, kCEpiWarps);
+      mbar_init(qdone0 + 8 * s, kCEpiWarps);
       mbar_init(freed0 + 8 * s, 1);
     }
     mbar_init(drain, 1);
@@ -287,7 +310,8 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
       }
     }
   } else {
-    const int quarter = warp & 3;  // TMEM lane quarter of this warp
+    const int quarter = warp & 3;           // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;       // its 64 columns: blocks 2 half, 2 half + 1
     const int i0 = quarter * 32, i = i0 + lane;
     int64_t g[kCSlots] = {0, 1};
     int op[kCSlots] = {0, 0};
@@ -306,7 +330,9 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
         const uint32_t base = slots + s * kSlotSize;
         const uint32_t mP = base, mA = base + kMat, mQ = base + 2 * kMat;
         const uint32_t acc0 = tmem_base + ((uint32_t)i0 << 16) + (uint32_t)(s * 256), acc1 = acc0 + 128;
-        for (int cb = quarter; cb < CM / 32; ++cb) {  // blocks on or above the diagonal
+        // whole rows for the next products; Q_k: blocks on or above the
+        // diagonal, mirrored
+        for (int cb = o.epi == kEpiOut ? max(quarter, 2 * half) : 2 * half; cb < 2 * half + 2; ++cb) {
           const int col0 = cb * 32;
           float v[32];
           tmem_ld32(acc0 + col0, v);
@@ -314,27 +340,29 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
           switch (o.epi) {
             case kEpiT:
             case kEpiA:
+              put_full(mA, i, col0, p, v);
+              break;
             case kEpiOut:
-              put_sym(o.epi == kEpiOut ? mQ : mA, i, i0, col0, p, v);
+              put_sym(mQ, i, i0, col0, p, v);
               break;
             case kEpiTQ:
-              put_sym(mA, i, i0, col0, p, v);
+              put_full(mA, i, col0, p, v);
               tmem_ld32(acc1 + col0, w);
-              put_sym(mQ, i, i0, col0, p, w);
+              put_full(mQ, i, col0, p, w);
               break;
             case kEpiAP:
             case kEpiP:
 #pragma unroll
               for (int k = 0; k < 32; ++k) w[k] = o.b * v[k] + (i == col0 + k ? o.a : 0.f);
-              if (o.epi == kEpiAP) put_sym(mA, i, i0, col0, p, v);
-              put_sym(mP, i, i0, col0, p, w);
+              if (o.epi == kEpiAP) put_full(mA, i, col0, p, v);
+              put_full(mP, i, col0, p, w);
               break;
             default: {  // kEpiSq
               float am[32];
               get_row(mA, i, col0, am);
 #pragma unroll
               for (int k = 0; k < 32; ++k) w[k] = o.c * v[k] + o.b * am[k] + (i == col0 + k ? o.a : 0.f);
-              put_sym(mP, i, i0, col0, p, w);
+              put_full(mP, i, col0, p, w);
               break;
             }
           }
