@@ -368,7 +368,7 @@ def gbo_struct_size(which):
 
 def gbo_testing_set_small_chain(enable):
     """Whether plans created from now on run the Gram route's p x p
-    iterations of matrices with p <= 128 (bf16) in one on-chip chain launch.
+    iterations of matrices with p <= 192 (bf16) in one on-chip chain launch.
     Returns the previous setting."""
     return bool(lib().gbo_testing_set_small_chain(1 if enable else 0))
 

@@ -88,7 +88,7 @@ enum GemmMode : int32_t {
   kProduct = 3,   // C = P X;    write X' = s C
   kFinal = 4,     // C = P X;    O = s C; update the weight (+ dbg)
   kGramAP = 5,    // C symmetric; write A = s^2 C and P = a I + b A
-  kChain = 6,     // the Gram route's p x p chain on chip (p <= 128): A_0, P_0 -> Q_k
+  kChain = 6,     // the Gram route's p x p chain on chip (p <= kChainMaxP): A_0, P_0 -> Q_k
 };
 
 // Operand shapes of one tensor-core GEMM job.  X is p x q ("wide") or, for
@@ -174,12 +174,14 @@ int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &glob
                       void *stream, int64_t *n_launch);
 int launch_ns_gemm_tf32(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
                         void *stream, int64_t *n_launch);
-// kChain jobs (bf16, p <= 128): opA = P_0, opB = A_0, out = Q_k regions;
-// every job of one call has the same steps and abc.
+// kChain jobs (bf16, p <= kChainMaxP): opA = P_0, opB = A_0, out = Q_k
+// regions; every job of one call has the same steps and abc.
+constexpr int kChainMaxP = 192;
 int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
                        void *stream, int64_t *n_launch);
-// FLOPs the chain kernel executes for one p x p matrix (p <= 128) over k
-// iterations with coefficients abc: 128 x 128 (or x 256) tiles, K padded to 64.
+// FLOPs the chain kernel executes for one p x p matrix (p <= kChainMaxP)
+// over k iterations with coefficients abc: 128 x 128 (or x 256) tiles for
+// p <= 128, two 128 x 192 row halves for larger p, K padded to 64.
 double tc_chain_flops(int p, int k, const float *abc);
 // FLOPs the tensor-core kernel executes for one p x q matrix and one
 // iteration (Gram over the upper block-triangle of tiles, square when c != 0,

@@ -1,11 +1,11 @@
-// The Gram route's p x p iterations for matrices of at most 128 rows, on
+// The Gram route's p x p iterations for matrices of at most 192 rows, on
 // chip (bf16 mode).  With A_0 = X_0 X_0^T and P_0 from the Gram launch, the
 // iterations of eq. (5) of the NorMuon paper (zskr.cn, section 2.2) become
 // products of commuting symmetric p x p matrices,
 //   T = P_j A_j,  Q_{j+1} = P_j Q_j (Q_1 = P_0),  A_{j+1} = P_j T,
 //   P_{j+1} = a I + b A_{j+1} (+ c A_{j+1}^2),
 // and only Q_k is needed for X_k = Q_k X_0.  For a small matrix every one of
-// these products is a single 128 x 128 tile, so instead of one launch per
+// these products is one or two 128-row tiles, so instead of one launch per
 // product, with each p x p result making a round trip through HBM, one CTA
 // keeps the matrix's P, A (or T) and Q in shared memory as bf16 MMA operands
 // and runs the whole chain: loads A_0 and P_0 by TMA, runs each product on
@@ -18,13 +18,20 @@
 // triangle, as the tile kernel's epilogue stores symmetric results, because
 // the product of a tall X_0 with Q_k takes Q_k's rows as its columns.
 //
-// Persistent CTA (320 threads, one per SM), two matrices in flight:
+// Two geometries (template parameter kH, 128-row halves of a matrix):
+//   kH = 1  p <= 128: 128 x 128 matrices (32 KB each), two matrices in
+//           flight per CTA so the epilogue of one slot's product overlaps
+//           the other slot's MMAs; T and Q_{j+1} form together (N = 256)
+//   kH = 2  128 < p <= 192: 192 x 192 matrices (72 KB each), one matrix per
+//           CTA; each product is two M = 128 row halves with N = 192, and
+//           T and Q_{j+1} are separate products (their accumulators would
+//           not fit TMEM together)
+// Persistent CTA (320 threads, one per SM):
 //   warp 0      TMA loads (one lane): A_0, P_0 (into P and Q) of the next
 //               matrix of each slot
 //   warp 1      TMEM owner and MMA issuer (one lane), alternating slots
-//   warps 2..9  epilogue, two per TMEM lane quarter (columns 0-63 and
-//               64-127 of the quarter's rows); the epilogue of one
-//               slot's product overlaps the other slot's MMAs
+//   warps 2..9  epilogue, two per TMEM lane quarter, each taking half of
+//               the column blocks of the quarter's rows
 // Every wait is bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT,
 // lets its own copies and MMAs land (bounded), frees TMEM and returns.
 #include <cuda.h>
@@ -44,36 +51,47 @@ namespace gbo {
 
 namespace {
 
-constexpr int CM = 128;                       // rows (and columns) of a slot matrix
 constexpr int CK = 64;                        // 64 bf16: one 128-byte swizzle row
-constexpr int kBlk = CM * CK * 2;             // 16 KB: one 64-column block of a slot matrix
-constexpr int kMat = 2 * kBlk;                // 32 KB: a 128 x 128 bf16 matrix, K-major
-constexpr int kSlotMats = 3;                  // P, A (or T), Q
-constexpr int kSlotSize = kSlotMats * kMat;
-constexpr int kCSlots = 2;
 constexpr int kCEpiWarps = 8;
 constexpr int kCThreads = 64 + 32 * kCEpiWarps;
-constexpr int kCSmem = 1024 /*align*/ + kCSlots * kSlotSize + 256 /*barriers*/;
-static_assert(kCSmem <= 232448, "shared memory per CTA");
-constexpr int kMaxOps = 3 * GBO_MAX_NS_STEPS + 1;
-constexpr int kCTmemCols = 512;               // per slot: two 128-column accumulators (+ spare)
+constexpr int kMaxOps = 4 * GBO_MAX_NS_STEPS + 1;
+constexpr int kCTmemCols = 512;
+
+// Shared-memory geometry of one slot matrix (K-major rows of 128 bytes in
+// 64-column blocks, 128-byte swizzle, as TMA writes it).
+template <int kH>
+struct Geo {
+  static constexpr int R = kH == 1 ? 128 : 192;  // rows (= columns) of a slot matrix
+  static constexpr int KB = R / CK;              // 64-column blocks
+  static constexpr int Blk = R * 128;            // bytes of one 64-column block
+  static constexpr int Mat = KB * Blk;           // 32 KB or 72 KB
+  static constexpr int Slots = kH == 1 ? 2 : 1;
+  static constexpr int SlotSize = 3 * Mat;       // P, A (or T), Q
+  static constexpr int Smem = 1024 /*align*/ + Slots * SlotSize + 256 /*barriers*/;
+  static constexpr int WarpBlocks = R / 64;      // 32-column blocks per epilogue warp and row block
+  // kind::f16: fp32 accumulator, bf16 A and B, A K-major, B MN-major, M = 128, N = R
+  static constexpr uint32_t Idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                    ((uint32_t)(R >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+};
+static_assert(Geo<1>::Smem <= 232448 && Geo<2>::Smem <= 232448, "shared memory per CTA");
 
 // Products of slot matrices (L R: L read K-major, R MN-major) and
 // epilogues of one op of the chain.
 enum ChainMma : int32_t {
   kMmaPA = 0,   // acc0 = P A
-  kMmaPAQ = 1,  // acc0 = P A, acc1 = P Q
+  kMmaPAQ = 1,  // acc0 = P A, acc1 = P Q (kH = 1)
   kMmaAA = 2,   // acc0 = A A
   kMmaPQ = 3,   // acc0 = P Q
 };
 enum ChainEpi : int32_t {
   kEpiT = 0,    // A <- acc0 (T)
-  kEpiTQ = 1,   // A <- acc0 (T), Q <- acc1
+  kEpiTQ = 1,   // A <- acc0 (T), Q <- acc1 (kH = 1)
   kEpiAP = 2,   // A <- acc0, P <- a I + b acc0
   kEpiA = 3,    // A <- acc0
   kEpiP = 4,    // P <- a I + b acc0
   kEpiSq = 5,   // P <- a I + b A + c acc0 (acc0 = A A)
   kEpiOut = 6,  // Q <- acc0, then Q is stored to HBM
+  kEpiQ = 7,    // Q <- acc0 (kH = 2)
 };
 
 struct ChainOp {
@@ -82,7 +100,7 @@ struct ChainOp {
 };
 
 struct ChainParams {
-  CUtensorMap mapP[kMaxClassesPerLaunch];  // P_0 (loads: 64 x 128 boxes, 128-byte swizzle)
+  CUtensorMap mapP[kMaxClassesPerLaunch];  // P_0 (loads: 64-column boxes of R rows, 128-byte swizzle)
   CUtensorMap mapA[kMaxClassesPerLaunch];  // A_0
   CUtensorMap mapQ[kMaxClassesPerLaunch];  // Q_k (stores, same boxes)
   int64_t mat_start[kMaxClassesPerLaunch + 1];
@@ -92,70 +110,73 @@ struct ChainParams {
   ChainOp ops[kMaxOps];
 };
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A
-// K-major, B MN-major, M = 128, N = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(128 >> 3) << 17) |
-                            ((uint32_t)(128 >> 4) << 24);
-
+template <int kH>
 __device__ __forceinline__ void chain_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(Geo<kH>::Idesc), "r"(accumulate)
       : "memory");
 }
 
-// D = L R over kit 64-wide K blocks, in 16-wide K steps; L and R are slot
-// matrices at shared-memory addresses l and r.  L is K-major: a K step of 16
-// is 32 bytes along its rows, a K block the next 64-column block.  R is
-// MN-major: its rows are K, a K step is two 8-row groups (2048 bytes), a K
-// block 64 rows (8192 bytes), and its N columns continue in the next
-// 64-column block (leading byte offset kBlk).
-__device__ __forceinline__ void chain_product(uint32_t d_tmem, uint32_t l, uint32_t r, int kit) {
-  const uint64_t ld = smem_desc(l, 16, 1024), rd = smem_desc(r, kBlk, 1024);
+// Row half h of D = L R over kit 64-wide K blocks, in 16-wide K steps; L and
+// R are slot matrices at shared-memory addresses l and r.  L is K-major: its
+// rows 128 h .. start 16 KB into each block, a K step of 16 is 32 bytes
+// along its rows, a K block the next 64-column block.  R is MN-major: its
+// rows are K, a K step is two 8-row groups (2048 bytes), a K block 64 rows
+// (8192 bytes), and its N columns continue in the next 64-column block
+// (leading byte offset Blk).  Rows 192 .. 255 of an L with kH = 2 lie in the
+// buffer after it (A after P, Q after A): they feed only accumulator rows
+// that are never written back.
+template <int kH>
+__device__ __forceinline__ void chain_product(uint32_t d_tmem, uint32_t l, uint32_t r, int kit, int h) {
+  const uint64_t ld = smem_desc(l + (uint32_t)h * 16384u, 16, 1024), rd = smem_desc(r, Geo<kH>::Blk, 1024);
   for (int kb = 0; kb < kit; ++kb)
 #pragma unroll
     for (int k = 0; k < CK / 16; ++k)
-      chain_mma(d_tmem, ld + ((uint32_t)(kb * kBlk + k * 32) >> 4), rd + ((uint32_t)(kb * 8192 + k * 2048) >> 4),
-                (kb | k) != 0);
+      chain_mma<kH>(d_tmem, ld + ((uint32_t)(kb * Geo<kH>::Blk + k * 32) >> 4),
+                    rd + ((uint32_t)(kb * 8192 + k * 2048) >> 4), (kb | k) != 0);
 }
 
 // Byte offset of 16-byte chunk q (columns 8q .. 8q + 7) of row r of a slot
-// matrix: two 64-column blocks, rows of 128 bytes, 128-byte swizzle (the
-// chunk index within a row XOR the row index mod 8), as TMA writes it.
+// matrix: the chunk index within a 128-byte row XOR the row index mod 8.
+template <int kH>
 __device__ __forceinline__ uint32_t sw128(int r, int q) {
-  return (uint32_t)((q >> 3) * kBlk + r * 128 + (((q & 7) ^ (r & 7)) << 4));
+  return (uint32_t)((q >> 3) * Geo<kH>::Blk + r * 128 + (((q & 7) ^ (r & 7)) << 4));
 }
 
-// Lane r writes row i = i0 + r, columns col0 .. col0 + 31 (col0 a multiple
-// of 32), as bf16.
+// Lane r writes row i, columns col0 .. col0 + 31 (col0 a multiple of 32),
+// as bf16.
+template <int kH>
 __device__ __forceinline__ void put_row(uint32_t m, int i, int col0, const float (&o)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(m + sw128(i, col0 / 8 + q)),
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(m + sw128<kH>(i, col0 / 8 + q)),
                  "r"(pack_bf16(o[8 * q], o[8 * q + 1])), "r"(pack_bf16(o[8 * q + 2], o[8 * q + 3])),
                  "r"(pack_bf16(o[8 * q + 4], o[8 * q + 5])), "r"(pack_bf16(o[8 * q + 6], o[8 * q + 7]))
                  : "memory");
 }
 
 // The transpose: element (i, col0 + k) goes to (col0 + k, i).
+template <int kH>
 __device__ __forceinline__ void put_col(uint32_t m, int i, int col0, const float (&o)[32]) {
   const uint32_t byte = (uint32_t)((i & 7) * 2);
 #pragma unroll
   for (int k = 0; k < 32; ++k)
-    asm volatile("st.shared.b16 [%0], %1;" ::"r"(m + sw128(col0 + k, i >> 3) + byte),
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(m + sw128<kH>(col0 + k, i >> 3) + byte),
                  "h"(__bfloat16_as_ushort(__float2bfloat16_rn(o[k])))
                  : "memory");
 }
 
+template <int kH>
 __device__ __forceinline__ void get_row(uint32_t m, int i, int col0, float (&o)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t w[4];
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                 : "r"(m + sw128(i, col0 / 8 + q))
+                 : "r"(m + sw128<kH>(i, col0 / 8 + q))
                  : "memory");
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -182,15 +203,17 @@ __device__ __forceinline__ void mask_pad(int i, int col0, int p, float (&o)[32])
 // Q_k leaves the accumulator as the tile kernel stores a symmetric result:
 // of the 32 x 32 blocks, one on the diagonal is written whole, one above it
 // is written with its mirror, one below it is skipped.
+template <int kH>
 __device__ __forceinline__ void put_sym(uint32_t m, int i, int i0, int col0, int p, float (&o)[32]) {
   mask_pad(i, col0, p, o);
-  put_row(m, i, col0, o);
-  if (col0 >= i0 + 32) put_col(m, i, col0, o);
+  put_row<kH>(m, i, col0, o);
+  if (col0 >= i0 + 32) put_col<kH>(m, i, col0, o);
 }
 
+template <int kH>
 __device__ __forceinline__ void put_full(uint32_t m, int i, int col0, int p, float (&o)[32]) {
   mask_pad(i, col0, p, o);
-  put_row(m, i, col0, o);
+  put_row<kH>(m, i, col0, o);
 }
 
 __device__ __forceinline__ int chain_class(const ChainParams &P, int64_t t) {
@@ -199,11 +222,14 @@ __device__ __forceinline__ int chain_class(const ChainParams &P, int64_t t) {
   return c;
 }
 
+template <int kH>
 __global__ void __launch_bounds__(kCThreads, 1)
 ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ PhaseArgs A) {
+  using G = Geo<kH>;
+  constexpr int S = G::Slots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kCSlots * kSlotSize);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * G::SlotSize);
   // bars: loaded[2], mmad[2], epid[2], qdone[2], freed[2], drain, then the
   // TMEM address and the abort flag
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
@@ -212,7 +238,7 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
   const uint32_t qdone0 = smem_u32(bars + 6), freed0 = smem_u32(bars + 8), drain = smem_u32(bars + 10);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kCSlots; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(loaded0 + 8 * s, 1);
       mbar_init(mmad0 + 8 * s, 1);
       mbar_init(epid0 + 8 * s, kCEpiWarps);
@@ -235,7 +261,7 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
   const uint32_t tmem_base = *tmem_slot;
   const int64_t total = P.mat_start[P.n];
   const uint32_t slots = smem_u32(smem);
-  // matrix g of this CTA is blockIdx.x + g * gridDim.x, in slot g % 2; a
+  // matrix g of this CTA is blockIdx.x + g * gridDim.x, in slot g % S; a
   // slot's matrices run P.n_ops ops each, counted by u (barrier phases)
   auto mat_of = [&](int64_t g) { return (int64_t)blockIdx.x + g * (int64_t)gridDim.x; };
   auto give_up = [&]() {
@@ -245,63 +271,68 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
 
   if (warp == 0) {
     if (lane == 0) {
-      int64_t armed[kCSlots] = {-1, -1};
+      int64_t armed[S];
+      for (int s = 0; s < S; ++s) armed[s] = -1;
       for (int64_t g = 0; mat_of(g) < total && !*abort_flag; ++g) {
-        const int s = (int)(g & 1);
-        if (g >= 2 && !mbar_wait(freed0 + 8 * s, (uint32_t)(((g >> 1) - 1) & 1))) {
+        const int s = (int)(g % S);
+        const int64_t gs = g / S;  // the slot's matrix count so far
+        if (gs >= 1 && !mbar_wait(freed0 + 8 * s, (uint32_t)((gs - 1) & 1))) {
           give_up();
           break;
         }
         const int64_t t = mat_of(g);
         const int c = chain_class(P, t);
         const int mat = (int)(t - P.mat_start[c]);
-        const uint32_t base = slots + s * kSlotSize, bar = loaded0 + 8 * s;
-        mbar_expect_tx(bar, 3 * kMat);
-        armed[s] = g;
-        for (int kb = 0; kb < 2; ++kb) {
-          tma_load_3d(base + kb * kBlk, &P.mapP[c], bar, kb * CK, 0, mat);             // P <- P_0
-          tma_load_3d(base + kMat + kb * kBlk, &P.mapA[c], bar, kb * CK, 0, mat);      // A <- A_0
-          tma_load_3d(base + 2 * kMat + kb * kBlk, &P.mapP[c], bar, kb * CK, 0, mat);  // Q <- Q_1 = P_0
+        const uint32_t base = slots + s * G::SlotSize, bar = loaded0 + 8 * s;
+        mbar_expect_tx(bar, 3 * G::Mat);
+        armed[s] = gs;
+        for (int kb = 0; kb < G::KB; ++kb) {
+          tma_load_3d(base + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);               // P <- P_0
+          tma_load_3d(base + G::Mat + kb * G::Blk, &P.mapA[c], bar, kb * CK, 0, mat);      // A <- A_0
+          tma_load_3d(base + 2 * G::Mat + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);  // Q <- Q_1 = P_0
         }
       }
       if (*abort_flag)  // let the copies armed here land before shared memory goes away
-        for (int s = 0; s < kCSlots; ++s)
-          if (armed[s] >= 0) (void)mbar_wait(loaded0 + 8 * s, (uint32_t)((armed[s] >> 1) & 1));
+        for (int s = 0; s < S; ++s)
+          if (armed[s] >= 0) (void)mbar_wait(loaded0 + 8 * s, (uint32_t)(armed[s] & 1));
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int64_t g[kCSlots] = {0, 1};
-      int op[kCSlots] = {0, 0};
-      uint32_t u[kCSlots] = {0, 0};
+      int64_t g[S];
+      int op[S];
+      uint32_t u[S];
+      for (int s = 0; s < S; ++s) g[s] = s, op[s] = 0, u[s] = 0;
       bool issued = false;
       for (bool any = true; any && !*abort_flag;) {
         any = false;
-        for (int s = 0; s < kCSlots && !*abort_flag; ++s) {
+        for (int s = 0; s < S && !*abort_flag; ++s) {
           const int64_t t = mat_of(g[s]);
           if (t >= total) continue;
           any = true;
           // the slot's previous epilogue has read its accumulators and
           // written the operands; a new matrix's loads have landed
           if (u[s] > 0 && !mbar_wait(epid0 + 8 * s, (u[s] - 1) & 1)) { give_up(); break; }
-          if (op[s] == 0 && !mbar_wait(loaded0 + 8 * s, (uint32_t)((g[s] >> 1) & 1))) { give_up(); break; }
+          if (op[s] == 0 && !mbar_wait(loaded0 + 8 * s, (uint32_t)((g[s] / S) & 1))) { give_up(); break; }
           tc_fence_after();
           const int kit = (P.p[chain_class(P, t)] + CK - 1) / CK;
-          const uint32_t base = slots + s * kSlotSize;
-          const uint32_t mP = base, mA = base + kMat, mQ = base + 2 * kMat;
-          const uint32_t acc0 = tmem_base + (uint32_t)(s * 256), acc1 = acc0 + 128;
-          switch (P.ops[op[s]].mma) {
-            case kMmaPA: chain_product(acc0, mP, mA, kit); break;
-            case kMmaPAQ:
-              chain_product(acc0, mP, mA, kit);
-              chain_product(acc1, mP, mQ, kit);
-              break;
-            case kMmaAA: chain_product(acc0, mA, mA, kit); break;
-            default: chain_product(acc0, mP, mQ, kit); break;
+          const uint32_t base = slots + s * G::SlotSize;
+          const uint32_t mP = base, mA = base + G::Mat, mQ = base + 2 * G::Mat;
+          const uint32_t acc = tmem_base + (uint32_t)(s * 256);
+          const int mma = P.ops[op[s]].mma;
+          for (int h = 0; h < kH; ++h) {
+            const uint32_t d = acc + (uint32_t)(h * 256);
+            if (mma == kMmaPA) chain_product<kH>(d, mP, mA, kit, h);
+            else if (mma == kMmaAA) chain_product<kH>(d, mA, mA, kit, h);
+            else if (mma == kMmaPQ) chain_product<kH>(d, mP, mQ, kit, h);
+            else {  // kMmaPAQ
+              chain_product<kH>(d, mP, mA, kit, h);
+              chain_product<kH>(d + 128, mP, mQ, kit, h);
+            }
           }
           issued = true;
           mma_commit_one(mmad0 + 8 * s);
           ++u[s];
-          if (++op[s] == P.n_ops) op[s] = 0, g[s] += kCSlots;
+          if (++op[s] == P.n_ops) op[s] = 0, g[s] += S;
         }
       }
       if (*abort_flag && issued) {  // the outstanding MMAs complete before TMEM is released
@@ -310,15 +341,16 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
       }
     }
   } else {
-    const int quarter = warp & 3;           // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;       // its 64 columns: blocks 2 half, 2 half + 1
-    const int i0 = quarter * 32, i = i0 + lane;
-    int64_t g[kCSlots] = {0, 1};
-    int op[kCSlots] = {0, 0};
-    uint32_t u[kCSlots] = {0, 0};
+    const int quarter = warp & 3;      // TMEM lane quarter of this warp
+    const int wh = (warp - 2) >> 2;    // its column blocks: wh * WarpBlocks ..
+    const int cb0 = wh * G::WarpBlocks, cb1 = cb0 + G::WarpBlocks;
+    int64_t g[S];
+    int op[S];
+    uint32_t u[S];
+    for (int s = 0; s < S; ++s) g[s] = s, op[s] = 0, u[s] = 0;
     for (bool any = true; any && !*abort_flag;) {
       any = false;
-      for (int s = 0; s < kCSlots && !*abort_flag; ++s) {
+      for (int s = 0; s < S && !*abort_flag; ++s) {
         const int64_t t = mat_of(g[s]);
         if (t >= total) continue;
         any = true;
@@ -327,43 +359,51 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
         const int c = chain_class(P, t);
         const int p = P.p[c];
         const ChainOp o = P.ops[op[s]];
-        const uint32_t base = slots + s * kSlotSize;
-        const uint32_t mP = base, mA = base + kMat, mQ = base + 2 * kMat;
-        const uint32_t acc0 = tmem_base + ((uint32_t)i0 << 16) + (uint32_t)(s * 256), acc1 = acc0 + 128;
-        // whole rows for the next products; Q_k: blocks on or above the
-        // diagonal, mirrored
-        for (int cb = o.epi == kEpiOut ? max(quarter, 2 * half) : 2 * half; cb < 2 * half + 2; ++cb) {
-          const int col0 = cb * 32;
-          float v[32];
-          tmem_ld32(acc0 + col0, v);
-          float w[32];
-          switch (o.epi) {
-            case kEpiT:
-            case kEpiA:
-              put_full(mA, i, col0, p, v);
-              break;
-            case kEpiOut:
-              put_sym(mQ, i, i0, col0, p, v);
-              break;
-            case kEpiTQ:
-              put_full(mA, i, col0, p, v);
-              tmem_ld32(acc1 + col0, w);
-              put_full(mQ, i, col0, p, w);
-              break;
-            case kEpiAP:
-            case kEpiP:
+        const uint32_t base = slots + s * G::SlotSize;
+        const uint32_t mP = base, mA = base + G::Mat, mQ = base + 2 * G::Mat;
+        for (int h = 0; h < kH; ++h) {
+          const int i0 = h * 128 + quarter * 32, i = i0 + lane;
+          if (i0 >= G::R) continue;  // kH = 2: rows 192 .. 255 are padding
+          const uint32_t acc0 = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(s * 256 + h * 256);
+          const uint32_t acc1 = acc0 + 128;
+          // whole rows for the next products; Q_k: blocks on or above the
+          // diagonal, mirrored
+          for (int cb = o.epi == kEpiOut ? max(i0 / 32, cb0) : cb0; cb < cb1; ++cb) {
+            const int col0 = cb * 32;
+            float v[32];
+            tmem_ld32(acc0 + col0, v);
+            float w[32];
+            switch (o.epi) {
+              case kEpiT:
+              case kEpiA:
+                put_full<kH>(mA, i, col0, p, v);
+                break;
+              case kEpiQ:
+                put_full<kH>(mQ, i, col0, p, v);
+                break;
+              case kEpiOut:
+                put_sym<kH>(mQ, i, i0, col0, p, v);
+                break;
+              case kEpiTQ:
+                put_full<kH>(mA, i, col0, p, v);
+                tmem_ld32(acc1 + col0, w);
+                put_full<kH>(mQ, i, col0, p, w);
+                break;
+              case kEpiAP:
+              case kEpiP:
 #pragma unroll
-              for (int k = 0; k < 32; ++k) w[k] = o.b * v[k] + (i == col0 + k ? o.a : 0.f);
-              if (o.epi == kEpiAP) put_full(mA, i, col0, p, v);
-              put_full(mP, i, col0, p, w);
-              break;
-            default: {  // kEpiSq
-              float am[32];
-              get_row(mA, i, col0, am);
+                for (int k = 0; k < 32; ++k) w[k] = o.b * v[k] + (i == col0 + k ? o.a : 0.f);
+                if (o.epi == kEpiAP) put_full<kH>(mA, i, col0, p, v);
+                put_full<kH>(mP, i, col0, p, w);
+                break;
+              default: {  // kEpiSq
+                float am[32];
+                get_row<kH>(mA, i, col0, am);
 #pragma unroll
-              for (int k = 0; k < 32; ++k) w[k] = o.c * v[k] + o.b * am[k] + (i == col0 + k ? o.a : 0.f);
-              put_full(mP, i, col0, p, w);
-              break;
+                for (int k = 0; k < 32; ++k) w[k] = o.c * v[k] + o.b * am[k] + (i == col0 + k ? o.a : 0.f);
+                put_full<kH>(mP, i, col0, p, w);
+                break;
+              }
             }
           }
         }
@@ -373,15 +413,15 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
         tc_fence_before();
         __syncwarp();
         if (o.epi == kEpiOut) {
-          // Q_k to HBM once all four warps have written it; the slot is free
-          // for its next matrix when the store has read it
+          // Q_k to HBM once all epilogue warps have written it; the slot is
+          // free for its next matrix when the store has read it
           if (lane == 0) mbar_arrive(qdone0 + 8 * s);
           if (warp == 2) {
-            const uint32_t qpar = (uint32_t)((g[s] >> 1) & 1);
+            const uint32_t qpar = (uint32_t)((g[s] / S) & 1);
             if (!mbar_wait(qdone0 + 8 * s, qpar)) { give_up(); break; }
             if (lane == 0) {
               const int mat = (int)(t - P.mat_start[c]);
-              for (int kb = 0; kb * CK < p; ++kb) tma_store_3d(&P.mapQ[c], mQ + kb * kBlk, kb * CK, 0, mat);
+              for (int kb = 0; kb * CK < p; ++kb) tma_store_3d(&P.mapQ[c], mQ + kb * G::Blk, kb * CK, 0, mat);
               bulk_commit();
               bulk_wait_read<0>();
               mbar_arrive(freed0 + 8 * s);
@@ -391,7 +431,7 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
         }
         if (lane == 0) mbar_arrive(epid0 + 8 * s);
         ++u[s];
-        if (++op[s] == P.n_ops) op[s] = 0, g[s] += kCSlots;
+        if (++op[s] == P.n_ops) op[s] = 0, g[s] += S;
       }
     }
     if (lane == 0) bulk_wait_all();  // this warp's stores complete before the kernel ends
@@ -408,12 +448,20 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
 
 // The ops of one matrix's chain for k iterations with coefficients abc
 // (3 per iteration): iteration j < k - 1 forms T = P_j A_j (with
-// Q_{j+1} = P_j Q_j from j = 1), then A_{j+1} = P_j T and P_{j+1} (through a
-// square of A_{j+1} when its c != 0); Q_k = P_{k-1} Q_{k-1} closes the chain.
-int chain_ops(int k, const float *abc, ChainOp *ops) {
+// Q_{j+1} = P_j Q_j from j = 1: together when kH = 1, as a second product
+// when kH = 2), then A_{j+1} = P_j T and P_{j+1} (through a square of
+// A_{j+1} when its c != 0); Q_k = P_{k-1} Q_{k-1} closes the chain.
+int chain_ops(int kh, int k, const float *abc, ChainOp *ops) {
   int n = 0;
   for (int j = 0; j + 1 < k; ++j) {
-    ops[n++] = ChainOp{j == 0 ? kMmaPA : kMmaPAQ, j == 0 ? kEpiT : kEpiTQ, 0.f, 0.f, 0.f};
+    if (j == 0) {
+      ops[n++] = ChainOp{kMmaPA, kEpiT, 0.f, 0.f, 0.f};
+    } else if (kh == 1) {
+      ops[n++] = ChainOp{kMmaPAQ, kEpiTQ, 0.f, 0.f, 0.f};
+    } else {
+      ops[n++] = ChainOp{kMmaPA, kEpiT, 0.f, 0.f, 0.f};
+      ops[n++] = ChainOp{kMmaPQ, kEpiQ, 0.f, 0.f, 0.f};
+    }
     const float *t = abc + 3 * (j + 1);
     if (t[2] != 0.f) {
       ops[n++] = ChainOp{kMmaPA, kEpiA, 0.f, 0.f, 0.f};
@@ -426,23 +474,16 @@ int chain_ops(int k, const float *abc, ChainOp *ops) {
   return n;
 }
 
-}  // namespace
+int chain_halves(int p) { return p <= 128 ? 1 : 2; }
 
-double tc_chain_flops(int p, int k, const float *abc) {
-  std::vector<ChainOp> ops(kMaxOps);
-  const int n = chain_ops(k, abc, ops.data());
-  const double kdim = (double)((p + CK - 1) / CK) * CK;
-  double f = 0;
-  for (int j = 0; j < n; ++j) f += 2.0 * CM * (ops[j].mma == kMmaPAQ ? 2 * CM : CM) * kdim;
-  return f;
-}
-
-int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count,
-                       void *stream, int64_t *n_launch) {
+template <int kH>
+int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count, void *stream,
+                    int64_t *n_launch) {
+  using G = Geo<kH>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(ns_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCSmem);
+    attr_err = cudaFuncSetAttribute(ns_chain_kernel<kH>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::Smem);
   });
   if (attr_err != cudaSuccess) return (int)attr_err;
   for (int32_t j0 = 0; j0 < n_jobs; j0 += kMaxClassesPerLaunch) {
@@ -451,15 +492,16 @@ int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseAr
     T.n = std::min(kMaxClassesPerLaunch, n_jobs - j0);
     const GemmJob &J0 = *jobs[j0];
     if (J0.steps < 2 || J0.steps > GBO_MAX_NS_STEPS || !J0.abc) return (int)cudaErrorInvalidValue;
-    T.n_ops = chain_ops(J0.steps, J0.abc, T.ops);
+    T.n_ops = chain_ops(kH, J0.steps, J0.abc, T.ops);
     for (int k = 0; k < T.n; ++k) {
       const GemmJob &J = *jobs[j0 + k];
       const ShapeClass &C = *J.cls;
-      if (C.p > CM || J.steps != J0.steps || J.abc != J0.abc) return (int)cudaErrorInvalidValue;
+      if (chain_halves(C.p) != kH || C.p > G::R || J.steps != J0.steps || J.abc != J0.abc)
+        return (int)cudaErrorInvalidValue;
       auto at = [&](const void *region) { return static_cast<char *>(const_cast<void *>(region)) + C.p_base * 2; };
-      const bool ok = encode_map(&T.mapP[k], at(J.opA), C.p, C.p, C.count, C.ldp, CK, CM) &&
-                      encode_map(&T.mapA[k], at(J.opB), C.p, C.p, C.count, C.ldp, CK, CM) &&
-                      encode_map(&T.mapQ[k], at(J.out), C.p, C.p, C.count, C.ldp, CK, CM);
+      const bool ok = encode_map(&T.mapP[k], at(J.opA), C.p, C.p, C.count, C.ldp, CK, G::R) &&
+                      encode_map(&T.mapA[k], at(J.opB), C.p, C.p, C.count, C.ldp, CK, G::R) &&
+                      encode_map(&T.mapQ[k], at(J.out), C.p, C.p, C.count, C.ldp, CK, G::R);
       if (!ok) return (int)cudaErrorInvalidValue;
       T.p[k] = C.p;
       T.mat_start[k + 1] = T.mat_start[k] + C.count;
@@ -467,13 +509,38 @@ int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseAr
     const int64_t total = T.mat_start[T.n];
     if (total == 0) continue;
     const unsigned grid = (unsigned)std::min<int64_t>(total, sm_count);  // one CTA per SM
-    ns_chain_kernel<<<grid, kCThreads, kCSmem, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
+    ns_chain_kernel<kH><<<grid, kCThreads, G::Smem, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
     count_launches(1);
     if (n_launch) ++*n_launch;
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return (int)err;
   }
   return 0;
+}
+
+}  // namespace
+
+double tc_chain_flops(int p, int k, const float *abc) {
+  const int kh = chain_halves(p);
+  const int n_cols = kh == 1 ? 128 : 192;
+  std::vector<ChainOp> ops(kMaxOps);
+  const int n = chain_ops(kh, k, abc, ops.data());
+  const double kdim = (double)((p + CK - 1) / CK) * CK;
+  double f = 0;
+  for (int j = 0; j < n; ++j) f += kh * 2.0 * 128 * (ops[j].mma == kMmaPAQ ? 2 * n_cols : n_cols) * kdim;
+  return f;
+}
+
+int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count,
+                       void *stream, int64_t *n_launch) {
+  std::vector<const GemmJob *> one, two;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    if (jobs[j]->cls->p > kChainMaxP) return (int)cudaErrorInvalidValue;
+    (chain_halves(jobs[j]->cls->p) == 1 ? one : two).push_back(jobs[j]);
+  }
+  const int err = launch_geometry<1>(one.data(), (int32_t)one.size(), args, sm_count, stream, n_launch);
+  if (err) return err;
+  return launch_geometry<2>(two.data(), (int32_t)two.size(), args, sm_count, stream, n_launch);
 }
 
 }  // namespace gbo

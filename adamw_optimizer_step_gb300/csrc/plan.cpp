@@ -165,10 +165,10 @@ int squares(const gbo_plan *P) {
   return n;
 }
 
-// Gram-route classes of at most 128 rows run their p x p iterations in the
-// on-chip chain kernel (bf16 mode).
+// Gram-route classes of at most kChainMaxP rows run their p x p iterations
+// in the on-chip chain kernel (bf16 mode).
 bool uses_chain(const gbo_plan *P, const ShapeClass &C) {
-  return P->small_chain && P->x_dtype == GBO_BF16 && C.route == kRouteGram && single_mode(C.p) &&
+  return P->small_chain && P->x_dtype == GBO_BF16 && C.route == kRouteGram && C.p <= kChainMaxP &&
          P->opts.ns_steps >= 2;
 }
 

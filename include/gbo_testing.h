@@ -25,7 +25,7 @@ int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_
 
 /*
  * Whether Muon plans created from now on (any thread) run the Gram route's
- * p x p iterations of matrices with p <= 128 in bf16 mode as one on-chip
+ * p x p iterations of matrices with p <= 192 in bf16 mode as one on-chip
  * chain launch (enable != 0, the default) or as one tensor-core launch per
  * product with every p x p result stored in the workspace (enable == 0).
  * Both round and mirror every p x p result the same way; tests compare them.

@@ -207,11 +207,11 @@ def test_flop_count_and_launches(L):
 
 
 def test_small_chain_counts(L):
-    """Gram-route matrices of at most 128 rows (bf16) run their p x p
+    """Gram-route matrices of at most 192 rows (bf16) run their p x p
     iterations in one on-chip launch: the Gram, the chain, the product with
-    X_0.  Each op of the chain is one 128 x 128 tile (128 x 256 when T and Q
-    are formed together) with K padded to 64; with the chain switched off
-    every p x p product is a tile-kernel launch of its own."""
+    X_0.  For p <= 128 each op of the chain is one 128 x 128 tile (128 x 256
+    when T and Q are formed together) with K padded to 64; with the chain
+    switched off every p x p product is a tile-kernel launch of its own."""
     d = lambda: [desc(0, 4 * 96, 1000, (4, 96, 1000))]  # four 96 x 1000 matrices: p = 96, q = 1000
     tile = 2 * 128 * 256            # one single-CTA tile of the tile kernel, per unit of K
     gram, prod, sym = tile * 1024, 4 * tile * 128, tile * 128
@@ -230,8 +230,21 @@ def test_small_chain_counts(L):
     assert i.launches_per_step == 2 + 4
     assert i.ns_flops_executed == 4 * (gram + sym + quintic_chain + prod)
     L.gbo_muon_plan_destroy(plan)
-    # the fp32 mode and classes on CTA pairs keep one launch per product
+    # 128 < p <= 192: two 128-row halves with N = 192, T and Q as separate
+    # products: T, A_1/P_1, 3 x (T, Q, A/P), Q_5; the Gram and the product
+    # with X_0 run on CTA pairs (256 x 256 tiles, K padded to 128)
+    rc, plan = create(L, [desc(0, 2 * 192, 1536, (2, 192, 1536))], route=B.GBO_ROUTE_GRAM)
+    i = info(L, plan)
+    pair = 2 * 256 * 256
+    chain192 = 12 * 2 * (2 * 128 * 192 * 192)
+    assert i.launches_per_step == 2 + 3
+    assert i.ns_flops_executed == 2 * (pair * 1536 + chain192 + 6 * pair * 256)
+    L.gbo_muon_plan_destroy(plan)
+    # the fp32 mode and larger p keep one launch per product
     rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM, precision=B.GBO_NS_F32)
+    assert info(L, plan).launches_per_step == 2 + 11
+    L.gbo_muon_plan_destroy(plan)
+    rc, plan = create(L, [desc(0, 200, 1536)], route=B.GBO_ROUTE_GRAM)
     assert info(L, plan).launches_per_step == 2 + 11
     L.gbo_muon_plan_destroy(plan)
     prev = L.gbo_testing_set_small_chain(0)

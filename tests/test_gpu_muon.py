@@ -146,7 +146,9 @@ def test_routes_with_square(route, precision, abc):
 
 
 SMALL = [(4 * 96, 1000, (4, 96, 1000), None), (300, 100, None, None), (40, 300, None, None),
-         (128, 512, None, None), (640, 192, (2, 5, 64, 192), (20, 44))]
+         (128, 512, None, None), (640, 192, (2, 5, 64, 192), (20, 44)),
+         (2 * 192, 1536, (2, 192, 1536), None), (700, 150, None, None), (129, 600, None, None),
+         (2 * 160, 900, (2, 160, 900), None)]
 
 
 @pytest.mark.parametrize("abc,ns_steps", [
@@ -156,7 +158,8 @@ SMALL = [(4 * 96, 1000, (4, 96, 1000), None), (300, 100, None, None), (40, 300, 
 def test_small_chain_matches_launches(abc, ns_steps):
     """Matrices of at most 128 rows on the Gram route: the on-chip chain
     (one launch for all p x p products) against one launch per product, for
-    p = 20 .. 128, wide and tall, c == 0 and c != 0, k = 2 .. 5.  The two
+    p = 20 .. 192 (one and two 128-row halves), wide and tall, c == 0 and
+    c != 0, k = 2 .. 5.  The two
     round every p x p result to bf16 once; the launches mirror symmetric
     results from their upper triangle and the chain writes them whole, so
     they agree to bf16 rounding (1e-2 relative per weight, ten times inside
