@@ -428,7 +428,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
                                     ? static_cast<const CUtensorMap *>(A.wmaps) + S.wmap
                                     : nullptr;
       const bool wtma = wmap != nullptr && i0 + 32 <= rows;
-      if (wtma) weight_loads_begin(wmap, stage, wbar0, tc.tn * BN, cols, (int)(S.r0 + i0), lane, winfl);
+      if (wtma) weight_loads_begin<!kPair>(wmap, stage, wbar0, tc.tn * BN, cols, (int)(S.r0 + i0), lane, winfl);
       else if (J.mode == kFinal) prefetch_weight_tile(S, i0, tc.tn * BN, rows, cols, lane);
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
       tc_fence_after();
@@ -436,7 +436,8 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (i0 < rows) {  // warps whose rows are all padding have nothing to write
         if (wtma) {
-          if (!final_tile_bf16_tma(A, S, s, i0, tc.tn * BN, cols, trow, lane, wmap, stage, wbar0, wpar, winfl)) {
+          if (!final_tile_bf16_tma<!kPair>(A, S, s, i0, tc.tn * BN, cols, trow, lane, wmap, stage, wbar0, wpar,
+                                            winfl)) {
             give_up();
             break;
           }

@@ -530,9 +530,12 @@ __device__ __forceinline__ int weight_chunks(int tile_col0, int cols) {
   return min(BN / 32, (cols - tile_col0 + 31) / 32);
 }
 
+// kTwo: the tile's chunks are updated in pairs (final_tile_bf16_tma), and
+// the first two pairs are loaded here.
+template <bool kTwo>
 __device__ __forceinline__ void weight_loads_begin(const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
                                                    int tile_col0, int cols, int row0, int lane, uint32_t &winfl) {
-  const int n0 = min(kWAhead, weight_chunks(tile_col0, cols));
+  const int n0 = min(kTwo ? kWBufs : kWAhead, weight_chunks(tile_col0, cols));
   if (lane == 0) {
     bulk_wait_read<0>();  // earlier stores from the staging area have read it
     for (int c = 0; c < n0; ++c) weight_load_chunk(wmap, stage, wbar0, c, tile_col0 + 32 * c, row0);
@@ -559,13 +562,18 @@ __device__ __forceinline__ void stage_read_row(uint32_t src, float (&o)[32], int
   }
 }
 
-// Returns false on a time-out of a load wait.
-__device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const DevSub &S, float s, int i0,
+// One chunk at a time, loads kWAhead chunks ahead.  Returns false on a
+// time-out of a load wait.
+__device__ __forceinline__ bool final_tile_bf16_tma_one(const PhaseArgs &A, const DevSub &S, float s, int i0,
                                                     int tile_col0, int cols, uint32_t trow, int lane,
                                                     const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
                                                     uint32_t &wpar, uint32_t &winfl) {
   const int nch = weight_chunks(tile_col0, cols);
   const float lr = A.lr * S.lr_mult, su = S.scale * s;
+  // W - lr (wd W + su C) as one multiply-add per element: decay factor and
+  // update factor folded (the same result up to one fp32 rounding)
+  const float keep = 1.0f - lr * S.wd, step = lr * su;
+  const bool decay = S.wd != 0.f;
   const int row0 = (int)(S.r0 + i0);
   const int64_t wrow = (S.r0 + i0 + lane) * S.cols;
 #pragma unroll 1
@@ -580,10 +588,12 @@ __device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const De
     winfl &= ~(1u << b);
     float w[32];
     stage_read_row(buf, w, lane);
+    if (decay) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      u[k] *= su;
-      w[k] = w[k] - lr * (S.wd * w[k] + u[k]);
+      for (int k = 0; k < 32; ++k) w[k] = fmaf(-step, u[k], keep * w[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) w[k] = fmaf(-step, u[k], w[k]);
     }
     stage_rows(buf, w, lane);
     fence_async_smem();
@@ -601,6 +611,8 @@ __device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const De
     }
     if (more) winfl |= 1u << ((ch + kWAhead) & (kWBufs - 1));
     if (A.dbg) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) u[k] *= su;
       const uint32_t mask = prefix_mask(cols - col0);
       float *d = A.dbg + S.dbg_off + wrow + col0;
       store_row32(d, u, mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0, mask);
@@ -609,6 +621,98 @@ __device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const De
   if (lane == 0) bulk_wait_read<0>();  // the staging area is free for the other epilogues
   __syncwarp();
   return true;
+}
+
+// Chunks in pairs (chunks 2j, 2j + 1 in buffers 2j % 4, 2j % 4 + 1): one
+// fence, one commit and one read-wait per pair; the next pair is loaded
+// into the buffers of the previous one.  Its two accumulator chunks take 64
+// more registers, which the single-CTA kernel (HBM-bound last products on
+// small matrices) can spare: measured 3.77 -> 3.63 ms on the MLA/KDA set,
+// while the CTA-pair kernel ran its other launches about 1% slower with
+// them.  Returns false on a time-out of a load wait.
+__device__ __forceinline__ bool final_tile_bf16_tma_two(const PhaseArgs &A, const DevSub &S, float s, int i0,
+                                                    int tile_col0, int cols, uint32_t trow, int lane,
+                                                    const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
+                                                    uint32_t &wpar, uint32_t &winfl) {
+  const int nch = weight_chunks(tile_col0, cols);
+  const float lr = A.lr * S.lr_mult, su = S.scale * s;
+  const float keep = 1.0f - lr * S.wd, step = lr * su;
+  const bool decay = S.wd != 0.f;
+  const int row0 = (int)(S.r0 + i0);
+  const int64_t wrow = (S.r0 + i0 + lane) * S.cols;
+#pragma unroll 1
+  for (int c0 = 0; c0 < nch; c0 += 2) {
+    const bool two = c0 + 1 < nch;
+    if (c0 >= 2 && c0 + 2 < nch) {
+      // the next pair goes into the buffers of the previous one, whose
+      // stores are the latest group
+      if (lane == 0) {
+        bulk_wait_read<0>();
+        weight_load_chunk(wmap, stage, wbar0, c0 + 2, tile_col0 + 32 * (c0 + 2), row0);
+        if (c0 + 3 < nch) weight_load_chunk(wmap, stage, wbar0, c0 + 3, tile_col0 + 32 * (c0 + 3), row0);
+      }
+      winfl |= 1u << ((c0 + 2) & (kWBufs - 1));
+      if (c0 + 3 < nch) winfl |= 1u << ((c0 + 3) & (kWBufs - 1));
+    }
+    float u0[32], u1[32];
+    tmem_ld32(trow + c0 * 32, u0);
+    if (two) tmem_ld32(trow + (c0 + 1) * 32, u1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (h == 1 && !two) break;
+      const int ch = c0 + h;
+      const uint32_t b = (uint32_t)(ch & (kWBufs - 1));
+      const uint32_t buf = stage + b * kWBufBytes;
+      if (!mbar_wait(wbar0 + 8 * b, (wpar >> b) & 1u)) return false;
+      wpar ^= 1u << b;
+      winfl &= ~(1u << b);
+      float (&u)[32] = h == 0 ? u0 : u1;
+      float w[32];
+      stage_read_row(buf, w, lane);
+      if (decay) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w[k] = fmaf(-step, u[k], keep * w[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w[k] = fmaf(-step, u[k], w[k]);
+      }
+      stage_rows(buf, w, lane);
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(wmap, stage + (uint32_t)(c0 & (kWBufs - 1)) * kWBufBytes, tile_col0 + 32 * c0, row0, 0);
+      if (two) tma_store_3d(wmap, stage + (uint32_t)((c0 + 1) & (kWBufs - 1)) * kWBufBytes, tile_col0 + 32 * (c0 + 1), row0, 0);
+      bulk_commit();
+    }
+    if (A.dbg) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !two) break;
+        float (&u)[32] = h == 0 ? u0 : u1;
+        const int col0 = tile_col0 + 32 * (c0 + h);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) u[k] *= su;
+        const uint32_t mask = prefix_mask(cols - col0);
+        float *d = A.dbg + S.dbg_off + wrow + col0;
+        store_row32(d, u, mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0, mask);
+      }
+    }
+  }
+  if (lane == 0) bulk_wait_read<0>();  // the staging area is free for the other epilogues
+  __syncwarp();
+  return true;
+}
+
+template <bool kTwo>
+__device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const DevSub &S, float s, int i0,
+                                                    int tile_col0, int cols, uint32_t trow, int lane,
+                                                    const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
+                                                    uint32_t &wpar, uint32_t &winfl) {
+  if constexpr (kTwo)
+    return final_tile_bf16_tma_two(A, S, s, i0, tile_col0, cols, trow, lane, wmap, stage, wbar0, wpar, winfl);
+  else
+    return final_tile_bf16_tma_one(A, S, s, i0, tile_col0, cols, trow, lane, wmap, stage, wbar0, wpar, winfl);
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *p) {
