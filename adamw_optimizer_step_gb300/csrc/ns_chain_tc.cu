@@ -21,7 +21,8 @@
 // Two geometries (template parameter kH, 128-row halves of a matrix):
 //   kH = 1  p <= 128: 128 x 128 matrices (32 KB each), two matrices in
 //           flight per CTA so the epilogue of one slot's product overlaps
-//           the other slot's MMAs; T and Q_{j+1} form together (N = 256)
+//           the other slot's MMAs; T and Q_{j+1} are one op (two N = 128
+//           accumulators side by side)
 //   kH = 2  128 < p <= 192: 192 x 192 matrices (72 KB each), one matrix per
 //           CTA; each product is two M = 128 row halves with N = 192, and
 //           T and Q_{j+1} are separate products (their accumulators would
