@@ -399,9 +399,11 @@ def run_ours(args):
     t_wall0 = time.time()
     l0 = gbo.gbo_launch_count()
     start, end = ev(), ev()
+    marks = [ev() for _ in range(args.steps)]  # after each step: per-step times
     start.record(stream)
     for k in range(args.steps):
         step(adam_ev[k])
+        marks[k].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -410,6 +412,7 @@ def run_ours(args):
     phases = gbo.gbo_muon_plan_phase_times(plan)
     gbo.gbo_muon_plan_set_timing(plan, False)
     elapsed = start.elapsed_time(end) / 1e3
+    step_ms = sorted((marks[k - 1] if k else start).elapsed_time(marks[k]) for k in range(args.steps))
     elapsed_max = max_over_ranks(elapsed, world)
     adam_ms = sum(a.elapsed_time(b) for a, b in adam_ev) / args.steps
     value = aggregate(args.steps, elapsed_max, world)
@@ -468,6 +471,15 @@ def run_ours(args):
                "sample": desc}
     hbm = peaks.get("hbm_gbs", 6800.0)
     adam_bytes = 32.0 * n_adam
+    # The step's floor: the executed tensor FLOPs at the tensor peak, or the
+    # algorithmic bytes at HBM bandwidth, whichever is longer (perfect overlap
+    # of the two).  Bytes: per Muon parameter G read, B read and written, W
+    # read and written; per AdamW parameter 32 B.
+    w_es = torch.empty(0, dtype=wl.w_dtype).element_size()
+    g_es = torch.empty(0, dtype=wl.g_dtype).element_size()
+    floor_bytes = (g_es + 8 + 2 * w_es) * wl.muon_params + adam_bytes
+    floor_tensor_ms = flops / (peak_tf * 1e12) * 1e3
+    floor_hbm_ms = floor_bytes / (hbm * 1e9) * 1e3
     out = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -485,6 +497,11 @@ def run_ours(args):
                      "peak_source": peak_src, "traffic": traffic,
                      "flops_per_launch": flops / gemm_launches, "ms_per_launch": gemm_ms / gemm_launches},
         "phases_ms_per_step": {k: v[0] / args.steps for k, v in phases.items()},
+        "step_ms": {"median": step_ms[len(step_ms) // 2], "min": step_ms[0], "max": step_ms[-1]},
+        "step_floor": {"ms": max(floor_tensor_ms, floor_hbm_ms), "frac": max(floor_tensor_ms, floor_hbm_ms) / ms_step,
+                       "tensor_ms": floor_tensor_ms, "hbm_ms": floor_hbm_ms, "bytes_per_step": floor_bytes,
+                       "basis": "max(executed NS FLOPs / tensor peak, (G + B + W Muon traffic + 32 B per AdamW "
+                                "parameter) / HBM copy bandwidth)"},
         "adamw_clip": {"ms": adam_ms, "GB/s": adam_bytes / (adam_ms / 1e3) / 1e9,
                        "frac_of_hbm": adam_bytes / (adam_ms / 1e3) / 1e9 / hbm,
                        "stream": "side stream, overlapped with the Muon GEMMs" if overlap else "main stream"},
