@@ -135,7 +135,7 @@ __device__ __forceinline__ void adam_elem(float &p, float g, float &m, float &v,
 }
 
 #ifndef GBO_ADAM_MIN_BLOCKS
-#define GBO_ADAM_MIN_BLOCKS 1  // compiler choice (58 regs, 4 blocks/SM): measured faster than forcing 5 or 6
+#define GBO_ADAM_MIN_BLOCKS 1  // compiler choice (80 regs, 3 blocks/SM): forcing 4 measured 1.39 ms against 1.26
 #endif
 __global__ void __launch_bounds__(kThreads, GBO_ADAM_MIN_BLOCKS)
 adamw_kernel(const __grid_constant__ AdamTable T, const __grid_constant__ AdamScalars s0,
