@@ -30,6 +30,7 @@ struct DevSub {
   int64_t dbg_off;  // element offset of the weight's first element in dbg_update
   int64_t tile0;    // first momentum tile of this matrix (global tile index)
   int64_t rb0;      // first NorMuon row block of this matrix
+  int64_t ss_off;   // NorMuon (bf16 mode): first of this matrix's m x ss_ntn row-statistics partials
   int32_t m, n;     // stored rows, cols
   int32_t p, q;     // oriented rows, cols
   int32_t ld;       // X row stride (elements)
@@ -48,7 +49,7 @@ struct DevSub {
   int32_t w_vec;    // weight rows start on 16-byte boundaries (vector read-modify-write)
   int32_t x_sel;    // X buffer (0 or 1) that holds the last iterate (NorMuon rows read it)
   int32_t wmap;     // index of the weight's TMA map (bf16 weights with 16-byte rows), or -1
-  int32_t pad2;
+  int32_t ss_ntn;   // NorMuon (bf16 mode): partials per stored row, one per 256-column output tile
 };
 
 // Matrices of one oriented shape (p, q), stored back to back in the
@@ -127,7 +128,8 @@ struct GemmJob {
   float a, b, c;
   const void *opA, *opB;
   void *out, *out2;  // out: P, A, T, Q or X'; out2: A of kGramAP
-  const void *aux;   // kSquare: the A matrix read by the epilogue
+  const void *aux;   // kSquare: the A matrix read by the epilogue; kProduct: NorMuon
+                     // row-statistics partials (fp32) when this is the last product
   int32_t steps;     // kChain: iterations k and their coefficients (3 per iteration)
   const float *abc;
 };
@@ -153,10 +155,12 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
 // NorMuon rows; with rms_target > 0 a statistics pass, the per-matrix
 // RMS-keeping scale and a write pass (rowf: n_row_blocks * kRowBlock floats,
 // rowpart: n_row_blocks, mscale: n_subs), else one fused pass.
+// rowss: the last product's per-(row, 256-column tile) sums of squares of
+// X_k (bf16 mode), or nullptr to take the statistics from X_k itself.
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
                         int32_t *status, float rms_target, float *rowf, float *rowpart, float *mscale,
-                        int sm_count, void *stream);
+                        const float *rowss, int sm_count, void *stream);
 int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
                                  int32_t w_dtype, float beta2, float eps, float scale, float lr,
                                  float wd, float *dbg, void *stream);

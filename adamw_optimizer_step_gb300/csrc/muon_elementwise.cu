@@ -270,9 +270,12 @@ __device__ __forceinline__ void weight_rmw8(const DevSub &S, int64_t widx, int v
 // update) is read from the workspace.  Row statistics, v update, then the
 // weight write, with 16-byte accesses throughout.
 //   untransposed: warp w takes stored rows w, w + 8, ... of the block; a
-//     row is X's row, read twice (statistics, then the write), two 256-element
-//     segments per step with every load issued before the stores (two
-//     segments kept 64 registers; four took 119 and were slower)
+//     row is X's row.  Its statistics come from the last product's partial
+//     sums of squares (rowss, bf16 mode: one per 256-column tile of the
+//     row, summed in a fixed order), or from a first read of the row; the
+//     write reads it (again), two 256-element segments per step with every
+//     load issued before the stores (two segments kept 64 registers; four
+//     took 119 and were slower)
 //   transposed (fp32 mode): stored row i is column i of X; the block reads
 //     32 x 64 tiles of X (8 threads per 64-column row segment), keeps
 //     per-column sums, then transposes tiles through shared memory for the
@@ -288,7 +291,8 @@ __global__ void __launch_bounds__(256)
 normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_blocks,
                     const XT *__restrict__ xbuf0, const XT *__restrict__ xbuf1, float beta2, float eps, float lr,
                     float *__restrict__ dbg, int32_t *status, float *__restrict__ rowf,
-                    float *__restrict__ rowpart, const float *__restrict__ mscale) {
+                    float *__restrict__ rowpart, const float *__restrict__ mscale,
+                    const float *__restrict__ rowss) {
   __shared__ float tileT[32][kRowBlock + 1];
   __shared__ float colsum[32][kRowBlock + 1];
   __shared__ float rfac[kRowBlock];
@@ -312,7 +316,11 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
         float f;
         if constexpr (kMode != 2) {
           float ss = 0.f;
-          int j = lane * 8;
+          int j = rowss ? S.n : lane * 8;  // with the partials, X is not read here
+          if (rowss) {
+            const float *part = rowss + S.ss_off + (int64_t)row * S.ss_ntn;
+            for (int t = lane; t < S.ss_ntn; t += 32) ss += part[t];
+          }
           for (; j + 1 * 256 + 8 <= S.n; j += 2 * 256) {  // two whole segments: loads first
             float o[2][8];
 #pragma unroll
@@ -561,7 +569,7 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
                         int32_t *status, float rms_target, float *rowf, float *rowpart, float *mscale,
-                        int sm_count, void *stream) {
+                        const float *rowss, int sm_count, void *stream) {
   if (n_row_blocks == 0) return 0;
   const int64_t grid = std::min<int64_t>(n_row_blocks, (int64_t)sm_count * 8);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -570,11 +578,11 @@ int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks
     if (x_dtype == GBO_BF16)
       normuon_rows_kernel<__nv_bfloat16, kMode><<<(unsigned)grid, 256, 0, st>>>(
           subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x0),
-          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf, rowpart, mscale);
+          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf, rowpart, mscale, rowss);
     else
       normuon_rows_kernel<float, kMode><<<(unsigned)grid, 256, 0, st>>>(
           subs, n_subs, n_row_blocks, reinterpret_cast<const float *>(x0), reinterpret_cast<const float *>(x1),
-          beta2, eps, lr, dbg, status, rowf, rowpart, mscale);
+          beta2, eps, lr, dbg, status, rowf, rowpart, mscale, nullptr);
     count_launches(1);
   };
   if (rms_target > 0.f) {

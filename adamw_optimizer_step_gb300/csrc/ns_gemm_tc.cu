@@ -444,6 +444,10 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
         } else if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
           final_tile_bf16(A, S, s, i0, tc.tn * BN, rows, cols, trow, lane);
         } else {
+          // the NorMuon last product also leaves each row's sum of squares of
+          // the bf16 values it stores, one partial per 256-column tile
+          const bool stats = J.mode == kProduct && J.aux != nullptr;
+          float rss = 0.f;
 #pragma unroll 1
           for (int ch = 0; ch < BN / 32; ++ch) {
             const int col0 = tc.tn * BN + ch * 32;
@@ -451,7 +455,16 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
             float v[32];
             tmem_ld32(trow + ch * 32, v);
             epilogue_block(P, A, tc.c, tc.mat, S, s, i0, col0, v, stage, slot, lane);
+            if (stats) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const float r = __bfloat162float(__float2bfloat16_rn(s * v[k]));
+                rss = fmaf(r, r, rss);
+              }
+            }
           }
+          if (stats && i0 + lane < rows)
+            static_cast<float *>(const_cast<void *>(J.aux))[S.ss_off + (int64_t)(i0 + lane) * S.ss_ntn + tc.tn] = rss;
         }
       }
       tc_fence_before();

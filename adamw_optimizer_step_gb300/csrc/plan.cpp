@@ -137,6 +137,8 @@ struct gbo_plan {
   size_t off_g[6] = {0, 0, 0, 0, 0, 0};
   // NorMuon RMS-keeping scale: per-row factors, row-block partials, per-matrix scales
   size_t off_rowf = 0, off_rowpart = 0, off_mscale = 0;
+  // NorMuon, bf16 mode: the last product's row-statistics partials
+  size_t off_rowss = 0;
   uint64_t hash = 0;
   gbo_plan_info info{};
   // device state, set by the first step
@@ -384,6 +386,14 @@ int validate_and_expand(gbo_plan *P) {
   }
   P->n_tiles = tiles;
   P->n_row_blocks = rbs;
+  // NorMuon row statistics from the last product (bf16 mode): per stored row
+  // of each matrix, one partial per 256-column tile of its output
+  int64_t rowss = 0;
+  for (DevSub &S : subs) {
+    S.ss_ntn = (S.n + 255) / 256;
+    S.ss_off = rowss;
+    if (o.normuon && tc_path) rowss += (int64_t)S.m * S.ss_ntn;
+  }
   P->subs = std::move(subs);
   // workspace layout
   size_t off = 0;
@@ -408,6 +418,7 @@ int validate_and_expand(gbo_plan *P) {
   P->off_rowf = region(rms ? (size_t)rbs * kRowBlock * sizeof(float) : 0);
   P->off_rowpart = region(rms ? (size_t)rbs * sizeof(float) : 0);
   P->off_mscale = region(rms ? P->subs.size() * sizeof(float) : 0);
+  P->off_rowss = region((size_t)rowss * sizeof(float));
   P->ws_bytes = off;
   // info
   gbo_plan_info &I = P->info;
@@ -481,6 +492,12 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
   void *gQ[2] = {R(P->off_g[4]), R(P->off_g[5])};
   void *xt[2] = {R(P->off_xt[0]), R(P->off_xt[1])};
   const bool f32 = P->x_dtype == GBO_F32;
+  // the NorMuon last product's row-statistics partials (bf16 mode)
+  void *rowss = (normuon && !f32) ? R(P->off_rowss) : nullptr;
+  auto last_product = [&](GemmJob J) {
+    if (J.mode == kProduct) J.aux = rowss;
+    return J;
+  };
   auto job = [](const ShapeClass *C, int mode, int kind, int first, const float *abc, const void *opA,
                 const void *opB, void *out, void *out2 = nullptr, const void *aux = nullptr) {
     GemmJob J{};
@@ -532,7 +549,8 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
         }
         const bool last = it == k - 1;
         const int mode = (last && !normuon) ? kFinal : kProduct;
-        at(xs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct).jobs.push_back(product(mode, first, abc, pb, cur));
+        const GemmJob pj = product(mode, first, abc, pb, cur);
+        at(xs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct).jobs.push_back(last ? last_product(pj) : pj);
         cur ^= 1;
       }
     } else {
@@ -551,7 +569,8 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
         J.abc = P->abc.data();
         at(gs, i++, kPhaseProduct).jobs.push_back(J);
         const int mode = normuon ? kProduct : kFinal;
-        at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct).jobs.push_back(product(mode, 1, nullptr, gQ[k & 1], 0));
+        at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
+            .jobs.push_back(last_product(product(mode, 1, nullptr, gQ[k & 1], 0)));
         continue;
       }
       for (int j = 0; j + 1 < k; ++j) {
@@ -577,7 +596,8 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
           .jobs.push_back(job(&C, kGramA, kKindSym, 0, nullptr, gP[(k - 1) & 1], k == 2 ? gP[0] : gQ[(k - 1) & 1],
                               gQ[k & 1]));
       const int mode = normuon ? kProduct : kFinal;
-      at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct).jobs.push_back(product(mode, 1, nullptr, gQ[k & 1], 0));
+      at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
+          .jobs.push_back(last_product(product(mode, 1, nullptr, gQ[k & 1], 0)));
     }
   }
   std::vector<TcStep> steps(std::max(xs.size(), gs.size()));
@@ -828,7 +848,9 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
                               P->opts.eps, lr, dbg_update, dev_status, P->opts.rms_target,
                               reinterpret_cast<float *>(ws + P->off_rowf),
                               reinterpret_cast<float *>(ws + P->off_rowpart),
-                              reinterpret_cast<float *>(ws + P->off_mscale), P->sm_count, st);
+                              reinterpret_cast<float *>(ws + P->off_mscale),
+                              P->x_dtype == GBO_BF16 ? reinterpret_cast<const float *>(ws + P->off_rowss) : nullptr,
+                              P->sm_count, st);
     if (err) return cuda_fail(err, "NorMuon rows kernel");
     mark(kPhaseRows, P->opts.rms_target > 0.f ? 3 : 1);
   }
