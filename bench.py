@@ -243,15 +243,19 @@ def traffic_record(kernel_files):
     return rec
 
 
-def run_e2e(n_steps, world, bufs, step, total):
+def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     """Steps/s with each step's gradients copied in from pinned host memory
     and the step's gradient norm read back on the host.  ``bufs`` holds two
     (Muon, AdamW) flat gradient buffer pairs, each bound to its own plan:
     the upload of step n + 1's gradients runs on a copy stream into one pair
     while step n computes on the other, as a trainer overlaps its input
-    transfers.  Every step's copy and read stay inside the timed region.
-    Returns (steps/s over all ranks, bytes copied in per step, the upload's
-    GB/s when it runs alone)."""
+    transfers.  The upload starts once step n's momentum pass is done
+    (``after_momentum[b]``, recorded by buffer pair b's plan), so it runs
+    under the Newton-Schulz GEMMs, which leave most of the HBM bandwidth
+    free, rather than under the memory-bound momentum pass.  Every step's
+    copy and read stay inside the timed region.  Returns (steps/s over all
+    ranks, bytes copied in per step, the upload's GB/s when it runs
+    alone)."""
     import torch
     g_flat, ag_flat = bufs[0]
     h_g = torch.empty(g_flat.numel(), dtype=g_flat.dtype, pin_memory=True)
@@ -263,8 +267,10 @@ def run_e2e(n_steps, world, bufs, step, total):
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def upload(b):
+    def upload(b, after=None):
         copy.wait_event(done[b])  # the step that last read buffer pair b has finished
+        if after is not None:
+            copy.wait_event(after)
         with torch.cuda.stream(copy):
             bufs[b][0].copy_(h_g, non_blocking=True)
             bufs[b][1].copy_(h_ag, non_blocking=True)
@@ -288,7 +294,7 @@ def run_e2e(n_steps, world, bufs, step, total):
         step(buf=b)
         done[b].record(compute)
         if n + 1 < n_steps:
-            upload(1 - b)
+            upload(1 - b, after_momentum[b])
         _ = float(total.item())  # the step's result on the host
     torch.cuda.synchronize()
     e2e_t = max_over_ranks(time.perf_counter() - t0, world)
@@ -353,9 +359,9 @@ def run_ours(args):
     step_no = [0]
     overlap = args.overlap
 
-    after_momentum = torch.cuda.Event()
-    if overlap:
-        gbo.gbo_muon_plan_set_event(plan, 0, after_momentum)
+    # recorded by each buffer pair's plan right after its momentum pass
+    after_momentum = [torch.cuda.Event(), torch.cuda.Event()]
+    gbo.gbo_muon_plan_set_event(plan, 0, after_momentum[0])
 
     def step(record=None, buf=0):
         """One optimizer step: Muon, then clip + AdamW, on one stream.  With
@@ -371,7 +377,7 @@ def run_ours(args):
         gbo.gbo_muon_step(plan_b, wl.lr, ws, dev_status=status, stream=stream)
         adam_stream = side if overlap else stream
         if overlap:
-            side.wait_event(after_momentum)
+            side.wait_event(after_momentum[buf])
         if record is not None:
             record[0].record(adam_stream)
         gbo.gbo_clip_norm(adam_grads, 1.0, total, coef, cws, dev_status=status, stream=adam_stream)
@@ -434,7 +440,9 @@ def run_ours(args):
             off += g.numel()
         plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon)
         bound.append((plan2, params2, [p[1] for p in params2]))
-        e2e_value, h2d, up_gbs = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total)
+        gbo.gbo_muon_plan_set_event(plan2, 0, after_momentum[1])
+        e2e_value, h2d, up_gbs = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step,
+                                         total, after_momentum)
 
     if rank != 0:
         return
