@@ -175,8 +175,10 @@ bool uses_chain(const gbo_plan *P, const ShapeClass &C) {
 }
 
 // Route of a p x q class: the Gram route needs k >= 2; AUTO takes it when it
-// executes at least 10% fewer FLOPs (in practice: whenever q is clearly
-// above p).
+// executes at least 10% fewer FLOPs, counting the on-chip chain where the
+// class would run it (in practice: whenever q is clearly above p, and for
+// every matrix of at most kChainMaxP rows in bf16 mode, where the chain also
+// replaces 2k launches by three).
 int32_t choose_route(const gbo_plan *P, int p, int q, bool tall) {
   const int k = P->opts.ns_steps;
   if (k < 2 || P->opts.route == GBO_ROUTE_X) return kRouteX;
@@ -184,7 +186,10 @@ int32_t choose_route(const gbo_plan *P, int p, int q, bool tall) {
   const bool x_tall = P->x_dtype == GBO_BF16 && tall;
   double fx = 0;
   for (int it = 0; it < k; ++it) fx += tc_executed_flops(p, q, P->abc[3 * it + 2] != 0.f, x_tall);
-  return tc_gram_route_flops(p, q, k, squares(P), x_tall) < 0.9 * fx ? kRouteGram : kRouteX;
+  const bool chain = P->small_chain && P->x_dtype == GBO_BF16 && p <= kChainMaxP;
+  const double fg = chain ? tc_gram_chain_flops(p, q, k, P->abc.data(), x_tall)
+                          : tc_gram_route_flops(p, q, k, squares(P), x_tall);
+  return fg < 0.9 * fx ? kRouteGram : kRouteX;
 }
 
 int validate_and_expand(gbo_plan *P) {

@@ -201,9 +201,18 @@ def test_flop_count_and_launches(L):
     assert rc == 0 and info(L, plan).n_gram_route == 3 and info(L, plan).launches_per_step == 2 + 11
     L.gbo_muon_plan_destroy(plan)
     assert create(L, descs(), route=3)[0] == -1
-    rc, plan = create(L, [desc(0, 64, 64)], abc=(15 / 8, -5 / 4, 3 / 8))
+    rc, plan = create(L, [desc(0, 64, 64)], abc=(15 / 8, -5 / 4, 3 / 8), route=B.GBO_ROUTE_X)
     assert info(L, plan).launches_per_step == 2 + 5 * 3
     L.gbo_muon_plan_destroy(plan)
+    # a matrix of at most 192 rows takes the Gram route with the on-chip
+    # chain automatically, square or not: Gram (+ square of A_0), chain,
+    # product -- each a single-CTA and a CTA-pair launch (p = 64 and 150),
+    # the chain one launch per geometry
+    for abc, launches in (((1.5, -0.5, 0.0), 2 + 2 * 3), ((15 / 8, -5 / 4, 3 / 8), 2 + 2 * 4)):
+        rc, plan = create(L, [desc(0, 64, 64), desc(1, 150, 150)], abc=abc)
+        i = info(L, plan)
+        assert i.n_gram_route == 2 and i.launches_per_step == launches
+        L.gbo_muon_plan_destroy(plan)
 
 
 def test_small_chain_counts(L):

@@ -186,8 +186,9 @@ def test_small_chain_matches_launches(abc, ns_steps):
 @pytest.mark.parametrize("ns_steps", [3, 5])
 def test_normuon_gram_route(ns_steps):
     """NorMuon rows read the last iterate from the buffer each route leaves
-    it in: mixed X-route (square) and Gram-route (rectangular) classes."""
-    shapes = [(600, 130, None, None), (130, 600, None, None), (96, 96, None, None)]
+    it in: mixed X-route (square, above the chain's 192 rows) and Gram-route
+    (rectangular) classes."""
+    shapes = [(600, 130, None, None), (130, 600, None, None), (256, 256, None, None)]
     entries = random_entries(shapes, seed=22, normuon=True, b_std=1e-3)
     gpu, status, plan = run_muon_gpu(entries, lr=0.02, precision="bf16", normuon=True, beta2=0.95, eps=1e-8,
                                      ns_steps=ns_steps)
