@@ -139,7 +139,10 @@ typedef struct {
  *         runs once: X_k = Q_k X_0.  Executes p^2 q + (3k - 3) p^3 + 2 p^2 q
  *         instead of about k (p^2 q + 2 p^2 q) FLOPs (plus one p x p square
  *         of A per iteration with c != 0, on both routes); needs k >= 2.
- *   AUTO  GRAM where it is allowed and executes fewer FLOPs (q > p), else X.
+ *   AUTO  GRAM where it is allowed and executes at least 10% fewer FLOPs
+ *         (q > p), else X.  In bf16 mode the p x p iterations of a matrix of
+ *         at most 192 rows run in one on-chip launch, counted as such: those
+ *         matrices take GRAM even when square.
  * Both precisions run on the tensor cores: bf16 operands, or in the fp32
  * mode fp32 operands as three TF32 products (hi hi + hi lo + lo hi).
  */
