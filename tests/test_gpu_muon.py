@@ -152,14 +152,15 @@ SMALL = [(4 * 96, 1000, (4, 96, 1000), None), (300, 100, None, None), (40, 300, 
 
 
 @pytest.mark.parametrize("abc,ns_steps", [
-    (CUBIC, 5), (CUBIC, 2), (QUINTIC, 3),
+    (CUBIC, 5), (CUBIC, 2), (QUINTIC, 3), (CUBIC, 16),
     (CUBIC + QUINTIC + (2.0, -1.5, 0.5) + CUBIC + (1.2, -0.3, 0.1), 5),
 ])
 def test_small_chain_matches_launches(abc, ns_steps):
     """Matrices of at most 128 rows on the Gram route: the on-chip chain
     (one launch for all p x p products) against one launch per product, for
     p = 20 .. 192 (one and two 128-row halves), wide and tall, c == 0 and
-    c != 0, k = 2 .. 5.  The two
+    c != 0, k = 2 .. 16 (46 chain ops a matrix, barrier phases over many
+    products).  The two
     round every p x p result to bf16 once; the launches mirror symmetric
     results from their upper triangle and the chain writes them whole, so
     they agree to bf16 rounding (1e-2 relative per weight, ten times inside
