@@ -159,7 +159,7 @@ def test_small_chain_matches_launches(abc, ns_steps):
     """Matrices of at most 128 rows on the Gram route: the on-chip chain
     (one launch for all p x p products) against one launch per product, for
     p = 20 .. 192 (one and two 128-row halves), wide and tall, c == 0 and
-    c != 0, k = 2 .. 16 (46 chain ops a matrix, barrier phases over many
+    c != 0, k = 2 .. 16 (up to 45 chain ops a matrix, barrier phases over many
     products).  The two
     round every p x p result to bf16 once; the launches mirror symmetric
     results from their upper triangle and the chain writes them whole, so
