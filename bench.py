@@ -497,6 +497,8 @@ def run_ours(args):
                    "ns_precision": ("fp32 operands as three TF32 products, fp32 accumulate" if f32
                                     else "bf16 operands, fp32 accumulate"),
                    "parallelism": "replicas" if world > 1 else "single",
+                   "device": torch.cuda.get_device_name(),
+                   "seed": "one seeded draw per tensor and role (workloads.seed: workload, tensor index, role)",
                    "l2": "working set ~20 GB per GPU, far above the 129 MB L2: no flush needed"},
         "roofline": {"bound": "tensor",
                      "kernel": ("ns_gemm_tf32_kernel" if f32 else "ns_gemm_tc_kernel")
