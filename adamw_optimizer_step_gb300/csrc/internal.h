@@ -49,7 +49,7 @@ struct DevSub {
   int32_t w_vec;    // weight rows start on 16-byte boundaries (vector read-modify-write)
   int32_t x_sel;    // X buffer (0 or 1) that holds the last iterate (NorMuon rows read it)
   int32_t wmap;     // index of the weight's TMA map (bf16 weights with 16-byte rows), or -1
-  int32_t ss_ntn;   // NorMuon (bf16 mode): partials per stored row, one per 256-column output tile
+  int32_t ss_ntn;   // NorMuon (bf16 mode): partials per stored row, one per 128 output columns
 };
 
 // Matrices of one oriented shape (p, q), stored back to back in the
@@ -155,7 +155,7 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
 // NorMuon rows; with rms_target > 0 a statistics pass, the per-matrix
 // RMS-keeping scale and a write pass (rowf: n_row_blocks * kRowBlock floats,
 // rowpart: n_row_blocks, mscale: n_subs), else one fused pass.
-// rowss: the last product's per-(row, 256-column tile) sums of squares of
+// rowss: the last product's per-(row, 128 columns) sums of squares of
 // X_k (bf16 mode), or nullptr to take the statistics from X_k itself.
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,

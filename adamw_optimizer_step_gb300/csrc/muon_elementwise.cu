@@ -271,8 +271,8 @@ __device__ __forceinline__ void weight_rmw8(const DevSub &S, int64_t widx, int v
 // weight write, with 16-byte accesses throughout.
 //   untransposed: warp w takes stored rows w, w + 8, ... of the block; a
 //     row is X's row.  Its statistics come from the last product's partial
-//     sums of squares (rowss, bf16 mode: one per 256-column tile of the
-//     row, summed in a fixed order), or from a first read of the row; the
+//     sums of squares (rowss, bf16 mode: one per 128 columns of the row,
+//     summed in a fixed order), or from a first read of the row; the
 //     write reads it (again), two 256-element segments per step with every
 //     load issued before the stores (two segments kept 64 registers; four
 //     took 119 and were slower)

@@ -13,10 +13,12 @@
 // of a launch is a job with its own operands, output and epilogue, so one
 // launch may run X-route and Gram-route steps (see internal.h) side by side.
 //
-// Persistent, warp-specialised CTA (192 threads, one CTA per SM):
+// Persistent, warp-specialised CTA (one CTA per SM; 192 threads, 320 in
+// single mode):
 //   warp 0      TMA producer (one lane), STAGES-deep ring of A/B tiles
 //   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2..5  epilogue, one per TMEM lane quarter: TMEM -> registers ->
+//   warps 2..   epilogue, one per TMEM lane quarter (two, each over half of
+//               the tile's columns, in single mode): TMEM -> registers ->
 //               a 64-byte-swizzled staging slot -> TMA store; in the last
 //               product, full 32-row blocks of bf16 weights are loaded by
 //               TMA into the staging area three 32 x 32 blocks ahead,
@@ -68,15 +70,27 @@ struct Mode {
 constexpr int kRingBytes = 6 * (A_BYTES + B_HALF);
 static_assert(Mode<true>::kStages * Mode<true>::kStageBytes == kRingBytes, "ring size");
 static_assert(Mode<false>::kStages * Mode<false>::kStageBytes == kRingBytes, "ring size");
-// Epilogue warps: one per TMEM lane quarter.
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-// Per epilogue warp: two store slots (kSlotBytes each, tc_common.cuh).
-constexpr int kWarpStageBytes = 2 * kSlotBytes;
-constexpr int kStageBytes = kEpiWarps * kWarpStageBytes;
+// Epilogue warps.  Pair mode: one per TMEM lane quarter, each over the
+// tile's 256 columns, with two store slots (kSlotBytes each, tc_common.cuh)
+// or four weight buffers.  Single mode: two per lane quarter, each over 128
+// of the columns, with one slot or two weight buffers: its HBM-bound last
+// products on small matrices are limited by the epilogue warps' latency, and
+// two warps per scheduler hide more of it.  Both stage 32 KB in all.
+template <bool kPair>
+struct Epi {
+  static constexpr int kWarps = kPair ? 4 : 8;
+  static constexpr int kSplit = kWarps / 4;           // warps per lane quarter
+  static constexpr int kSpan = BN / kSplit;           // columns a warp covers
+  static constexpr int kThreads = 64 + 32 * kWarps;
+  static constexpr int kWarpStage = 8 * 1024 / kSplit;
+  static constexpr int kSlots = kWarpStage / kSlotBytes;
+  static constexpr int kWBufs = kWarpStage / kWBufBytes;
+};
+constexpr int kStageBytes = 32 * 1024;
+static_assert(Epi<true>::kWarps * Epi<true>::kWarpStage == kStageBytes, "staging size");
+static_assert(Epi<false>::kWarps * Epi<false>::kWarpStage == kStageBytes, "staging size");
 constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + kStageBytes + 512 /*barriers*/;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kWBufs * kWBufBytes <= kWarpStageBytes, "weight buffers fit a warp's staging area");
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
 // each K-major or MN-major, N = 256, M = 128 (one CTA) or 256 (pair).
 __host__ __device__ constexpr uint32_t make_idesc(int a_mn_major, int b_mn_major, int m) {
@@ -118,6 +132,7 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
 // matrix's folded pre-normalisation factor (1 unless the job folds it).
 // Outputs other than the weights leave through TMA stores from the warp's
 // staging slots (`stage`, `slot`).
+template <int kSlots>
 __device__ __forceinline__ void epilogue_block(const TcParams &P, const PhaseArgs &A, int c, int mat,
                                                const DevSub &S, float s, int i0, int col0, float (&v)[32],
                                                uint32_t stage, int &slot, int lane) {
@@ -127,7 +142,7 @@ __device__ __forceinline__ void epilogue_block(const TcParams &P, const PhaseArg
     float o[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = s * v[k];
-    tma_store_block(&P.mapO[c], stage, slot, o, false, col0, i0, mat, lane);
+    tma_store_block<kSlots>(&P.mapO[c], stage, slot, o, false, col0, i0, mat, lane);
     return;
   }
   if (J.mode == kFinal) {  // fp32 weights: O = s * C, the update direction is scale * O
@@ -168,11 +183,11 @@ __device__ __forceinline__ void epilogue_block(const TcParams &P, const PhaseArg
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = s2 * v[k];
   }
-  tma_store_block(&P.mapO[c], stage, slot, o, mirror, col0, i0, mat, lane);
+  tma_store_block<kSlots>(&P.mapO[c], stage, slot, o, mirror, col0, i0, mat, lane);
   if (J.mode == kGramAP) {  // and A = s^2 C
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = s2 * v[k];
-    tma_store_block(&P.mapO2[c], stage, slot, o, mirror, col0, i0, mat, lane);
+    tma_store_block<kSlots>(&P.mapO2[c], stage, slot, o, mirror, col0, i0, mat, lane);
   }
 }
 
@@ -272,7 +287,7 @@ __device__ __forceinline__ bool mma_tile(uint8_t *smem, uint32_t full0, uint32_t
 }
 
 template <bool kPair>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Epi<kPair>::kThreads, 1)
 ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ PhaseArgs A) {
   constexpr int STAGES = Mode<kPair>::kStages;
   constexpr int kRows = Mode<kPair>::kRows;
@@ -280,7 +295,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes + kStageBytes);
   // bars: full[STAGES], empty[STAGES], accf[2], acce[2], drain, (TMEM
-  // address, abort flag), then kWBufs weight-load barriers per epilogue warp
+  // address, abort flag), then the weight-load barriers of the epilogue warps
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
   uint64_t *wbars = bars + 2 * STAGES + 6;
@@ -307,10 +322,10 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf0 + 8 * a, 1);
-      mbar_init(acce0 + 8 * a, (kPair ? 2 : 1) * kEpiWarps);
+      mbar_init(acce0 + 8 * a, (kPair ? 2 : 1) * Epi<kPair>::kWarps);
     }
     mbar_init(drain, 1);
-    for (int b = 0; b < kEpiWarps * kWBufs; ++b) mbar_init(smem_u32(wbars + b), 1);
+    for (int b = 0; b < Epi<kPair>::kWarps * Epi<kPair>::kWBufs; ++b) mbar_init(smem_u32(wbars + b), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -405,10 +420,13 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       }
     }
   } else {
-    // epilogue warps: TMEM lane quarter = warp % 4
+    // epilogue warps: TMEM lane quarter = warp % 4; in single mode two warps
+    // per quarter, each over half of the tile's columns
+    using E = Epi<kPair>;
     const int quarter = warp & 3;
-    const uint32_t stage = smem_u32(stage_base + (warp - 2) * kWarpStageBytes);
-    const uint32_t wbar0 = smem_u32(wbars + (warp - 2) * kWBufs);
+    const int part = (warp - 2) / 4;                  // which span of the tile's columns
+    const uint32_t stage = smem_u32(stage_base + (warp - 2) * E::kWarpStage);
+    const uint32_t wbar0 = smem_u32(wbars + (warp - 2) * E::kWBufs);
     uint32_t wpar = 0, winfl = 0;  // weight-load barriers: next parities, loads in flight
     int slot = 0;
     int acc = 0;
@@ -419,6 +437,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const DevSub &S = A.subs[sub];
       const TcJob &J = P.job[tc.c];
       const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
+      const int c0 = tc.tn * BN + part * E::kSpan;    // this warp's first column
       // the job's output is rows x cols (stored orientation for the weights)
       const int rows = kind_rows(J.kind, S.p, S.q), cols = kind_cols(J.kind, S.p, S.q);
       // bf16 weights in blocks of 32 whole rows with a TMA map move by TMA
@@ -427,44 +446,53 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const CUtensorMap *wmap = (J.mode == kFinal && S.w_dtype == GBO_BF16 && S.wmap >= 0)
                                     ? static_cast<const CUtensorMap *>(A.wmaps) + S.wmap
                                     : nullptr;
-      const bool wtma = wmap != nullptr && i0 + 32 <= rows;
-      if (wtma) weight_loads_begin<!kPair>(wmap, stage, wbar0, tc.tn * BN, cols, (int)(S.r0 + i0), lane, winfl);
-      else if (J.mode == kFinal) prefetch_weight_tile(S, i0, tc.tn * BN, rows, cols, lane);
+      const bool live = i0 < rows && c0 < cols;      // this warp's part of the tile holds outputs
+      const bool wtma = live && wmap != nullptr && i0 + 32 <= rows;
+      if (wtma) weight_loads_begin<E::kWBufs>(wmap, stage, wbar0, c0, cols, (int)(S.r0 + i0), lane, winfl, E::kSpan);
+      else if (live && J.mode == kFinal) prefetch_weight_tile(S, i0, c0, rows, cols, lane, E::kSpan);
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
       tc_fence_after();
       const float s = J.first ? A.alpha[sub] : 1.0f;
-      const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      if (i0 < rows) {  // warps whose rows are all padding have nothing to write
+      const uint32_t trow =
+          tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + part * E::kSpan);
+      if (live) {  // warps whose rows or columns are all padding have nothing to write
         if (wtma) {
-          if (!final_tile_bf16_tma<!kPair>(A, S, s, i0, tc.tn * BN, cols, trow, lane, wmap, stage, wbar0, wpar,
-                                            winfl)) {
+          if (!final_tile_bf16_tma<E::kWBufs>(A, S, s, i0, c0, cols, trow, lane, wmap, stage, wbar0, wpar, winfl,
+                                              E::kSpan)) {
             give_up();
             break;
           }
         } else if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
-          final_tile_bf16(A, S, s, i0, tc.tn * BN, rows, cols, trow, lane);
+          final_tile_bf16(A, S, s, i0, c0, rows, cols, trow, lane, E::kSpan);
         } else {
           // the NorMuon last product also leaves each row's sum of squares of
-          // the bf16 values it stores, one partial per 256-column tile
+          // the bf16 values it stores, one partial per 128 columns
           const bool stats = J.mode == kProduct && J.aux != nullptr;
-          float rss = 0.f;
+          float rss[E::kSpan / 128] = {};
 #pragma unroll 1
-          for (int ch = 0; ch < BN / 32; ++ch) {
-            const int col0 = tc.tn * BN + ch * 32;
+          for (int ch = 0; ch < E::kSpan / 32; ++ch) {
+            const int col0 = c0 + ch * 32;
             if (col0 >= cols) break;  // column chunks past the output hold nothing to write
             float v[32];
             tmem_ld32(trow + ch * 32, v);
-            epilogue_block(P, A, tc.c, tc.mat, S, s, i0, col0, v, stage, slot, lane);
+            epilogue_block<E::kSlots>(P, A, tc.c, tc.mat, S, s, i0, col0, v, stage, slot, lane);
             if (stats) {
+              float r2 = 0.f;
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
                 const float r = __bfloat162float(__float2bfloat16_rn(s * v[k]));
-                rss = fmaf(r, r, rss);
+                r2 = fmaf(r, r, r2);
               }
+              rss[ch / 4] += r2;
             }
           }
-          if (stats && i0 + lane < rows)
-            static_cast<float *>(const_cast<void *>(J.aux))[S.ss_off + (int64_t)(i0 + lane) * S.ss_ntn + tc.tn] = rss;
+          if (stats && i0 + lane < rows) {
+            float *part_out = static_cast<float *>(const_cast<void *>(J.aux)) + S.ss_off +
+                              (int64_t)(i0 + lane) * S.ss_ntn + c0 / 128;
+#pragma unroll
+            for (int h = 0; h < E::kSpan / 128; ++h)
+              if (c0 + 128 * h < cols) part_out[h] = rss[h];
+          }
         }
       }
       tc_fence_before();
@@ -477,7 +505,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     }
     // weight loads of an abandoned tile land, and this warp's TMA stores
     // complete, before the kernel ends
-    for (int b = 0; b < kWBufs; ++b)
+    for (int b = 0; b < E::kWBufs; ++b)
       if (winfl >> b & 1u) (void)mbar_wait(wbar0 + 8 * b, (wpar >> b) & 1u);
     if (lane == 0) bulk_wait_all();
     __syncwarp();
@@ -648,7 +676,7 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
     if (total == 0) continue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Epi<kPair>::kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     if constexpr (kPair) {

@@ -392,10 +392,10 @@ int validate_and_expand(gbo_plan *P) {
   P->n_tiles = tiles;
   P->n_row_blocks = rbs;
   // NorMuon row statistics from the last product (bf16 mode): per stored row
-  // of each matrix, one partial per 256-column tile of its output
+  // of each matrix, one partial per 128 columns of its output
   int64_t rowss = 0;
   for (DevSub &S : subs) {
-    S.ss_ntn = (S.n + 255) / 256;
+    S.ss_ntn = (S.n + 127) / 128;
     S.ss_off = rowss;
     if (o.normuon && tc_path) rowss += (int64_t)S.m * S.ss_ntn;
   }

@@ -386,13 +386,14 @@ __device__ __forceinline__ void stage_cols(uint32_t dst, const float (&o)[32], i
 }
 
 // Store a warp's 32 x 32 block at (x0, y0) of matrix z, and with `mirror`
-// its transpose at (y0, x0), through the next of the warp's two staging
-// slots; TMA drops whatever falls outside the tensor.
+// its transpose at (y0, x0), through the next of the warp's kSlots staging
+// slots (two, or one); TMA drops whatever falls outside the tensor.
+template <int kSlots = 2>
 __device__ __forceinline__ void tma_store_block(const CUtensorMap *map, uint32_t stage, int &slot,
                                                 const float (&o)[32], bool mirror, int x0, int y0, int z, int lane) {
   const uint32_t dst = stage + (uint32_t)(slot * kSlotBytes);
-  slot ^= 1;
-  if (lane == 0) bulk_wait_read<1>();  // the stores that last used this slot have read it
+  if constexpr (kSlots == 2) slot ^= 1;
+  if (lane == 0) bulk_wait_read<kSlots - 1>();  // the stores that last used this slot have read it
   __syncwarp();
   stage_rows(dst, o, lane);
   if (mirror) stage_cols(dst + 2048, o, lane);
@@ -469,8 +470,8 @@ __device__ __forceinline__ void wseg_unpack(const WSeg &r, float (&o)[32]) {
 // r0 + i0 + r.  The weights of chunk ch + 1 are loaded before chunk ch is
 // computed, so a load of each lane's row segment is always in flight.
 __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub &S, float s, int i0, int tile_col0,
-                                                int rows, int cols, uint32_t trow, int lane) {
-  const int nch = min(BN / 32, (cols - tile_col0 + 31) / 32);  // chunks holding columns < cols
+                                                int rows, int cols, uint32_t trow, int lane, int span = BN) {
+  const int nch = min(span / 32, (cols - tile_col0 + 31) / 32);  // chunks holding columns < cols
   const float lr = A.lr * S.lr_mult, su = S.scale * s;
   __nv_bfloat16 *W = reinterpret_cast<__nv_bfloat16 *>(S.w);
   const bool ok = i0 + lane < rows;
@@ -512,13 +513,14 @@ __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub
 // map (`wmap`: the whole weight, 32 x 32 boxes, 64-byte swizzle): the weights
 // travel by TMA both ways.  Column chunk c (a 32 x 32 block) is loaded into
 // buffer c % kWBufs of the warp's staging area, updated in place and stored
-// from there.  Loads run kWAhead chunks ahead of the chunk being updated;
-// the first kWAhead are issued before the accumulator is ready
+// from there.  Loads run kWBufs - 1 chunks ahead of the chunk being updated;
+// the first ones are issued before the accumulator is ready
 // (weight_loads_begin).  Each buffer has an mbarrier (wbar0 + 8 b); wpar
 // holds the parity each waits for next (bit b) and winfl the buffers with a
 // load in flight (bit b).  The warp's state is uniform across its lanes.
-constexpr int kWBufs = 4, kWAhead = 3, kWBufBytes = 2048;
+constexpr int kWBufBytes = 2048;
 
+template <int kWBufs>
 __device__ __forceinline__ void weight_load_chunk(const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0, int c,
                                                   int col0, int row0) {
   const uint32_t b = (uint32_t)(c & (kWBufs - 1));
@@ -526,19 +528,20 @@ __device__ __forceinline__ void weight_load_chunk(const CUtensorMap *wmap, uint3
   tma_load_3d(stage + b * kWBufBytes, wmap, wbar0 + 8 * b, col0, row0, 0);
 }
 
-__device__ __forceinline__ int weight_chunks(int tile_col0, int cols) {
-  return min(BN / 32, (cols - tile_col0 + 31) / 32);
+__device__ __forceinline__ int weight_chunks(int tile_col0, int cols, int span) {
+  return min(span / 32, (cols - tile_col0 + 31) / 32);
 }
 
-// kTwo: the tile's chunks are updated in pairs (final_tile_bf16_tma), and
-// the first two pairs are loaded here.
-template <bool kTwo>
+// kWBufs buffers: kWBufs - 1 chunks are loaded here, ahead of the first
+// update (final_tile_bf16_tma).
+template <int kWBufs>
 __device__ __forceinline__ void weight_loads_begin(const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
-                                                   int tile_col0, int cols, int row0, int lane, uint32_t &winfl) {
-  const int n0 = min(kTwo ? kWBufs : kWAhead, weight_chunks(tile_col0, cols));
+                                                   int tile_col0, int cols, int row0, int lane, uint32_t &winfl,
+                                                   int span) {
+  const int n0 = min(kWBufs - 1, weight_chunks(tile_col0, cols, span));
   if (lane == 0) {
     bulk_wait_read<0>();  // earlier stores from the staging area have read it
-    for (int c = 0; c < n0; ++c) weight_load_chunk(wmap, stage, wbar0, c, tile_col0 + 32 * c, row0);
+    for (int c = 0; c < n0; ++c) weight_load_chunk<kWBufs>(wmap, stage, wbar0, c, tile_col0 + 32 * c, row0);
   }
   __syncwarp();
   winfl |= (1u << n0) - 1u;
@@ -562,13 +565,16 @@ __device__ __forceinline__ void stage_read_row(uint32_t src, float (&o)[32], int
   }
 }
 
-// One chunk at a time, loads kWAhead chunks ahead.  Returns false on a
+// kWBufs buffers, loads kWBufs - 1 chunks ahead of the update.  `span`: the
+// columns of the tile this warp covers, from tile_col0.  Returns false on a
 // time-out of a load wait.
-__device__ __forceinline__ bool final_tile_bf16_tma_one(const PhaseArgs &A, const DevSub &S, float s, int i0,
+template <int kWBufs>
+__device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const DevSub &S, float s, int i0,
                                                     int tile_col0, int cols, uint32_t trow, int lane,
                                                     const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
-                                                    uint32_t &wpar, uint32_t &winfl) {
-  const int nch = weight_chunks(tile_col0, cols);
+                                                    uint32_t &wpar, uint32_t &winfl, int span) {
+  constexpr int kWAhead = kWBufs - 1;
+  const int nch = weight_chunks(tile_col0, cols, span);
   const float lr = A.lr * S.lr_mult, su = S.scale * s;
   // W - lr (wd W + su C) as one multiply-add per element: decay factor and
   // update factor folded (the same result up to one fp32 rounding)
@@ -606,7 +612,7 @@ __device__ __forceinline__ bool final_tile_bf16_tma_one(const PhaseArgs &A, cons
         // the buffer of chunk ch + kWAhead was last stored from by chunk
         // ch - 1: at most this chunk's store may still read the staging area
         bulk_wait_read<1>();
-        weight_load_chunk(wmap, stage, wbar0, ch + kWAhead, col0 + 32 * kWAhead, row0);
+        weight_load_chunk<kWBufs>(wmap, stage, wbar0, ch + kWAhead, col0 + 32 * kWAhead, row0);
       }
     }
     if (more) winfl |= 1u << ((ch + kWAhead) & (kWBufs - 1));
@@ -623,98 +629,6 @@ __device__ __forceinline__ bool final_tile_bf16_tma_one(const PhaseArgs &A, cons
   return true;
 }
 
-// Chunks in pairs (chunks 2j, 2j + 1 in buffers 2j % 4, 2j % 4 + 1): one
-// fence, one commit and one read-wait per pair; the next pair is loaded
-// into the buffers of the previous one.  Its two accumulator chunks take 64
-// more registers, which the single-CTA kernel (HBM-bound last products on
-// small matrices) can spare: measured 3.77 -> 3.63 ms on the MLA/KDA set,
-// while the CTA-pair kernel ran its other launches about 1% slower with
-// them.  Returns false on a time-out of a load wait.
-__device__ __forceinline__ bool final_tile_bf16_tma_two(const PhaseArgs &A, const DevSub &S, float s, int i0,
-                                                    int tile_col0, int cols, uint32_t trow, int lane,
-                                                    const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
-                                                    uint32_t &wpar, uint32_t &winfl) {
-  const int nch = weight_chunks(tile_col0, cols);
-  const float lr = A.lr * S.lr_mult, su = S.scale * s;
-  const float keep = 1.0f - lr * S.wd, step = lr * su;
-  const bool decay = S.wd != 0.f;
-  const int row0 = (int)(S.r0 + i0);
-  const int64_t wrow = (S.r0 + i0 + lane) * S.cols;
-#pragma unroll 1
-  for (int c0 = 0; c0 < nch; c0 += 2) {
-    const bool two = c0 + 1 < nch;
-    if (c0 >= 2 && c0 + 2 < nch) {
-      // the next pair goes into the buffers of the previous one, whose
-      // stores are the latest group
-      if (lane == 0) {
-        bulk_wait_read<0>();
-        weight_load_chunk(wmap, stage, wbar0, c0 + 2, tile_col0 + 32 * (c0 + 2), row0);
-        if (c0 + 3 < nch) weight_load_chunk(wmap, stage, wbar0, c0 + 3, tile_col0 + 32 * (c0 + 3), row0);
-      }
-      winfl |= 1u << ((c0 + 2) & (kWBufs - 1));
-      if (c0 + 3 < nch) winfl |= 1u << ((c0 + 3) & (kWBufs - 1));
-    }
-    float u0[32], u1[32];
-    tmem_ld32(trow + c0 * 32, u0);
-    if (two) tmem_ld32(trow + (c0 + 1) * 32, u1);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (h == 1 && !two) break;
-      const int ch = c0 + h;
-      const uint32_t b = (uint32_t)(ch & (kWBufs - 1));
-      const uint32_t buf = stage + b * kWBufBytes;
-      if (!mbar_wait(wbar0 + 8 * b, (wpar >> b) & 1u)) return false;
-      wpar ^= 1u << b;
-      winfl &= ~(1u << b);
-      float (&u)[32] = h == 0 ? u0 : u1;
-      float w[32];
-      stage_read_row(buf, w, lane);
-      if (decay) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = fmaf(-step, u[k], keep * w[k]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = fmaf(-step, u[k], w[k]);
-      }
-      stage_rows(buf, w, lane);
-    }
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_3d(wmap, stage + (uint32_t)(c0 & (kWBufs - 1)) * kWBufBytes, tile_col0 + 32 * c0, row0, 0);
-      if (two) tma_store_3d(wmap, stage + (uint32_t)((c0 + 1) & (kWBufs - 1)) * kWBufBytes, tile_col0 + 32 * (c0 + 1), row0, 0);
-      bulk_commit();
-    }
-    if (A.dbg) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (h == 1 && !two) break;
-        float (&u)[32] = h == 0 ? u0 : u1;
-        const int col0 = tile_col0 + 32 * (c0 + h);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) u[k] *= su;
-        const uint32_t mask = prefix_mask(cols - col0);
-        float *d = A.dbg + S.dbg_off + wrow + col0;
-        store_row32(d, u, mask == 0xffffffffu && (reinterpret_cast<uintptr_t>(d) & 15) == 0, mask);
-      }
-    }
-  }
-  if (lane == 0) bulk_wait_read<0>();  // the staging area is free for the other epilogues
-  __syncwarp();
-  return true;
-}
-
-template <bool kTwo>
-__device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const DevSub &S, float s, int i0,
-                                                    int tile_col0, int cols, uint32_t trow, int lane,
-                                                    const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
-                                                    uint32_t &wpar, uint32_t &winfl) {
-  if constexpr (kTwo)
-    return final_tile_bf16_tma_two(A, S, s, i0, tile_col0, cols, trow, lane, wmap, stage, wbar0, wpar, winfl);
-  else
-    return final_tile_bf16_tma_one(A, S, s, i0, tile_col0, cols, trow, lane, wmap, stage, wbar0, wpar, winfl);
-}
-
 __device__ __forceinline__ void prefetch_l2(const void *p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -723,12 +637,12 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
 // warp will read-modify-write for the tile at (i0.., col0 .. col0 + BN) of
 // the stored-orientation output (rows x cols).
 __device__ __forceinline__ void prefetch_weight_tile(const DevSub &S, int i0, int col0, int rows, int cols,
-                                                     int lane) {
+                                                     int lane, int span = BN) {
   const int64_t es = S.w_dtype == GBO_BF16 ? 2 : 4;
   const char *w = static_cast<const char *>(S.w);
   const int i = i0 + lane;
   if (i >= rows) return;
-  const int c1 = min(cols, col0 + BN);
+  const int c1 = min(cols, col0 + span);
   for (int c = col0; c < c1; c += (int)(128 / es)) prefetch_l2(w + ((S.r0 + i) * S.cols + c) * es);
 }
 
