@@ -157,10 +157,12 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
 // rowpart: n_row_blocks, mscale: n_subs), else one fused pass.
 // rowss: the last product's per-(row, 128 columns) sums of squares of
 // X_k (bf16 mode), or nullptr to take the statistics from X_k itself.
+// streamed: every matrix has bf16 X and bf16 weight rows on 16-byte
+// boundaries, so the write pass streams rows through shared memory.
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
                         int32_t *status, float rms_target, float *rowf, float *rowpart, float *mscale,
-                        const float *rowss, int sm_count, void *stream);
+                        const float *rowss, bool streamed, int sm_count, void *stream);
 int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
                                  int32_t w_dtype, float beta2, float eps, float scale, float lr,
                                  float wd, float *dbg, void *stream);

@@ -19,6 +19,7 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace gbo {
 
@@ -470,6 +471,168 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
   }
 }
 
+// The NorMuon write pass streamed through shared memory (bf16 X and bf16
+// weights whose rows start on 16-byte boundaries): each warp takes whole
+// stored rows and moves them in 2048-element segments, X's and W's, by bulk
+// copies into a ring of kWStages stages of its own, kept full across its
+// rows, so the loads run ahead without holding registers; the warp reads a
+// landed stage, computes the new weights and stores them with 16-byte vector
+// stores.  The row factors come from the statistics pass (rowf, 1 / (sqrt(v)
+// + eps)), times the rectangular scale (kMode 0) or the RMS scale (kMode 2);
+// each is read when its row's first segment is loaded, so no row waits for
+// it (NorMuon paper, section 3.1, as normuon_rows_kernel).
+constexpr int kSeg = 2048;
+constexpr int kWStages = 3;
+constexpr int kWWarps = 8;
+constexpr int kWStageBytes = 2 * kSeg * 2;  // a segment of X and of W, bf16
+constexpr int kWSmem = 128 /*align*/ + kWWarps * kWStages * kWStageBytes;
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// A warp's walk over stored rows: row slots slot, slot + stride, ... of the
+// plan's row blocks (kRowBlock slots each), skipping slots past a matrix's
+// rows.
+struct RowCursor {
+  int64_t slot;
+  int si, row, seg;  // matrix, row within it, segment
+};
+
+__device__ __forceinline__ bool row_at(const DevSub *subs, int32_t n_subs, int64_t n_slots, int64_t stride,
+                                       RowCursor &c) {
+  for (; c.slot < n_slots; c.slot += stride) {
+    const int64_t b = c.slot / kRowBlock;
+    c.si = find_owner(b, n_subs, [&](int k) { return subs[k].rb0; });
+    c.row = (int)(b - subs[c.si].rb0) * kRowBlock + (int)(c.slot % kRowBlock);
+    if (c.row < subs[c.si].m) {
+      c.seg = 0;
+      return true;
+    }
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool row_next(const DevSub *subs, int32_t n_subs, int64_t n_slots, int64_t stride,
+                                         RowCursor &c) {
+  if (++c.seg * kSeg < subs[c.si].n) return true;
+  c.slot += stride;
+  return row_at(subs, n_subs, n_slots, stride, c);
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kWWarps * 32, 1)
+normuon_write_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_slots,
+                     const __nv_bfloat16 *__restrict__ xbuf0, const __nv_bfloat16 *__restrict__ xbuf1, float beta2,
+                     float eps, float lr, float *__restrict__ dbg, int32_t *status, const float *__restrict__ rowf,
+                     const float *__restrict__ mscale) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bars[kWWarps * kWStages];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ring = smem_u32(smem) + (uint32_t)(warp * kWStages * kWStageBytes);
+  const uint32_t bar0 = smem_u32(&bars[warp * kWStages]);
+  if (lane == 0) {
+    for (int st = 0; st < kWStages; ++st) mbar_init(bar0 + 8 * st, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  const int64_t stride = (int64_t)gridDim.x * kWWarps;
+  RowCursor ic{(int64_t)blockIdx.x * kWWarps + warp, 0, 0, 0};
+  bool ic_ok = row_at(subs, n_subs, n_slots, stride, ic);
+  RowCursor cc = ic;
+  bool cc_ok = ic_ok;
+  uint32_t issued = 0, consumed = 0;
+  float fq[kWStages];  // lane 0: the row factor of each stage's segment
+  // lane 0 loads the stream's next segment into its stage
+  auto issue = [&]() {
+    const DevSub &S = subs[ic.si];
+    const __nv_bfloat16 *X = (S.x_sel ? xbuf1 : xbuf0) + S.x_off + (int64_t)ic.row * S.ld + (int64_t)ic.seg * kSeg;
+    const __nv_bfloat16 *W =
+        reinterpret_cast<const __nv_bfloat16 *>(S.w) + (S.r0 + ic.row) * S.cols + (int64_t)ic.seg * kSeg;
+    const uint32_t bytes = (uint32_t)min(kSeg, S.n - ic.seg * kSeg) * 2u;
+    const uint32_t st = issued % kWStages, bar = bar0 + 8 * st, dst = ring + st * kWStageBytes;
+    mbar_expect_tx(bar, 2 * bytes);
+    bulk_load(dst, X, bytes, bar);
+    bulk_load(dst + kSeg * 2, W, bytes, bar);
+    const float g = ic.seg == 0 ? rowf[ic.slot] * (kMode == 0 ? S.scale : mscale[ic.si]) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kWStages; ++k)
+      if (k == (int)st) fq[k] = g;
+  };
+  while (ic_ok && issued < (uint32_t)kWStages) {
+    if (lane == 0) issue();
+    ++issued;
+    ic_ok = row_next(subs, n_subs, n_slots, stride, ic);
+  }
+  float f = 0.f;
+  bool timed_out = false;
+  while (cc_ok) {
+    const DevSub &S = subs[cc.si];
+    const int64_t vrow = S.r0 + cc.row;
+    const uint32_t st = consumed % kWStages;
+    if (cc.seg == 0) {  // the row's factor, loaded with its first segment
+      float g = 0.f;
+#pragma unroll
+      for (int k = 0; k < kWStages; ++k)
+        if (k == (int)st) g = fq[k];
+      f = __shfl_sync(0xffffffffu, g, 0);
+    }
+    if (!mbar_wait(bar0 + 8 * st, (consumed / kWStages) & 1u)) {
+      flag_status(status, GBO_STATUS_TIMEOUT);
+      timed_out = true;
+      break;
+    }
+    const uint32_t xs = ring + st * kWStageBytes, ws = xs + kSeg * 2;
+    const int base = cc.seg * kSeg, len = min(kSeg, S.n - base);
+    const float lrm = lr * S.lr_mult;
+    __nv_bfloat16 *W = reinterpret_cast<__nv_bfloat16 *>(S.w) + vrow * S.cols + base;
+    for (int g = lane; g * 8 < len; g += 32) {  // eight elements per lane and step
+      uint32_t xr[4], wr[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(xr[0]), "=r"(xr[1]), "=r"(xr[2]), "=r"(xr[3])
+                   : "r"(xs + g * 16)
+                   : "memory");
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(wr[0]), "=r"(wr[1]), "=r"(wr[2]), "=r"(wr[3])
+                   : "r"(ws + g * 16)
+                   : "memory");
+      float o[8], w[8], u[8];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 xb = *reinterpret_cast<const __nv_bfloat162 *>(&xr[h]);
+        const __nv_bfloat162 wb = *reinterpret_cast<const __nv_bfloat162 *>(&wr[h]);
+        o[2 * h] = __low2float(xb);
+        o[2 * h + 1] = __high2float(xb);
+        w[2 * h] = __low2float(wb);
+        w[2 * h + 1] = __high2float(wb);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        u[e] = f * o[e];
+        w[e] = w[e] - lrm * (S.wd * w[e] + u[e]);
+      }
+      store8(W + g * 8, w, 8, true);
+      if (dbg) {
+        float *d = dbg + S.dbg_off + vrow * S.cols + base + g * 8;
+        store8(d, u, 8, (reinterpret_cast<uintptr_t>(d) & 15) == 0);
+      }
+    }
+    __syncwarp();  // every lane has read the stage
+    ++consumed;
+    cc_ok = row_next(subs, n_subs, n_slots, stride, cc);
+    if (ic_ok) {
+      if (lane == 0) issue();
+      ++issued;
+      ic_ok = row_next(subs, n_subs, n_slots, stride, ic);
+    }
+  }
+  if (timed_out)  // the copies in flight land before shared memory goes away
+    for (uint32_t k = consumed; k < issued; ++k) (void)mbar_wait(bar0 + 8 * (k % kWStages), (k / kWStages) & 1u);
+}
+
 // The RMS-keeping scale of each matrix (one block per matrix): the row-block
 // partials of ||O_hat||_F^2 summed in a fixed order, then
 // rho * sqrt(m n) / ||O_hat||_F; an all-zero update keeps a zero scale.
@@ -569,13 +732,24 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
                         int32_t *status, float rms_target, float *rowf, float *rowpart, float *mscale,
-                        const float *rowss, int sm_count, void *stream) {
+                        const float *rowss, bool streamed, int sm_count, void *stream) {
   if (n_row_blocks == 0) return 0;
   const int64_t grid = std::min<int64_t>(n_row_blocks, (int64_t)sm_count * 8);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  static cudaError_t attr_err = [] {
+    cudaError_t e = cudaFuncSetAttribute(normuon_write_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(normuon_write_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+    return e;
+  }();
+  if (streamed && attr_err != cudaSuccess) return (int)attr_err;
   auto rows = [&](auto mode) {
     constexpr int kMode = decltype(mode)::value;
-    if (x_dtype == GBO_BF16)
+    if (streamed && kMode != 1)
+      normuon_write_kernel<kMode><<<(unsigned)sm_count, kWWarps * 32, kWSmem, st>>>(
+          subs, n_subs, n_row_blocks * kRowBlock, reinterpret_cast<const __nv_bfloat16 *>(x0),
+          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf, mscale);
+    else if (x_dtype == GBO_BF16)
       normuon_rows_kernel<__nv_bfloat16, kMode><<<(unsigned)grid, 256, 0, st>>>(
           subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x0),
           reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf, rowpart, mscale, rowss);
@@ -590,6 +764,9 @@ int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks
     normuon_scale_kernel<<<(unsigned)n_subs, 256, 0, st>>>(subs, rowpart, rms_target, mscale, status);
     count_launches(1);
     rows(std::integral_constant<int, 2>());
+  } else if (streamed) {  // the statistics pass (row factors), then the streamed write
+    rows(std::integral_constant<int, 1>());
+    rows(std::integral_constant<int, 0>());
   } else {
     rows(std::integral_constant<int, 0>());
   }

@@ -137,8 +137,10 @@ struct gbo_plan {
   size_t off_g[6] = {0, 0, 0, 0, 0, 0};
   // NorMuon RMS-keeping scale: per-row factors, row-block partials, per-matrix scales
   size_t off_rowf = 0, off_rowpart = 0, off_mscale = 0;
-  // NorMuon, bf16 mode: the last product's row-statistics partials
+  // NorMuon, bf16 mode: the last product's row-statistics partials, and
+  // whether every matrix's weight rows allow the streamed write pass
   size_t off_rowss = 0;
+  bool rows_streamed = false;
   uint64_t hash = 0;
   gbo_plan_info info{};
   // device state, set by the first step
@@ -394,7 +396,9 @@ int validate_and_expand(gbo_plan *P) {
   // NorMuon row statistics from the last product (bf16 mode): per stored row
   // of each matrix, one partial per 128 columns of its output
   int64_t rowss = 0;
+  P->rows_streamed = o.normuon && tc_path;
   for (DevSub &S : subs) {
+    P->rows_streamed = P->rows_streamed && S.w_dtype == GBO_BF16 && S.w_vec && !S.transposed && S.n % 8 == 0;
     S.ss_ntn = (S.n + 127) / 128;
     S.ss_off = rowss;
     if (o.normuon && tc_path) rowss += (int64_t)S.m * S.ss_ntn;
@@ -420,8 +424,11 @@ int validate_and_expand(gbo_plan *P) {
   P->off_alpha = region(P->subs.size() * sizeof(float));
   P->off_part = region((size_t)tiles * 8 * 2 * sizeof(float));  // (max, sum of squares) per warp of a tile
   const bool rms = o.normuon && o.rms_target > 0.f;
-  P->off_rowf = region(rms ? (size_t)rbs * kRowBlock * sizeof(float) : 0);
-  P->off_rowpart = region(rms ? (size_t)rbs * sizeof(float) : 0);
+  // per-row factors: the RMS scale's statistics pass, or the streamed write
+  // pass's statistics pass
+  const bool rowf = rms || P->rows_streamed;
+  P->off_rowf = region(rowf ? (size_t)rbs * kRowBlock * sizeof(float) : 0);
+  P->off_rowpart = region(rowf ? (size_t)rbs * sizeof(float) : 0);
   P->off_mscale = region(rms ? P->subs.size() * sizeof(float) : 0);
   P->off_rowss = region((size_t)rowss * sizeof(float));
   P->ws_bytes = off;
@@ -712,7 +719,8 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   int64_t gemm = 0;
   for (const TcStep &st : build_schedule(P, nullptr)) gemm += tc_step_launches(st);
   P->info.launches_per_step =
-      P->subs.empty() ? 0 : 2 + gemm + (opts->normuon ? (opts->rms_target > 0.f ? 3 : 1) : 0);
+      P->subs.empty() ? 0
+                      : 2 + gemm + (opts->normuon ? (opts->rms_target > 0.f ? 3 : (P->rows_streamed ? 2 : 1)) : 0);
   *out = P;
   return ok();
 }
@@ -855,7 +863,7 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
                               reinterpret_cast<float *>(ws + P->off_rowpart),
                               reinterpret_cast<float *>(ws + P->off_mscale),
                               P->x_dtype == GBO_BF16 ? reinterpret_cast<const float *>(ws + P->off_rowss) : nullptr,
-                              P->sm_count, st);
+                              P->rows_streamed, P->sm_count, st);
     if (err) return cuda_fail(err, "NorMuon rows kernel");
     mark(kPhaseRows, P->opts.rms_target > 0.f ? 3 : 1);
   }
