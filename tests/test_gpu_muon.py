@@ -210,6 +210,28 @@ def test_normuon_rows(precision):
     check_muon(entries, gpu, ora, lr=0.02, precision=precision)
 
 
+@pytest.mark.parametrize("rms_target", [0.0, 0.2])
+def test_normuon_streamed_write(rms_target):
+    """bf16 weights whose rows all start on 16-byte boundaries take the
+    streamed write pass (a statistics pass, then rows streamed through
+    shared memory in 2048-element segments): rows longer and shorter than a
+    segment, ragged tails, wide and tall, X and Gram routes, a split view,
+    with and without the RMS-keeping scale, from a nonzero v."""
+    shapes = [(256, 4104, None, None), (4104, 256, None, None), (96, 96, None, None),
+              (240, 512, (2, 120, 512), (40, 80)), (300, 2048, None, None, 1.5, 0.05)]
+    entries = random_entries(shapes, seed=27, normuon=True, b_std=1e-3)
+    kw = dict(normuon=True, beta2=0.95, eps=1e-8, rms_target=rms_target)
+    gpu, status, plan = run_muon_gpu(entries, lr=0.02, precision="bf16", **kw)
+    if not rms_target:  # one launch more than the single rows kernel: the statistics pass
+        fp32w = [dict(e, w=e["w"].float()) for e in entries]
+        _, _, plan32 = run_muon_gpu(fp32w, lr=0.02, precision="bf16", **kw)
+        assert (B.gbo_muon_plan_info(plan)["launches_per_step"]
+                == B.gbo_muon_plan_info(plan32)["launches_per_step"] + 1)
+    ora = run_muon_oracle(entries, lr=0.02, **kw)
+    assert status == 0
+    check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
+
+
 @pytest.mark.parametrize("precision", ["bf16", "f32"])
 @pytest.mark.parametrize("route", ["x", "gram"])
 def test_skip_zero_and_nonfinite(route, precision):
