@@ -249,7 +249,9 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     (Muon, AdamW) flat gradient buffer pairs, each bound to its own plan:
     the upload of step n + 1's gradients runs on a copy stream into one pair
     while step n computes on the other, as a trainer overlaps its input
-    transfers.  The upload starts once step n's momentum pass is done
+    transfers: the Muon gradients first, which step n + 1 needs at its start,
+    then the AdamW gradients, which it needs only for its clip and AdamW
+    after its GEMMs.  The upload starts once step n's momentum pass is done
     (``after_momentum[b]``, recorded by buffer pair b's plan), so it runs
     under the Newton-Schulz GEMMs, which leave most of the HBM bandwidth
     free, rather than under the memory-bound momentum pass.  Every step's
@@ -264,17 +266,21 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     h_ag.copy_(ag_flat)
     compute = torch.cuda.current_stream()
     copy = torch.cuda.Stream()
-    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    copied = [torch.cuda.Event(), torch.cuda.Event()]       # Muon gradients in
+    copied_adam = [torch.cuda.Event(), torch.cuda.Event()]  # AdamW gradients in
     done = [torch.cuda.Event(), torch.cuda.Event()]
 
     def upload(b, after=None):
+        # the Muon gradients first: a step needs them at its start, its AdamW
+        # gradients only after the Newton-Schulz GEMMs
         copy.wait_event(done[b])  # the step that last read buffer pair b has finished
         if after is not None:
             copy.wait_event(after)
         with torch.cuda.stream(copy):
             bufs[b][0].copy_(h_g, non_blocking=True)
+            copied[b].record(copy)
             bufs[b][1].copy_(h_ag, non_blocking=True)
-        copied[b].record(copy)
+        copied_adam[b].record(copy)
 
     # the upload alone (after one untimed copy), to tell a copy-bound host
     # from a compute-bound one: the host side of this path varies between hosts
@@ -291,7 +297,7 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     for n in range(n_steps):
         b = n % 2
         compute.wait_event(copied[b])
-        step(buf=b)
+        step(buf=b, before_adamw=copied_adam[b])
         done[b].record(compute)
         if n + 1 < n_steps:
             upload(1 - b, after_momentum[b])
@@ -363,7 +369,7 @@ def run_ours(args):
     after_momentum = [torch.cuda.Event(), torch.cuda.Event()]
     gbo.gbo_muon_plan_set_event(plan, 0, after_momentum[0])
 
-    def step(record=None, buf=0):
+    def step(record=None, buf=0, before_adamw=None):
         """One optimizer step: Muon, then clip + AdamW, on one stream.  With
         --overlap the AdamW path (independent of the Muon path) runs on a side
         stream that starts once the momentum kernel is done, overlapping the
@@ -378,6 +384,8 @@ def run_ours(args):
         adam_stream = side if overlap else stream
         if overlap:
             side.wait_event(after_momentum[buf])
+        if before_adamw is not None:  # this step's AdamW gradients have landed
+            adam_stream.wait_event(before_adamw)
         if record is not None:
             record[0].record(adam_stream)
         gbo.gbo_clip_norm(adam_grads, 1.0, total, coef, cws, dev_status=status, stream=adam_stream)
