@@ -108,6 +108,7 @@ def lib():
                                      c_void_p, c_void_p]),
         "gbo_testing_wait_timeout": (c_int32, [c_void_p, ctypes.c_uint32, c_void_p]),
         "gbo_testing_set_small_chain": (c_int32, [c_int32]),
+        "gbo_testing_set_fused_gram": (c_int32, [c_int32]),
         "gbo_last_error": (ctypes.c_char_p, []),
         "gbo_abi_version": (c_int32, []),
         "gbo_struct_size": (c_size_t, [c_int32]),
@@ -371,6 +372,14 @@ def gbo_testing_set_small_chain(enable):
     iterations of matrices with p <= 192 (bf16) in one on-chip chain launch.
     Returns the previous setting."""
     return bool(lib().gbo_testing_set_small_chain(1 if enable else 0))
+
+
+def gbo_testing_set_fused_gram(enable):
+    """Whether plans created from now on run the Gram of the chain's wide
+    matrices with p <= 128 inside the chain launch (X_0 streamed through
+    shared memory) rather than as a launch of its own.  Returns the previous
+    setting."""
+    return bool(lib().gbo_testing_set_fused_gram(1 if enable else 0))
 
 
 def gbo_testing_wait_timeout(dev_status, limit_us, stream=None):

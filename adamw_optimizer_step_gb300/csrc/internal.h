@@ -181,10 +181,19 @@ int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &glob
 int launch_ns_gemm_tf32(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
                         void *stream, int64_t *n_launch);
 // kChain jobs (bf16, p <= kChainMaxP): opA = P_0, opB = A_0, out = Q_k
-// regions; every job of one call has the same steps and abc.
+// regions; or, for a wide class of p <= 128 (kind kKindGram), opA = X_0:
+// the Gram runs on chip too.  Every job of one call has the same steps and
+// abc.
 constexpr int kChainMaxP = 192;
 int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
                        void *stream, int64_t *n_launch);
+// The chain kernel's launch groups: the Gram on chip (p <= 128, wide),
+// p <= 128, 128 < p <= kChainMaxP.
+enum ChainGeometry : int32_t { kChainFused = 0, kChainOne = 1, kChainTwo = 2 };
+int chain_geometry(const GemmJob &J);
+// FLOPs of the on-chip Gram of one p x q matrix: a 128 x 128 tile, K = q
+// padded to 64, and with c_0 != 0 the square of A_0 (K = p padded to 64).
+double tc_fused_gram_flops(int p, int q, const float *abc);
 // FLOPs the chain kernel executes for one p x p matrix (p <= kChainMaxP)
 // over k iterations with coefficients abc: 128 x 128 (or x 256) tiles for
 // p <= 128, two 128 x 192 row halves for larger p, K padded to 64.
@@ -199,8 +208,9 @@ double tc_executed_flops(int p, int q, bool square, bool tall);
 // of `squares` iterations with c != 0, the product with X_0.
 double tc_gram_route_flops(int p, int q, int k, int squares, bool tall);
 // The same when the p x p chain runs on chip: the Gram (and the square of
-// A_0 when c_0 != 0), the chain, the product with X_0.
-double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall);
+// A_0 when c_0 != 0) on the tile kernel or, `fused`, on chip, the chain,
+// the product with X_0.
+double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall, bool fused);
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);

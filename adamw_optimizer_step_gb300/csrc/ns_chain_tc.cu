@@ -18,6 +18,17 @@
 // triangle, as the tile kernel's epilogue stores symmetric results, because
 // the product of a tall X_0 with Q_k takes Q_k's rows as its columns.
 //
+// For a matrix with p <= 128 the Gram itself runs here too (kFuse): X_0
+// streams in by TMA, 64 columns at a time (64 rows of an X_0 held tall, q x
+// p, whose Gram X_0^T X_0 reads both operands MN-major), through a ring of
+// six 16 KB stages laid over the slot's own P, A and Q (free until the
+// Gram's epilogue writes them), the MMAs accumulate the Gram in the slot's
+// TMEM columns, and the epilogue folds in the pre-normalisation factor and
+// writes A_0, P_0 and Q_1 = P_0 (with c != 0, A_0 and then P_0 from an
+// on-chip square).  The MMA issuer and the epilogue warps then poll both
+// slots instead of taking them in turn, so one slot's X_0 stream (bound by
+// HBM) runs under the other slot's chain (bound by latency).
+//
 // Two geometries (template parameter kH, 128-row halves of a matrix):
 //   kH = 1  p <= 128: 128 x 128 matrices (32 KB each), two matrices in
 //           flight per CTA so the epilogue of one slot's product overlaps
@@ -29,7 +40,7 @@
 //           not fit TMEM together)
 // Persistent CTA (320 threads, one per SM):
 //   warp 0      TMA loads (one lane): A_0, P_0 (into P and Q) of the next
-//               matrix of each slot
+//               matrix of each slot, or its X_0 blocks (kFuse)
 //   warp 1      TMEM owner and MMA issuer (one lane), alternating slots
 //   warps 2..9  epilogue, two per TMEM lane quarter, each taking half of
 //               the column blocks of the quarter's rows
@@ -57,6 +68,10 @@ constexpr int kCEpiWarps = 8;
 constexpr int kCThreads = 64 + 32 * kCEpiWarps;
 constexpr int kMaxOps = 4 * GBO_MAX_NS_STEPS + 1;
 constexpr int kCTmemCols = 512;
+constexpr int kRing = 6;                 // X_0 blocks in flight per slot (kFuse)
+constexpr int kRingBytes = 128 * CK * 2; // one 128-row, 64-column bf16 block of X_0
+constexpr int kNBars = 11 + 4 * kRing;   // loaded, mmad, epid, qdone, freed (2 each), drain, full/empty rings
+constexpr int kNClocks = 10;             // idle-stretch starts: one per warp
 
 // Shared-memory geometry of one slot matrix (K-major rows of 128 bytes in
 // 64-column blocks, 128-byte swizzle, as TMA writes it).
@@ -68,13 +83,19 @@ struct Geo {
   static constexpr int Mat = KB * Blk;           // 32 KB or 72 KB
   static constexpr int Slots = kH == 1 ? 2 : 1;
   static constexpr int SlotSize = 3 * Mat;       // P, A (or T), Q
-  static constexpr int Smem = 1024 /*align*/ + Slots * SlotSize + 256 /*barriers*/;
+  static constexpr int Smem = 1024 /*align*/ + Slots * SlotSize + 512 /*barriers*/;
   static constexpr int WarpBlocks = R / 64;      // 32-column blocks per epilogue warp and row block
   // kind::f16: fp32 accumulator, bf16 A and B, A K-major, B MN-major, M = 128, N = R
   static constexpr uint32_t Idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                     ((uint32_t)(R >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  // the Gram: A and B K-major (rows of a wide X_0) or both MN-major (an
+  // X_0 held tall)
+  static constexpr uint32_t IdescK = Idesc & ~(1u << 16);
+  static constexpr uint32_t IdescMN = Idesc | (1u << 15);
 };
 static_assert(Geo<1>::Smem <= 232448 && Geo<2>::Smem <= 232448, "shared memory per CTA");
+static_assert(kRing * kRingBytes <= Geo<1>::SlotSize, "the X_0 ring lies within one slot");
+static_assert((kNBars + 1 + kNClocks) * 8 <= 512, "barriers, TMEM address, abort flag and idle clocks");
 
 // Products of slot matrices (L R: L read K-major, R MN-major) and
 // epilogues of one op of the chain.
@@ -83,6 +104,7 @@ enum ChainMma : int32_t {
   kMmaPAQ = 1,  // acc0 = P A, acc1 = P Q (kH = 1)
   kMmaAA = 2,   // acc0 = A A
   kMmaPQ = 3,   // acc0 = P Q
+  kMmaGram = 4, // acc0 = X_0 X_0^T, streamed (kFuse)
 };
 enum ChainEpi : int32_t {
   kEpiT = 0,    // A <- acc0 (T)
@@ -93,6 +115,9 @@ enum ChainEpi : int32_t {
   kEpiSq = 5,   // P <- a I + b A + c acc0 (acc0 = A A)
   kEpiOut = 6,  // Q <- acc0, then Q is stored to HBM
   kEpiQ = 7,    // Q <- acc0 (kH = 2)
+  kEpiGram = 8, // A <- s^2 acc0, P and Q <- a I + b s^2 acc0 (kFuse, c == 0)
+  kEpiGramA = 9,// A <- s^2 acc0 (kFuse, c != 0)
+  kEpiSqQ = 10, // P and Q <- a I + b A + c acc0 (acc0 = A A; kFuse, c != 0)
 };
 
 struct ChainOp {
@@ -104,20 +129,26 @@ struct ChainParams {
   CUtensorMap mapP[kMaxClassesPerLaunch];  // P_0 (loads: 64-column boxes of R rows, 128-byte swizzle)
   CUtensorMap mapA[kMaxClassesPerLaunch];  // A_0
   CUtensorMap mapQ[kMaxClassesPerLaunch];  // Q_k (stores, same boxes)
+  CUtensorMap mapX[kMaxClassesPerLaunch];  // X_0 (kFuse): p x q in 64-column boxes of 128 rows, or q x p
+                                           // (tall) in 64 x 64 boxes
   int64_t mat_start[kMaxClassesPerLaunch + 1];
   int32_t p[kMaxClassesPerLaunch];
+  int32_t q[kMaxClassesPerLaunch];         // kFuse: the Gram's K (columns of X_0, rows when tall)
+  int32_t tall[kMaxClassesPerLaunch];      // kFuse: X_0 held q x p
+  int32_t sub0[kMaxClassesPerLaunch];      // kFuse: the class's first matrix in the pre-normalisation factors
   int32_t n;
   int32_t n_ops;
   ChainOp ops[kMaxOps];
 };
 
 template <int kH>
-__device__ __forceinline__ void chain_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void chain_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate,
+                                          uint32_t idesc = Geo<kH>::Idesc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(Geo<kH>::Idesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -223,20 +254,126 @@ __device__ __forceinline__ int chain_class(const ChainParams &P, int64_t t) {
   return c;
 }
 
-template <int kH>
+// One op's epilogue for the rows of one TMEM lane quarter and column blocks
+// cb0 .. cb1 - 1 of a slot's matrices at mP, mA, mQ; acc0 is the quarter's
+// first accumulator column of the slot, s2 the square of the matrix's
+// pre-normalisation factor (the Gram ops).
+template <int kH, bool kFuse>
+__device__ __forceinline__ void chain_epilogue(const ChainOp &o, uint32_t acc_row, int quarter, int lane, int cb0,
+                                               int cb1, int p, float s2, uint32_t mP, uint32_t mA, uint32_t mQ) {
+  using G = Geo<kH>;
+  for (int h = 0; h < kH; ++h) {
+    const int i0 = h * 128 + quarter * 32, i = i0 + lane;
+    if (i0 >= G::R) continue;  // kH = 2: rows 192 .. 255 are padding
+    const uint32_t acc0 = acc_row + (uint32_t)(h * 256);
+    const uint32_t acc1 = acc0 + 128;
+    // whole rows for the next products; Q_k: blocks on or above the
+    // diagonal, mirrored
+    for (int cb = o.epi == kEpiOut ? max(i0 / 32, cb0) : cb0; cb < cb1; ++cb) {
+      const int col0 = cb * 32;
+      float v[32];
+      tmem_ld32(acc0 + col0, v);
+      float w[32];
+      switch (o.epi) {
+        case kEpiT:
+        case kEpiA:
+          put_full<kH>(mA, i, col0, p, v);
+          break;
+        case kEpiQ:
+          put_full<kH>(mQ, i, col0, p, v);
+          break;
+        case kEpiOut:
+          put_sym<kH>(mQ, i, i0, col0, p, v);
+          break;
+        case kEpiTQ:
+          put_full<kH>(mA, i, col0, p, v);
+          tmem_ld32(acc1 + col0, w);
+          put_full<kH>(mQ, i, col0, p, w);
+          break;
+        case kEpiAP:
+        case kEpiP:
+#pragma unroll
+          for (int k = 0; k < 32; ++k) w[k] = o.b * v[k] + (i == col0 + k ? o.a : 0.f);
+          if (o.epi == kEpiAP) put_full<kH>(mA, i, col0, p, v);
+          put_full<kH>(mP, i, col0, p, w);
+          break;
+        case kEpiGram: {  // A first, then P and Q from a second read of the accumulator
+          if constexpr (!kFuse) break;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] *= s2;
+          put_full<kH>(mA, i, col0, p, v);
+          tmem_ld32(acc0 + col0, v);
+          const float bs2 = o.b * s2;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = bs2 * v[k] + (i == col0 + k ? o.a : 0.f);
+          put_full<kH>(mP, i, col0, p, v);
+          put_full<kH>(mQ, i, col0, p, v);
+          break;
+        }
+        case kEpiGramA:
+          if constexpr (!kFuse) break;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] *= s2;
+          put_full<kH>(mA, i, col0, p, v);
+          break;
+        default: {  // kEpiSq, kEpiSqQ
+          float am[32];
+          get_row<kH>(mA, i, col0, am);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) w[k] = o.c * v[k] + o.b * am[k] + (i == col0 + k ? o.a : 0.f);
+          put_full<kH>(mP, i, col0, p, w);
+          if (kFuse && o.epi == kEpiSqQ) put_full<kH>(mQ, i, col0, p, w);
+          break;
+        }
+      }
+    }
+  }
+}
+
+// Warp-uniform test of an mbarrier phase (lane 0 polls, the warp follows).
+__device__ __forceinline__ bool warp_try(uint32_t bar, uint32_t parity, int lane) {
+  int ok = 0;
+  if (lane == 0) ok = mbar_try(bar, parity) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// A polling loop's bound: true once nothing has moved for kWaitNs.  The
+// start of the idle stretch is kept in shared memory (at t0), not in a
+// register across the loop.
+struct IdleClock {
+  volatile uint64_t *t0;
+  uint32_t spin = 0;
+  __device__ __forceinline__ explicit IdleClock(uint64_t *at) : t0(at) {}
+  __device__ __forceinline__ bool expired(bool moved) {
+    if (moved) {
+      spin = 0;
+      return false;
+    }
+    if (spin++ == 0) *t0 = global_ns();
+    return (spin & 255u) == 0 && global_ns() - *t0 > kWaitNs;
+  }
+};
+
+template <int kH, bool kFuse>
 __global__ void __launch_bounds__(kCThreads, 1)
 ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ PhaseArgs A) {
   using G = Geo<kH>;
+  static_assert(!kFuse || kH == 1, "the Gram runs on chip for p <= 128 only");
   constexpr int S = G::Slots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * G::SlotSize);
-  // bars: loaded[2], mmad[2], epid[2], qdone[2], freed[2], drain, then the
-  // TMEM address and the abort flag
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+  // bars: loaded[2], mmad[2], epid[2], qdone[2], freed[2], drain, full[2][kRing],
+  // empty[2][kRing], then the TMEM address and the abort flag, then one
+  // idle clock per warp
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNBars);
+  uint64_t *clocks = bars + kNBars + 1;
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
   const uint32_t loaded0 = smem_u32(bars), mmad0 = smem_u32(bars + 2), epid0 = smem_u32(bars + 4);
   const uint32_t qdone0 = smem_u32(bars + 6), freed0 = smem_u32(bars + 8), drain = smem_u32(bars + 10);
+  const uint32_t full0 = smem_u32(bars + 11), empty0 = smem_u32(bars + 11 + 2 * kRing);
+  auto full_bar = [&](int s, int st) { return full0 + (uint32_t)(8 * (s * kRing + st)); };
+  auto empty_bar = [&](int s, int st) { return empty0 + (uint32_t)(8 * (s * kRing + st)); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -245,6 +382,11 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
       mbar_init(epid0 + 8 * s, kCEpiWarps);
       mbar_init(qdone0 + 8 * s, kCEpiWarps);
       mbar_init(freed0 + 8 * s, 1);
+      if (kFuse)
+        for (int st = 0; st < kRing; ++st) {
+          mbar_init(full_bar(s, st), 1);
+          mbar_init(empty_bar(s, st), 1);
+        }
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -272,9 +414,10 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
 
   if (warp == 0) {
     if (lane == 0) {
-      int64_t armed[S];
-      for (int s = 0; s < S; ++s) armed[s] = -1;
-      for (int64_t g = 0; mat_of(g) < total && !*abort_flag; ++g) {
+      int64_t armed[S], ring_n[S];  // the loads of the slot's last matrix; X_0 blocks loaded
+      for (int s = 0; s < S; ++s) armed[s] = -1, ring_n[s] = 0;
+      bool stop = false;
+      for (int64_t g = 0; mat_of(g) < total && !stop && !*abort_flag; ++g) {
         const int s = (int)(g % S);
         const int64_t gs = g / S;  // the slot's matrix count so far
         if (gs >= 1 && !mbar_wait(freed0 + 8 * s, (uint32_t)((gs - 1) & 1))) {
@@ -284,57 +427,122 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
         const int64_t t = mat_of(g);
         const int c = chain_class(P, t);
         const int mat = (int)(t - P.mat_start[c]);
-        const uint32_t base = slots + s * G::SlotSize, bar = loaded0 + 8 * s;
-        mbar_expect_tx(bar, 3 * G::Mat);
-        armed[s] = gs;
-        for (int kb = 0; kb < G::KB; ++kb) {
-          tma_load_3d(base + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);               // P <- P_0
-          tma_load_3d(base + G::Mat + kb * G::Blk, &P.mapA[c], bar, kb * CK, 0, mat);      // A <- A_0
-          tma_load_3d(base + 2 * G::Mat + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);  // Q <- Q_1 = P_0
+        const uint32_t base = slots + s * G::SlotSize;
+        if constexpr (kFuse) {
+          // X_0 in blocks of 64 along K (a tall X_0's 64-row block as two
+          // 64 x 64 boxes, the second holding columns 64 .. 127); a stage is
+          // reloaded once the MMAs that read it have completed
+          const int nk = (P.q[c] + CK - 1) / CK;
+          for (int kb = 0; kb < nk; ++kb) {
+            const int64_t n = ring_n[s];
+            const int st = (int)(n % kRing);
+            if (n >= kRing && !mbar_wait(empty_bar(s, st), (uint32_t)((n / kRing - 1) & 1))) {
+              give_up();
+              stop = true;
+              break;
+            }
+            const uint32_t dst = base + st * kRingBytes;
+            mbar_expect_tx(full_bar(s, st), kRingBytes);
+            if (P.tall[c]) {
+              tma_load_3d(dst, &P.mapX[c], full_bar(s, st), 0, kb * CK, mat);
+              tma_load_3d(dst + kRingBytes / 2, &P.mapX[c], full_bar(s, st), CK, kb * CK, mat);
+            } else {
+              tma_load_3d(dst, &P.mapX[c], full_bar(s, st), kb * CK, 0, mat);
+            }
+            ring_n[s] = n + 1;
+          }
+        } else {
+          const uint32_t bar = loaded0 + 8 * s;
+          mbar_expect_tx(bar, 3 * G::Mat);
+          armed[s] = gs;
+          for (int kb = 0; kb < G::KB; ++kb) {
+            tma_load_3d(base + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);               // P <- P_0
+            tma_load_3d(base + G::Mat + kb * G::Blk, &P.mapA[c], bar, kb * CK, 0, mat);      // A <- A_0
+            tma_load_3d(base + 2 * G::Mat + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);  // Q <- Q_1 = P_0
+          }
         }
       }
       if (*abort_flag)  // let the copies armed here land before shared memory goes away
-        for (int s = 0; s < S; ++s)
+        for (int s = 0; s < S; ++s) {
           if (armed[s] >= 0) (void)mbar_wait(loaded0 + 8 * s, (uint32_t)(armed[s] & 1));
+          for (int64_t n = ring_n[s] > kRing ? ring_n[s] - kRing : 0; n < ring_n[s]; ++n)
+            (void)mbar_wait(full_bar(s, (int)(n % kRing)), (uint32_t)((n / kRing) & 1));
+        }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int64_t g[S];
-      int op[S];
+      int64_t g[S], ring_c[S];
+      int op[S], kb[S];
       uint32_t u[S];
-      for (int s = 0; s < S; ++s) g[s] = s, op[s] = 0, u[s] = 0;
+      for (int s = 0; s < S; ++s) g[s] = s, ring_c[s] = 0, op[s] = 0, kb[s] = 0, u[s] = 0;
       bool issued = false;
+      IdleClock idle(clocks + warp);
       for (bool any = true; any && !*abort_flag;) {
         any = false;
+        bool moved = false;
         for (int s = 0; s < S && !*abort_flag; ++s) {
           const int64_t t = mat_of(g[s]);
           if (t >= total) continue;
           any = true;
-          // the slot's previous epilogue has read its accumulators and
-          // written the operands; a new matrix's loads have landed
-          if (u[s] > 0 && !mbar_wait(epid0 + 8 * s, (u[s] - 1) & 1)) { give_up(); break; }
-          if (op[s] == 0 && !mbar_wait(loaded0 + 8 * s, (uint32_t)((g[s] / S) & 1))) { give_up(); break; }
-          tc_fence_after();
-          const int kit = (P.p[chain_class(P, t)] + CK - 1) / CK;
           const uint32_t base = slots + s * G::SlotSize;
-          const uint32_t mP = base, mA = base + G::Mat, mQ = base + 2 * G::Mat;
           const uint32_t acc = tmem_base + (uint32_t)(s * 256);
-          const int mma = P.ops[op[s]].mma;
-          for (int h = 0; h < kH; ++h) {
-            const uint32_t d = acc + (uint32_t)(h * 256);
-            if (mma == kMmaPA) chain_product<kH>(d, mP, mA, kit, h);
-            else if (mma == kMmaAA) chain_product<kH>(d, mA, mA, kit, h);
-            else if (mma == kMmaPQ) chain_product<kH>(d, mP, mQ, kit, h);
-            else {  // kMmaPAQ
-              chain_product<kH>(d, mP, mA, kit, h);
-              chain_product<kH>(d + 128, mP, mQ, kit, h);
+          if (kFuse && op[s] == 0) {
+            // the Gram, block by block as X_0 lands, once the slot's
+            // previous matrix's last epilogue has read the accumulator
+            if (kb[s] == 0 && u[s] > 0 && !mbar_try(epid0 + 8 * s, (u[s] - 1) & 1)) continue;
+            const int c = chain_class(P, t);
+            const int nk = (P.q[c] + CK - 1) / CK;
+            // wide: K-major rows, a K step 32 bytes along them; tall: K is
+            // the stage's rows (16 rows = 2048 bytes a step), its two 64-column
+            // halves 8 KB apart
+            const bool tall = P.tall[c] != 0;
+            const uint32_t lbo = tall ? kRingBytes / 2 : 16, kstep = tall ? 2048 >> 4 : 32 >> 4;
+            const uint32_t idesc = tall ? G::IdescMN : G::IdescK;
+            while (kb[s] < nk) {
+              const int st = (int)(ring_c[s] % kRing);
+              if (!mbar_try(full_bar(s, st), (uint32_t)((ring_c[s] / kRing) & 1))) break;
+              tc_fence_after();
+              const uint64_t d = smem_desc(base + (uint32_t)(st * kRingBytes), lbo, 1024);
+#pragma unroll
+              for (int k = 0; k < CK / 16; ++k)
+                chain_mma<kH>(acc, d + k * kstep, d + k * kstep, (kb[s] | k) != 0, idesc);
+              mma_commit_one(empty_bar(s, st));
+              ++kb[s];
+              ++ring_c[s];
+              moved = issued = true;
+            }
+            if (kb[s] < nk) continue;
+            kb[s] = 0;
+          } else {
+            // the slot's previous epilogue has read its accumulators and
+            // written the operands; a new matrix's loads have landed
+            if (kFuse) {
+              if (!mbar_try(epid0 + 8 * s, (u[s] - 1) & 1)) continue;
+            } else {
+              if (u[s] > 0 && !mbar_wait(epid0 + 8 * s, (u[s] - 1) & 1)) { give_up(); break; }
+              if (op[s] == 0 && !mbar_wait(loaded0 + 8 * s, (uint32_t)((g[s] / S) & 1))) { give_up(); break; }
+            }
+            tc_fence_after();
+            const int kit = (P.p[chain_class(P, t)] + CK - 1) / CK;
+            const uint32_t mP = base, mA = base + G::Mat, mQ = base + 2 * G::Mat;
+            const int mma = P.ops[op[s]].mma;
+            for (int h = 0; h < kH; ++h) {
+              const uint32_t d = acc + (uint32_t)(h * 256);
+              if (mma == kMmaPA) chain_product<kH>(d, mP, mA, kit, h);
+              else if (mma == kMmaAA) chain_product<kH>(d, mA, mA, kit, h);
+              else if (mma == kMmaPQ) chain_product<kH>(d, mP, mQ, kit, h);
+              else {  // kMmaPAQ
+                chain_product<kH>(d, mP, mA, kit, h);
+                chain_product<kH>(d + 128, mP, mQ, kit, h);
+              }
             }
           }
-          issued = true;
+          issued = moved = true;
           mma_commit_one(mmad0 + 8 * s);
           ++u[s];
           if (++op[s] == P.n_ops) op[s] = 0, g[s] += S;
         }
+        if (kFuse && any && idle.expired(moved)) give_up();
       }
       if (*abort_flag && issued) {  // the outstanding MMAs complete before TMEM is released
         mma_commit_one(drain);
@@ -349,65 +557,37 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
     int op[S];
     uint32_t u[S];
     for (int s = 0; s < S; ++s) g[s] = s, op[s] = 0, u[s] = 0;
-    for (bool any = true; any && !*abort_flag;) {
+    bool stop = false;
+    IdleClock idle(clocks + warp);
+    for (bool any = true; any && !stop && !*abort_flag;) {
       any = false;
-      for (int s = 0; s < S && !*abort_flag; ++s) {
+      bool moved = false;
+      for (int s = 0; s < S && !stop && !*abort_flag; ++s) {
         const int64_t t = mat_of(g[s]);
         if (t >= total) continue;
         any = true;
-        if (!mbar_wait(mmad0 + 8 * s, u[s] & 1)) { give_up(); break; }
+        if (kFuse) {
+          if (!warp_try(mmad0 + 8 * s, u[s] & 1, lane)) continue;
+          // every lane's own acquire of the completed phase (it cannot move
+          // on before this warp's arrival, so the wait returns at once)
+          (void)mbar_wait(mmad0 + 8 * s, u[s] & 1);
+        } else if (!mbar_wait(mmad0 + 8 * s, u[s] & 1)) {
+          give_up();
+          stop = true;
+          break;
+        }
         tc_fence_after();
         const int c = chain_class(P, t);
-        const int p = P.p[c];
         const ChainOp o = P.ops[op[s]];
         const uint32_t base = slots + s * G::SlotSize;
         const uint32_t mP = base, mA = base + G::Mat, mQ = base + 2 * G::Mat;
-        for (int h = 0; h < kH; ++h) {
-          const int i0 = h * 128 + quarter * 32, i = i0 + lane;
-          if (i0 >= G::R) continue;  // kH = 2: rows 192 .. 255 are padding
-          const uint32_t acc0 = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(s * 256 + h * 256);
-          const uint32_t acc1 = acc0 + 128;
-          // whole rows for the next products; Q_k: blocks on or above the
-          // diagonal, mirrored
-          for (int cb = o.epi == kEpiOut ? max(i0 / 32, cb0) : cb0; cb < cb1; ++cb) {
-            const int col0 = cb * 32;
-            float v[32];
-            tmem_ld32(acc0 + col0, v);
-            float w[32];
-            switch (o.epi) {
-              case kEpiT:
-              case kEpiA:
-                put_full<kH>(mA, i, col0, p, v);
-                break;
-              case kEpiQ:
-                put_full<kH>(mQ, i, col0, p, v);
-                break;
-              case kEpiOut:
-                put_sym<kH>(mQ, i, i0, col0, p, v);
-                break;
-              case kEpiTQ:
-                put_full<kH>(mA, i, col0, p, v);
-                tmem_ld32(acc1 + col0, w);
-                put_full<kH>(mQ, i, col0, p, w);
-                break;
-              case kEpiAP:
-              case kEpiP:
-#pragma unroll
-                for (int k = 0; k < 32; ++k) w[k] = o.b * v[k] + (i == col0 + k ? o.a : 0.f);
-                if (o.epi == kEpiAP) put_full<kH>(mA, i, col0, p, v);
-                put_full<kH>(mP, i, col0, p, w);
-                break;
-              default: {  // kEpiSq
-                float am[32];
-                get_row<kH>(mA, i, col0, am);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) w[k] = o.c * v[k] + o.b * am[k] + (i == col0 + k ? o.a : 0.f);
-                put_full<kH>(mP, i, col0, p, w);
-                break;
-              }
-            }
-          }
+        float s2 = 1.f;
+        if (kFuse && (o.epi == kEpiGram || o.epi == kEpiGramA)) {
+          const float al = A.alpha[P.sub0[c] + (t - P.mat_start[c])];
+          s2 = al * al;
         }
+        chain_epilogue<kH, kFuse>(o, tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(s * 256), quarter, lane,
+                           cb0, cb1, P.p[c], s2, mP, mA, mQ);
         // the writes reach the tensor cores' and TMA's proxy; the
         // accumulators have been read
         fence_async_smem();
@@ -419,10 +599,14 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
           if (lane == 0) mbar_arrive(qdone0 + 8 * s);
           if (warp == 2) {
             const uint32_t qpar = (uint32_t)((g[s] / S) & 1);
-            if (!mbar_wait(qdone0 + 8 * s, qpar)) { give_up(); break; }
+            if (!mbar_wait(qdone0 + 8 * s, qpar)) {
+              give_up();
+              stop = true;
+              break;
+            }
             if (lane == 0) {
               const int mat = (int)(t - P.mat_start[c]);
-              for (int kb = 0; kb * CK < p; ++kb) tma_store_3d(&P.mapQ[c], mQ + kb * G::Blk, kb * CK, 0, mat);
+              for (int kb = 0; kb * CK < P.p[c]; ++kb) tma_store_3d(&P.mapQ[c], mQ + kb * G::Blk, kb * CK, 0, mat);
               bulk_commit();
               bulk_wait_read<0>();
               mbar_arrive(freed0 + 8 * s);
@@ -431,8 +615,17 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
           }
         }
         if (lane == 0) mbar_arrive(epid0 + 8 * s);
+        moved = true;
         ++u[s];
         if (++op[s] == P.n_ops) op[s] = 0, g[s] += S;
+      }
+      if (kFuse && any && !stop) {
+        int late = 0;
+        if (lane == 0) late = idle.expired(moved) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, late, 0)) {
+          if (lane == 0) give_up();
+          stop = true;
+        }
       }
     }
     if (lane == 0) bulk_wait_all();  // this warp's stores complete before the kernel ends
@@ -475,16 +668,30 @@ int chain_ops(int kh, int k, const float *abc, ChainOp *ops) {
   return n;
 }
 
+// The ops of a chain that starts from X_0 (kFuse): the Gram, with c != 0 the
+// square of A_0 that gives P_0, then the chain's own ops.
+int fused_ops(int k, const float *abc, ChainOp *ops) {
+  int n = 0;
+  if (abc[2] != 0.f) {
+    ops[n++] = ChainOp{kMmaGram, kEpiGramA, abc[0], abc[1], abc[2]};
+    ops[n++] = ChainOp{kMmaAA, kEpiSqQ, abc[0], abc[1], abc[2]};
+  } else {
+    ops[n++] = ChainOp{kMmaGram, kEpiGram, abc[0], abc[1], 0.f};
+  }
+  return n + chain_ops(1, k, abc, ops + n);
+}
+
 int chain_halves(int p) { return p <= 128 ? 1 : 2; }
 
-template <int kH>
+template <int kH, bool kFuse>
 int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count, void *stream,
                     int64_t *n_launch) {
   using G = Geo<kH>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(ns_chain_kernel<kH>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::Smem);
+    attr_err =
+        cudaFuncSetAttribute(ns_chain_kernel<kH, kFuse>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::Smem);
   });
   if (attr_err != cudaSuccess) return (int)attr_err;
   for (int32_t j0 = 0; j0 < n_jobs; j0 += kMaxClassesPerLaunch) {
@@ -493,24 +700,35 @@ int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
     T.n = std::min(kMaxClassesPerLaunch, n_jobs - j0);
     const GemmJob &J0 = *jobs[j0];
     if (J0.steps < 2 || J0.steps > GBO_MAX_NS_STEPS || !J0.abc) return (int)cudaErrorInvalidValue;
-    T.n_ops = chain_ops(kH, J0.steps, J0.abc, T.ops);
+    T.n_ops = kFuse ? fused_ops(J0.steps, J0.abc, T.ops) : chain_ops(kH, J0.steps, J0.abc, T.ops);
     for (int k = 0; k < T.n; ++k) {
       const GemmJob &J = *jobs[j0 + k];
       const ShapeClass &C = *J.cls;
-      if (chain_halves(C.p) != kH || C.p > G::R || J.steps != J0.steps || J.abc != J0.abc)
+      const bool gram = J.kind == kKindGram || J.kind == kKindGramT;
+      if (chain_halves(C.p) != kH || C.p > G::R || J.steps != J0.steps || J.abc != J0.abc || gram != kFuse ||
+          (kFuse && (J.kind == kKindGramT) != (C.x_tall != 0)))
         return (int)cudaErrorInvalidValue;
       auto at = [&](const void *region) { return static_cast<char *>(const_cast<void *>(region)) + C.p_base * 2; };
-      const bool ok = encode_map(&T.mapP[k], at(J.opA), C.p, C.p, C.count, C.ldp, CK, G::R) &&
-                      encode_map(&T.mapA[k], at(J.opB), C.p, C.p, C.count, C.ldp, CK, G::R) &&
-                      encode_map(&T.mapQ[k], at(J.out), C.p, C.p, C.count, C.ldp, CK, G::R);
+      bool ok = encode_map(&T.mapQ[k], at(J.out), C.p, C.p, C.count, C.ldp, CK, G::R);
+      if (kFuse) {  // X_0 in x-space: count matrices of p rows (q when tall), row stride ld
+        char *x = static_cast<char *>(const_cast<void *>(J.opA)) + C.x_base * 2;
+        ok = ok && (C.x_tall ? encode_map(&T.mapX[k], x, C.p, C.q, C.count, C.ld, CK, CK)
+                             : encode_map(&T.mapX[k], x, C.q, C.p, C.count, C.ld, CK, 128));
+      } else {
+        ok = ok && encode_map(&T.mapP[k], at(J.opA), C.p, C.p, C.count, C.ldp, CK, G::R) &&
+             encode_map(&T.mapA[k], at(J.opB), C.p, C.p, C.count, C.ldp, CK, G::R);
+      }
       if (!ok) return (int)cudaErrorInvalidValue;
       T.p[k] = C.p;
+      T.q[k] = C.q;
+      T.tall[k] = C.x_tall;
+      T.sub0[k] = C.sub0;
       T.mat_start[k + 1] = T.mat_start[k] + C.count;
     }
     const int64_t total = T.mat_start[T.n];
     if (total == 0) continue;
     const unsigned grid = (unsigned)std::min<int64_t>(total, sm_count);  // one CTA per SM
-    ns_chain_kernel<kH><<<grid, kCThreads, G::Smem, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
+    ns_chain_kernel<kH, kFuse><<<grid, kCThreads, G::Smem, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
     count_launches(1);
     if (n_launch) ++*n_launch;
     const cudaError_t err = cudaGetLastError();
@@ -532,16 +750,31 @@ double tc_chain_flops(int p, int k, const float *abc) {
   return f;
 }
 
+double tc_fused_gram_flops(int p, int q, const float *abc) {
+  const double tile = 2.0 * 128 * 128;
+  return tile * (double)((q + CK - 1) / CK) * CK + (abc[2] != 0.f ? tile * (double)((p + CK - 1) / CK) * CK : 0.0);
+}
+
+int chain_geometry(const GemmJob &J) {
+  if (J.kind == kKindGram || J.kind == kKindGramT) return kChainFused;
+  return chain_halves(J.cls->p) == 1 ? kChainOne : kChainTwo;
+}
+
 int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count,
                        void *stream, int64_t *n_launch) {
-  std::vector<const GemmJob *> one, two;
+  std::vector<const GemmJob *> by[3];
   for (int32_t j = 0; j < n_jobs; ++j) {
     if (jobs[j]->cls->p > kChainMaxP) return (int)cudaErrorInvalidValue;
-    (chain_halves(jobs[j]->cls->p) == 1 ? one : two).push_back(jobs[j]);
+    by[chain_geometry(*jobs[j])].push_back(jobs[j]);
   }
-  const int err = launch_geometry<1>(one.data(), (int32_t)one.size(), args, sm_count, stream, n_launch);
+  int err = launch_geometry<1, true>(by[kChainFused].data(), (int32_t)by[kChainFused].size(), args, sm_count,
+                                     stream, n_launch);
   if (err) return err;
-  return launch_geometry<2>(two.data(), (int32_t)two.size(), args, sm_count, stream, n_launch);
+  err = launch_geometry<1, false>(by[kChainOne].data(), (int32_t)by[kChainOne].size(), args, sm_count, stream,
+                                  n_launch);
+  if (err) return err;
+  return launch_geometry<2, false>(by[kChainTwo].data(), (int32_t)by[kChainTwo].size(), args, sm_count, stream,
+                                   n_launch);
 }
 
 }  // namespace gbo

@@ -575,9 +575,11 @@ double tc_gram_route_flops(int p, int q, int k, int squares, bool tall) {
          product_flops(p, q, tall);
 }
 
-double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall) {
-  return sym_items_of(p) * item_flops(p, q) + (abc[2] != 0.f ? sym_items_of(p) * item_flops(p, p) : 0.0) +
-         tc_chain_flops(p, k, abc) + product_flops(p, q, tall);
+double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall, bool fused) {
+  const double gram = fused ? tc_fused_gram_flops(p, q, abc)
+                            : sym_items_of(p) * item_flops(p, q) +
+                                  (abc[2] != 0.f ? sym_items_of(p) * item_flops(p, p) : 0.0);
+  return gram + tc_chain_flops(p, k, abc) + product_flops(p, q, tall);
 }
 
 namespace {

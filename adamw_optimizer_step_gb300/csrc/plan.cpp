@@ -24,6 +24,7 @@ namespace gbo {
 
 static std::atomic<uint64_t> g_launches{0};
 static std::atomic<int32_t> g_small_chain{1};  // see gbo_testing_set_small_chain
+static std::atomic<int32_t> g_fused_gram{1};   // see gbo_testing_set_fused_gram
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 namespace {
@@ -126,7 +127,8 @@ struct gbo_plan {
   std::vector<float> abc;  // 3 * ns_steps
   bool any_c = false;
   bool any_gram = false;     // some class takes the Gram route
-  bool small_chain = true;   // Gram-route classes with p <= 128 run the on-chip chain (bf16)
+  bool small_chain = true;   // Gram-route classes with p <= kChainMaxP run the on-chip chain (bf16)
+  bool fused_gram = true;    // ... and those of p <= 128 held wide start it from X_0
   std::vector<DevSub> subs;  // sorted by shape class
   std::vector<ShapeClass> classes;
   int64_t n_tiles = 0, n_row_blocks = 0;
@@ -176,6 +178,11 @@ bool uses_chain(const gbo_plan *P, const ShapeClass &C) {
          P->opts.ns_steps >= 2;
 }
 
+// Of those, the classes of at most 128 rows run their Gram in the chain
+// kernel too, streaming X_0 through the shared memory of the matrix.
+bool fuses_gram(const gbo_plan *P, int p) { return P->fused_gram && p <= 128; }
+bool fuses_gram(const gbo_plan *P, const ShapeClass &C) { return uses_chain(P, C) && fuses_gram(P, C.p); }
+
 // Route of a p x q class: the Gram route needs k >= 2; AUTO takes it when it
 // executes at least 10% fewer FLOPs, counting the on-chip chain where the
 // class would run it (in practice: whenever q is clearly above p, and for
@@ -189,7 +196,7 @@ int32_t choose_route(const gbo_plan *P, int p, int q, bool tall) {
   double fx = 0;
   for (int it = 0; it < k; ++it) fx += tc_executed_flops(p, q, P->abc[3 * it + 2] != 0.f, x_tall);
   const bool chain = P->small_chain && P->x_dtype == GBO_BF16 && p <= kChainMaxP;
-  const double fg = chain ? tc_gram_chain_flops(p, q, k, P->abc.data(), x_tall)
+  const double fg = chain ? tc_gram_chain_flops(p, q, k, P->abc.data(), x_tall, fuses_gram(P, p))
                           : tc_gram_route_flops(p, q, k, squares(P), x_tall);
   return fg < 0.9 * fx ? kRouteGram : kRouteX;
 }
@@ -453,7 +460,8 @@ int validate_and_expand(gbo_plan *P) {
     double ex = 0;
     for (const ShapeClass &C : P->classes) {
       if (C.route == kRouteGram) {
-        ex += C.count * (uses_chain(P, C) ? tc_gram_chain_flops(C.p, C.q, o.ns_steps, P->abc.data(), C.x_tall != 0)
+        ex += C.count * (uses_chain(P, C) ? tc_gram_chain_flops(C.p, C.q, o.ns_steps, P->abc.data(),
+                                                                C.x_tall != 0, fuses_gram(P, C))
                                           : tc_gram_route_flops(C.p, C.q, o.ns_steps, squares(P), C.x_tall != 0));
         I.n_gram_route += C.count;
       } else {
@@ -490,9 +498,13 @@ struct TcStep {
 };
 
 // The tensor-core schedule of one Muon step (bf16 mode).  The X route takes
-// 2k steps (3 per iteration when c != 0), the Gram route 2k + 1; step i of
-// the step runs step i of both routes, whose classes and buffers are
-// disjoint.  With ws == nullptr the pointers are offsets (for counting).
+// 2k steps (3 per iteration when c != 0), the Gram route 2k + 1, or with the
+// on-chip chain three: the Gram (and the square of A_0 when c_0 != 0), the
+// chain, the last product.  A chain that runs its own Gram takes the chain's
+// step, so every class's last product shares a step.  Step i of the step
+// runs step i of both routes, whose classes and buffers are disjoint; steps
+// left empty are dropped.  With ws == nullptr the pointers are offsets (for
+// counting).
 std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
   const int k = P->opts.ns_steps;
   const bool normuon = P->opts.normuon != 0;
@@ -569,6 +581,20 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
       // A_0 = alpha^2 X_0 X_0^T and P_0;  Q_1 = P_0.  An iteration with c != 0
       // writes A only and takes P = a I + b A + c A^2 from a square of A.
       size_t i = 0;
+      if (fuses_gram(P, C)) {
+        // the Gram, the square of A_0 and every p x p product in one
+        // on-chip launch, in the step where the other classes' chains run
+        // (so that all last products share one step)
+        GemmJob J = job(&C, kChain, kGramK, 1, &P->abc[0], x[0], x[0], gQ[k & 1]);
+        J.steps = k;
+        J.abc = P->abc.data();
+        i = P->abc[2] != 0.f ? 2 : 1;
+        at(gs, i++, kPhaseProduct).jobs.push_back(J);
+        const int mode = normuon ? kProduct : kFinal;
+        at(gs, i++, mode == kFinal ? kPhaseFinal : kPhaseProduct)
+            .jobs.push_back(last_product(product(mode, 1, nullptr, gQ[k & 1], 0)));
+        continue;
+      }
       if (P->abc[2] == 0.f) {
         at(gs, i++, kPhaseGram).jobs.push_back(job(&C, kGramAP, kGramK, 1, &P->abc[0], x[0], x[0], gP[0], gA));
       } else {
@@ -612,16 +638,18 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
           .jobs.push_back(last_product(product(mode, 1, nullptr, gQ[k & 1], 0)));
     }
   }
-  std::vector<TcStep> steps(std::max(xs.size(), gs.size()));
-  for (size_t i = 0; i < steps.size(); ++i) {
+  std::vector<TcStep> steps;
+  for (size_t i = 0; i < std::max(xs.size(), gs.size()); ++i) {
+    TcStep st;
     if (i < gs.size()) {
-      steps[i].phase = gs[i].phase;
-      steps[i].jobs = gs[i].jobs;
+      st.phase = gs[i].phase;
+      st.jobs = gs[i].jobs;
     }
     if (i < xs.size()) {  // label by the X route where it has a step
-      steps[i].phase = xs[i].phase;
-      steps[i].jobs.insert(steps[i].jobs.end(), xs[i].jobs.begin(), xs[i].jobs.end());
+      st.phase = xs[i].phase;
+      st.jobs.insert(st.jobs.end(), xs[i].jobs.begin(), xs[i].jobs.end());
     }
+    if (!st.jobs.empty()) steps.push_back(st);  // steps the on-chip Gram left empty
   }
   return steps;
 }
@@ -629,10 +657,13 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
 // Kernel launches of one step of the schedule (classes go 8 to a launch,
 // pairs and single CTAs separately).
 int64_t tc_step_launches(const TcStep &st) {
-  int64_t single = 0, pair = 0;
-  for (const GemmJob &J : st.jobs) (single_mode(J.cls->p) ? single : pair)++;
+  int64_t single = 0, pair = 0, chain[3] = {0, 0, 0};
+  for (const GemmJob &J : st.jobs) {
+    if (J.mode == kChain) ++chain[chain_geometry(J)];
+    else (single_mode(J.cls->p) ? single : pair)++;
+  }
   auto groups = [](int64_t n) { return (n + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch; };
-  return groups(single) + groups(pair);
+  return groups(single) + groups(pair) + groups(chain[0]) + groups(chain[1]) + groups(chain[2]);
 }
 
 cudaEvent_t take_event(gbo_plan *P) {
@@ -710,6 +741,7 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   for (int it = 0; it < k; ++it) P->any_c |= P->abc[3 * it + 2] != 0.f;
   P->x_dtype = opts->precision == GBO_NS_F32 ? GBO_F32 : GBO_BF16;
   P->small_chain = g_small_chain.load() != 0;
+  P->fused_gram = g_fused_gram.load() != 0;
   const int rc = validate_and_expand(P);
   if (rc != GBO_OK) {
     delete P;
@@ -891,6 +923,8 @@ int gbo_normuon_rownorm(const float *O, int64_t rows, int64_t cols, float *row_v
 }
 
 int32_t gbo_testing_set_small_chain(int32_t enable) { return g_small_chain.exchange(enable != 0 ? 1 : 0); }
+
+int32_t gbo_testing_set_fused_gram(int32_t enable) { return g_fused_gram.exchange(enable != 0 ? 1 : 0); }
 
 int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream) {
   if (!dev_status || !aligned(dev_status, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_status is NULL or misaligned");

@@ -16,6 +16,7 @@ import argparse
 import hashlib
 import json
 import os
+import statistics
 import subprocess
 import sys
 import tempfile
@@ -34,7 +35,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
@@ -257,7 +258,11 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     free, rather than under the memory-bound momentum pass.  Every step's
     copy and read stay inside the timed region.  Returns (steps/s over all
     ranks, bytes copied in per step, the upload's GB/s when it runs
-    alone)."""
+    alone, each step's host wall time in ms up to its norm read).  A single
+    step has been seen to stall for ~150 ms on a host whose previous process
+    had just exited (the upload's wait, not the GPU's work): the per-step
+    times show such a stall, and the default 40 steps bound its weight in
+    the mean."""
     import torch
     g_flat, ag_flat = bufs[0]
     h_g = torch.empty(g_flat.numel(), dtype=g_flat.dtype, pin_memory=True)
@@ -294,6 +299,7 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     barrier(world)
     t0 = time.perf_counter()
     upload(0)
+    wall, t_prev = [], t0
     for n in range(n_steps):
         b = n % 2
         compute.wait_event(copied[b])
@@ -302,9 +308,12 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
         if n + 1 < n_steps:
             upload(1 - b, after_momentum[b])
         _ = float(total.item())  # the step's result on the host
+        t_now = time.perf_counter()
+        wall.append((t_now - t_prev) * 1e3)
+        t_prev = t_now
     torch.cuda.synchronize()
     e2e_t = max_over_ranks(time.perf_counter() - t0, world)
-    return aggregate(n_steps, e2e_t, world), h2d, up_gbs
+    return aggregate(n_steps, e2e_t, world), h2d, up_gbs, wall
 
 
 def run_ours(args):
@@ -434,7 +443,7 @@ def run_ours(args):
         raise RuntimeError("device status %d during the timed steps" % int(status.item()))
 
     # end to end: gradients from pinned host memory, norm read back
-    e2e_value, h2d, up_gbs = None, 0, None
+    e2e_value, h2d, up_gbs, e2e_wall = None, 0, None, []
     if args.e2e_steps > 0:
         g_flat2, ag_flat2 = torch.empty_like(g_flat), torch.empty_like(ag_flat)
         entries2, off = [], 0
@@ -449,8 +458,8 @@ def run_ours(args):
         plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon)
         bound.append((plan2, params2, [p[1] for p in params2]))
         gbo.gbo_muon_plan_set_event(plan2, 0, after_momentum[1])
-        e2e_value, h2d, up_gbs = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step,
-                                         total, after_momentum)
+        e2e_value, h2d, up_gbs, e2e_wall = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)],
+                                                   step, total, after_momentum)
 
     if rank != 0:
         return
@@ -530,7 +539,12 @@ def run_ours(args):
                                                "overlap": "step n+1's gradient upload runs during step n "
                                                           "(two gradient buffers)",
                                                "upload_GBps_alone": up_gbs,
-                                               "upload_ms_alone": None if not up_gbs else h2d / up_gbs / 1e6},
+                                               "upload_ms_alone": None if not up_gbs else h2d / up_gbs / 1e6,
+                                               "steps": len(e2e_wall),
+                                               "step_ms": {"median": statistics.median(e2e_wall),
+                                                           "max": max(e2e_wall),
+                                                           "basis": "host wall time per step, up to its norm read; "
+                                                                    "the first includes the first upload"}},
         "gpu_launches": int(launches),
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -28,10 +28,20 @@ int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_
  * p x p iterations of matrices with p <= 192 in bf16 mode as one on-chip
  * chain launch (enable != 0, the default) or as one tensor-core launch per
  * product with every p x p result stored in the workspace (enable == 0).
- * Both round and mirror every p x p result the same way; tests compare them.
+ * Both round every p x p result to bf16 once; tests compare them.
  * Returns the previous setting.  Plans already created keep theirs.
  */
 int32_t gbo_testing_set_small_chain(int32_t enable);
+
+/*
+ * Whether Muon plans created from now on (any thread) run the Gram
+ * X_0 X_0^T of the chain's wide matrices with p <= 128 inside the chain
+ * launch, streaming X_0 through the matrix's shared memory (enable != 0, the
+ * default), or as a tensor-core launch of its own that stores A_0 and P_0
+ * for the chain to load (enable == 0).  Returns the previous setting.
+ * Plans already created keep theirs.
+ */
+int32_t gbo_testing_set_fused_gram(int32_t enable);
 
 #ifdef __cplusplus
 }

@@ -205,10 +205,13 @@ def test_flop_count_and_launches(L):
     assert info(L, plan).launches_per_step == 2 + 5 * 3
     L.gbo_muon_plan_destroy(plan)
     # a matrix of at most 192 rows takes the Gram route with the on-chip
-    # chain automatically, square or not: Gram (+ square of A_0), chain,
-    # product -- each a single-CTA and a CTA-pair launch (p = 64 and 150),
-    # the chain one launch per geometry
-    for abc, launches in (((1.5, -0.5, 0.0), 2 + 2 * 3), ((15 / 8, -5 / 4, 3 / 8), 2 + 2 * 4)):
+    # chain automatically, square or not.  p = 64: the chain from X_0 (its
+    # Gram and square on chip), then the product on single CTAs; p = 150:
+    # the Gram (and the square of A_0) on CTA pairs, the chain, the product.
+    # The chain from X_0 runs in the step of the other chain, so the products
+    # share a step.  Launches by step, cubic: {Gram}, {both chains}, {both
+    # products}; quintic: {Gram}, {square}, {both chains}, {both products}
+    for abc, launches in (((1.5, -0.5, 0.0), 2 + 1 + 2 + 2), ((15 / 8, -5 / 4, 3 / 8), 2 + 1 + 1 + 2 + 2)):
         rc, plan = create(L, [desc(0, 64, 64), desc(1, 150, 150)], abc=abc)
         i = info(L, plan)
         assert i.n_gram_route == 2 and i.launches_per_step == launches
@@ -217,27 +220,52 @@ def test_flop_count_and_launches(L):
 
 def test_small_chain_counts(L):
     """Gram-route matrices of at most 192 rows (bf16) run their p x p
-    iterations in one on-chip launch: the Gram, the chain, the product with
-    X_0.  For p <= 128 each op of the chain is one 128 x 128 tile (128 x 256
-    when T and Q are formed together) with K padded to 64; with the chain
-    switched off every p x p product is a tile-kernel launch of its own."""
+    iterations in one on-chip launch.  For a wide matrix of p <= 128 the
+    chain starts from X_0 (the Gram, and the square of A_0 when c != 0, on
+    chip: 128 x 128 tiles, K padded to 64), then the product with X_0: two
+    launches.  Otherwise the Gram is a tile-kernel launch of its own.  Each
+    op of the chain is one 128 x 128 tile (128 x 256 when T and Q are formed
+    together) with K padded to 64; with the chain switched off every p x p
+    product is a tile-kernel launch of its own."""
     d = lambda: [desc(0, 4 * 96, 1000, (4, 96, 1000))]  # four 96 x 1000 matrices: p = 96, q = 1000
     tile = 2 * 128 * 256            # one single-CTA tile of the tile kernel, per unit of K
     gram, prod, sym = tile * 1024, 4 * tile * 128, tile * 128
     op128, op256 = 2 * 128 * 128 * 128, 2 * 128 * 256 * 128
+    gram_chip = 2 * 128 * 128 * 1024  # the on-chip Gram: one 128 x 128 tile, K = 1000 padded to 1024
     # cubic, k = 5: T, A_1/P_1, then 3 x (T with Q, A/P), Q_5
     cubic_chain = 6 * op128 + 3 * op256
     # quintic, k = 5: T, A_1, square; 3 x (T with Q, A, square); Q_5 -- plus the square of A_0
     quintic_chain = 10 * op128 + 3 * op256
     rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM)
     i = info(L, plan)
-    assert i.n_gram_route == 4 and i.launches_per_step == 2 + 3
-    assert i.ns_flops_executed == 4 * (gram + cubic_chain + prod)
+    assert i.n_gram_route == 4 and i.launches_per_step == 2 + 2
+    assert i.ns_flops_executed == 4 * (gram_chip + cubic_chain + prod)
     L.gbo_muon_plan_destroy(plan)
     rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM, abc=(15 / 8, -5 / 4, 3 / 8))
     i = info(L, plan)
-    assert i.launches_per_step == 2 + 4
-    assert i.ns_flops_executed == 4 * (gram + sym + quintic_chain + prod)
+    assert i.launches_per_step == 2 + 2
+    assert i.ns_flops_executed == 4 * (gram_chip + op128 + quintic_chain + prod)
+    L.gbo_muon_plan_destroy(plan)
+    # with the Gram as a launch of its own (and the square of A_0 another)
+    prev = L.gbo_testing_set_fused_gram(0)
+    try:
+        rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM)
+        i = info(L, plan)
+        assert i.launches_per_step == 2 + 3 and i.ns_flops_executed == 4 * (gram + cubic_chain + prod)
+        L.gbo_muon_plan_destroy(plan)
+        rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM, abc=(15 / 8, -5 / 4, 3 / 8))
+        i = info(L, plan)
+        assert i.launches_per_step == 2 + 4 and i.ns_flops_executed == 4 * (gram + sym + quintic_chain + prod)
+        L.gbo_muon_plan_destroy(plan)
+    finally:
+        L.gbo_testing_set_fused_gram(prev)
+    # a matrix held tall (its stored rows > columns: X is q x p) too: its
+    # Gram X^T X reads X_0 in 64-row blocks; 200 x 96 stored, p = 96, q = 200
+    # (K padded to 256); the product runs on X held tall (q x p output)
+    rc, plan = create(L, [desc(0, 200, 96)], route=B.GBO_ROUTE_GRAM)
+    i = info(L, plan)
+    assert i.launches_per_step == 2 + 2
+    assert i.ns_flops_executed == 2 * 128 * 128 * 256 + cubic_chain + 2 * tile * 128  # 200 output rows: two tiles
     L.gbo_muon_plan_destroy(plan)
     # 128 < p <= 192: two 128-row halves with N = 192, T and Q as separate
     # products: T, A_1/P_1, 3 x (T, Q, A/P), Q_5; the Gram and the product

@@ -156,15 +156,17 @@ SMALL = [(4 * 96, 1000, (4, 96, 1000), None), (300, 100, None, None), (40, 300, 
     (CUBIC + QUINTIC + (2.0, -1.5, 0.5) + CUBIC + (1.2, -0.3, 0.1), 5),
 ])
 def test_small_chain_matches_launches(abc, ns_steps):
-    """Matrices of at most 128 rows on the Gram route: the on-chip chain
-    (one launch for all p x p products) against one launch per product, for
-    p = 20 .. 192 (one and two 128-row halves), wide and tall, c == 0 and
-    c != 0, k = 2 .. 16 (up to 45 chain ops a matrix, barrier phases over many
-    products).  The two
-    round every p x p result to bf16 once; the launches mirror symmetric
-    results from their upper triangle and the chain writes them whole, so
-    they agree to bf16 rounding (1e-2 relative per weight, ten times inside
-    the oracle tolerance) and both match the oracle."""
+    """Matrices of at most 192 rows on the Gram route, three ways: one
+    launch per p x p product; the on-chip chain (one launch for all p x p
+    products) after a Gram launch; and, for the wide matrices of at most 128
+    rows, the chain starting from X_0 (its Gram streamed through shared
+    memory in the same launch).  p = 20 .. 192 (one and two 128-row halves),
+    wide and tall, c == 0 and c != 0, k = 2 .. 16 (up to 32 ops a matrix,
+    barrier phases over many products and X_0 blocks).  All round every
+    p x p result to bf16 once; the launches mirror symmetric results from
+    their upper triangle and the chain writes them whole, so they agree to
+    bf16 rounding (1e-2 relative per weight, ten times inside the oracle
+    tolerance) and all match the oracle."""
     entries = random_entries(SMALL, seed=31, b_std=1e-3)
     kw = dict(lr=0.02, precision="bf16", abc=abc, ns_steps=ns_steps, route=B.GBO_ROUTE_GRAM)
     prev = B.gbo_testing_set_small_chain(False)
@@ -173,14 +175,26 @@ def test_small_chain_matches_launches(abc, ns_steps):
     finally:
         B.gbo_testing_set_small_chain(prev)
     B.gbo_testing_set_small_chain(True)
-    gpu, st1, plan1 = run_muon_gpu(entries, **kw)
-    B.gbo_testing_set_small_chain(prev)
-    assert st0 == 0 and st1 == 0
-    assert B.gbo_muon_plan_info(plan1)["launches_per_step"] < B.gbo_muon_plan_info(plan0)["launches_per_step"]
-    for a, b in zip(ref, gpu):
+    prev_fused = B.gbo_testing_set_fused_gram(False)
+    try:
+        sep, st1, plan1 = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_fused_gram(prev_fused)
+    B.gbo_testing_set_fused_gram(True)
+    try:
+        gpu, st2, plan2 = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_small_chain(prev)
+        B.gbo_testing_set_fused_gram(prev_fused)
+    assert st0 == 0 and st1 == 0 and st2 == 0
+    n0, n1, n2 = (B.gbo_muon_plan_info(q)["launches_per_step"] for q in (plan0, plan1, plan2))
+    assert n2 <= n1 < n0
+    for a, b, c in zip(ref, sep, gpu):
         assert rel_fro(f64(b["U"]), f64(a["U"])) <= 1e-2
+        assert rel_fro(f64(c["U"]), f64(a["U"])) <= 1e-2
     ora = run_muon_oracle(entries, lr=0.02, abc=abc, ns_steps=ns_steps)
     check_muon(entries, ref, ora, lr=0.02, precision="bf16")
+    check_muon(entries, sep, ora, lr=0.02, precision="bf16")
     check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
 
 
