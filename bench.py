@@ -43,6 +43,9 @@ def parse():
                     help="Newton-Schulz operands: bf16 (the benchmark) or the fp32 mode (three TF32 products)")
     ap.add_argument("--overlap", action="store_true",
                     help="run clip + AdamW on a side stream that starts after the momentum phase")
+    ap.add_argument("--separate-gram", action="store_true",
+                    help="A/B: run the Gram of the on-chip chain's matrices (p <= 128) as a tile-kernel "
+                         "launch of its own instead of inside the chain launch (workload 4)")
     ap.add_argument("--workload", type=int, default=WORKLOAD,
                     help="synthetic set: 3 = the 1.23B OMN-shaped set (the benchmark); 2 = one "
                          "d=2048 layer, 4 = many small MLA/KDA matrices, 5 = 7B NorMuon (profiling)")
@@ -328,6 +331,9 @@ def run_ours(args):
     from adamw_optimizer_step_gb300 import workloads as wk
 
     gbo.lib()
+    if args.separate_gram:
+        from adamw_optimizer_step_gb300 import _binding
+        _binding.gbo_testing_set_fused_gram(False)
     wl = wk.workload(args.workload)
     if args.layers:
         wl = wk.first_layers(wl, args.layers)
@@ -514,6 +520,7 @@ def run_ours(args):
                    "ns_precision": ("fp32 operands as three TF32 products, fp32 accumulate" if f32
                                     else "bf16 operands, fp32 accumulate"),
                    "parallelism": "replicas" if world > 1 else "single",
+                   "chain_gram": "separate launch" if args.separate_gram else "on chip (p <= 128)",
                    "device": torch.cuda.get_device_name(),
                    "seed": "one seeded draw per tensor and role (workloads.seed: workload, tensor index, role)",
                    "l2": "working set ~20 GB per GPU, far above the 129 MB L2: no flush needed"},
