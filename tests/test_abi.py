@@ -218,6 +218,27 @@ def test_flop_count_and_launches(L):
         L.gbo_muon_plan_destroy(plan)
 
 
+# eleven shape classes of at most 128 rows, wide and tall, with K ragged
+CHAIN_CLASSES = [(8, 200, None), (200, 8, None), (24, 72, None), (130, 60, None), (64, 64, None),
+                 (100, 1000, None), (1000, 100, None), (127, 129, None), (129, 127, None),
+                 (2 * 40, 520, (2, 40, 520)), (3 * 16, 48, (3, 16, 48))]
+
+
+def test_chain_gram_launch_groups(L):
+    """Eleven Gram-route classes of at most 128 rows: the chain with its
+    Gram on chip takes eight classes to a launch, so two chain launches and
+    two product launches follow momentum and the pre-normalisation, for
+    the cubic and for c != 0 (whose square of A_0 also runs on chip)."""
+    ds = [desc(i, r, c, v) for i, (r, c, v) in enumerate(CHAIN_CLASSES)]
+    for abc in ((1.5, -0.5, 0.0), (15 / 8, -5 / 4, 3 / 8)):
+        rc, plan = create(L, ds, route=B.GBO_ROUTE_GRAM, abc=abc)
+        assert rc == 0, L.gbo_last_error()
+        i = info(L, plan)
+        assert i.n_shape_classes == 11 and i.n_gram_route == 9 + 2 + 3
+        assert i.launches_per_step == 2 + 2 + 2
+        L.gbo_muon_plan_destroy(plan)
+
+
 def test_small_chain_counts(L):
     """Gram-route matrices of at most 192 rows (bf16) run their p x p
     iterations in one on-chip launch.  For a wide matrix of p <= 128 the

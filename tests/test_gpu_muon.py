@@ -198,6 +198,36 @@ def test_small_chain_matches_launches(abc, ns_steps):
     check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
 
 
+# eleven shape classes of at most 128 rows (p = 8 .. 127), wide and tall,
+# with K ragged (q = 48 .. 1000): two launches of the chain with its Gram on
+# chip, eight classes to a launch
+CHAIN_CLASSES = [(8, 200, None, None), (200, 8, None, None), (24, 72, None, None), (130, 60, None, None),
+                 (64, 64, None, None), (100, 1000, None, None), (1000, 100, None, None),
+                 (127, 129, None, None), (129, 127, None, None), (2 * 40, 520, (2, 40, 520), None),
+                 (3 * 16, 48, (3, 16, 48), None)]
+
+
+@pytest.mark.parametrize("abc", [CUBIC, QUINTIC])
+def test_chain_gram_launch_groups(abc):
+    """The chain with its Gram on chip over two launches (classes 1-8 and
+    9-11) against the same chain after a Gram launch of its own (agreement
+    to bf16 rounding) and against the oracle."""
+    entries = random_entries(CHAIN_CLASSES, seed=37, b_std=1e-3)
+    kw = dict(lr=0.02, precision="bf16", abc=abc, ns_steps=5, route=B.GBO_ROUTE_GRAM)
+    prev = B.gbo_testing_set_fused_gram(False)
+    try:
+        sep, st1, plan1 = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_fused_gram(prev)
+    gpu, st2, plan2 = run_muon_gpu(entries, **kw)
+    assert st1 == 0 and st2 == 0
+    assert B.gbo_muon_plan_info(plan2)["launches_per_step"] == 2 + 2 + 2
+    for a, b in zip(sep, gpu):
+        assert rel_fro(f64(b["U"]), f64(a["U"])) <= 1e-2
+    ora = run_muon_oracle(entries, lr=0.02, abc=abc, ns_steps=5)
+    check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
+
+
 @pytest.mark.parametrize("ns_steps", [3, 5])
 def test_normuon_gram_route(ns_steps):
     """NorMuon rows read the last iterate from the buffer each route leaves
