@@ -64,32 +64,37 @@ struct Mode {
   static constexpr int kSub = kPair ? 2 : 1;  // BK-wide K blocks per stage
   static constexpr int kSubBytes = A_BYTES + (kPair ? B_HALF : 2 * B_HALF);
   static constexpr int kStageBytes = kSub * kSubBytes;
-  static constexpr int kStages = kPair ? 3 : 4;
+  // pairs: 3 x 64 KB; single CTAs: 3 x 48 KB, leaving room for deeper
+  // weight loads in the epilogue staging
+  static constexpr int kStages = 3;
   static constexpr int kRows = kPair ? 2 : 1;  // 128-row tiles per work item
+  static constexpr int kRingBytes = kStages * kStageBytes;
 };
-constexpr int kRingBytes = 6 * (A_BYTES + B_HALF);
-static_assert(Mode<true>::kStages * Mode<true>::kStageBytes == kRingBytes, "ring size");
-static_assert(Mode<false>::kStages * Mode<false>::kStageBytes == kRingBytes, "ring size");
 // Epilogue warps.  Pair mode: one per TMEM lane quarter, each over the
 // tile's 256 columns, with two store slots (kSlotBytes each, tc_common.cuh)
-// or four weight buffers.  Single mode: two per lane quarter, each over 128
-// of the columns, with one slot or two weight buffers: its HBM-bound last
-// products on small matrices are limited by the epilogue warps' latency, and
-// two warps per scheduler hide more of it.  Both stage 32 KB in all.
+// or four weight buffers (8 KB a warp, 32 KB in all).  Single mode: two per
+// lane quarter, each over 128 of the columns, with two slots or four weight
+// buffers (8 KB a warp, 64 KB in all): its HBM-bound last products on small
+// matrices are limited by latency, and two warps per scheduler, each with
+// three weight blocks in flight, hide more of it.
 template <bool kPair>
 struct Epi {
   static constexpr int kWarps = kPair ? 4 : 8;
   static constexpr int kSplit = kWarps / 4;           // warps per lane quarter
   static constexpr int kSpan = BN / kSplit;           // columns a warp covers
   static constexpr int kThreads = 64 + 32 * kWarps;
-  static constexpr int kWarpStage = 8 * 1024 / kSplit;
+  static constexpr int kWarpStage = 8 * 1024;
   static constexpr int kSlots = kWarpStage / kSlotBytes;
   static constexpr int kWBufs = kWarpStage / kWBufBytes;
+  static constexpr int kStagingBytes = kWarps * kWarpStage;
+  static_assert((kWBufs & (kWBufs - 1)) == 0, "weight buffers are indexed modulo a power of two");
 };
-constexpr int kStageBytes = 32 * 1024;
-static_assert(Epi<true>::kWarps * Epi<true>::kWarpStage == kStageBytes, "staging size");
-static_assert(Epi<false>::kWarps * Epi<false>::kWarpStage == kStageBytes, "staging size");
-constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + kStageBytes + 512 /*barriers*/;
+// ring, then staging, then barriers; one size for both modes (the larger)
+template <bool kPair>
+__host__ __device__ constexpr int smem_used() { return Mode<kPair>::kRingBytes + Epi<kPair>::kStagingBytes; }
+constexpr int kSmemBytes =
+    1024 /*align*/ + (smem_used<true>() > smem_used<false>() ? smem_used<true>() : smem_used<false>()) +
+    512 /*barriers*/;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
 // each K-major or MN-major, N = 256, M = 128 (one CTA) or 256 (pair).
@@ -293,13 +298,13 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   constexpr int kRows = Mode<kPair>::kRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes + kStageBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + smem_used<kPair>());
   // bars: full[STAGES], empty[STAGES], accf[2], acce[2], drain, (TMEM
   // address, abort flag), then the weight-load barriers of the epilogue warps
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
   uint64_t *wbars = bars + 2 * STAGES + 6;
-  uint8_t *stage_base = smem + kRingBytes;  // epilogue staging, 1024-byte aligned
+  uint8_t *stage_base = smem + Mode<kPair>::kRingBytes;  // epilogue staging, 1024-byte aligned
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
