@@ -92,9 +92,13 @@ struct Geo {
   // X_0 held tall)
   static constexpr uint32_t IdescK = Idesc & ~(1u << 16);
   static constexpr uint32_t IdescMN = Idesc | (1u << 15);
+  // N = 256 (kH = 1): T and Q_{j+1} in one product, B = [A | Q], the two
+  // matrices side by side in shared memory
+  static constexpr uint32_t IdescN2 = (Idesc & ~(0x3Fu << 17)) | ((uint32_t)(2 * R >> 3) << 17);
 };
 static_assert(Geo<1>::Smem <= 232448 && Geo<2>::Smem <= 232448, "shared memory per CTA");
 static_assert(kRing * kRingBytes <= Geo<1>::SlotSize, "the X_0 ring lies within one slot");
+static_assert(Geo<1>::Mat == 2 * Geo<1>::Blk, "kH = 1: Q's two 64-column blocks follow A's, one N = 256 operand");
 static_assert((kNBars + 1 + kNClocks) * 8 <= 512, "barriers, TMEM address, abort flag and idle clocks");
 
 // Products of slot matrices (L R: L read K-major, R MN-major) and
@@ -153,7 +157,8 @@ __device__ __forceinline__ void chain_mma(uint32_t d_tmem, uint64_t adesc, uint6
 }
 
 // Row half h of D = L R over kit 64-wide K blocks, in 16-wide K steps; L and
-// R are slot matrices at shared-memory addresses l and r.  L is K-major: its
+// R are slot matrices at shared-memory addresses l and r (with the N = 256
+// descriptor, R and the matrix after it).  L is K-major: its
 // rows 128 h .. start 16 KB into each block, a K step of 16 is 32 bytes
 // along its rows, a K block the next 64-column block.  R is MN-major: its
 // rows are K, a K step is two 8-row groups (2048 bytes), a K block 64 rows
@@ -162,13 +167,14 @@ __device__ __forceinline__ void chain_mma(uint32_t d_tmem, uint64_t adesc, uint6
 // buffer after it (A after P, Q after A): they feed only accumulator rows
 // that are never written back.
 template <int kH>
-__device__ __forceinline__ void chain_product(uint32_t d_tmem, uint32_t l, uint32_t r, int kit, int h) {
+__device__ __forceinline__ void chain_product(uint32_t d_tmem, uint32_t l, uint32_t r, int kit, int h,
+                                              uint32_t idesc = Geo<kH>::Idesc) {
   const uint64_t ld = smem_desc(l + (uint32_t)h * 16384u, 16, 1024), rd = smem_desc(r, Geo<kH>::Blk, 1024);
   for (int kb = 0; kb < kit; ++kb)
 #pragma unroll
     for (int k = 0; k < CK / 16; ++k)
       chain_mma<kH>(d_tmem, ld + ((uint32_t)(kb * Geo<kH>::Blk + k * 32) >> 4),
-                    rd + ((uint32_t)(kb * 8192 + k * 2048) >> 4), (kb | k) != 0);
+                    rd + ((uint32_t)(kb * 8192 + k * 2048) >> 4), (kb | k) != 0, idesc);
 }
 
 // Byte offset of 16-byte chunk q (columns 8q .. 8q + 7) of row r of a slot
@@ -531,10 +537,8 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
               if (mma == kMmaPA) chain_product<kH>(d, mP, mA, kit, h);
               else if (mma == kMmaAA) chain_product<kH>(d, mA, mA, kit, h);
               else if (mma == kMmaPQ) chain_product<kH>(d, mP, mQ, kit, h);
-              else {  // kMmaPAQ
-                chain_product<kH>(d, mP, mA, kit, h);
-                chain_product<kH>(d + 128, mP, mQ, kit, h);
-              }
+              else  // kMmaPAQ (kH = 1): acc0 = P A, acc1 = P Q from one N = 256 product over [A | Q]
+                chain_product<kH>(d, mP, mA, kit, h, G::IdescN2);
             }
           }
           issued = moved = true;
