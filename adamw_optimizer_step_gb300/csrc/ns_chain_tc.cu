@@ -41,9 +41,12 @@
 // Persistent CTA (320 threads, one per SM):
 //   warp 0      TMA loads (one lane): A_0, P_0 (into P and Q) of the next
 //               matrix of each slot, or its X_0 blocks (kFuse)
-//   warp 1      TMEM owner and MMA issuer (one lane), alternating slots
+//   warp 1      TMEM owner and MMA issuer (one lane): alternating slots, or
+//               (kFuse) slot 0 only
 //   warps 2..9  epilogue, two per TMEM lane quarter, each taking half of
 //               the column blocks of the quarter's rows
+//   warp 10     (kFuse) MMA issuer of slot 1, so that neither slot's chain
+//               ops queue behind the other slot's bursts of Gram MMAs
 // Every wait is bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT,
 // lets its own copies and MMAs land (bounded), frees TMEM and returns.
 #include <cuda.h>
@@ -70,8 +73,14 @@ constexpr int kMaxOps = 4 * GBO_MAX_NS_STEPS + 1;
 constexpr int kCTmemCols = 512;
 constexpr int kRing = 6;                 // X_0 blocks in flight per slot (kFuse)
 constexpr int kRingBytes = 128 * CK * 2; // one 128-row, 64-column bf16 block of X_0
-constexpr int kNBars = 11 + 4 * kRing;   // loaded, mmad, epid, qdone, freed (2 each), drain, full/empty rings
-constexpr int kNClocks = 10;             // idle-stretch starts: one per warp
+constexpr int kNBars = 12 + 4 * kRing;   // loaded, mmad, epid, qdone, freed (2 each), drain, full/empty rings, drain2
+constexpr int kNClocks = 11;             // idle-stretch starts: one per warp
+// kFuse: a second MMA issuer warp (slot 1) after the epilogue warps; with
+// 11 warps a scheduler still holds at most three, so the register budget
+// per thread is that of 10
+constexpr int kIssuer2 = kCThreads / 32;
+template <bool kFuse>
+constexpr int chain_threads() { return kCThreads + (kFuse ? 32 : 0); }
 
 // Shared-memory geometry of one slot matrix (K-major rows of 128 bytes in
 // 64-column blocks, 128-byte swizzle, as TMA writes it).
@@ -303,24 +312,25 @@ __device__ __forceinline__ void chain_epilogue(const ChainOp &o, uint32_t acc_ro
           if (o.epi == kEpiAP) put_full<kH>(mA, i, col0, p, v);
           put_full<kH>(mP, i, col0, p, w);
           break;
-        case kEpiGram: {  // A first, then P and Q from a second read of the accumulator
-          if constexpr (!kFuse) break;
+        case kEpiGram:  // A first, then P and Q from a second read of the accumulator
+          if constexpr (kFuse) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] *= s2;
-          put_full<kH>(mA, i, col0, p, v);
-          tmem_ld32(acc0 + col0, v);
-          const float bs2 = o.b * s2;
+            for (int k = 0; k < 32; ++k) v[k] *= s2;
+            put_full<kH>(mA, i, col0, p, v);
+            tmem_ld32(acc0 + col0, v);
+            const float bs2 = o.b * s2;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = bs2 * v[k] + (i == col0 + k ? o.a : 0.f);
-          put_full<kH>(mP, i, col0, p, v);
-          put_full<kH>(mQ, i, col0, p, v);
+            for (int k = 0; k < 32; ++k) v[k] = bs2 * v[k] + (i == col0 + k ? o.a : 0.f);
+            put_full<kH>(mP, i, col0, p, v);
+            put_full<kH>(mQ, i, col0, p, v);
+          }
           break;
-        }
         case kEpiGramA:
-          if constexpr (!kFuse) break;
+          if constexpr (kFuse) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] *= s2;
-          put_full<kH>(mA, i, col0, p, v);
+            for (int k = 0; k < 32; ++k) v[k] *= s2;
+            put_full<kH>(mA, i, col0, p, v);
+          }
           break;
         default: {  // kEpiSq, kEpiSqQ
           float am[32];
@@ -361,7 +371,7 @@ struct IdleClock {
 };
 
 template <int kH, bool kFuse>
-__global__ void __launch_bounds__(kCThreads, 1)
+__global__ void __launch_bounds__(chain_threads<kFuse>(), 1)
 ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ PhaseArgs A) {
   using G = Geo<kH>;
   static_assert(!kFuse || kH == 1, "the Gram runs on chip for p <= 128 only");
@@ -370,14 +380,15 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * G::SlotSize);
   // bars: loaded[2], mmad[2], epid[2], qdone[2], freed[2], drain, full[2][kRing],
-  // empty[2][kRing], then the TMEM address and the abort flag, then one
-  // idle clock per warp
+  // empty[2][kRing], drain2, then the TMEM address and the abort flag, then
+  // one idle clock per warp
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNBars);
   uint64_t *clocks = bars + kNBars + 1;
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
   const uint32_t loaded0 = smem_u32(bars), mmad0 = smem_u32(bars + 2), epid0 = smem_u32(bars + 4);
   const uint32_t qdone0 = smem_u32(bars + 6), freed0 = smem_u32(bars + 8), drain = smem_u32(bars + 10);
   const uint32_t full0 = smem_u32(bars + 11), empty0 = smem_u32(bars + 11 + 2 * kRing);
+  const uint32_t drain2 = smem_u32(bars + 11 + 4 * kRing);
   auto full_bar = [&](int s, int st) { return full0 + (uint32_t)(8 * (s * kRing + st)); };
   auto empty_bar = [&](int s, int st) { return empty0 + (uint32_t)(8 * (s * kRing + st)); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -395,6 +406,7 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
         }
     }
     mbar_init(drain, 1);
+    mbar_init(drain2, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -475,62 +487,93 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
             (void)mbar_wait(full_bar(s, (int)(n % kRing)), (uint32_t)((n / kRing) & 1));
         }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (kFuse && warp == kIssuer2)) {
     if (lane == 0) {
-      int64_t g[S], ring_c[S];
-      int op[S], kb[S];
-      uint32_t u[S];
-      for (int s = 0; s < S; ++s) g[s] = s, ring_c[s] = 0, op[s] = 0, kb[s] = 0, u[s] = 0;
-      bool issued = false;
-      IdleClock idle(clocks + warp);
-      for (bool any = true; any && !*abort_flag;) {
-        any = false;
-        bool moved = false;
-        for (int s = 0; s < S && !*abort_flag; ++s) {
-          const int64_t t = mat_of(g[s]);
-          if (t >= total) continue;
-          any = true;
-          const uint32_t base = slots + s * G::SlotSize;
-          const uint32_t acc = tmem_base + (uint32_t)(s * 256);
-          if (kFuse && op[s] == 0) {
-            // the Gram, block by block as X_0 lands, once the slot's
-            // previous matrix's last epilogue has read the accumulator
-            if (kb[s] == 0 && u[s] > 0 && !mbar_try(epid0 + 8 * s, (u[s] - 1) & 1)) continue;
-            const int c = chain_class(P, t);
-            const int nk = (P.q[c] + CK - 1) / CK;
-            // wide: K-major rows, a K step 32 bytes along them; tall: K is
-            // the stage's rows (16 rows = 2048 bytes a step), its two 64-column
-            // halves 8 KB apart
-            const bool tall = P.tall[c] != 0;
-            const uint32_t lbo = tall ? kRingBytes / 2 : 16, kstep = tall ? 2048 >> 4 : 32 >> 4;
-            const uint32_t idesc = tall ? G::IdescMN : G::IdescK;
-            while (kb[s] < nk) {
-              const int st = (int)(ring_c[s] % kRing);
-              if (!mbar_try(full_bar(s, st), (uint32_t)((ring_c[s] / kRing) & 1))) break;
-              tc_fence_after();
-              const uint64_t d = smem_desc(base + (uint32_t)(st * kRingBytes), lbo, 1024);
-#pragma unroll
-              for (int k = 0; k < CK / 16; ++k)
-                chain_mma<kH>(acc, d + k * kstep, d + k * kstep, (kb[s] | k) != 0, idesc);
-              mma_commit_one(empty_bar(s, st));
-              ++kb[s];
-              ++ring_c[s];
-              moved = issued = true;
-            }
-            if (kb[s] < nk) continue;
-            kb[s] = 0;
-          } else {
-            // the slot's previous epilogue has read its accumulators and
-            // written the operands; a new matrix's loads have landed
-            if (kFuse) {
-              if (!mbar_try(epid0 + 8 * s, (u[s] - 1) & 1)) continue;
-            } else {
-              if (u[s] > 0 && !mbar_wait(epid0 + 8 * s, (u[s] - 1) & 1)) { give_up(); break; }
-              if (op[s] == 0 && !mbar_wait(loaded0 + 8 * s, (uint32_t)((g[s] / S) & 1))) { give_up(); break; }
+      if constexpr (kFuse) {
+        // one MMA issuer per slot: warp 1 takes slot 0, warp kIssuer2 slot 1
+        const int s = warp == 1 ? 0 : 1;
+        const uint32_t base = slots + s * G::SlotSize;
+        const uint32_t acc = tmem_base + (uint32_t)(s * 256);
+        const uint32_t mP = base, mA = base + G::Mat, mQ = base + 2 * G::Mat;
+        int64_t ring_c = 0;  // X_0 blocks consumed in this slot
+        uint32_t u = 0;      // ops issued in this slot (barrier phases)
+        bool issued = false, ok = true;
+        for (int64_t g = s; ok && mat_of(g) < total && !*abort_flag; g += S) {
+          const int c = chain_class(P, mat_of(g));
+          const int kit = (P.p[c] + CK - 1) / CK;
+          for (int op = 0; op < P.n_ops && !*abort_flag; ++op) {
+            // the slot's previous epilogue has read the accumulators and
+            // written the operands
+            if (u > 0 && !mbar_wait(epid0 + 8 * s, (u - 1) & 1)) {
+              give_up();
+              ok = false;
+              break;
             }
             tc_fence_after();
+            if (op == 0) {
+              // the Gram, block by block as X_0 lands.  Wide: K-major rows,
+              // a K step 32 bytes along them; tall: K is the stage's rows
+              // (16 rows = 2048 bytes a step), its two 64-column halves 8 KB
+              // apart
+              const int nk = (P.q[c] + CK - 1) / CK;
+              const bool tall = P.tall[c] != 0;
+              const uint32_t lbo = tall ? kRingBytes / 2 : 16, kstep = tall ? 2048 >> 4 : 32 >> 4;
+              const uint32_t idesc = tall ? G::IdescMN : G::IdescK;
+              for (int kb = 0; kb < nk; ++kb, ++ring_c) {
+                const int st = (int)(ring_c % kRing);
+                if (!mbar_wait(full_bar(s, st), (uint32_t)((ring_c / kRing) & 1))) {
+                  give_up();
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t d = smem_desc(base + (uint32_t)(st * kRingBytes), lbo, 1024);
+#pragma unroll
+                for (int k = 0; k < CK / 16; ++k)
+                  chain_mma<kH>(acc, d + k * kstep, d + k * kstep, (kb | k) != 0, idesc);
+                mma_commit_one(empty_bar(s, st));
+                issued = true;
+              }
+              if (!ok) break;
+            } else {
+              const int mma = P.ops[op].mma;
+              if (mma == kMmaPA) chain_product<kH>(acc, mP, mA, kit, 0);
+              else if (mma == kMmaAA) chain_product<kH>(acc, mA, mA, kit, 0);
+              else if (mma == kMmaPQ) chain_product<kH>(acc, mP, mQ, kit, 0);
+              else  // kMmaPAQ: acc0 = P A, acc1 = P Q from one N = 256 product over [A | Q]
+                chain_product<kH>(acc, mP, mA, kit, 0, G::IdescN2);
+            }
+            issued = true;
+            mma_commit_one(mmad0 + 8 * s);
+            ++u;
+          }
+        }
+        if (*abort_flag && issued) {  // the outstanding MMAs complete before TMEM is released
+          const uint32_t dr = s == 0 ? drain : drain2;
+          mma_commit_one(dr);
+          (void)mbar_wait(dr, 0);
+        }
+      } else {
+        int64_t g[S];
+        int op[S];
+        uint32_t u[S];
+        for (int s = 0; s < S; ++s) g[s] = s, op[s] = 0, u[s] = 0;
+        bool issued = false;
+        for (bool any = true; any && !*abort_flag;) {
+          any = false;
+          for (int s = 0; s < S && !*abort_flag; ++s) {
+            const int64_t t = mat_of(g[s]);
+            if (t >= total) continue;
+            any = true;
+            // the slot's previous epilogue has read its accumulators and
+            // written the operands; a new matrix's loads have landed
+            if (u[s] > 0 && !mbar_wait(epid0 + 8 * s, (u[s] - 1) & 1)) { give_up(); break; }
+            if (op[s] == 0 && !mbar_wait(loaded0 + 8 * s, (uint32_t)((g[s] / S) & 1))) { give_up(); break; }
+            tc_fence_after();
             const int kit = (P.p[chain_class(P, t)] + CK - 1) / CK;
+            const uint32_t base = slots + s * G::SlotSize;
             const uint32_t mP = base, mA = base + G::Mat, mQ = base + 2 * G::Mat;
+            const uint32_t acc = tmem_base + (uint32_t)(s * 256);
             const int mma = P.ops[op[s]].mma;
             for (int h = 0; h < kH; ++h) {
               const uint32_t d = acc + (uint32_t)(h * 256);
@@ -540,20 +583,19 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
               else  // kMmaPAQ (kH = 1): acc0 = P A, acc1 = P Q from one N = 256 product over [A | Q]
                 chain_product<kH>(d, mP, mA, kit, h, G::IdescN2);
             }
+            issued = true;
+            mma_commit_one(mmad0 + 8 * s);
+            ++u[s];
+            if (++op[s] == P.n_ops) op[s] = 0, g[s] += S;
           }
-          issued = moved = true;
-          mma_commit_one(mmad0 + 8 * s);
-          ++u[s];
-          if (++op[s] == P.n_ops) op[s] = 0, g[s] += S;
         }
-        if (kFuse && any && idle.expired(moved)) give_up();
-      }
-      if (*abort_flag && issued) {  // the outstanding MMAs complete before TMEM is released
-        mma_commit_one(drain);
-        (void)mbar_wait(drain, 0);
+        if (*abort_flag && issued) {  // the outstanding MMAs complete before TMEM is released
+          mma_commit_one(drain);
+          (void)mbar_wait(drain, 0);
+        }
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + kCEpiWarps) {
     const int quarter = warp & 3;      // TMEM lane quarter of this warp
     const int wh = (warp - 2) >> 2;    // its column blocks: wh * WarpBlocks ..
     const int cb0 = wh * G::WarpBlocks, cb1 = cb0 + G::WarpBlocks;
@@ -732,7 +774,8 @@ int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
     const int64_t total = T.mat_start[T.n];
     if (total == 0) continue;
     const unsigned grid = (unsigned)std::min<int64_t>(total, sm_count);  // one CTA per SM
-    ns_chain_kernel<kH, kFuse><<<grid, kCThreads, G::Smem, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
+    ns_chain_kernel<kH, kFuse><<<grid, chain_threads<kFuse>(), G::Smem, reinterpret_cast<cudaStream_t>(stream)>>>(T,
+                                                                                                        args);
     count_launches(1);
     if (n_launch) ++*n_launch;
     const cudaError_t err = cudaGetLastError();
