@@ -25,9 +25,10 @@
 // Gram's epilogue writes them), the MMAs accumulate the Gram in the slot's
 // TMEM columns, and the epilogue folds in the pre-normalisation factor and
 // writes A_0, P_0 and Q_1 = P_0 (with c != 0, A_0 and then P_0 from an
-// on-chip square).  The MMA issuer and the epilogue warps then poll both
-// slots instead of taking them in turn, so one slot's X_0 stream (bound by
-// HBM) runs under the other slot's chain (bound by latency).
+// on-chip square).  Each slot then has an MMA issuer of its own, and the
+// epilogue warps poll both slots instead of taking them in turn, so one
+// slot's X_0 stream (bound by HBM) runs under the other slot's chain (bound
+// by latency) and neither slot's ops queue behind the other's issue.
 //
 // Two geometries (template parameter kH, 128-row halves of a matrix):
 //   kH = 1  p <= 128: 128 x 128 matrices (32 KB each), two matrices in
