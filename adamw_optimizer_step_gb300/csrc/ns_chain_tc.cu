@@ -33,13 +33,13 @@
 // Two geometries (template parameter kH, 128-row halves of a matrix):
 //   kH = 1  p <= 128: 128 x 128 matrices (32 KB each), two matrices in
 //           flight per CTA so the epilogue of one slot's product overlaps
-//           the other slot's MMAs; T and Q_{j+1} are one op (two N = 128
-//           accumulators side by side)
+//           the other slot's MMAs; T and Q_{j+1} are one N = 256 product
+//           over [A | Q] (two 128-column accumulators side by side)
 //   kH = 2  128 < p <= 192: 192 x 192 matrices (72 KB each), one matrix per
 //           CTA; each product is two M = 128 row halves with N = 192, and
 //           T and Q_{j+1} are separate products (their accumulators would
 //           not fit TMEM together)
-// Persistent CTA (320 threads, one per SM):
+// Persistent CTA (320 threads, 352 with kFuse; one per SM):
 //   warp 0      TMA loads (one lane): A_0, P_0 (into P and Q) of the next
 //               matrix of each slot, or its X_0 blocks (kFuse)
 //   warp 1      TMEM owner and MMA issuer (one lane): alternating slots, or
