@@ -15,8 +15,10 @@
 // race on it; calls in one stream are ordered and safe.  The array keeps
 // the last call's partial sums; nothing needs clearing, because every slot
 // a call reads is written earlier in that same call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 
@@ -32,14 +34,57 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-float *g_scratch_addr[kMaxDevices] = {};
+// Per device: the CUDA context the address was looked up in (its
+// process-unique ID, never reused) and the address.  A device reset, or
+// anything else that replaces the context, makes the next call look the
+// address up again instead of using one from a context that is gone.
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;
+  bool known = false;
+  float *addr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of g_clip_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_fn(const char *name) {
+  void *p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+// ID of the context current on this thread (the runtime has made the
+// device's primary context current by the time this runs).
+int current_context_id(unsigned long long *id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, id) != CUDA_SUCCESS)
+    return report_error(GBO_ERR_CUDA, "cannot identify the current CUDA context");
+  return GBO_OK;
+}
+
+// Device address of g_clip_scratch on the current device.  The set-up --
+// cudaGetSymbolAddress with that device current -- runs on the first call
+// in each context of a device and is cached for the later ones.
 int scratch_on_device(int dev, float **out) {
   if (dev < 0 || dev >= kMaxDevices) return report_error(GBO_ERR_UNSUPPORTED, "device index above 63");
+  unsigned long long ctx_id = 0;
+  int rc = current_context_id(&ctx_id);
+  if (rc != GBO_OK) return rc;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr &c = g_scratch[dev];
+  if (!c.known || c.ctx_id != ctx_id) {
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_clip_scratch);
     if (e != cudaSuccess) {
@@ -47,9 +92,11 @@ int scratch_on_device(int dev, float **out) {
       snprintf(msg, sizeof msg, "cudaGetSymbolAddress(clip scratch): %s", cudaGetErrorString(e));
       return report_error(GBO_ERR_CUDA, msg);
     }
-    g_scratch_addr[dev] = static_cast<float *>(p);
+    c.addr = static_cast<float *>(p);
+    c.ctx_id = ctx_id;
+    c.known = true;
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return GBO_OK;
 }
 
@@ -70,7 +117,8 @@ extern "C" int gbo_clip_norm_noalloc(const gbo_tensor *grads, int32_t n, float m
              kClipBlocks, GBO_CLIP_NOALLOC_MAX_TENSORS);
     return report_error(GBO_ERR_INVALID_ARG, msg);
   }
-  if (!(max_norm > 0.f) || !(max_norm < 3.4e38f)) return report_error(GBO_ERR_INVALID_ARG, "max_norm must be > 0");
+  // the same rule as gbo_clip_norm: any finite positive max_norm
+  if (!(max_norm > 0.f) || !std::isfinite(max_norm)) return report_error(GBO_ERR_INVALID_ARG, "max_norm must be > 0");
   for (int32_t i = 0; i < n; ++i) {
     const gbo_tensor &t = grads[i];
     if (t.dtype != GBO_F32 && t.dtype != GBO_BF16) return report_error(GBO_ERR_DTYPE, "bad gradient dtype");

@@ -263,7 +263,9 @@ int gbo_clip_norm(const gbo_tensor *grads, int32_t n, float max_norm, float *dev
  *   n           at most GBO_CLIP_NOALLOC_MAX_TENSORS tensors (any sizes);
  *               more is refused with GBO_ERR_INVALID_ARG
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
+ * device current) and caches it for the device's current CUDA context; the
+ * first call in a new context (after a device reset, for instance) looks it
+ * up again.  Make the first call before any stream capture.  Every
  * call shares the one array, so calls whose work overlaps on the GPU race
  * (use one stream, or order them); it keeps the last call's contents, and no
  * slot needs clearing because each call writes every slot it reads.

@@ -10,6 +10,7 @@ failure has run every other test before it."""
 import pytest
 import torch
 
+import oracle
 from adamw_optimizer_step_gb300 import _binding as B
 
 pytestmark = pytest.mark.gpu
@@ -61,6 +62,13 @@ def test_noalloc_matches_workspace_version_on_consecutive_calls():
         ref_total, ref_coef = with_workspace(grads, 1.0)
         assert abs(total - ref_total) <= 1e-6 * ref_total
         assert abs(coef - ref_coef) <= 1e-6 * ref_coef
+        # and the fp64 oracle's global norm and clip coefficient, on the same
+        # values (bf16 gradients widened exactly)
+        host = [g.double().cpu().numpy() for g in grads]
+        o_total = oracle.global_grad_norm(host)
+        o_coef = oracle.clip_coefficient(o_total, 1.0)
+        assert abs(total - o_total) <= 1e-6 * o_total
+        assert abs(coef - o_coef) <= 1e-6 * o_coef
     # the second set is large: clipping is active; the first is not
     assert results[0][1] == 1.0 and results[1][1] < 1.0
 
