@@ -10,7 +10,7 @@ import torch
 import oracle
 from oracle.views import sub_matrices
 from tests.parity import TOL, f64, ulp
-from tests.test_routing import Toy
+from tests.test_routing import LAYOUTS, Toy, ToyFused
 
 pytestmark = pytest.mark.gpu
 
@@ -22,30 +22,32 @@ def built():
     B.lib()
 
 
-def make_model(seed):
+def make_model(seed, cls=Toy):
     torch.manual_seed(seed)
-    m = Toy().cuda()
+    m = cls().cuda()
     for p in m.parameters():
         if p.requires_grad:
             p.grad = torch.randn_like(p) * 1e-2
     return m
 
 
-def test_hybrid_step_matches_oracle():
+def check_step_against_oracle(model, **kw):
+    """One HybridOptimizer step, route by route (row blocks of a fused
+    weight included) against the oracle: Muon routes on their rows with
+    their view, AdamW routes with the clip over every AdamW gradient."""
     from adamw_optimizer_step_gb300.routing import HybridOptimizer
-    model = make_model(1)
     before = {n: (p.detach().clone(), p.grad.clone()) for n, p in model.named_parameters() if p.requires_grad}
-    opt = HybridOptimizer(model, muon_lr=0.02, adamw_lr=1e-3, weight_decay=0.1, precision="bf16")
+    opt = HybridOptimizer(model, muon_lr=0.02, adamw_lr=1e-3, weight_decay=0.1, precision="bf16", **kw)
     norm = opt.step()
     torch.cuda.synchronize()
     assert int(opt.status.item()) == 0
-    adam_grads = [f64(before[r.name][1]) for r in opt.adamw]
+    adam_grads = [f64(r.part(before[r.name][1])) for r in opt.adamw]
     N = oracle.global_grad_norm(adam_grads)
     assert abs(float(norm.item()) - N) <= 1e-6 * N
     c = oracle.clip_coefficient(N, 1.0)
     for r in opt.routes:
-        W0, G = (f64(t) for t in before[r.name])
-        got = f64(r.param.detach())
+        W0, G = (f64(r.part(t)) for t in before[r.name])
+        got = f64(r.part(r.param.detach()))
         if r.algorithm == "muon":
             Wn, _, _, U = oracle.muon_step_tensor(W0, G, np.zeros_like(G), view=r.view, split=r.split,
                                                   lr=0.02, wd=r.weight_decay)
@@ -53,11 +55,25 @@ def test_hybrid_step_matches_oracle():
                 sl = slice(r0, r0 + m)
                 bound = (np.linalg.norm(ulp(Wn[sl], torch.float32)) + 0.02 * TOL["bf16"] * np.linalg.norm(U[sl])
                          + 1e-6 * np.linalg.norm(W0[sl]))
-                assert np.linalg.norm(got[sl] - Wn[sl]) <= bound, r.name
+                assert np.linalg.norm(got[sl] - Wn[sl]) <= bound, r.key
         else:
             pn, _, _ = oracle.adamw_update(W0, G, np.zeros_like(G), np.zeros_like(G), coef=c, lr=1e-3,
                                            wd=r.weight_decay, t=1)
-            assert np.max(np.abs(got - pn) - (1e-6 * 1e-3 + 2 ** -23 * np.abs(pn))) <= 0, r.name
+            assert np.max(np.abs(got - pn) - (1e-6 * 1e-3 + 2 ** -23 * np.abs(pn))) <= 0, r.key
+    return opt
+
+
+def test_hybrid_step_matches_oracle():
+    check_step_against_oracle(make_model(1))
+
+
+def test_hybrid_step_with_excluded_blocks_matches_oracle():
+    """A fused projection whose gate and per-head vector rows are excluded
+    from Muon: its Muon blocks match the oracle on their own rows and views,
+    its excluded blocks take AdamW (and count in the clip norm)."""
+    opt = check_step_against_oracle(make_model(4, ToyFused), layouts=LAYOUTS)
+    kinds = [(r.algorithm, r.rows) for r in opt.routes if r.name == "gdn.in_proj.weight"]
+    assert kinds == [("muon", (0, 16)), ("muon", (16, 28)), ("adamw", (28, 40)), ("adamw", (40, 44))]
 
 
 def test_hybrid_state_round_trip():

@@ -133,3 +133,87 @@ def test_omn_routing_counts():
     assert sum(r.param.numel() for r in muon) == c["muon_params"]
     assert sum(r.param.numel() for r in adamw) == c["adamw_params"]
     assert all(not r.decay for r in adamw)
+
+
+# ---------------------------------------------------------------------------
+# fused projections with excluded row blocks (Qwen3.8-Flash-Next optimizer
+# notes, section 4: split by meaning, orthogonalise each real sub-matrix,
+# send gate and vector sub-blocks to AdamW, gather back into the fused layout)
+
+from adamw_optimizer_step_gb300.routing import STANDARD_LAYOUTS, Block, Layout  # noqa: E402
+
+
+class FusedGDN(nn.Module):
+    """One fused input projection of a gated linear-attention block: per-head
+    Q and K rows, per-head V rows, an output-gate block, and one decay and one
+    beta row per head (scalars per head, vector-like), stored as one Linear."""
+
+    def __init__(self, H=2, D=4, Dv=6, C=8):
+        super().__init__()
+        self.num_heads, self.d_head, self.dv_head = H, D, Dv
+        self.in_proj = nn.Linear(C, 2 * H * D + 2 * H * Dv + 2 * H, bias=False)
+
+
+def _gdn_blocks(f, lin):
+    H, D, Dv, C = f.num_heads, f.d_head, f.dv_head, lin.in_features
+    return (Block(2 * H * D, view=(2, H, D, C)),   # Q and K per head: Muon
+            Block(H * Dv, view=(H, Dv, C)),         # V per head: Muon
+            Block(H * Dv, path="adamw"),            # output gate: excluded
+            Block(2 * H, path="adamw"))             # decay and beta rows: excluded
+
+
+GDN_LAYOUT = Layout("in_proj", ("num_heads", "d_head", "dv_head"), _gdn_blocks)
+LAYOUTS = STANDARD_LAYOUTS + (GDN_LAYOUT,)
+
+
+class ToyFused(Toy):
+    def __init__(self):
+        super().__init__()
+        self.gdn = FusedGDN()
+
+
+def test_excluded_blocks_route_every_row_once():
+    model = ToyFused()
+    routes = build_parameter_groups(model, weight_decay=0.1, layouts=LAYOUTS)
+    w = model.gdn.in_proj.weight
+    parts = [r for r in routes if r.param is w]
+    assert [(r.algorithm, r.rows) for r in parts] == [
+        ("muon", (0, 16)), ("muon", (16, 28)), ("adamw", (28, 40)), ("adamw", (40, 44))]
+    # every row of the fused weight exactly once, in order
+    covered = [i for r in parts for i in range(*r.rows)]
+    assert covered == list(range(w.shape[0]))
+    assert parts[0].view == (2, 2, 4, 8) and parts[1].view == (2, 6, 8)
+    # excluded blocks keep the matrix's decay; Muon blocks are decayed
+    assert all(r.decay and r.weight_decay == 0.1 for r in parts)
+    # the route keys are unique and name the rows
+    keys = [r.key for r in routes]
+    assert len(keys) == len(set(keys)) and "gdn.in_proj.weight[28:40]" in keys
+    assert parts[2].shape == (12, 8) and parts[3].numel() == 4 * 8
+    # row views are contiguous slices of the parameter
+    assert parts[2].part(w).data_ptr() == w[28:].data_ptr() and parts[2].part(w).is_contiguous()
+    # every trainable element is routed exactly once over the whole model
+    n_routed = sum(r.numel() for r in routes)
+    assert n_routed == sum(p.numel() for p in {id(p): p for p in model.parameters() if p.requires_grad}.values())
+    # without the layout the fused weight is one Muon matrix
+    plain = {r.key: r for r in build_parameter_groups(ToyFused())}
+    assert plain["gdn.in_proj.weight"].algorithm == "muon" and plain["gdn.in_proj.weight"].rows is None
+
+
+def test_layout_refusals():
+    def bad(blocks):
+        return (Layout("in_proj", ("num_heads", "d_head", "dv_head"), lambda f, lin: blocks),)
+
+    with pytest.raises(ValueError):  # rows do not tile the weight
+        build_parameter_groups(FusedGDN(), layouts=bad((Block(16), Block(20, path="adamw"))))
+    with pytest.raises(ValueError):  # a view that does not flatten to its block
+        build_parameter_groups(FusedGDN(), layouts=bad((Block(16, view=(2, 2, 5, 8)), Block(28, path="adamw"))))
+    with pytest.raises(ValueError):  # split sizes that do not sum to the view's row axis
+        build_parameter_groups(FusedGDN(), layouts=bad((Block(16, view=(2, 8, 8), split=(3, 4)),
+                                                        Block(28, path="adamw"))))
+    with pytest.raises(ValueError):  # an excluded block with a view
+        build_parameter_groups(FusedGDN(), layouts=bad((Block(16, path="adamw", view=(2, 8, 8)),
+                                                        Block(28, path="adamw"))))
+    # two layouts declaring different geometry for one weight
+    other = Layout("in_proj", ("num_heads",), lambda f, lin: (Block(44),))
+    with pytest.raises(ValueError):
+        build_parameter_groups(FusedGDN(), layouts=(GDN_LAYOUT, other))
