@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--separate-gram", action="store_true",
                     help="A/B: run the Gram of the on-chip chain's matrices (p <= 128) as a tile-kernel "
                          "launch of its own instead of inside the chain launch (workload 4)")
+    ap.add_argument("--extra", default="2,4,5",
+                    help="after the headline run, time these other workloads in the same process "
+                         "(comma-separated indices, or 'none'); reported under extra_workloads")
     ap.add_argument("--workload", type=int, default=WORKLOAD,
                     help="synthetic set: 3 = the 1.23B OMN-shaped set (the benchmark); 2 = one "
                          "d=2048 layer, 4 = many small MLA/KDA matrices, 5 = 7B NorMuon (profiling)")
@@ -143,9 +146,10 @@ class ClockSampler:
 # the fp64 oracle on a bounded sample (CPU baseline and the reference arm)
 
 def oracle_sample_time(wl, budget_elems=4_000_000):
-    """Time the oracle on one matrix of every distinct oriented shape plus an
-    AdamW slice, and extrapolate to the whole step.  Returns (seconds per
-    full step, description)."""
+    """Time the oracle on one matrix of every distinct oriented shape plus
+    AdamW on ``budget_elems`` elements (all of them with ``budget_elems=None``,
+    in slices of 16M), and extrapolate to the whole step.  Returns (seconds
+    per full step, description)."""
     import numpy as np
     import torch
 
@@ -173,16 +177,22 @@ def oracle_sample_time(wl, budget_elems=4_000_000):
         parts.append("%dx%d x%d" % (m, n, c))
     n_adam = wl.adamw_params
     if n_adam:
-        k = min(budget_elems, n_adam)
+        k = n_adam if budget_elems is None else min(budget_elems, n_adam)
+        # the AdamW oracle is elementwise: a full pass runs slice by slice
+        # (the clip norm over all slices first, as the step does)
+        piece = min(k, 16 * 1024 * 1024)
         g = torch.Generator().manual_seed(7)
-        p, gr, mm, vv = (torch.randn(k, generator=g).double().numpy() for _ in range(4))
+        p, gr, mm, vv = (torch.randn(piece, generator=g).double().numpy() for _ in range(4))
         vv = np.abs(vv)
+        slices = [piece] * (k // piece) + ([k % piece] if k % piece else [])
         t0 = time.perf_counter()
-        N = oracle.global_grad_norm([gr])
-        oracle.adamw_update(p, gr, mm, vv, coef=oracle.clip_coefficient(N, 1.0), lr=3e-4, t=1)
+        N = oracle.global_grad_norm([gr[:n] for n in slices])
+        c = oracle.clip_coefficient(N, 1.0)
+        for n in slices:
+            oracle.adamw_update(p[:n], gr[:n], mm[:n], vv[:n], coef=c, lr=3e-4, t=1)
         dt = time.perf_counter() - t0
         total += dt * n_adam / k
-        parts.append("AdamW %d of %d elements" % (k, n_adam))
+        parts.append("AdamW %s %d of %d elements" % ("all" if k == n_adam else "sampled,", k, n_adam))
     return total, "one matrix per shape (%s), scaled by count; %s" % (", ".join(parts[:-1]), parts[-1])
 
 
@@ -211,7 +221,12 @@ def run_reference(args):
     value = 1.0 / per_step
     out = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "ms_per_step_extrapolated": True,
+        "ms_per_step_basis": "extrapolated, not wall time: each timed step runs the oracle on one matrix of "
+                             "every shape and a 4M-element AdamW slice and scales each part by its count to "
+                             "the full step (steps x ms_per_step is far above this run's wall time)",
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "muon_params": wl.muon_params,
                    "adamw_params": wl.adamw_params},
@@ -334,6 +349,124 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     run(n_steps, wall)
     e2e_t = max_over_ranks(time.perf_counter() - t0, world)
     return aggregate(n_steps, e2e_t, world), h2d, up_gbs, wall
+
+
+# nominal GB300 figures (NVIDIA's datasheet: dense bf16 without sparsity,
+# HBM3e bandwidth), reported beside the measured denominators
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
+
+
+def load_peaks():
+    """The measured roofline denominators (MEASURED_PEAKS.json), else the
+    fallbacks, and where each came from."""
+    measured = {}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        measured = json.load(open(path))
+    burst = measured.get("bf16_tflops")
+    sustained = measured.get("bf16_tflops_sustained")
+    hbm = measured.get("hbm_gbs")
+    src = "measured (MEASURED_PEAKS.json)"
+    if burst is None or hbm is None:
+        burst, sustained, hbm, src = 1900.0, 1700.0, 6800.0, "fallback"
+    return {"burst": burst, "sustained": sustained or burst, "hbm": hbm, "source": src}
+
+
+def step_floor(flops, floor_bytes, peaks):
+    """(tensor ms, HBM ms): executed tensor FLOPs at the burst bf16 rate and
+    the algorithmic bytes at the HBM copy rate; the floor is the larger."""
+    tensor_ms = flops / (peaks["burst"] * 1e12) * 1e3
+    hbm_ms = floor_bytes / (peaks["hbm"] * 1e9) * 1e3
+    return tensor_ms, hbm_ms
+
+
+def floor_bytes_of(wl, torch):
+    """Per Muon parameter G read, B read and written, W read and written;
+    32 B per AdamW parameter (the clip pass and the update)."""
+    w_es = torch.empty(0, dtype=wl.w_dtype).element_size()
+    g_es = torch.empty(0, dtype=wl.g_dtype).element_size()
+    return (g_es + 8 + 2 * w_es) * wl.muon_params + 32.0 * wl.adamw_params
+
+
+EXTRA_STEPS = {2: 200, 4: 30, 5: 5}  # about 0.2 to 1 s of timed work each
+
+
+def run_extra_workload(index, peaks, local, warmup=3):
+    """Steps/s of another synthetic set, timed like the headline run (CUDA
+    events on the launching stream, inputs resident in HBM, clocks sampled
+    during the timed region).  The step is Muon on every matrix, plus clip +
+    AdamW when the set has AdamW parameters."""
+    import torch
+    import adamw_optimizer_step_gb300 as gbo
+    from adamw_optimizer_step_gb300 import workloads as wk
+
+    wl = wk.workload(index)
+    dev = "cuda"
+    entries = []
+    for i, t in enumerate(wl.muon):
+        W, G, Bm, v = wk.muon_tensor_inputs(wl, i, device=dev)
+        entries.append(dict(w=W, g=G, mom=Bm, row_v=v, view=t.view, split=t.split))
+    params = [wk.adamw_tensor_inputs(wl, i, device=dev) for i in range(len(wl.adamw))]
+    plan = gbo.gbo_muon_plan_create(entries, normuon=wl.normuon)
+    info = gbo.gbo_muon_plan_info(plan)
+    ws = torch.empty(gbo.gbo_muon_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+    cws = torch.empty(gbo.gbo_clip_norm_workspace_bytes(), dtype=torch.uint8, device=dev)
+    total = torch.zeros(1, device=dev)
+    coef = torch.zeros(1, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    n = [0]
+
+    def step():
+        n[0] += 1
+        gbo.gbo_muon_step(plan, wl.lr, ws, dev_status=status, stream=stream)
+        if params:
+            gbo.gbo_clip_norm([p[1] for p in params], 1.0, total, coef, cws, dev_status=status, stream=stream)
+            gbo.gbo_adamw_step(params, lr=wl.adamw_lr, step=n[0], coef=coef, dev_status=status, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = EXTRA_STEPS.get(index, 10)
+    gbo.gbo_muon_plan_set_timing(plan, True)
+    gbo.gbo_muon_plan_phase_times(plan)  # reset
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)  # let the sampler start
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    start, end = ev(), ev()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    l0 = gbo.gbo_launch_count()
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    launches = gbo.gbo_launch_count() - l0
+    clk = clocks.stop(t_wall0, time.time())
+    phases = gbo.gbo_muon_plan_phase_times(plan)
+    gbo.gbo_muon_plan_set_timing(plan, False)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d during workload %d" % (int(status.item()), index))
+    ms = start.elapsed_time(end) / steps
+    gemm_ms = sum(phases[k][0] for k in ("gram", "product", "square", "final")) / steps
+    flops = info["ns_flops_executed"]
+    tensor_ms, hbm_ms = step_floor(flops, floor_bytes_of(wl, torch), peaks)
+    ns_tf = flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    return {
+        "workload": wl.name, "description": wl.description, "muon_params": wl.muon_params,
+        "adamw_params": wl.adamw_params, "matrices": info["n_matrices"], "normuon": wl.normuon,
+        "steps": steps, "warmup": warmup, "value": 1e3 / ms, "unit": "steps/s", "ms_per_step": ms,
+        "step_floor": {"ms": max(tensor_ms, hbm_ms), "frac": max(tensor_ms, hbm_ms) / ms, "tensor_ms": tensor_ms,
+                       "hbm_ms": hbm_ms},
+        "ns_tflops_executed": ns_tf,
+        "ns_frac_of_burst": None if ns_tf is None else ns_tf / peaks["burst"],
+        "phases_ms_per_step": {k: v[0] / steps for k, v in phases.items()},
+        "gpu_launches_per_step": launches / steps,
+        "clocks": clk,
+    }
 
 
 def run_ours(args):
@@ -497,16 +630,16 @@ def run_ours(args):
     flops = info["ns_flops_executed"] * (3 if f32 else 1)
     achieved_tf = flops / (gemm_ms / 1e3) / 1e12
     counted_tf = info["ns_flops"] / (gemm_ms / 1e3) / 1e12
-    peaks = {}
-    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk_path):
-        peaks = json.load(open(pk_path))
-    peak_tf = peaks.get("bf16_tflops_sustained")
-    peak_src = "measured (sustained, MEASURED_PEAKS.json)"
-    if peak_tf is None:
-        peak_tf, peak_src = 1700.0, "fallback sustained"
+    peaks = load_peaks()
+    # the Newton-Schulz launches are timed back to back inside 20 ms steps:
+    # the burst bf16 rate is the denominator (the sustained, seconds-long
+    # figure and the nominal datasheet peak are reported beside it)
+    peak_tf = peaks["burst"]
+    peak_src = peaks["source"] + ", burst"
+    scale = 1.0
     if f32:  # TF32 runs at the nominal 1.1 / 2.25 of the bf16 dense rate
-        peak_tf *= 1.1 / 2.25
+        scale = 1.1 / 2.25
+        peak_tf *= scale
         peak_src += " x nominal TF32/bf16 ratio 1.1/2.25"
     tr = traffic_record(TC_KERNEL_SOURCES) if not f32 else None
     traffic = None
@@ -514,20 +647,18 @@ def run_ours(args):
         traffic = tr["bytes_per_unit"] * (flops / gemm_launches) / tr["unit_flops"]
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        t_cpu, desc = oracle_sample_time(wl)
+        t_cpu, desc = oracle_sample_time(wl, budget_elems=None)
         cpu = {"value": 1.0 / t_cpu, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": desc}
-    hbm = peaks.get("hbm_gbs", 6800.0)
+               "sample": desc, "extrapolated": "the Muon part (one matrix per shape x count); AdamW + clip "
+                                               "timed over every element"}
+    hbm = peaks["hbm"]
     adam_bytes = 32.0 * n_adam
     # The step's floor: the executed tensor FLOPs at the tensor peak, or the
     # algorithmic bytes at HBM bandwidth, whichever is longer (perfect overlap
     # of the two).  Bytes: per Muon parameter G read, B read and written, W
     # read and written; per AdamW parameter 32 B.
-    w_es = torch.empty(0, dtype=wl.w_dtype).element_size()
-    g_es = torch.empty(0, dtype=wl.g_dtype).element_size()
-    floor_bytes = (g_es + 8 + 2 * w_es) * wl.muon_params + adam_bytes
-    floor_tensor_ms = flops / (peak_tf * 1e12) * 1e3
-    floor_hbm_ms = floor_bytes / (hbm * 1e9) * 1e3
+    floor_bytes = floor_bytes_of(wl, torch)
+    floor_tensor_ms, floor_hbm_ms = step_floor(flops / scale, floor_bytes, peaks)
     out = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -546,6 +677,9 @@ def run_ours(args):
                                + " (all Newton-Schulz launches), executed FLOPs",
                      "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
                      "peak_source": peak_src, "traffic": traffic,
+                     "frac_of_sustained": achieved_tf / (peaks["sustained"] * scale),
+                     "frac_of_nominal": achieved_tf / (NOMINAL_BF16_TFLOPS * scale),
+                     "nominal_source": "NVIDIA GB300 datasheet: 2.25 PFLOP/s dense bf16 (TF32 1.1)",
                      "flops_per_launch": flops / gemm_launches, "ms_per_launch": gemm_ms / gemm_launches},
         "phases_ms_per_step": {k: v[0] / args.steps for k, v in phases.items()},
         "step_ms": {"median": step_ms[len(step_ms) // 2], "min": step_ms[0], "max": step_ms[-1]},
@@ -555,6 +689,7 @@ def run_ours(args):
                                 "parameter) / HBM copy bandwidth)"},
         "adamw_clip": {"ms": adam_ms, "GB/s": adam_bytes / (adam_ms / 1e3) / 1e9,
                        "frac_of_hbm": adam_bytes / (adam_ms / 1e3) / 1e9 / hbm,
+                       "frac_of_nominal_hbm": adam_bytes / (adam_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                        "stream": "side stream, overlapped with the Muon GEMMs" if overlap else "main stream"},
         "ns_tflops": {"executed": achieved_tf, "counted_dense": counted_tf,
                       "executed_tflop_per_step": flops / 1e12, "counted_tflop_per_step": info["ns_flops"] / 1e12},
@@ -576,16 +711,32 @@ def run_ours(args):
         "clocks": clk,
         "cpu_baseline": cpu,
     }
-    print(json.dumps(out), flush=True)
+    return out
 
 
 def main():
     args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
         run_reference(args)
     else:
-        run_ours(args)
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+        out = run_ours(args)
+        if out is not None:
+            extra = [] if args.extra in ("", "none") else [int(x) for x in args.extra.split(",")]
+            extra = [x for x in extra if x != args.workload and not args.layers]
+            if extra and world == 1:
+                # the headline run's buffers are gone with run_ours; each set
+                # is built, timed and freed in turn
+                import gc
+                import torch
+                gc.collect()
+                torch.cuda.empty_cache()
+                peaks = load_peaks()
+                out["extra_workloads"] = {}
+                for index in extra:
+                    out["extra_workloads"][str(index)] = run_extra_workload(index, peaks, dist_env()[2])
+                    gc.collect()
+            print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
         if dist.is_initialized():
