@@ -70,7 +70,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("n_weights", c_int64), ("n_active", c_int64), ("n_matrices", c_int64),
                 ("n_shape_classes", c_int64), ("muon_params", c_int64), ("ns_flops", ctypes.c_double),
                 ("ns_flops_executed", ctypes.c_double), ("launches_per_step", c_int64),
-                ("n_gram_route", c_int64)]
+                ("n_gram_route", c_int64), ("n_mom_fused", c_int64)]
 
 
 _STRUCTS = (MuonDesc, MuonOpts, Tensor, AdamWDesc, AdamWOpts, PlanInfo)
@@ -109,11 +109,13 @@ def lib():
         "gbo_testing_wait_timeout": (c_int32, [c_void_p, ctypes.c_uint32, c_void_p]),
         "gbo_testing_set_small_chain": (c_int32, [c_int32]),
         "gbo_testing_set_fused_gram": (c_int32, [c_int32]),
+        "gbo_testing_set_fused_momentum": (c_int32, [c_int32]),
         "gbo_last_error": (ctypes.c_char_p, []),
         "gbo_abi_version": (c_int32, []),
         "gbo_struct_size": (c_size_t, [c_int32]),
         "gbo_launch_count": (ctypes.c_uint64, []),
         "gbo_muon_plan_info": (c_int32, [c_void_p, ctypes.POINTER(PlanInfo)]),
+        "gbo_muon_plan_desc_flops": (c_int32, [c_void_p, ctypes.POINTER(ctypes.c_double), c_int32]),
         "gbo_muon_plan_set_timing": (c_int32, [c_void_p, c_int32]),
         "gbo_muon_plan_set_event": (c_int32, [c_void_p, c_int32, c_void_p]),
         "gbo_muon_plan_phase_times": (c_int32, [c_void_p, ctypes.POINTER(c_float), ctypes.POINTER(c_int64),
@@ -144,10 +146,10 @@ def _dtype(t):
     raise TypeError("tensor dtype must be float32 or bfloat16, got %s" % t.dtype)
 
 
-def _dev_ptr(t, what):
+def _dev_ptr(t, what, allow_host=False):
     if t is None:
         return None
-    if not t.is_cuda:
+    if not t.is_cuda and not allow_host:
         raise ValueError("%s must be a CUDA tensor" % what)
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % what)
@@ -168,9 +170,10 @@ def _stream(stream):
 class MuonPlan:
     """Owns a ``gbo_plan*`` and keeps the tensors it points to alive."""
 
-    def __init__(self, handle, keepalive):
+    def __init__(self, handle, keepalive, n_descs=0):
         self.handle = handle
         self._keep = keepalive
+        self.n_descs = n_descs
 
     def __del__(self):
         if getattr(self, "handle", None) and _lib is not None:
@@ -178,12 +181,15 @@ class MuonPlan:
             self.handle = None
 
 
-def muon_desc_table(entries):
+def muon_desc_table(entries, allow_host=False):
     """Marshal Muon weights into a ``gbo_muon_desc`` array and a split pool.
 
     Each entry is a dict with ``w`` (rows x cols, float32/bfloat16), ``g``
     (same shape, or None to skip), ``mom`` (float32), optional ``row_v``
     (float32, rows), ``view`` (tuple), ``split`` (tuple), ``lr_mult``, ``wd``.
+    ``allow_host``: accept host tensors, for a plan that is only queried
+    (plan creation never dereferences the pointers; such a plan must never
+    be stepped).
     """
     arr = (MuonDesc * len(entries))()
     pool = []
@@ -192,10 +198,10 @@ def muon_desc_table(entries):
         w, g, mom, rv = e["w"], e.get("g"), e.get("mom"), e.get("row_v")
         if w.dim() != 2:
             raise ValueError("Muon weights are 2-D")
-        d.w = _dev_ptr(w, "w")
-        d.g = _dev_ptr(g, "g")
-        d.mom = _dev_ptr(mom, "mom")
-        d.row_v = _dev_ptr(rv, "row_v")
+        d.w = _dev_ptr(w, "w", allow_host)
+        d.g = _dev_ptr(g, "g", allow_host)
+        d.mom = _dev_ptr(mom, "mom", allow_host)
+        d.row_v = _dev_ptr(rv, "row_v", allow_host)
         d.rows, d.cols = w.shape
         d.w_dtype = _dtype(w)
         d.g_dtype = _dtype(g) if g is not None else d.w_dtype
@@ -219,12 +225,12 @@ def muon_desc_table(entries):
 
 def gbo_muon_plan_create(entries, *, abc=(1.5, -0.5, 0.0), ns_steps=5, mu=0.95, nesterov=True,
                          precision=GBO_NS_BF16, normuon=False, beta2=0.95, eps=1e-8, route=GBO_ROUTE_AUTO,
-                         rms_target=0.0):
+                         rms_target=0.0, _query_only=False):
     """Validate a Muon table and build a plan (``abc``: one triple or one per step;
     ``route``: GBO_ROUTE_AUTO, GBO_ROUTE_X or GBO_ROUTE_GRAM; ``rms_target`` > 0
     with NorMuon: each matrix's update is scaled to that RMS)."""
     L = lib()
-    arr, pool, keep = muon_desc_table(entries)
+    arr, pool, keep = muon_desc_table(entries, allow_host=_query_only)
     flat = []
     for t in ([abc] if len(abc) and not hasattr(abc[0], "__len__") else abc):
         flat += [float(x) for x in t]
@@ -236,7 +242,7 @@ def gbo_muon_plan_create(entries, *, abc=(1.5, -0.5, 0.0), ns_steps=5, mu=0.95, 
     cpool = (c_int64 * max(1, len(pool)))(*pool)
     out = c_void_p()
     _check(L.gbo_muon_plan_create(arr, len(entries), cpool, len(pool), ctypes.byref(opts), ctypes.byref(out)))
-    return MuonPlan(out.value, keep)
+    return MuonPlan(out.value, keep, len(entries))
 
 
 def gbo_muon_plan_destroy(plan):
@@ -257,6 +263,24 @@ def gbo_muon_plan_info(plan):
     info = PlanInfo()
     _check(lib().gbo_muon_plan_info(plan.handle, ctypes.byref(info)))
     return {k: getattr(info, k) for k, _ in PlanInfo._fields_}
+
+
+def muon_desc_flops(entries, **opts):
+    """Executed Newton-Schulz FLOPs per step of every entry (host or device
+    tensors), from a plan built only to be queried and then dropped."""
+    plan = gbo_muon_plan_create(entries, _query_only=True, **opts)
+    try:
+        return gbo_muon_plan_desc_flops(plan)
+    finally:
+        gbo_muon_plan_destroy(plan)
+
+
+def gbo_muon_plan_desc_flops(plan):
+    """Executed Newton-Schulz FLOPs per step of every descriptor, in table order."""
+    n = plan.n_descs
+    out = (ctypes.c_double * max(1, n))()
+    _check(lib().gbo_muon_plan_desc_flops(plan.handle, out, n))
+    return [float(out[i]) for i in range(n)]
 
 
 def gbo_muon_step(plan, lr, workspace, dbg_update=None, dev_status=None, stream=None):
@@ -380,6 +404,14 @@ def gbo_testing_set_fused_gram(enable):
     shared memory) rather than as a launch of its own.  Returns the previous
     setting."""
     return bool(lib().gbo_testing_set_fused_gram(1 if enable else 0))
+
+
+def gbo_testing_set_fused_momentum(enable):
+    """Whether plans created from now on run the momentum pass of the chain's
+    wide p <= 128 matrices with bf16 gradients inside the chain launch (G and
+    B streamed through shared memory) rather than in the momentum kernel
+    (the default).  Returns the previous setting."""
+    return bool(lib().gbo_testing_set_fused_momentum(1 if enable else 0))
 
 
 def gbo_testing_wait_timeout(dev_status, limit_us, stream=None):

@@ -50,6 +50,10 @@ struct DevSub {
   int32_t x_sel;    // X buffer (0 or 1) that holds the last iterate (NorMuon rows read it)
   int32_t wmap;     // index of the weight's TMA map (bf16 weights with 16-byte rows), or -1
   int32_t ss_ntn;   // NorMuon (bf16 mode): partials per stored row, one per 128 output columns
+  int32_t mom_fused; // the momentum pass of this matrix runs inside the chain kernel (no momentum tiles)
+  int32_t gbmap;     // with mom_fused: index of its pair of G and B TMA maps (2 * gbmap, 2 * gbmap + 1)
+  int32_t desc;      // the descriptor (stored weight) this matrix belongs to
+  int32_t pad0;
 };
 
 // Matrices of one oriented shape (p, q), stored back to back in the
@@ -73,7 +77,7 @@ struct ShapeClass {
   int32_t tall;   // the stored matrix has more rows than columns (m > n)
   int32_t x_tall; // bf16 mode: X holds a tall matrix in stored orientation, q x p
   int32_t ldt;    // fp32 mode: row stride of XT, X's transposed twin (q x p)
-  int32_t pad1;
+  int32_t mom_fused; // the chain kernel streams G and B and runs the momentum pass of these matrices
   int64_t xt_base; // element offset of the class in each XT buffer
   int64_t x_base; // element offset of the class in each X buffer
   int64_t p_base; // element offset of the class in its p x p buffers (its route's space)
@@ -143,6 +147,10 @@ struct PhaseArgs {
   const float *alpha; // per matrix pre-normalisation factor
   float *dbg;         // dbg_update or nullptr
   int32_t *status;
+  const void *gbmaps; // device array of G and B TMA maps (CUtensorMap) of the matrices with mom_fused
+  float *alpha_out;   // the same factors, written by the chain kernel for its matrices with mom_fused
+  float mu;           // momentum coefficient and Nesterov flag, for the chain kernel's momentum pass
+  int32_t nesterov;
 };
 
 // Launchers (implemented in the .cu files).  Each returns a cudaError_t as
@@ -182,14 +190,22 @@ int launch_ns_gemm_tf32(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &gl
                         void *stream, int64_t *n_launch);
 // kChain jobs (bf16, p <= kChainMaxP): opA = P_0, opB = A_0, out = Q_k
 // regions; or, for a wide class of p <= 128 (kind kKindGram), opA = X_0:
-// the Gram runs on chip too.  Every job of one call has the same steps and
-// abc.
+// the Gram runs on chip too; and when the class has mom_fused, the kernel
+// streams G and B instead, runs the momentum pass, writes X_0 to opA and
+// the pre-normalisation factors to globals.alpha_out.  Every job of one
+// call has the same steps and abc.
 constexpr int kChainMaxP = 192;
 int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &globals, int sm_count,
                        void *stream, int64_t *n_launch);
 // The chain kernel's launch groups: the Gram on chip (p <= 128, wide),
-// p <= 128, 128 < p <= kChainMaxP.
-enum ChainGeometry : int32_t { kChainFused = 0, kChainOne = 1, kChainTwo = 2 };
+// p <= 128, 128 < p <= kChainMaxP, the momentum pass and the Gram on chip
+// (p <= 128, wide, bf16 G).
+enum ChainGeometry : int32_t { kChainFused = 0, kChainOne = 1, kChainTwo = 2, kChainFusedMom = 3 };
+constexpr int kChainGeometries = 4;
+// G and B TMA maps of one weight for matrices of `rows` rows: 2-D over the
+// weight's rows x cols, boxes of 64 columns x rows (bf16 G, fp32 B), no
+// swizzle.  Returns false if the driver refuses them.
+bool encode_gb_maps(void *maps2, const void *g, const float *mom, int64_t rows, int64_t cols, int box_rows);
 int chain_geometry(const GemmJob &J);
 // FLOPs of the on-chip Gram of one p x q matrix: a 128 x 128 tile, K = q
 // padded to 64, and with c_0 != 0 the square of A_0 (K = p padded to 64).

@@ -30,6 +30,23 @@
 // slot's X_0 stream (bound by HBM) runs under the other slot's chain (bound
 // by latency) and neither slot's ops queue behind the other's issue.
 //
+// The momentum pass can run here too (kMom, with kFuse, for wide matrices
+// with bf16 gradients on 16-byte rows): instead of X_0, G and B stream in
+// by TMA through per-weight maps, 64 columns of the matrix's rows at a
+// time, in two 48 KB stages per slot laid over the slot's P, A and Q.  The
+// epilogue warps, between their chain epilogues, turn each landed stage
+// into B <- mu B + G and D = G + mu B (NorMuon paper, section 2.2, eq. (1);
+// OMN page, Muon path), write B and X_0 = bf16(D) to HBM and bf16(D) in
+// place over G as the Gram's K-major operand, and keep per-thread running
+// statistics (max |D| and the sum of (D / max)^2, rescaled when the max
+// grows, so nothing can overflow).  After a matrix's last stage every warp
+// publishes its statistics; the Gram epilogue combines them in a fixed
+// order into the pre-normalisation factor (OMN page: max-abs rescale, then
+// the Frobenius norm, each with its 1e-7), which it folds into A_0 and also
+// writes out for the last product.  X_0 is then never read back for the
+// Gram, and the memory-bound momentum pass of these matrices runs under the
+// latency-bound chain of the other slot.
+//
 // Two geometries (template parameter kH, 128-row halves of a matrix):
 //   kH = 1  p <= 128: 128 x 128 matrices (32 KB each), two matrices in
 //           flight per CTA so the epilogue of one slot's product overlaps
@@ -74,14 +91,31 @@ constexpr int kMaxOps = 4 * GBO_MAX_NS_STEPS + 1;
 constexpr int kCTmemCols = 512;
 constexpr int kRing = 6;                 // X_0 blocks in flight per slot (kFuse)
 constexpr int kRingBytes = 128 * CK * 2; // one 128-row, 64-column bf16 block of X_0
-constexpr int kNBars = 12 + 4 * kRing;   // loaded, mmad, epid, qdone, freed (2 each), drain, full/empty rings, drain2
-constexpr int kNClocks = 11;             // idle-stretch starts: one per warp
+constexpr int kMRing = 2;                // kMom: G and B blocks in flight per slot
+constexpr int kMGBytes = 128 * CK * 2;   // kMom: a stage's G block (p x 64 bf16, then X_0's operand in place)
+constexpr int kMStage = kMGBytes + 128 * CK * 4;  // ... followed by its B block (p x 64 fp32): 48 KB
+// loaded, mmad, epid, qdone, freed (2 each), drain, full/empty rings, drain2,
+// then (kMom) the rings' computed barriers and the statistics barriers
+constexpr int kNBars = 12 + 4 * kRing + 2 * kRing + 2;
+constexpr int kNClocks = 20;             // idle-stretch starts: one per warp
 // kFuse: a second MMA issuer warp (slot 1) after the epilogue warps; with
 // 11 warps a scheduler still holds at most three, so the register budget
 // per thread is that of 10
 constexpr int kIssuer2 = kCThreads / 32;
-template <bool kFuse>
-constexpr int chain_threads() { return kCThreads + (kFuse ? 32 : 0); }
+// kMom: five warpgroups.  Warp 0 loads, warps 1 and 2 issue slot 0's and
+// slot 1's MMAs, warp 3 idles; warps 4..11 are the chain's epilogue warps;
+// warps 12..19 run the momentum pass.  setmaxnreg moves registers from the
+// first and last groups to the epilogue warps; the shares must not exceed
+// the launch's 640 threads x registers per thread (checked before launch).
+constexpr int kMomWarps = 8;
+constexpr int kMomWarp0 = 12;
+constexpr int kRegsCtl = 48, kRegsEpi = 152, kRegsMom = 56;
+constexpr int kMomRegShares = 128 * kRegsCtl + 256 * kRegsEpi + 256 * kRegsMom;
+template <bool kFuse, bool kMom = false>
+constexpr int chain_threads() { return kMom ? 32 * (kMomWarp0 + kMomWarps) : kCThreads + (kFuse ? 32 : 0); }
+// first epilogue warp
+template <bool kMom>
+constexpr int epi_warp0() { return kMom ? 4 : 2; }
 
 // Shared-memory geometry of one slot matrix (K-major rows of 128 bytes in
 // 64-column blocks, 128-byte swizzle, as TMA writes it).
@@ -93,7 +127,7 @@ struct Geo {
   static constexpr int Mat = KB * Blk;           // 32 KB or 72 KB
   static constexpr int Slots = kH == 1 ? 2 : 1;
   static constexpr int SlotSize = 3 * Mat;       // P, A (or T), Q
-  static constexpr int Smem = 1024 /*align*/ + Slots * SlotSize + 512 /*barriers*/;
+  static constexpr int Smem = 1024 /*align*/ + Slots * SlotSize + 1024 /*barriers, statistics*/;
   static constexpr int WarpBlocks = R / 64;      // 32-column blocks per epilogue warp and row block
   // kind::f16: fp32 accumulator, bf16 A and B, A K-major, B MN-major, M = 128, N = R
   static constexpr uint32_t Idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
@@ -109,7 +143,9 @@ struct Geo {
 static_assert(Geo<1>::Smem <= 232448 && Geo<2>::Smem <= 232448, "shared memory per CTA");
 static_assert(kRing * kRingBytes <= Geo<1>::SlotSize, "the X_0 ring lies within one slot");
 static_assert(Geo<1>::Mat == 2 * Geo<1>::Blk, "kH = 1: Q's two 64-column blocks follow A's, one N = 256 operand");
-static_assert((kNBars + 1 + kNClocks) * 8 <= 512, "barriers, TMEM address, abort flag and idle clocks");
+static_assert(kMRing * kMStage <= Geo<1>::SlotSize, "the G and B ring lies within one slot");
+static_assert((kNBars + 1 + kNClocks) * 8 + 2 * 2 * kMomWarps * 4 <= 1024,
+              "barriers, TMEM address, abort flag, idle clocks and the momentum statistics");
 
 // Products of slot matrices (L R: L read K-major, R MN-major) and
 // epilogues of one op of the chain.
@@ -150,6 +186,7 @@ struct ChainParams {
   int32_t q[kMaxClassesPerLaunch];         // kFuse: the Gram's K (columns of X_0, rows when tall)
   int32_t tall[kMaxClassesPerLaunch];      // kFuse: X_0 held q x p
   int32_t sub0[kMaxClassesPerLaunch];      // kFuse: the class's first matrix in the pre-normalisation factors
+  void *x0;                                // kMom: the X_0 region (each matrix at its DevSub x_off)
   int32_t n;
   int32_t n_ops;
   ChainOp ops[kMaxOps];
@@ -347,10 +384,12 @@ __device__ __forceinline__ void chain_epilogue(const ChainOp &o, uint32_t acc_ro
   }
 }
 
-// Warp-uniform test of an mbarrier phase (lane 0 polls, the warp follows).
+// Warp-uniform test of an mbarrier phase (lane 0 polls, the warp follows);
+// non-blocking, since the caller polls other barriers when this one is not
+// ready.
 __device__ __forceinline__ bool warp_try(uint32_t bar, uint32_t parity, int lane) {
   int ok = 0;
-  if (lane == 0) ok = mbar_try(bar, parity) ? 1 : 0;
+  if (lane == 0) ok = mbar_test(bar, parity) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -371,11 +410,104 @@ struct IdleClock {
   }
 };
 
-template <int kH, bool kFuse>
-__global__ void __launch_bounds__(chain_threads<kFuse>(), 1)
+// kMom: a thread's running statistics of the direction D over its elements:
+// m = max |D|, ss = sum of (D / m)^2 (rescaled whenever m grows), inv = 1 / m.
+struct MomStats {
+  float m, ss, inv;
+};
+
+__device__ __forceinline__ void mom_accumulate(MomStats &st, const float (&d)[4]) {
+  const float gm = fmaxf(fmaxf(fabsf(d[0]), fabsf(d[1])), fmaxf(fabsf(d[2]), fabsf(d[3])));
+  if (gm > st.m) {
+    const float inv = 1.0f / gm;
+    const float r = st.m * inv;
+    st.ss *= r * r;
+    st.m = gm;
+    st.inv = inv;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float y = d[k] * st.inv;
+    st.ss = fmaf(y, y, st.ss);
+  }
+}
+
+// kMom: the momentum pass over one landed stage (columns 64 kb .. + 63 of
+// matrix S) for the rows of epilogue warp ew: rows 2 ew + 16 j + (lane >> 4),
+// columns 4 (lane & 15) .. + 3 of the block.  B <- mu B + G and X_0 =
+// bf16(D) go to HBM (columns past the matrix are not stored); bf16(D)
+// replaces G in the stage as the Gram's K-major operand (128-byte swizzle),
+// for every column of the block (TMA filled the ones past the matrix with
+// zeros, so D is zero there).  Rows at or past the matrix's are left alone:
+// they feed only accumulator entries the Gram epilogue discards.
+__device__ __forceinline__ void mom_stage(uint32_t stage, const DevSub &S, __nv_bfloat16 *x0, int kb, int ew,
+                                          int lane, float mu, int nesterov, MomStats &st) {
+  // the matrix's fields in registers: the stores below could alias the
+  // table as far as the compiler knows, and would force a reload of each
+  // field after every store
+  const int m = S.m;
+  const int64_t cols = S.cols, ld = S.ld;
+  const int c4 = lane & 15;
+  const int col = kb * CK + 4 * c4;
+  const bool colok = col < S.n;
+  float *__restrict__ bg = S.mom + S.r0 * cols + col;
+  __nv_bfloat16 *__restrict__ xg = x0 + S.x_off + col;
+  for (int j = 0; j < 128 / 16; j += 2) {
+    uint32_t gv[2][2] = {}, bv[2][4] = {};
+    int rr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      rr[h] = (j + h) * 16 + 2 * ew + (lane >> 4);
+      if (rr[h] < m) {
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                     : "=r"(gv[h][0]), "=r"(gv[h][1])
+                     : "r"(stage + (uint32_t)(rr[h] * 128 + c4 * 8))
+                     : "memory");
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(bv[h][0]), "=r"(bv[h][1]), "=r"(bv[h][2]), "=r"(bv[h][3])
+                     : "r"(stage + (uint32_t)(kMGBytes + rr[h] * 256 + c4 * 16))
+                     : "memory");
+      }
+    }
+    __syncwarp();  // every lane has read its G before the rows are overwritten in place
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = rr[h];
+      if (r >= m) continue;
+      float g[4], nb[4], d[4];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&gv[h][k]);
+        g[2 * k] = __low2float(b2);
+        g[2 * k + 1] = __high2float(b2);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        nb[k] = fmaf(mu, __uint_as_float(bv[h][k]), g[k]);
+        d[k] = nesterov ? fmaf(mu, nb[k], g[k]) : nb[k];
+      }
+      const uint32_t p01 = pack_bf16(d[0], d[1]), p23 = pack_bf16(d[2], d[3]);
+      if (colok) {
+        *reinterpret_cast<float4 *>(bg + (int64_t)r * cols) = make_float4(nb[0], nb[1], nb[2], nb[3]);
+        *reinterpret_cast<uint2 *>(xg + (int64_t)r * ld) = make_uint2(p01, p23);
+      }
+      asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(stage + (uint32_t)(r * 128 + ((((c4 >> 1) ^ (r & 7))) << 4) +
+                                                                          (c4 & 1) * 8)),
+                   "r"(p01), "r"(p23)
+                   : "memory");
+      mom_accumulate(st, d);
+    }
+  }
+}
+
+template <int kH, bool kFuse, bool kMom>
+__global__ void __launch_bounds__(chain_threads<kFuse, kMom>(), 1)
 ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ PhaseArgs A) {
   using G = Geo<kH>;
   static_assert(!kFuse || kH == 1, "the Gram runs on chip for p <= 128 only");
+  static_assert(!kMom || kFuse, "the momentum pass runs on chip only with the Gram");
+  constexpr int kStages = kMom ? kMRing : kRing;         // ring stages per slot
+  constexpr int kStageBytes = kMom ? kMStage : kRingBytes;
   constexpr int S = G::Slots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -385,13 +517,19 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
   // one idle clock per warp
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNBars);
   uint64_t *clocks = bars + kNBars + 1;
+  // kMom: per slot and epilogue warp, (max |D|, sum of (D / max)^2)
+  volatile float *mpart = reinterpret_cast<volatile float *>(clocks + kNClocks);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
   const uint32_t loaded0 = smem_u32(bars), mmad0 = smem_u32(bars + 2), epid0 = smem_u32(bars + 4);
   const uint32_t qdone0 = smem_u32(bars + 6), freed0 = smem_u32(bars + 8), drain = smem_u32(bars + 10);
   const uint32_t full0 = smem_u32(bars + 11), empty0 = smem_u32(bars + 11 + 2 * kRing);
   const uint32_t drain2 = smem_u32(bars + 11 + 4 * kRing);
+  const uint32_t cfull0 = smem_u32(bars + 12 + 4 * kRing), momdone0 = smem_u32(bars + 12 + 6 * kRing);
   auto full_bar = [&](int s, int st) { return full0 + (uint32_t)(8 * (s * kRing + st)); };
   auto empty_bar = [&](int s, int st) { return empty0 + (uint32_t)(8 * (s * kRing + st)); };
+  // kMom: a stage's momentum pass is done (all epilogue warps) and its
+  // operand may be read; a slot's matrix has its statistics published
+  auto cfull_bar = [&](int s, int st) { return cfull0 + (uint32_t)(8 * (s * kRing + st)); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -401,10 +539,12 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
       mbar_init(qdone0 + 8 * s, kCEpiWarps);
       mbar_init(freed0 + 8 * s, 1);
       if (kFuse)
-        for (int st = 0; st < kRing; ++st) {
+        for (int st = 0; st < kStages; ++st) {
           mbar_init(full_bar(s, st), 1);
           mbar_init(empty_bar(s, st), 1);
+          if (kMom) mbar_init(cfull_bar(s, st), kMomWarps);
         }
+      if (kMom) mbar_init(momdone0 + 8 * s, kMomWarps);
     }
     mbar_init(drain, 1);
     mbar_init(drain2, 1);
@@ -430,68 +570,128 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
     *abort_flag = 1;
     flag_status(A.status, GBO_STATUS_TIMEOUT);
   };
+  constexpr int kE0 = epi_warp0<kMom>();
+  const int issuer1 = kMom ? 2 : kIssuer2;
+  // kMom: each role branch first sets its warpgroup's register share (all
+  // four warps of a warpgroup take the same one), so that the compiler
+  // allocates the branch's code within it
 
   if (warp == 0) {
+    if constexpr (kMom) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (lane == 0) {
       int64_t armed[S], ring_n[S];  // the loads of the slot's last matrix; X_0 blocks loaded
       for (int s = 0; s < S; ++s) armed[s] = -1, ring_n[s] = 0;
       bool stop = false;
-      for (int64_t g = 0; mat_of(g) < total && !stop && !*abort_flag; ++g) {
-        const int s = (int)(g % S);
-        const int64_t gs = g / S;  // the slot's matrix count so far
-        if (gs >= 1 && !mbar_wait(freed0 + 8 * s, (uint32_t)((gs - 1) & 1))) {
-          give_up();
-          break;
-        }
-        const int64_t t = mat_of(g);
-        const int c = chain_class(P, t);
-        const int mat = (int)(t - P.mat_start[c]);
-        const uint32_t base = slots + s * G::SlotSize;
-        if constexpr (kFuse) {
-          // X_0 in blocks of 64 along K (a tall X_0's 64-row block as two
-          // 64 x 64 boxes, the second holding columns 64 .. 127); a stage is
-          // reloaded once the MMAs that read it have completed
-          const int nk = (P.q[c] + CK - 1) / CK;
-          for (int kb = 0; kb < nk; ++kb) {
+      if constexpr (kMom) {
+        // Both slots stream at once: polling the two, each slot's next block
+        // is issued as soon as its ring has a free stage (and, for the
+        // slot's next matrix, once the previous one has left the slot), so
+        // one slot's loads keep going while the other slot's chain runs and
+        // the bytes in flight are not capped by one slot's ring.  (The
+        // X_0-streaming variant loads matrix by matrix: there the chain, not
+        // the stream, bounds the time, and streaming both slots at once
+        // delays both chains; measured slower.)
+        int64_t cur[S];  // the slot's current matrix
+        int kbn[S];      // its next block
+        bool open[S];    // the slot's previous matrix has left it
+        for (int s = 0; s < S; ++s) cur[s] = s, kbn[s] = 0, open[s] = false;
+        IdleClock idle(clocks + warp);
+        for (bool any = true; any && !stop && !*abort_flag;) {
+          any = false;
+          bool moved = false;
+          for (int s = 0; s < S; ++s) {
+            const int64_t t = mat_of(cur[s]);
+            if (t >= total) continue;
+            any = true;
+            const int64_t gs = cur[s] / S;  // the slot's matrix count so far
+            if (!open[s]) {
+              if (gs >= 1 && !mbar_test(freed0 + 8 * s, (uint32_t)((gs - 1) & 1))) continue;
+              open[s] = true;
+            }
             const int64_t n = ring_n[s];
-            const int st = (int)(n % kRing);
-            if (n >= kRing && !mbar_wait(empty_bar(s, st), (uint32_t)((n / kRing - 1) & 1))) {
-              give_up();
-              stop = true;
-              break;
-            }
-            const uint32_t dst = base + st * kRingBytes;
-            mbar_expect_tx(full_bar(s, st), kRingBytes);
-            if (P.tall[c]) {
-              tma_load_3d(dst, &P.mapX[c], full_bar(s, st), 0, kb * CK, mat);
-              tma_load_3d(dst + kRingBytes / 2, &P.mapX[c], full_bar(s, st), CK, kb * CK, mat);
-            } else {
-              tma_load_3d(dst, &P.mapX[c], full_bar(s, st), kb * CK, 0, mat);
-            }
+            const int st = (int)(n % kStages);
+            // a stage is reloaded once the MMAs that read it have completed
+            if (n >= kStages && !mbar_test(empty_bar(s, st), (uint32_t)((n / kStages - 1) & 1))) continue;
+            const int c = chain_class(P, t);
+            const int mat = (int)(t - P.mat_start[c]);
+            const int nk = (P.q[c] + CK - 1) / CK;
+            const int kb = kbn[s];
+            const uint32_t dst = slots + s * G::SlotSize + st * kStageBytes;
+            // G and B: 64 columns of the matrix's rows, through its weight's maps
+            const DevSub &Sd = A.subs[P.sub0[c] + mat];
+            const CUtensorMap *gmap = static_cast<const CUtensorMap *>(A.gbmaps) + 2 * Sd.gbmap;
+            mbar_expect_tx(full_bar(s, st), (uint32_t)P.p[c] * (CK * 2 + CK * 4));
+            tma_load_3d(dst, gmap, full_bar(s, st), kb * CK, (int)Sd.r0, 0);
+            tma_load_3d(dst + kMGBytes, gmap + 1, full_bar(s, st), kb * CK, (int)Sd.r0, 0);
             ring_n[s] = n + 1;
+            moved = true;
+            if (++kbn[s] == nk) kbn[s] = 0, cur[s] += S, open[s] = false;
           }
-        } else {
-          const uint32_t bar = loaded0 + 8 * s;
-          mbar_expect_tx(bar, 3 * G::Mat);
-          armed[s] = gs;
-          for (int kb = 0; kb < G::KB; ++kb) {
-            tma_load_3d(base + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);               // P <- P_0
-            tma_load_3d(base + G::Mat + kb * G::Blk, &P.mapA[c], bar, kb * CK, 0, mat);      // A <- A_0
-            tma_load_3d(base + 2 * G::Mat + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);  // Q <- Q_1 = P_0
+          if (any && idle.expired(moved)) {
+            give_up();
+            stop = true;
+          }
+          if (!moved) __nanosleep(64);  // a pass with nothing to issue: leave the issue slots to others
+        }
+      } else {
+        for (int64_t g = 0; mat_of(g) < total && !stop && !*abort_flag; ++g) {
+          const int s = (int)(g % S);
+          const int64_t gs = g / S;  // the slot's matrix count so far
+          if (gs >= 1 && !mbar_wait(freed0 + 8 * s, (uint32_t)((gs - 1) & 1))) {
+            give_up();
+            break;
+          }
+          const int64_t t = mat_of(g);
+          const int c = chain_class(P, t);
+          const int mat = (int)(t - P.mat_start[c]);
+          const uint32_t base = slots + s * G::SlotSize;
+          if constexpr (kFuse) {
+            // X_0 in blocks of 64 along K (a tall X_0's 64-row block as two
+            // 64 x 64 boxes, the second holding columns 64 .. 127); a stage is
+            // reloaded once the MMAs that read it have completed
+            const int nk = (P.q[c] + CK - 1) / CK;
+            for (int kb = 0; kb < nk; ++kb) {
+              const int64_t n = ring_n[s];
+              const int st = (int)(n % kRing);
+              if (n >= kRing && !mbar_wait(empty_bar(s, st), (uint32_t)((n / kRing - 1) & 1))) {
+                give_up();
+                stop = true;
+                break;
+              }
+              const uint32_t dst = base + st * kRingBytes;
+              mbar_expect_tx(full_bar(s, st), kRingBytes);
+              if (P.tall[c]) {
+                tma_load_3d(dst, &P.mapX[c], full_bar(s, st), 0, kb * CK, mat);
+                tma_load_3d(dst + kRingBytes / 2, &P.mapX[c], full_bar(s, st), CK, kb * CK, mat);
+              } else {
+                tma_load_3d(dst, &P.mapX[c], full_bar(s, st), kb * CK, 0, mat);
+              }
+              ring_n[s] = n + 1;
+            }
+          } else {
+            const uint32_t bar = loaded0 + 8 * s;
+            mbar_expect_tx(bar, 3 * G::Mat);
+            armed[s] = gs;
+            for (int kb = 0; kb < G::KB; ++kb) {
+              tma_load_3d(base + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);               // P <- P_0
+              tma_load_3d(base + G::Mat + kb * G::Blk, &P.mapA[c], bar, kb * CK, 0, mat);      // A <- A_0
+              tma_load_3d(base + 2 * G::Mat + kb * G::Blk, &P.mapP[c], bar, kb * CK, 0, mat);  // Q <- Q_1 = P_0
+            }
           }
         }
       }
       if (*abort_flag)  // let the copies armed here land before shared memory goes away
         for (int s = 0; s < S; ++s) {
           if (armed[s] >= 0) (void)mbar_wait(loaded0 + 8 * s, (uint32_t)(armed[s] & 1));
-          for (int64_t n = ring_n[s] > kRing ? ring_n[s] - kRing : 0; n < ring_n[s]; ++n)
-            (void)mbar_wait(full_bar(s, (int)(n % kRing)), (uint32_t)((n / kRing) & 1));
+          for (int64_t n = ring_n[s] > kStages ? ring_n[s] - kStages : 0; n < ring_n[s]; ++n)
+            (void)mbar_wait(full_bar(s, (int)(n % kStages)), (uint32_t)((n / kStages) & 1));
         }
     }
-  } else if (warp == 1 || (kFuse && warp == kIssuer2)) {
+  } else if (warp == 1 || (kFuse && warp == issuer1)) {
+    if constexpr (kMom) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (lane == 0) {
       if constexpr (kFuse) {
-        // one MMA issuer per slot: warp 1 takes slot 0, warp kIssuer2 slot 1
+        // one MMA issuer per slot: warp 1 takes slot 0, warp issuer1 slot 1
         const int s = warp == 1 ? 0 : 1;
         const uint32_t base = slots + s * G::SlotSize;
         const uint32_t acc = tmem_base + (uint32_t)(s * 256);
@@ -521,14 +721,16 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
               const uint32_t lbo = tall ? kRingBytes / 2 : 16, kstep = tall ? 2048 >> 4 : 32 >> 4;
               const uint32_t idesc = tall ? G::IdescMN : G::IdescK;
               for (int kb = 0; kb < nk; ++kb, ++ring_c) {
-                const int st = (int)(ring_c % kRing);
-                if (!mbar_wait(full_bar(s, st), (uint32_t)((ring_c / kRing) & 1))) {
+                const int st = (int)(ring_c % kStages);
+                // the landed block, or (kMom) the operand the momentum pass made of it
+                const uint32_t ready = kMom ? cfull_bar(s, st) : full_bar(s, st);
+                if (!mbar_wait(ready, (uint32_t)((ring_c / kStages) & 1))) {
                   give_up();
                   ok = false;
                   break;
                 }
                 tc_fence_after();
-                const uint64_t d = smem_desc(base + (uint32_t)(st * kRingBytes), lbo, 1024);
+                const uint64_t d = smem_desc(base + (uint32_t)(st * kStageBytes), lbo, 1024);
 #pragma unroll
                 for (int k = 0; k < CK / 16; ++k)
                   chain_mma<kH>(acc, d + k * kstep, d + k * kstep, (kb | k) != 0, idesc);
@@ -596,9 +798,10 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
         }
       }
     }
-  } else if (warp >= 2 && warp < 2 + kCEpiWarps) {
+  } else if (warp >= kE0 && warp < kE0 + kCEpiWarps) {
+    if constexpr (kMom) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
     const int quarter = warp & 3;      // TMEM lane quarter of this warp
-    const int wh = (warp - 2) >> 2;    // its column blocks: wh * WarpBlocks ..
+    const int wh = (warp - kE0) >> 2;  // its column blocks: wh * WarpBlocks ..
     const int cb0 = wh * G::WarpBlocks, cb1 = cb0 + G::WarpBlocks;
     int64_t g[S];
     int op[S];
@@ -630,7 +833,39 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
         const uint32_t mP = base, mA = base + G::Mat, mQ = base + 2 * G::Mat;
         float s2 = 1.f;
         if (kFuse && (o.epi == kEpiGram || o.epi == kEpiGramA)) {
-          const float al = A.alpha[P.sub0[c] + (t - P.mat_start[c])];
+          const int64_t si = P.sub0[c] + (t - P.mat_start[c]);
+          float al;
+          if constexpr (kMom) {
+            // the pre-normalisation factor from the eight warps' statistics,
+            // combined in a fixed order (as the momentum kernel's partials
+            // are): s = max(max |D|, 1e-7), alpha = 1 / (s (||D / s||_F + 1e-7))
+            if (!mbar_wait(momdone0 + 8 * s, (uint32_t)((g[s] / S) & 1))) {
+              give_up();
+              stop = true;
+              break;
+            }
+            float M = 0.f;
+            for (int w = 0; w < kMomWarps; ++w) M = fmaxf(M, mpart[(s * kMomWarps + w) * 2]);
+            float ss = 0.f;
+            if (M > 0.f) {
+              const float inv = 1.0f / M;
+              for (int w = 0; w < kMomWarps; ++w) {
+                const float r = mpart[(s * kMomWarps + w) * 2] * inv;
+                ss = fmaf(mpart[(s * kMomWarps + w) * 2 + 1], r * r, ss);
+              }
+            }
+            const float sc = fmaxf(M, 1e-7f);
+            const float norm_y = (M / sc) * sqrtf(ss);
+            al = 1.0f / (sc * (norm_y + 1e-7f));
+            const bool bad = !isfinite(M) || !isfinite(ss) || !isfinite(al);
+            if (bad) al = __int_as_float(0x7fc00000);
+            if (warp == kE0 && lane == 0) {
+              A.alpha_out[si] = al;
+              if (bad) flag_status(A.status, GBO_STATUS_NONFINITE);
+            }
+          } else {
+            al = A.alpha[si];
+          }
           s2 = al * al;
         }
         chain_epilogue<kH, kFuse>(o, tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(s * 256), quarter, lane,
@@ -644,7 +879,7 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
           // Q_k to HBM once all epilogue warps have written it; the slot is
           // free for its next matrix when the store has read it
           if (lane == 0) mbar_arrive(qdone0 + 8 * s);
-          if (warp == 2) {
+          if (warp == kE0) {
             const uint32_t qpar = (uint32_t)((g[s] / S) & 1);
             if (!mbar_wait(qdone0 + 8 * s, qpar)) {
               give_up();
@@ -673,10 +908,87 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
           if (lane == 0) give_up();
           stop = true;
         }
+        if (!moved) __nanosleep(32);
       }
     }
     if (lane == 0) bulk_wait_all();  // this warp's stores complete before the kernel ends
     __syncwarp();
+  } else if (kMom && warp >= kMomWarp0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMom));
+    // The momentum pass: each landed stage of either slot, in the slot's
+    // order, by all eight warps (each its rows); after a matrix's last
+    // stage each warp publishes its statistics, before releasing that stage
+    // to the MMA issuer, so they are in place by the time the Gram's MMAs
+    // (and so its epilogue) complete.
+    const int mw = warp - kMomWarp0;
+    int64_t g[S];     // the slot's current matrix
+    int64_t mrc[S];   // G and B stages consumed in the slot
+    int mkb[S];       // stages of the slot's current matrix done
+    MomStats mst[S];  // this thread's statistics of the slot's current matrix
+    for (int s = 0; s < S; ++s) g[s] = s, mrc[s] = 0, mkb[s] = 0, mst[s] = MomStats{0.f, 0.f, 0.f};
+    bool stop = false;
+    IdleClock idle(clocks + warp);
+    for (bool any = true; any && !stop && !*abort_flag;) {
+      any = false;
+      bool moved = false;
+      // the slot holding the older matrix first, so that it finishes its
+      // stream (and starts its chain) while the other slot still streams,
+      // rather than the two slots streaming and then chaining in lockstep
+      const int first = (S > 1 && g[1] < g[0]) ? 1 : 0;
+      for (int k = 0; k < S && !*abort_flag; ++k) {
+        const int s = k == 0 ? first : 1 - first;
+        const int64_t t = mat_of(g[s]);
+        if (t >= total) continue;
+        any = true;
+        const int cm = chain_class(P, t);
+        const int nk = (P.q[cm] + CK - 1) / CK;
+        const int64_t n = mrc[s];
+        const int st = (int)(n % kStages);
+        const uint32_t par = (uint32_t)((n / kStages) & 1);
+        if (!warp_try(full_bar(s, st), par, lane)) continue;
+        (void)mbar_wait(full_bar(s, st), par);  // every lane's own acquire (completes at once)
+        const DevSub &Sd = A.subs[P.sub0[cm] + (t - P.mat_start[cm])];
+        MomStats stt = mst[s];
+        mom_stage(slots + s * G::SlotSize + st * kStageBytes, Sd, static_cast<__nv_bfloat16 *>(P.x0), mkb[s], mw,
+                  lane, A.mu, A.nesterov, stt);
+        const bool last = mkb[s] + 1 == nk;
+        if (last) {
+          const float mx = warp_max(stt.m);
+          float sw = 0.f;
+          if (mx > 0.f) {
+            const float r = stt.m / mx;
+            sw = stt.ss * r * r;
+          }
+          sw = warp_sum(sw);
+          if (lane == 0) {
+            mpart[(s * kMomWarps + mw) * 2] = mx;
+            mpart[(s * kMomWarps + mw) * 2 + 1] = sw;
+            mbar_arrive(momdone0 + 8 * s);
+          }
+          stt = MomStats{0.f, 0.f, 0.f};
+        }
+        mst[s] = stt;
+        fence_async_smem();  // the operand written in place reaches the tensor cores' proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cfull_bar(s, st));
+        mrc[s] = n + 1;
+        if (last) mkb[s] = 0, g[s] += S;
+        else ++mkb[s];
+        moved = true;
+        break;  // poll again from the older slot
+      }
+      if (any) {
+        int late = 0;
+        if (lane == 0) late = idle.expired(moved) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, late, 0)) {
+          if (lane == 0) give_up();
+          stop = true;
+        }
+        if (!moved) __nanosleep(32);
+      }
+    }
+  } else if (kMom) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));  // warp 3: no role
   }
 
   tc_fence_before();
@@ -730,7 +1042,7 @@ int fused_ops(int k, const float *abc, ChainOp *ops) {
 
 int chain_halves(int p) { return p <= 128 ? 1 : 2; }
 
-template <int kH, bool kFuse>
+template <int kH, bool kFuse, bool kMom>
 int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count, void *stream,
                     int64_t *n_launch) {
   using G = Geo<kH>;
@@ -738,7 +1050,15 @@ int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
     attr_err =
-        cudaFuncSetAttribute(ns_chain_kernel<kH, kFuse>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::Smem);
+        cudaFuncSetAttribute(ns_chain_kernel<kH, kFuse, kMom>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::Smem);
+    if (kMom && attr_err == cudaSuccess) {
+      // setmaxnreg.inc waits until the registers it asks for are free: the
+      // warpgroups' shares must fit in what the block is launched with
+      cudaFuncAttributes fa;
+      attr_err = cudaFuncGetAttributes(&fa, ns_chain_kernel<kH, kFuse, kMom>);
+      if (attr_err == cudaSuccess && (int64_t)fa.numRegs * chain_threads<kFuse, kMom>() < kMomRegShares)
+        attr_err = cudaErrorInvalidConfiguration;
+    }
   });
   if (attr_err != cudaSuccess) return (int)attr_err;
   for (int32_t j0 = 0; j0 < n_jobs; j0 += kMaxClassesPerLaunch) {
@@ -753,11 +1073,14 @@ int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
       const ShapeClass &C = *J.cls;
       const bool gram = J.kind == kKindGram || J.kind == kKindGramT;
       if (chain_halves(C.p) != kH || C.p > G::R || J.steps != J0.steps || J.abc != J0.abc || gram != kFuse ||
-          (kFuse && (J.kind == kKindGramT) != (C.x_tall != 0)))
+          (kFuse && (J.kind == kKindGramT) != (C.x_tall != 0)) || (C.mom_fused != 0) != kMom ||
+          (kMom && (C.x_tall || J.opA != J0.opA || !args.gbmaps || !args.alpha_out)))
         return (int)cudaErrorInvalidValue;
       auto at = [&](const void *region) { return static_cast<char *>(const_cast<void *>(region)) + C.p_base * 2; };
       bool ok = encode_map(&T.mapQ[k], at(J.out), C.p, C.p, C.count, C.ldp, CK, G::R);
-      if (kFuse) {  // X_0 in x-space: count matrices of p rows (q when tall), row stride ld
+      if (kMom) {  // X_0 is written, not read: its region base
+        T.x0 = const_cast<void *>(J.opA);
+      } else if (kFuse) {  // X_0 in x-space: count matrices of p rows (q when tall), row stride ld
         char *x = static_cast<char *>(const_cast<void *>(J.opA)) + C.x_base * 2;
         ok = ok && (C.x_tall ? encode_map(&T.mapX[k], x, C.p, C.q, C.count, C.ld, CK, CK)
                              : encode_map(&T.mapX[k], x, C.q, C.p, C.count, C.ld, CK, 128));
@@ -775,8 +1098,8 @@ int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
     const int64_t total = T.mat_start[T.n];
     if (total == 0) continue;
     const unsigned grid = (unsigned)std::min<int64_t>(total, sm_count);  // one CTA per SM
-    ns_chain_kernel<kH, kFuse><<<grid, chain_threads<kFuse>(), G::Smem, reinterpret_cast<cudaStream_t>(stream)>>>(T,
-                                                                                                        args);
+    ns_chain_kernel<kH, kFuse, kMom>
+        <<<grid, chain_threads<kFuse, kMom>(), G::Smem, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
     count_launches(1);
     if (n_launch) ++*n_launch;
     const cudaError_t err = cudaGetLastError();
@@ -803,26 +1126,40 @@ double tc_fused_gram_flops(int p, int q, const float *abc) {
   return tile * (double)((q + CK - 1) / CK) * CK + (abc[2] != 0.f ? tile * (double)((p + CK - 1) / CK) * CK : 0.0);
 }
 
+static_assert(sizeof(CUtensorMap) == 128, "tensor map size assumed by the plan's G and B map table");
+
+bool encode_gb_maps(void *maps2, const void *g, const float *mom, int64_t rows, int64_t cols, int box_rows) {
+  CUtensorMap *m = static_cast<CUtensorMap *>(maps2);
+  return encode_map(&m[0], const_cast<void *>(g), cols, rows, 1, cols, CK, (uint32_t)box_rows,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2) &&
+         encode_map(&m[1], const_cast<float *>(mom), cols, rows, 1, cols, CK, (uint32_t)box_rows,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4);
+}
+
 int chain_geometry(const GemmJob &J) {
-  if (J.kind == kKindGram || J.kind == kKindGramT) return kChainFused;
+  if (J.kind == kKindGram || J.kind == kKindGramT) return J.cls->mom_fused ? kChainFusedMom : kChainFused;
   return chain_halves(J.cls->p) == 1 ? kChainOne : kChainTwo;
 }
 
 int launch_ns_chain_tc(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &args, int sm_count,
                        void *stream, int64_t *n_launch) {
-  std::vector<const GemmJob *> by[3];
+  std::vector<const GemmJob *> by[kChainGeometries];
   for (int32_t j = 0; j < n_jobs; ++j) {
     if (jobs[j]->cls->p > kChainMaxP) return (int)cudaErrorInvalidValue;
     by[chain_geometry(*jobs[j])].push_back(jobs[j]);
   }
-  int err = launch_geometry<1, true>(by[kChainFused].data(), (int32_t)by[kChainFused].size(), args, sm_count,
-                                     stream, n_launch);
+  // the momentum pass first: it writes the X_0 and factors other launches read
+  int err = launch_geometry<1, true, true>(by[kChainFusedMom].data(), (int32_t)by[kChainFusedMom].size(), args,
+                                           sm_count, stream, n_launch);
   if (err) return err;
-  err = launch_geometry<1, false>(by[kChainOne].data(), (int32_t)by[kChainOne].size(), args, sm_count, stream,
-                                  n_launch);
+  err = launch_geometry<1, true, false>(by[kChainFused].data(), (int32_t)by[kChainFused].size(), args, sm_count,
+                                        stream, n_launch);
   if (err) return err;
-  return launch_geometry<2, false>(by[kChainTwo].data(), (int32_t)by[kChainTwo].size(), args, sm_count, stream,
-                                   n_launch);
+  err = launch_geometry<1, false, false>(by[kChainOne].data(), (int32_t)by[kChainOne].size(), args, sm_count,
+                                         stream, n_launch);
+  if (err) return err;
+  return launch_geometry<2, false, false>(by[kChainTwo].data(), (int32_t)by[kChainTwo].size(), args, sm_count,
+                                          stream, n_launch);
 }
 
 }  // namespace gbo

@@ -9,6 +9,8 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <memory>
+#include <cstdlib>
 #include <tuple>
 #include <mutex>
 #include <string>
@@ -25,6 +27,7 @@ namespace gbo {
 static std::atomic<uint64_t> g_launches{0};
 static std::atomic<int32_t> g_small_chain{1};  // see gbo_testing_set_small_chain
 static std::atomic<int32_t> g_fused_gram{1};   // see gbo_testing_set_fused_gram
+static std::atomic<int32_t> g_fused_mom{0};    // see gbo_testing_set_fused_momentum (off: measured slower)
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 namespace {
@@ -129,6 +132,11 @@ struct gbo_plan {
   bool any_gram = false;     // some class takes the Gram route
   bool small_chain = true;   // Gram-route classes with p <= kChainMaxP run the on-chip chain (bf16)
   bool fused_gram = true;    // ... and those of p <= 128 held wide start it from X_0
+  bool fused_mom = false;    // ... and those with bf16 G on 16-byte rows run their momentum pass there too
+  bool any_mom_fused = false;
+  int64_t n_unfused = 0;     // matrices whose momentum pass is the momentum kernel's
+  // (descriptor, rows) of every G and B TMA map pair the fused momentum pass uses
+  std::vector<std::pair<int32_t, int32_t>> gb_pairs;
   std::vector<DevSub> subs;  // sorted by shape class
   std::vector<ShapeClass> classes;
   int64_t n_tiles = 0, n_row_blocks = 0;
@@ -145,11 +153,13 @@ struct gbo_plan {
   bool rows_streamed = false;
   uint64_t hash = 0;
   gbo_plan_info info{};
+  std::vector<double> class_flops;  // executed Newton-Schulz FLOPs of one matrix of each class
   // device state, set by the first step
   int device = -1;
   int sm_count = 0;
   DevSub *d_subs = nullptr;
   void *d_wmaps = nullptr;  // the weights' TMA maps (bf16 mode)
+  void *d_gbmaps = nullptr; // the G and B TMA maps of the fused momentum pass
   // phase timing
   bool timing = false;
   struct Interval {
@@ -311,6 +321,8 @@ int validate_and_expand(gbo_plan *P) {
         S.lr_mult = d.lr_mult;
         S.wd = d.wd;
         S.dbg_off = this_dbg;
+        S.gbmap = t;  // the descriptor, until the fused momentum pass's maps are numbered
+        S.desc = t;
         const ClassKey key(S.p, S.q, S.m > S.n ? 1 : 0);
         auto it = class_of.find(key);
         if (it == class_of.end()) {
@@ -339,8 +351,16 @@ int validate_and_expand(gbo_plan *P) {
   // order by class (stable: table order within a class)
   std::stable_sort(subs.begin(), subs.end(), [](const DevSub &a, const DevSub &b) { return a.cls < b.cls; });
   const size_t es = P->x_dtype == GBO_BF16 ? 2 : 4;
+  // classes whose every matrix can stream G and B through the chain kernel:
+  // bf16 G, and G and B rows on 16-byte boundaries (the TMA maps' strides)
+  std::vector<char> mom_ok(class_shapes.size(), 1);
+  for (const DevSub &S : subs)
+    if (S.g_dtype != GBO_BF16 || !S.vec_ok) mom_ok[S.cls] = 0;
   P->classes.clear();
   P->any_gram = false;
+  P->any_mom_fused = false;
+  P->gb_pairs.clear();
+  std::map<std::pair<int32_t, int32_t>, int32_t> gb_index;
   int64_t xoff = 0, xtoff = 0, poff = 0, goff = 0, x_route_end = 0;
   for (size_t c = 0; c < order.size(); ++c) {
     ShapeClass C{};
@@ -360,6 +380,9 @@ int validate_and_expand(gbo_plan *P) {
     // p x p buffers: the X route's P (and A) space, or the Gram route's own space
     int64_t &pspace = C.route == kRouteGram ? goff : poff;
     C.p_base = pspace;
+    // the momentum pass in the chain kernel: wide classes whose Gram runs on chip
+    C.mom_fused = (P->fused_mom && tc_path && !C.x_tall && fuses_gram(P, C) && mom_ok[c]) ? 1 : 0;
+    P->any_mom_fused = P->any_mom_fused || C.mom_fused;
     for (size_t k = 0; k < subs.size(); ++k)
       if (subs[k].cls == (int32_t)c) {
         if (C.sub0 < 0) C.sub0 = (int32_t)k;
@@ -373,6 +396,18 @@ int validate_and_expand(gbo_plan *P) {
         // the last iterate: X_k of the X route alternates buffers from X0;
         // the Gram route writes X_k = Q_k X_0 into the second buffer
         S.x_sel = C.route == kRouteGram ? 1 : (o.ns_steps & 1);
+        S.mom_fused = C.mom_fused;
+        if (C.mom_fused) {  // one G and B map pair per (descriptor, rows)
+          const std::pair<int32_t, int32_t> key(S.gbmap, S.m);
+          auto it = gb_index.find(key);
+          if (it == gb_index.end()) {
+            it = gb_index.emplace(key, (int32_t)P->gb_pairs.size()).first;
+            P->gb_pairs.push_back(key);
+          }
+          S.gbmap = it->second;
+        } else {
+          S.gbmap = -1;
+        }
         C.count++;
       }
     xoff = round_up(xoff + (int64_t)C.count * xrows * C.ld, 128);
@@ -384,7 +419,17 @@ int validate_and_expand(gbo_plan *P) {
   }
   // momentum tiles and NorMuon row blocks, in table order of subs
   int64_t tiles = 0, rbs = 0;
+  P->n_unfused = 0;
   for (DevSub &S : subs) {
+    if (S.mom_fused) {  // no momentum tiles: the chain kernel runs its momentum pass
+      S.tiles_c = 0;
+      S.ntiles = 0;
+      S.tile0 = tiles;
+      S.rb0 = rbs;
+      rbs += (S.m + kRowBlock - 1) / kRowBlock;
+      continue;
+    }
+    P->n_unfused++;
     // A matrix that is not transposed is one contiguous block of its weight
     // (views split rows only), and so is its X when ld == n: its momentum
     // tiles are flat runs of 4096 elements.  Tall matrices use 64 x 64 tiles
@@ -455,19 +500,26 @@ int validate_and_expand(gbo_plan *P) {
   }
   I.ns_flops = fl;
   I.n_gram_route = 0;
+  I.n_mom_fused = 0;
+  for (const DevSub &S : P->subs) I.n_mom_fused += S.mom_fused;
   {
     // the tile FLOPs of one pass (the fp32 kernel runs each as three TF32 products)
     double ex = 0;
-    for (const ShapeClass &C : P->classes) {
+    P->class_flops.assign(P->classes.size(), 0.0);
+    for (size_t k = 0; k < P->classes.size(); ++k) {
+      const ShapeClass &C = P->classes[k];
+      double per = 0;  // one matrix of the class
       if (C.route == kRouteGram) {
-        ex += C.count * (uses_chain(P, C) ? tc_gram_chain_flops(C.p, C.q, o.ns_steps, P->abc.data(),
-                                                                C.x_tall != 0, fuses_gram(P, C))
-                                          : tc_gram_route_flops(C.p, C.q, o.ns_steps, squares(P), C.x_tall != 0));
+        per = uses_chain(P, C) ? tc_gram_chain_flops(C.p, C.q, o.ns_steps, P->abc.data(), C.x_tall != 0,
+                                                     fuses_gram(P, C))
+                               : tc_gram_route_flops(C.p, C.q, o.ns_steps, squares(P), C.x_tall != 0);
         I.n_gram_route += C.count;
       } else {
         for (int it = 0; it < o.ns_steps; ++it)
-          ex += C.count * tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f, C.x_tall != 0);
+          per += tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f, C.x_tall != 0);
       }
+      P->class_flops[k] = per;
+      ex += C.count * per;
     }
     I.ns_flops_executed = ex;
   }
@@ -657,13 +709,15 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
 // Kernel launches of one step of the schedule (classes go 8 to a launch,
 // pairs and single CTAs separately).
 int64_t tc_step_launches(const TcStep &st) {
-  int64_t single = 0, pair = 0, chain[3] = {0, 0, 0};
+  int64_t single = 0, pair = 0, chain[kChainGeometries] = {};
   for (const GemmJob &J : st.jobs) {
     if (J.mode == kChain) ++chain[chain_geometry(J)];
     else (single_mode(J.cls->p) ? single : pair)++;
   }
   auto groups = [](int64_t n) { return (n + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch; };
-  return groups(single) + groups(pair) + groups(chain[0]) + groups(chain[1]) + groups(chain[2]);
+  int64_t n = groups(single) + groups(pair);
+  for (int g = 0; g < kChainGeometries; ++g) n += groups(chain[g]);
+  return n;
 }
 
 cudaEvent_t take_event(gbo_plan *P) {
@@ -742,6 +796,7 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   P->x_dtype = opts->precision == GBO_NS_F32 ? GBO_F32 : GBO_BF16;
   P->small_chain = g_small_chain.load() != 0;
   P->fused_gram = g_fused_gram.load() != 0;
+  P->fused_mom = g_fused_mom.load() != 0;
   const int rc = validate_and_expand(P);
   if (rc != GBO_OK) {
     delete P;
@@ -752,7 +807,8 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   for (const TcStep &st : build_schedule(P, nullptr)) gemm += tc_step_launches(st);
   P->info.launches_per_step =
       P->subs.empty() ? 0
-                      : 2 + gemm + (opts->normuon ? (opts->rms_target > 0.f ? 3 : (P->rows_streamed ? 2 : 1)) : 0);
+                      : (P->n_tiles > 0) + (P->n_unfused > 0) + gemm +
+                            (opts->normuon ? (opts->rms_target > 0.f ? 3 : (P->rows_streamed ? 2 : 1)) : 0);
   *out = P;
   return ok();
 }
@@ -761,6 +817,7 @@ void gbo_muon_plan_destroy(gbo_plan *P) {
   if (!P) return;
   if (P->d_subs) cudaFree(P->d_subs);
   if (P->d_wmaps) cudaFree(P->d_wmaps);
+  if (P->d_gbmaps) cudaFree(P->d_gbmaps);
   for (auto &iv : P->pending) {
     cudaEventDestroy(iv.a);
     cudaEventDestroy(iv.b);
@@ -776,6 +833,14 @@ uint64_t gbo_desc_hash(const gbo_plan *P) { return P ? P->hash : 0; }
 int gbo_muon_plan_info(const gbo_plan *P, gbo_plan_info *out) {
   if (!P || !out) return fail(GBO_ERR_INVALID_ARG, "NULL argument");
   *out = P->info;
+  return ok();
+}
+
+int gbo_muon_plan_desc_flops(const gbo_plan *P, double *flops, int32_t n) {
+  if (!P || !flops || n != (int32_t)P->descs.size())
+    return fail(GBO_ERR_INVALID_ARG, "plan, output or descriptor count (%d) does not match", n);
+  for (int32_t t = 0; t < n; ++t) flops[t] = 0.0;
+  for (const DevSub &S : P->subs) flops[S.desc] += P->class_flops[S.cls];
   return ok();
 }
 
@@ -841,6 +906,23 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
       const int me = build_weight_maps(P->descs.data(), (int32_t)P->descs.size(), &P->d_wmaps);
       if (me) return cuda_fail(me, "weight tensor maps");
     }
+    if (!P->gb_pairs.empty()) {  // the fused momentum pass's G and B maps, two per pair
+      const size_t map_bytes = 128;  // sizeof(CUtensorMap), 64-byte aligned
+      const size_t bytes = P->gb_pairs.size() * 2 * map_bytes;
+      std::unique_ptr<unsigned char, void (*)(void *)> maps(static_cast<unsigned char *>(std::aligned_alloc(64, bytes)),
+                                                           std::free);
+      if (!maps) return fail(GBO_ERR_CUDA, "host memory for the G and B tensor maps");
+      std::memset(maps.get(), 0, bytes);
+      for (size_t k = 0; k < P->gb_pairs.size(); ++k) {
+        const gbo_muon_desc &d = P->descs[P->gb_pairs[k].first];
+        if (!encode_gb_maps(maps.get() + k * 2 * map_bytes, d.g, d.mom, d.rows, d.cols, P->gb_pairs[k].second))
+          return fail(GBO_ERR_CUDA, "G and B tensor maps of desc %d refused", P->gb_pairs[k].first);
+      }
+      e = cudaMalloc(&P->d_gbmaps, bytes);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(G and B tensor maps)");
+      e = cudaMemcpy(P->d_gbmaps, maps.get(), bytes, cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(G and B tensor maps)");
+    }
     P->device = dev;
     P->sm_count = di.sm_count;
   } else if (P->device != dev) {
@@ -852,8 +934,23 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   float *partials = reinterpret_cast<float *>(ws + P->off_part);
   void *st = stream;
   cudaEvent_t last = nullptr;
-  auto mark = [&](int phase, int64_t n_launch) {
-    if (P->after_phase[phase]) cudaEventRecord(P->after_phase[phase], reinterpret_cast<cudaStream_t>(stream));
+  // the caller's event after the momentum pass (the gradients are no longer
+  // read) follows the chain launch that runs the fused matrices' momentum
+  // pass, if there is one
+  bool mom_event_due = P->after_phase[kPhaseMomentum] != nullptr;
+  auto mark = [&](int phase, int64_t n_launch, bool mom_done = true) {
+    if (phase == kPhaseMomentum) {
+      if (mom_event_due && mom_done) {
+        cudaEventRecord(P->after_phase[phase], reinterpret_cast<cudaStream_t>(stream));
+        mom_event_due = false;
+      }
+    } else if (P->after_phase[phase]) {
+      cudaEventRecord(P->after_phase[phase], reinterpret_cast<cudaStream_t>(stream));
+    }
+    if (mom_event_due && mom_done && phase != kPhaseMomentum) {
+      cudaEventRecord(P->after_phase[kPhaseMomentum], reinterpret_cast<cudaStream_t>(stream));
+      mom_event_due = false;
+    }
     if (!P->timing) return;
     cudaEvent_t b = take_event(P);
     cudaEventRecord(b, reinterpret_cast<cudaStream_t>(stream));
@@ -870,9 +967,11 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   int err = launch_momentum(P->d_subs, nsub, P->n_tiles, P->opts.mu, P->opts.nesterov, x[0], x0t, P->x_dtype,
                             partials, P->sm_count, st);
   if (err) return cuda_fail(err, "momentum kernel");
-  err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, st);
-  if (err) return cuda_fail(err, "pre-normalisation kernel");
-  mark(kPhaseMomentum, 2);
+  if (P->n_unfused > 0) {
+    err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, st);
+    if (err) return cuda_fail(err, "pre-normalisation kernel");
+  }
+  mark(kPhaseMomentum, (P->n_tiles > 0) + (P->n_unfused > 0), !P->any_mom_fused);
   PhaseArgs A{};
   A.subs = P->d_subs;
   A.wmaps = P->d_wmaps;
@@ -880,13 +979,21 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   A.dbg = dbg_update;
   A.status = dev_status;
   A.lr = lr;
+  A.gbmaps = P->d_gbmaps;
+  A.alpha_out = alpha;
+  A.mu = P->opts.mu;
+  A.nesterov = P->opts.nesterov;
+  bool fused_left = P->any_mom_fused;  // a fused momentum pass is still to be launched
   for (const TcStep &step : build_schedule(P, ws)) {
     int64_t nl = 0;
     err = P->x_dtype == GBO_BF16
               ? launch_ns_gemm_tc(step.jobs.data(), (int32_t)step.jobs.size(), A, P->sm_count, st, &nl)
               : launch_ns_gemm_tf32(step.jobs.data(), (int32_t)step.jobs.size(), A, P->sm_count, st, &nl);
     if (err) return cuda_fail(err, "Newton-Schulz kernel");
-    mark(step.phase, nl);
+    if (fused_left)
+      for (const GemmJob &J : step.jobs)
+        if (J.mode == kChain && J.cls->mom_fused) fused_left = false;
+    mark(step.phase, nl, !fused_left);
   }
   if (P->opts.normuon) {
     err = launch_normuon_rows(P->d_subs, nsub, P->n_row_blocks, x[0], x[1], P->x_dtype, P->opts.beta2,
@@ -925,6 +1032,8 @@ int gbo_normuon_rownorm(const float *O, int64_t rows, int64_t cols, float *row_v
 int32_t gbo_testing_set_small_chain(int32_t enable) { return g_small_chain.exchange(enable != 0 ? 1 : 0); }
 
 int32_t gbo_testing_set_fused_gram(int32_t enable) { return g_fused_gram.exchange(enable != 0 ? 1 : 0); }
+
+int32_t gbo_testing_set_fused_momentum(int32_t enable) { return g_fused_mom.exchange(enable != 0 ? 1 : 0); }
 
 int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream) {
   if (!dev_status || !aligned(dev_status, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_status is NULL or misaligned");

@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define GBO_ABI_VERSION 4
+#define GBO_ABI_VERSION 5
 
 /* ---- status codes (return values) ------------------------------------ */
 #define GBO_OK 0
@@ -339,17 +339,33 @@ typedef struct {
   double ns_flops_executed;/* FLOPs the kernels execute (same unless symmetric) */
   int64_t launches_per_step; /* kernels one gbo_muon_step launches              */
   int64_t n_gram_route;    /* matrices whose iterations take the Gram route     */
+  int64_t n_mom_fused;     /* matrices whose momentum pass runs inside the
+                              Newton-Schulz chain launch (wide, at most 128
+                              rows, bf16 G on 16-byte rows)                     */
 } gbo_plan_info;
 
 int gbo_muon_plan_info(const gbo_plan *plan, gbo_plan_info *out);
+
+/*
+ * Executed Newton-Schulz FLOPs per step of every descriptor of the plan (the
+ * sum over its matrices; 0 for a descriptor whose g is NULL), in table
+ * order: the cost a static partition of whole matrices over devices
+ * balances (Qwen3.8-Flash-Next optimizer notes, distributed Muon: the
+ * partitioner assigns complete matrices by estimated NS FLOPs; NorMuon
+ * paper, section 3.2: each parameter has one owner that orthogonalises
+ * it).  flops: host array of n doubles, n = the plan's descriptor count.
+ * Errors: INVALID_ARG.
+ */
+int gbo_muon_plan_desc_flops(const gbo_plan *plan, double *flops, int32_t n);
 
 /*
  * Phase timing.  When enabled, gbo_muon_step records CUDA events around its
  * phases on its stream.  gbo_muon_plan_phase_times synchronises on the last
  * recorded event, adds the elapsed milliseconds of every step since the last
  * reset into ms[phase] and the number of kernel launches into
- * launches[phase], then resets.  Phases: 0 momentum (+ the norm reduction),
- * 1 Newton-Schulz Gram products, 2 Newton-Schulz products back onto X
+ * launches[phase], then resets.  Phases: 0 momentum (+ the norm reduction;
+ * the momentum pass of n_mom_fused matrices runs in the chain launch, timed
+ * under phase 2), 1 Newton-Schulz Gram products, 2 Newton-Schulz products back onto X
  * except the one that writes the weights, 3 Gram squares (c != 0), 4 NorMuon
  * rows and weight write, 5 the last product with the weight write (no
  * NorMuon).  n_phases is the array length (<= GBO_N_PHASES).
@@ -359,8 +375,10 @@ int gbo_muon_plan_info(const gbo_plan *plan, gbo_plan_info *out);
 /*
  * Record `event` (a cudaEvent_t, created by the caller) on the step's stream
  * right after phase `phase` of every later gbo_muon_step, or stop doing so
- * when `event` is NULL.  Phase numbers as above; after phase 0 the momentum
- * buffers are updated and the gradients are no longer read, so work on
+ * when `event` is NULL.  Phase numbers as above; the phase-0 event is
+ * recorded once the momentum buffers are updated and the gradients are no
+ * longer read (after the chain launch that runs the momentum pass of the
+ * n_mom_fused matrices, when there are any), so work on
  * another stream that waits on the event (the AdamW path, the next
  * gradients) overlaps the Newton-Schulz GEMMs.  Errors: INVALID_ARG.
  */

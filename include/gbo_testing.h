@@ -43,6 +43,20 @@ int32_t gbo_testing_set_small_chain(int32_t enable);
  */
 int32_t gbo_testing_set_fused_gram(int32_t enable);
 
+/*
+ * Test and A/B switch for plans created after the call: the on-chip Gram of
+ * wide matrices of at most 128 rows with bf16 gradients on 16-byte rows
+ * also runs their momentum pass (enable != 0): the chain kernel streams G
+ * and B, writes B, and forms X_0 = bf16(D) and the pre-normalisation factor
+ * itself (OMN page, Muon path: momentum, Nesterov direction, max-abs
+ * rescale and Frobenius norm), so X_0 is not read back for the Gram; or
+ * their momentum pass runs in the momentum kernel and the chain kernel
+ * streams X_0 (enable == 0, the default: on a GB300 the momentum kernel's
+ * many warps stream faster than the chain kernel's eight momentum warps).
+ * Returns the previous setting.  Plans already created keep theirs.
+ */
+int32_t gbo_testing_set_fused_momentum(int32_t enable);
+
 #ifdef __cplusplus
 }
 #endif

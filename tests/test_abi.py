@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(L):
     assert "gbo_muon_step" in names and "gbo_adamw_step" in names
     for n in names:
         assert hasattr(L, n), n
-    assert B.gbo_abi_version() == 4
+    assert B.gbo_abi_version() == 5
     for i, S in enumerate(B._STRUCTS):
         assert B.gbo_struct_size(i) == ctypes.sizeof(S)
 
@@ -259,7 +259,7 @@ def test_small_chain_counts(L):
     quintic_chain = 10 * op128 + 3 * op256
     rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM)
     i = info(L, plan)
-    assert i.n_gram_route == 4 and i.launches_per_step == 2 + 2
+    assert i.n_gram_route == 4 and i.n_mom_fused == 0 and i.launches_per_step == 2 + 2
     assert i.ns_flops_executed == 4 * (gram_chip + cubic_chain + prod)
     L.gbo_muon_plan_destroy(plan)
     rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM, abc=(15 / 8, -5 / 4, 3 / 8))
@@ -267,6 +267,17 @@ def test_small_chain_counts(L):
     assert i.launches_per_step == 2 + 2
     assert i.ns_flops_executed == 4 * (gram_chip + op128 + quintic_chain + prod)
     L.gbo_muon_plan_destroy(plan)
+    # with the momentum pass in the chain launch too (bf16 G on 16-byte rows):
+    # no momentum or pre-normalisation launch
+    prev = L.gbo_testing_set_fused_momentum(1)
+    try:
+        rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM)
+        i = info(L, plan)
+        assert i.n_mom_fused == 4 and i.launches_per_step == 2
+        assert i.ns_flops_executed == 4 * (gram_chip + cubic_chain + prod)
+        L.gbo_muon_plan_destroy(plan)
+    finally:
+        L.gbo_testing_set_fused_momentum(prev)
     # with the Gram as a launch of its own (and the square of A_0 another)
     prev = L.gbo_testing_set_fused_gram(0)
     try:
@@ -343,3 +354,59 @@ def test_step_without_device_reports_error(L):
     _, plan = create(L, [desc(0, 8, 8)])
     assert L.gbo_muon_step(plan, 0.02, FAKE, 16, None, None, None) == -6
     L.gbo_muon_plan_destroy(plan)
+
+
+def test_fused_momentum_eligibility(L):
+    """Which matrices run their momentum pass inside the chain launch: wide
+    (rows <= cols) matrices of at most 128 rows on the on-chip Gram, with
+    bf16 gradients whose rows start on 16-byte boundaries; a class runs it
+    there only if every one of its matrices can.  Everything else keeps the
+    momentum kernel (and its pre-normalisation launch)."""
+    ok = lambda i: desc(i, 2 * 64, 512, (2, 64, 512))  # two 64 x 512 matrices
+    rc, plan = create(L, [ok(0)])
+    assert rc == 0 and info(L, plan).n_mom_fused == 0  # off by default
+    L.gbo_muon_plan_destroy(plan)
+    prev = L.gbo_testing_set_fused_momentum(1)
+    try:
+        _eligibility_cases(L, ok)
+    finally:
+        L.gbo_testing_set_fused_momentum(prev)
+
+
+def _eligibility_cases(L, ok):
+    rc, plan = create(L, [ok(0)])
+    i = info(L, plan)
+    assert rc == 0 and i.n_mom_fused == 2 and i.launches_per_step == 2
+    L.gbo_muon_plan_destroy(plan)
+    cases = {
+        "fp32 gradient": lambda: [dict_desc(ok(0), g_dtype=B.GBO_F32)],
+        "row not a multiple of 8": lambda: [desc(0, 64, 500)],
+        "gradient off 16 bytes": lambda: [dict_desc(ok(0), g_off=8)],
+        "tall": lambda: [desc(0, 512, 64)],
+        "more than 128 rows": lambda: [desc(0, 160, 1024)],
+    }
+    for why, make in cases.items():
+        rc, plan = create(L, make())
+        i = info(L, plan)
+        assert rc == 0 and i.n_mom_fused == 0, why
+        L.gbo_muon_plan_destroy(plan)
+    for kw in (dict(route=B.GBO_ROUTE_X), dict(precision=B.GBO_NS_F32)):
+        rc, plan = create(L, [ok(0)], **kw)
+        assert rc == 0 and info(L, plan).n_mom_fused == 0, kw
+        L.gbo_muon_plan_destroy(plan)
+    # one matrix of a class that cannot keeps the whole class on the momentum
+    # kernel; another class still fuses (plus the momentum kernel and its
+    # pre-normalisation launch for the rest)
+    mixed = [ok(0), dict_desc(desc(1, 64, 512), g_dtype=B.GBO_F32), desc(2, 96, 1024)]
+    rc, plan = create(L, mixed)
+    i = info(L, plan)
+    assert rc == 0 and i.n_matrices == 4 and i.n_mom_fused == 1
+    L.gbo_muon_plan_destroy(plan)
+
+
+def dict_desc(d, g_dtype=None, g_off=0):
+    if g_dtype is not None:
+        d.g_dtype = g_dtype
+    if g_off:
+        d.g = d.g + g_off
+    return d

@@ -219,13 +219,77 @@ def test_chain_gram_launch_groups(abc):
         sep, st1, plan1 = run_muon_gpu(entries, **kw)
     finally:
         B.gbo_testing_set_fused_gram(prev)
-    gpu, st2, plan2 = run_muon_gpu(entries, **kw)
-    assert st1 == 0 and st2 == 0
+    # the chain streaming X_0 for every class: classes 1-8 and 9-11
+    prev_mom = B.gbo_testing_set_fused_momentum(False)
+    try:
+        x0s, st2, plan2 = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_fused_momentum(prev_mom)
+    # the six wide classes on 16-byte rows stream G and B (one launch), the
+    # other five X_0 (another)
+    prev_mom = B.gbo_testing_set_fused_momentum(True)
+    try:
+        gpu, st3, plan3 = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_fused_momentum(prev_mom)
+    assert st1 == 0 and st2 == 0 and st3 == 0
     assert B.gbo_muon_plan_info(plan2)["launches_per_step"] == 2 + 2 + 2
-    for a, b in zip(sep, gpu):
+    assert B.gbo_muon_plan_info(plan3)["launches_per_step"] == 2 + 2 + 2
+    assert B.gbo_muon_plan_info(plan3)["n_mom_fused"] == 1 + 1 + 1 + 1 + 2 + 3
+    for a, b, c in zip(sep, x0s, gpu):
         assert rel_fro(f64(b["U"]), f64(a["U"])) <= 1e-2
+        assert rel_fro(f64(c["U"]), f64(a["U"])) <= 1e-2
     ora = run_muon_oracle(entries, lr=0.02, abc=abc, ns_steps=5)
+    check_muon(entries, x0s, ora, lr=0.02, precision="bf16")
     check_muon(entries, gpu, ora, lr=0.02, precision="bf16")
+
+
+# wide matrices of at most 128 rows with bf16 gradients on 16-byte rows: the
+# chain kernel runs their momentum pass (G and B streamed in 64-column
+# stages); rows 1 .. 128, K ragged against the stages (q = 8 .. 4104), split
+# views whose row blocks start mid-weight, plus classes that stay on the
+# momentum kernel (a tall one, a row of 300 elements) in the same step
+FUSED_MOM = [(1, 64, None, None), (3 * 7, 8, (3, 7, 8), None), (128, 4104, None, None), (96, 1000, None, None),
+             (2 * 100, 520, (2, 100, 520), (37, 63)), (64, 64, None, None), (5 * 24, 72, (5, 24, 72), None),
+             (300, 100, None, None), (40, 300, None, None)]
+
+
+@pytest.mark.parametrize("nesterov", [True, False])
+def test_fused_momentum_matches_momentum_kernel(nesterov):
+    """Two steps from a nonzero momentum with the momentum pass inside the
+    chain launch, against the same steps with it in the momentum kernel: the
+    momentum buffers bitwise equal (the same fp32 operations per element),
+    the updates equal to bf16 rounding (the pre-normalisation factor is
+    reduced in another fixed order), and both match the oracle."""
+    entries = random_entries(FUSED_MOM, seed=41, b_std=1e-3)
+    kw = dict(lr=0.02, precision="bf16", steps=2, nesterov=nesterov, route=B.GBO_ROUTE_GRAM)
+    prev = B.gbo_testing_set_fused_momentum(False)
+    try:
+        ref, st0, plan0 = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_fused_momentum(prev)
+    B.gbo_testing_set_fused_momentum(True)
+    try:
+        gpu, st1, plan1 = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_fused_momentum(prev)
+    assert st0 == 0 and st1 == 0
+    i0, i1 = B.gbo_muon_plan_info(plan0), B.gbo_muon_plan_info(plan1)
+    assert i0["n_mom_fused"] == 0 and i1["n_mom_fused"] == 1 + 3 + 1 + 1 + 4 + 1 + 5
+    for a, b in zip(ref, gpu):
+        assert torch.equal(a["B"], b["B"])
+        assert rel_fro(f64(b["U"]), f64(a["U"])) <= 1e-2
+        assert rel_fro(f64(b["W"]), f64(a["W"])) <= 1e-2
+    # one step of the fused path against the oracle (every acceptance check)
+    B.gbo_testing_set_fused_momentum(True)
+    try:
+        one, st2, plan2 = run_muon_gpu(entries, **dict(kw, steps=1))
+    finally:
+        B.gbo_testing_set_fused_momentum(prev)
+    assert B.gbo_muon_plan_info(plan2)["n_mom_fused"] == i1["n_mom_fused"]
+    assert st2 == 0
+    ora = run_muon_oracle(entries, lr=0.02, nesterov=nesterov)
+    check_muon(entries, one, ora, lr=0.02, precision="bf16")
 
 
 @pytest.mark.parametrize("ns_steps", [3, 5])
@@ -471,8 +535,11 @@ def test_standalone_rownorm():
 
 def test_after_momentum_event_and_side_stream():
     """An event recorded after the momentum phase lets another stream start
-    (here: a copy of the updated momentum); results match a plain step."""
-    entries = random_entries([(256, 160, None, None), (160, 256, None, None)], seed=31, b_std=1e-3)
+    (here: a copy of the updated momentum); results match a plain step.  The
+    third weight's momentum pass runs in the chain launch, after which the
+    event is recorded."""
+    entries = random_entries([(256, 160, None, None), (160, 256, None, None), (128, 512, None, None)], seed=31,
+                             b_std=1e-3)
     plain, _, _ = run_muon_gpu(entries, lr=0.02, precision="bf16")
     dev = []
     for e in entries:
@@ -480,7 +547,11 @@ def test_after_momentum_event_and_side_stream():
         for k in ("w", "g", "mom"):
             d[k] = d[k].cuda()
         dev.append(d)
-    plan = B.gbo_muon_plan_create(dev)
+    prev = B.gbo_testing_set_fused_momentum(True)
+    try:
+        plan = B.gbo_muon_plan_create(dev)
+    finally:
+        B.gbo_testing_set_fused_momentum(prev)
     ev = torch.cuda.Event()
     B.gbo_muon_plan_set_event(plan, 0, ev)
     ws = torch.empty(B.gbo_muon_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
@@ -488,9 +559,11 @@ def test_after_momentum_event_and_side_stream():
     B.gbo_muon_step(plan, 0.02, ws)
     side.wait_event(ev)
     with torch.cuda.stream(side):
-        mom_copy = dev[0]["mom"].clone()
+        mom_copy = [d["mom"].clone() for d in dev]
     torch.cuda.synchronize()
-    assert torch.equal(mom_copy, plain[0]["B"].cuda())
+    assert B.gbo_muon_plan_info(plan)["n_mom_fused"] == 1
+    for m, p in zip(mom_copy, plain):
+        assert torch.equal(m, p["B"].cuda())
     for d, p in zip(dev, plain):
         assert torch.equal(d["w"].cpu(), p["W"]) and torch.equal(d["mom"].cpu(), p["B"])
     B.gbo_muon_plan_set_event(plan, 0, None)
