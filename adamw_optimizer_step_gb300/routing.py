@@ -327,14 +327,25 @@ class HybridOptimizer:
     gradient tensors change) runs directly, then one step is captured in a
     CUDA graph, with the AdamW step count kept on the device, and later
     steps replay it.  The learning rates are fixed at capture.
+
+    ``process_group`` (data parallelism over more than one rank, gradients
+    already all-reduced): each Muon weight gets one owner rank, by LPT over
+    its executed Newton-Schulz FLOPs (:class:`.sharding.MuonShards`); a rank
+    steps only the Muon weights it owns, and an all-gather after the Muon
+    step hands every rank the owners' updated weights.  The AdamW path runs
+    on every rank, on identical inputs.  Not combined with ``graph``.
     """
 
     def __init__(self, model, *, muon_lr=0.01, adamw_lr=3e-4, weight_decay=0.0, auxiliary_decay=True, mu=0.95,
                  ns_steps=5, abc=(1.5, -0.5, 0.0), normuon=False, beta2_rows=0.95, eps_rows=1e-8,
                  rms_target=0.0, betas=(0.9, 0.95), eps=1e-8, max_norm=1.0, precision="bf16", route="auto",
-                 graph=False, layouts=STANDARD_LAYOUTS):
+                 graph=False, layouts=STANDARD_LAYOUTS, process_group=None):
         from . import _binding as B
         self.B = B
+        self.group = process_group
+        self.shards = None
+        if process_group is not None and graph:
+            raise ValueError("graph mode is not combined with a process group")
         self.routes = build_parameter_groups(model, weight_decay, auxiliary_decay, layouts)
         self.muon = [r for r in self.routes if r.algorithm == "muon"]
         self.adamw = [r for r in self.routes if r.algorithm == "adamw"]
@@ -370,12 +381,22 @@ class HybridOptimizer:
         self._graph_key = None  # the tensors it was captured with
         self._step_t = torch.zeros(1, dtype=torch.int32, device=dev)  # AdamW t on the device
 
-    def _muon_entries(self):
+    def _muon_entries(self, local=True):
+        """Plan entries of the Muon routes; ``local``: with the gradients of
+        weights another rank owns dropped."""
         out = []
         for r in self.muon:
             st = self.state[r.key]
             out.append(dict(w=r.part(r.param.data), g=r.part(r.param.grad), mom=st["mom"], row_v=st.get("row_v"),
                             view=r.view, split=r.split, wd=r.weight_decay))
+        if local and self.group is not None:
+            import torch.distributed as dist
+            world, rank = dist.get_world_size(self.group), dist.get_rank(self.group)
+            if world > 1:
+                from .sharding import MuonShards
+                if self.shards is None:
+                    self.shards = MuonShards(self._muon_entries(local=False), world, rank, **self.opts)
+                out = self.shards.local_entries(out)
         return out
 
     def _ensure_plan(self):
@@ -399,6 +420,8 @@ class HybridOptimizer:
         with ``dev_step`` the device one."""
         if self.muon:
             self.B.gbo_muon_step(self._plan, self.muon_lr, self._ws, dev_status=self.status)
+            if self.shards is not None:  # every rank takes the owners' updated weights
+                self.shards.gather([r.part(r.param.data) for r in self.muon], group=self.group)
         active = [r for r in self.adamw if r.param.grad is not None]
         if active:
             self.B.gbo_clip_norm([r.part(r.param.grad) for r in active], self.max_norm, self.total_norm,
