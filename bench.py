@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--separate-gram", action="store_true",
                     help="A/B: run the Gram of the on-chip chain's matrices (p <= 128) as a tile-kernel "
                          "launch of its own instead of inside the chain launch (workload 4)")
+    ap.add_argument("--fused-momentum", action="store_true",
+                    help="A/B: run the momentum pass of the chain's wide p <= 128 matrices inside the chain launch "
+                         "instead of in the momentum kernel (workload 4; measured slower)")
     ap.add_argument("--extra", default="2,4,5",
                     help="after the headline run, time these other workloads in the same process "
                          "(comma-separated indices, or 'none'); reported under extra_workloads")
@@ -282,9 +285,13 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     times show such a stall, and the default 40 steps bound its weight in
     the mean."""
     import torch
+    from adamw_optimizer_step_gb300 import hostmem
     g_flat, ag_flat = bufs[0]
-    h_g = torch.empty(g_flat.numel(), dtype=g_flat.dtype, pin_memory=True)
-    h_ag = torch.empty(ag_flat.numel(), dtype=ag_flat.dtype, pin_memory=True)
+    # page-locked host buffers on huge pages (hostmem: fewer and shorter
+    # copy stalls than the driver's small-page pinned memory)
+    h_g = hostmem.pinned_empty(g_flat.numel(), g_flat.dtype)
+    h_ag = hostmem.pinned_empty(ag_flat.numel(), ag_flat.dtype)
+    assert h_g.is_pinned() and h_ag.is_pinned()
     h_g.copy_(g_flat)
     h_ag.copy_(ag_flat)
     compute = torch.cuda.current_stream()
@@ -293,17 +300,23 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     copied_adam = [torch.cuda.Event(), torch.cuda.Event()]  # AdamW gradients in
     done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def upload(b, after=None):
+    def upload(b, after=None, timed=None):
         # the Muon gradients first: a step needs them at its start, its AdamW
         # gradients only after the Newton-Schulz GEMMs
         copy.wait_event(done[b])  # the step that last read buffer pair b has finished
         if after is not None:
             copy.wait_event(after)
+        if timed is not None:  # the copies' own duration on the copy stream
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(copy)
         with torch.cuda.stream(copy):
             bufs[b][0].copy_(h_g, non_blocking=True)
             copied[b].record(copy)
             bufs[b][1].copy_(h_ag, non_blocking=True)
         copied_adam[b].record(copy)
+        if timed is not None:
+            ev1.record(copy)
+            timed.append((ev0, ev1))
 
     # the step's result comes back through a pinned buffer (no pageable copy)
     h_total = torch.empty(total.shape, dtype=total.dtype, pin_memory=True)
@@ -320,21 +333,27 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     h2d = h_g.numel() * h_g.element_size() + h_ag.numel() * h_ag.element_size()
     upload(0)
     torch.cuda.synchronize()
-    t_up = time.perf_counter()
-    upload(0)
-    torch.cuda.synchronize()
-    up_gbs = h2d / (time.perf_counter() - t_up) / 1e9
-
-    def run(n_run, wall=None):
+    alone = []  # three uploads on their own (host wall time each)
+    for _ in range(3):
+        t_up = time.perf_counter()
         upload(0)
+        torch.cuda.synchronize()
+        alone.append(time.perf_counter() - t_up)
+    up_gbs = h2d / statistics.median(alone) / 1e9
+
+    def run(n_run, wall=None, timed=None, enqueue=None):
+        upload(0, timed=timed)
         t_prev = time.perf_counter()
         for n in range(n_run):
             b = n % 2
+            t_q = time.perf_counter()
             compute.wait_event(copied[b])
             step(buf=b, before_adamw=copied_adam[b])
             done[b].record(compute)
             if n + 1 < n_run:
-                upload(1 - b, after_momentum[b])
+                upload(1 - b, after_momentum[b], timed=timed)
+            if enqueue is not None:
+                enqueue.append((time.perf_counter() - t_q) * 1e3)
             _ = read_result()  # the step's result on the host
             if wall is not None:
                 t_now = time.perf_counter()
@@ -344,11 +363,19 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
 
     run(2)  # untimed: each buffer pair's plan runs once (its first step sets it up on the device)
     barrier(world)
-    wall = []
+    wall, timed, enqueue = [], [], []
     t0 = time.perf_counter()
-    run(n_steps, wall)
+    run(n_steps, wall, timed, enqueue)
     e2e_t = max_over_ranks(time.perf_counter() - t0, world)
-    return aggregate(n_steps, e2e_t, world), h2d, up_gbs, wall
+    up_ms = [a.elapsed_time(b) for a, b in timed]
+    diag = {"upload_alone_ms": [x * 1e3 for x in alone],
+            "upload_copy_ms": {"median": statistics.median(up_ms), "max": max(up_ms),
+                               "over_2x_median": sum(u > 2 * statistics.median(up_ms) for u in up_ms),
+                               "basis": "each upload's own duration on the copy stream (CUDA events after its "
+                                        "waits)"},
+            "enqueue_ms": {"median": statistics.median(enqueue), "max": max(enqueue),
+                           "basis": "host time to enqueue a step and the next upload"}}
+    return aggregate(n_steps, e2e_t, world), h2d, up_gbs, wall, diag
 
 
 # nominal GB300 figures (NVIDIA's datasheet: dense bf16 without sparsity,
@@ -484,6 +511,9 @@ def run_ours(args):
     if args.separate_gram:
         from adamw_optimizer_step_gb300 import _binding
         _binding.gbo_testing_set_fused_gram(False)
+    if args.fused_momentum:
+        from adamw_optimizer_step_gb300 import _binding
+        _binding.gbo_testing_set_fused_momentum(True)
     wl = wk.workload(args.workload)
     if args.layers:
         wl = wk.first_layers(wl, args.layers)
@@ -599,7 +629,7 @@ def run_ours(args):
         raise RuntimeError("device status %d during the timed steps" % int(status.item()))
 
     # end to end: gradients from pinned host memory, norm read back
-    e2e_value, h2d, up_gbs, e2e_wall = None, 0, None, []
+    e2e_value, h2d, up_gbs, e2e_wall, e2e_diag = None, 0, None, [], {}
     if args.e2e_steps > 0:
         g_flat2, ag_flat2 = torch.empty_like(g_flat), torch.empty_like(ag_flat)
         entries2, off = [], 0
@@ -614,8 +644,8 @@ def run_ours(args):
         plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon)
         bound.append((plan2, params2, [p[1] for p in params2]))
         gbo.gbo_muon_plan_set_event(plan2, 0, after_momentum[1])
-        e2e_value, h2d, up_gbs, e2e_wall = run_e2e(args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)],
-                                                   step, total, after_momentum)
+        e2e_value, h2d, up_gbs, e2e_wall, e2e_diag = run_e2e(
+            args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total, after_momentum)
 
     if rank != 0:
         return
@@ -669,6 +699,8 @@ def run_ours(args):
                                     else "bf16 operands, fp32 accumulate"),
                    "parallelism": "replicas" if world > 1 else "single",
                    "chain_gram": "separate launch" if args.separate_gram else "on chip (p <= 128)",
+                   "chain_momentum": ("in the chain launch (wide p <= 128, bf16 G)"
+                                      if args.fused_momentum and not args.separate_gram else "momentum kernel"),
                    "device": torch.cuda.get_device_name(),
                    "seed": "one seeded draw per tensor and role (workloads.seed: workload, tensor index, role)",
                    "l2": "working set ~20 GB per GPU, far above the 129 MB L2: no flush needed"},
@@ -697,6 +729,7 @@ def run_ours(args):
                                                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4,
                                                "overlap": "step n+1's gradient upload runs during step n "
                                                           "(two gradient buffers)",
+                                               "host_buffers": "page-locked, huge-page backed (hostmem)",
                                                "upload_GBps_alone": up_gbs,
                                                "upload_ms_alone": None if not up_gbs else h2d / up_gbs / 1e6,
                                                "steps": len(e2e_wall),
@@ -706,7 +739,8 @@ def run_ours(args):
                                                                w > 2 * statistics.median(e2e_wall)
                                                                for w in e2e_wall),
                                                            "basis": "host wall time per step, up to its norm read; "
-                                                                    "the first includes the first upload"}},
+                                                                    "the first includes the first upload"},
+                                               **e2e_diag},
         "gpu_launches": int(launches),
         "clocks": clk,
         "cpu_baseline": cpu,
