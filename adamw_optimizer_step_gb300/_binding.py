@@ -49,7 +49,8 @@ class MuonOpts(ctypes.Structure):
     _fields_ = [("abc", ctypes.POINTER(c_float)), ("mu", c_float), ("beta2", c_float),
                 ("eps", c_float), ("nesterov", c_int32), ("ns_steps", c_int32),
                 ("abc_per_step", c_int32), ("precision", c_int32), ("normuon", c_int32),
-                ("route", c_int32), ("rms_target", c_float)]
+                ("route", c_int32), ("rms_target", c_float), ("reserved", c_int32),
+                ("workspace_cap", c_int64)]
 
 
 class Tensor(ctypes.Structure):
@@ -225,10 +226,11 @@ def muon_desc_table(entries, allow_host=False):
 
 def gbo_muon_plan_create(entries, *, abc=(1.5, -0.5, 0.0), ns_steps=5, mu=0.95, nesterov=True,
                          precision=GBO_NS_BF16, normuon=False, beta2=0.95, eps=1e-8, route=GBO_ROUTE_AUTO,
-                         rms_target=0.0, _query_only=False):
+                         rms_target=0.0, workspace_cap=0, _query_only=False):
     """Validate a Muon table and build a plan (``abc``: one triple or one per step;
     ``route``: GBO_ROUTE_AUTO, GBO_ROUTE_X or GBO_ROUTE_GRAM; ``rms_target`` > 0
-    with NorMuon: each matrix's update is scaled to that RMS)."""
+    with NorMuon: each matrix's update is scaled to that RMS; ``workspace_cap``
+    > 0: the step runs the table in groups whose workspace fits the cap)."""
     L = lib()
     arr, pool, keep = muon_desc_table(entries, allow_host=_query_only)
     flat = []
@@ -238,7 +240,7 @@ def gbo_muon_plan_create(entries, *, abc=(1.5, -0.5, 0.0), ns_steps=5, mu=0.95, 
     cabc = (c_float * len(flat))(*flat)
     opts = MuonOpts(ctypes.cast(cabc, ctypes.POINTER(c_float)), mu, beta2, eps, int(bool(nesterov)),
                     int(ns_steps), int(per_step), int(precision), int(bool(normuon)), int(route),
-                    float(rms_target))
+                    float(rms_target), 0, int(workspace_cap))
     cpool = (c_int64 * max(1, len(pool)))(*pool)
     out = c_void_p()
     _check(L.gbo_muon_plan_create(arr, len(entries), cpool, len(pool), ctypes.byref(opts), ctypes.byref(out)))

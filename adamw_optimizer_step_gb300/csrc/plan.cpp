@@ -170,6 +170,11 @@ struct gbo_plan {
   std::vector<Interval> pending;
   std::vector<cudaEvent_t> event_pool;
   cudaEvent_t after_phase[8] = {};  // caller events recorded after a phase
+  // workspace cap: plans of consecutive descriptor groups, stepped in turn on
+  // one workspace (this plan keeps the whole table's layout for its info,
+  // hash and per-descriptor FLOPs, but runs nothing itself)
+  std::vector<gbo_plan *> kids;
+  int64_t dbg_base = 0;  // a group's first element in the whole table's dbg_update
 };
 
 namespace {
@@ -753,8 +758,12 @@ size_t gbo_struct_size(int32_t which) {
 
 uint64_t gbo_launch_count(void) { return g_launches.load(); }
 
-int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *split_pool,
-                         int32_t pool_len, const gbo_muon_opts *opts, gbo_plan **out) {
+}  // extern "C"
+
+namespace {
+
+int make_plan(const gbo_muon_desc *descs, int32_t n, const int64_t *split_pool, int32_t pool_len,
+              const gbo_muon_opts *opts, gbo_plan **out) {
   if (!out) return fail(GBO_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!opts) return fail(GBO_ERR_INVALID_ARG, "opts is NULL");
@@ -813,8 +822,94 @@ int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *s
   return ok();
 }
 
+// The plan of descriptors t0 .. t1 - 1 alone (no cap), or nullptr with the
+// error recorded.
+gbo_plan *group_plan(const gbo_muon_desc *descs, int32_t t0, int32_t t1, const int64_t *pool, int32_t pool_len,
+                     const gbo_muon_opts *opts) {
+  gbo_muon_opts o = *opts;
+  o.workspace_cap = 0;
+  gbo_plan *q = nullptr;
+  return make_plan(descs + t0, t1 - t0, pool, pool_len, &o, &q) == GBO_OK ? q : nullptr;
+}
+
+// Split the table into groups of consecutive descriptors, each the longest
+// run from its first descriptor whose plan's workspace fits the cap (found
+// by doubling, then bisection: a longer run never needs less workspace).
+int split_into_groups(gbo_plan *P, const gbo_muon_desc *descs, int32_t n, const int64_t *pool, int32_t pool_len,
+                      const gbo_muon_opts *opts) {
+  const int64_t cap = opts->workspace_cap;
+  auto fits = [&](int32_t t0, int32_t t1) {
+    gbo_plan *q = group_plan(descs, t0, t1, pool, pool_len, opts);
+    const bool f = q && (int64_t)q->ws_bytes <= cap;
+    gbo_muon_plan_destroy(q);
+    return f;
+  };
+  int64_t base = 0;
+  for (int32_t t0 = 0; t0 < n;) {
+    if (!fits(t0, t0 + 1)) {
+      gbo_plan *q = group_plan(descs, t0, t0 + 1, pool, pool_len, opts);
+      const size_t need = q ? q->ws_bytes : 0;
+      gbo_muon_plan_destroy(q);
+      return fail(GBO_ERR_WORKSPACE, "desc %d alone needs %zu bytes of workspace, above the cap of %lld", t0, need,
+                  (long long)cap);
+    }
+    int32_t good = t0 + 1, bad = -1;
+    while (good < n) {
+      const int32_t cand = std::min<int64_t>(n, t0 + 2 * (int64_t)(good - t0));
+      if (fits(t0, cand)) {
+        good = cand;
+      } else {
+        bad = cand;
+        break;
+      }
+    }
+    while (bad > good + 1) {
+      const int32_t mid = good + (bad - good) / 2;
+      if (fits(t0, mid)) good = mid;
+      else bad = mid;
+    }
+    gbo_plan *q = group_plan(descs, t0, good, pool, pool_len, opts);
+    if (!q) return GBO_ERR_INVALID_ARG;
+    q->dbg_base = base;
+    for (int32_t t = t0; t < good; ++t) base += descs[t].rows * descs[t].cols;
+    P->kids.push_back(q);
+    t0 = good;
+  }
+  size_t ws = 0;
+  int64_t launches = 0;
+  for (const gbo_plan *q : P->kids) {
+    ws = std::max(ws, q->ws_bytes);
+    launches += q->info.launches_per_step;
+  }
+  P->ws_bytes = ws;
+  P->info.launches_per_step = launches;
+  return GBO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gbo_muon_plan_create(const gbo_muon_desc *descs, int32_t n, const int64_t *split_pool,
+                         int32_t pool_len, const gbo_muon_opts *opts, gbo_plan **out) {
+  if (opts && opts->workspace_cap < 0) return fail(GBO_ERR_INVALID_ARG, "workspace_cap must be >= 0");
+  const int rc = make_plan(descs, n, split_pool, pool_len, opts, out);
+  if (rc != GBO_OK) return rc;
+  gbo_plan *P = *out;
+  if (opts->workspace_cap > 0 && (int64_t)P->ws_bytes > opts->workspace_cap) {
+    const int src = split_into_groups(P, descs, n, split_pool, pool_len, opts);
+    if (src != GBO_OK) {
+      gbo_muon_plan_destroy(P);
+      *out = nullptr;
+      return src;
+    }
+  }
+  return ok();
+}
+
 void gbo_muon_plan_destroy(gbo_plan *P) {
   if (!P) return;
+  for (gbo_plan *q : P->kids) gbo_muon_plan_destroy(q);
   if (P->d_subs) cudaFree(P->d_subs);
   if (P->d_wmaps) cudaFree(P->d_wmaps);
   if (P->d_gbmaps) cudaFree(P->d_gbmaps);
@@ -847,12 +942,15 @@ int gbo_muon_plan_desc_flops(const gbo_plan *P, double *flops, int32_t n) {
 int gbo_muon_plan_set_timing(gbo_plan *P, int32_t enable) {
   if (!P) return fail(GBO_ERR_INVALID_ARG, "plan is NULL");
   P->timing = enable != 0;
+  for (gbo_plan *q : P->kids) q->timing = P->timing;
   return ok();
 }
 
 int gbo_muon_plan_set_event(gbo_plan *P, int32_t phase, void *event) {
   if (!P || phase < 0 || phase >= GBO_N_PHASES) return fail(GBO_ERR_INVALID_ARG, "bad plan or phase");
-  P->after_phase[phase] = static_cast<cudaEvent_t>(event);
+  // in groups, the last group's occurrence of the phase is the step's last
+  gbo_plan *target = P->kids.empty() ? P : P->kids.back();
+  target->after_phase[phase] = static_cast<cudaEvent_t>(event);
   return ok();
 }
 
@@ -862,6 +960,19 @@ int gbo_muon_plan_phase_times(gbo_plan *P, float *ms, int64_t *launches, int32_t
   for (int i = 0; i < n_phases; ++i) {
     ms[i] = 0.f;
     launches[i] = 0;
+  }
+  if (!P->kids.empty()) {  // the sum over the groups
+    std::vector<float> km(n_phases);
+    std::vector<int64_t> kl(n_phases);
+    for (gbo_plan *q : P->kids) {
+      const int rc = gbo_muon_plan_phase_times(q, km.data(), kl.data(), n_phases);
+      if (rc != GBO_OK) return rc;
+      for (int i = 0; i < n_phases; ++i) {
+        ms[i] += km[i];
+        launches[i] += kl[i];
+      }
+    }
+    return ok();
   }
   if (!P->pending.empty()) {
     cudaError_t e = cudaEventSynchronize(P->pending.back().b);
@@ -886,6 +997,16 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
                   int32_t *dev_status, gbo_stream_t stream) {
   if (!P) return fail(GBO_ERR_INVALID_ARG, "plan is NULL");
   if (!std::isfinite(lr)) return fail(GBO_ERR_INVALID_ARG, "lr is not finite");
+  if (!P->kids.empty()) {  // the groups in turn, on the same workspace
+    if (!workspace || ws_bytes < P->ws_bytes)
+      return fail(GBO_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P->ws_bytes, ws_bytes);
+    for (gbo_plan *q : P->kids) {
+      const int rc = gbo_muon_step(q, lr, workspace, ws_bytes, dbg_update ? dbg_update + q->dbg_base : nullptr,
+                                   dev_status, stream);
+      if (rc != GBO_OK) return rc;
+    }
+    return ok();
+  }
   if (P->subs.empty()) return ok();
   if (!workspace || ws_bytes < P->ws_bytes)
     return fail(GBO_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P->ws_bytes, ws_bytes);

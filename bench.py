@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--fused-momentum", action="store_true",
                     help="A/B: run the momentum pass of the chain's wide p <= 128 matrices inside the chain launch "
                          "instead of in the momentum kernel (workload 4; measured slower)")
+    ap.add_argument("--workspace-cap-frac", type=float, default=0.0,
+                    help="cap the Muon workspace at this fraction of what the whole table needs (0: no cap); "
+                         "the step then runs in groups of weights on the smaller workspace")
     ap.add_argument("--extra", default="2,4,5",
                     help="after the headline run, time these other workloads in the same process "
                          "(comma-separated indices, or 'none'); reported under extra_workloads")
@@ -545,6 +548,10 @@ def run_ours(args):
     f32 = args.precision == "f32"
     prec = gbo.GBO_NS_F32 if f32 else gbo.GBO_NS_BF16
     plan = gbo.gbo_muon_plan_create(entries, precision=prec, normuon=wl.normuon)
+    ws_whole = gbo.gbo_muon_workspace_bytes(plan)
+    cap = int(ws_whole * args.workspace_cap_frac) if args.workspace_cap_frac > 0 else 0
+    if cap:
+        plan = gbo.gbo_muon_plan_create(entries, precision=prec, normuon=wl.normuon, workspace_cap=cap)
     info = gbo.gbo_muon_plan_info(plan)
     ws = torch.empty(gbo.gbo_muon_workspace_bytes(plan), dtype=torch.uint8, device=dev)
     cws = torch.empty(gbo.gbo_clip_norm_workspace_bytes(), dtype=torch.uint8, device=dev)
@@ -641,7 +648,7 @@ def run_ours(args):
         for p, g, m, v in params:
             params2.append((p, ag_flat2[off:off + g.numel()].view(g.shape), m, v))
             off += g.numel()
-        plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon)
+        plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon, workspace_cap=cap)
         bound.append((plan2, params2, [p[1] for p in params2]))
         gbo.gbo_muon_plan_set_event(plan2, 0, after_momentum[1])
         e2e_value, h2d, up_gbs, e2e_wall, e2e_diag = run_e2e(
@@ -699,6 +706,8 @@ def run_ours(args):
                                     else "bf16 operands, fp32 accumulate"),
                    "parallelism": "replicas" if world > 1 else "single",
                    "chain_gram": "separate launch" if args.separate_gram else "on chip (p <= 128)",
+                   "workspace_bytes": int(ws.numel()), "workspace_cap": cap or None,
+                   "workspace_whole_table_bytes": int(ws_whole),
                    "chain_momentum": ("in the chain launch (wide p <= 128, bf16 G)"
                                       if args.fused_momentum and not args.separate_gram else "momentum kernel"),
                    "device": torch.cuda.get_device_name(),

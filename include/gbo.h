@@ -127,7 +127,21 @@ typedef struct {
   int32_t normuon;       /* 1: NorMuon row normalisation; every desc needs row_v        */
   int32_t route;         /* GBO_ROUTE_AUTO (0) | GBO_ROUTE_X | GBO_ROUTE_GRAM          */
   float rms_target;      /* NorMuon only: > 0 scales each matrix's update to this RMS  */
+  int32_t reserved;      /* set to 0                                                    */
+  int64_t workspace_cap; /* 0: one schedule over every matrix; > 0: see below           */
 } gbo_muon_opts;
+
+/*
+ * Workspace cap.  The step's scratch (each matrix's Newton-Schulz iterates and
+ * polynomial matrices) grows with the model.  With workspace_cap > 0 the plan
+ * splits its descriptor table into groups of consecutive descriptors, each as
+ * large as fits the cap, and the step runs the groups one after another on the
+ * same workspace: gbo_muon_workspace_bytes is then at most the cap.  Every
+ * matrix is computed exactly as without the cap (its reductions and products
+ * never involve other matrices), so the results are bitwise the same; the cost
+ * is more, smaller launches.  gbo_muon_plan_create fails with
+ * GBO_ERR_WORKSPACE when a single descriptor needs more than the cap.
+ */
 
 /*
  * Route of the k iterations of one shape class (bf16 mode).  Both give the

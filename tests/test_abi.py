@@ -65,11 +65,11 @@ def desc(i, rows, cols, view=None, split_off=0, n_split=0, w_dtype=B.GBO_BF16, g
 
 
 def create(L, descs, pool=(), ns_steps=5, abc=(1.5, -0.5, 0.0), precision=B.GBO_NS_BF16, normuon=0,
-           route=B.GBO_ROUTE_AUTO, rms_target=0.0):
+           route=B.GBO_ROUTE_AUTO, rms_target=0.0, workspace_cap=0):
     arr = (B.MuonDesc * max(1, len(descs)))(*descs)
     cabc = (ctypes.c_float * len(abc))(*abc)
     opts = B.MuonOpts(ctypes.cast(cabc, ctypes.POINTER(ctypes.c_float)), 0.95, 0.95, 1e-8, 1, ns_steps,
-                      int(len(abc) > 3), precision, normuon, route, rms_target)
+                      int(len(abc) > 3), precision, normuon, route, rms_target, 0, workspace_cap)
     cpool = (ctypes.c_int64 * max(1, len(pool)))(*pool)
     out = ctypes.c_void_p()
     rc = L.gbo_muon_plan_create(arr, len(descs), cpool, len(pool), ctypes.byref(opts), ctypes.byref(out))
@@ -410,3 +410,42 @@ def dict_desc(d, g_dtype=None, g_off=0):
     if g_off:
         d.g = d.g + g_off
     return d
+
+
+def test_workspace_cap_groups(L):
+    """With a workspace cap the plan runs its table in groups of consecutive
+    descriptors: the workspace it asks for fits the cap, the layout hash,
+    matrix count and per-descriptor FLOPs are those of the whole table, the
+    step takes more launches, and a descriptor that alone exceeds the cap is
+    refused."""
+    descs = lambda: [desc(i, 512 * (1 + i % 3), 1024) for i in range(9)]
+    rc, whole = create(L, descs())
+    assert rc == 0
+    wi = info(L, whole)
+    full = L.gbo_muon_workspace_bytes(whole)
+    h = L.gbo_desc_hash(whole)
+    f_whole = (ctypes.c_double * 9)()
+    assert L.gbo_muon_plan_desc_flops(whole, f_whole, 9) == 0
+    for frac in (2, 3, 5):
+        cap = full // frac
+        rc, plan = create(L, descs(), workspace_cap=cap)
+        assert rc == 0, B.gbo_last_error()
+        i = info(L, plan)
+        ws = L.gbo_muon_workspace_bytes(plan)
+        assert 0 < ws <= cap
+        assert L.gbo_desc_hash(plan) == h and i.n_matrices == wi.n_matrices
+        assert i.launches_per_step > wi.launches_per_step
+        f = (ctypes.c_double * 9)()
+        assert L.gbo_muon_plan_desc_flops(plan, f, 9) == 0 and list(f) == list(f_whole)
+        L.gbo_muon_plan_destroy(plan)
+    # a cap the whole table fits: one schedule, as without a cap
+    rc, plan = create(L, descs(), workspace_cap=full)
+    assert rc == 0 and info(L, plan).launches_per_step == wi.launches_per_step
+    assert L.gbo_muon_workspace_bytes(plan) == full
+    L.gbo_muon_plan_destroy(plan)
+    # below what one descriptor needs: refused
+    rc, plan = create(L, descs(), workspace_cap=1024)
+    assert rc == -6 and not plan and "above the cap" in B.gbo_last_error()  # GBO_ERR_WORKSPACE
+    rc, plan = create(L, descs(), workspace_cap=-1)
+    assert rc == -1  # GBO_ERR_INVALID_ARG
+    L.gbo_muon_plan_destroy(whole)

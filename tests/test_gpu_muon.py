@@ -292,6 +292,32 @@ def test_fused_momentum_matches_momentum_kernel(nesterov):
     check_muon(entries, one, ora, lr=0.02, precision="bf16")
 
 
+@pytest.mark.parametrize("normuon", [False, True])
+def test_workspace_cap_bitwise(normuon):
+    """A workspace cap runs the table in groups of consecutive weights on one
+    smaller workspace: weights, momentum, row moments and the exported
+    update are bitwise those of the uncapped plan (every matrix is computed
+    the same way), and match the oracle."""
+    shapes = [(600, 130, None, None), (130, 600, None, None), (256, 256, None, None), (4 * 96, 1000, (4, 96, 1000), None),
+              (200, 40, (2, 100, 40), (30, 70)), (2 * 192, 1536, (2, 192, 1536), None), (128, 512, None, None)]
+    entries = random_entries(shapes, seed=43, normuon=normuon, b_std=1e-3)
+    kw = dict(lr=0.02, precision="bf16", steps=2, normuon=normuon, beta2=0.95, eps=1e-8)
+    ref, st0, plan0 = run_muon_gpu(entries, **kw)
+    full = B.gbo_muon_workspace_bytes(plan0)
+    gpu, st1, plan1 = run_muon_gpu(entries, workspace_cap=full // 2, **kw)
+    assert st0 == 0 and st1 == 0
+    assert 0 < B.gbo_muon_workspace_bytes(plan1) <= full // 2
+    assert B.gbo_muon_plan_info(plan1)["launches_per_step"] > B.gbo_muon_plan_info(plan0)["launches_per_step"]
+    for a, b in zip(ref, gpu):
+        assert torch.equal(a["W"], b["W"]) and torch.equal(a["B"], b["B"]) and torch.equal(a["U"], b["U"])
+        if normuon:
+            assert torch.equal(a["v"], b["v"])
+    one, st2, _ = run_muon_gpu(entries, workspace_cap=full // 2, **dict(kw, steps=1))
+    assert st2 == 0
+    ora = run_muon_oracle(entries, lr=0.02, normuon=normuon, beta2=0.95, eps=1e-8)
+    check_muon(entries, one, ora, lr=0.02, precision="bf16")
+
+
 @pytest.mark.parametrize("ns_steps", [3, 5])
 def test_normuon_gram_route(ns_steps):
     """NorMuon rows read the last iterate from the buffer each route leaves
