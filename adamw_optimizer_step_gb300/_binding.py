@@ -118,6 +118,7 @@ def lib():
         "gbo_muon_plan_info": (c_int32, [c_void_p, ctypes.POINTER(PlanInfo)]),
         "gbo_muon_plan_desc_flops": (c_int32, [c_void_p, ctypes.POINTER(ctypes.c_double), c_int32]),
         "gbo_muon_plan_set_timing": (c_int32, [c_void_p, c_int32]),
+        "gbo_muon_plan_set_stats": (c_int32, [c_void_p, c_void_p]),
         "gbo_muon_plan_set_event": (c_int32, [c_void_p, c_int32, c_void_p]),
         "gbo_muon_plan_phase_times": (c_int32, [c_void_p, ctypes.POINTER(c_float), ctypes.POINTER(c_int64),
                                                 c_int32]),
@@ -291,6 +292,20 @@ def gbo_muon_step(plan, lr, workspace, dbg_update=None, dev_status=None, stream=
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().gbo_muon_step(plan.handle, float(lr), ws, nbytes, _dev_ptr(dbg_update, "dbg_update"),
                                _dev_ptr(dev_status, "dev_status"), _stream(stream)))
+
+
+def gbo_muon_plan_set_stats(plan, stats):
+    """Per-matrix norms from later steps: ``stats`` is a float32 CUDA tensor of
+    2 * n_matrices values (||D||_F, ||U||_F per matrix, table order), or None
+    to stop."""
+    if stats is not None and (stats.dtype != torch.float32 or stats.numel() < 2 * plan_matrices(plan)):
+        raise ValueError("stats must be float32 with 2 values per matrix")
+    plan._stats = stats  # kept alive while the plan writes to it
+    _check(lib().gbo_muon_plan_set_stats(plan.handle, _dev_ptr(stats, "stats")))
+
+
+def plan_matrices(plan):
+    return gbo_muon_plan_info(plan)["n_matrices"]
 
 
 def gbo_muon_plan_set_timing(plan, enable=True):

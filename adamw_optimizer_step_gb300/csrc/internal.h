@@ -53,7 +53,7 @@ struct DevSub {
   int32_t mom_fused; // the momentum pass of this matrix runs inside the chain kernel (no momentum tiles)
   int32_t gbmap;     // with mom_fused: index of its pair of G and B TMA maps (2 * gbmap, 2 * gbmap + 1)
   int32_t desc;      // the descriptor (stored weight) this matrix belongs to
-  int32_t pad0;
+  int32_t mat_idx;   // its place among the plan's matrices in table order (per-matrix statistics)
 };
 
 // Matrices of one oriented shape (p, q), stored back to back in the
@@ -151,6 +151,7 @@ struct PhaseArgs {
   float *alpha_out;   // the same factors, written by the chain kernel for its matrices with mom_fused
   float mu;           // momentum coefficient and Nesterov flag, for the chain kernel's momentum pass
   int32_t nesterov;
+  float *stats;       // per-matrix norms (||D||_F, ||U||_F) at 2 * mat_idx, or nullptr
 };
 
 // Launchers (implemented in the .cu files).  Each returns a cudaError_t as
@@ -158,8 +159,14 @@ struct PhaseArgs {
 // x0t: X0's transposed twin (fp32 mode), or nullptr.
 int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float mu, int32_t nesterov,
                     void *x0, void *x0t, int32_t x_dtype, float *partials, int sm_count, void *stream);
+// stats: nullptr, or where each matrix's ||D||_F goes (2 * mat_idx)
 int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials,
-                            float *alpha, int32_t *status, void *stream);
+                            float *alpha, int32_t *status, float *stats, void *stream);
+// Per-matrix ||U||_F into stats[2 * mat_idx + 1]: from the last product's
+// per-(row, 128 columns) sums of U^2 (rowss), or with NorMuon from the rows
+// kernels' per-row-block sums of (1 / (sqrt(v) + eps))^2 ||X_i||^2 (rowpart).
+int launch_stats_finalize(const DevSub *subs, int32_t n_subs, int32_t normuon, float rms_target,
+                          const float *rowss, const float *rowpart, float *stats, void *stream);
 // NorMuon rows; with rms_target > 0 a statistics pass, the per-matrix
 // RMS-keeping scale and a write pass (rowf: n_row_blocks * kRowBlock floats,
 // rowpart: n_row_blocks, mscale: n_subs), else one fused pass.
@@ -167,10 +174,12 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
 // X_k (bf16 mode), or nullptr to take the statistics from X_k itself.
 // streamed: every matrix has bf16 X and bf16 weight rows on 16-byte
 // boundaries, so the write pass streams rows through shared memory.
+// stats: the single pass also leaves per-row-block sums of
+// (1 / (sqrt(v) + eps))^2 ||X_i||^2 in rowpart (the two-pass modes do anyway).
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
                         int32_t *status, float rms_target, float *rowf, float *rowpart, float *mscale,
-                        const float *rowss, bool streamed, int sm_count, void *stream);
+                        const float *rowss, bool streamed, bool stats, int sm_count, void *stream);
 int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
                                  int32_t w_dtype, float beta2, float eps, float scale, float lr,
                                  float wd, float *dbg, void *stream);

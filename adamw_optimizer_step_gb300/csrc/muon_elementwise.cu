@@ -189,9 +189,10 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
 // X0 = alpha * D.
 __global__ void __launch_bounds__(256)
 prenorm_finalize_kernel(const DevSub *__restrict__ subs, const float *__restrict__ partials,
-                        float *__restrict__ alpha, int32_t *status) {
+                        float *__restrict__ alpha, int32_t *status, float *__restrict__ stats) {
   __shared__ float red[32];
   const DevSub &S = subs[blockIdx.x];
+  if (S.mom_fused) return;  // the chain kernel forms this matrix's factor
   const int64_t nt = (int64_t)S.ntiles * kMomWarps;
   const float *P = partials + 2 * S.tile0 * kMomWarps;
   float M = 0.f;
@@ -215,6 +216,39 @@ prenorm_finalize_kernel(const DevSub *__restrict__ subs, const float *__restrict
       a = __int_as_float(0x7fc00000);
     }
     alpha[blockIdx.x] = a;
+    if (stats) stats[2 * S.mat_idx] = M > 0.f ? M * sqrtf(ss) : (isfinite(M) ? 0.f : M);  // ||D||_F
+  }
+}
+
+// ||U||_F of every matrix (one block each), from partial sums the step left
+// in the workspace, combined in a fixed order:
+//   without NorMuon  the last product's per-(stored row, 128 columns) sums of
+//                    U^2 (rowss, m x ss_ntn values from ss_off)
+//   NorMuon          the rows pass's per-row-block sums of
+//                    (1 / (sqrt(v) + eps))^2 ||X_i||^2 = ||O_hat||_F^2 of the
+//                    block (rowpart, from rb0); U = scale * O_hat, or with
+//                    the RMS-keeping scale rms sqrt(m n) O_hat / ||O_hat||_F
+__global__ void __launch_bounds__(256)
+stats_finalize_kernel(const DevSub *__restrict__ subs, int32_t normuon, float rms_target,
+                      const float *__restrict__ rowss, const float *__restrict__ rowpart,
+                      float *__restrict__ stats) {
+  __shared__ float red[32];
+  const DevSub &S = subs[blockIdx.x];
+  float t = 0.f;
+  if (normuon) {
+    const int nb = (S.m + kRowBlock - 1) / kRowBlock;
+    for (int k = threadIdx.x; k < nb; k += blockDim.x) t += rowpart[S.rb0 + k];
+  } else {
+    const int64_t n = (int64_t)S.m * S.ss_ntn;
+    for (int64_t k = threadIdx.x; k < n; k += blockDim.x) t += rowss[S.ss_off + k];
+  }
+  t = block_sum(t, red);
+  if (threadIdx.x == 0) {
+    float u;
+    if (!normuon) u = sqrtf(t);
+    else if (rms_target > 0.f) u = t > 0.f ? rms_target * sqrtf((float)S.m * (float)S.n) : (t == 0.f ? 0.f : t);
+    else u = S.scale * sqrtf(t);
+    stats[2 * S.mat_idx + 1] = u;
   }
 }
 
@@ -346,6 +380,9 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
           if constexpr (kMode == 1) {
             if (lane == 0) rf[r] = f;
             part = fmaf(f * f, ss, part);
+          } else {
+            const float g = 1.0f / (sqrtf(v) + eps);  // the row's factor without the scale
+            part = fmaf(g * g, ss, part);             // (its share of ||O_hat||_F^2, for the norms)
           }
         } else {
           f = mscale[si] * rf[r];
@@ -384,7 +421,7 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
           }
         }
       }
-      if constexpr (kMode == 1) {  // fixed-order block sum of the warps' shares
+      if (kMode == 1 || (kMode == 0 && rowpart)) {  // fixed-order block sum of the warps' shares
         if (lane == 0) red[warp] = part;
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -425,9 +462,12 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
           if constexpr (kMode == 1) {
             rf[threadIdx.x] = f;
             part = f * f * ss;
+          } else {
+            const float g = 1.0f / (sqrtf(v) + eps);
+            part = g * g * ss;
           }
         }
-        if constexpr (kMode == 1) {
+        if (kMode == 1 || rowpart) {
           if (threadIdx.x < kRowBlock) red[threadIdx.x] = part;
           __syncthreads();
           if (threadIdx.x == 0) {
@@ -721,10 +761,19 @@ int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float m
 }
 
 int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials, float *alpha,
-                            int32_t *status, void *stream) {
+                            int32_t *status, float *stats, void *stream) {
   if (n_subs == 0) return 0;
   prenorm_finalize_kernel<<<n_subs, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(subs, partials,
-                                                                                      alpha, status);
+                                                                                      alpha, status, stats);
+  count_launches(1);
+  return (int)cudaGetLastError();
+}
+
+int launch_stats_finalize(const DevSub *subs, int32_t n_subs, int32_t normuon, float rms_target,
+                          const float *rowss, const float *rowpart, float *stats, void *stream) {
+  if (n_subs == 0) return 0;
+  stats_finalize_kernel<<<n_subs, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(subs, normuon, rms_target,
+                                                                                    rowss, rowpart, stats);
   count_launches(1);
   return (int)cudaGetLastError();
 }
@@ -732,7 +781,7 @@ int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *par
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
                         const void *x1, int32_t x_dtype, float beta2, float eps, float lr, float *dbg,
                         int32_t *status, float rms_target, float *rowf, float *rowpart, float *mscale,
-                        const float *rowss, bool streamed, int sm_count, void *stream) {
+                        const float *rowss, bool streamed, bool stats, int sm_count, void *stream) {
   if (n_row_blocks == 0) return 0;
   const int64_t grid = std::min<int64_t>(n_row_blocks, (int64_t)sm_count * 8);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -752,11 +801,12 @@ int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks
     else if (x_dtype == GBO_BF16)
       normuon_rows_kernel<__nv_bfloat16, kMode><<<(unsigned)grid, 256, 0, st>>>(
           subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x0),
-          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf, rowpart, mscale, rowss);
+          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf,
+          (kMode == 0 && !stats) ? nullptr : rowpart, mscale, rowss);
     else
       normuon_rows_kernel<float, kMode><<<(unsigned)grid, 256, 0, st>>>(
           subs, n_subs, n_row_blocks, reinterpret_cast<const float *>(x0), reinterpret_cast<const float *>(x1),
-          beta2, eps, lr, dbg, status, rowf, rowpart, mscale, nullptr);
+          beta2, eps, lr, dbg, status, rowf, (kMode == 0 && !stats) ? nullptr : rowpart, mscale, nullptr);
     count_launches(1);
   };
   if (rms_target > 0.f) {

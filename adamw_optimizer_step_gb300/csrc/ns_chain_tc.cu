@@ -862,6 +862,7 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
             if (warp == kE0 && lane == 0) {
               A.alpha_out[si] = al;
               if (bad) flag_status(A.status, GBO_STATUS_NONFINITE);
+              if (A.stats) A.stats[2 * A.subs[si].mat_idx] = M > 0.f ? M * sqrtf(ss) : (isfinite(M) ? 0.f : M);
             }
           } else {
             al = A.alpha[si];

@@ -460,20 +460,22 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       const float s = J.first ? A.alpha[sub] : 1.0f;
       const uint32_t trow =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + part * E::kSpan);
+      // the NorMuon last product leaves each row's sum of squares of the bf16
+      // values it stores, one partial per 128 columns; with the per-matrix
+      // norms asked for, the weight-writing last product leaves those of the
+      // update direction
+      const bool stats = (J.mode == kProduct || J.mode == kFinal) && J.aux != nullptr;
+      float rss[E::kSpan / 128] = {};
       if (live) {  // warps whose rows or columns are all padding have nothing to write
         if (wtma) {
           if (!final_tile_bf16_tma<E::kWBufs>(A, S, s, i0, c0, cols, trow, lane, wmap, stage, wbar0, wpar, winfl,
-                                              E::kSpan)) {
+                                              E::kSpan, stats ? rss : nullptr)) {
             give_up();
             break;
           }
         } else if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
-          final_tile_bf16(A, S, s, i0, c0, rows, cols, trow, lane, E::kSpan);
+          final_tile_bf16(A, S, s, i0, c0, rows, cols, trow, lane, E::kSpan, stats ? rss : nullptr);
         } else {
-          // the NorMuon last product also leaves each row's sum of squares of
-          // the bf16 values it stores, one partial per 128 columns
-          const bool stats = J.mode == kProduct && J.aux != nullptr;
-          float rss[E::kSpan / 128] = {};
 #pragma unroll 1
           for (int ch = 0; ch < E::kSpan / 32; ++ch) {
             const int col0 = c0 + ch * 32;
@@ -483,21 +485,22 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
             epilogue_block<E::kSlots>(P, A, tc.c, tc.mat, S, s, i0, col0, v, stage, slot, lane);
             if (stats) {
               float r2 = 0.f;
+              const float f = J.mode == kFinal ? S.scale * s : s;
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
-                const float r = __bfloat162float(__float2bfloat16_rn(s * v[k]));
+                const float r = J.mode == kFinal ? f * v[k] : __bfloat162float(__float2bfloat16_rn(f * v[k]));
                 r2 = fmaf(r, r, r2);
               }
               rss[ch / 4] += r2;
             }
           }
-          if (stats && i0 + lane < rows) {
-            float *part_out = static_cast<float *>(const_cast<void *>(J.aux)) + S.ss_off +
-                              (int64_t)(i0 + lane) * S.ss_ntn + c0 / 128;
+        }
+        if (stats && i0 + lane < rows) {
+          float *part_out = static_cast<float *>(const_cast<void *>(J.aux)) + S.ss_off +
+                            (int64_t)(i0 + lane) * S.ss_ntn + c0 / 128;
 #pragma unroll
-            for (int h = 0; h < E::kSpan / 128; ++h)
-              if (c0 + 128 * h < cols) part_out[h] = rss[h];
-          }
+          for (int h = 0; h < E::kSpan / 128; ++h)
+            if (c0 + 128 * h < cols) part_out[h] = rss[h];
         }
       }
       tc_fence_before();

@@ -415,17 +415,37 @@ ns_gemm_tf32_kernel(const __grid_constant__ TcParams P, const __grid_constant__ 
       const float s = J.first ? A.alpha[sub] : 1.0f;
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (i0 < rows) {
+        // with the per-matrix norms asked for, the weight-writing last product
+        // leaves each row's sum of squares of the update direction, one
+        // partial per 128 columns
+        const bool stats = J.mode == kFinal && J.aux != nullptr;
+        float rss[BN / 128] = {};
+        const int c0 = tc.tn * BN;
         if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
-          final_tile_bf16(A, S, s, i0, tc.tn * BN, rows, cols, trow, lane);
+          final_tile_bf16(A, S, s, i0, c0, rows, cols, trow, lane, BN, stats ? rss : nullptr);
         } else {
 #pragma unroll 1
           for (int ch = 0; ch < BN / 32; ++ch) {
-            const int col0 = tc.tn * BN + ch * 32;
+            const int col0 = c0 + ch * 32;
             if (col0 >= cols) break;
             float v[32];
             tmem_ld32(trow + ch * 32, v);
             epilogue_block_f32(P, A, tc.c, tc.mat, S, s, i0, col0, v, slot, lane);
+            if (stats) {
+              float r2 = 0.f;
+              const float f = S.scale * s;
+#pragma unroll
+              for (int k = 0; k < 32; ++k) r2 = fmaf(f * v[k], f * v[k], r2);
+              rss[ch / 4] += r2;
+            }
           }
+        }
+        if (stats && i0 + lane < rows) {
+          float *part_out = static_cast<float *>(const_cast<void *>(J.aux)) + S.ss_off +
+                            (int64_t)(i0 + lane) * S.ss_ntn + c0 / 128;
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            if (c0 + 128 * h < cols) part_out[h] = rss[h];
         }
       }
       tc_fence_before();

@@ -175,6 +175,8 @@ struct gbo_plan {
   // hash and per-descriptor FLOPs, but runs nothing itself)
   std::vector<gbo_plan *> kids;
   int64_t dbg_base = 0;  // a group's first element in the whole table's dbg_update
+  int64_t mat_base = 0;  // a group's first matrix among the whole table's
+  float *stats = nullptr;  // per-matrix norms (gbo_muon_plan_set_stats), or nullptr
 };
 
 namespace {
@@ -328,6 +330,7 @@ int validate_and_expand(gbo_plan *P) {
         S.dbg_off = this_dbg;
         S.gbmap = t;  // the descriptor, until the fused momentum pass's maps are numbered
         S.desc = t;
+        S.mat_idx = (int32_t)subs.size();  // table order: the matrices are pushed in it
         const ClassKey key(S.p, S.q, S.m > S.n ? 1 : 0);
         auto it = class_of.find(key);
         if (it == class_of.end()) {
@@ -452,13 +455,15 @@ int validate_and_expand(gbo_plan *P) {
   P->n_row_blocks = rbs;
   // NorMuon row statistics from the last product (bf16 mode): per stored row
   // of each matrix, one partial per 128 columns of its output
+  // and, for the per-matrix norms, the last product's sums of squares of
+  // the update in any mode (one float per stored row and 128 columns)
   int64_t rowss = 0;
   P->rows_streamed = o.normuon && tc_path;
   for (DevSub &S : subs) {
     P->rows_streamed = P->rows_streamed && S.w_dtype == GBO_BF16 && S.w_vec && !S.transposed && S.n % 8 == 0;
     S.ss_ntn = (S.n + 127) / 128;
     S.ss_off = rowss;
-    if (o.normuon && tc_path) rowss += (int64_t)S.m * S.ss_ntn;
+    rowss += (int64_t)S.m * S.ss_ntn;
   }
   P->subs = std::move(subs);
   // workspace layout
@@ -485,7 +490,7 @@ int validate_and_expand(gbo_plan *P) {
   // pass's statistics pass
   const bool rowf = rms || P->rows_streamed;
   P->off_rowf = region(rowf ? (size_t)rbs * kRowBlock * sizeof(float) : 0);
-  P->off_rowpart = region(rowf ? (size_t)rbs * sizeof(float) : 0);
+  P->off_rowpart = region(o.normuon ? (size_t)rbs * sizeof(float) : 0);
   P->off_mscale = region(rms ? P->subs.size() * sizeof(float) : 0);
   P->off_rowss = region((size_t)rowss * sizeof(float));
   P->ws_bytes = off;
@@ -573,10 +578,14 @@ std::vector<TcStep> build_schedule(const gbo_plan *P, char *ws) {
   void *gQ[2] = {R(P->off_g[4]), R(P->off_g[5])};
   void *xt[2] = {R(P->off_xt[0]), R(P->off_xt[1])};
   const bool f32 = P->x_dtype == GBO_F32;
-  // the NorMuon last product's row-statistics partials (bf16 mode)
+  // the NorMuon last product's row-statistics partials (bf16 mode), and the
+  // weight-writing last product's sums of squares of the update when the
+  // per-matrix norms are asked for
   void *rowss = (normuon && !f32) ? R(P->off_rowss) : nullptr;
+  void *uss = P->stats ? R(P->off_rowss) : nullptr;
   auto last_product = [&](GemmJob J) {
     if (J.mode == kProduct) J.aux = rowss;
+    else if (J.mode == kFinal) J.aux = uss;
     return J;
   };
   auto job = [](const ShapeClass *C, int mode, int kind, int first, const float *abc, const void *opA,
@@ -844,7 +853,7 @@ int split_into_groups(gbo_plan *P, const gbo_muon_desc *descs, int32_t n, const 
     gbo_muon_plan_destroy(q);
     return f;
   };
-  int64_t base = 0;
+  int64_t base = 0, mats = 0;
   for (int32_t t0 = 0; t0 < n;) {
     if (!fits(t0, t0 + 1)) {
       gbo_plan *q = group_plan(descs, t0, t0 + 1, pool, pool_len, opts);
@@ -871,6 +880,8 @@ int split_into_groups(gbo_plan *P, const gbo_muon_desc *descs, int32_t n, const 
     gbo_plan *q = group_plan(descs, t0, good, pool, pool_len, opts);
     if (!q) return GBO_ERR_INVALID_ARG;
     q->dbg_base = base;
+    q->mat_base = mats;
+    mats += (int64_t)q->subs.size();
     for (int32_t t = t0; t < good; ++t) base += descs[t].rows * descs[t].cols;
     P->kids.push_back(q);
     t0 = good;
@@ -936,6 +947,14 @@ int gbo_muon_plan_desc_flops(const gbo_plan *P, double *flops, int32_t n) {
     return fail(GBO_ERR_INVALID_ARG, "plan, output or descriptor count (%d) does not match", n);
   for (int32_t t = 0; t < n; ++t) flops[t] = 0.0;
   for (const DevSub &S : P->subs) flops[S.desc] += P->class_flops[S.cls];
+  return ok();
+}
+
+int gbo_muon_plan_set_stats(gbo_plan *P, float *dev_stats) {
+  if (!P) return fail(GBO_ERR_INVALID_ARG, "plan is NULL");
+  if (!aligned(dev_stats, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_stats misaligned");
+  P->stats = dev_stats;
+  for (gbo_plan *q : P->kids) q->stats = dev_stats ? dev_stats + 2 * q->mat_base : nullptr;
   return ok();
 }
 
@@ -1089,7 +1108,7 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
                             partials, P->sm_count, st);
   if (err) return cuda_fail(err, "momentum kernel");
   if (P->n_unfused > 0) {
-    err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, st);
+    err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, P->stats, st);
     if (err) return cuda_fail(err, "pre-normalisation kernel");
   }
   mark(kPhaseMomentum, (P->n_tiles > 0) + (P->n_unfused > 0), !P->any_mom_fused);
@@ -1104,6 +1123,7 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   A.alpha_out = alpha;
   A.mu = P->opts.mu;
   A.nesterov = P->opts.nesterov;
+  A.stats = P->stats;
   bool fused_left = P->any_mom_fused;  // a fused momentum pass is still to be launched
   for (const TcStep &step : build_schedule(P, ws)) {
     int64_t nl = 0;
@@ -1123,9 +1143,15 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
                               reinterpret_cast<float *>(ws + P->off_rowpart),
                               reinterpret_cast<float *>(ws + P->off_mscale),
                               P->x_dtype == GBO_BF16 ? reinterpret_cast<const float *>(ws + P->off_rowss) : nullptr,
-                              P->rows_streamed, P->sm_count, st);
+                              P->rows_streamed, P->stats != nullptr, P->sm_count, st);
     if (err) return cuda_fail(err, "NorMuon rows kernel");
     mark(kPhaseRows, P->opts.rms_target > 0.f ? 3 : 1);
+  }
+  if (P->stats) {  // ||U||_F of every matrix, from the partial sums the step left
+    err = launch_stats_finalize(P->d_subs, nsub, P->opts.normuon, P->opts.rms_target,
+                                reinterpret_cast<const float *>(ws + P->off_rowss),
+                                reinterpret_cast<const float *>(ws + P->off_rowpart), P->stats, st);
+    if (err) return cuda_fail(err, "statistics kernel");
   }
   if (P->timing && last) P->event_pool.push_back(last);
   return ok();

@@ -484,8 +484,11 @@ __device__ __forceinline__ void wseg_unpack(const WSeg &r, float (&o)[32]) {
 // orientation (rows x cols of the matrix); lane r owns stored row
 // r0 + i0 + r.  The weights of chunk ch + 1 are loaded before chunk ch is
 // computed, so a load of each lane's row segment is always in flight.
+// rss (nullable): per 128 columns of the span, this lane's sum of squares of
+// the update direction, added to.
 __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub &S, float s, int i0, int tile_col0,
-                                                int rows, int cols, uint32_t trow, int lane, int span = BN) {
+                                                int rows, int cols, uint32_t trow, int lane, int span = BN,
+                                                float *rss = nullptr) {
   const int nch = min(span / 32, (cols - tile_col0 + 31) / 32);  // chunks holding columns < cols
   const float lr = A.lr * S.lr_mult, su = S.scale * s;
   __nv_bfloat16 *W = reinterpret_cast<__nv_bfloat16 *>(S.w);
@@ -514,6 +517,12 @@ __device__ __forceinline__ void final_tile_bf16(const PhaseArgs &A, const DevSub
       for (int k = 0; k < 32; ++k) {
         u[k] *= su;
         w[k] = w[k] - lr * (S.wd * w[k] + u[k]);
+      }
+      if (rss) {
+        float a = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) a = fmaf(u[k], u[k], a);  // columns past the matrix hold zeros
+        rss[ch >> 2] += a;
       }
       store_row32(W + wrow + col0, w, S.w_vec && mask == 0xffffffffu, mask);
       if (A.dbg) {
@@ -587,7 +596,7 @@ template <int kWBufs>
 __device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const DevSub &S, float s, int i0,
                                                     int tile_col0, int cols, uint32_t trow, int lane,
                                                     const CUtensorMap *wmap, uint32_t stage, uint32_t wbar0,
-                                                    uint32_t &wpar, uint32_t &winfl, int span) {
+                                                    uint32_t &wpar, uint32_t &winfl, int span, float *rss = nullptr) {
   constexpr int kWAhead = kWBufs - 1;
   const int nch = weight_chunks(tile_col0, cols, span);
   const float lr = A.lr * S.lr_mult, su = S.scale * s;
@@ -604,6 +613,12 @@ __device__ __forceinline__ bool final_tile_bf16_tma(const PhaseArgs &A, const De
     const int col0 = tile_col0 + ch * 32;
     float u[32];
     tmem_ld32(trow + ch * 32, u);
+    if (rss) {  // the update direction is su * u; columns past the matrix hold zeros
+      float a = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) a = fmaf(u[k], u[k], a);
+      rss[ch >> 2] += su * su * a;
+    }
     if (!mbar_wait(wbar0 + 8 * b, (wpar >> b) & 1u)) return false;
     wpar ^= 1u << b;
     winfl &= ~(1u << b);

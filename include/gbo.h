@@ -387,6 +387,23 @@ int gbo_muon_plan_desc_flops(const gbo_plan *plan, double *flops, int32_t n);
 #define GBO_N_PHASES 6
 
 /*
+ * Per-matrix norms, for monitoring a run (the OMN page's matched comparison
+ * tracks gradient and update norms).  After the call, every later
+ * gbo_muon_step writes two floats per matrix of the plan's active weights,
+ * in table order (a weight's matrices in view order): stats[2 j] = ||D_j||_F,
+ * the Frobenius norm of the momentum direction the matrix is orthogonalised
+ * from (before the pre-normalisation), and stats[2 j + 1] = ||U_j||_F, the
+ * norm of the update direction the weight moves along (scale * O, row-
+ * normalised with NorMuon; the weight moves by lr * lr_mult * U).  The
+ * sums are taken in a fixed order from the reductions the step already
+ * runs: the pre-normalisation's, and per-row partial sums of squares the
+ * last product (or the NorMuon rows pass) leaves in the workspace; a
+ * non-finite norm is written as such.  dev_stats: device fp32, 2 *
+ * gbo_plan_info.n_matrices values; NULL stops.  Errors: INVALID_ARG.
+ */
+int gbo_muon_plan_set_stats(gbo_plan *plan, float *dev_stats);
+
+/*
  * Record `event` (a cudaEvent_t, created by the caller) on the step's stream
  * right after phase `phase` of every later gbo_muon_step, or stop doing so
  * when `event` is NULL.  Phase numbers as above; the phase-0 event is
