@@ -74,6 +74,8 @@ __device__ __forceinline__ float4 load_g4(const void *g, int32_t dtype, int64_t 
 
 __global__ void __launch_bounds__(kThreads)
 clip_partial_kernel(const __grid_constant__ ClipTable T, float *__restrict__ partials) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   __shared__ float red[32];
   Kahan acc;
   const int64_t n_chunks = T.chunk0[T.n];
@@ -107,6 +109,8 @@ clip_partial_kernel(const __grid_constant__ ClipTable T, float *__restrict__ par
 __global__ void __launch_bounds__(kThreads)
 clip_finalize_kernel(const float *__restrict__ partials, int n_partials, float max_norm,
                      float *total_out, float *coef_out, int32_t *status) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   __shared__ float red[32];
   Kahan acc;
   for (int i = threadIdx.x; i < n_partials; i += kThreads) acc.add(partials[i]);
@@ -140,6 +144,8 @@ __device__ __forceinline__ void adam_elem(float &p, float g, float &m, float &v,
 __global__ void __launch_bounds__(kThreads, GBO_ADAM_MIN_BLOCKS)
 adamw_kernel(const __grid_constant__ AdamTable T, const __grid_constant__ AdamScalars s0,
              const float *__restrict__ coef_ptr, const int32_t *__restrict__ dev_step) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   const float coef = coef_ptr ? __ldg(coef_ptr) : 1.0f;
   // the bias corrections, from a device step count when one is given
   // (computed as on the host, in double, once per block)
@@ -229,16 +235,17 @@ int launch_clip_norm(const gbo_tensor *grads, int32_t n, float max_norm, float *
       T.chunk0[k + 1] = T.chunk0[k] + (t.numel + kChunk - 1) / kChunk;
     }
     const int grid = per_launch;
-    clip_partial_kernel<<<grid, kThreads, 0, st>>>(T, partials + used);
+    const cudaError_t err = launch_kernel(clip_partial_kernel, dim3(grid), dim3(kThreads), 0, st, 1, T, partials + used);
     count_launches(1);
     used += grid;
-    const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return (int)err;
   }
   (void)sm_count;
-  clip_finalize_kernel<<<1, kThreads, 0, st>>>(partials, used, max_norm, total, coef, status);
+  const cudaError_t err =
+      launch_kernel(clip_finalize_kernel, dim3(1), dim3(kThreads), 0, st, 1, (const float *)partials, used, max_norm,
+                    total, coef, status);
   count_launches(1);
-  return (int)cudaGetLastError();
+  return (int)err;
 }
 
 int launch_adamw(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *opts,
@@ -276,9 +283,8 @@ int launch_adamw(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *o
     const int64_t chunks = T.chunk0[T.n];
     if (chunks == 0) continue;
     const unsigned grid = (unsigned)std::min<int64_t>(chunks, (int64_t)sm_count * 8);
-    adamw_kernel<<<grid, kThreads, 0, st>>>(T, s, coef, opts->dev_step);
+    const cudaError_t err = launch_kernel(adamw_kernel, dim3(grid), dim3(kThreads), 0, st, 1, T, s, coef, opts->dev_step);
     count_launches(1);
-    const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return (int)err;
   }
   return 0;

@@ -6,9 +6,50 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "internal.h"
 
 namespace gbo {
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with cudaLaunchAttributeProgrammaticStreamSerialization (launch_kernel
+// below), so it may be scheduled while the kernel before it on the stream
+// is still finishing: each kernel calls pdl_launch() as it starts, letting
+// the next one be scheduled as SMs free up, and pdl_wait() after its
+// prologue (barrier set-up, TMEM allocation) and before its first access to
+// global memory, which returns once the previous kernel has completed and
+// its writes are visible.  A kernel that follows a launch from elsewhere has
+// no such dependency, and pdl_wait() returns at once.
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel` with programmatic stream serialization (and, with
+// cluster > 1, clusters of that many CTAs along x).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 int cluster, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ float ld_elem(const void *base, int32_t dtype, int64_t idx) {
   if (dtype == GBO_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[idx]);

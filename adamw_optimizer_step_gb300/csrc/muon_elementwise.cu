@@ -39,6 +39,8 @@ template <typename XT>
 __global__ void __launch_bounds__(kMomThreads, GBO_MOM_MIN_BLOCKS)
 momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles, float mu,
                 int32_t nesterov, XT *__restrict__ x0, XT *__restrict__ x0t, float *__restrict__ partials) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   __shared__ float tile[kMomTile][kMomTile + 1];
   const int cg = threadIdx.x & 7;
   const int rr = threadIdx.x >> 3;
@@ -190,6 +192,8 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
 __global__ void __launch_bounds__(256)
 prenorm_finalize_kernel(const DevSub *__restrict__ subs, const float *__restrict__ partials,
                         float *__restrict__ alpha, int32_t *status, float *__restrict__ stats) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   __shared__ float red[32];
   const DevSub &S = subs[blockIdx.x];
   if (S.mom_fused) return;  // the chain kernel forms this matrix's factor
@@ -232,6 +236,8 @@ __global__ void __launch_bounds__(256)
 stats_finalize_kernel(const DevSub *__restrict__ subs, int32_t normuon, float rms_target,
                       const float *__restrict__ rowss, const float *__restrict__ rowpart,
                       float *__restrict__ stats) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   __shared__ float red[32];
   const DevSub &S = subs[blockIdx.x];
   float t = 0.f;
@@ -328,6 +334,8 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
                     float *__restrict__ dbg, int32_t *status, float *__restrict__ rowf,
                     float *__restrict__ rowpart, const float *__restrict__ mscale,
                     const float *__restrict__ rowss) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   __shared__ float tileT[32][kRowBlock + 1];
   __shared__ float colsum[32][kRowBlock + 1];
   __shared__ float rfac[kRowBlock];
@@ -568,6 +576,8 @@ normuon_write_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_
                      const __nv_bfloat16 *__restrict__ xbuf0, const __nv_bfloat16 *__restrict__ xbuf1, float beta2,
                      float eps, float lr, float *__restrict__ dbg, int32_t *status, const float *__restrict__ rowf,
                      const float *__restrict__ mscale) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[kWWarps * kWStages];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
@@ -679,6 +689,8 @@ normuon_write_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_
 __global__ void __launch_bounds__(256)
 normuon_scale_kernel(const DevSub *__restrict__ subs, const float *__restrict__ rowpart, float rho,
                      float *__restrict__ mscale, int32_t *status) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   __shared__ float red[32];
   const DevSub &S = subs[blockIdx.x];
   const int nb = (S.m + kRowBlock - 1) / kRowBlock;
@@ -701,6 +713,8 @@ __global__ void __launch_bounds__(256)
 rownorm_plain_kernel(const float *__restrict__ O, int64_t rows, int64_t cols, float *__restrict__ row_v,
                      void *w, int32_t w_dtype, float beta2, float eps, float scale, float lr,
                      float wd, float *__restrict__ dbg) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
   __shared__ float rinv[kRowBlock];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int64_t b = blockIdx.x; b * kRowBlock < rows; b += gridDim.x) {
@@ -748,34 +762,36 @@ int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float m
   }
   const int64_t grid = std::min<int64_t>(n_tiles, (int64_t)sm_count * resident[which]);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (x_dtype == GBO_BF16)
-    momentum_kernel<__nv_bfloat16><<<(unsigned)grid, kMomThreads, 0, st>>>(
-        subs, n_subs, n_tiles, mu, nesterov, reinterpret_cast<__nv_bfloat16 *>(x0),
-        reinterpret_cast<__nv_bfloat16 *>(x0t), partials);
-  else
-    momentum_kernel<float><<<(unsigned)grid, kMomThreads, 0, st>>>(
-        subs, n_subs, n_tiles, mu, nesterov, reinterpret_cast<float *>(x0), reinterpret_cast<float *>(x0t),
-        partials);
+  const cudaError_t err =
+      x_dtype == GBO_BF16
+          ? launch_kernel(momentum_kernel<__nv_bfloat16>, dim3((unsigned)grid), dim3(kMomThreads), 0, st, 1, subs,
+                          n_subs, n_tiles, mu, nesterov, reinterpret_cast<__nv_bfloat16 *>(x0),
+                          reinterpret_cast<__nv_bfloat16 *>(x0t), partials)
+          : launch_kernel(momentum_kernel<float>, dim3((unsigned)grid), dim3(kMomThreads), 0, st, 1, subs, n_subs,
+                          n_tiles, mu, nesterov, reinterpret_cast<float *>(x0), reinterpret_cast<float *>(x0t),
+                          partials);
   count_launches(1);
-  return (int)cudaGetLastError();
+  return (int)err;
 }
 
 int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials, float *alpha,
                             int32_t *status, float *stats, void *stream) {
   if (n_subs == 0) return 0;
-  prenorm_finalize_kernel<<<n_subs, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(subs, partials,
-                                                                                      alpha, status, stats);
+  const cudaError_t err = launch_kernel(prenorm_finalize_kernel, dim3(n_subs), dim3(256), 0,
+                                        reinterpret_cast<cudaStream_t>(stream), 1, subs, partials, alpha, status,
+                                        stats);
   count_launches(1);
-  return (int)cudaGetLastError();
+  return (int)err;
 }
 
 int launch_stats_finalize(const DevSub *subs, int32_t n_subs, int32_t normuon, float rms_target,
                           const float *rowss, const float *rowpart, float *stats, void *stream) {
   if (n_subs == 0) return 0;
-  stats_finalize_kernel<<<n_subs, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(subs, normuon, rms_target,
-                                                                                    rowss, rowpart, stats);
+  const cudaError_t err = launch_kernel(stats_finalize_kernel, dim3(n_subs), dim3(256), 0,
+                                        reinterpret_cast<cudaStream_t>(stream), 1, subs, normuon, rms_target, rowss,
+                                        rowpart, stats);
   count_launches(1);
-  return (int)cudaGetLastError();
+  return (int)err;
 }
 
 int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks, const void *x0,
@@ -792,26 +808,32 @@ int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks
     return e;
   }();
   if (streamed && attr_err != cudaSuccess) return (int)attr_err;
+  cudaError_t err = cudaSuccess;
   auto rows = [&](auto mode) {
     constexpr int kMode = decltype(mode)::value;
+    if (err != cudaSuccess) return;
     if (streamed && kMode != 1)
-      normuon_write_kernel<kMode><<<(unsigned)sm_count, kWWarps * 32, kWSmem, st>>>(
-          subs, n_subs, n_row_blocks * kRowBlock, reinterpret_cast<const __nv_bfloat16 *>(x0),
-          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf, mscale);
+      err = launch_kernel(normuon_write_kernel<kMode>, dim3((unsigned)sm_count), dim3(kWWarps * 32), kWSmem, st, 1,
+                          subs, n_subs, n_row_blocks * kRowBlock, reinterpret_cast<const __nv_bfloat16 *>(x0),
+                          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf,
+                          (const float *)mscale);
     else if (x_dtype == GBO_BF16)
-      normuon_rows_kernel<__nv_bfloat16, kMode><<<(unsigned)grid, 256, 0, st>>>(
-          subs, n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x0),
-          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf,
-          (kMode == 0 && !stats) ? nullptr : rowpart, mscale, rowss);
+      err = launch_kernel(normuon_rows_kernel<__nv_bfloat16, kMode>, dim3((unsigned)grid), dim3(256), 0, st, 1, subs,
+                          n_subs, n_row_blocks, reinterpret_cast<const __nv_bfloat16 *>(x0),
+                          reinterpret_cast<const __nv_bfloat16 *>(x1), beta2, eps, lr, dbg, status, rowf,
+                          (kMode == 0 && !stats) ? nullptr : rowpart, (const float *)mscale, rowss);
     else
-      normuon_rows_kernel<float, kMode><<<(unsigned)grid, 256, 0, st>>>(
-          subs, n_subs, n_row_blocks, reinterpret_cast<const float *>(x0), reinterpret_cast<const float *>(x1),
-          beta2, eps, lr, dbg, status, rowf, (kMode == 0 && !stats) ? nullptr : rowpart, mscale, nullptr);
+      err = launch_kernel(normuon_rows_kernel<float, kMode>, dim3((unsigned)grid), dim3(256), 0, st, 1, subs, n_subs,
+                          n_row_blocks, reinterpret_cast<const float *>(x0), reinterpret_cast<const float *>(x1),
+                          beta2, eps, lr, dbg, status, rowf, (kMode == 0 && !stats) ? nullptr : rowpart,
+                          (const float *)mscale, (const float *)nullptr);
     count_launches(1);
   };
   if (rms_target > 0.f) {
     rows(std::integral_constant<int, 1>());
-    normuon_scale_kernel<<<(unsigned)n_subs, 256, 0, st>>>(subs, rowpart, rms_target, mscale, status);
+    if (err == cudaSuccess)
+      err = launch_kernel(normuon_scale_kernel, dim3((unsigned)n_subs), dim3(256), 0, st, 1, subs,
+                          (const float *)rowpart, rms_target, mscale, status);
     count_launches(1);
     rows(std::integral_constant<int, 2>());
   } else if (streamed) {  // the statistics pass (row factors), then the streamed write
@@ -820,7 +842,7 @@ int launch_normuon_rows(const DevSub *subs, int32_t n_subs, int64_t n_row_blocks
   } else {
     rows(std::integral_constant<int, 0>());
   }
-  return (int)cudaGetLastError();
+  return (int)err;
 }
 
 int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, float *row_v, void *w,
@@ -829,10 +851,11 @@ int launch_normuon_rownorm_plain(const float *O, int64_t rows, int64_t cols, flo
   if (rows == 0 || cols == 0) return 0;
   const int64_t nb = (rows + kRowBlock - 1) / kRowBlock;
   const unsigned grid = (unsigned)std::min<int64_t>(nb, 65535);
-  rownorm_plain_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      O, rows, cols, row_v, w, w_dtype, beta2, eps, scale, lr, wd, dbg);
+  const cudaError_t err = launch_kernel(rownorm_plain_kernel, dim3(grid), dim3(256), 0,
+                                        reinterpret_cast<cudaStream_t>(stream), 1, O, rows, cols, row_v, w, w_dtype,
+                                        beta2, eps, scale, lr, wd, dbg);
   count_launches(1);
-  return (int)cudaGetLastError();
+  return (int)err;
 }
 
 }  // namespace gbo

@@ -503,6 +503,7 @@ __device__ __forceinline__ void mom_stage(uint32_t stage, const DevSub &S, __nv_
 template <int kH, bool kFuse, bool kMom>
 __global__ void __launch_bounds__(chain_threads<kFuse, kMom>(), 1)
 ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ PhaseArgs A) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up (see device_common.cuh)
   using G = Geo<kH>;
   static_assert(!kFuse || kH == 1, "the Gram runs on chip for p <= 128 only");
   static_assert(!kMom || kFuse, "the momentum pass runs on chip only with the Gram");
@@ -561,6 +562,7 @@ ns_chain_kernel(const __grid_constant__ ChainParams P, const __grid_constant__ P
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int64_t total = P.mat_start[P.n];
   const uint32_t slots = smem_u32(smem);
   // matrix g of this CTA is blockIdx.x + g * gridDim.x, in slot g % S; a
@@ -1099,11 +1101,10 @@ int launch_geometry(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
     const int64_t total = T.mat_start[T.n];
     if (total == 0) continue;
     const unsigned grid = (unsigned)std::min<int64_t>(total, sm_count);  // one CTA per SM
-    ns_chain_kernel<kH, kFuse, kMom>
-        <<<grid, chain_threads<kFuse, kMom>(), G::Smem, reinterpret_cast<cudaStream_t>(stream)>>>(T, args);
+    const cudaError_t err = launch_kernel(ns_chain_kernel<kH, kFuse, kMom>, dim3(grid), dim3(chain_threads<kFuse, kMom>()),
+                                          G::Smem, reinterpret_cast<cudaStream_t>(stream), 1, T, args);
     count_launches(1);
     if (n_launch) ++*n_launch;
-    const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return (int)err;
   }
   return 0;

@@ -294,6 +294,7 @@ __device__ __forceinline__ bool mma_tile(uint8_t *smem, uint32_t full0, uint32_t
 template <bool kPair>
 __global__ void __launch_bounds__(Epi<kPair>::kThreads, 1)
 ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ PhaseArgs A) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up (see device_common.cuh)
   constexpr int STAGES = Mode<kPair>::kStages;
   constexpr int kRows = Mode<kPair>::kRows;
   extern __shared__ uint8_t smem_raw[];
@@ -352,6 +353,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   tc_fence_after();
   if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before any remote arrive
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int64_t total = P.tile_start[P.n];
   const int64_t cid = kPair ? (blockIdx.x >> 1) : blockIdx.x;
   const int64_t ncl = kPair ? (gridDim.x >> 1) : gridDim.x;
@@ -710,6 +712,16 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
     } else {
       cfg.gridDim = dim3((unsigned)std::min<int64_t>(total, sm_count));  // one CTA per SM
     }
+    // programmatic stream serialization (this kernel waits for the previous
+    // one after its prologue), and the pair's cluster
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (kPair) attrs[na++] = attr[0];
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
     const cudaError_t lerr = cudaLaunchKernelEx(&cfg, ns_gemm_tc_kernel<kPair>, T, args);
     if (lerr != cudaSuccess) return (int)lerr;
     count_launches(1);

@@ -196,6 +196,7 @@ __device__ __forceinline__ void epilogue_block_f32(const TcParams &P, const Phas
 template <bool kPair>
 __global__ void __launch_bounds__(kFThreads, 1)
 ns_gemm_tf32_kernel(const __grid_constant__ TcParams P, const __grid_constant__ PhaseArgs A) {
+  pdl_launch();  // the next kernel may be scheduled as SMs free up (see device_common.cuh)
   constexpr int STAGES = FMode<kPair>::kStages;
   constexpr int RAW = FMode<kPair>::kRawBytes;
   constexpr int kRows = FMode<kPair>::kRows;
@@ -253,6 +254,7 @@ ns_gemm_tf32_kernel(const __grid_constant__ TcParams P, const __grid_constant__ 
   tc_fence_after();
   if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before any remote arrive
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int64_t total = P.tile_start[P.n];
   const int64_t cid = kPair ? (blockIdx.x >> 1) : blockIdx.x;
   const int64_t ncl = kPair ? (gridDim.x >> 1) : gridDim.x;
@@ -590,6 +592,16 @@ int launch_mode_f32(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
     } else {
       cfg.gridDim = dim3((unsigned)std::min<int64_t>(total, sm_count));
     }
+    // programmatic stream serialization (this kernel waits for the previous
+    // one after its prologue), and the pair's cluster
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (kPair) attrs[na++] = attr[0];
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
     const cudaError_t lerr = cudaLaunchKernelEx(&cfg, ns_gemm_tf32_kernel<kPair>, T, args);
     if (lerr != cudaSuccess) return (int)lerr;
     count_launches(1);
