@@ -111,6 +111,7 @@ def lib():
         "gbo_testing_set_small_chain": (c_int32, [c_int32]),
         "gbo_testing_set_fused_gram": (c_int32, [c_int32]),
         "gbo_testing_set_fused_momentum": (c_int32, [c_int32]),
+        "gbo_testing_set_tail_split": (c_int32, [c_int32]),
         "gbo_last_error": (ctypes.c_char_p, []),
         "gbo_abi_version": (c_int32, []),
         "gbo_struct_size": (c_size_t, [c_int32]),
@@ -429,6 +430,13 @@ def gbo_testing_set_fused_momentum(enable):
     B streamed through shared memory) rather than in the momentum kernel
     (the default).  Returns the previous setting."""
     return bool(lib().gbo_testing_set_fused_momentum(1 if enable else 0))
+
+
+def gbo_testing_set_tail_split(enable):
+    """Whether launches of the bf16 CTA-pair kernel from now on run a last
+    wave of at most half the resident pairs as 256 x 128 half tiles (the
+    default).  Returns the previous setting."""
+    return bool(lib().gbo_testing_set_tail_split(1 if enable else 0))
 
 
 def gbo_testing_wait_timeout(dev_status, limit_us, stream=None):

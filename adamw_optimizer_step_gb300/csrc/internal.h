@@ -239,6 +239,9 @@ double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall, boo
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);
+// The bf16 pair kernel's tail split on (1, the default) or off; returns the
+// previous setting (gbo_testing_set_tail_split).
+int32_t set_tail_split(int32_t enable);
 // One 3-D TMA map (columns, rows, 1) per descriptor for the last product's
 // weight stores: 32 x 32 boxes, 64-byte swizzle, for bf16 weights whose rows
 // start on 16-byte boundaries (others zero, and their matrices carry wmap =

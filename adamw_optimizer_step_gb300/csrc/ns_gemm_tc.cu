@@ -25,7 +25,10 @@
 //               updated in place and stored by TMA, through a map of the
 //               weight
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the
-// epilogue of one tile overlaps the MMAs of the next.  Every wait is
+// epilogue of one tile overlaps the MMAs of the next.  Work items are dealt
+// round-robin over the resident CTA pairs; when a launch's last wave would
+// occupy at most half of them, its tiles run as 256 x 128 halves instead
+// (tail split, item_of below).  Every wait is
 // bounded: on time-out the kernel flags GBO_STATUS_TIMEOUT, waits (bounded)
 // for its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -33,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -46,6 +50,8 @@ namespace gbo {
 namespace {
 
 constexpr int BK = 64;   // 64 bf16 = one 128-byte swizzle row
+
+std::atomic<int32_t> g_tail_split{1};  // see gbo_testing_set_tail_split
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's rows of A
 constexpr int B_HALF = (BN / 2) * BK * 2;        // 16 KB: 128 rows of B
 // Two modes share the kernel source:
@@ -98,14 +104,31 @@ constexpr int kSmemBytes =
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
 // each K-major or MN-major, N = 256, M = 128 (one CTA) or 256 (pair).
-__host__ __device__ constexpr uint32_t make_idesc(int a_mn_major, int b_mn_major, int m) {
+__host__ __device__ constexpr uint32_t make_idesc(int a_mn_major, int b_mn_major, int m, int n = BN) {
   return (1u << 4)                      // D format: f32
          | (1u << 7)                    // A format: bf16
          | (1u << 10)                   // B format: bf16
          | ((uint32_t)a_mn_major << 15) // A major-ness
          | ((uint32_t)b_mn_major << 16) // B major-ness
-         | ((uint32_t)(BN >> 3) << 17)  // N / 8
+         | ((uint32_t)(n >> 3) << 17)   // N / 8
          | ((uint32_t)(m >> 4) << 24);  // M / 16
+}
+
+// Work item t of a launch: its tile, and which 128-column half of it when
+// the item lies in the launch's split tail (half = -1: the whole tile).
+// The tail split runs a launch's last partial wave of pair tiles as twice as
+// many half tiles (N = 128), so it ends after half a tile's time instead of
+// a whole one; each output element still sums the same products in the same
+// order.
+template <int kRows>
+__device__ __forceinline__ TileCoord item_of(const TcParams &P, int64_t t, int &half) {
+  if (t < P.split_base) {
+    half = -1;
+    return decode<kRows>(P, t);
+  }
+  const int64_t u = t - P.split_base;
+  half = (int)(u & 1);
+  return decode<kRows>(P, P.split_base + (u >> 1));
 }
 
 // One 128 x 256 x 16 MMA of this CTA (cta_group::1).
@@ -200,7 +223,7 @@ __device__ __forceinline__ void epilogue_block(const TcParams &P, const PhaseArg
 // operand layouts (A, B K-major or MN-major), so that the single-thread
 // issue loops carry no per-k-block choices.  Return false on a time-out.
 template <bool kPair, bool kAmn, bool kBmn>
-__device__ __forceinline__ bool produce_tile(const TcParams &P, const TileCoord &tc, int tm, uint8_t *smem,
+__device__ __forceinline__ bool produce_tile(const TcParams &P, const TileCoord &tc, int half, int tm, uint8_t *smem,
                                              uint32_t full0, uint32_t empty0, uint32_t full_lead0, bool leader,
                                              uint32_t crank, int &stage, uint32_t &phase, uint32_t *armed_parity,
                                              bool *armed, volatile int32_t *abort_flag) {
@@ -209,12 +232,20 @@ __device__ __forceinline__ bool produce_tile(const TcParams &P, const TileCoord 
   const CUtensorMap *ma = &P.mapA[tc.c], *mb = &P.mapB[tc.c];
   const int kit = P.k_iters[tc.c];
   const int m0 = tm * BM;
-  const int n0 = tc.tn * BN + (kPair ? (int)crank * (BN / 2) : 0);  // this CTA's first B row (column of C)
+  // this CTA's first B row (column of C): a pair's N columns are split
+  // between its two CTAs, N / 2 each.  A half tile (N = 128) loads 64 rows
+  // of B per CTA: a 64-row box when B is K-major, one 64-column box when it
+  // is MN-major.
+  const int n0 = tc.tn * BN + (half >= 0 ? half * (BN / 2) + (int)crank * (BN / 4)
+                                         : (kPair ? (int)crank * (BN / 2) : 0));
+  const CUtensorMap *mbh = &P.mapBh[tc.c];
+  constexpr int kHalfSaved = Mode<kPair>::kSub * (B_HALF / 2);  // B bytes per CTA a half tile's stage skips
+  const uint32_t stage_tx = (uint32_t)((kPair ? 2 : 1) * (STAGE_BYTES - (half >= 0 ? kHalfSaved : 0)));
   for (int kb = 0; kb < kit; ++kb) {
     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) return false;
     if (*abort_flag) return true;
     if (leader) {
-      mbar_expect_tx(full0 + 8 * stage, (kPair ? 2 : 1) * STAGE_BYTES);
+      mbar_expect_tx(full0 + 8 * stage, stage_tx);
       armed[stage] = true;
       armed_parity[stage] = phase;
     }
@@ -232,10 +263,10 @@ __device__ __forceinline__ bool produce_tile(const TcParams &P, const TileCoord 
         for (int h = 0; h < BM / 64; ++h) tma_load_3d_pair(sa + h * 8192, ma, fb, m0 + h * 64, k0, tc.mat);
       }
       if constexpr (!kBmn) {
-        tma_load_3d_pair(sb, mb, fb, k0, n0, tc.mat);
+        tma_load_3d_pair(sb, half >= 0 ? mbh : mb, fb, k0, n0, tc.mat);
       } else {
-#pragma unroll
-        for (int h = 0; h < BN / 128; ++h) tma_load_3d_pair(sb + h * 8192, mb, fb, n0 + h * 64, k0, tc.mat);
+        for (int h = 0; h < (half >= 0 ? 1 : BN / 128); ++h)
+          tma_load_3d_pair(sb + h * 8192, mb, fb, n0 + h * 64, k0, tc.mat);
       }
     } else {
       const uint32_t fb = full0 + 8 * stage;
@@ -261,10 +292,12 @@ __device__ __forceinline__ bool produce_tile(const TcParams &P, const TileCoord 
 
 template <bool kPair, bool kAmn, bool kBmn>
 __device__ __forceinline__ bool mma_tile(uint8_t *smem, uint32_t full0, uint32_t empty0, uint32_t d_tmem, int kit,
-                                         int &stage, uint32_t &phase, bool &issued) {
+                                         bool half, int &stage, uint32_t &phase, bool &issued) {
   constexpr int STAGES = Mode<kPair>::kStages;
   constexpr int STAGE_BYTES = Mode<kPair>::kStageBytes;
-  constexpr uint32_t idesc = make_idesc(kAmn, kBmn, Mode<kPair>::kRows * BM);
+  constexpr uint32_t idesc_full = make_idesc(kAmn, kBmn, Mode<kPair>::kRows * BM);
+  constexpr uint32_t idesc_half = make_idesc(kAmn, kBmn, Mode<kPair>::kRows * BM, BN / 2);
+  const uint32_t idesc = half ? idesc_half : idesc_full;
   // descriptors of stage 0, K step 0: a stage is STAGE_BYTES further, a K
   // step of 16 is 32 bytes (K-major) or two 8-row groups, 2048 bytes (MN-major)
   const uint64_t a0 = smem_desc(smem_u32(smem), kAmn ? 8192 : 16, 1024);
@@ -354,7 +387,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
   if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before any remote arrive
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the previous kernel has completed and its writes are visible
-  const int64_t total = P.tile_start[P.n];
+  const int64_t total = P.n_items;
   const int64_t cid = kPair ? (blockIdx.x >> 1) : blockIdx.x;
   const int64_t ncl = kPair ? (gridDim.x >> 1) : gridDim.x;
   const uint32_t full_lead0 = kPair ? map_to_rank(full0, 0) : full0;
@@ -373,19 +406,20 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       bool armed[STAGES];
       for (int s = 0; s < STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
       for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
-        const TileCoord tc = decode<kRows>(P, t);
+        int half;
+        const TileCoord tc = item_of<kRows>(P, t, half);
         const int tm = kRows * tc.tm + (int)crank;
         const int kind = P.job[tc.c].kind;
         bool ok;
         if (kind == kKindGramT)
-          ok = produce_tile<kPair, true, true>(P, tc, tm, smem, full0, empty0, full_lead0, leader, crank, stage, phase,
-                                               armed_parity, armed, abort_flag);
+          ok = produce_tile<kPair, true, true>(P, tc, half, tm, smem, full0, empty0, full_lead0, leader, crank, stage,
+                                               phase, armed_parity, armed, abort_flag);
         else if (kind == kKindProd)
-          ok = produce_tile<kPair, false, true>(P, tc, tm, smem, full0, empty0, full_lead0, leader, crank, stage,
-                                                phase, armed_parity, armed, abort_flag);
+          ok = produce_tile<kPair, false, true>(P, tc, half, tm, smem, full0, empty0, full_lead0, leader, crank,
+                                                stage, phase, armed_parity, armed, abort_flag);
         else
-          ok = produce_tile<kPair, false, false>(P, tc, tm, smem, full0, empty0, full_lead0, leader, crank, stage,
-                                                 phase, armed_parity, armed, abort_flag);
+          ok = produce_tile<kPair, false, false>(P, tc, half, tm, smem, full0, empty0, full_lead0, leader, crank,
+                                                 stage, phase, armed_parity, armed, abort_flag);
         if (!ok) { give_up(); break; }
       }
       if (*abort_flag && leader) {
@@ -402,7 +436,8 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       uint32_t acc_phase = 0;
       bool issued = false;
       for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
-        const TileCoord tc = decode<kRows>(P, t);
+        int half;
+        const TileCoord tc = item_of<kRows>(P, t, half);
         const int kit = P.k_iters[tc.c];
         const int kind = P.job[tc.c].kind;
         const bool freed = kPair ? mbar_wait_cluster(acce0 + 8 * acc, acc_phase ^ 1)
@@ -411,9 +446,13 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         bool ok;
-        if (kind == kKindGramT) ok = mma_tile<kPair, true, true>(smem, full0, empty0, d_tmem, kit, stage, phase, issued);
-        else if (kind == kKindProd) ok = mma_tile<kPair, false, true>(smem, full0, empty0, d_tmem, kit, stage, phase, issued);
-        else ok = mma_tile<kPair, false, false>(smem, full0, empty0, d_tmem, kit, stage, phase, issued);
+        const bool hf = half >= 0;
+        if (kind == kKindGramT)
+          ok = mma_tile<kPair, true, true>(smem, full0, empty0, d_tmem, kit, hf, stage, phase, issued);
+        else if (kind == kKindProd)
+          ok = mma_tile<kPair, false, true>(smem, full0, empty0, d_tmem, kit, hf, stage, phase, issued);
+        else
+          ok = mma_tile<kPair, false, false>(smem, full0, empty0, d_tmem, kit, hf, stage, phase, issued);
         if (!ok) { give_up(); break; }
         if constexpr (kPair) mma_commit_pair_mc(accf0 + 8 * acc, 0x3);  // accumulator ready in both TMEMs
         else mma_commit_one(accf0 + 8 * acc);
@@ -439,12 +478,16 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = cid; t < total && !*abort_flag; t += ncl) {
-      const TileCoord tc = decode<kRows>(P, t);
+      int half;
+      const TileCoord tc = item_of<kRows>(P, t, half);
       const int sub = P.sub0[tc.c] + tc.mat;
       const DevSub &S = A.subs[sub];
       const TcJob &J = P.job[tc.c];
       const int i0 = (kRows * tc.tm + (int)crank) * BM + quarter * 32;
-      const int c0 = tc.tn * BN + part * E::kSpan;    // this warp's first column
+      // this warp's first column and the columns it covers (a half tile's
+      // accumulator is the first 128 columns of its TMEM buffer)
+      const int span = half >= 0 ? BN / 2 : E::kSpan;
+      const int c0 = tc.tn * BN + (half >= 0 ? half * (BN / 2) : part * E::kSpan);
       // the job's output is rows x cols (stored orientation for the weights)
       const int rows = kind_rows(J.kind, S.p, S.q), cols = kind_cols(J.kind, S.p, S.q);
       // bf16 weights in blocks of 32 whole rows with a TMA map move by TMA
@@ -455,8 +498,8 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
                                     : nullptr;
       const bool live = i0 < rows && c0 < cols;      // this warp's part of the tile holds outputs
       const bool wtma = live && wmap != nullptr && i0 + 32 <= rows;
-      if (wtma) weight_loads_begin<E::kWBufs>(wmap, stage, wbar0, c0, cols, (int)(S.r0 + i0), lane, winfl, E::kSpan);
-      else if (live && J.mode == kFinal) prefetch_weight_tile(S, i0, c0, rows, cols, lane, E::kSpan);
+      if (wtma) weight_loads_begin<E::kWBufs>(wmap, stage, wbar0, c0, cols, (int)(S.r0 + i0), lane, winfl, span);
+      else if (live && J.mode == kFinal) prefetch_weight_tile(S, i0, c0, rows, cols, lane, span);
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) { give_up(); break; }
       tc_fence_after();
       const float s = J.first ? A.alpha[sub] : 1.0f;
@@ -471,15 +514,15 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
       if (live) {  // warps whose rows or columns are all padding have nothing to write
         if (wtma) {
           if (!final_tile_bf16_tma<E::kWBufs>(A, S, s, i0, c0, cols, trow, lane, wmap, stage, wbar0, wpar, winfl,
-                                              E::kSpan, stats ? rss : nullptr)) {
+                                              span, stats ? rss : nullptr)) {
             give_up();
             break;
           }
         } else if (J.mode == kFinal && S.w_dtype == GBO_BF16) {
-          final_tile_bf16(A, S, s, i0, c0, rows, cols, trow, lane, E::kSpan, stats ? rss : nullptr);
+          final_tile_bf16(A, S, s, i0, c0, rows, cols, trow, lane, span, stats ? rss : nullptr);
         } else {
 #pragma unroll 1
-          for (int ch = 0; ch < E::kSpan / 32; ++ch) {
+          for (int ch = 0; ch < span / 32; ++ch) {
             const int col0 = c0 + ch * 32;
             if (col0 >= cols) break;  // column chunks past the output hold nothing to write
             float v[32];
@@ -502,7 +545,7 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
                             (int64_t)(i0 + lane) * S.ss_ntn + c0 / 128;
 #pragma unroll
           for (int h = 0; h < E::kSpan / 128; ++h)
-            if (c0 + 128 * h < cols) part_out[h] = rss[h];
+            if (128 * h < span && c0 + 128 * h < cols) part_out[h] = rss[h];
         }
       }
       tc_fence_before();
@@ -627,7 +670,8 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
       void *x = const_cast<char *>(xbase(J.kind == kKindProd ? J.opB : J.opA, C));
       if (J.kind == kKindGram) {  // X wide: A = X rows, B = X rows, K = q
         ok = encode_map(&T.mapA[k], x, C.q, C.p, C.count, C.ld, BK, BM) &&
-             encode_map(&T.mapB[k], x, C.q, C.p, C.count, C.ld, BK, BN / 2);
+             encode_map(&T.mapB[k], x, C.q, C.p, C.count, C.ld, BK, BN / 2) &&
+             (!kPair || encode_map(&T.mapBh[k], x, C.q, C.p, C.count, C.ld, BK, BN / 4));
         Mdim = C.p, Ndim = C.p, Kdim = C.q;
       } else if (J.kind == kKindGramT) {  // X tall: A and B = columns of X (MN-major boxes), K = q
         ok = encode_map(&T.mapA[k], x, C.p, C.q, C.count, C.ld, 64, BK) &&
@@ -635,7 +679,9 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
         Mdim = C.p, Ndim = C.p, Kdim = C.q;
       } else if (J.kind == kKindSym) {  // A = L rows, B = R rows (R symmetric), K = p
         ok = encode_map(&T.mapA[k], const_cast<char *>(pbase(J.opA, C)), C.p, C.p, C.count, C.ldp, BK, BM) &&
-             encode_map(&T.mapB[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 2);
+             encode_map(&T.mapB[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 2) &&
+             (!kPair ||
+              encode_map(&T.mapBh[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 4));
         Mdim = C.p, Ndim = C.p, Kdim = C.p;
       } else if (J.kind == kKindProd) {  // X wide: A = L rows (K = p), B = X with rows as K, columns as N
         ok = encode_map(&T.mapA[k], const_cast<char *>(pbase(J.opA, C)), C.p, C.p, C.count, C.ldp, BK, BM) &&
@@ -643,7 +689,9 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
         Mdim = C.p, Ndim = C.q, Kdim = C.p;
       } else {  // kKindProdT, X tall: A = X rows (K = p), B = L rows (L symmetric)
         ok = encode_map(&T.mapA[k], x, C.p, C.q, C.count, C.ld, BK, BM) &&
-             encode_map(&T.mapB[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 2);
+             encode_map(&T.mapB[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 2) &&
+             (!kPair ||
+              encode_map(&T.mapBh[k], const_cast<char *>(pbase(J.opB, C)), C.p, C.p, C.count, C.ldp, BK, BN / 4));
         Mdim = C.q, Ndim = C.p, Kdim = C.p;
       }
       // outputs stored by TMA: a p x p matrix in the class's p-space, or X'
@@ -706,10 +754,17 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
         if (cudaOccupancyMaxActiveClusters(&max_clusters, ns_gemm_tc_kernel<true>, &cfg) != cudaSuccess)
           max_clusters = 0;
       });
-      const int clusters =
-          (int)std::min<int64_t>(total, max_clusters > 0 ? max_clusters : std::max(1, sm_count / 2));
+      const int64_t resident = max_clusters > 0 ? max_clusters : std::max(1, sm_count / 2);
+      // tail split: a last partial wave of at most half the resident pairs
+      // runs as half tiles, one per pair
+      const int64_t rem = total % resident;
+      const int64_t n_split = (g_tail_split.load() != 0 && rem > 0 && 2 * rem <= resident) ? rem : 0;
+      T.split_base = total - n_split;
+      T.n_items = total + n_split;
+      const int clusters = (int)std::min<int64_t>(T.n_items, resident);
       cfg.gridDim = dim3(2 * clusters);
     } else {
+      T.split_base = T.n_items = total;
       cfg.gridDim = dim3((unsigned)std::min<int64_t>(total, sm_count));  // one CTA per SM
     }
     // programmatic stream serialization (this kernel waits for the previous
@@ -749,6 +804,8 @@ __global__ void wait_timeout_kernel(int32_t *status, uint64_t limit_ns) {
 }
 
 }  // namespace
+
+int32_t set_tail_split(int32_t enable) { return g_tail_split.exchange(enable != 0 ? 1 : 0); }
 
 int launch_wait_timeout(int32_t *status, uint64_t limit_ns, void *stream) {
   wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, limit_ns);

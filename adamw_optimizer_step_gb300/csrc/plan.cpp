@@ -1182,6 +1182,8 @@ int32_t gbo_testing_set_fused_gram(int32_t enable) { return g_fused_gram.exchang
 
 int32_t gbo_testing_set_fused_momentum(int32_t enable) { return g_fused_mom.exchange(enable != 0 ? 1 : 0); }
 
+int32_t gbo_testing_set_tail_split(int32_t enable) { return gbo::set_tail_split(enable); }
+
 int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream) {
   if (!dev_status || !aligned(dev_status, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_status is NULL or misaligned");
   if (limit_us == 0 || limit_us > 10000000u) return fail(GBO_ERR_INVALID_ARG, "limit_us must be in 1..10^7");

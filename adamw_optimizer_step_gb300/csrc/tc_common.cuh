@@ -41,6 +41,7 @@ struct TcParams {
   CUtensorMap mapB[kMaxClassesPerLaunch];  // B operand, likewise
   CUtensorMap mapO[kMaxClassesPerLaunch];  // output (TMA store), box 32 x 32
   CUtensorMap mapO2[kMaxClassesPerLaunch]; // second output: A of kGramAP, or X'T of an fp32 product
+  CUtensorMap mapBh[kMaxClassesPerLaunch]; // bf16 pair kernel: K-major B in 64-row boxes, for half tiles
   int64_t tile_start[kMaxClassesPerLaunch + 1];
   int32_t tiles_n[kMaxClassesPerLaunch];
   int32_t k_iters[kMaxClassesPerLaunch];
@@ -48,6 +49,12 @@ struct TcParams {
   int32_t tiles_per_mat[kMaxClassesPerLaunch];
   TcJob job[kMaxClassesPerLaunch];
   int32_t n;
+  // tail split (bf16 pair kernel only): work items split_base .. of the
+  // launch's tile_start[n] items run as two halves of 128 columns each, so
+  // the launch has n_items = tile_start[n] + (tile_start[n] - split_base)
+  // work items; without a split, split_base = n_items = tile_start[n]
+  int64_t split_base;
+  int64_t n_items;
 };
 
 // ---------------------------------------------------------------------------

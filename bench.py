@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--fused-momentum", action="store_true",
                     help="A/B: run the momentum pass of the chain's wide p <= 128 matrices inside the chain launch "
                          "instead of in the momentum kernel (workload 4; measured slower)")
+    ap.add_argument("--no-tail-split", action="store_true",
+                    help="A/B: run a CTA-pair launch's last partial wave as whole 256 x 256 tiles instead of "
+                         "256 x 128 halves")
     ap.add_argument("--workspace-cap-frac", type=float, default=0.0,
                     help="cap the Muon workspace at this fraction of what the whole table needs (0: no cap); "
                          "the step then runs in groups of weights on the smaller workspace")
@@ -517,6 +520,9 @@ def run_ours(args):
     if args.fused_momentum:
         from adamw_optimizer_step_gb300 import _binding
         _binding.gbo_testing_set_fused_momentum(True)
+    if args.no_tail_split:
+        from adamw_optimizer_step_gb300 import _binding
+        _binding.gbo_testing_set_tail_split(False)
     wl = wk.workload(args.workload)
     if args.layers:
         wl = wk.first_layers(wl, args.layers)
@@ -706,6 +712,7 @@ def run_ours(args):
                                     else "bf16 operands, fp32 accumulate"),
                    "parallelism": "replicas" if world > 1 else "single",
                    "chain_gram": "separate launch" if args.separate_gram else "on chip (p <= 128)",
+                   "tail_split": not args.no_tail_split,
                    "workspace_bytes": int(ws.numel()), "workspace_cap": cap or None,
                    "workspace_whole_table_bytes": int(ws_whole),
                    "chain_momentum": ("in the chain launch (wide p <= 128, bf16 G)"

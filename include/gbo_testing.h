@@ -57,6 +57,17 @@ int32_t gbo_testing_set_fused_gram(int32_t enable);
  */
 int32_t gbo_testing_set_fused_momentum(int32_t enable);
 
+/*
+ * Test and A/B switch, read at each launch of the bf16 CTA-pair
+ * Newton-Schulz kernel: a launch whose last wave of 256 x 256 tiles would
+ * occupy at most half of the resident CTA pairs runs those tiles as two
+ * 256 x 128 halves each, so the launch ends after half a tile's time
+ * (enable != 0, the default), or runs them whole (enable == 0).  Both give
+ * the same results: every output element sums the same products in the
+ * same order.  Returns the previous setting.
+ */
+int32_t gbo_testing_set_tail_split(int32_t enable);
+
 #ifdef __cplusplus
 }
 #endif

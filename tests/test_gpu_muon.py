@@ -593,3 +593,35 @@ def test_after_momentum_event_and_side_stream():
     for d, p in zip(dev, plain):
         assert torch.equal(d["w"].cpu(), p["W"]) and torch.equal(d["mom"].cpu(), p["B"])
     B.gbo_muon_plan_set_event(plan, 0, None)
+
+
+TAIL_SPLIT = [(1024, 1024, None, None), (2048, 2048, None, None), (384, 1536, None, None),
+              (1536, 384, None, None), (1000, 700, None, None), (700, 1000, None, None),
+              (3 * 320, 1280, (3, 320, 1280), None, 1.0, 0.1)]
+
+
+@pytest.mark.parametrize("normuon", [False, True])
+@pytest.mark.parametrize("shape", TAIL_SPLIT, ids=lambda s: "%dx%d" % s[:2])
+def test_tail_split_bitwise(shape, normuon):
+    """A weight alone in its plan gives launches of at most a few dozen CTA-pair
+    tiles, so most run as 256 x 128 halves (Gram, products, the weight-writing
+    last product, both routes, tall and wide): weights, momentum, row moments
+    and the exported update are bitwise those of whole tiles, and match the
+    oracle."""
+    entries = random_entries([shape], seed=47, normuon=normuon, b_std=1e-3)
+    kw = dict(lr=0.02, precision="bf16", steps=2, normuon=normuon, beta2=0.95, eps=1e-8)
+    prev = B.gbo_testing_set_tail_split(False)
+    try:
+        whole, st0, _ = run_muon_gpu(entries, **kw)
+        B.gbo_testing_set_tail_split(True)
+        split, st1, _ = run_muon_gpu(entries, **kw)
+        one, st2, _ = run_muon_gpu(entries, **dict(kw, steps=1))
+    finally:
+        B.gbo_testing_set_tail_split(prev)
+    assert st0 == 0 and st1 == 0 and st2 == 0
+    for a, b in zip(whole, split):
+        assert torch.equal(a["W"], b["W"]) and torch.equal(a["B"], b["B"]) and torch.equal(a["U"], b["U"])
+        if normuon:
+            assert torch.equal(a["v"], b["v"])
+    ora = run_muon_oracle(entries, lr=0.02, normuon=normuon, beta2=0.95, eps=1e-8)
+    check_muon(entries, one, ora, lr=0.02, precision="bf16")
