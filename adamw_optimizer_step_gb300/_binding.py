@@ -103,6 +103,8 @@ def lib():
         "gbo_clip_norm_workspace_bytes": (c_size_t, []),
         "gbo_clip_norm": (c_int32, [ctypes.POINTER(Tensor), c_int32, c_float, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_size_t, c_void_p]),
+        "gbo_h2d_copy": (c_int32, [c_void_p, c_void_p, ctypes.c_int64, c_int32, c_void_p]),
+        "gbo_muon_plan_set_free_sms": (c_int32, [c_void_p, c_int32]),
         "gbo_clip_norm_noalloc": (c_int32, [ctypes.POINTER(Tensor), c_int32, c_float, c_void_p, c_void_p,
                                             c_void_p, c_void_p]),
         "gbo_adamw_step": (c_int32, [ctypes.POINTER(AdamWDesc), c_int32, ctypes.POINTER(AdamWOpts), c_void_p,
@@ -112,6 +114,7 @@ def lib():
         "gbo_testing_set_fused_gram": (c_int32, [c_int32]),
         "gbo_testing_set_fused_momentum": (c_int32, [c_int32]),
         "gbo_testing_set_tail_split": (c_int32, [c_int32]),
+        "gbo_testing_pair_residency": (c_int32, []),
         "gbo_last_error": (ctypes.c_char_p, []),
         "gbo_abi_version": (c_int32, []),
         "gbo_struct_size": (c_size_t, [c_int32]),
@@ -295,6 +298,12 @@ def gbo_muon_step(plan, lr, workspace, dbg_update=None, dev_status=None, stream=
                                _dev_ptr(dev_status, "dev_status"), _stream(stream)))
 
 
+def gbo_muon_plan_set_free_sms(plan, n):
+    """Leave ``n`` SMs free of the plan's persistent Newton-Schulz kernels in
+    later steps (for gbo_h2d_copy with ``n`` blocks on another stream)."""
+    _check(lib().gbo_muon_plan_set_free_sms(plan.handle, int(n)))
+
+
 def gbo_muon_plan_set_stats(plan, stats):
     """Per-matrix norms from later steps: ``stats`` is a float32 CUDA tensor of
     2 * n_matrices values (||D||_F, ||U||_F per matrix, table order), or None
@@ -374,6 +383,21 @@ def gbo_clip_norm_noalloc(grads, max_norm, total_norm, coef, dev_status=None, st
                                        _stream(stream)))
 
 
+def gbo_h2d_copy(dst, src, blocks=0, stream=None):
+    """Copy the page-locked host tensor ``src`` into the device tensor
+    ``dst`` (both contiguous, the same number of bytes) with the library's
+    copy kernel (``blocks`` SMs; 0: all), asynchronously on ``stream``."""
+    if not (dst.is_cuda and dst.is_contiguous()):
+        raise ValueError("dst must be a contiguous CUDA tensor")
+    if src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous host tensor")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src differ in size")
+    _check(lib().gbo_h2d_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nbytes,
+                              int(blocks), _stream(stream)))
+
+
 def gbo_adamw_step(params, *, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0, step=1,
                    coef=None, dev_status=None, stream=None, dev_step=None):
     """AdamW on ``params``: a list of (p, g, m, v) tensors (p, m, v float32).
@@ -437,6 +461,12 @@ def gbo_testing_set_tail_split(enable):
     wave of at most half the resident pairs as 256 x 128 half tiles (the
     default).  Returns the previous setting."""
     return bool(lib().gbo_testing_set_tail_split(1 if enable else 0))
+
+
+def gbo_testing_pair_residency():
+    """CTA pairs of the bf16 Newton-Schulz kernel the current device holds at
+    once (its pair launches' persistent grid)."""
+    return int(lib().gbo_testing_pair_residency())
 
 
 def gbo_testing_wait_timeout(dev_status, limit_us, stream=None):

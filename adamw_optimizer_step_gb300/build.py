@@ -20,7 +20,7 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libgbo.so")
 
 SOURCES = ["plan.cpp", "muon_elementwise.cu", "ns_gemm_tc.cu", "ns_gemm_tf32.cu", "adamw.cu",
-           "clip_noalloc.cu", "ns_chain_tc.cu"]
+           "clip_noalloc.cu", "ns_chain_tc.cu", "h2d.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--expt-relaxed-constexpr"]

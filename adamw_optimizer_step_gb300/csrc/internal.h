@@ -12,6 +12,7 @@ constexpr int kMomTile = 64;        // momentum tiles: 64 x 64 elements of a mat
 constexpr int kMomFlat = kMomTile * kMomTile;  // 4096 consecutive elements of a matrix
 constexpr int kRowBlock = 64;       // NorMuon: stored rows per block
 constexpr int kMaxClassesPerLaunch = 8;
+constexpr int kMaxFreeSms = 64;  // gbo_muon_plan_set_free_sms
 
 // One independent matrix (a view block or split range of a stored weight),
 // as the kernels see it.  Orientation: the stored matrix is m x n; the
@@ -242,6 +243,9 @@ bool single_mode(int p);
 // The bf16 pair kernel's tail split on (1, the default) or off; returns the
 // previous setting (gbo_testing_set_tail_split).
 int32_t set_tail_split(int32_t enable);
+// How many CTA pairs of the bf16 Newton-Schulz kernel fit on the current
+// device at once (gbo_testing_pair_residency); -1 on a CUDA error.
+int32_t pair_residency();
 // One 3-D TMA map (columns, rows, 1) per descriptor for the last product's
 // weight stores: 32 x 32 boxes, 64-byte swizzle, for bf16 weights whose rows
 // start on 16-byte boundaries (others zero, and their matrices carry wmap =

@@ -754,7 +754,8 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
         if (cudaOccupancyMaxActiveClusters(&max_clusters, ns_gemm_tc_kernel<true>, &cfg) != cudaSuccess)
           max_clusters = 0;
       });
-      const int64_t resident = max_clusters > 0 ? max_clusters : std::max(1, sm_count / 2);
+      // every pair the device holds, within the SMs this launch may use
+      const int64_t resident = std::max(1, max_clusters > 0 ? std::min(max_clusters, sm_count / 2) : sm_count / 2);
       // tail split: a last partial wave of at most half the resident pairs
       // runs as half tiles, one per pair
       const int64_t rem = total % resident;
@@ -806,6 +807,28 @@ __global__ void wait_timeout_kernel(int32_t *status, uint64_t limit_ns) {
 }  // namespace
 
 int32_t set_tail_split(int32_t enable) { return g_tail_split.exchange(enable != 0 ? 1 : 0); }
+
+int32_t pair_residency() {
+  if (cudaFuncSetAttribute(ns_gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(Epi<true>::kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int dev = 0, sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  cfg.gridDim = dim3(2 * std::max(1, sm / 2));
+  int n = 0;
+  return cudaOccupancyMaxActiveClusters(&n, ns_gemm_tc_kernel<true>, &cfg) == cudaSuccess ? n : -1;
+}
 
 int launch_wait_timeout(int32_t *status, uint64_t limit_ns, void *stream) {
   wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, limit_ns);

@@ -587,7 +587,8 @@ int launch_mode_f32(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
           max_clusters = 0;
       });
       const int clusters =
-          (int)std::min<int64_t>(total, max_clusters > 0 ? max_clusters : std::max(1, sm_count / 2));
+          (int)std::min<int64_t>(total, std::max(1, max_clusters > 0 ? std::min(max_clusters, sm_count / 2)
+                                                                        : sm_count / 2));
       cfg.gridDim = dim3(2 * clusters);
     } else {
       cfg.gridDim = dim3((unsigned)std::min<int64_t>(total, sm_count));

@@ -177,6 +177,7 @@ struct gbo_plan {
   int64_t dbg_base = 0;  // a group's first element in the whole table's dbg_update
   int64_t mat_base = 0;  // a group's first matrix among the whole table's
   float *stats = nullptr;  // per-matrix norms (gbo_muon_plan_set_stats), or nullptr
+  int32_t free_sms = 0;     // SMs the Newton-Schulz kernels leave free (gbo_muon_plan_set_free_sms)
 };
 
 namespace {
@@ -958,6 +959,14 @@ int gbo_muon_plan_set_stats(gbo_plan *P, float *dev_stats) {
   return ok();
 }
 
+int gbo_muon_plan_set_free_sms(gbo_plan *P, int32_t n) {
+  if (!P) return fail(GBO_ERR_INVALID_ARG, "plan is NULL");
+  if (n < 0 || n > kMaxFreeSms) return fail(GBO_ERR_INVALID_ARG, "free SMs must be in 0 .. %d", kMaxFreeSms);
+  P->free_sms = n;
+  for (gbo_plan *q : P->kids) q->free_sms = n;
+  return ok();
+}
+
 int gbo_muon_plan_set_timing(gbo_plan *P, int32_t enable) {
   if (!P) return fail(GBO_ERR_INVALID_ARG, "plan is NULL");
   P->timing = enable != 0;
@@ -1125,11 +1134,13 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   A.nesterov = P->opts.nesterov;
   A.stats = P->stats;
   bool fused_left = P->any_mom_fused;  // a fused momentum pass is still to be launched
+  // the persistent Newton-Schulz kernels' SMs: all but the free ones
+  const int ns_sms = std::max(2, P->sm_count - P->free_sms);
   for (const TcStep &step : build_schedule(P, ws)) {
     int64_t nl = 0;
     err = P->x_dtype == GBO_BF16
-              ? launch_ns_gemm_tc(step.jobs.data(), (int32_t)step.jobs.size(), A, P->sm_count, st, &nl)
-              : launch_ns_gemm_tf32(step.jobs.data(), (int32_t)step.jobs.size(), A, P->sm_count, st, &nl);
+              ? launch_ns_gemm_tc(step.jobs.data(), (int32_t)step.jobs.size(), A, ns_sms, st, &nl)
+              : launch_ns_gemm_tf32(step.jobs.data(), (int32_t)step.jobs.size(), A, ns_sms, st, &nl);
     if (err) return cuda_fail(err, "Newton-Schulz kernel");
     if (fused_left)
       for (const GemmJob &J : step.jobs)
@@ -1183,6 +1194,8 @@ int32_t gbo_testing_set_fused_gram(int32_t enable) { return g_fused_gram.exchang
 int32_t gbo_testing_set_fused_momentum(int32_t enable) { return g_fused_mom.exchange(enable != 0 ? 1 : 0); }
 
 int32_t gbo_testing_set_tail_split(int32_t enable) { return gbo::set_tail_split(enable); }
+
+int32_t gbo_testing_pair_residency(void) { return gbo::pair_residency(); }
 
 int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream) {
   if (!dev_status || !aligned(dev_status, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_status is NULL or misaligned");

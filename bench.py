@@ -49,6 +49,11 @@ def parse():
     ap.add_argument("--fused-momentum", action="store_true",
                     help="A/B: run the momentum pass of the chain's wide p <= 128 matrices inside the chain launch "
                          "instead of in the momentum kernel (workload 4; measured slower)")
+    ap.add_argument("--e2e-copy", choices=["kernel", "engine"], default="engine",
+                    help="e2e uploads by the copy engine, or by the library's copy kernel (gbo_h2d_copy) on "
+                         "--e2e-copy-sms SMs the plans leave free")
+    ap.add_argument("--e2e-copy-sms", type=int, default=4,
+                    help="SMs of the e2e copy kernel, left free of the Newton-Schulz kernels during e2e steps")
     ap.add_argument("--no-tail-split", action="store_true",
                     help="A/B: run a CTA-pair launch's last partial wave as whole 256 x 256 tiles instead of "
                          "256 x 128 halves")
@@ -271,7 +276,7 @@ def traffic_record(kernel_files):
     return rec
 
 
-def run_e2e(n_steps, world, bufs, step, total, after_momentum):
+def run_e2e(n_steps, world, bufs, step, total, after_momentum, copy_blocks=0):
     """Steps/s with each step's gradients copied in from pinned host memory
     and the step's gradient norm read back on the host.  ``bufs`` holds two
     (Muon, AdamW) flat gradient buffer pairs, each bound to its own plan:
@@ -289,9 +294,12 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
     step has been seen to stall for ~150 ms on a host whose previous process
     had just exited (the upload's wait, not the GPU's work): the per-step
     times show such a stall, and the default 40 steps bound its weight in
-    the mean."""
+    the mean.  ``copy_blocks`` > 0: the uploads are made by the library's
+    copy kernel on that many SMs, which the plans leave free (gbo_h2d_copy:
+    SM loads of the page-locked host buffers); 0: by the copy engine
+    (cudaMemcpyAsync through torch)."""
     import torch
-    from adamw_optimizer_step_gb300 import hostmem
+    from adamw_optimizer_step_gb300 import _binding, hostmem
     g_flat, ag_flat = bufs[0]
     # page-locked host buffers on huge pages (hostmem: fewer and shorter
     # copy stalls than the driver's small-page pinned memory)
@@ -315,10 +323,15 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum):
         if timed is not None:  # the copies' own duration on the copy stream
             ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ev0.record(copy)
-        with torch.cuda.stream(copy):
-            bufs[b][0].copy_(h_g, non_blocking=True)
+        if copy_blocks:
+            _binding.gbo_h2d_copy(bufs[b][0], h_g, blocks=copy_blocks, stream=copy)
             copied[b].record(copy)
-            bufs[b][1].copy_(h_ag, non_blocking=True)
+            _binding.gbo_h2d_copy(bufs[b][1], h_ag, blocks=copy_blocks, stream=copy)
+        else:
+            with torch.cuda.stream(copy):
+                bufs[b][0].copy_(h_g, non_blocking=True)
+                copied[b].record(copy)
+                bufs[b][1].copy_(h_ag, non_blocking=True)
         copied_adam[b].record(copy)
         if timed is not None:
             ev1.record(copy)
@@ -657,8 +670,12 @@ def run_ours(args):
         plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon, workspace_cap=cap)
         bound.append((plan2, params2, [p[1] for p in params2]))
         gbo.gbo_muon_plan_set_event(plan2, 0, after_momentum[1])
+        if args.e2e_copy == "kernel":  # the copy kernel's SMs stay free of the GEMMs
+            for pl in (plan, plan2):
+                gbo.gbo_muon_plan_set_free_sms(pl, args.e2e_copy_sms)
         e2e_value, h2d, up_gbs, e2e_wall, e2e_diag = run_e2e(
-            args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total, after_momentum)
+            args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total, after_momentum,
+            copy_blocks=args.e2e_copy_sms if args.e2e_copy == "kernel" else 0)
 
     if rank != 0:
         return
@@ -746,6 +763,10 @@ def run_ours(args):
                                                "overlap": "step n+1's gradient upload runs during step n "
                                                           "(two gradient buffers)",
                                                "host_buffers": "page-locked, huge-page backed (hostmem)",
+                                               "upload": ("copy kernel on %d SMs the plans leave free "
+                                                          "(gbo_h2d_copy: SM loads over the C2C link)"
+                                                          % args.e2e_copy_sms if args.e2e_copy == "kernel"
+                                                          else "copy engine (cudaMemcpyAsync)"),
                                                "upload_GBps_alone": up_gbs,
                                                "upload_ms_alone": None if not up_gbs else h2d / up_gbs / 1e6,
                                                "steps": len(e2e_wall),

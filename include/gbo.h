@@ -326,6 +326,36 @@ typedef struct {
 int gbo_adamw_step(const gbo_adamw_desc *descs, int32_t n, const gbo_adamw_opts *opts,
                    const float *dev_coef, int32_t *dev_status, gbo_stream_t stream);
 
+/* ---- host-to-device transfer -------------------------------------------- */
+
+/*
+ * gbo_h2d_copy -- copy nbytes from page-locked host memory to device memory
+ * with a kernel whose threads load the host memory over the chip-to-chip
+ * link, instead of a copy engine.  The source pages have no counterpart:
+ * this moves a step's inputs (the gradients) onto the device.
+ *
+ * On a GB300 host both routes move ~200 GB/s, but copy-engine uploads of a
+ * few GB stall now and then for tens to hundreds of milliseconds; this
+ * kernel's did not.  It runs `blocks` blocks of 1024 threads (0: one per
+ * SM), each holding a whole SM to itself: a block reserves more than half
+ * of an SM's shared memory, so no SM runs two of them or one beside a
+ * Newton-Schulz CTA.  To overlap the copy with a step, leave that many SMs
+ * free in the step's plan (gbo_muon_plan_set_free_sms).  Measured on a
+ * GB300: a block moves ~50 GB/s alone (four: ~200 GB/s, the link's rate),
+ * ~27 GB/s beside a step's GEMMs.
+ *   dst     device memory, 16-byte aligned, nbytes writable
+ *   src     page-locked host memory mapped for the device (cudaHostRegister,
+ *           cudaMallocHost, or pinned tensors), 16-byte aligned; the
+ *           first and last byte are checked
+ *   nbytes  >= 0; any size (the last nbytes % 16 are copied bytewise)
+ *   blocks  >= 0
+ * Asynchronous on `stream`, like cudaMemcpyAsync: src must stay valid and
+ * unchanged, and dst unread, until the stream reaches the copy.  The caller
+ * owns both buffers.  Errors: INVALID_ARG (NULL, misaligned, negative size
+ * or blocks, src not page-locked and mapped, dst not device memory), CUDA.
+ */
+int gbo_h2d_copy(void *dst, const void *src, int64_t nbytes, int32_t blocks, gbo_stream_t stream);
+
 /* ---- diagnostics ---------------------------------------------------------- */
 
 /* Message for the last non-zero return on this host thread ("" if none). */
@@ -414,6 +444,16 @@ int gbo_muon_plan_set_stats(gbo_plan *plan, float *dev_stats);
  * gradients) overlaps the Newton-Schulz GEMMs.  Errors: INVALID_ARG.
  */
 int gbo_muon_plan_set_event(gbo_plan *plan, int32_t phase, void *event);
+/*
+ * Leave n SMs free of the persistent Newton-Schulz kernels in every later
+ * gbo_muon_step: the CTA-pair kernel then runs at most (SMs - n) / 2 pairs,
+ * the single-CTA and chain kernels at most SMs - n CTAs, so that work on
+ * another stream that needs whole SMs (gbo_h2d_copy with n blocks) runs
+ * beside the step.  The results do not change (each output element sums
+ * the same products in the same order); the GEMMs lose about n / SMs of
+ * their rate.  0 <= n <= 64; default 0.  Errors: INVALID_ARG.
+ */
+int gbo_muon_plan_set_free_sms(gbo_plan *plan, int32_t n);
 int gbo_muon_plan_set_timing(gbo_plan *plan, int32_t enable);
 int gbo_muon_plan_phase_times(gbo_plan *plan, float *ms, int64_t *launches, int32_t n_phases);
 

@@ -68,6 +68,15 @@ int32_t gbo_testing_set_fused_momentum(int32_t enable);
  */
 int32_t gbo_testing_set_tail_split(int32_t enable);
 
+/*
+ * How many CTA pairs (2-CTA clusters) of the bf16 Newton-Schulz kernel the
+ * current device holds at once: the persistent grid of its pair launches.
+ * Where the device's SMs do not all pair up within their clusters'
+ * placement groups, the rest stay free while those launches run.  -1 on a
+ * CUDA error (no device).
+ */
+int32_t gbo_testing_pair_residency(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,9 +40,10 @@ def ulp(x, dtype):
     return np.exp2(e - mant)
 
 
-def run_muon_gpu(entries, *, lr, precision, steps=1, dbg=True, **opts):
+def run_muon_gpu(entries, *, lr, precision, steps=1, dbg=True, free_sms=0, **opts):
     """Copy ``entries`` (CPU tensors) to the GPU, run ``steps`` Muon steps,
-    return CPU results: list of dicts W, B, v, U plus the status word."""
+    return CPU results: list of dicts W, B, v, U plus the status word.
+    ``free_sms``: SMs the plan's Newton-Schulz kernels leave free."""
     dev = []
     for e in entries:
         d = dict(e)
@@ -52,6 +53,8 @@ def run_muon_gpu(entries, *, lr, precision, steps=1, dbg=True, **opts):
         dev.append(d)
     plan = B.gbo_muon_plan_create(dev, precision=B.GBO_NS_F32 if precision == "f32" else B.GBO_NS_BF16,
                                   **opts)
+    if free_sms:
+        B.gbo_muon_plan_set_free_sms(plan, free_sms)
     ws = torch.empty(max(1, B.gbo_muon_workspace_bytes(plan)), dtype=torch.uint8, device="cuda")
     total = sum(e["w"].numel() for e in entries)
     U = torch.full((total,), float("nan"), dtype=torch.float32, device="cuda") if dbg else None

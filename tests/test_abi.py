@@ -356,6 +356,32 @@ def test_step_without_device_reports_error(L):
     L.gbo_muon_plan_destroy(plan)
 
 
+def test_h2d_copy_argument_refusals(L):
+    """gbo_h2d_copy checks its arguments before it touches a device."""
+    assert L.gbo_h2d_copy(FAKE, FAKE, 0, 0, None) == 0
+    assert L.gbo_h2d_copy(FAKE, FAKE, -1, 0, None) == -1
+    assert L.gbo_h2d_copy(FAKE, FAKE, 16, -1, None) == -1
+    assert L.gbo_h2d_copy(None, FAKE, 16, 0, None) == -1
+    assert L.gbo_h2d_copy(FAKE, None, 16, 0, None) == -1
+    assert L.gbo_h2d_copy(FAKE + 8, FAKE, 16, 0, None) == -1
+    assert L.gbo_h2d_copy(FAKE, FAKE + 4, 16, 0, None) == -1
+    import torch
+    if not torch.cuda.is_available():
+        assert L.gbo_h2d_copy(FAKE, FAKE, 16, 4, None) in (-7, -8)
+
+
+def test_free_sms_setting(L):
+    """gbo_muon_plan_set_free_sms takes 0 .. 64 and refuses the rest."""
+    _, plan = create(L, [desc(0, 8, 8)])
+    assert L.gbo_muon_plan_set_free_sms(plan, 0) == 0
+    assert L.gbo_muon_plan_set_free_sms(plan, 4) == 0
+    assert L.gbo_muon_plan_set_free_sms(plan, 64) == 0
+    assert L.gbo_muon_plan_set_free_sms(plan, -1) == -1
+    assert L.gbo_muon_plan_set_free_sms(plan, 65) == -1
+    assert L.gbo_muon_plan_set_free_sms(None, 4) == -1
+    L.gbo_muon_plan_destroy(plan)
+
+
 def test_fused_momentum_eligibility(L):
     """Which matrices run their momentum pass inside the chain launch: wide
     (rows <= cols) matrices of at most 128 rows on the on-chip Gram, with

@@ -625,3 +625,23 @@ def test_tail_split_bitwise(shape, normuon):
             assert torch.equal(a["v"], b["v"])
     ora = run_muon_oracle(entries, lr=0.02, normuon=normuon, beta2=0.95, eps=1e-8)
     check_muon(entries, one, ora, lr=0.02, precision="bf16")
+
+
+@pytest.mark.parametrize("free_sms", [4, 37])
+def test_free_sms_bitwise(free_sms):
+    """A plan that leaves SMs free runs its persistent kernels on fewer CTAs
+    (CTA pairs, single CTAs and the on-chip chain, with a workspace cap's
+    groups): the results are bitwise those of the whole device."""
+    shapes = [(2048, 2048, None, None), (1536, 384, None, None), (4 * 96, 1000, (4, 96, 1000), None),
+              (2 * 192, 1536, (2, 192, 1536), None), (130, 600, None, None), (64, 64, None, None)]
+    entries = random_entries(shapes, seed=53, b_std=1e-3)
+    kw = dict(lr=0.02, precision="bf16", steps=2)
+    whole, st0, plan0 = run_muon_gpu(entries, **kw)
+    part, st1, _ = run_muon_gpu(entries, free_sms=free_sms, **kw)
+    full = B.gbo_muon_workspace_bytes(plan0)
+    capped, st2, plan2 = run_muon_gpu(entries, free_sms=free_sms, workspace_cap=int(full * 0.85), **kw)
+    assert st0 == 0 and st1 == 0 and st2 == 0
+    assert B.gbo_muon_plan_info(plan2)["launches_per_step"] > B.gbo_muon_plan_info(plan0)["launches_per_step"]
+    for a, b, c in zip(whole, part, capped):
+        for k in ("W", "B", "U"):
+            assert torch.equal(a[k], b[k]) and torch.equal(a[k], c[k]), k
