@@ -135,7 +135,9 @@ __device__ __forceinline__ void adam_elem(float &p, float g, float &m, float &v,
   m = fmaf(s.beta1, m, (1.0f - s.beta1) * gg);
   v = fmaf(s.beta2, v, (1.0f - s.beta2) * gg * gg);
   const float denom = sqrtf(v) * s.inv_sqrt_bc2 + s.eps;
-  p = p - s.lr * s.wd * p - s.step_size * (m / denom);
+  // the decay and the Adam step summed first (at their own, small,
+  // magnitude), so p itself is rounded once
+  p = p + fmaf(-s.lr * s.wd, p, -s.step_size * (m / denom));
 }
 
 #ifndef GBO_ADAM_MIN_BLOCKS

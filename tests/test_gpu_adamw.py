@@ -50,6 +50,14 @@ def check(params, dev, *, lr, t, coef, wd=0.0, b1=0.9, b2=0.95, eps=1e-8):
         assert np.all(np.abs(f64(pd) - po) <= slack), "p mismatch"
 
 
+def test_adamw_with_decay_rounds_p_once():
+    """With weight decay the new p is the oracle's within one fp32 rounding
+    of p (decay and Adam step summed before they meet p)."""
+    params = tiny_params("random")
+    dev, _, coef, _ = run(params, lr=3e-4, t=5, wd=0.1)
+    check(params, [tuple(x.cpu() for x in d) for d in dev], lr=3e-4, t=5, coef=coef, wd=0.1)
+
+
 def tiny_params(state):
     wl = wk.workload(1)
     return [wk.adamw_tensor_inputs(wl, i, state=state) for i in range(len(wl.adamw))]
@@ -181,3 +189,4 @@ def test_device_step_in_cuda_graph():
     for a, b in zip(devs[0], devs[1]):
         for x, y in zip(a, b):
             assert torch.equal(x, y)
+
