@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--fused-momentum", action="store_true",
                     help="A/B: run the momentum pass of the chain's wide p <= 128 matrices inside the chain launch "
                          "instead of in the momentum kernel (workload 4; measured slower)")
+    ap.add_argument("--e2e-buffers", type=int, default=3,
+                    help="gradient buffer sets of the end-to-end run (each with its plan): uploads run up to "
+                         "this many steps minus one ahead of the step that uses them")
     ap.add_argument("--e2e-copy", choices=["kernel", "engine"], default="engine",
                     help="e2e uploads by the copy engine, or by the library's copy kernel (gbo_h2d_copy) on "
                          "--e2e-copy-sms SMs the plans leave free")
@@ -278,16 +281,18 @@ def traffic_record(kernel_files):
 
 def run_e2e(n_steps, world, bufs, step, total, after_momentum, copy_blocks=0):
     """Steps/s with each step's gradients copied in from pinned host memory
-    and the step's gradient norm read back on the host.  ``bufs`` holds two
-    (Muon, AdamW) flat gradient buffer pairs, each bound to its own plan:
-    the upload of step n + 1's gradients runs on a copy stream into one pair
-    while step n computes on the other, as a trainer overlaps its input
-    transfers: the Muon gradients first, which step n + 1 needs at its start,
-    then the AdamW gradients, which it needs only for its clip and AdamW
-    after its GEMMs.  The upload starts once step n's momentum pass is done
-    (``after_momentum[b]``, recorded by buffer pair b's plan), so it runs
-    under the Newton-Schulz GEMMs, which leave most of the HBM bandwidth
-    free, rather than under the memory-bound momentum pass.  Every step's
+    and the step's gradient norm read back on the host.  ``bufs`` holds K
+    (Muon, AdamW) flat gradient buffer sets, each bound to its own plan:
+    uploads run on a copy stream, in step order, up to K - 1 steps ahead of
+    the step that computes, as a trainer prefetches its inputs: the Muon
+    gradients first, which a step needs at its start, then the AdamW
+    gradients, which it needs only for its clip and AdamW after its GEMMs.
+    The upload enqueued with step n starts once step n's momentum pass is
+    done (``after_momentum[b]``, recorded by buffer set b's plan), so it
+    runs under the Newton-Schulz GEMMs, which leave most of the HBM
+    bandwidth free, rather than under the memory-bound momentum pass; with
+    K > 2 a copy that stalls is absorbed by the lead the uploads have built
+    up (each upload is shorter than a step).  Every step's
     copy and read stay inside the timed region.  Returns (steps/s over all
     ranks, bytes copied in per step, the upload's GB/s when it runs
     alone, each step's host wall time in ms up to its norm read).  A single
@@ -310,9 +315,10 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum, copy_blocks=0):
     h_ag.copy_(ag_flat)
     compute = torch.cuda.current_stream()
     copy = torch.cuda.Stream()
-    copied = [torch.cuda.Event(), torch.cuda.Event()]       # Muon gradients in
-    copied_adam = [torch.cuda.Event(), torch.cuda.Event()]  # AdamW gradients in
-    done = [torch.cuda.Event(), torch.cuda.Event()]
+    nb = len(bufs)
+    copied = [torch.cuda.Event() for _ in range(nb)]       # Muon gradients in
+    copied_adam = [torch.cuda.Event() for _ in range(nb)]  # AdamW gradients in
+    done = [torch.cuda.Event() for _ in range(nb)]
 
     def upload(b, after=None, timed=None):
         # the Muon gradients first: a step needs them at its start, its AdamW
@@ -361,16 +367,21 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum, copy_blocks=0):
     up_gbs = h2d / statistics.median(alone) / 1e9
 
     def run(n_run, wall=None, timed=None, enqueue=None):
-        upload(0, timed=timed)
+        # the uploads of steps 0 .. nb - 2 first; then, as step n is
+        # enqueued, the upload of step n + nb - 1 into the buffer set step
+        # n - 1 used (it starts once step n - 1 is done and step n's
+        # momentum pass is, and after the uploads before it)
+        for m in range(min(nb - 1, n_run)):
+            upload(m, timed=timed)
         t_prev = time.perf_counter()
         for n in range(n_run):
-            b = n % 2
+            b = n % nb
             t_q = time.perf_counter()
             compute.wait_event(copied[b])
             step(buf=b, before_adamw=copied_adam[b])
             done[b].record(compute)
-            if n + 1 < n_run:
-                upload(1 - b, after_momentum[b], timed=timed)
+            if n + nb - 1 < n_run:
+                upload((n + nb - 1) % nb, after_momentum[b], timed=timed)
             if enqueue is not None:
                 enqueue.append((time.perf_counter() - t_q) * 1e3)
             _ = read_result()  # the step's result on the host
@@ -380,7 +391,7 @@ def run_e2e(n_steps, world, bufs, step, total, after_momentum, copy_blocks=0):
                 t_prev = t_now
         torch.cuda.synchronize()
 
-    run(2)  # untimed: each buffer pair's plan runs once (its first step sets it up on the device)
+    run(nb)  # untimed: each buffer set's plan runs once (its first step sets it up on the device)
     barrier(world)
     wall, timed, enqueue = [], [], []
     t0 = time.perf_counter()
@@ -587,7 +598,7 @@ def run_ours(args):
     overlap = args.overlap
 
     # recorded by each buffer pair's plan right after its momentum pass
-    after_momentum = [torch.cuda.Event(), torch.cuda.Event()]
+    after_momentum = [torch.cuda.Event()]
     gbo.gbo_muon_plan_set_event(plan, 0, after_momentum[0])
 
     def step(record=None, buf=0, before_adamw=None):
@@ -657,24 +668,30 @@ def run_ours(args):
     # end to end: gradients from pinned host memory, norm read back
     e2e_value, h2d, up_gbs, e2e_wall, e2e_diag = None, 0, None, [], {}
     if args.e2e_steps > 0:
-        g_flat2, ag_flat2 = torch.empty_like(g_flat), torch.empty_like(ag_flat)
-        entries2, off = [], 0
-        for e in entries:
-            n = e["w"].numel()
-            entries2.append(dict(e, g=g_flat2[off:off + n].view(e["w"].shape)))
-            off += n
-        params2, off = [], 0
-        for p, g, m, v in params:
-            params2.append((p, ag_flat2[off:off + g.numel()].view(g.shape), m, v))
-            off += g.numel()
-        plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon, workspace_cap=cap)
-        bound.append((plan2, params2, [p[1] for p in params2]))
-        gbo.gbo_muon_plan_set_event(plan2, 0, after_momentum[1])
+        bufs = [(g_flat, ag_flat)]
+        plans = [plan]
+        for _ in range(1, args.e2e_buffers):  # one more gradient buffer set, and its plan, each
+            g_flat2, ag_flat2 = torch.empty_like(g_flat), torch.empty_like(ag_flat)
+            entries2, off = [], 0
+            for e in entries:
+                n = e["w"].numel()
+                entries2.append(dict(e, g=g_flat2[off:off + n].view(e["w"].shape)))
+                off += n
+            params2, off = [], 0
+            for p, g, m, v in params:
+                params2.append((p, ag_flat2[off:off + g.numel()].view(g.shape), m, v))
+                off += g.numel()
+            plan2 = gbo.gbo_muon_plan_create(entries2, precision=prec, normuon=wl.normuon, workspace_cap=cap)
+            after_momentum.append(torch.cuda.Event())
+            gbo.gbo_muon_plan_set_event(plan2, 0, after_momentum[len(bufs)])
+            bound.append((plan2, params2, [p[1] for p in params2]))
+            bufs.append((g_flat2, ag_flat2))
+            plans.append(plan2)
         if args.e2e_copy == "kernel":  # the copy kernel's SMs stay free of the GEMMs
-            for pl in (plan, plan2):
+            for pl in plans:
                 gbo.gbo_muon_plan_set_free_sms(pl, args.e2e_copy_sms)
         e2e_value, h2d, up_gbs, e2e_wall, e2e_diag = run_e2e(
-            args.e2e_steps, world, [(g_flat, ag_flat), (g_flat2, ag_flat2)], step, total, after_momentum,
+            args.e2e_steps, world, bufs, step, total, after_momentum,
             copy_blocks=args.e2e_copy_sms if args.e2e_copy == "kernel" else 0)
 
     if rank != 0:
@@ -760,8 +777,9 @@ def run_ours(args):
                       "executed_tflop_per_step": flops / 1e12, "counted_tflop_per_step": info["ns_flops"] / 1e12},
         "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "steps/s",
                                                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4,
-                                               "overlap": "step n+1's gradient upload runs during step n "
-                                                          "(two gradient buffers)",
+                                               "overlap": ("gradient uploads run up to %d steps ahead of the "
+                                                           "step that uses them (%d gradient buffer sets)"
+                                                           % (args.e2e_buffers - 1, args.e2e_buffers)),
                                                "host_buffers": "page-locked, huge-page backed (hostmem)",
                                                "upload": ("copy kernel on %d SMs the plans leave free "
                                                           "(gbo_h2d_copy: SM loads over the C2C link)"
