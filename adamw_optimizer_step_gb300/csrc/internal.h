@@ -162,7 +162,7 @@ int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float m
                     void *x0, void *x0t, int32_t x_dtype, float *partials, int sm_count, void *stream);
 // stats: nullptr, or where each matrix's ||D||_F goes (2 * mat_idx)
 int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials,
-                            float *alpha, int32_t *status, float *stats, void *stream);
+                            float *alpha, int32_t *status, float *stats, int sm_count, void *stream);
 // Per-matrix ||U||_F into stats[2 * mat_idx + 1]: from the last product's
 // per-(row, 128 columns) sums of U^2 (rowss), or with NorMuon from the rows
 // kernels' per-row-block sums of (1 / (sqrt(v) + eps))^2 ||X_i||^2 (rowpart).

@@ -186,41 +186,113 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
   }
 }
 
-// One block per matrix: combine the tile partials in a fixed order into
+// The finalize sums each matrix's partials as kFinLanes virtual lanes (lane v
+// takes partials v, v + kFinLanes, ... in order), then in a fixed tree: the
+// 32 lanes of each virtual warp, then the 32 warps.  A block of kT threads
+// runs kFinLanes / kT lanes per thread, so the sums do not depend on kT
+// (1024 threads when there are fewer matrices than SMs, so that a few large
+// matrices are reduced by many threads; 256 when there are many).  The max
+// comes first, from a block reduction (a max is the same in any order).
+constexpr int kFinLanes = 1024;
+
+// One block per matrix: combine the tile partials (max |D| and the sum of
+// (D / max)^2 of each warp's elements) in that fixed order into
 // alpha = 1 / (s * (||D / s||_F + 1e-7)), s = max(max|D|, 1e-7), so that
 // X0 = alpha * D.
-__global__ void __launch_bounds__(256)
+template <int kT>
+__global__ void __launch_bounds__(kT)
 prenorm_finalize_kernel(const DevSub *__restrict__ subs, const float *__restrict__ partials,
                         float *__restrict__ alpha, int32_t *status, float *__restrict__ stats) {
   pdl_launch();  // the next kernel may be scheduled as SMs free up
   pdl_wait();    // the previous kernel has completed and its writes are visible
+  constexpr int R = kFinLanes / kT;  // virtual lanes per thread
+  static_assert(R >= 1 && kFinLanes % kT == 0 && kFinLanes / 32 == 32, "lane layout");
   __shared__ float red[32];
   const DevSub &S = subs[blockIdx.x];
   if (S.mom_fused) return;  // the chain kernel forms this matrix's factor
   const int64_t nt = (int64_t)S.ntiles * kMomWarps;
-  const float *P = partials + 2 * S.tile0 * kMomWarps;
+  const float2 *P = reinterpret_cast<const float2 *>(partials) + S.tile0 * kMomWarps;
+  // the max, four partials in flight per thread
   float M = 0.f;
-  for (int64_t k = threadIdx.x; k < nt; k += blockDim.x) M = fmaxf(M, P[2 * k]);
+  {
+    int64_t k = threadIdx.x;
+    for (; k + 3 * kT < nt; k += 4 * kT) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = P[k + u * kT].x;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) M = fmaxf(M, v[u]);
+    }
+    for (; k < nt; k += kT) M = fmaxf(M, P[k].x);
+  }
   M = block_max(M, red);
-  float ss = 0.f;
+  // the sum of squares relative to M, lane by lane
+  float ss[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) ss[r] = 0.f;
   if (M > 0.f) {
     const float inv = 1.0f / M;
-    for (int64_t k = threadIdx.x; k < nt; k += blockDim.x) {
-      const float r = P[2 * k] * inv;
-      ss = fmaf(P[2 * k + 1], r * r, ss);
+    if constexpr (R == 1) {  // four of the lane's partials in flight, summed in order
+      int64_t k = threadIdx.x;
+      for (; k + 3 * kFinLanes < nt; k += 4 * kFinLanes) {
+        float2 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = P[k + u * kFinLanes];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float x = v[u].x * inv;
+          ss[0] = fmaf(v[u].y, x * x, ss[0]);
+        }
+      }
+      for (; k < nt; k += kFinLanes) {
+        const float2 v = P[k];
+        const float x = v.x * inv;
+        ss[0] = fmaf(v.y, x * x, ss[0]);
+      }
+    } else {  // one partial of each of the thread's R lanes in flight
+      for (int64_t k = threadIdx.x; k < nt; k += kFinLanes) {
+        float2 v[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (k + r * kT < nt) v[r] = P[k + r * kT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (k + r * kT < nt) {
+            const float x = v[r].x * inv;
+            ss[r] = fmaf(v[r].y, x * x, ss[r]);
+          }
+      }
     }
   }
-  ss = block_sum(ss, red);
-  if (threadIdx.x == 0) {
+  // each virtual warp's 32 lanes (the physical warp's lanes), then the
+  // warps; warps without partials hold zeros and skip their shuffles
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();  // red is free again
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int vw = warp + r * (kT / 32);
+    float t = ss[r];
+    if ((int64_t)vw * 32 < nt) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+    }
+    if (lane == 0) red[vw] = t;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float t = red[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+  if (lane == 0) {
     const float s = fmaxf(M, 1e-7f);
-    const float normY = (M / s) * sqrtf(ss);
+    const float normY = (M / s) * sqrtf(t);
     float a = 1.0f / (s * (normY + 1e-7f));
-    if (!isfinite(M) || !isfinite(ss) || !isfinite(a)) {
+    if (!isfinite(M) || !isfinite(t) || !isfinite(a)) {
       flag_status(status, GBO_STATUS_NONFINITE);
       a = __int_as_float(0x7fc00000);
     }
     alpha[blockIdx.x] = a;
-    if (stats) stats[2 * S.mat_idx] = M > 0.f ? M * sqrtf(ss) : (isfinite(M) ? 0.f : M);  // ||D||_F
+    if (stats) stats[2 * S.mat_idx] = M > 0.f ? M * sqrtf(t) : (isfinite(M) ? 0.f : M);  // ||D||_F
   }
 }
 
@@ -775,11 +847,15 @@ int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float m
 }
 
 int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials, float *alpha,
-                            int32_t *status, float *stats, void *stream) {
+                            int32_t *status, float *stats, int sm_count, void *stream) {
   if (n_subs == 0) return 0;
-  const cudaError_t err = launch_kernel(prenorm_finalize_kernel, dim3(n_subs), dim3(256), 0,
-                                        reinterpret_cast<cudaStream_t>(stream), 1, subs, partials, alpha, status,
-                                        stats);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t err =
+      n_subs < sm_count
+          ? launch_kernel(prenorm_finalize_kernel<1024>, dim3(n_subs), dim3(1024), 0, st, 1, subs, partials, alpha,
+                          status, stats)
+          : launch_kernel(prenorm_finalize_kernel<256>, dim3(n_subs), dim3(256), 0, st, 1, subs, partials, alpha,
+                          status, stats);
   count_launches(1);
   return (int)err;
 }

@@ -1117,7 +1117,7 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
                             partials, P->sm_count, st);
   if (err) return cuda_fail(err, "momentum kernel");
   if (P->n_unfused > 0) {
-    err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, P->stats, st);
+    err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, P->stats, P->sm_count, st);
     if (err) return cuda_fail(err, "pre-normalisation kernel");
   }
   mark(kPhaseMomentum, (P->n_tiles > 0) + (P->n_unfused > 0), !P->any_mom_fused);

@@ -645,3 +645,24 @@ def test_free_sms_bitwise(free_sms):
     for a, b, c in zip(whole, part, capped):
         for k in ("W", "B", "U"):
             assert torch.equal(a[k], b[k]) and torch.equal(a[k], c[k]), k
+
+
+def test_prenorm_finalize_independent_of_block_size():
+    """The pre-normalisation factors reduce each matrix's partials as 1024
+    virtual lanes in a fixed tree, run by 256-thread blocks when the table
+    has at least as many matrices as SMs and by 1024-thread blocks when it
+    has fewer: a table of 170 matrices and the same table stepped in
+    capped groups of fewer matrices give the same bits."""
+    shapes = [(2048, 2048, None, None)] + [(96, 320, None, None)] * 168 + [(1024, 3000, None, None)]
+    entries = random_entries(shapes, seed=59, b_std=1e-3)
+    kw = dict(lr=0.02, precision="bf16", steps=1)
+    whole, st0, plan0 = run_muon_gpu(entries, **kw)
+    full = B.gbo_muon_workspace_bytes(plan0)
+    groups, st1, plan1 = run_muon_gpu(entries, workspace_cap=int(full * 0.6), **kw)
+    assert st0 == 0 and st1 == 0
+    assert B.gbo_muon_plan_info(plan1)["launches_per_step"] > B.gbo_muon_plan_info(plan0)["launches_per_step"]
+    for a, b in zip(whole, groups):
+        for k in ("W", "B", "U"):
+            assert torch.equal(a[k], b[k]), k
+    ora = run_muon_oracle(entries[:1] + entries[-1:], lr=0.02)
+    check_muon(entries[:1] + entries[-1:], whole[:1] + whole[-1:], ora, lr=0.02, precision="bf16")
