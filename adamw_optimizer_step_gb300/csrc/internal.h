@@ -227,19 +227,24 @@ double tc_chain_flops(int p, int k, const float *abc);
 // FLOPs the tensor-core kernel executes for one p x q matrix and one
 // iteration (Gram over the upper block-triangle of tiles, square when c != 0,
 // product), counting the zero padding of partial tiles; `tall`: X is held
-// q x p and the product runs transposed.
-double tc_executed_flops(int p, int q, bool square, bool tall);
+// q x p and the product runs transposed; `final`: the product is the
+// weight-writing last one (see single_job).
+double tc_executed_flops(int p, int q, bool square, bool tall, bool final);
 // FLOPs executed for one p x q matrix over k iterations on the Gram route:
 // the Gram, 3k - 3 symmetric p x p products plus one square of A for each
 // of `squares` iterations with c != 0, the product with X_0.
-double tc_gram_route_flops(int p, int q, int k, int squares, bool tall);
+double tc_gram_route_flops(int p, int q, int k, int squares, bool tall, bool final);
 // The same when the p x p chain runs on chip: the Gram (and the square of
 // A_0 when c_0 != 0) on the tile kernel or, `fused`, on chip, the chain,
 // the product with X_0.
-double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall, bool fused);
+double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall, bool fused, bool final);
 // Whether the tensor-core kernel runs a shape class of p oriented rows on
 // single CTAs (p <= 128) rather than on CTA pairs.
 bool single_mode(int p);
+// Whether a job of that class in epilogue mode `mode` runs on single CTAs:
+// single_mode(p), or the weight-writing last product (kFinal) of a class of
+// at most 256 rows.
+bool single_job(int p, int32_t mode);
 // The bf16 pair kernel's tail split on (1, the default) or off; returns the
 // previous setting (gbo_testing_set_tail_split).
 int32_t set_tail_split(int32_t enable);

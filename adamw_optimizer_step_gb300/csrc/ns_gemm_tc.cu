@@ -584,55 +584,66 @@ ns_gemm_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ Ph
 // pairs.
 bool single_mode(int p) { return p <= BM; }
 
+// The weight-writing last product of a class of at most 256 rows runs on
+// single CTAs too: with K = p its MMAs are short, its HBM-bound weight
+// traffic is what limits it, and the single-CTA kernel has twice the
+// epilogue warps per SM to hide that traffic's latency.
+bool single_job(int p, int32_t mode) { return p <= BM || (mode == kFinal && p <= 2 * BM); }
+
 namespace {
 
-// Work items of one matrix of a class with p oriented rows: kRows
-// consecutive 128-row tiles x one column tile, over an output of `rows`
-// rows; in pair mode an odd tile-row count runs one all-padding tile in the
-// last pair.
-int items_m_of(int p, int rows) {
-  const int k = single_mode(p) ? 1 : 2;
+// Work items of one matrix: kRows consecutive 128-row tiles (1 on single
+// CTAs, 2 on pairs) x one column tile, over an output of `rows` rows; in
+// pair mode an odd tile-row count runs one all-padding tile in the last
+// pair.
+int items_m_of(bool single, int rows) {
+  const int k = single ? 1 : 2;
   return ((rows + BM - 1) / BM + k - 1) / k;
 }
 
 int64_t sym_items_of(int p) {
-  const int rows = single_mode(p) ? 1 : 2;
+  const bool single = single_mode(p);
+  const int rows = single ? 1 : 2;
   const int tiles_n = (p + BN - 1) / BN;
   int64_t n = 0;
-  for (int r = 0; r < items_m_of(p, p); ++r) n += std::max(0, tiles_n - tri_tn_min(rows * r));
+  for (int r = 0; r < items_m_of(single, p); ++r) n += std::max(0, tiles_n - tri_tn_min(rows * r));
   return n;
 }
 
-double item_flops(int p, int kdim) {  // one work item: rows x 128 x 256 outputs, K padded to a stage
-  const int rows = single_mode(p) ? 1 : 2;
+double item_flops(bool single, int kdim) {  // one work item: rows x 128 x 256 outputs, K padded to a stage
+  const int rows = single ? 1 : 2;
   const int kstage = rows * BK;  // pairs stage two BK-wide blocks, single CTAs one
   return 2.0 * rows * BM * BN * (double)((kdim + kstage - 1) / kstage) * kstage;
 }
 
-// The p x q product (wide: p x q output) or its transpose (tall: q x p).
-double product_flops(int p, int q, bool tall) {
-  return tall ? (double)items_m_of(p, q) * ((p + BN - 1) / BN) * item_flops(p, p)
-              : (double)items_m_of(p, p) * ((q + BN - 1) / BN) * item_flops(p, p);
+double item_flops(int p, int kdim) { return item_flops(single_mode(p), kdim); }
+
+// The p x q product (wide: p x q output) or its transpose (tall: q x p);
+// `final`: the weight-writing last product.
+double product_flops(int p, int q, bool tall, bool final) {
+  const bool single = single_job(p, final ? kFinal : kProduct);
+  return tall ? (double)items_m_of(single, q) * ((p + BN - 1) / BN) * item_flops(single, p)
+              : (double)items_m_of(single, p) * ((q + BN - 1) / BN) * item_flops(single, p);
 }
 
 }  // namespace
 
-double tc_executed_flops(int p, int q, bool square, bool tall) {
+double tc_executed_flops(int p, int q, bool square, bool tall, bool final) {
   double f = sym_items_of(p) * item_flops(p, q);                  // Gram, K = q
   if (square) f += sym_items_of(p) * item_flops(p, p);            // A A
-  return f + product_flops(p, q, tall);                           // product, K = p
+  return f + product_flops(p, q, tall, final);                    // product, K = p
 }
 
-double tc_gram_route_flops(int p, int q, int k, int squares, bool tall) {
+double tc_gram_route_flops(int p, int q, int k, int squares, bool tall, bool final) {
   return sym_items_of(p) * item_flops(p, q) + (3.0 * k - 3.0 + squares) * sym_items_of(p) * item_flops(p, p) +
-         product_flops(p, q, tall);
+         product_flops(p, q, tall, final);
 }
 
-double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall, bool fused) {
+double tc_gram_chain_flops(int p, int q, int k, const float *abc, bool tall, bool fused, bool final) {
   const double gram = fused ? tc_fused_gram_flops(p, q, abc)
                             : sym_items_of(p) * item_flops(p, q) +
                                   (abc[2] != 0.f ? sym_items_of(p) * item_flops(p, p) : 0.0);
-  return gram + tc_chain_flops(p, k, abc) + product_flops(p, q, tall);
+  return gram + tc_chain_flops(p, k, abc) + product_flops(p, q, tall, final);
 }
 
 namespace {
@@ -865,7 +876,7 @@ int launch_ns_gemm_tc(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &glob
   for (int32_t j = 0; j < n_jobs; ++j) {
     if (jobs[j].cls->count == 0) continue;
     if (jobs[j].mode == kChain) chain.push_back(&jobs[j]);
-    else (single_mode(jobs[j].cls->p) ? single : pair).push_back(&jobs[j]);
+    else (single_job(jobs[j].cls->p, jobs[j].mode) ? single : pair).push_back(&jobs[j]);
   }
   int err = launch_mode<true>(pair.data(), (int32_t)pair.size(), globals, sm_count, stream, n_launch);
   if (err) return err;

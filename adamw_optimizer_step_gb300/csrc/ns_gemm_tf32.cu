@@ -620,7 +620,7 @@ int launch_ns_gemm_tf32(const GemmJob *jobs, int32_t n_jobs, const PhaseArgs &gl
   std::vector<const GemmJob *> single, pair;
   for (int32_t j = 0; j < n_jobs; ++j) {
     if (jobs[j].cls->count == 0) continue;
-    (single_mode(jobs[j].cls->p) ? single : pair).push_back(&jobs[j]);
+    (single_job(jobs[j].cls->p, jobs[j].mode) ? single : pair).push_back(&jobs[j]);
   }
   int err = launch_mode_f32<true>(pair.data(), (int32_t)pair.size(), globals, sm_count, stream, n_launch);
   if (err) return err;

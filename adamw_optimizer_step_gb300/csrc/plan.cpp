@@ -211,11 +211,12 @@ int32_t choose_route(const gbo_plan *P, int p, int q, bool tall) {
   if (k < 2 || P->opts.route == GBO_ROUTE_X) return kRouteX;
   if (P->opts.route == GBO_ROUTE_GRAM) return kRouteGram;
   const bool x_tall = P->x_dtype == GBO_BF16 && tall;
+  const bool fin = !P->opts.normuon;  // the last product writes the weights (NorMuon: X, for the rows pass)
   double fx = 0;
-  for (int it = 0; it < k; ++it) fx += tc_executed_flops(p, q, P->abc[3 * it + 2] != 0.f, x_tall);
+  for (int it = 0; it < k; ++it) fx += tc_executed_flops(p, q, P->abc[3 * it + 2] != 0.f, x_tall, fin && it == k - 1);
   const bool chain = P->small_chain && P->x_dtype == GBO_BF16 && p <= kChainMaxP;
-  const double fg = chain ? tc_gram_chain_flops(p, q, k, P->abc.data(), x_tall, fuses_gram(P, p))
-                          : tc_gram_route_flops(p, q, k, squares(P), x_tall);
+  const double fg = chain ? tc_gram_chain_flops(p, q, k, P->abc.data(), x_tall, fuses_gram(P, p), fin)
+                          : tc_gram_route_flops(p, q, k, squares(P), x_tall, fin);
   return fg < 0.9 * fx ? kRouteGram : kRouteX;
 }
 
@@ -520,14 +521,15 @@ int validate_and_expand(gbo_plan *P) {
     for (size_t k = 0; k < P->classes.size(); ++k) {
       const ShapeClass &C = P->classes[k];
       double per = 0;  // one matrix of the class
+      const bool fin = !o.normuon;  // the last product writes the weights
       if (C.route == kRouteGram) {
         per = uses_chain(P, C) ? tc_gram_chain_flops(C.p, C.q, o.ns_steps, P->abc.data(), C.x_tall != 0,
-                                                     fuses_gram(P, C))
-                               : tc_gram_route_flops(C.p, C.q, o.ns_steps, squares(P), C.x_tall != 0);
+                                                     fuses_gram(P, C), fin)
+                               : tc_gram_route_flops(C.p, C.q, o.ns_steps, squares(P), C.x_tall != 0, fin);
         I.n_gram_route += C.count;
       } else {
         for (int it = 0; it < o.ns_steps; ++it)
-          per += tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f, C.x_tall != 0);
+          per += tc_executed_flops(C.p, C.q, P->abc[3 * it + 2] != 0.f, C.x_tall != 0, fin && it == o.ns_steps - 1);
       }
       P->class_flops[k] = per;
       ex += C.count * per;
@@ -727,7 +729,7 @@ int64_t tc_step_launches(const TcStep &st) {
   int64_t single = 0, pair = 0, chain[kChainGeometries] = {};
   for (const GemmJob &J : st.jobs) {
     if (J.mode == kChain) ++chain[chain_geometry(J)];
-    else (single_mode(J.cls->p) ? single : pair)++;
+    else (single_job(J.cls->p, J.mode) ? single : pair)++;
   }
   auto groups = [](int64_t n) { return (n + kMaxClassesPerLaunch - 1) / kMaxClassesPerLaunch; };
   int64_t n = groups(single) + groups(pair);

@@ -209,9 +209,11 @@ def test_flop_count_and_launches(L):
     # Gram and square on chip), then the product on single CTAs; p = 150:
     # the Gram (and the square of A_0) on CTA pairs, the chain, the product.
     # The chain from X_0 runs in the step of the other chain, so the products
-    # share a step.  Launches by step, cubic: {Gram}, {both chains}, {both
-    # products}; quintic: {Gram}, {square}, {both chains}, {both products}
-    for abc, launches in (((1.5, -0.5, 0.0), 2 + 1 + 2 + 2), ((15 / 8, -5 / 4, 3 / 8), 2 + 1 + 1 + 2 + 2)):
+    # share a step, and one single-CTA launch (the weight-writing last product
+    # of a class of at most 256 rows runs on single CTAs).  Launches by step,
+    # cubic: {Gram}, {both chains}, {both products}; quintic: {Gram},
+    # {square}, {both chains}, {both products}
+    for abc, launches in (((1.5, -0.5, 0.0), 2 + 1 + 2 + 1), ((15 / 8, -5 / 4, 3 / 8), 2 + 1 + 1 + 2 + 1)):
         rc, plan = create(L, [desc(0, 64, 64), desc(1, 150, 150)], abc=abc)
         i = info(L, plan)
         assert i.n_gram_route == 2 and i.launches_per_step == launches
@@ -300,14 +302,17 @@ def test_small_chain_counts(L):
     assert i.ns_flops_executed == 2 * 128 * 128 * 256 + cubic_chain + 2 * tile * 128  # 200 output rows: two tiles
     L.gbo_muon_plan_destroy(plan)
     # 128 < p <= 192: two 128-row halves with N = 192, T and Q as separate
-    # products: T, A_1/P_1, 3 x (T, Q, A/P), Q_5; the Gram and the product
-    # with X_0 run on CTA pairs (256 x 256 tiles, K padded to 128)
+    # products: T, A_1/P_1, 3 x (T, Q, A/P), Q_5; the Gram runs on CTA pairs
+    # (256 x 256 tiles, K padded to 128), the weight-writing product with X_0
+    # on single CTAs (two 128-row tiles x 6 column tiles, K = 192 in 64-wide
+    # blocks)
     rc, plan = create(L, [desc(0, 2 * 192, 1536, (2, 192, 1536))], route=B.GBO_ROUTE_GRAM)
     i = info(L, plan)
     pair = 2 * 256 * 256
+    single = 2 * 128 * 256
     chain192 = 12 * 2 * (2 * 128 * 192 * 192)
     assert i.launches_per_step == 2 + 3
-    assert i.ns_flops_executed == 2 * (pair * 1536 + chain192 + 6 * pair * 256)
+    assert i.ns_flops_executed == 2 * (pair * 1536 + chain192 + 12 * single * 192)
     L.gbo_muon_plan_destroy(plan)
     # the fp32 mode and larger p keep one launch per product
     rc, plan = create(L, d(), route=B.GBO_ROUTE_GRAM, precision=B.GBO_NS_F32)
