@@ -115,6 +115,7 @@ def lib():
         "gbo_testing_set_fused_momentum": (c_int32, [c_int32]),
         "gbo_testing_set_tail_split": (c_int32, [c_int32]),
         "gbo_testing_pair_residency": (c_int32, []),
+        "gbo_testing_set_pdl": (c_int32, [c_int32]),
         "gbo_last_error": (ctypes.c_char_p, []),
         "gbo_abi_version": (c_int32, []),
         "gbo_struct_size": (c_size_t, [c_int32]),
@@ -467,6 +468,12 @@ def gbo_testing_pair_residency():
     """CTA pairs of the bf16 Newton-Schulz kernel the current device holds at
     once (its pair launches' persistent grid)."""
     return int(lib().gbo_testing_pair_residency())
+
+
+def gbo_testing_set_pdl(enable):
+    """Whether launches from now on carry the programmatic-dependent-launch
+    attribute (off by default).  Returns the previous setting."""
+    return bool(lib().gbo_testing_set_pdl(1 if enable else 0))
 
 
 def gbo_testing_wait_timeout(dev_status, limit_us, stream=None):

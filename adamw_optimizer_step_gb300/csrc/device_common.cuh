@@ -12,20 +12,22 @@
 
 namespace gbo {
 
-// Programmatic dependent launch.  Every kernel of the library is launched
-// with cudaLaunchAttributeProgrammaticStreamSerialization (launch_kernel
-// below), so it may be scheduled while the kernel before it on the stream
-// is still finishing: each kernel calls pdl_launch() as it starts, letting
-// the next one be scheduled as SMs free up, and pdl_wait() after its
-// prologue (barrier set-up, TMEM allocation) and before its first access to
-// global memory, which returns once the previous kernel has completed and
-// its writes are visible.  A kernel that follows a launch from elsewhere has
-// no such dependency, and pdl_wait() returns at once.
+// Programmatic dependent launch.  Every kernel of the library calls
+// pdl_launch() as it starts, letting the next kernel on the stream be
+// scheduled as SMs free up, and pdl_wait() after its prologue (barrier
+// set-up, TMEM allocation) and before its first access to global memory,
+// which returns once the previous kernel has completed and its writes are
+// visible.  These take effect only when the launch carries
+// cudaLaunchAttributeProgrammaticStreamSerialization, which launch_kernel
+// below sets when pdl_enabled() (gbo_testing_set_pdl; off by default: on a
+// GB300 it made the many-small-matrix step 12.7% slower, the dependent
+// grids' early CTAs holding SMs that the kernel before them still needed,
+// and gained nothing measurable elsewhere).  Without it both return at once.
 __device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Launch `kernel` with programmatic stream serialization (and, with
-// cluster > 1, clusters of that many CTAs along x).
+// Launch `kernel` (with programmatic stream serialization when enabled, and,
+// with cluster > 1, clusters of that many CTAs along x).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                                  int cluster, Args &&...args) {
@@ -37,7 +39,7 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
   cfg.stream = stream;
   int n = 0;
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  attr[n].val.programmaticStreamSerializationAllowed = pdl_enabled();
   ++n;
   if (cluster > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;

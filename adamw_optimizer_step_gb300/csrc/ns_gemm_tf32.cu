@@ -593,13 +593,13 @@ int launch_mode_f32(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs 
     } else {
       cfg.gridDim = dim3((unsigned)std::min<int64_t>(total, sm_count));
     }
-    // programmatic stream serialization (this kernel waits for the previous
-    // one after its prologue), and the pair's cluster
+    // programmatic stream serialization when enabled (this kernel waits for
+    // the previous one after its prologue), and the pair's cluster
     cudaLaunchAttribute attrs[2];
     int na = 0;
     if (kPair) attrs[na++] = attr[0];
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    attrs[na].val.programmaticStreamSerializationAllowed = pdl_enabled();
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = na;

@@ -29,6 +29,8 @@ static std::atomic<int32_t> g_small_chain{1};  // see gbo_testing_set_small_chai
 static std::atomic<int32_t> g_fused_gram{1};   // see gbo_testing_set_fused_gram
 static std::atomic<int32_t> g_fused_mom{0};    // see gbo_testing_set_fused_momentum (off: measured slower)
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+static std::atomic<int32_t> g_pdl{0};  // see gbo_testing_set_pdl (off: measured slower)
+int32_t pdl_enabled() { return g_pdl.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -1198,6 +1200,8 @@ int32_t gbo_testing_set_fused_momentum(int32_t enable) { return g_fused_mom.exch
 int32_t gbo_testing_set_tail_split(int32_t enable) { return gbo::set_tail_split(enable); }
 
 int32_t gbo_testing_pair_residency(void) { return gbo::pair_residency(); }
+
+int32_t gbo_testing_set_pdl(int32_t enable) { return gbo::g_pdl.exchange(enable != 0 ? 1 : 0); }
 
 int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream) {
   if (!dev_status || !aligned(dev_status, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_status is NULL or misaligned");

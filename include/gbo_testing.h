@@ -77,6 +77,17 @@ int32_t gbo_testing_set_tail_split(int32_t enable);
  */
 int32_t gbo_testing_pair_residency(void);
 
+/*
+ * Test and A/B switch, read at every launch: launches carry the
+ * programmatic-dependent-launch attribute, so that each kernel's prologue
+ * (barrier set-up, TMEM allocation) runs under the previous kernel's tail
+ * (enable != 0), or not (enable == 0, the default: on a GB300 it made the
+ * many-small-matrix step 12.7% slower and gained nothing measurable on the
+ * other sets).  Results are the same either way.  Returns the previous
+ * setting.
+ */
+int32_t gbo_testing_set_pdl(int32_t enable);
+
 #ifdef __cplusplus
 }
 #endif
