@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--fused-momentum", action="store_true",
                     help="A/B: run the momentum pass of the chain's wide p <= 128 matrices inside the chain launch "
                          "instead of in the momentum kernel (workload 4; measured slower)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch the timed steps directly instead of replaying one step (Muon, clip, AdamW "
+                         "with the step count on the device) captured in a CUDA graph")
     ap.add_argument("--e2e-buffers", type=int, default=3,
                     help="gradient buffer sets of the end-to-end run (each with its plan): uploads run up to "
                          "this many steps minus one ahead of the step that uses them")
@@ -449,7 +452,7 @@ def floor_bytes_of(wl, torch):
 EXTRA_STEPS = {2: 200, 4: 30, 5: 5}  # about 0.2 to 1 s of timed work each
 
 
-def run_extra_workload(index, peaks, local, warmup=3):
+def run_extra_workload(index, peaks, local, warmup=3, use_graph=True):
     """Steps/s of another synthetic set, timed like the headline run (CUDA
     events on the launching stream, inputs resident in HBM, clocks sampled
     during the timed region).  The step is Muon on every matrix, plus clip +
@@ -486,6 +489,21 @@ def run_extra_workload(index, peaks, local, warmup=3):
         step()
     torch.cuda.synchronize()
     steps = EXTRA_STEPS.get(index, 10)
+    graph = None
+    if use_graph:  # one step captured in a CUDA graph, the step count on the device
+        dev_step = torch.full((1,), n[0], dtype=torch.int32, device=dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cs = torch.cuda.current_stream()
+            gbo.gbo_muon_step(plan, wl.lr, ws, dev_status=status, stream=cs)
+            if params:
+                dev_step.add_(1)
+                gbo.gbo_clip_norm([p[1] for p in params], 1.0, total, coef, cws, dev_status=status, stream=cs)
+                gbo.gbo_adamw_step(params, lr=wl.adamw_lr, coef=coef, dev_status=status, stream=cs,
+                                   dev_step=dev_step)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)  # let the sampler start
@@ -496,20 +514,28 @@ def run_extra_workload(index, peaks, local, warmup=3):
     l0 = gbo.gbo_launch_count()
     start.record(stream)  # the steps as a user runs them, without phase events
     for _ in range(steps):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     end.record(stream)
     torch.cuda.synchronize()
     launches = gbo.gbo_launch_count() - l0
     clk = clocks.stop(t_wall0, time.time())
+    if graph is not None:
+        n[0] += steps + 2  # the replays advanced the device's step count
     # the phase times from a second run of as many steps, with the plan's
     # phase events
     gbo.gbo_muon_plan_set_timing(plan, True)
     gbo.gbo_muon_plan_phase_times(plan)  # reset
+    lp0 = gbo.gbo_launch_count()
     for _ in range(steps):
         step()
     torch.cuda.synchronize()
     phases = gbo.gbo_muon_plan_phase_times(plan)
     gbo.gbo_muon_plan_set_timing(plan, False)
+    if graph is not None:  # the graph replays the kernels of one direct step
+        launches = gbo.gbo_launch_count() - lp0
     if int(status.item()) != 0:
         raise RuntimeError("device status %d during workload %d" % (int(status.item()), index))
     ms = start.elapsed_time(end) / steps
@@ -637,6 +663,23 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
 
+    # --graph: the step (Muon, clip, AdamW with the step count on the device)
+    # captured once in a CUDA graph and replayed
+    graph = None
+    if args.graph and not overlap:
+        dev_step = torch.full((1,), step_no[0], dtype=torch.int32, device=dev)
+        plan0, params0, adam_grads0 = bound[0]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cs = torch.cuda.current_stream()
+            dev_step.add_(1)
+            gbo.gbo_muon_step(plan0, wl.lr, ws, dev_status=status, stream=cs)
+            gbo.gbo_clip_norm(adam_grads0, 1.0, total, coef, cws, dev_status=status, stream=cs)
+            gbo.gbo_adamw_step(params0, lr=wl.adamw_lr, coef=coef, dev_status=status, stream=cs, dev_step=dev_step)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+
     # timed region: inputs resident in HBM (the working set is ~20 GB, far
     # above the 129 MB L2, so every step streams from HBM).  The step runs
     # as a user runs it, without the plan's phase events: recording events
@@ -654,12 +697,17 @@ def run_ours(args):
     marks = [ev() for _ in range(args.steps)]  # after each step: per-step times
     start.record(stream)
     for k in range(args.steps):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
         marks[k].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    launches = gbo.gbo_launch_count() - l0
+    launches = gbo.gbo_launch_count() - l0  # a graph's replays launch without the library counting them
+    if graph is not None:
+        step_no[0] += args.steps + 2  # the replays advanced the device's step count
     clk = clocks.stop(t_wall0, time.time())
     # the phase run: the same steps with the plan's phase events and the
     # AdamW path bracketed by events
@@ -667,11 +715,14 @@ def run_ours(args):
     gbo.gbo_muon_plan_phase_times(plan)  # reset
     adam_ev = [(ev(), ev()) for _ in range(args.steps)]
     p_start, p_end = ev(), ev()
+    lp0 = gbo.gbo_launch_count()
     p_start.record(stream)
     for k in range(args.steps):
         step(adam_ev[k])
     p_end.record(stream)
     torch.cuda.synchronize()
+    if graph is not None:  # the graph replays the kernels of one direct step
+        launches = gbo.gbo_launch_count() - lp0
     phases = gbo.gbo_muon_plan_phase_times(plan)
     gbo.gbo_muon_plan_set_timing(plan, False)
     phase_run_ms = p_start.elapsed_time(p_end) / args.steps
@@ -765,6 +816,7 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single",
                    "chain_gram": "separate launch" if args.separate_gram else "on chip (p <= 128)",
                    "tail_split": not args.no_tail_split,
+                   "cuda_graph": graph is not None,
                    "workspace_bytes": int(ws.numel()), "workspace_cap": cap or None,
                    "workspace_whole_table_bytes": int(ws_whole),
                    "chain_momentum": ("in the chain launch (wide p <= 128, bf16 G)"
@@ -845,7 +897,8 @@ def main():
                 peaks = load_peaks()
                 out["extra_workloads"] = {}
                 for index in extra:
-                    out["extra_workloads"][str(index)] = run_extra_workload(index, peaks, dist_env()[2])
+                    out["extra_workloads"][str(index)] = run_extra_workload(index, peaks, dist_env()[2],
+                                                                            use_graph=args.graph)
                     gc.collect()
             print(json.dumps(out), flush=True)
     if world > 1:
