@@ -470,10 +470,11 @@ def gbo_testing_pair_residency():
     return int(lib().gbo_testing_pair_residency())
 
 
-def gbo_testing_set_pdl(enable):
-    """Whether launches from now on carry the programmatic-dependent-launch
-    attribute (off by default).  Returns the previous setting."""
-    return bool(lib().gbo_testing_set_pdl(1 if enable else 0))
+def gbo_testing_set_pdl(mode):
+    """When launches from now on carry the programmatic-dependent-launch
+    attribute: 0 never, 1 always, 2 (the default) in CUDA graph capture only.
+    Returns the previous mode."""
+    return int(lib().gbo_testing_set_pdl(int(mode)))
 
 
 def gbo_testing_wait_timeout(dev_status, limit_us, stream=None):

@@ -19,10 +19,11 @@ namespace gbo {
 // which returns once the previous kernel has completed and its writes are
 // visible.  These take effect only when the launch carries
 // cudaLaunchAttributeProgrammaticStreamSerialization, which launch_kernel
-// below sets when pdl_enabled() (gbo_testing_set_pdl; off by default: on a
-// GB300 it made the many-small-matrix step 12.7% slower, the dependent
-// grids' early CTAs holding SMs that the kernel before them still needed,
-// and gained nothing measurable elsewhere).  Without it both return at once.
+// below sets when pdl_enabled(stream): by default only while the stream is
+// being captured into a CUDA graph.  Measured on a GB300, in graph replays it
+// made the one-layer step ~1.7% faster (and the others slightly), while with
+// kernels launched directly on a stream it made the many-small-matrix step
+// 12.7% slower.  Without the attribute both calls return at once.
 __device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -39,7 +40,7 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
   cfg.stream = stream;
   int n = 0;
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[n].val.programmaticStreamSerializationAllowed = pdl_enabled();
+  attr[n].val.programmaticStreamSerializationAllowed = pdl_enabled(stream);
   ++n;
   if (cluster > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;

@@ -260,9 +260,10 @@ int build_weight_maps(const gbo_muon_desc *descs, int32_t n, void **out);
 int launch_wait_timeout(int32_t *status, uint64_t limit_ns, void *stream);
 
 void count_launches(uint64_t n);
-// Whether launches carry the programmatic-dependent-launch attribute
-// (gbo_testing_set_pdl; 0 by default).
-int32_t pdl_enabled();
+// Whether a launch on `stream` carries the programmatic-dependent-launch
+// attribute (gbo_testing_set_pdl; by default only while the stream is being
+// captured into a CUDA graph).
+int32_t pdl_enabled(void *stream);
 
 // Error and device helpers of the host code, for entry points that live in
 // other files: record a message for gbo_last_error, clear it, and check

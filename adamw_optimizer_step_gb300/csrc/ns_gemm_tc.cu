@@ -785,7 +785,7 @@ int launch_mode(const GemmJob *const *jobs, int32_t n_jobs, const PhaseArgs &arg
     int na = 0;
     if (kPair) attrs[na++] = attr[0];
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[na].val.programmaticStreamSerializationAllowed = pdl_enabled();
+    attrs[na].val.programmaticStreamSerializationAllowed = pdl_enabled(stream);
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = na;

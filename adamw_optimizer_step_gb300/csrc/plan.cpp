@@ -29,8 +29,18 @@ static std::atomic<int32_t> g_small_chain{1};  // see gbo_testing_set_small_chai
 static std::atomic<int32_t> g_fused_gram{1};   // see gbo_testing_set_fused_gram
 static std::atomic<int32_t> g_fused_mom{0};    // see gbo_testing_set_fused_momentum (off: measured slower)
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
-static std::atomic<int32_t> g_pdl{0};  // see gbo_testing_set_pdl (off: measured slower)
-int32_t pdl_enabled() { return g_pdl.load(std::memory_order_relaxed); }
+// see gbo_testing_set_pdl: 2 (the default) in CUDA graph capture only
+static std::atomic<int32_t> g_pdl{2};
+int32_t pdl_enabled(void *stream) {
+  const int32_t mode = g_pdl.load(std::memory_order_relaxed);
+  if (mode != 2) return mode;
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &st) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return st == cudaStreamCaptureStatusActive ? 1 : 0;
+}
 
 namespace {
 
@@ -1201,7 +1211,10 @@ int32_t gbo_testing_set_tail_split(int32_t enable) { return gbo::set_tail_split(
 
 int32_t gbo_testing_pair_residency(void) { return gbo::pair_residency(); }
 
-int32_t gbo_testing_set_pdl(int32_t enable) { return gbo::g_pdl.exchange(enable != 0 ? 1 : 0); }
+int32_t gbo_testing_set_pdl(int32_t mode) {
+  if (mode < 0 || mode > 2) return -1;
+  return gbo::g_pdl.exchange(mode);
+}
 
 int gbo_testing_wait_timeout(int32_t *dev_status, uint32_t limit_us, gbo_stream_t stream) {
   if (!dev_status || !aligned(dev_status, 4)) return fail(GBO_ERR_INVALID_ARG, "dev_status is NULL or misaligned");

@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--fused-momentum", action="store_true",
                     help="A/B: run the momentum pass of the chain's wide p <= 128 matrices inside the chain launch "
                          "instead of in the momentum kernel (workload 4; measured slower)")
+    ap.add_argument("--pdl", choices=["graph", "always", "never"], default="graph",
+                    help="A/B: when launches carry the programmatic-dependent-launch attribute (the library's "
+                         "default: in CUDA graph capture only)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the timed steps directly instead of replaying one step (Muon, clip, AdamW "
                          "with the step count on the device) captured in a CUDA graph")
@@ -578,6 +581,9 @@ def run_ours(args):
     if args.no_tail_split:
         from adamw_optimizer_step_gb300 import _binding
         _binding.gbo_testing_set_tail_split(False)
+    if args.pdl != "graph":
+        from adamw_optimizer_step_gb300 import _binding
+        _binding.gbo_testing_set_pdl({"never": 0, "always": 1}[args.pdl])
     wl = wk.workload(args.workload)
     if args.layers:
         wl = wk.first_layers(wl, args.layers)
@@ -817,6 +823,7 @@ def run_ours(args):
                    "chain_gram": "separate launch" if args.separate_gram else "on chip (p <= 128)",
                    "tail_split": not args.no_tail_split,
                    "cuda_graph": graph is not None,
+                   "pdl": args.pdl,
                    "workspace_bytes": int(ws.numel()), "workspace_cap": cap or None,
                    "workspace_whole_table_bytes": int(ws_whole),
                    "chain_momentum": ("in the chain launch (wide p <= 128, bf16 G)"

@@ -78,15 +78,16 @@ int32_t gbo_testing_set_tail_split(int32_t enable);
 int32_t gbo_testing_pair_residency(void);
 
 /*
- * Test and A/B switch, read at every launch: launches carry the
+ * Test and A/B switch, read at every launch: whether launches carry the
  * programmatic-dependent-launch attribute, so that each kernel's prologue
- * (barrier set-up, TMEM allocation) runs under the previous kernel's tail
- * (enable != 0), or not (enable == 0, the default: on a GB300 it made the
- * many-small-matrix step 12.7% slower and gained nothing measurable on the
- * other sets).  Results are the same either way.  Returns the previous
- * setting.
+ * (barrier set-up, TMEM allocation) runs under the previous kernel's tail:
+ * 0 never, 1 always, 2 (the default) only while the stream is being
+ * captured into a CUDA graph.  Measured on a GB300: in graph replays it made
+ * the one-layer step ~1.7% faster; launched directly on a stream it made the
+ * many-small-matrix step 12.7% slower.  Results are the same either way.
+ * Returns the previous setting, or -1 for a mode outside 0 .. 2.
  */
-int32_t gbo_testing_set_pdl(int32_t enable);
+int32_t gbo_testing_set_pdl(int32_t mode);
 
 #ifdef __cplusplus
 }

@@ -390,11 +390,22 @@ def test_skip_zero_and_nonfinite(route, precision):
     assert status & B.GBO_STATUS_NONFINITE
 
 
+@pytest.mark.parametrize("pdl", [0, 1, 2])
 @pytest.mark.parametrize("precision", ["bf16", "f32"])
-def test_cuda_graph_replay(precision):
+def test_cuda_graph_replay(precision, pdl):
     """Once a first call has set the plan up on the device, a Muon step
     captured in a CUDA graph replays the same launches: one direct step, a
-    capture and three replays give bitwise the state of four direct steps."""
+    capture and three replays give bitwise the state of four direct steps,
+    with programmatic dependent launch never, always or (the default) in
+    the capture only."""
+    prev = B.gbo_testing_set_pdl(pdl)
+    try:
+        _graph_replay_case(precision)
+    finally:
+        B.gbo_testing_set_pdl(prev)
+
+
+def _graph_replay_case(precision):
     shapes = [(300, 700, None, None), (700, 300, None, None), (64, 64, None, None),
               (200, 40, (2, 100, 40), (30, 70))]
     entries = random_entries(shapes, seed=31, b_std=1e-3)
