@@ -212,6 +212,12 @@ uint64_t gbo_desc_hash(const gbo_plan *plan);
  *               table order: receives scale*O (the update before lr) for
  *               every updated weight; untouched for skipped ones
  *   dev_status  device int32 or NULL (GBO_STATUS_* bits OR-ed in)
+ * Asynchronous on `stream`.  The first call of a plan sets up its device
+ * tables (it allocates and copies, synchronously); later calls only launch
+ * kernels, so a later call may be captured into a CUDA graph and replayed.
+ * While the stream is being captured, the launches carry the
+ * programmatic-dependent-launch attribute (each kernel's prologue overlaps
+ * the previous kernel's tail; see gbo_testing_set_pdl).
  * Errors: INVALID_ARG, WORKSPACE, UNSUPPORTED (device is not sm_103),
  * CUDA.
  */
