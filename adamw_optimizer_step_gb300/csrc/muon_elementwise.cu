@@ -593,7 +593,7 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
 
 // The NorMuon write pass streamed through shared memory (bf16 X and bf16
 // weights whose rows start on 16-byte boundaries): each warp takes whole
-// stored rows and moves them in 2048-element segments, X's and W's, by bulk
+// stored rows and moves them in 512-element segments, X's and W's, by bulk
 // copies into a ring of kWStages stages of its own, kept full across its
 // rows, so the loads run ahead without holding registers; the warp reads a
 // landed stage, computes the new weights and stores them with 16-byte vector
@@ -601,9 +601,9 @@ normuon_rows_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_b
 // + eps)), times the rectangular scale (kMode 0) or the RMS scale (kMode 2);
 // each is read when its row's first segment is loaded, so no row waits for
 // it (NorMuon paper, section 3.1, as normuon_rows_kernel).
-constexpr int kSeg = 2048;
+constexpr int kSeg = 512;
 constexpr int kWStages = 3;
-constexpr int kWWarps = 8;
+constexpr int kWWarps = 32;  // 1024 threads, 192 KB of copies in flight per SM
 constexpr int kWStageBytes = 2 * kSeg * 2;  // a segment of X and of W, bf16
 constexpr int kWSmem = 128 /*align*/ + kWWarps * kWStages * kWStageBytes;
 

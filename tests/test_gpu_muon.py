@@ -348,7 +348,7 @@ def test_normuon_rows(precision):
 def test_normuon_streamed_write(rms_target):
     """bf16 weights whose rows all start on 16-byte boundaries take the
     streamed write pass (a statistics pass, then rows streamed through
-    shared memory in 2048-element segments): rows longer and shorter than a
+    shared memory in 512-element segments): rows longer and shorter than a
     segment, ragged tails, wide and tall, X and Gram routes, a split view,
     with and without the RMS-keeping scale, from a nonzero v."""
     shapes = [(256, 4104, None, None), (4104, 256, None, None), (96, 96, None, None),
