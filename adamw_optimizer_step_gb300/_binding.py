@@ -114,6 +114,7 @@ def lib():
         "gbo_testing_set_fused_gram": (c_int32, [c_int32]),
         "gbo_testing_set_fused_momentum": (c_int32, [c_int32]),
         "gbo_testing_set_tail_split": (c_int32, [c_int32]),
+        "gbo_testing_set_momentum_stream": (c_int32, [c_int32]),
         "gbo_testing_pair_residency": (c_int32, []),
         "gbo_testing_set_pdl": (c_int32, [c_int32]),
         "gbo_last_error": (ctypes.c_char_p, []),
@@ -462,6 +463,14 @@ def gbo_testing_set_tail_split(enable):
     wave of at most half the resident pairs as 256 x 128 half tiles (the
     default).  Returns the previous setting."""
     return bool(lib().gbo_testing_set_tail_split(1 if enable else 0))
+
+
+def gbo_testing_set_momentum_stream(enable):
+    """Whether momentum passes from now on stream their tiles through shared
+    memory where the plan allows it (the default) or take the register
+    kernel; the results are bitwise the same.  Returns the previous
+    setting."""
+    return bool(lib().gbo_testing_set_momentum_stream(1 if enable else 0))
 
 
 def gbo_testing_pair_residency():

@@ -158,8 +158,16 @@ struct PhaseArgs {
 // Launchers (implemented in the .cu files).  Each returns a cudaError_t as
 // int and adds its launches to the library's counter.
 // x0t: X0's transposed twin (fp32 mode), or nullptr.
+// stream_g: 0, or (every matrix with flat tiles, bf16 X) the element size of
+// G when all G are bf16 (2) or else 4: the tiles then stream through shared
+// memory by bulk copies (momentum_stream_kernel), with bitwise the same
+// results.  status: where a timed-out wait is flagged.
 int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float mu, int32_t nesterov,
-                    void *x0, void *x0t, int32_t x_dtype, float *partials, int sm_count, void *stream);
+                    void *x0, void *x0t, int32_t x_dtype, float *partials, int32_t stream_g, int32_t *status,
+                    int sm_count, void *stream);
+// Whether momentum_stream_kernel may run where the table allows it (on by
+// default); returns the previous setting (gbo_testing_set_momentum_stream).
+int32_t set_momentum_stream(int32_t enable);
 // stats: nullptr, or where each matrix's ||D||_F goes (2 * mat_idx)
 int launch_prenorm_finalize(const DevSub *subs, int32_t n_subs, const float *partials,
                             float *alpha, int32_t *status, float *stats, int sm_count, void *stream);

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "device_common.cuh"
@@ -180,6 +181,191 @@ momentum_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) {
       float *pp = partials + 2 * (t * kMomWarps + (threadIdx.x >> 5));
+      pp[0] = M;
+      pp[1] = ss;
+    }
+  }
+}
+
+// One bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// into shared memory, completing on the mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// The momentum pass streamed through shared memory, for tables whose every
+// matrix has flat tiles (bf16 X in stored orientation, G and B rows on
+// 16-byte boundaries).  One block per SM takes a contiguous range of tiles.
+// Its producer warp moves each tile's G and B into shared memory by bulk
+// copies, running ahead of the consumers without holding registers.  The
+// consumers are kMsGroups groups of eight warps: the range's tile i goes to
+// group i % kMsGroups, as that group's tile j = i / kMsGroups, into the
+// group's own ring of kPer stages (stage j % kPer).  A stage is thus waited
+// on by one group in order, never a full phase ahead of its barrier (a
+// parity wait cannot tell that phase from the one before it).  Each group
+// takes momentum_kernel's flat-tile path on its landed stage, with the same
+// elements per thread, the same operations in the same order and the same
+// per-warp partials, so B, X_0 and the partials are bitwise those of
+// momentum_kernel.  kG is G's element size: 2 when every G is bf16 (24 KB
+// stages), else 4 (32 KB stages; a bf16 G fills half of its slot).
+#ifndef GBO_MS_GROUPS
+#define GBO_MS_GROUPS 3
+#endif
+constexpr int kMsGroups = GBO_MS_GROUPS;
+constexpr int kMsThreads = kMsGroups * kMomThreads + 32;  // the consumer groups and the producer warp
+constexpr int kMsBudget = 216 * 1024;                     // shared memory for stages
+template <int kG>
+struct MsRing {
+  static constexpr int kGBytes = kMomFlat * kG;
+  static constexpr int kStageBytes = kGBytes + kMomFlat * 4;
+  static constexpr int kPer = kMsBudget / (kMsGroups * kStageBytes);  // stages per group
+  static constexpr int kStages = kPer * kMsGroups;
+  static constexpr int kSmem = 128 /*align*/ + kStages * kStageBytes;
+  static_assert(kPer >= 2, "each consumer group needs two stages at least");
+};
+
+template <int kG>
+__global__ void __launch_bounds__(kMsThreads, 1)
+momentum_stream_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles, float mu,
+                       int32_t nesterov, __nv_bfloat16 *__restrict__ x0, float *__restrict__ partials,
+                       int32_t *status) {
+  using R = MsRing<kG>;
+  pdl_launch();  // the next kernel may be scheduled as SMs free up
+  pdl_wait();    // the previous kernel has completed and its writes are visible
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[R::kStages], empty[R::kStages];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+  const uint32_t ring = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < R::kStages; ++st) {
+      mbar_init(smem_u32(&full[st]), 1);
+      mbar_init(smem_u32(&empty[st]), kMomWarps);  // one arrival per warp of the stage's group
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // the stage of the range's tile i, and the use of that stage it is (its barriers' phase)
+  auto stage_of = [](uint32_t i) { return (i % kMsGroups) * R::kPer + (i / kMsGroups) % R::kPer; };
+  auto use_of = [](uint32_t i) { return (i / kMsGroups) / R::kPer; };
+  const int64_t per = (n_tiles + gridDim.x - 1) / gridDim.x;
+  const int64_t t_begin = (int64_t)blockIdx.x * per;
+  const int64_t t_end = min(n_tiles, t_begin + per);
+  if (t_begin >= t_end) return;
+  int si = find_owner(t_begin, n_subs, [&](int k) { return subs[k].tile0; });
+  if (warp == kMsGroups * kMomWarps) {  // the producer: lane 0 issues every copy
+    if (lane != 0) return;
+    uint32_t i = 0;
+    for (int64_t t = t_begin; t < t_end; ++t, ++i) {
+      while (si + 1 < n_subs && subs[si + 1].tile0 <= t) ++si;
+      const DevSub &S = subs[si];
+      const uint32_t st = stage_of(i), use = use_of(i);
+      if (use > 0 && !mbar_wait(smem_u32(&empty[st]), (use - 1) & 1u)) {
+        flag_status(status, GBO_STATUS_TIMEOUT);
+        break;
+      }
+      const int64_t e0 = (t - S.tile0) * kMomFlat, w = S.r0 * S.cols + e0;
+      const uint32_t n = (uint32_t)min((int64_t)kMomFlat, (int64_t)S.m * S.n - e0);
+      const uint32_t gsz = S.g_dtype == GBO_BF16 ? 2u : 4u;
+      const uint32_t bar = smem_u32(&full[st]), dst = ring + st * R::kStageBytes;
+      mbar_expect_tx(bar, n * (gsz + 4u));
+      bulk_load(dst, reinterpret_cast<const uint8_t *>(S.g) + w * gsz, n * gsz, bar);
+      bulk_load(dst + R::kGBytes, S.mom + w, n * 4u, bar);
+    }
+    // after a timeout: the copies in flight land before shared memory goes
+    // away (tiles are issued round-robin over the groups, so the last kStages
+    // issued use each stage once, each its latest use)
+    if (i < (uint32_t)(t_end - t_begin))
+      for (uint32_t k = i > (uint32_t)R::kStages ? i - R::kStages : 0u; k < i; ++k)
+        (void)mbar_wait(smem_u32(&full[stage_of(k)]), use_of(k) & 1u);
+    return;
+  }
+  const int grp = warp / kMomWarps, cw = warp % kMomWarps, ct = threadIdx.x % kMomThreads;
+  uint32_t i = (uint32_t)grp;
+  for (int64_t t = t_begin + grp; t < t_end; t += kMsGroups, i += kMsGroups) {
+    while (si + 1 < n_subs && subs[si + 1].tile0 <= t) ++si;
+    const DevSub &S = subs[si];
+    const uint32_t st = stage_of(i);
+    if (!mbar_wait(smem_u32(&full[st]), use_of(i) & 1u)) {
+      flag_status(status, GBO_STATUS_TIMEOUT);
+      break;
+    }
+    const int64_t nel = (int64_t)S.m * S.n;
+    const int64_t e0 = (t - S.tile0) * kMomFlat;
+    const int64_t wbase = S.r0 * S.cols;
+    const uint32_t gs = ring + st * R::kStageBytes, bs = gs + R::kGBytes;
+    const bool gbf = S.g_dtype == GBO_BF16;
+    float g[2][8], b[2][8], d[2][8];
+    float lmax = 0.f;
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps) {
+      const int el = ps * (kMomFlat / 2) + ct * 8;  // element within the tile
+      const int valid = (int)max((int64_t)0, min((int64_t)8, nel - e0 - el));
+      uint32_t r[8];
+      if (gbf) {
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(gs + el * 2)
+                     : "memory");
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&r[h]);
+          g[ps][2 * h] = __low2float(v);
+          g[ps][2 * h + 1] = __high2float(v);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(g[ps][4 * h]), "=f"(g[ps][4 * h + 1]), "=f"(g[ps][4 * h + 2]), "=f"(g[ps][4 * h + 3])
+                       : "r"(gs + el * 4 + 16 * h)
+                       : "memory");
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(b[ps][4 * h]), "=f"(b[ps][4 * h + 1]), "=f"(b[ps][4 * h + 2]), "=f"(b[ps][4 * h + 3])
+                     : "r"(bs + el * 4 + 16 * h)
+                     : "memory");
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k >= valid) g[ps][k] = b[ps][k] = 0.f;  // past the matrix: what landed there is stale
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[st]));  // the warp has read the stage
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps) {
+      const int64_t e = e0 + ps * (kMomFlat / 2) + ct * 8;
+      const int valid = (int)max((int64_t)0, min((int64_t)8, nel - e));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float nb = mu * b[ps][k] + g[ps][k];
+        b[ps][k] = nb;
+        d[ps][k] = k < valid ? (nesterov ? g[ps][k] + mu * nb : nb) : 0.f;
+        lmax = fmaxf(lmax, fabsf(d[ps][k]));
+      }
+      if (valid > 0) {
+        store8(S.mom + wbase + e, b[ps], valid, true);
+        store8(x0 + S.x_off + e, d[ps], valid, true);
+      }
+    }
+    const float M = warp_max(lmax);
+    float ss = 0.f;
+    if (M > 0.f) {
+      const float inv = 1.0f / M;
+#pragma unroll
+      for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float y = d[ps][k] * inv;
+          ss = fmaf(y, y, ss);
+        }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) {
+      float *pp = partials + 2 * (t * kMomWarps + cw);
       pp[0] = M;
       pp[1] = ss;
     }
@@ -607,12 +793,6 @@ constexpr int kWWarps = 32;  // 1024 threads, 192 KB of copies in flight per SM
 constexpr int kWStageBytes = 2 * kSeg * 2;  // a segment of X and of W, bf16
 constexpr int kWSmem = 128 /*align*/ + kWWarps * kWStages * kWStageBytes;
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
 // A warp's walk over stored rows: row slots slot, slot + stride, ... of the
 // plan's row blocks (kRowBlock slots each), skipping slots past a matrix's
 // rows.
@@ -819,9 +999,38 @@ rownorm_plain_kernel(const float *__restrict__ O, int64_t rows, int64_t cols, fl
 
 }  // namespace
 
+namespace {
+std::atomic<int32_t> g_mom_stream{1};  // see gbo_testing_set_momentum_stream
+}  // namespace
+
+int32_t set_momentum_stream(int32_t enable) { return g_mom_stream.exchange(enable != 0 ? 1 : 0); }
+
 int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float mu, int32_t nesterov,
-                    void *x0, void *x0t, int32_t x_dtype, float *partials, int sm_count, void *stream) {
+                    void *x0, void *x0t, int32_t x_dtype, float *partials, int32_t stream_g, int32_t *status,
+                    int sm_count, void *stream) {
   if (n_tiles == 0) return 0;
+  if (stream_g && x_dtype == GBO_BF16 && g_mom_stream.load()) {
+    static const cudaError_t attr_err = [] {
+      cudaError_t e = cudaFuncSetAttribute(momentum_stream_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           MsRing<2>::kSmem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(momentum_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 MsRing<4>::kSmem);
+      return e;
+    }();
+    if (attr_err != cudaSuccess) return (int)attr_err;
+    const int64_t grid = std::min<int64_t>(n_tiles, (int64_t)sm_count);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    __nv_bfloat16 *x = reinterpret_cast<__nv_bfloat16 *>(x0);
+    const cudaError_t err =
+        stream_g == 2
+            ? launch_kernel(momentum_stream_kernel<2>, dim3((unsigned)grid), dim3(kMsThreads), MsRing<2>::kSmem, st, 1,
+                            subs, n_subs, n_tiles, mu, nesterov, x, partials, status)
+            : launch_kernel(momentum_stream_kernel<4>, dim3((unsigned)grid), dim3(kMsThreads), MsRing<4>::kSmem, st, 1,
+                            subs, n_subs, n_tiles, mu, nesterov, x, partials, status);
+    count_launches(1);
+    return (int)err;
+  }
   // one wave: as many blocks as can be resident, each a contiguous tile range
   static int resident[2] = {0, 0};
   const int which = x_dtype == GBO_BF16 ? 0 : 1;

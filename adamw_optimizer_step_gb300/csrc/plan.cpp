@@ -152,6 +152,9 @@ struct gbo_plan {
   std::vector<DevSub> subs;  // sorted by shape class
   std::vector<ShapeClass> classes;
   int64_t n_tiles = 0, n_row_blocks = 0;
+  // the momentum tiles stream through shared memory (every matrix with flat
+  // tiles, bf16 X): G's element size, 2 when all G are bf16, else 4; or 0
+  int32_t mom_stream_g = 0;
   int32_t x_dtype = GBO_BF16;
   size_t off_x[2] = {0, 0}, off_p = 0, off_a = 0, off_alpha = 0, off_part = 0, ws_bytes = 0;
   size_t off_xt[2] = {0, 0};  // fp32 mode: the X buffers' transposed twins
@@ -467,6 +470,13 @@ int validate_and_expand(gbo_plan *P) {
   }
   P->n_tiles = tiles;
   P->n_row_blocks = rbs;
+  bool all_flat = P->x_dtype == GBO_BF16, all_g16 = true;
+  for (const DevSub &S : subs)
+    if (!S.mom_fused) {
+      all_flat = all_flat && S.tiles_c == 0;
+      all_g16 = all_g16 && S.g_dtype == GBO_BF16;
+    }
+  P->mom_stream_g = all_flat ? (all_g16 ? 2 : 4) : 0;
   // NorMuon row statistics from the last product (bf16 mode): per stored row
   // of each matrix, one partial per 128 columns of its output
   // and, for the per-matrix norms, the last product's sums of squares of
@@ -1128,7 +1138,7 @@ int gbo_muon_step(gbo_plan *P, float lr, void *workspace, size_t ws_bytes, float
   const int32_t nsub = (int32_t)P->subs.size();
   void *x0t = P->x_dtype == GBO_F32 ? ws + P->off_xt[0] : nullptr;
   int err = launch_momentum(P->d_subs, nsub, P->n_tiles, P->opts.mu, P->opts.nesterov, x[0], x0t, P->x_dtype,
-                            partials, P->sm_count, st);
+                            partials, P->mom_stream_g, dev_status, P->sm_count, st);
   if (err) return cuda_fail(err, "momentum kernel");
   if (P->n_unfused > 0) {
     err = launch_prenorm_finalize(P->d_subs, nsub, partials, alpha, dev_status, P->stats, P->sm_count, st);
@@ -1208,6 +1218,8 @@ int32_t gbo_testing_set_fused_gram(int32_t enable) { return g_fused_gram.exchang
 int32_t gbo_testing_set_fused_momentum(int32_t enable) { return g_fused_mom.exchange(enable != 0 ? 1 : 0); }
 
 int32_t gbo_testing_set_tail_split(int32_t enable) { return gbo::set_tail_split(enable); }
+
+int32_t gbo_testing_set_momentum_stream(int32_t enable) { return gbo::set_momentum_stream(enable); }
 
 int32_t gbo_testing_pair_residency(void) { return gbo::pair_residency(); }
 

@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--no-tail-split", action="store_true",
                     help="A/B: run a CTA-pair launch's last partial wave as whole 256 x 256 tiles instead of "
                          "256 x 128 halves")
+    ap.add_argument("--no-momentum-stream", action="store_true",
+                    help="A/B: run the momentum pass as the register kernel (several blocks per SM) instead of "
+                         "streaming its tiles through shared memory by bulk copies")
     ap.add_argument("--workspace-cap-frac", type=float, default=0.0,
                     help="cap the Muon workspace at this fraction of what the whole table needs (0: no cap); "
                          "the step then runs in groups of weights on the smaller workspace")
@@ -581,6 +584,9 @@ def run_ours(args):
     if args.no_tail_split:
         from adamw_optimizer_step_gb300 import _binding
         _binding.gbo_testing_set_tail_split(False)
+    if args.no_momentum_stream:
+        from adamw_optimizer_step_gb300 import _binding
+        _binding.gbo_testing_set_momentum_stream(False)
     if args.pdl != "graph":
         from adamw_optimizer_step_gb300 import _binding
         _binding.gbo_testing_set_pdl({"never": 0, "always": 1}[args.pdl])
@@ -822,6 +828,7 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single",
                    "chain_gram": "separate launch" if args.separate_gram else "on chip (p <= 128)",
                    "tail_split": not args.no_tail_split,
+                   "momentum_stream": not args.no_momentum_stream,
                    "cuda_graph": graph is not None,
                    "pdl": args.pdl,
                    "workspace_bytes": int(ws.numel()), "workspace_cap": cap or None,

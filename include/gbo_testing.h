@@ -69,6 +69,18 @@ int32_t gbo_testing_set_fused_momentum(int32_t enable);
 int32_t gbo_testing_set_tail_split(int32_t enable);
 
 /*
+ * Test and A/B switch, read at each launch of the momentum pass: where every
+ * matrix of a bf16-mode plan has flat momentum tiles (G and B rows on
+ * 16-byte boundaries, X in stored orientation), the tiles stream through
+ * shared memory by bulk copies, one block per SM with a producer warp
+ * running ahead of eight consumer warps (enable != 0, the default), or take
+ * the register kernel, several blocks per SM each loading its own tiles
+ * (enable == 0).  Both give bitwise the same B, X_0 and norm partials: each
+ * element is computed by the same operations.  Returns the previous setting.
+ */
+int32_t gbo_testing_set_momentum_stream(int32_t enable);
+
+/*
  * How many CTA pairs (2-CTA clusters) of the bf16 Newton-Schulz kernel the
  * current device holds at once: the persistent grid of its pair launches.
  * Where the device's SMs do not all pair up within their clusters'

@@ -638,6 +638,66 @@ def test_tail_split_bitwise(shape, normuon):
     check_muon(entries, one, ora, lr=0.02, precision="bf16")
 
 
+@pytest.mark.parametrize("g_kind", ["bf16", "f32", "mixed", "unaligned"])
+def test_momentum_stream_bitwise(g_kind):
+    """The momentum pass streamed through shared memory (bf16 mode, every
+    matrix on 16-byte rows) against the register kernel: weights, momentum
+    and the exported update bitwise equal over two steps, with bf16, fp32
+    and mixed G (24 KB and 32 KB stages), ragged last tiles, matrices much
+    smaller than a tile, tile ranges crossing matrices, split views and more
+    tiles per block than ring stages; a table with a row off the 16-byte
+    grid takes the register kernel either way.  Both match the oracle."""
+    shapes = [(2048, 2048, None, None), (1536, 384, None, None), (136, 1000, None, None, 1.0, 0.1),
+              (8, 8, None, None), (4 * 96, 1000, (4, 96, 1000), None), (24, 4104, None, None),
+              (2 * 192, 1536, (2, 192, 1536), None), (72, 64, None, None)]
+    if g_kind == "unaligned":
+        shapes.append((40, 100, None, None))
+    entries = random_entries(shapes, seed=59, b_std=1e-3)
+    if g_kind == "f32":
+        for e in entries:
+            e["g"] = e["g"].float()
+    elif g_kind == "mixed":
+        for e in entries[1::2]:
+            e["g"] = e["g"].float()
+    kw = dict(lr=0.02, precision="bf16", steps=2)
+    prev = B.gbo_testing_set_momentum_stream(False)
+    try:
+        reg, st0, _ = run_muon_gpu(entries, **kw)
+        B.gbo_testing_set_momentum_stream(True)
+        streamed, st1, _ = run_muon_gpu(entries, **kw)
+        one, st2, _ = run_muon_gpu(entries, **dict(kw, steps=1))
+    finally:
+        B.gbo_testing_set_momentum_stream(prev)
+    assert st0 == 0 and st1 == 0 and st2 == 0
+    for a, b in zip(reg, streamed):
+        assert torch.equal(a["W"], b["W"]) and torch.equal(a["B"], b["B"]) and torch.equal(a["U"], b["U"])
+    ora = run_muon_oracle(entries, lr=0.02)
+    check_muon(entries, one, ora, lr=0.02, precision="bf16")
+
+
+@pytest.mark.parametrize("g_kind", ["bf16", "mixed"])
+def test_momentum_stream_many_tiles_per_block(g_kind):
+    """Tens of tiles per block, so every consumer group's ring of the
+    streamed momentum pass wraps many times (24 KB stages with bf16 G, 32 KB
+    with an fp32 G in the table): bitwise the register kernel's weights,
+    momentum and update over three steps."""
+    shapes = [(4096, 4096, None, None), (4096, 1024, None, None), (1000, 4096, None, None, 1.0, 0.1)]
+    entries = random_entries(shapes, seed=61, b_std=1e-3)
+    if g_kind == "mixed":
+        entries[1]["g"] = entries[1]["g"].float()
+    kw = dict(lr=0.02, precision="bf16", steps=3)
+    prev = B.gbo_testing_set_momentum_stream(False)
+    try:
+        reg, st0, _ = run_muon_gpu(entries, **kw)
+        B.gbo_testing_set_momentum_stream(True)
+        streamed, st1, _ = run_muon_gpu(entries, **kw)
+    finally:
+        B.gbo_testing_set_momentum_stream(prev)
+    assert st0 == 0 and st1 == 0
+    for a, b in zip(reg, streamed):
+        assert torch.equal(a["W"], b["W"]) and torch.equal(a["B"], b["B"]) and torch.equal(a["U"], b["U"])
+
+
 @pytest.mark.parametrize("free_sms", [4, 37])
 def test_free_sms_bitwise(free_sms):
     """A plan that leaves SMs free runs its persistent kernels on fewer CTAs
