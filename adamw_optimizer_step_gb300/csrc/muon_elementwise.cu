@@ -197,25 +197,31 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 
 // The momentum pass streamed through shared memory, for tables whose every
 // matrix has flat tiles (bf16 X in stored orientation, G and B rows on
-// 16-byte boundaries).  One block per SM takes a contiguous range of tiles.
-// Its producer warp moves each tile's G and B into shared memory by bulk
-// copies, running ahead of the consumers without holding registers.  The
-// consumers are kMsGroups groups of eight warps: the range's tile i goes to
-// group i % kMsGroups, as that group's tile j = i / kMsGroups, into the
-// group's own ring of kPer stages (stage j % kPer).  A stage is thus waited
-// on by one group in order, never a full phase ahead of its barrier (a
-// parity wait cannot tell that phase from the one before it).  Each group
-// takes momentum_kernel's flat-tile path on its landed stage, with the same
-// elements per thread, the same operations in the same order and the same
-// per-warp partials, so B, X_0 and the partials are bitwise those of
-// momentum_kernel.  kG is G's element size: 2 when every G is bf16 (24 KB
-// stages), else 4 (32 KB stages; a bf16 G fills half of its slot).
+// 16-byte boundaries).  One block per SM, taking either tiles dealt out
+// across the blocks (tables of large matrices: all SMs then stream from one
+// narrow window of each array at a time) or a contiguous range of tiles
+// (tables of many small matrices, where that measured faster).  A block's
+// producer warp finds each of its tiles' matrix, moves the tile's
+// G and B into shared memory by bulk copies, running ahead of the consumers
+// without holding registers, and leaves the tile's destinations and extent
+// in a small header beside the stage.  The consumers are kMsGroups groups
+// of eight warps: the block's tile i goes to group i % kMsGroups, as that
+// group's tile j = i / kMsGroups, into the group's own ring of kPer stages
+// (stage j % kPer).  A stage is thus waited on by one group in order, never
+// a full phase ahead of its barrier (a parity wait cannot tell that phase
+// from the one before it).  Each group takes momentum_kernel's flat-tile
+// path on its landed stage, with the same elements per thread, the same
+// operations in the same order and the same per-warp partials, so B, X_0
+// and the partials are bitwise those of momentum_kernel.  kG is G's element
+// size: 2 when every G is bf16 (24 KB stages), else 4 (32 KB stages; a bf16
+// G fills half of its slot).
 #ifndef GBO_MS_GROUPS
 #define GBO_MS_GROUPS 3
 #endif
 constexpr int kMsGroups = GBO_MS_GROUPS;
 constexpr int kMsThreads = kMsGroups * kMomThreads + 32;  // the consumer groups and the producer warp
 constexpr int kMsBudget = 216 * 1024;                     // shared memory for stages
+constexpr int kMsInterleaveTiles = 512;  // average tiles a matrix from which blocks take dealt-out tiles
 template <int kG>
 struct MsRing {
   static constexpr int kGBytes = kMomFlat * kG;
@@ -226,16 +232,25 @@ struct MsRing {
   static_assert(kPer >= 2, "each consumer group needs two stages at least");
 };
 
+// What the producer tells a stage's consumers about the tile in it.
+struct MsHdr {
+  float *b;            // B at the tile's first element
+  __nv_bfloat16 *x;    // X_0 at the tile's first element
+  int64_t rem;         // elements from the tile's first to the matrix's end
+  int32_t g_bf16, pad;
+};
+
 template <int kG>
 __global__ void __launch_bounds__(kMsThreads, 1)
 momentum_stream_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t n_tiles, float mu,
                        int32_t nesterov, __nv_bfloat16 *__restrict__ x0, float *__restrict__ partials,
-                       int32_t *status) {
+                       int32_t *status, int32_t interleave) {
   using R = MsRing<kG>;
   pdl_launch();  // the next kernel may be scheduled as SMs free up
   pdl_wait();    // the previous kernel has completed and its writes are visible
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[R::kStages], empty[R::kStages];
+  __shared__ MsHdr hdr[R::kStages];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
   const uint32_t ring = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -250,59 +265,99 @@ momentum_stream_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t 
   // the stage of the range's tile i, and the use of that stage it is (its barriers' phase)
   auto stage_of = [](uint32_t i) { return (i % kMsGroups) * R::kPer + (i / kMsGroups) % R::kPer; };
   auto use_of = [](uint32_t i) { return (i / kMsGroups) / R::kPer; };
-  const int64_t per = (n_tiles + gridDim.x - 1) / gridDim.x;
-  const int64_t t_begin = (int64_t)blockIdx.x * per;
-  const int64_t t_end = min(n_tiles, t_begin + per);
-  if (t_begin >= t_end) return;
-  int si = find_owner(t_begin, n_subs, [&](int k) { return subs[k].tile0; });
-  if (warp == kMsGroups * kMomWarps) {  // the producer: lane 0 issues every copy
-    if (lane != 0) return;
-    uint32_t i = 0;
-    for (int64_t t = t_begin; t < t_end; ++t, ++i) {
-      while (si + 1 < n_subs && subs[si + 1].tile0 <= t) ++si;
-      const DevSub &S = subs[si];
-      const uint32_t st = stage_of(i), use = use_of(i);
-      if (use > 0 && !mbar_wait(smem_u32(&empty[st]), (use - 1) & 1u)) {
-        flag_status(status, GBO_STATUS_TIMEOUT);
-        break;
+  // The block's tile i: with `interleave`, tiles are dealt out across the
+  // blocks (block b takes b, b + gridDim.x, ...), so all SMs stream from one
+  // narrow window of each array at a time; else each block takes a
+  // contiguous range.
+  const int64_t G = gridDim.x;
+  int64_t t_begin, t_step;
+  uint32_t n_mine;
+  if (interleave) {
+    t_begin = blockIdx.x;
+    t_step = G;
+    n_mine = n_tiles > t_begin ? (uint32_t)((n_tiles - t_begin + G - 1) / G) : 0u;
+  } else {
+    const int64_t per = (n_tiles + G - 1) / G;
+    t_begin = (int64_t)blockIdx.x * per;
+    t_step = 1;
+    n_mine = n_tiles > t_begin ? (uint32_t)min(per, n_tiles - t_begin) : 0u;
+  }
+  if (n_mine == 0) return;
+  if (warp == kMsGroups * kMomWarps) {  // the producer warp; lane 0 issues every copy
+    // The block's tiles are resolved 32 at a time, one per lane (its
+    // matrix by binary search, then the copy's sources and the header),
+    // while the ring is full; lane 0 then issues them in order.
+    int si = find_owner(t_begin, n_subs, [&](int k) { return subs[k].tile0; });
+    uint32_t issued = 0;
+    bool timed_out = false;
+    while (issued < n_mine && !timed_out) {
+      const uint32_t ij = min(issued + (uint32_t)lane, n_mine - 1);
+      const int64_t tj = t_begin + (int64_t)ij * t_step;
+      int lo = si, hi = n_subs - 1;  // the last matrix whose first tile is <= tj
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (subs[mid].tile0 <= tj) lo = mid;
+        else hi = mid - 1;
       }
-      const int64_t e0 = (t - S.tile0) * kMomFlat, w = S.r0 * S.cols + e0;
-      const uint32_t n = (uint32_t)min((int64_t)kMomFlat, (int64_t)S.m * S.n - e0);
+      const DevSub &S = subs[lo];
       const uint32_t gsz = S.g_dtype == GBO_BF16 ? 2u : 4u;
-      const uint32_t bar = smem_u32(&full[st]), dst = ring + st * R::kStageBytes;
-      mbar_expect_tx(bar, n * (gsz + 4u));
-      bulk_load(dst, reinterpret_cast<const uint8_t *>(S.g) + w * gsz, n * gsz, bar);
-      bulk_load(dst + R::kGBytes, S.mom + w, n * 4u, bar);
+      const int64_t e0 = (tj - S.tile0) * kMomFlat, w = S.r0 * S.cols + e0;
+      const uint64_t gsrc = reinterpret_cast<uint64_t>(reinterpret_cast<const uint8_t *>(S.g) + w * gsz);
+      const uint64_t bsrc = reinterpret_cast<uint64_t>(S.mom + w);
+      const uint64_t xdst = reinterpret_cast<uint64_t>(x0 + S.x_off + e0);
+      const int64_t rem = (int64_t)S.m * S.n - e0;
+      si = __shfl_sync(0xffffffffu, lo, 31);  // owners are nondecreasing over the lanes
+      const uint32_t batch = min(32u, n_mine - issued);
+      for (uint32_t j = 0; j < batch; ++j) {
+        const uint64_t g_j = __shfl_sync(0xffffffffu, gsrc, j), b_j = __shfl_sync(0xffffffffu, bsrc, j);
+        const uint64_t x_j = __shfl_sync(0xffffffffu, xdst, j);
+        const int64_t r_j = __shfl_sync(0xffffffffu, rem, j);
+        const uint32_t gz_j = __shfl_sync(0xffffffffu, gsz, j);
+        if (lane == 0) {
+          const uint32_t i = issued, st = stage_of(i), use = use_of(i);
+          if (use > 0 && !mbar_wait(smem_u32(&empty[st]), (use - 1) & 1u)) {
+            flag_status(status, GBO_STATUS_TIMEOUT);
+            timed_out = true;
+          } else {
+            const uint32_t n = (uint32_t)min((int64_t)kMomFlat, r_j);
+            hdr[st] = MsHdr{reinterpret_cast<float *>(b_j), reinterpret_cast<__nv_bfloat16 *>(x_j), r_j,
+                            gz_j == 2u ? 1 : 0};
+            const uint32_t bar = smem_u32(&full[st]), dst = ring + st * R::kStageBytes;
+            mbar_expect_tx(bar, n * (gz_j + 4u));  // releases the header to the stage's consumers
+            bulk_load(dst, reinterpret_cast<const void *>(g_j), n * gz_j, bar);
+            bulk_load(dst + R::kGBytes, reinterpret_cast<const void *>(b_j), n * 4u, bar);
+          }
+        }
+        timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
+        if (timed_out) break;
+        ++issued;
+      }
     }
     // after a timeout: the copies in flight land before shared memory goes
     // away (tiles are issued round-robin over the groups, so the last kStages
     // issued use each stage once, each its latest use)
-    if (i < (uint32_t)(t_end - t_begin))
-      for (uint32_t k = i > (uint32_t)R::kStages ? i - R::kStages : 0u; k < i; ++k)
+    if (lane == 0 && timed_out)
+      for (uint32_t k = issued > (uint32_t)R::kStages ? issued - R::kStages : 0u; k < issued; ++k)
         (void)mbar_wait(smem_u32(&full[stage_of(k)]), use_of(k) & 1u);
     return;
   }
   const int grp = warp / kMomWarps, cw = warp % kMomWarps, ct = threadIdx.x % kMomThreads;
-  uint32_t i = (uint32_t)grp;
-  for (int64_t t = t_begin + grp; t < t_end; t += kMsGroups, i += kMsGroups) {
-    while (si + 1 < n_subs && subs[si + 1].tile0 <= t) ++si;
-    const DevSub &S = subs[si];
+  for (uint32_t i = (uint32_t)grp; i < n_mine; i += kMsGroups) {
+    const int64_t t = t_begin + (int64_t)i * t_step;
     const uint32_t st = stage_of(i);
     if (!mbar_wait(smem_u32(&full[st]), use_of(i) & 1u)) {
       flag_status(status, GBO_STATUS_TIMEOUT);
       break;
     }
-    const int64_t nel = (int64_t)S.m * S.n;
-    const int64_t e0 = (t - S.tile0) * kMomFlat;
-    const int64_t wbase = S.r0 * S.cols;
+    const MsHdr hd = hdr[st];  // the tile's destinations and extent, from the producer
     const uint32_t gs = ring + st * R::kStageBytes, bs = gs + R::kGBytes;
-    const bool gbf = S.g_dtype == GBO_BF16;
+    const bool gbf = hd.g_bf16 != 0;
     float g[2][8], b[2][8], d[2][8];
     float lmax = 0.f;
 #pragma unroll
     for (int ps = 0; ps < 2; ++ps) {
       const int el = ps * (kMomFlat / 2) + ct * 8;  // element within the tile
-      const int valid = (int)max((int64_t)0, min((int64_t)8, nel - e0 - el));
+      const int valid = (int)max((int64_t)0, min((int64_t)8, hd.rem - el));
       uint32_t r[8];
       if (gbf) {
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -337,8 +392,8 @@ momentum_stream_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t 
     if (lane == 0) mbar_arrive(smem_u32(&empty[st]));  // the warp has read the stage
 #pragma unroll
     for (int ps = 0; ps < 2; ++ps) {
-      const int64_t e = e0 + ps * (kMomFlat / 2) + ct * 8;
-      const int valid = (int)max((int64_t)0, min((int64_t)8, nel - e));
+      const int el = ps * (kMomFlat / 2) + ct * 8;
+      const int valid = (int)max((int64_t)0, min((int64_t)8, hd.rem - el));
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float nb = mu * b[ps][k] + g[ps][k];
@@ -347,8 +402,8 @@ momentum_stream_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t 
         lmax = fmaxf(lmax, fabsf(d[ps][k]));
       }
       if (valid > 0) {
-        store8(S.mom + wbase + e, b[ps], valid, true);
-        store8(x0 + S.x_off + e, d[ps], valid, true);
+        store8(hd.b + el, b[ps], valid, true);
+        store8(hd.x + el, d[ps], valid, true);
       }
     }
     const float M = warp_max(lmax);
@@ -1020,14 +1075,19 @@ int launch_momentum(const DevSub *subs, int32_t n_subs, int64_t n_tiles, float m
     }();
     if (attr_err != cudaSuccess) return (int)attr_err;
     const int64_t grid = std::min<int64_t>(n_tiles, (int64_t)sm_count);
+    // tiles dealt out across the blocks when the matrices average at least
+    // kMsInterleaveTiles tiles: bench set (1792 a matrix) momentum 2.49 ->
+    // 2.37-2.43 ms, 7B set 13.2 -> 12.5 ms; the 9216 MLA/KDA matrices (82 a
+    // matrix) 5.85 -> 6.25 ms, so they keep contiguous ranges
+    const int32_t interleave = n_tiles >= (int64_t)kMsInterleaveTiles * n_subs ? 1 : 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     __nv_bfloat16 *x = reinterpret_cast<__nv_bfloat16 *>(x0);
     const cudaError_t err =
         stream_g == 2
             ? launch_kernel(momentum_stream_kernel<2>, dim3((unsigned)grid), dim3(kMsThreads), MsRing<2>::kSmem, st, 1,
-                            subs, n_subs, n_tiles, mu, nesterov, x, partials, status)
+                            subs, n_subs, n_tiles, mu, nesterov, x, partials, status, interleave)
             : launch_kernel(momentum_stream_kernel<4>, dim3((unsigned)grid), dim3(kMsThreads), MsRing<4>::kSmem, st, 1,
-                            subs, n_subs, n_tiles, mu, nesterov, x, partials, status);
+                            subs, n_subs, n_tiles, mu, nesterov, x, partials, status, interleave);
     count_launches(1);
     return (int)err;
   }

@@ -675,13 +675,19 @@ def test_momentum_stream_bitwise(g_kind):
     check_muon(entries, one, ora, lr=0.02, precision="bf16")
 
 
+@pytest.mark.parametrize("table", ["large", "small"])
 @pytest.mark.parametrize("g_kind", ["bf16", "mixed"])
-def test_momentum_stream_many_tiles_per_block(g_kind):
+def test_momentum_stream_many_tiles_per_block(g_kind, table):
     """Tens of tiles per block, so every consumer group's ring of the
     streamed momentum pass wraps many times (24 KB stages with bf16 G, 32 KB
-    with an fp32 G in the table): bitwise the register kernel's weights,
-    momentum and update over three steps."""
-    shapes = [(4096, 4096, None, None), (4096, 1024, None, None), (1000, 4096, None, None, 1.0, 0.1)]
+    with an fp32 G in the table), with tiles dealt out across the blocks
+    (three large matrices) or in contiguous ranges (300 matrices of 8 tiles
+    and one of 1024, so block ranges cross many matrices): bitwise the
+    register kernel's weights, momentum and update over three steps."""
+    if table == "large":
+        shapes = [(4096, 4096, None, None), (4096, 1024, None, None), (1000, 4096, None, None, 1.0, 0.1)]
+    else:
+        shapes = [(4096, 1024, None, None)] + [(64, 512, None, None)] * 300
     entries = random_entries(shapes, seed=61, b_std=1e-3)
     if g_kind == "mixed":
         entries[1]["g"] = entries[1]["g"].float()
