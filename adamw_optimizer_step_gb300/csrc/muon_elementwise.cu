@@ -262,7 +262,7 @@ momentum_stream_kernel(const DevSub *__restrict__ subs, int32_t n_subs, int64_t 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // the stage of the range's tile i, and the use of that stage it is (its barriers' phase)
+  // the stage of the block's tile i, and the use of that stage it is (its barriers' phase)
   auto stage_of = [](uint32_t i) { return (i % kMsGroups) * R::kPer + (i / kMsGroups) % R::kPer; };
   auto use_of = [](uint32_t i) { return (i / kMsGroups) / R::kPer; };
   // The block's tile i: with `interleave`, tiles are dealt out across the
