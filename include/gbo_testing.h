@@ -73,9 +73,9 @@ int32_t gbo_testing_set_tail_split(int32_t enable);
  * matrix of a bf16-mode plan has flat momentum tiles (G and B rows on
  * 16-byte boundaries, X in stored orientation), the tiles stream through
  * shared memory by bulk copies, one block per SM with a producer warp
- * running ahead of eight consumer warps (enable != 0, the default), or take
- * the register kernel, several blocks per SM each loading its own tiles
- * (enable == 0).  Both give bitwise the same B, X_0 and norm partials: each
+ * running ahead of three groups of eight consumer warps (enable != 0, the
+ * default), or take the register kernel, several blocks per SM each loading
+ * its own tiles (enable == 0).  Both give bitwise the same B, X_0 and norm partials: each
  * element is computed by the same operations.  Returns the previous setting.
  */
 int32_t gbo_testing_set_momentum_stream(int32_t enable);
